@@ -1,0 +1,596 @@
+// dattn oracle: a plain, slow fp64 CPU definition of one-token-per-stream decode
+// attention over per-stream KV caches, and of tree-verify windows.
+//
+// TEST INFRASTRUCTURE ONLY. Nothing in the library's product path links,
+// loads or calls this file; it shares no code, header, table or constant with
+// the CUDA library. Only the test suite, the smoke check and the benchmark's
+// CPU-baseline leg use it.
+//
+// Sources (page title, passage):
+//  * "vllm-omni commits" (Spark export), the score-space join commit: the cache
+//    and the new token are scored separately and the two score vectors are
+//    concatenated; the sliding cache is a ring of window-1 slots that needs no
+//    reordering, only a mask for unwritten slots; each layer returns the new
+//    K/V entry for the runtime to drop into its ring slot.
+//  * same page, the Spark model commit: sliding layers rotate all 256 head dims
+//    with theta 1e4, full layers the first quarter with theta 5e6; a head-wise
+//    sigmoid output gate scales each head's attention output.
+//  * same page, the talker export commit: grouped-query attention by reshaping
+//    the query (contiguous groups of query heads share one KV head).
+//  * "TensorFold PR #608": verify windows of up to 16 streams x 16 rows, each
+//    row under its own tree mask; a verify row equals serial decode.
+//  * "pega-omni PR #4": paged KV leases addressed through a page table.
+//
+// Readings where the pages are silent (each is listed in the design notes):
+//  R1 RoPE pairs (i, i + r/2) inside the first r dims (rotate-half); the
+//     frequencies are theta^(-2i/r); dims >= r pass through.
+//  R2 score scale 1/sqrt(head_dim), no softcap.
+//  R3 query head h uses KV head h / G, G = Hq / Hkv.
+//  R5 a ring's valid slots are the `count` slots before `head` (cyclically);
+//     the new entry is written at `head`.
+//  R6 the new K entry is bf16_RNE(x*c - y*s) computed in fp64, with c and s
+//     the fp32-rounded cosine and sine of angle = pos * inv_freq (fp64). The
+//     new token is scored with that bf16 entry, i.e. exactly the value that is
+//     stored in the cache, so the score-space join equals attention over the
+//     concatenated key matrix.
+//  R7 gate: out = sigmoid(g_h) * attention output of head h.
+//  R10 tree rows: parent[i] < i, -1 marks a root; depth(root) = 0; row i sits
+//     at position prefix_len + depth(i) and attends to the prefix, its
+//     ancestors and itself.
+//
+// Build: g++ -O2 -std=c++17 -shared -fPIC -ffp-contract=off (oracle/build.py).
+// A compile-time ORACLE_MUTATION=n plants one known mistake, so the test suite
+// can show that its pins catch it; the default build plants none.
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+#ifndef ORACLE_MUTATION
+#define ORACLE_MUTATION 0
+#endif
+
+namespace {
+
+// ---------------------------------------------------------------- numbers
+
+double bf16_value(uint16_t h) {
+  uint32_t u = static_cast<uint32_t>(h) << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return static_cast<double>(f);
+}
+
+// Round an fp64 value to the nearest bf16, ties to even, in one step (no
+// intermediate fp32 rounding). bf16 keeps 8 significant bits and fp32's
+// exponent range, so the spacing of representable values around |t| is
+// 2^(e-7), with e the exponent of the leading bit, clamped at -126 below which
+// the spacing is that of the subnormals.
+uint16_t bf16_round(double t) {
+  if (std::isnan(t)) return 0x7fc0;
+  if (std::isinf(t)) return t > 0 ? 0x7f80 : 0xff80;
+  if (t == 0.0) return std::signbit(t) ? 0x8000 : 0x0000;
+  int e2;
+  std::frexp(std::fabs(t), &e2);  // |t| = f * 2^e2, f in [0.5, 1)
+  int lead = e2 - 1;
+  if (lead < -126) lead = -126;
+  const double spacing = std::ldexp(1.0, lead - 7);
+#if ORACLE_MUTATION == 14
+  double q = std::trunc(t / spacing) * spacing;  // planted: truncation
+#else
+  double q = std::nearbyint(t / spacing) * spacing;  // default mode: nearest-even
+#endif
+  if (std::fabs(q) >= std::ldexp(1.0, 128)) return std::signbit(t) ? 0xff80 : 0x7f80;
+  float f = static_cast<float>(q);  // exact: q has at most 8 significant bits
+  uint32_t u;
+  std::memcpy(&u, &f, sizeof u);
+  return static_cast<uint16_t>(u >> 16);
+}
+
+// ---------------------------------------------------------------- RoPE (R1, R6)
+
+// cos and sin of the rotation of pair i at position pos, each rounded to fp32.
+void rope_cos_sin(int r, double theta, int64_t pos, int i, double* c, double* s) {
+#if ORACLE_MUTATION == 7
+  (void)r;
+  const double expo = -static_cast<double>(2 * i) / 256.0;  // planted: freq over 256 dims
+#else
+  const double expo = -static_cast<double>(2 * i) / static_cast<double>(r);
+#endif
+  const double inv_freq = std::pow(theta, expo);
+  const double angle = static_cast<double>(pos) * inv_freq;
+  *c = static_cast<double>(static_cast<float>(std::cos(angle)));
+  *s = static_cast<double>(static_cast<float>(std::sin(angle)));
+}
+
+// Rotate the bf16 vector x (length D) at position pos. The result is fp64;
+// each product of a bf16 value and an fp32 value is exact in fp64, so the only
+// rounding is that of the final difference or sum.
+void rope_rotate(const uint16_t* x, int D, int r, double theta, int64_t pos, double* out) {
+  for (int d = 0; d < D; ++d) out[d] = bf16_value(x[d]);
+  const int half = r / 2;
+  for (int i = 0; i < half; ++i) {
+    double c, s;
+    rope_cos_sin(r, theta, pos, i, &c, &s);
+#if ORACLE_MUTATION == 6
+    // planted: adjacent pairs (2i, 2i+1) instead of (i, i + r/2)
+    const double a = bf16_value(x[2 * i]), b = bf16_value(x[2 * i + 1]);
+    out[2 * i] = a * c - b * s;
+    out[2 * i + 1] = b * c + a * s;
+#elif ORACLE_MUTATION == 5
+    const double a = bf16_value(x[i]), b = bf16_value(x[i + half]);
+    out[i] = a * c + b * s;  // planted: wrong sign
+    out[i + half] = b * c - a * s;
+#else
+    const double a = bf16_value(x[i]), b = bf16_value(x[i + half]);
+    out[i] = a * c - b * s;
+    out[i + half] = b * c + a * s;
+#endif
+  }
+}
+
+// The K entry the layer hands back: the rotated key rounded to bf16 (R6).
+void rope_entry(const uint16_t* x, int D, int r, double theta, int64_t pos, uint16_t* entry) {
+  std::vector<double> tmp(D);
+  rope_rotate(x, D, r, theta, pos, tmp.data());
+  for (int d = 0; d < D; ++d) entry[d] = bf16_round(tmp[d]);
+}
+
+double sigmoid(double g) {
+#if ORACLE_MUTATION == 12
+  return 1.0 / (1.0 + std::exp(g));  // planted: sigmoid(-g)
+#else
+  return 1.0 / (1.0 + std::exp(-g));
+#endif
+}
+
+double score_scale(int D) {
+#if ORACLE_MUTATION == 8
+  return 1.0 / static_cast<double>(D);  // planted: 1/D
+#else
+  return 1.0 / std::sqrt(static_cast<double>(D));
+#endif
+}
+
+int kv_head_of(int h, int Hq, int Hkv) {
+#if ORACLE_MUTATION == 3
+  (void)Hq;
+  return h % Hkv;  // planted: interleaved groups
+#else
+  return h / (Hq / Hkv);
+#endif
+}
+
+// ---------------------------------------------------------------- attention
+
+// One query row against a list of cached (key, value) rows plus a separately
+// held set of extra rows (the new token, or a verify row's tree path), joined
+// in score space: the two score vectors are concatenated, then one softmax.
+//   cached_k[t], cached_v[t]: bf16 rows of length D (t < n_cached)
+//   extra_k[a] (fp64, already rounded to bf16 values), extra_v[a] (bf16 rows)
+void attend_score_space(const double* qhat, int D,
+                        const std::vector<const uint16_t*>& cached_k,
+                        const std::vector<const uint16_t*>& cached_v,
+                        const std::vector<const double*>& extra_k,
+                        const std::vector<const uint16_t*>& extra_v,
+                        double* o) {
+  const double scale = score_scale(D);
+  const size_t n = cached_k.size();
+  std::vector<double> s_cache(n);
+  for (size_t t = 0; t < n; ++t) {
+    double acc = 0.0;
+    for (int d = 0; d < D; ++d) acc += qhat[d] * bf16_value(cached_k[t][d]);
+    s_cache[t] = acc * scale;
+  }
+  const size_t ne = extra_k.size();
+  std::vector<double> s_extra(ne);
+  for (size_t a = 0; a < ne; ++a) {
+    double acc = 0.0;
+    for (int d = 0; d < D; ++d) acc += qhat[d] * extra_k[a][d];
+    s_extra[a] = acc * scale;
+  }
+  // concatenate the score vectors: [s_cache (length n) | s_extra (length ne)]
+  std::vector<double> s(s_cache);
+#if ORACLE_MUTATION != 2
+  s.insert(s.end(), s_extra.begin(), s_extra.end());
+#endif
+  double m = -INFINITY;
+  for (double v : s) m = std::max(m, v);
+  std::vector<double> p(s.size());
+  double z = 0.0;
+  for (size_t t = 0; t < s.size(); ++t) {
+    p[t] = std::exp(s[t] - m);
+    z += p[t];
+  }
+  for (int d = 0; d < D; ++d) o[d] = 0.0;
+  for (size_t t = 0; t < n; ++t) {
+#if ORACLE_MUTATION == 13
+    const uint16_t* vrow = cached_k[t];  // planted: values taken from keys
+#else
+    const uint16_t* vrow = cached_v[t];
+#endif
+    for (int d = 0; d < D; ++d) o[d] += p[t] * bf16_value(vrow[d]);
+  }
+  for (size_t a = 0; a < s.size() - n; ++a)
+    for (int d = 0; d < D; ++d) o[d] += p[n + a] * bf16_value(extra_v[a][d]);
+  for (int d = 0; d < D; ++d) o[d] /= z;
+}
+
+// Key-space form: the keys (already rotated, as fp64 values of bf16 numbers)
+// and values are stacked into explicit matrices and attended in one pass.
+void attend_key_matrix(const double* qhat, int D, const std::vector<double>& K,
+                       const std::vector<double>& V, size_t rows, double* o) {
+  const double scale = 1.0 / std::sqrt(static_cast<double>(D));
+  std::vector<double> s(rows);
+  double m = -INFINITY;
+  for (size_t t = 0; t < rows; ++t) {
+    double acc = 0.0;
+    for (int d = 0; d < D; ++d) acc += qhat[d] * K[t * D + d];
+    s[t] = acc * scale;
+    m = std::max(m, s[t]);
+  }
+  double z = 0.0;
+  for (size_t t = 0; t < rows; ++t) {
+    s[t] = std::exp(s[t] - m);
+    z += s[t];
+  }
+  for (int d = 0; d < D; ++d) {
+    double acc = 0.0;
+    for (size_t t = 0; t < rows; ++t) acc += s[t] * V[t * D + d];
+    o[d] = acc / z;
+  }
+}
+
+// Run fn(item) for item in [0, n) on n_threads threads (0 = all cores).
+template <class Fn>
+void parallel_for(int n, int n_threads, Fn fn) {
+  if (n_threads <= 0) n_threads = static_cast<int>(std::thread::hardware_concurrency());
+  if (n_threads < 1) n_threads = 1;
+  if (n_threads > n) n_threads = n;
+  if (n_threads <= 1) {
+    for (int i = 0; i < n; ++i) fn(i);
+    return;
+  }
+  std::atomic<int> next{0};
+  std::vector<std::thread> pool;
+  for (int t = 0; t < n_threads; ++t)
+    pool.emplace_back([&] {
+      for (int i = next.fetch_add(1); i < n; i = next.fetch_add(1)) fn(i);
+    });
+  for (auto& th : pool) th.join();
+}
+
+struct DecodeTail {
+  const uint16_t* q;      // [B, Hq, D]
+  const uint16_t* k_new;  // [B, Hkv, D]
+  const uint16_t* v_new;  // [B, Hkv, D]
+  const uint16_t* gate;   // [B, Hq] or null
+  const int32_t* pos;     // [B]
+  double* out;            // [B, Hq, D]
+  uint16_t* k_entry;      // [B, Hkv, D] or null
+  uint16_t* v_entry;      // [B, Hkv, D] or null
+};
+
+// Shared per-(stream, KV head) step of every decode form once the list of
+// valid cached rows is known: rotate, score in score space, gate, entries.
+void decode_one(int b, int j, int Hq, int Hkv, int D, int r, double theta,
+                const std::vector<const uint16_t*>& ck, const std::vector<const uint16_t*>& cv,
+                const DecodeTail& a) {
+  const int64_t pos = a.pos[b];
+  const uint16_t* kn = a.k_new + (static_cast<size_t>(b) * Hkv + j) * D;
+  const uint16_t* vn = a.v_new + (static_cast<size_t>(b) * Hkv + j) * D;
+  std::vector<uint16_t> entry(D);
+  rope_entry(kn, D, r, theta, pos, entry.data());
+  std::vector<double> kent(D);
+  for (int d = 0; d < D; ++d) kent[d] = bf16_value(entry[d]);
+  if (a.k_entry) std::memcpy(a.k_entry + (static_cast<size_t>(b) * Hkv + j) * D, entry.data(), D * 2);
+  if (a.v_entry) std::memcpy(a.v_entry + (static_cast<size_t>(b) * Hkv + j) * D, vn, D * 2);
+  std::vector<double> qhat(D);
+  for (int h = 0; h < Hq; ++h) {
+    if (kv_head_of(h, Hq, Hkv) != j) continue;
+    rope_rotate(a.q + (static_cast<size_t>(b) * Hq + h) * D, D, r, theta, pos, qhat.data());
+    double* o = a.out + (static_cast<size_t>(b) * Hq + h) * D;
+    attend_score_space(qhat.data(), D, ck, cv, {kent.data()}, {vn}, o);
+#if ORACLE_MUTATION != 4
+    if (a.gate) {
+      const double g = sigmoid(bf16_value(a.gate[static_cast<size_t>(b) * Hq + h]));
+      for (int d = 0; d < D; ++d) o[d] *= g;
+    }
+#endif
+  }
+}
+
+bool shape_ok(int Hq, int Hkv, int D, int r) {
+  return Hq > 0 && Hkv > 0 && Hq % Hkv == 0 && D > 0 && r >= 0 && r <= D && r % 2 == 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+// ----- numbers and RoPE, exposed for the pins
+
+uint16_t oracle_bf16_round(double t) { return bf16_round(t); }
+
+int oracle_rope_f64(const uint16_t* x, int D, int r, double theta, int64_t pos, double* out) {
+  if (D <= 0 || r < 0 || r > D || r % 2) return 1;
+  rope_rotate(x, D, r, theta, pos, out);
+  return 0;
+}
+
+int oracle_rope_bf16(const uint16_t* x, int D, int r, double theta, int64_t pos, uint16_t* out) {
+  if (D <= 0 || r < 0 || r > D || r % 2) return 1;
+  rope_entry(x, D, r, theta, pos, out);
+  return 0;
+}
+
+// ----- decode over a ring of R slots per (row, KV head): k_ring/v_ring are
+// [n_rows, Hkv, R, D] bf16. Call row b uses ring row stream_rows[b] (identity
+// if null); its valid slots are the ring_count[b] slots before ring_head[b].
+int oracle_decode_ring(int B, int Hq, int Hkv, int D, int r, double theta,
+                       const uint16_t* k_ring, const uint16_t* v_ring, int n_rows, int R,
+                       const int32_t* stream_rows, const int32_t* ring_head,
+                       const int32_t* ring_count, const uint16_t* q, const uint16_t* k_new,
+                       const uint16_t* v_new, const uint16_t* gate, const int32_t* pos,
+                       double* out, uint16_t* k_entry, uint16_t* v_entry, int n_threads) {
+  if (!shape_ok(Hq, Hkv, D, r) || R <= 0) return 1;
+  for (int b = 0; b < B; ++b) {
+    const int row = stream_rows ? stream_rows[b] : b;
+    if (row < 0 || row >= n_rows) return 2;
+    if (ring_head[b] < 0 || ring_head[b] >= R || ring_count[b] < 0 || ring_count[b] > R) return 2;
+  }
+  const DecodeTail tail{q, k_new, v_new, gate, pos, out, k_entry, v_entry};
+  parallel_for(B * Hkv, n_threads, [&](int item) {
+    const int b = item / Hkv, j = item % Hkv;
+    const int row = stream_rows ? stream_rows[b] : b;
+    const size_t base = (static_cast<size_t>(row) * Hkv + j) * R;
+    std::vector<const uint16_t*> ck, cv;
+    for (int i = 0; i < ring_count[b]; ++i) {
+#if ORACLE_MUTATION == 1
+      const int slot = ((ring_head[b] - i) % R + R) % R;  // planted: off by one
+#else
+      const int slot = ((ring_head[b] - 1 - i) % R + R) % R;
+#endif
+      ck.push_back(k_ring + (base + slot) * D);
+      cv.push_back(v_ring + (base + slot) * D);
+    }
+    decode_one(b, j, Hq, Hkv, D, r, theta, ck, cv, tail);
+  });
+  return 0;
+}
+
+// ----- decode over paged leases: k_pages/v_pages are [num_pages, Hkv, P, D]
+// bf16; token t of stream b lives in page block_table[b*bt_stride + t/P] at
+// offset t % P; the stream holds seq_len[b] cached tokens.
+int oracle_decode_paged(int B, int Hq, int Hkv, int D, int r, double theta,
+                        const uint16_t* k_pages, const uint16_t* v_pages, int num_pages, int P,
+                        const int32_t* block_table, int bt_stride, const int32_t* seq_len,
+                        const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                        const uint16_t* gate, const int32_t* pos, double* out,
+                        uint16_t* k_entry, uint16_t* v_entry, int n_threads) {
+  if (!shape_ok(Hq, Hkv, D, r) || P <= 0) return 1;
+  for (int b = 0; b < B; ++b) {
+    if (seq_len[b] < 0 || (seq_len[b] + P - 1) / P > bt_stride) return 2;
+    for (int t = 0; t < seq_len[b]; t += P) {
+      const int pg = block_table[static_cast<size_t>(b) * bt_stride + t / P];
+      if (pg < 0 || pg >= num_pages) return 2;
+    }
+  }
+  const DecodeTail tail{q, k_new, v_new, gate, pos, out, k_entry, v_entry};
+  parallel_for(B * Hkv, n_threads, [&](int item) {
+    const int b = item / Hkv, j = item % Hkv;
+    std::vector<const uint16_t*> ck, cv;
+    for (int t = 0; t < seq_len[b]; ++t) {
+      const int pg = block_table[static_cast<size_t>(b) * bt_stride + t / P];
+#if ORACLE_MUTATION == 11
+      const int off = (t + 1) % P;  // planted: offset off by one
+#else
+      const int off = t % P;
+#endif
+      const size_t row = ((static_cast<size_t>(pg) * Hkv + j) * P + off) * D;
+      ck.push_back(k_pages + row);
+      cv.push_back(v_pages + row);
+    }
+    decode_one(b, j, Hq, Hkv, D, r, theta, ck, cv, tail);
+  });
+  return 0;
+}
+
+// ----- the key-space twin over a chronological ("roll") cache: k_chrono and
+// v_chrono are [B, Hkv, cap, D] bf16, oldest first, count[b] rows valid. The
+// new key is rotated, rounded to its bf16 entry and appended as one more row
+// of an explicit key matrix; attention runs over that matrix.
+int oracle_decode_concat(int B, int Hq, int Hkv, int D, int r, double theta,
+                         const uint16_t* k_chrono, const uint16_t* v_chrono, int cap,
+                         const int32_t* count, const uint16_t* q, const uint16_t* k_new,
+                         const uint16_t* v_new, const uint16_t* gate, const int32_t* pos,
+                         double* out, int n_threads) {
+  if (!shape_ok(Hq, Hkv, D, r)) return 1;
+  for (int b = 0; b < B; ++b)
+    if (count[b] < 0 || count[b] > cap) return 2;
+  parallel_for(B, n_threads, [&](int b) {
+    const int G = Hq / Hkv;
+    for (int h = 0; h < Hq; ++h) {
+      const int j = h / G;
+      const size_t base = (static_cast<size_t>(b) * Hkv + j) * cap;
+      const size_t rows = static_cast<size_t>(count[b]) + 1;
+      std::vector<double> K(rows * D), V(rows * D);
+      for (int t = 0; t < count[b]; ++t)
+        for (int d = 0; d < D; ++d) {
+          K[t * D + d] = bf16_value(k_chrono[(base + t) * D + d]);
+          V[t * D + d] = bf16_value(v_chrono[(base + t) * D + d]);
+        }
+      std::vector<uint16_t> entry(D);
+      const size_t nb = (static_cast<size_t>(b) * Hkv + j) * D;
+      rope_entry(k_new + nb, D, r, theta, pos[b], entry.data());
+      for (int d = 0; d < D; ++d) {
+        K[(rows - 1) * D + d] = bf16_value(entry[d]);
+        V[(rows - 1) * D + d] = bf16_value(v_new[nb + d]);
+      }
+      std::vector<double> qhat(D);
+      rope_rotate(q + (static_cast<size_t>(b) * Hq + h) * D, D, r, theta, pos[b], qhat.data());
+      double* o = out + (static_cast<size_t>(b) * Hq + h) * D;
+      attend_key_matrix(qhat.data(), D, K, V, rows, o);
+      if (gate) {
+        const double g = 1.0 / (1.0 + std::exp(-bf16_value(gate[static_cast<size_t>(b) * Hq + h])));
+        for (int d = 0; d < D; ++d) o[d] *= g;
+      }
+    }
+  });
+  return 0;
+}
+
+// ----- tree verify: S streams, T rows each. q [S,T,Hq,D], k/v [S,T,Hkv,D]
+// (k not yet rotated), parent [S,T] (parent[i] < i, -1 = root), prefix in
+// paged leases with prefix_len[s] tokens. Row i sits at position
+// prefix_len + depth(i); it attends to the whole prefix, its ancestors and
+// itself, each window key rotated at its own position. out [S,T,Hq,D];
+// k_entry [S,T,Hkv,D] receives every window key's bf16 entry.
+int oracle_verify(int S, int T, int Hq, int Hkv, int D, int r, double theta,
+                  const uint16_t* k_pages, const uint16_t* v_pages, int num_pages, int P,
+                  const int32_t* block_table, int bt_stride, const int32_t* prefix_len,
+                  const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                  const int32_t* parent, const uint16_t* gate, double* out,
+                  uint16_t* k_entry, int n_threads) {
+  if (!shape_ok(Hq, Hkv, D, r) || P <= 0 || T <= 0) return 1;
+  for (int s = 0; s < S; ++s) {
+    if (prefix_len[s] < 0 || (prefix_len[s] + P - 1) / P > bt_stride) return 2;
+    for (int t = 0; t < prefix_len[s]; t += P) {
+      const int pg = block_table[static_cast<size_t>(s) * bt_stride + t / P];
+      if (pg < 0 || pg >= num_pages) return 2;
+    }
+    for (int i = 0; i < T; ++i) {
+      const int pa = parent[static_cast<size_t>(s) * T + i];
+      if (pa < -1 || pa >= i) return 3;
+    }
+  }
+  parallel_for(S * Hkv, n_threads, [&](int item) {
+    const int s = item / Hkv, j = item % Hkv;
+    const int32_t* par = parent + static_cast<size_t>(s) * T;
+    // depth of each node by walking to its root
+    std::vector<int> depth(T);
+    for (int i = 0; i < T; ++i) {
+      int dpt = 0;
+      for (int a = par[i]; a >= 0; a = par[a]) ++dpt;
+#if ORACLE_MUTATION == 9
+      depth[i] = dpt + 1;  // planted: depth counted from 1
+#else
+      depth[i] = dpt;
+#endif
+    }
+    // rotated bf16 entries of the window keys, each at its own position
+    std::vector<uint16_t> ent(static_cast<size_t>(T) * D);
+    std::vector<double> entd(static_cast<size_t>(T) * D);
+    for (int i = 0; i < T; ++i) {
+      const size_t src = ((static_cast<size_t>(s) * T + i) * Hkv + j) * D;
+      rope_entry(k + src, D, r, theta, prefix_len[s] + depth[i], ent.data() + static_cast<size_t>(i) * D);
+      for (int d = 0; d < D; ++d) entd[static_cast<size_t>(i) * D + d] = bf16_value(ent[static_cast<size_t>(i) * D + d]);
+      if (k_entry) std::memcpy(k_entry + src, ent.data() + static_cast<size_t>(i) * D, D * 2);
+    }
+    // the prefix rows
+    std::vector<const uint16_t*> ck, cv;
+    for (int t = 0; t < prefix_len[s]; ++t) {
+      const int pg = block_table[static_cast<size_t>(s) * bt_stride + t / P];
+      const size_t row = ((static_cast<size_t>(pg) * Hkv + j) * P + t % P) * D;
+      ck.push_back(k_pages + row);
+      cv.push_back(v_pages + row);
+    }
+    std::vector<double> qhat(D);
+    for (int i = 0; i < T; ++i) {
+      // the row's tree path: itself and its ancestors
+      std::vector<const double*> ek;
+      std::vector<const uint16_t*> ev;
+#if ORACLE_MUTATION == 10
+      for (int a = 0; a < T; ++a) {  // planted: no tree mask
+#else
+      for (int a = i; a >= 0; a = par[a]) {
+#endif
+        ek.push_back(entd.data() + static_cast<size_t>(a) * D);
+        ev.push_back(v + ((static_cast<size_t>(s) * T + a) * Hkv + j) * D);
+      }
+      for (int h = 0; h < Hq; ++h) {
+        if (kv_head_of(h, Hq, Hkv) != j) continue;
+        const size_t qi = (static_cast<size_t>(s) * T + i) * Hq + h;
+        rope_rotate(q + qi * D, D, r, theta, prefix_len[s] + depth[i], qhat.data());
+        double* o = out + qi * D;
+        attend_score_space(qhat.data(), D, ck, cv, ek, ev, o);
+        if (gate) {
+          const double g = sigmoid(bf16_value(gate[qi]));
+          for (int d = 0; d < D; ++d) o[d] *= g;
+        }
+      }
+    }
+  });
+  return 0;
+}
+
+// ----- bulk append. Token t (< count[b]) of call row b goes to cache index
+// start_index[b] + t and, when rotate != 0, is rotated at position
+// start_pos[b] + t. k/v are [B, Tmax, Hkv, D]. The caches are updated in place.
+// Ring: index i of row stream_rows[b] is slot i mod R of [n_rows, Hkv, R, D].
+int oracle_append_ring(int B, int Tmax, int Hkv, int D, int r, double theta,
+                       uint16_t* k_ring, uint16_t* v_ring, int n_rows, int R,
+                       const int32_t* stream_rows, const int32_t* start_index,
+                       const int32_t* start_pos, const int32_t* count,
+                       const uint16_t* k, const uint16_t* v, int rotate) {
+  if (D <= 0 || r < 0 || r > D || r % 2 || R <= 0) return 1;
+  std::vector<uint16_t> entry(D);
+  for (int b = 0; b < B; ++b) {
+    const int row = stream_rows ? stream_rows[b] : b;
+    if (row < 0 || row >= n_rows || count[b] < 0 || count[b] > Tmax || start_index[b] < 0) return 2;
+    for (int t = 0; t < count[b]; ++t)
+      for (int j = 0; j < Hkv; ++j) {
+        const size_t src = ((static_cast<size_t>(b) * Tmax + t) * Hkv + j) * D;
+        const int slot = (start_index[b] + t) % R;
+        const size_t dst = ((static_cast<size_t>(row) * Hkv + j) * R + slot) * D;
+        if (rotate)
+          rope_entry(k + src, D, r, theta, start_pos[b] + t, entry.data());
+        else
+          std::memcpy(entry.data(), k + src, D * 2);
+        std::memcpy(k_ring + dst, entry.data(), D * 2);
+        std::memcpy(v_ring + dst, v + src, D * 2);
+      }
+  }
+  return 0;
+}
+
+// Paged: index i of row b is offset i % P of page block_table[b*bt_stride + i/P].
+int oracle_append_paged(int B, int Tmax, int Hkv, int D, int r, double theta,
+                        uint16_t* k_pages, uint16_t* v_pages, int num_pages, int P,
+                        const int32_t* block_table, int bt_stride, const int32_t* start_index,
+                        const int32_t* start_pos, const int32_t* count,
+                        const uint16_t* k, const uint16_t* v, int rotate) {
+  if (D <= 0 || r < 0 || r > D || r % 2 || P <= 0) return 1;
+  std::vector<uint16_t> entry(D);
+  for (int b = 0; b < B; ++b) {
+    if (count[b] < 0 || count[b] > Tmax || start_index[b] < 0) return 2;
+    if (count[b] > 0 && (start_index[b] + count[b] - 1) / P >= bt_stride) return 2;
+    for (int t = 0; t < count[b]; ++t) {
+      const int idx = start_index[b] + t;
+      const int pg = block_table[static_cast<size_t>(b) * bt_stride + idx / P];
+      if (pg < 0 || pg >= num_pages) return 2;
+      for (int j = 0; j < Hkv; ++j) {
+        const size_t src = ((static_cast<size_t>(b) * Tmax + t) * Hkv + j) * D;
+        const size_t dst = ((static_cast<size_t>(pg) * Hkv + j) * P + idx % P) * D;
+        if (rotate)
+          rope_entry(k + src, D, r, theta, start_pos[b] + t, entry.data());
+        else
+          std::memcpy(entry.data(), k + src, D * 2);
+        std::memcpy(k_pages + dst, entry.data(), D * 2);
+        std::memcpy(v_pages + dst, v + src, D * 2);
+      }
+    }
+  }
+  return 0;
+}
+
+int oracle_hardware_threads(void) {
+  return static_cast<int>(std::thread::hardware_concurrency());
+}
+
+int oracle_mutation(void) { return ORACLE_MUTATION; }
+
+}  // extern "C"

@@ -1,0 +1,495 @@
+"""Pins of the fp64 oracle to facts fixed outside it.
+
+Each check takes a loaded oracle build and raises AssertionError when the
+oracle disagrees with a closed form, a hand-derived golden value, a library
+routine on a special case, or an invariant the pages state. test_oracle_pins
+runs them all against the real oracle; test_oracle_mutations shows that every
+planted mistake in the oracle fails at least one of them.
+
+Passages (page title, section):
+  * vllm-omni commits, score-space join commit: cache and new token scored
+    separately, scores concatenated; ring of window-1 slots, order-free, masked
+    unwritten slots; a test pins ring and roll to the same output on a shared
+    history.
+  * vllm-omni commits, Spark model commit: per-layer-type RoPE; head-wise
+    sigmoid output gate.
+  * vllm-omni commits, talker export commit: GQA by reshaping the query.
+  * TensorFold PR #608: verify windows under tree masks; drafted == serial;
+    concurrent == alone.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+NAN = 0x7FC0
+
+
+def bf16(x):
+    """bf16 bits of values exactly representable in bf16 (test constants)."""
+    a = torch.tensor(np.asarray(x, np.float32)).to(torch.bfloat16)
+    return a.view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_val(bits):
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def rand_bf16(shape, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(shape, generator=g).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def f32(x):
+    return float(np.float32(x))
+
+
+def sigmoid(g):
+    return 1.0 / (1.0 + math.exp(-g))
+
+
+def close(a, b, tol, what):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    assert a.shape == b.shape, (what, a.shape, b.shape)
+    assert np.all(np.isfinite(a)), f"{what}: non-finite values"
+    err = np.max(np.abs(a - b)) if a.size else 0.0
+    assert err <= tol, f"{what}: max |diff| {err:.3e} > {tol:.1e}"
+
+
+def _parse_pow2(expr: str) -> float:
+    """Evaluate the small arithmetic used in the golden file (powers of 2)."""
+    return float(eval(expr.replace("^", "**"), {"__builtins__": {}}, {}))
+
+
+# ------------------------------------------------------------------ numbers
+
+def pin_bf16_rounding_golden(o):
+    cases = json.load(open(os.path.join(GOLDEN, "bf16_rounding.json")))["cases"]
+    for c in cases:
+        x = _parse_pow2(c["x"])
+        got = o.bf16_round(x)
+        assert got == int(c["bits"], 16), f"bf16({c['x']}) = {got:#06x}, want {c['bits']} ({c['why']})"
+
+
+def pin_bf16_rounding_matches_fp32_conversion(o):
+    """For values exactly representable in fp32, one-step rounding from fp64
+    equals the library's fp32 -> bf16 round-to-nearest-even conversion."""
+    g = torch.Generator().manual_seed(7)
+    x = torch.randn(4000, generator=g) * torch.exp(torch.randn(4000, generator=g) * 8)
+    want = x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([o.bf16_round(float(v)) for v in x.numpy()], np.uint16)
+    assert np.array_equal(got, want), f"{np.sum(got != want)} of 4000 differ"
+
+
+# ------------------------------------------------------------------ RoPE
+
+def _golden_sym(expr: str) -> float:
+    env = {"c": lambda a: f32(math.cos(a)), "s": lambda a: f32(math.sin(a))}
+    return float(eval(expr, {"__builtins__": {}}, env))
+
+
+def pin_rope_golden(o):
+    cases = json.load(open(os.path.join(GOLDEN, "rope_cases.json")))["cases"]
+    for c in cases:
+        D = c["D"]
+        x = np.zeros(D, np.float32)
+        for k, val in c["x"].items():
+            x[int(k)] = val
+        want = x.astype(np.float64)
+        for k in c["x"]:
+            if k not in c["expect"]:
+                want[int(k)] = 0.0
+        for k, e in c["expect"].items():
+            want[int(k)] = _golden_sym(e)
+        got = o.rope_f64(bf16(x), c["r"], c["theta"], c["pos"])
+        close(got, want, 1e-15, f"rope golden ({c['why']})")
+
+
+def pin_rope_r2_is_complex_multiplication(o):
+    """r = 2: the single pair turns like (x0 + i x1) * exp(i pos)."""
+    x = rand_bf16(2, 11)
+    xv = bf16_val(x)
+    for pos in (1, 2, 7, 100, 4097, 1 << 20):
+        z = complex(xv[0], xv[1]) * complex(f32(math.cos(pos)), f32(math.sin(pos)))
+        got = o.rope_f64(x, 2, 12345.0, pos)
+        close(got, [z.real, z.imag], 1e-15, f"r=2 pos={pos}")
+
+
+def pin_rope_norm_and_relative_position(o):
+    """Rotation keeps the norm, and <R(m) q, R(n) k> depends only on m - n
+    (up to the fp32 rounding of cos and sin)."""
+    q = rand_bf16(64, 12)
+    k = rand_bf16(64, 13)
+    nq = np.linalg.norm(bf16_val(q))
+    for r, theta in ((64, 1e4), (16, 5e6)):
+        for m in (0, 5, 300, 70000):
+            close([np.linalg.norm(o.rope_f64(q, r, theta, m))], [nq], 1e-5 * nq, "norm")
+        base = np.dot(o.rope_f64(q, r, theta, 40), o.rope_f64(k, r, theta, 10))
+        for shift in (1, 17, 1000):
+            other = np.dot(o.rope_f64(q, r, theta, 40 + shift), o.rope_f64(k, r, theta, 10 + shift))
+            close([other], [base], 1e-4, f"relative position shift {shift}")
+
+
+def pin_rope_entry_identity(o):
+    """At position 0, and with no rotary dims, the K entry is the key itself."""
+    x = rand_bf16(256, 14)
+    assert np.array_equal(o.rope_bf16(x, 256, 1e4, 0), x)
+    assert np.array_equal(o.rope_bf16(x, 0, 1e4, 999), x)
+
+
+# ------------------------------------------------------------------ decode helpers
+
+def ring_decode(o, K, V, head, count, q, kn, vn, pos, r=0, theta=1e4, gate=None):
+    """K, V: [R, Hkv, D] float data for one stream, laid out per slot."""
+    Kb = bf16(K).transpose(1, 0, 2)[None].copy()
+    Vb = bf16(V).transpose(1, 0, 2)[None].copy()
+    out, ke, ve = o.decode_ring(Kb, Vb, [head], [count], bf16(q)[None], bf16(kn)[None],
+                                bf16(vn)[None], [pos], r, theta,
+                                gate=None if gate is None else bf16(gate)[None])
+    return out[0], ke[0], ve[0]
+
+
+def _nan_ring(R, Hkv, D):
+    K = np.full((R, Hkv, D), np.nan, np.float32)
+    V = np.full((R, Hkv, D), np.nan, np.float32)
+    return K, V
+
+
+# ------------------------------------------------------------------ closed forms
+
+def pin_empty_cache_is_gated_v_new(o):
+    """No cached token: the softmax has one entry, out = sigmoid(g) * v_new."""
+    D, Hq, Hkv, R = 8, 4, 2, 5
+    K, V = _nan_ring(R, Hkv, D)
+    q = bf16_val(rand_bf16((Hq, D), 21)).astype(np.float32)
+    kn = bf16_val(rand_bf16((Hkv, D), 22)).astype(np.float32)
+    vn = bf16_val(rand_bf16((Hkv, D), 23)).astype(np.float32)
+    g = np.array([0.5, -1.0, 2.0, 0.0], np.float32)
+    out, _, _ = ring_decode(o, K, V, 3, 0, q, kn, vn, 17, r=8, theta=1e4, gate=g)
+    want = np.stack([sigmoid(float(g[h])) * vn[h // 2].astype(np.float64) for h in range(Hq)])
+    close(out, want, 1e-15, "empty cache")
+
+
+def pin_two_keys_logistic(o):
+    """One cached key: the two-way softmax is the logistic function of the score
+    difference. q = a e0, cached key e0, new key 0, position 0 (no turn):
+    s_cache = a / sqrt(D), s_new = 0."""
+    for D in (4, 16):
+        Hq = Hkv = 1
+        R = 3
+        K, V = _nan_ring(R, Hkv, D)
+        K[1, 0] = 0.0
+        K[1, 0, 0] = 1.0
+        V[1, 0] = bf16_val(rand_bf16(D, 31 + D))
+        vn = bf16_val(rand_bf16((1, D), 41 + D)).astype(np.float32)
+        a = 3.0
+        q = np.zeros((Hq, D), np.float32)
+        q[0, 0] = a
+        kn = np.zeros((Hkv, D), np.float32)
+        out, _, _ = ring_decode(o, K, V, 2, 1, q, kn, vn, 0, r=D)
+        p1 = 1.0 / (1.0 + math.exp(-a / math.sqrt(D)))
+        want = p1 * V[1, 0].astype(np.float64) + (1 - p1) * vn[0].astype(np.float64)
+        close(out[0], want, 1e-14, f"two-key logistic D={D}")
+
+
+def pin_uniform_weights_when_q_is_zero(o):
+    """q = 0 gives every key the same score: out = mean of the attended values."""
+    D, Hq, Hkv, R = 8, 2, 1, 9
+    K, V = _nan_ring(R, Hkv, D)
+    head, count = 4, 6
+    slots = [(head - 1 - i) % R for i in range(count)]
+    for s in slots:
+        K[s] = bf16_val(rand_bf16((Hkv, D), 50 + s))
+        V[s] = bf16_val(rand_bf16((Hkv, D), 60 + s))
+    vn = bf16_val(rand_bf16((Hkv, D), 70)).astype(np.float32)
+    kn = bf16_val(rand_bf16((Hkv, D), 71)).astype(np.float32)
+    out, _, _ = ring_decode(o, K, V, head, count, np.zeros((Hq, D), np.float32), kn, vn, 33, r=8)
+    want = (sum(V[s, 0].astype(np.float64) for s in slots) + vn[0]) / (count + 1)
+    close(out, np.stack([want, want]), 1e-15, "q = 0 mean")
+
+
+def pin_ring_valid_slots_onehot(o):
+    """A ring's valid slots are the `count` slots before `head` (cyclically).
+    With q = 0 and V[slot] = e_slot, the output spells out the set that was
+    attended; unwritten slots hold NaN. Hand-derived: R = 5, head = 1, count = 3
+    attends slots {0, 4, 3}; head = 0, count = 5 attends all five."""
+    D, R = 8, 5
+    for head, count, want_slots in ((1, 3, [0, 4, 3]), (0, 5, [0, 1, 2, 3, 4]), (3, 1, [2])):
+        K, V = _nan_ring(R, 1, D)
+        for s in want_slots:
+            K[s, 0] = 0.0
+            V[s, 0] = 0.0
+            V[s, 0, s] = 1.0
+        vn = np.zeros((1, D), np.float32)
+        vn[0, 7] = 1.0
+        out, _, _ = ring_decode(o, K, V, head, count, np.zeros((1, D), np.float32),
+                                np.zeros((1, D), np.float32), vn, 9, r=8)
+        want = np.zeros(D)
+        want[want_slots] = 1.0 / (count + 1)
+        want[7] = 1.0 / (count + 1)
+        close(out[0], want, 1e-15, f"ring slots head={head} count={count}")
+
+
+def pin_paged_traversal_onehot(o):
+    """Token t of a stream lives at offset t % P of page block_table[t // P].
+    With q = 0 and V = e_t at token t, the output is the uniform mix of the
+    first seq_len tokens and the new one; the free slot holds NaN."""
+    D, P, Hkv = 8, 2, 1
+    bt = np.array([[2, 0, 1]], np.int32)
+    n = 5
+    Kp = np.full((3, Hkv, P, D), np.nan, np.float32)
+    Vp = np.full((3, Hkv, P, D), np.nan, np.float32)
+    for t in range(n):
+        pg, off = bt[0, t // P], t % P
+        Kp[pg, 0, off] = 0.0
+        Vp[pg, 0, off] = 0.0
+        Vp[pg, 0, off, t] = 1.0
+    vn = np.zeros((1, 1, D), np.float32)
+    vn[0, 0, 7] = 1.0
+    out, _, _ = o.decode_paged(bf16(Kp), bf16(Vp), bt, [n], bf16(np.zeros((1, 1, D))),
+                               bf16(np.zeros((1, 1, D))), bf16(vn), [n], 8, 1e4)
+    want = np.zeros(D)
+    want[:n] = 1.0 / (n + 1)
+    want[7] = 1.0 / (n + 1)
+    close(out[0, 0], want, 1e-15, "paged traversal")
+
+
+def pin_gqa_contiguous_groups(o):
+    """Query head h reads KV head h // G (the query is reshaped into groups)."""
+    D, Hq, Hkv, R = 4, 4, 2, 3
+    K = np.zeros((R, Hkv, D), np.float32)
+    V = np.zeros((R, Hkv, D), np.float32)
+    V[:, 0] = 1.0
+    V[:, 1] = -1.0
+    vn = np.array([[1.0] * D, [-1.0] * D], np.float32)
+    q = bf16_val(rand_bf16((Hq, D), 80)).astype(np.float32)
+    out, _, _ = ring_decode(o, K, V, 0, 3, q, np.zeros((Hkv, D), np.float32), vn, 4, r=4)
+    close(out, np.array([[1.0] * D, [1.0] * D, [-1.0] * D, [-1.0] * D]), 1e-15, "gqa map")
+
+
+def pin_gate_scales_by_sigmoid(o):
+    """out_gated = sigmoid(g) * out_ungated; g = 0 halves the output."""
+    D, Hq, Hkv, R = 8, 2, 1, 6
+    K = bf16_val(rand_bf16((R, Hkv, D), 90)).astype(np.float32)
+    V = bf16_val(rand_bf16((R, Hkv, D), 91)).astype(np.float32)
+    q = bf16_val(rand_bf16((Hq, D), 92)).astype(np.float32)
+    kn = bf16_val(rand_bf16((Hkv, D), 93)).astype(np.float32)
+    vn = bf16_val(rand_bf16((Hkv, D), 94)).astype(np.float32)
+    base, _, _ = ring_decode(o, K, V, 2, 6, q, kn, vn, 20, r=8)
+    g = np.array([0.0, 2.0], np.float32)
+    gated, _, _ = ring_decode(o, K, V, 2, 6, q, kn, vn, 20, r=8, gate=g)
+    close(gated, base * np.array([[0.5], [sigmoid(2.0)]]), 1e-15, "gate")
+
+
+# ------------------------------------------------------------------ invariants
+
+def pin_score_space_join_equals_key_concat(o):
+    """Scoring the cache and the new token separately and concatenating the
+    score vectors equals attention over the concatenated key matrix."""
+    B, Hq, Hkv, D, R = 3, 8, 2, 32, 13
+    counts = [13, 7, 0]
+    heads = [5, 12, 3]
+    hist_k = rand_bf16((B, Hkv, R, D), 100)
+    hist_v = rand_bf16((B, Hkv, R, D), 101)
+    Kr = np.full((B, Hkv, R, D), NAN, np.uint16)
+    Vr = np.full((B, Hkv, R, D), NAN, np.uint16)
+    for b in range(B):
+        for t in range(counts[b]):  # oldest first: token t sits count - t slots before head
+            slot = (heads[b] - counts[b] + t) % R
+            Kr[b, :, slot] = hist_k[b, :, t]
+            Vr[b, :, slot] = hist_v[b, :, t]
+    q = rand_bf16((B, Hq, D), 102)
+    kn = rand_bf16((B, Hkv, D), 103)
+    vn = rand_bf16((B, Hkv, D), 104)
+    g = rand_bf16((B, Hq), 105)
+    pos = [40, 41, 0]
+    join, _, _ = o.decode_ring(Kr, Vr, heads, counts, q, kn, vn, pos, 32, 1e4, gate=g)
+    cat = o.decode_concat(hist_k, hist_v, counts, q, kn, vn, pos, 32, 1e4, gate=g)
+    close(join, cat, 1e-12, "join vs concat")
+
+
+def pin_ring_equals_roll_over_history(o):
+    """Ring (write at head, no reordering) and roll (append, drop the oldest,
+    concatenate keys) give the same output at every step of a shared history
+    longer than the ring."""
+    Hq, Hkv, D, R = 4, 2, 16, 7
+    r, theta = 16, 1e4
+    Kr = np.full((1, Hkv, R, D), NAN, np.uint16)
+    Vr = np.full((1, Hkv, R, D), NAN, np.uint16)
+    roll_k, roll_v = [], []  # chronological lists of [Hkv, D] entries
+    head, count = 0, 0
+    for step in range(20):
+        q = rand_bf16((1, Hq, D), 200 + step)
+        kn = rand_bf16((1, Hkv, D), 300 + step)
+        vn = rand_bf16((1, Hkv, D), 400 + step)
+        out_ring, ke, ve = o.decode_ring(Kr, Vr, [head], [count], q, kn, vn, [step], r, theta)
+        kc = np.full((1, Hkv, R, D), NAN, np.uint16)
+        vc = np.full((1, Hkv, R, D), NAN, np.uint16)
+        for t, (a, b_) in enumerate(zip(roll_k, roll_v)):
+            kc[0, :, t] = a
+            vc[0, :, t] = b_
+        out_roll = o.decode_concat(kc, vc, [len(roll_k)], q, kn, vn, [step], r, theta)
+        close(out_ring, out_roll, 1e-12, f"ring vs roll step {step}")
+        # ring: drop the entry into slot `head`; roll: append, slice off the oldest
+        Kr[0, :, head] = ke[0]
+        Vr[0, :, head] = ve[0]
+        head = (head + 1) % R
+        count = min(count + 1, R)
+        roll_k.append(ke[0])
+        roll_v.append(ve[0])
+        if len(roll_k) > R:
+            roll_k.pop(0)
+            roll_v.pop(0)
+
+
+def pin_slot_order_irrelevant_and_masked_nan(o):
+    """Permuting the physical pages of a paged cache, or adding NaN-filled
+    unused pages, changes nothing."""
+    B, Hq, Hkv, D, P = 2, 4, 2, 16, 4
+    lens = [9, 14]
+    toks_k = rand_bf16((B, 16, Hkv, D), 500)
+    toks_v = rand_bf16((B, 16, Hkv, D), 501)
+    q, kn, vn = rand_bf16((B, Hq, D), 502), rand_bf16((B, Hkv, D), 503), rand_bf16((B, Hkv, D), 504)
+    outs = []
+    for perm_seed in (None, 1, 2):
+        n_pages = 12
+        phys = np.arange(n_pages) if perm_seed is None else \
+            np.random.default_rng(perm_seed).permutation(n_pages)
+        Kp = np.full((n_pages, Hkv, P, D), NAN, np.uint16)
+        Vp = np.full((n_pages, Hkv, P, D), NAN, np.uint16)
+        bt = np.full((B, 4), -1, np.int32)
+        nxt = 0
+        for b in range(B):
+            for pg in range((lens[b] + P - 1) // P):
+                bt[b, pg] = phys[nxt]
+                nxt += 1
+            for t in range(lens[b]):
+                Kp[bt[b, t // P], :, t % P] = toks_k[b, t]
+                Vp[bt[b, t // P], :, t % P] = toks_v[b, t]
+        out, _, _ = o.decode_paged(Kp, Vp, bt, lens, q, kn, vn, lens, 16, 1e6)
+        outs.append(out)
+    close(outs[1], outs[0], 1e-15, "page permutation 1")
+    close(outs[2], outs[0], 1e-15, "page permutation 2")
+
+
+def pin_batch_equals_alone(o):
+    """A stream's result does not depend on the other streams in the call."""
+    B, Hq, Hkv, D, R = 4, 4, 2, 16, 9
+    Kr = rand_bf16((B, Hkv, R, D), 600)
+    Vr = rand_bf16((B, Hkv, R, D), 601)
+    q, kn, vn = rand_bf16((B, Hq, D), 602), rand_bf16((B, Hkv, D), 603), rand_bf16((B, Hkv, D), 604)
+    g = rand_bf16((B, Hq), 605)
+    heads, counts, pos = [0, 3, 8, 5], [9, 4, 2, 0], [11, 4, 2, 0]
+    full, ke, ve = o.decode_ring(Kr, Vr, heads, counts, q, kn, vn, pos, 16, 1e4, gate=g)
+    for b in range(B):
+        one, k1, v1 = o.decode_ring(Kr[b:b + 1], Vr[b:b + 1], heads[b:b + 1], counts[b:b + 1],
+                                    q[b:b + 1], kn[b:b + 1], vn[b:b + 1], pos[b:b + 1], 16, 1e4,
+                                    gate=g[b:b + 1])
+        assert np.array_equal(one[0], full[b]) and np.array_equal(k1[0], ke[b])
+
+
+# ------------------------------------------------------------------ verify
+
+def _prefix_pool(S, Hkv, D, P, lens, room, seed):
+    pages = [(n + room + P - 1) // P for n in lens]
+    n_pages = sum(pages) + 1
+    phys = np.random.default_rng(seed).permutation(n_pages)
+    Kp = np.full((n_pages, Hkv, P, D), NAN, np.uint16)
+    Vp = np.full((n_pages, Hkv, P, D), NAN, np.uint16)
+    bt = np.full((S, max(pages)), -1, np.int32)
+    nxt = 0
+    for s in range(S):
+        bt[s, :pages[s]] = phys[nxt:nxt + pages[s]]
+        nxt += pages[s]
+        kk = rand_bf16((lens[s], Hkv, D), seed + 10 + s)
+        vv = rand_bf16((lens[s], Hkv, D), seed + 40 + s)
+        for t in range(lens[s]):
+            Kp[bt[s, t // P], :, t % P] = kk[t]
+            Vp[bt[s, t // P], :, t % P] = vv[t]
+    return Kp, Vp, bt
+
+
+def pin_verify_row_equals_decode_of_its_path(o):
+    """Each verify row equals a plain decode of that row's token after its
+    root-to-parent path has been appended to the prefix at positions
+    prefix_len + depth (drafted == serial)."""
+    S, T, Hq, Hkv, D, P = 2, 8, 6, 2, 16, 4
+    r, theta = 8, 5e6
+    lens = [10, 5]
+    parent = np.array([[-1, 0, 0, 1, 3, 2, 4, -1], [-1, 0, 1, 2, 3, 4, 5, 6]], np.int32)
+    Kp, Vp, bt = _prefix_pool(S, Hkv, D, P, lens, T + 1, 700)
+    q = rand_bf16((S, T, Hq, D), 701)
+    k = rand_bf16((S, T, Hkv, D), 702)
+    v = rand_bf16((S, T, Hkv, D), 703)
+    g = rand_bf16((S, T, Hq), 704)
+    out, ke = o.verify(Kp, Vp, bt, lens, q, k, v, parent, r, theta, gate=g)
+    for s in range(S):
+        for i in range(T):
+            path = []
+            a = parent[s, i]
+            while a >= 0:
+                path.append(a)
+                a = parent[s, a]
+            path.reverse()  # root first; node path[d] has depth d
+            Kd, Vd = Kp.copy(), Vp.copy()
+            for d, a in enumerate(path):
+                t = lens[s] + d
+                Kd[bt[s, t // P], :, t % P] = [o.rope_bf16(k[s, a, j], r, theta, t) for j in range(Hkv)]
+                Vd[bt[s, t // P], :, t % P] = v[s, a]
+            n = lens[s] + len(path)
+            dec, kent, _ = o.decode_paged(Kd, Vd, bt[s:s + 1], [n], q[s, i][None], k[s, i][None],
+                                          v[s, i][None], [n], r, theta, gate=g[s, i][None])
+            close(out[s, i], dec[0], 1e-12, f"verify row {s},{i}")
+            assert np.array_equal(ke[s, i], kent[0]), "window entry differs from the decode entry"
+
+
+def pin_verify_chain_equals_sequential_decodes(o):
+    """A chain tree is T serial decode steps, each appending its entry."""
+    S, T, Hq, Hkv, D, P = 1, 6, 4, 2, 16, 4
+    r, theta = 16, 1e4
+    lens = [7]
+    Kp, Vp, bt = _prefix_pool(S, Hkv, D, P, lens, T + 1, 800)
+    q = rand_bf16((S, T, Hq, D), 801)
+    k = rand_bf16((S, T, Hkv, D), 802)
+    v = rand_bf16((S, T, Hkv, D), 803)
+    parent = np.arange(-1, T - 1, dtype=np.int32)[None]
+    out, _ = o.verify(Kp, Vp, bt, lens, q, k, v, parent, r, theta)
+    Kd, Vd = Kp.copy(), Vp.copy()
+    n = lens[0]
+    for i in range(T):
+        dec, ke, ve = o.decode_paged(Kd, Vd, bt, [n], q[0, i][None], k[0, i][None], v[0, i][None],
+                                     [n], r, theta)
+        close(out[0, i], dec[0], 1e-12, f"chain step {i}")
+        Kd[bt[0, n // P], :, n % P] = ke[0]
+        Vd[bt[0, n // P], :, n % P] = ve[0]
+        n += 1
+
+
+def pin_append_places_rotated_entries(o):
+    """Bulk append writes token t at cache index start + t, rotated at its own
+    position; the one-hot layout shows where each token landed."""
+    Hkv, D, P = 2, 8, 4
+    bt = np.array([[3, 1, 0], [2, 4, -1]], np.int32)
+    Kp = np.full((5, Hkv, P, D), NAN, np.uint16)
+    Vp = Kp.copy()
+    Tm = 5
+    k = rand_bf16((2, Tm, Hkv, D), 900)
+    v = rand_bf16((2, Tm, Hkv, D), 901)
+    start_index, start_pos, count = [2, 1], [100, 7], [5, 4]
+    Ko, Vo = o.append_paged(Kp, Vp, bt, start_index, start_pos, count, k, v, 8, 1e4, rotate=True)
+    for b in range(2):
+        for t in range(count[b]):
+            i = start_index[b] + t
+            for j in range(Hkv):
+                assert np.array_equal(Ko[bt[b, i // P], j, i % P],
+                                      o.rope_bf16(k[b, t, j], 8, 1e4, start_pos[b] + t))
+                assert np.array_equal(Vo[bt[b, i // P], j, i % P], v[b, t, j])
+    written = sum(count) * Hkv * D
+    assert np.sum(Ko != NAN) == written and np.sum(Vo != NAN) == written
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -1,0 +1,29 @@
+"""Every planted mistake in the oracle fails at least one pin.
+
+Each mutation is a build of the oracle with one plausible error compiled in
+(ORACLE_MUTATION in dattn_oracle.cpp): an off-by-one ring slot, a dropped new
+token, a wrong KV-head map, a skipped gate, a RoPE sign flip, adjacent RoPE
+pairs, frequencies over the wrong width, a wrong score scale, a tree depth off
+by one, a missing tree mask, a page offset off by one, sigmoid(-g), values
+taken from keys, truncation instead of rounding. If one of them passed every
+pin, the pins would not be sharp enough to trust the oracle.
+"""
+import pytest
+
+import oracle as oracle_pkg
+from oracle_pins import ALL_PINS
+
+MUTATIONS = list(range(1, 15))
+
+
+@pytest.mark.parametrize("mutation", MUTATIONS)
+def test_mutation_is_caught(mutation):
+    o = oracle_pkg.Oracle(mutation)
+    assert o.lib.oracle_mutation() == mutation
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin(o)
+        except (AssertionError, ValueError, FloatingPointError):
+            caught.append(pin.__name__)
+    assert caught, f"mutation {mutation} passed every pin"
