@@ -1,0 +1,501 @@
+#!/usr/bin/env python
+"""Throughput of decode attention over per-stream KV caches on one GB300.
+
+Workload (one "step"): the 28-layer hybrid decode step, [sliding x3, full] x7,
+8 query / 2 KV heads, head_dim 256, 64 streams at context 4096. Sliding layers
+hold full rings of 511 slots (RoPE on 256 dims, theta 1e4); full layers hold
+4096 tokens in 16-token pages from a permuted pool (RoPE on the first 64 dims,
+theta 5e6); every layer applies the sigmoid head gate and writes its new K/V
+entry back. Synthetic data: bf16 N(0, 1), drawn on the device with a seeded
+generator. A step moves ~5.2 GB of K/V, far more than the 129 MB L2, so no L2
+flush is needed between steps.
+
+Metric: algorithmic HBM GB/s (bytes the method must move / time) and attended
+KV tokens/s. The 28 calls of a step are captured in one CUDA graph; K steps are
+timed with CUDA events between a barrier and a synchronize on both sides.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dattn|reference]
+
+`--impl reference` times the fp64 CPU oracle on a bounded sample of the same
+workload (it is the only reference this method has). Under torchrun (N > 1)
+every rank runs its own replica of the workload (weak scaling, no collective on
+the data path); rank 0 prints one JSON line.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attention achieved HBM GB/s (% of GB300 peak) and attended KV tokens/s"
+B_STREAMS = 64
+CONTEXT = 4096
+HQ, HKV, D = 8, 2, 256
+SEED = 1
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------- accounting
+
+def layer_bytes(kind, B, n_cached, P=16):
+    """Algorithmic bytes of one decode call: the cached K/V read once, plus the
+    call's small inputs and outputs (q, k_new, v_new, gate, out, the written
+    entry, and the index metadata read)."""
+    kv = B * n_cached * 2 * HKV * D * 2
+    io = B * (HQ * D * 2 + 2 * HKV * D * 2 + HQ * 2 + HQ * D * 4 + 2 * HKV * D * 2)
+    if kind == "sliding":
+        meta = B * 3 * 4
+    else:
+        meta = B * (4 + 4 + ((n_cached + P) // P) * 4)
+    return kv, io + meta
+
+
+def step_accounting(B, context):
+    kv_total = io_total = tokens = 0
+    per_kind = {}
+    import synth
+    for kind in synth.HYBRID_PATTERN:
+        n = min(context, 511) if kind == "sliding" else context
+        kv, io = layer_bytes(kind, B, n)
+        kv_total += kv
+        io_total += io
+        tokens += B * (n + 1)
+        per_kind[kind] = (kv, io, B * (n + 1))
+    return kv_total + io_total, tokens, per_kind
+
+
+def peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax.append(float(p[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, p[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value of x over the ranks (x itself when there is one rank)."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- the step
+
+class Step:
+    def __init__(self, B, context, seed, device="cuda"):
+        import decode_attention_kv_dattn_gb300 as dattn
+        import synth
+        self.dattn = dattn
+        self.B, self.context = B, context
+        self.layers = synth.hybrid_step_device(seed, B, context, device)
+        cfgs = []
+        for L in self.layers:
+            if L["kind"] == "sliding":
+                cfgs.append({"kind": dattn.CACHE_RING, "ring_slots": L["R"],
+                             "rotary_dim": L["rope"].rotary_dim, "rope_theta": L["rope"].theta})
+            else:
+                cfgs.append({"kind": dattn.CACHE_PAGED, "page_size": L["P"],
+                             "rotary_dim": L["rope"].rotary_dim, "rope_theta": L["rope"].theta})
+        self.h = dattn.Handle(HQ, HKV, D, cfgs, B, max_context=context)
+        self.descs = []
+        for L in self.layers:
+            if L["kind"] == "sliding":
+                self.descs.append(dattn.ring_cache(L["k"], L["v"], L["head"], L["count"], L["rows"]))
+            else:
+                self.descs.append(dattn.paged_cache(L["k"], L["v"], L["block_table"], L["seq_len"]))
+        # the per-step inputs live in one packed device buffer (so the end-to-end
+        # leg can refresh them with one host-to-device copy) and the outputs in one
+        self.in_elems = [L["q"].numel() + L["k_new"].numel() + L["v_new"].numel() + L["gate"].numel()
+                         for L in self.layers]
+        total = sum(self.in_elems)
+        self.inbuf = torch.empty(total, dtype=torch.bfloat16, device=device)
+        off = 0
+        for L in self.layers:
+            for name in ("q", "k_new", "v_new", "gate"):
+                n = L[name].numel()
+                view = self.inbuf[off:off + n].view(L[name].shape)
+                view.copy_(L[name])
+                L[name] = view
+                off += n
+        self.out = torch.empty((len(self.layers), B, HQ, D), dtype=torch.float32, device=device)
+        self.graph = None
+
+    def run_layer(self, l, stream=None):
+        L = self.layers[l]
+        self.h.decode(l, self.descs[l], L["q"], L["k_new"], L["v_new"], L["pos"], self.out[l],
+                      gate=L["gate"], max_seq_len=self.context if L["kind"] == "full" else 0,
+                      write_back=True, stream=stream)
+
+    def run_eager(self):
+        for l in range(len(self.layers)):
+            self.run_layer(l)
+
+    def capture(self):
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.run_eager()  # first calls set kernel attributes outside the capture
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.run_eager()
+        torch.cuda.synchronize()
+
+    def launches_per_step(self):
+        return 3 * len(self.layers)
+
+
+def time_graph(step, K, W, world):
+    for _ in range(W):
+        step.graph.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        step.graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    return e0.elapsed_time(e1) / 1e3
+
+
+def time_layers(step, K):
+    """Per-call device time of each layer (CUDA events on the launch stream
+    around each call: the call's RoPE, split and combine kernels)."""
+    n = len(step.layers)
+    reps = max(3, min(K, 50))
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)] for _ in range(reps)]
+    for r in range(reps):
+        for l in range(n):
+            ev[r][l][0].record()
+            step.run_layer(l)
+            ev[r][l][1].record()
+    torch.cuda.synchronize()
+    per = [statistics.mean(ev[r][l][0].elapsed_time(ev[r][l][1]) for r in range(reps)) / 1e3
+           for l in range(n)]
+    return per
+
+
+def time_e2e(step, K, W, world):
+    """Through the public API with host buffers: every step copies its inputs
+    from pinned host memory, replays the 28 calls and reads the outputs back."""
+    host_in = torch.empty(step.inbuf.shape, dtype=step.inbuf.dtype, pin_memory=True)
+    host_in.copy_(step.inbuf)
+    host_out = torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
+    s = torch.cuda.current_stream()
+
+    def one():
+        step.inbuf.copy_(host_in, non_blocking=True)
+        step.graph.replay()
+        host_out.copy_(step.out, non_blocking=True)
+
+    for _ in range(W):
+        one()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(K):
+        one()
+    e1.record(s)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier(world)
+    h2d = host_in.numel() * host_in.element_size()
+    d2h = host_out.numel() * host_out.element_size()
+    return max(e0.elapsed_time(e1) / 1e3, wall), h2d, d2h
+
+
+# ---------------------------------------------------------------- oracle baseline
+
+def oracle_sample_inputs(step, streams, layers):
+    """Host copies of the sampled streams of the chosen layers, with each
+    full layer's pages gathered into a compact pool."""
+    out = []
+    u16 = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    sel = torch.tensor(streams, device=step.inbuf.device)
+    for l in layers:
+        L = step.layers[l]
+        d = {"kind": L["kind"], "rope": L["rope"], "q": u16(L["q"][sel]), "k_new": u16(L["k_new"][sel]),
+             "v_new": u16(L["v_new"][sel]), "gate": u16(L["gate"][sel]),
+             "pos": L["pos"][sel].cpu().numpy()}
+        if L["kind"] == "sliding":
+            d.update(k=u16(L["k"][sel]), v=u16(L["v"][sel]), head=L["head"][sel].cpu().numpy(),
+                     count=L["count"][sel].cpu().numpy())
+        else:
+            bt = L["block_table"][sel]
+            pages = bt.reshape(-1)
+            d.update(k=u16(L["k"][pages]), v=u16(L["v"][pages]),
+                     block_table=np.arange(pages.numel(), dtype=np.int32).reshape(bt.shape),
+                     seq_len=L["seq_len"][sel].cpu().numpy())
+        out.append(d)
+    return out
+
+
+def oracle_pass(o, sample):
+    for d in sample:
+        r, th = d["rope"].rotary_dim, d["rope"].theta
+        if d["kind"] == "sliding":
+            o.decode_ring(d["k"], d["v"], d["head"], d["count"], d["q"], d["k_new"], d["v_new"],
+                          d["pos"], r, th, gate=d["gate"])
+        else:
+            o.decode_paged(d["k"], d["v"], d["block_table"], d["seq_len"], d["q"], d["k_new"],
+                           d["v_new"], d["pos"], r, th, gate=d["gate"])
+
+
+def sample_bytes_tokens(sample):
+    by = tok = 0
+    for d in sample:
+        n = int(d["count"][0]) if d["kind"] == "sliding" else int(d["seq_len"][0])
+        Bs = d["q"].shape[0]
+        kv, io = layer_bytes(d["kind"], Bs, n)
+        by += kv + io
+        tok += Bs * (n + 1)
+    return by, tok
+
+
+def cpu_baseline(step, budget_s=15.0):
+    import oracle as oracle_pkg
+    o = oracle_pkg.get()
+    layers = list(range(28))
+    sample = oracle_sample_inputs(step, [0, 1], layers)
+    t0 = time.perf_counter()
+    oracle_pass(o, sample)
+    t1 = time.perf_counter() - t0
+    reps = max(1, int(budget_s / max(t1, 1e-3)) - 1)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle_pass(o, sample)
+    t = (time.perf_counter() - t0) / reps
+    by, tok = sample_bytes_tokens(sample)
+    return {"value": by / t / 1e9, "unit": "GB/s", "tokens_per_s": tok / t,
+            "cores": min(o.hardware_threads(), 2 * HKV), "kind": "oracle",
+            "sample": f"2 of {step.B} streams x all 28 layers (the oracle threads over "
+                      f"(stream, KV head): 4 work items), {reps} passes of {t:.3f} s"}
+
+
+# ---------------------------------------------------------------- arms
+
+def run_reference(args, world, rank):
+    """The fp64 CPU oracle as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return
+    import oracle as oracle_pkg
+    import synth
+    o = oracle_pkg.get()
+    # one stream of the workload's first four layers (3 sliding + 1 full) per step
+    cases = [synth.hybrid_layer(SEED, l, 1, CONTEXT) for l in range(4)]
+    sample = []
+    for c in cases:
+        x, ca = c.inputs, c.cache
+        d = {"kind": "sliding" if c.kind == "ring" else "full", "rope": c.rope, "q": x.q,
+             "k_new": x.k_new, "v_new": x.v_new, "gate": x.gate, "pos": x.pos}
+        if c.kind == "ring":
+            d.update(k=ca.k, v=ca.v, head=ca.head, count=ca.count)
+        else:
+            d.update(k=ca.k, v=ca.v, block_table=ca.block_table, seq_len=ca.seq_len)
+        sample.append(d)
+    for _ in range(args.warmup):
+        oracle_pass(o, sample)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_pass(o, sample)
+    t = time.perf_counter() - t0
+    by, tok = sample_bytes_tokens(sample)
+    value = by * args.steps / t / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "hybrid 28-layer decode step (8 q / 2 KV heads, head_dim 256), "
+                                   "sampled: 1 stream x layers 0-3 (3 sliding + 1 full) at context 4096",
+                       "context": CONTEXT},
+            "attended_kv_tokens_per_s": tok * args.steps / t,
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": min(o.hardware_threads(), HKV), "kind": "oracle",
+                             "sample": "1 stream x layers 0-3 per step"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_dattn(args, world, rank, local):
+    assert torch.cuda.is_available(), "bench.py needs a GPU"
+    step = Step(B_STREAMS, CONTEXT, SEED + rank)
+    step.capture()
+    bytes_step, tokens_step, per_kind = step_accounting(B_STREAMS, CONTEXT)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    t = time_graph(step, args.steps, args.warmup, world)
+    clk = clocks.stop()
+    t = max_over_ranks(t, world)
+    value = bytes_step * world * args.steps / t / 1e9
+    tok_s = tokens_step * world * args.steps / t
+
+    # per-call times of the dominant call (the full layers' split-K pass)
+    per = time_layers(step, args.steps)
+    full = [per[l] for l, L in enumerate(step.layers) if L["kind"] == "full"]
+    slid = [per[l] for l, L in enumerate(step.layers) if L["kind"] == "sliding"]
+    t_full = statistics.mean(full)
+    kv_full = per_kind["full"][0]
+    peak, peak_src = peak_hbm()
+    achieved = kv_full / t_full / 1e9
+
+    e2e_t, h2d, d2h = time_e2e(step, max(10, args.steps // 5), max(3, args.warmup), world)
+    e2e_t = max_over_ranks(e2e_t, world)
+    e2e_steps = max(10, args.steps // 5)
+
+    base = cpu_baseline(step) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    if rank != 0:
+        return
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        try:
+            traffic = json.load(open(tpath)).get("decode_split_full_layer_bytes")
+        except Exception:
+            traffic = None
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (bf16 N(0,1) K/V and inputs drawn on the device, seeded)",
+        "config": {"workload": "hybrid 28-layer decode step: [sliding x3, full] x7, 8 q / 2 KV heads, "
+                               "head_dim 256, 64 streams, context 4096",
+                   "streams": B_STREAMS, "context": CONTEXT, "sliding_ring_slots": 511,
+                   "full_page_size": 16, "gate": True, "write_back": True,
+                   "l2": "inputs larger than L2: 5.2 GB of K/V per step vs 129 MB L2",
+                   "timing": "one CUDA graph of 28 calls per step, CUDA events",
+                   "parallelism": f"replicas x{world}"},
+        "attended_kv_tokens_per_s": tok_s,
+        "frac_of_peak": value / peak,
+        "peak_gbs": peak, "peak_source": peak_src,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "decode_split (full layers, 64 streams x 4096 tokens)",
+                     "note": "achieved = cached K/V bytes of one full-layer call / that call's "
+                             "CUDA-event time (RoPE + split + combine), of " + peak_src},
+        "per_call_us": {"full": t_full * 1e6, "sliding": statistics.mean(slid) * 1e6},
+        "cpu_baseline": base,
+        "e2e": {"value": bytes_step * world * e2e_steps / e2e_t / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": step.launches_per_step() * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="dattn", choices=["dattn", "reference"])
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_dattn(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

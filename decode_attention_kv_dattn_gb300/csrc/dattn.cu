@@ -1,0 +1,362 @@
+// Host side of the dattn C ABI: argument checks, the split-K plan, the
+// workspace, and the launch sequence of each call.
+//
+// A decode call is three launches on the caller's stream, each a programmatic
+// dependent of the previous one:
+//   1. rope      - rotates q (fp32, pre-scaled) and k (bf16 entry) at pos;
+//   2. split     - S CTAs per (stream, KV head) stream the cached K/V through
+//                  shared memory and leave partial softmax states (m, l, o);
+//   3. combine   - merges the partials, joins the new token in score space,
+//                  applies the gate, stores fp32 and writes the new entry back.
+// The new entry is written in (3), after (2) has completed: when a ring is
+// full the new entry takes the oldest token's slot, which (2) still reads.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "dattn.h"
+#include "kernels.h"
+
+using namespace dattn;
+
+struct dattn_handle {
+  int device = 0;
+  int Hq = 0, Hkv = 0, D = 0, G = 0, GP = 0;
+  int max_streams = 0, max_context = 0, max_verify_rows = 0;
+  std::vector<dattn_layer_config> layers;
+  std::vector<double*> inv_freq;  // device, per layer ([r/2] or null)
+  int num_sms = 0;
+  int split_resident = 0;  // resident split CTAs on the whole GPU
+  size_t part_units = 0;   // capacity of the partials, in (stream, head, split) units
+  float* qhat = nullptr;
+  uint16_t* khat = nullptr;
+  float* part = nullptr;
+  int* err = nullptr;
+};
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int padded_group(int G) { return G <= 2 ? 2 : (G <= 4 ? 4 : (G <= 8 ? 8 : 0)); }
+
+// Make `dev` current for the duration of a call and restore the caller's.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) {
+      ok = false;
+      return;
+    }
+    if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return DATTN_OK;
+  if (e == cudaErrorNotSupported) {
+    cudaGetLastError();
+    return DATTN_EUNSUPPORTED;
+  }
+  return DATTN_ECUDA;
+}
+
+// Split-K plan: enough CTAs for about two waves of resident split CTAs, and
+// splits of at least 64 keys (a multiple of 64).
+void plan_splits(const dattn_handle* h, int units, int n_max, int* chunk, int* splits) {
+  if (n_max <= 0) {
+    *chunk = 64;
+    *splits = 1;
+    return;
+  }
+  const int target = 2 * h->split_resident;
+  int S = (target + units - 1) / units;
+  const int by_len = (n_max + 63) / 64;
+  if (S > by_len) S = by_len;
+  if (S < 1) S = 1;
+  int c = (n_max + S - 1) / S;
+  c = (c + 63) / 64 * 64;
+  *chunk = c;
+  *splits = (n_max + c - 1) / c;
+}
+
+CacheView make_view(const dattn_handle* h, const dattn_layer_config& L, const dattn_cache* c) {
+  CacheView v{};
+  v.k = static_cast<uint16_t*>(c->k);
+  v.v = static_cast<uint16_t*>(c->v);
+  v.paged = L.cache_kind == DATTN_CACHE_PAGED;
+  v.n_rows = c->n_rows;
+  v.R = L.ring_slots;
+  v.P = L.page_size;
+  v.ring_head = c->ring_head;
+  v.ring_count = c->ring_count;
+  v.stream_rows = c->stream_rows;
+  v.block_table = c->block_table;
+  v.bt_stride = c->bt_stride;
+  v.seq_len = c->seq_len;
+  (void)h;
+  return v;
+}
+
+int check_cache(const dattn_layer_config& L, const dattn_cache* c) {
+  if (!c || !c->k || !c->v || c->n_rows <= 0) return DATTN_EINVAL;
+  if (!aligned16(c->k) || !aligned16(c->v)) return DATTN_EINVAL;
+  if (L.cache_kind == DATTN_CACHE_RING) {
+    if (!c->ring_head || !c->ring_count) return DATTN_EINVAL;
+  } else {
+    if (!c->block_table || !c->seq_len || c->bt_stride <= 0) return DATTN_EINVAL;
+  }
+  return DATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dattn_error_string(int code) {
+  switch (code) {
+    case DATTN_OK: return "ok";
+    case DATTN_EINVAL: return "invalid argument";
+    case DATTN_EXCEEDS: return "request exceeds what the handle was created for";
+    case DATTN_ECUDA: return "CUDA runtime error";
+    case DATTN_EINDEX: return "device metadata out of range (page id, ring slot, tree parent)";
+    case DATTN_ETIMEOUT: return "a bounded device wait timed out";
+    case DATTN_EUNSUPPORTED: return "shape not supported by this build";
+    case DATTN_ELENGTH: return "a stream is longer than the call's bound";
+    default: return "unknown dattn status";
+  }
+}
+
+int dattn_create(const dattn_config* cfg, int device, dattn_t** out) {
+  if (!cfg || !out) return DATTN_EINVAL;
+  *out = nullptr;
+  const int Hq = cfg->num_q_heads, Hkv = cfg->num_kv_heads, D = cfg->head_dim;
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return DATTN_EINVAL;
+  if (D != 128 && D != 256) return DATTN_EUNSUPPORTED;
+  const int G = Hq / Hkv;
+  if (padded_group(G) == 0) return DATTN_EUNSUPPORTED;
+  if (cfg->max_streams <= 0 || cfg->max_context < 0 || cfg->num_layers <= 0 || !cfg->layers)
+    return DATTN_EINVAL;
+  if (cfg->max_verify_rows < 0 || cfg->max_verify_rows > 16) return DATTN_EINVAL;
+  for (int l = 0; l < cfg->num_layers; ++l) {
+    const dattn_layer_config& L = cfg->layers[l];
+    if (L.cache_kind == DATTN_CACHE_RING) {
+      if (L.ring_slots <= 0) return DATTN_EINVAL;
+    } else if (L.cache_kind == DATTN_CACHE_PAGED) {
+      if (L.page_size <= 0) return DATTN_EINVAL;
+    } else {
+      return DATTN_EINVAL;
+    }
+    if (L.rotary_dim < 0 || L.rotary_dim > D || L.rotary_dim % 2) return DATTN_EINVAL;
+    if (L.rotary_dim > 0 && !(L.rope_theta > 0.0)) return DATTN_EINVAL;
+  }
+  DeviceGuard guard(device);
+  if (!guard.ok) return DATTN_ECUDA;
+
+  dattn_handle* h = new (std::nothrow) dattn_handle();
+  if (!h) return DATTN_ECUDA;
+  h->device = device;
+  h->Hq = Hq;
+  h->Hkv = Hkv;
+  h->D = D;
+  h->G = G;
+  h->GP = padded_group(G);
+  h->max_streams = cfg->max_streams;
+  h->max_context = cfg->max_context;
+  h->max_verify_rows = cfg->max_verify_rows;
+  h->layers.assign(cfg->layers, cfg->layers + cfg->num_layers);
+
+  auto fail = [&](int code) {
+    dattn_destroy(h);
+    return code;
+  };
+  if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+    return fail(DATTN_ECUDA);
+  h->split_resident = h->num_sms * decode_split_ctas_per_sm(D, G);
+  if (h->split_resident <= 0) return fail(DATTN_EUNSUPPORTED);
+
+  // RoPE inverse frequencies theta^(-2i/r), fp64, one table per layer
+  for (const dattn_layer_config& L : h->layers) {
+    double* dev = nullptr;
+    if (L.rotary_dim > 0) {
+      std::vector<double> f(L.rotary_dim / 2);
+      for (int i = 0; i < L.rotary_dim / 2; ++i)
+        f[i] = std::pow(L.rope_theta, -static_cast<double>(2 * i) / static_cast<double>(L.rotary_dim));
+      if (cudaMalloc(&dev, f.size() * sizeof(double)) != cudaSuccess) return fail(DATTN_ECUDA);
+      h->inv_freq.push_back(dev);
+      if (cudaMemcpy(dev, f.data(), f.size() * sizeof(double), cudaMemcpyHostToDevice) != cudaSuccess)
+        return fail(DATTN_ECUDA);
+    } else {
+      h->inv_freq.push_back(nullptr);
+    }
+  }
+
+  // Workspace. Rows of rotated q/k: one per stream (decode) or per verify row.
+  const size_t rows = static_cast<size_t>(h->max_streams) *
+                      (h->max_verify_rows > 1 ? h->max_verify_rows : 1);
+  if (cudaMalloc(&h->qhat, rows * Hq * D * sizeof(float)) != cudaSuccess) return fail(DATTN_ECUDA);
+  if (cudaMalloc(&h->khat, rows * Hkv * D * sizeof(uint16_t)) != cudaSuccess) return fail(DATTN_ECUDA);
+  // Partials: the plan keeps units * splits <= 2 * resident + units.
+  h->part_units = 2 * static_cast<size_t>(h->split_resident) + static_cast<size_t>(h->max_streams) * Hkv;
+  const size_t part_floats = h->part_units * h->GP * (D + 2);
+  if (cudaMalloc(&h->part, part_floats * sizeof(float)) != cudaSuccess) return fail(DATTN_ECUDA);
+  if (cudaMalloc(&h->err, sizeof(int)) != cudaSuccess) return fail(DATTN_ECUDA);
+  if (cudaMemset(h->err, 0, sizeof(int)) != cudaSuccess) return fail(DATTN_ECUDA);
+  *out = h;
+  return DATTN_OK;
+}
+
+void dattn_destroy(dattn_t* h) {
+  if (!h) return;
+  DeviceGuard guard(h->device);
+  for (double* p : h->inv_freq) cudaFree(p);
+  cudaFree(h->qhat);
+  cudaFree(h->khat);
+  cudaFree(h->part);
+  cudaFree(h->err);
+  delete h;
+}
+
+int dattn_get_error(dattn_t* h, dattn_stream_t stream) {
+  if (!h) return DATTN_EINVAL;
+  DeviceGuard guard(h->device);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int bits = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DATTN_ECUDA;
+  if (cudaMemcpyAsync(&bits, h->err, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return DATTN_ECUDA;
+  if (cudaMemsetAsync(h->err, 0, sizeof(int), s) != cudaSuccess) return DATTN_ECUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DATTN_ECUDA;
+  if (bits & ERR_TIMEOUT) return DATTN_ETIMEOUT;
+  if (bits & ERR_INDEX) return DATTN_EINDEX;
+  if (bits & ERR_LENGTH) return DATTN_ELENGTH;
+  return DATTN_OK;
+}
+
+int dattn_append_kv(dattn_t* h, int layer, const dattn_cache* cache, int num_streams,
+                    int max_tokens, const int32_t* start_index, const int32_t* start_pos,
+                    const int32_t* count, const void* k, const void* v, int rotate,
+                    dattn_stream_t stream) {
+  if (!h || layer < 0 || layer >= static_cast<int>(h->layers.size())) return DATTN_EINVAL;
+  const dattn_layer_config& L = h->layers[layer];
+  int rc = check_cache(L, cache);
+  if (rc != DATTN_OK) return rc;
+  if (num_streams <= 0 || max_tokens < 0 || !start_index || !count || !k || !v) return DATTN_EINVAL;
+  if (rotate && L.rotary_dim > 0 && !start_pos) return DATTN_EINVAL;
+  if (!aligned16(k) || !aligned16(v)) return DATTN_EINVAL;
+  if (max_tokens == 0) return DATTN_OK;
+  if (max_tokens > 65535) return DATTN_EXCEEDS;
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return DATTN_ECUDA;
+  AppendArgs a{};
+  a.c = make_view(h, L, cache);
+  a.B = num_streams;
+  a.Tmax = max_tokens;
+  a.Hkv = h->Hkv;
+  a.D = h->D;
+  a.r = L.rotary_dim;
+  a.start_index = start_index;
+  a.start_pos = start_pos;
+  a.count = count;
+  a.k = static_cast<const uint16_t*>(k);
+  a.v = static_cast<const uint16_t*>(v);
+  a.rotate = rotate;
+  a.inv_freq = h->inv_freq[layer];
+  a.err = h->err;
+  return cuda_status(launch_append(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int dattn_decode(dattn_t* h, int layer, const dattn_cache* cache, const dattn_decode_args* args,
+                 dattn_stream_t stream) {
+  if (!h || !args || layer < 0 || layer >= static_cast<int>(h->layers.size())) return DATTN_EINVAL;
+  const dattn_layer_config& L = h->layers[layer];
+  int rc = check_cache(L, cache);
+  if (rc != DATTN_OK) return rc;
+  const int B = args->num_streams;
+  if (B <= 0) return DATTN_EINVAL;
+  if (B > h->max_streams) return DATTN_EXCEEDS;
+  if (!args->q || !args->k_new || !args->v_new || !args->pos || !args->out) return DATTN_EINVAL;
+  if (!aligned16(args->q) || !aligned16(args->k_new) || !aligned16(args->v_new) ||
+      !aligned16(args->out))
+    return DATTN_EINVAL;
+  int n_max;
+  if (L.cache_kind == DATTN_CACHE_RING) {
+    n_max = L.ring_slots;
+  } else {
+    n_max = args->max_seq_len > 0 ? args->max_seq_len : h->max_context;
+    if (n_max > h->max_context) return DATTN_EXCEEDS;
+    if (n_max > cache->bt_stride * L.page_size) return DATTN_EINVAL;
+  }
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return DATTN_ECUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  RopeArgs ra{};
+  ra.rows = B;
+  ra.Hq = h->Hq;
+  ra.Hkv = h->Hkv;
+  ra.D = h->D;
+  ra.r = L.rotary_dim;
+  ra.q = static_cast<const uint16_t*>(args->q);
+  ra.k = static_cast<const uint16_t*>(args->k_new);
+  ra.pos = args->pos;
+  ra.T = 1;
+  ra.inv_freq = h->inv_freq[layer];
+  ra.q_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(h->D)));
+  ra.qhat = h->qhat;
+  ra.khat = h->khat;
+  ra.err = h->err;
+  rc = cuda_status(launch_rope(ra, s));
+  if (rc != DATTN_OK) return rc;
+
+  int chunk, splits;
+  plan_splits(h, B * h->Hkv, n_max, &chunk, &splits);
+  if (static_cast<size_t>(B) * h->Hkv * splits > h->part_units) return DATTN_EXCEEDS;
+  SplitArgs sa{};
+  sa.c = make_view(h, L, cache);
+  sa.B = B;
+  sa.Hkv = h->Hkv;
+  sa.chunk = chunk;
+  sa.splits = splits;
+  sa.max_len = n_max;
+  sa.qhat = h->qhat;
+  sa.part = h->part;
+  sa.err = h->err;
+  rc = cuda_status(launch_decode_split(sa, h->D, h->G, s));
+  if (rc != DATTN_OK) return rc;
+
+  CombineArgs ca{};
+  ca.c = sa.c;
+  ca.B = B;
+  ca.Hkv = h->Hkv;
+  ca.chunk = chunk;
+  ca.splits = splits;
+  ca.max_len = n_max;
+  ca.qhat = h->qhat;
+  ca.khat = h->khat;
+  ca.v_new = static_cast<const uint16_t*>(args->v_new);
+  ca.gate = static_cast<const uint16_t*>(args->gate);
+  ca.part = h->part;
+  ca.out = args->out;
+  ca.write_back = args->write_back;
+  ca.err = h->err;
+  return cuda_status(launch_decode_combine(ca, h->D, h->G, s));
+}
+
+int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, const dattn_verify_args* args,
+                 dattn_stream_t stream) {
+  (void)cache;
+  (void)args;
+  (void)stream;
+  if (!h || layer < 0 || layer >= static_cast<int>(h->layers.size())) return DATTN_EINVAL;
+  return DATTN_EUNSUPPORTED;
+}
+
+}  // extern "C"

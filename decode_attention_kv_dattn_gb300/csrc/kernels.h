@@ -1,0 +1,120 @@
+// Internal interface between the host planner (dattn.cu) and the kernel
+// translation units. Not part of the public C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <utility>
+
+namespace dattn {
+
+// Sticky device error bits (see dattn_get_error).
+enum : int { ERR_INDEX = 1, ERR_TIMEOUT = 2, ERR_LENGTH = 4 };
+
+// One layer's cache as the kernels see it.
+struct CacheView {
+  uint16_t* k;                 // ring [n_rows, Hkv, R, D] / paged [pages, Hkv, P, D]
+  uint16_t* v;
+  int paged;                   // 0 = ring, 1 = paged
+  int n_rows;                  // ring rows or pages in the pool
+  int R;                       // ring slots
+  int P;                       // page size
+  const int32_t* ring_head;    // [B]
+  const int32_t* ring_count;   // [B]
+  const int32_t* stream_rows;  // [B] or null
+  const int32_t* block_table;  // [B, bt_stride]
+  int bt_stride;
+  const int32_t* seq_len;      // [B]
+};
+
+// RoPE prologue: rotates q (fp32 out, pre-scaled) and k (bf16 entry out) of
+// `rows` token rows. Decode: row = stream, position pos[row]. Verify: row =
+// s * T + i, position prefix_len[s] + depth(i) from the parent array.
+struct RopeArgs {
+  int rows;
+  int Hq, Hkv, D, r;
+  const uint16_t* q;           // [rows, Hq, D]
+  const uint16_t* k;           // [rows, Hkv, D]
+  const int32_t* pos;          // [rows] (decode) or null
+  const int32_t* prefix_len;   // [rows / T] (verify) or null
+  const int32_t* parent;       // [rows] (verify) or null
+  int T;
+  const double* inv_freq;      // [r / 2]
+  float q_scale;               // log2(e) / sqrt(D)
+  float* qhat;                 // [rows, Hq, D]
+  uint16_t* khat;              // [rows, Hkv, D]
+  int* err;
+};
+
+// Split-K pass over the cached keys of a decode call.
+struct SplitArgs {
+  CacheView c;
+  int B, Hkv;
+  int chunk;                   // keys per split
+  int splits;                  // S: grid.x
+  int max_len;                 // host bound on cached length (paged)
+  const float* qhat;           // [B, Hq, D]
+  float* part;                 // [B, Hkv, S, G*(D+2)]: o[G][D], m[G], l[G]
+  int* err;
+};
+
+// LSE combine + new-token join + gate + store + write-back.
+struct CombineArgs {
+  CacheView c;
+  int B, Hkv;
+  int chunk, splits, max_len;
+  const float* qhat;           // [B, Hq, D]
+  const uint16_t* khat;        // [B, Hkv, D]
+  const uint16_t* v_new;       // [B, Hkv, D]
+  const uint16_t* gate;        // [B, Hq] or null
+  const float* part;
+  float* out;                  // [B, Hq, D]
+  int write_back;
+  int* err;
+};
+
+struct AppendArgs {
+  CacheView c;
+  int B, Tmax, Hkv, D, r;
+  const int32_t* start_index;
+  const int32_t* start_pos;
+  const int32_t* count;
+  const uint16_t* k;           // [B, Tmax, Hkv, D]
+  const uint16_t* v;
+  int rotate;
+  const double* inv_freq;
+  int* err;
+};
+
+// Each returns cudaErrorNotSupported for a shape with no compiled kernel.
+cudaError_t launch_rope(const RopeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_split(const SplitArgs& a, int D, int G, cudaStream_t s);
+cudaError_t launch_decode_combine(const CombineArgs& a, int D, int G, cudaStream_t s);
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
+
+// Resident CTAs per SM of the split kernel for (D, G) (0 if unsupported).
+int decode_split_ctas_per_sm(int D, int G);
+// Keys per tile of the split kernel for (D, G).
+int decode_split_tile_keys(int D, int G);
+
+// Launch with programmatic stream serialization: the kernel may begin while
+// its predecessor in the stream finishes; every kernel here waits on the
+// predecessor (griddepcontrol.wait) before it touches the predecessor's output.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+}  // namespace dattn

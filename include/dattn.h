@@ -1,0 +1,196 @@
+/*
+ * dattn: decode attention over per-stream KV caches on one GB300 (sm_103a).
+ *
+ * One query token per stream attends to that stream's cached keys and values
+ * plus its own new key and value. Two cache layouts are supported:
+ *
+ *   ring  - a sliding-window layer keeps window-1 slots per (stream, KV head);
+ *           the valid slots are the `count` slots before `head` (cyclically),
+ *           in any order. ("vllm-omni commits", score-space join commit: the
+ *           ring needs no reordering because softmax is order-free and each
+ *           cached key already carries its rotary phase; only unwritten slots
+ *           are masked; a 512-token window holds 511 cached entries.)
+ *   paged - a full-attention layer keeps its tokens in fixed-size pages named
+ *           by a per-stream page table ("pega-omni PR #4": talker KV in paged
+ *           leases; padding rows of a call name a pad page).
+ *
+ * The new token is joined in score space: the cache and the new key are
+ * scored separately and the two score vectors meet in one softmax, so nothing
+ * cache-sized is copied; the call returns the new K/V entry by writing it into
+ * its slot (same commit). RoPE is applied per layer type to the new q and k
+ * ("vllm-omni commits", Spark model commit: sliding layers rotate all 256 dims
+ * with theta 1e4, full layers the first quarter with theta 5e6), and an
+ * optional head-wise sigmoid gate scales each head's output (same commit).
+ * Grouped-query attention maps query head h to KV head h / (Hq / Hkv)
+ * ("vllm-omni commits", talker export commit: GQA by reshaping the query).
+ * Tree verify scores up to 16 rows per stream, each under its own tree mask
+ * ("TensorFold PR #608": verify windows of up to 16 streams x 16 rows).
+ *
+ * Conventions for every entry point:
+ *   - All tensor and index pointers are DEVICE pointers on the handle's GPU,
+ *     owned by the caller, dense row-major in the layouts stated below. bf16
+ *     data is passed as raw 16-bit patterns. Pointers must be 16-byte aligned.
+ *   - Calls are asynchronous on `stream` (NULL = legacy default stream) and
+ *     may be captured in a CUDA graph. Calls that share one handle use its
+ *     workspace and must be ordered (one stream, or one handle per stream).
+ *   - The return value is a dattn status. Host-side argument checks return
+ *     DATTN_EINVAL / DATTN_EXCEEDS / DATTN_EUNSUPPORTED before anything is
+ *     launched. Bad device-side metadata (a page id outside the pool, a ring
+ *     head outside [0, R), a length above the planned bound, a bad tree parent)
+ *     never faults: the kernel skips or clamps the access and sets a sticky
+ *     device error word that dattn_get_error() reports.
+ *   - The library never mutates caller metadata: after a call the caller
+ *     advances ring head/count or seq_len itself.
+ */
+#ifndef DATTN_H
+#define DATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifndef DATTN_API
+#define DATTN_API __attribute__((visibility("default")))
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+enum {
+  DATTN_OK = 0,
+  DATTN_EINVAL = 1,        /* invalid argument (null pointer, bad shape)         */
+  DATTN_EXCEEDS = 2,       /* beyond what dattn_create planned for (cf. the
+                              pages' ExceedsPool: rejected, not queued forever)  */
+  DATTN_ECUDA = 3,         /* a CUDA runtime call failed                          */
+  DATTN_EINDEX = 4,        /* device metadata out of range (from dattn_get_error) */
+  DATTN_ETIMEOUT = 5,      /* a bounded device wait gave up (dattn_get_error)     */
+  DATTN_EUNSUPPORTED = 6,  /* a shape this build has no kernel for                */
+  DATTN_ELENGTH = 7        /* a stream longer than the call's bound (get_error)   */
+};
+
+enum { DATTN_CACHE_RING = 0, DATTN_CACHE_PAGED = 1 };
+
+/* cudaStream_t without including the CUDA headers. */
+typedef struct CUstream_st* dattn_stream_t;
+
+/* Per-layer description, copied by dattn_create. */
+typedef struct {
+  int cache_kind;     /* DATTN_CACHE_RING or DATTN_CACHE_PAGED                   */
+  int ring_slots;     /* ring: R = window - 1 slots per (row, KV head)           */
+  int page_size;      /* paged: P tokens per page (P * head_dim * 2 % 16 == 0)   */
+  int rotary_dim;     /* r: RoPE turns dims [0, r) in pairs (i, i + r/2); even,
+                         <= head_dim; 0 = no rotation                            */
+  double rope_theta;  /* base of the inverse frequencies theta^(-2i/r)           */
+} dattn_layer_config;
+
+typedef struct {
+  int num_q_heads;       /* Hq                                                   */
+  int num_kv_heads;      /* Hkv; Hq % Hkv == 0                                   */
+  int head_dim;          /* D: 128 or 256                                         */
+  int max_streams;       /* largest B of a decode call / S of a verify call       */
+  int max_context;       /* largest cached length of a paged stream; calls with a
+                            longer bound return DATTN_EXCEEDS                      */
+  int max_verify_rows;   /* largest T of a verify call (<= 16); 0 = no verify     */
+  int num_layers;
+  const dattn_layer_config* layers; /* [num_layers], host memory                  */
+} dattn_config;
+
+typedef struct dattn_handle dattn_t;
+
+/* One layer's cache as the caller holds it. Ring fields are read for ring
+ * layers, paged fields for paged layers.
+ *   ring : k, v = [n_rows, Hkv, R, D] bf16. Call row b uses ring row
+ *          stream_rows[b] (identity when NULL); its valid slots are the
+ *          ring_count[b] slots before ring_head[b]; the new entry is written
+ *          at slot ring_head[b].
+ *   paged: k, v = [n_rows (pages), Hkv, P, D] bf16. Token t of call row b is
+ *          offset t % P of page block_table[b * bt_stride + t / P]; the row
+ *          holds seq_len[b] cached tokens; the new entry is written at token
+ *          index seq_len[b]. */
+typedef struct {
+  void* k;
+  void* v;
+  int n_rows;
+  const int32_t* ring_head;    /* [B] */
+  const int32_t* ring_count;   /* [B] */
+  const int32_t* stream_rows;  /* [B] or NULL */
+  const int32_t* block_table;  /* [B, bt_stride] */
+  int bt_stride;
+  const int32_t* seq_len;      /* [B] */
+} dattn_cache;
+
+/* One decode step: B streams, one new token each. */
+typedef struct {
+  int num_streams;       /* B, 1 <= B <= max_streams                             */
+  const void* q;         /* [B, Hq, D] bf16                                       */
+  const void* k_new;     /* [B, Hkv, D] bf16, before RoPE                         */
+  const void* v_new;     /* [B, Hkv, D] bf16                                      */
+  const void* gate;      /* [B, Hq] bf16 gate logits, or NULL for no gate        */
+  const int32_t* pos;    /* [B] RoPE position of the new token                    */
+  float* out;            /* [B, Hq, D] fp32: sigmoid(gate) * attention output     */
+  int max_seq_len;       /* paged: host-side bound on seq_len[b] for this call
+                            (0 = max_context); sizes the key split. Ignored for
+                            ring layers (the bound is R).                          */
+  int write_back;        /* nonzero: store the rotated bf16 k_new and v_new into
+                            the new token's slot after every read of the cache   */
+} dattn_decode_args;
+
+/* One verify round: S streams x T rows. Row i of stream s sits at position
+ * seq_len[s] + depth(i); it attends to the stream's whole paged prefix
+ * (seq_len[s] tokens), to its ancestors in the tree and to itself, each
+ * window key rotated at its own position. */
+typedef struct {
+  int num_streams;       /* S                                                     */
+  int rows;              /* T, 1 <= T <= max_verify_rows                          */
+  const void* q;         /* [S, T, Hq, D] bf16                                    */
+  const void* k;         /* [S, T, Hkv, D] bf16, before RoPE                      */
+  const void* v;         /* [S, T, Hkv, D] bf16                                   */
+  const int32_t* parent; /* [S, T]: parent[i] < i, or -1 for a root              */
+  const void* gate;      /* [S, T, Hq] bf16 or NULL                               */
+  float* out;            /* [S, T, Hq, D] fp32                                    */
+  int max_prefix_len;    /* host bound on seq_len[s] (0 = max_context)            */
+  int write_back;        /* nonzero: window entry i goes to token index
+                            seq_len[s] + i (node order)                           */
+} dattn_verify_args;
+
+/* Create a handle on `device`: validates the config, uploads per-layer RoPE
+ * frequency tables (theta^(-2i/r) in fp64, computed on the host) and
+ * allocates the workspace for the split-K partials. The handle owns that
+ * memory until dattn_destroy. */
+DATTN_API int dattn_create(const dattn_config* cfg, int device, dattn_t** out);
+
+/* Bulk write (prefill or cache set-up): token t < count[b] of call row b goes
+ * to cache index start_index[b] + t (ring: slot (start_index[b] + t) mod R of
+ * row stream_rows[b]; paged: offset idx % P of page block_table[b][idx / P]).
+ * k, v = [B, max_tokens, Hkv, D] bf16. When rotate != 0 the key is turned at
+ * position start_pos[b] + t and rounded to bf16 (nearest-even, from fp64) -
+ * the same entry decode writes back. start_index, start_pos, count: [B]. */
+DATTN_API int dattn_append_kv(dattn_t* h, int layer, const dattn_cache* cache, int num_streams,
+                    int max_tokens, const int32_t* start_index, const int32_t* start_pos,
+                    const int32_t* count, const void* k, const void* v, int rotate,
+                    dattn_stream_t stream);
+
+/* Decode attention for one layer (see dattn_decode_args). */
+DATTN_API int dattn_decode(dattn_t* h, int layer, const dattn_cache* cache, const dattn_decode_args* args,
+                 dattn_stream_t stream);
+
+/* Tree verify for one paged layer (see dattn_verify_args). */
+DATTN_API int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, const dattn_verify_args* args,
+                 dattn_stream_t stream);
+
+/* Synchronize `stream`, then return and clear the sticky device error word:
+ * DATTN_OK, DATTN_EINDEX, DATTN_ELENGTH or DATTN_ETIMEOUT (the first found in
+ * that order of severity: ETIMEOUT, EINDEX, ELENGTH). */
+DATTN_API int dattn_get_error(dattn_t* h, dattn_stream_t stream);
+
+/* Static description of a status code. */
+DATTN_API const char* dattn_error_string(int code);
+
+/* Free the workspace and the handle. Safe on NULL. */
+DATTN_API void dattn_destroy(dattn_t* h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DATTN_H */

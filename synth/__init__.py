@@ -293,3 +293,42 @@ def long_context(seed: int = 4, B: int = 1, context: int = 1 << 20) -> DecodeCas
     cache = paged_cache(gen, B, Hkv, D, 64, [context] * B)
     inputs = decode_inputs(gen, B, Hq, Hkv, D, [context] * B, gate=False)
     return DecodeCase(Hq, Hkv, D, FULL_ROPE, cache, inputs)
+
+
+# ------------------------------------------------------------------ device-side generation
+
+def hybrid_step_device(seed: int, B: int, context: int, device="cuda"):
+    """The 28-layer hybrid step drawn directly on the GPU (same recipe as
+    hybrid_layer: bf16 N(0,1) K/V, full sliding rings of 511 slots with a
+    uniform random head per stream, full layers in 16-token pages from a
+    randomly permuted pool, gate logits N(0,1), positions = context). Returns a
+    list of per-layer dicts of device tensors."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    Hq, Hkv, D = 8, 2, 256
+
+    def randn(*shape):
+        return torch.randn(*shape, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+    layers = []
+    for kind in HYBRID_PATTERN:
+        L = {"kind": kind, "q": randn(B, Hq, D), "k_new": randn(B, Hkv, D),
+             "v_new": randn(B, Hkv, D), "gate": randn(B, Hq),
+             "pos": torch.full((B,), context, dtype=torch.int32, device=device)}
+        if kind == "sliding":
+            R = 511
+            n = min(context, R)
+            L.update(rope=SLIDING_ROPE, R=R, k=randn(B, Hkv, R, D), v=randn(B, Hkv, R, D),
+                     head=torch.randint(0, R, (B,), generator=g, device=device, dtype=torch.int32),
+                     count=torch.full((B,), n, dtype=torch.int32, device=device),
+                     rows=torch.arange(B, dtype=torch.int32, device=device))
+        else:
+            P = 16
+            per = (context + 1 + P - 1) // P
+            total = B * per + 3
+            perm = torch.randperm(total, generator=g, device=device).to(torch.int32)
+            L.update(rope=FULL_ROPE, P=P, k=randn(total, Hkv, P, D), v=randn(total, Hkv, P, D),
+                     block_table=perm[: B * per].reshape(B, per).contiguous(),
+                     seq_len=torch.full((B,), context, dtype=torch.int32, device=device))
+        layers.append(L)
+    return layers
