@@ -412,9 +412,10 @@ def run_reference(args, world, rank):
 
 def run_dattn(args, world, rank, local):
     assert torch.cuda.is_available(), "bench.py needs a GPU"
-    step = Step(B_STREAMS, CONTEXT, SEED + rank)
+    B, ctx = args.streams, args.context
+    step = Step(B, ctx, SEED + rank)
     step.capture()
-    bytes_step, tokens_step, per_kind = step_accounting(B_STREAMS, CONTEXT)
+    bytes_step, tokens_step, per_kind = step_accounting(B, ctx)
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -433,9 +434,13 @@ def run_dattn(args, world, rank, local):
     peak, peak_src = peak_hbm()
     achieved = kv_full / t_full / 1e9
 
-    e2e_t, h2d, d2h = time_e2e(step, max(10, args.steps // 5), max(3, args.warmup), world)
-    e2e_t = max_over_ranks(e2e_t, world)
-    e2e_steps = max(10, args.steps // 5)
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(10, args.steps // 5)
+        e2e_t, h2d, d2h = time_e2e(step, e2e_steps, max(3, args.warmup), world)
+        e2e_t = max_over_ranks(e2e_t, world)
+        e2e = {"value": bytes_step * world * e2e_steps / e2e_t / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     base = cpu_baseline(step) if (rank == 0 and world == 1 and not args.no_cpu) else None
     if rank != 0:
@@ -453,10 +458,10 @@ def run_dattn(args, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (bf16 N(0,1) K/V and inputs drawn on the device, seeded)",
         "config": {"workload": "hybrid 28-layer decode step: [sliding x3, full] x7, 8 q / 2 KV heads, "
-                               "head_dim 256, 64 streams, context 4096",
-                   "streams": B_STREAMS, "context": CONTEXT, "sliding_ring_slots": 511,
+                               f"head_dim 256, {B} streams, context {ctx}",
+                   "streams": B, "context": ctx, "sliding_ring_slots": 511,
                    "full_page_size": 16, "gate": True, "write_back": True,
-                   "l2": "inputs larger than L2: 5.2 GB of K/V per step vs 129 MB L2",
+                   "l2": f"inputs larger than L2: {bytes_step / 1e9:.2f} GB per step vs 129 MB L2",
                    "timing": "one CUDA graph of 28 calls per step, CUDA events",
                    "parallelism": f"replicas x{world}"},
         "attended_kv_tokens_per_s": tok_s,
@@ -464,13 +469,12 @@ def run_dattn(args, world, rank, local):
         "peak_gbs": peak, "peak_source": peak_src,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "decode_split (full layers, 64 streams x 4096 tokens)",
+                     "kernel": f"decode_split (full layers, {B} streams x {ctx} tokens)",
                      "note": "achieved = cached K/V bytes of one full-layer call / that call's "
                              "CUDA-event time (RoPE + split + combine), of " + peak_src},
         "per_call_us": {"full": t_full * 1e6, "sliding": statistics.mean(slid) * 1e6},
         "cpu_baseline": base,
-        "e2e": {"value": bytes_step * world * e2e_steps / e2e_t / 1e9, "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": e2e,
         "gpu_launches": step.launches_per_step() * args.steps,
         "clocks": clk,
     }
@@ -484,6 +488,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="dattn", choices=["dattn", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
+    ap.add_argument("--streams", type=int, default=B_STREAMS,
+                    help="streams per GPU (smaller values make short profiling runs)")
+    ap.add_argument("--context", type=int, default=CONTEXT)
     args = ap.parse_args()
     world, rank, local = dist_setup()
     try:
