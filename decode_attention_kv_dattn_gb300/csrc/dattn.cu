@@ -29,8 +29,9 @@ struct dattn_handle {
   std::vector<double*> inv_freq;  // device, per layer ([r/2] or null)
   int num_sms = 0;
   int split_resident = 0;  // resident split CTAs on the whole GPU
-  size_t part_units = 0;   // capacity of the partials, in (stream, head, split) units
+  size_t part_units = 0;   // capacity of the partials, in segment slots
   float* qhat = nullptr;
+  int* tiles = nullptr;    // tile prefix over units, from the split pass
   uint16_t* khat = nullptr;
   float* part = nullptr;
   int* err = nullptr;
@@ -68,23 +69,14 @@ int cuda_status(cudaError_t e) {
   return DATTN_ECUDA;
 }
 
-// Split-K plan: enough CTAs for about two waves of resident split CTAs, and
-// splits of at least 64 keys (a multiple of 64).
-void plan_splits(const dattn_handle* h, int units, int n_max, int* chunk, int* splits) {
-  if (n_max <= 0) {
-    *chunk = 64;
-    *splits = 1;
-    return;
-  }
-  const int target = 2 * h->split_resident;
-  int S = (target + units - 1) / units;
-  const int by_len = (n_max + 63) / 64;
-  if (S > by_len) S = by_len;
-  if (S < 1) S = 1;
-  int c = (n_max + S - 1) / S;
-  c = (c + 63) / 64 * 64;
-  *chunk = c;
-  *splits = (n_max + c - 1) / c;
+// Split grid: every resident split CTA, but at least 4 stage tiles (one per
+// warp) per CTA for the largest amount of work this call may have.
+int plan_split_ctas(const dattn_handle* h, int units, int n_max, int tile_keys) {
+  const int64_t tiles = static_cast<int64_t>(units) * ((n_max + tile_keys - 1) / tile_keys);
+  int64_t ctas = (tiles + 3) / 4;
+  if (ctas > h->split_resident) ctas = h->split_resident;
+  if (ctas < 1) ctas = 1;
+  return static_cast<int>(ctas);
 }
 
 CacheView make_view(const dattn_handle* h, const dattn_layer_config& L, const dattn_cache* c) {
@@ -203,8 +195,11 @@ int dattn_create(const dattn_config* cfg, int device, dattn_t** out) {
                       (h->max_verify_rows > 1 ? h->max_verify_rows : 1);
   if (cudaMalloc(&h->qhat, rows * Hq * D * sizeof(float)) != cudaSuccess) return fail(DATTN_ECUDA);
   if (cudaMalloc(&h->khat, rows * Hkv * D * sizeof(uint16_t)) != cudaSuccess) return fail(DATTN_ECUDA);
-  // Partials: the plan keeps units * splits <= 2 * resident + units.
-  h->part_units = 2 * static_cast<size_t>(h->split_resident) + static_cast<size_t>(h->max_streams) * Hkv;
+  // Partials: one slot per split CTA plus one per unit.
+  if (static_cast<int64_t>(h->max_streams) * Hkv > decode_max_units()) return fail(DATTN_EUNSUPPORTED);
+  h->part_units = static_cast<size_t>(h->split_resident) + static_cast<size_t>(h->max_streams) * Hkv;
+  if (cudaMalloc(&h->tiles, (static_cast<size_t>(h->max_streams) * Hkv + 1) * sizeof(int)) != cudaSuccess)
+    return fail(DATTN_ECUDA);
   const size_t part_floats = h->part_units * h->GP * (D + 2);
   if (cudaMalloc(&h->part, part_floats * sizeof(float)) != cudaSuccess) return fail(DATTN_ECUDA);
   if (cudaMalloc(&h->err, sizeof(int)) != cudaSuccess) return fail(DATTN_ECUDA);
@@ -220,6 +215,7 @@ void dattn_destroy(dattn_t* h) {
   cudaFree(h->qhat);
   cudaFree(h->khat);
   cudaFree(h->part);
+  cudaFree(h->tiles);
   cudaFree(h->err);
   delete h;
 }
@@ -292,7 +288,6 @@ int dattn_decode(dattn_t* h, int layer, const dattn_cache* cache, const dattn_de
   } else {
     n_max = args->max_seq_len > 0 ? args->max_seq_len : h->max_context;
     if (n_max > h->max_context) return DATTN_EXCEEDS;
-    if (n_max > cache->bt_stride * L.page_size) return DATTN_EINVAL;
   }
   DeviceGuard guard(h->device);
   if (!guard.ok) return DATTN_ECUDA;
@@ -316,18 +311,17 @@ int dattn_decode(dattn_t* h, int layer, const dattn_cache* cache, const dattn_de
   rc = cuda_status(launch_rope(ra, s));
   if (rc != DATTN_OK) return rc;
 
-  int chunk, splits;
-  plan_splits(h, B * h->Hkv, n_max, &chunk, &splits);
-  if (static_cast<size_t>(B) * h->Hkv * splits > h->part_units) return DATTN_EXCEEDS;
+  const int ctas = plan_split_ctas(h, B * h->Hkv, n_max, decode_split_tile_keys(h->D, h->G));
+  if (static_cast<size_t>(ctas) + static_cast<size_t>(B) * h->Hkv > h->part_units) return DATTN_EXCEEDS;
   SplitArgs sa{};
   sa.c = make_view(h, L, cache);
   sa.B = B;
   sa.Hkv = h->Hkv;
-  sa.chunk = chunk;
-  sa.splits = splits;
+  sa.ctas = ctas;
   sa.max_len = n_max;
   sa.qhat = h->qhat;
   sa.part = h->part;
+  sa.tiles = h->tiles;
   sa.err = h->err;
   rc = cuda_status(launch_decode_split(sa, h->D, h->G, s));
   if (rc != DATTN_OK) return rc;
@@ -336,8 +330,8 @@ int dattn_decode(dattn_t* h, int layer, const dattn_cache* cache, const dattn_de
   ca.c = sa.c;
   ca.B = B;
   ca.Hkv = h->Hkv;
-  ca.chunk = chunk;
-  ca.splits = splits;
+  ca.split_ctas = ctas;
+  ca.tiles = h->tiles;
   ca.max_len = n_max;
   ca.qhat = h->qhat;
   ca.khat = h->khat;

@@ -1,5 +1,5 @@
-// Decode attention: split-K pass over the cached keys and the LSE combine that
-// joins the new token in score space.
+// Decode attention: the split-K pass over the cached keys and the LSE combine
+// that joins the new token in score space.
 //
 // Method ("vllm-omni commits", score-space join commit): the cached keys (n of
 // them) and the new key are scored separately and their score vectors meet in
@@ -9,18 +9,29 @@
 // masked by never being read. Grouped-query attention shares each KV head's
 // loads among its G query heads ("vllm-omni commits", talker export commit).
 // Splitting the keys over many CTAs and merging their partial softmax states
-// follows "TensorFold PR #608" (the split "shared" kernel plus a merge, and the
-// lesson that a merge must not be a chain of dependent loads).
+// follows "TensorFold PR #608" (the split "shared" kernel plus a merge, the
+// lessons that the grid must fill the GPU and that a merge must not be a chain
+// of dependent loads).
 //
-// GB300 design. The KV stream is HBM-bound at G flops per byte, so the scores
-// and the value sum run on the FP32 pipes, not on tensor cores. Each warp owns
-// a private pipeline of KT-key tiles: one lane issues bulk TMA copies
-// (cp.async.bulk, global -> shared, completion counted on an mbarrier) for K
-// and V of the tile kStages ahead. A lane holds 8 dims (one 16-byte load) of a
-// key; the G per-head dot products of J keys (J * G = lanes per key) are
-// reduced across lanes by a transposing butterfly, which leaves exactly one
-// (key, head) score per lane, so the online softmax costs one exp2 per lane per
-// tile. Probabilities go through shared memory to all lanes for the value sum.
+// GB300 design.
+//  * Work split (stream-K). A "unit" is one (stream, KV head); its cached keys
+//    form ceil(n / SK) stage tiles. All units' tiles are laid end to end and the
+//    grid - exactly the CTAs that fit on the GPU at once - cuts that sequence
+//    into equal contiguous ranges, so every CTA moves the same number of bytes
+//    whatever the mix of lengths. Each piece of a unit inside one CTA (a
+//    "segment") leaves one partial softmax state (m, l, o); the combine merges
+//    a unit's segments.
+//  * Loads. Each warp owns a private ring of NS stage buffers. One lane issues
+//    bulk TMA copies (cp.async.bulk global -> shared, completion counted in
+//    transaction bytes on the stage's mbarrier) for the K and V rows of the
+//    warp's tile NS ahead; the ring keeps streaming across segment boundaries.
+//    Pages and ring wrap-around turn into one copy per contiguous run of rows.
+//  * Math. At G flops per byte the KV stream is HBM-bound, so scores and the
+//    value sum run on the FP32 pipes. A lane holds 8 dims (one 16-byte shared
+//    load) of a key; the per-head dot products of J keys are reduced across the
+//    lanes of a key by a transposing butterfly that leaves exactly one
+//    (key, head) score per lane, so the online softmax costs one exp2 per lane
+//    per sub-tile. Probabilities reach all lanes through shared memory.
 #include "common.cuh"
 
 namespace dattn {
@@ -29,25 +40,31 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kMaxUnits = 1024;   // (stream, KV head) units per call
 
 template <int D, int GP>
 struct Geo {
-  static constexpr int LPK = D / 8;         // lanes per key row (16 bytes each)
-  static constexpr int KPS = 32 / LPK;      // keys per warp-wide load
-  static constexpr int J = LPK / GP;        // loads per tile (J * GP scores per lane)
-  static constexpr int KT = J * KPS;        // keys per tile
-  static constexpr int ROW = D * 2;         // bytes per key row
-  static constexpr int TILE = KT * ROW;     // bytes of one K (or V) tile
+  static constexpr int LPK = D / 8;          // lanes per key row (16 bytes each)
+  static constexpr int KPS = 32 / LPK;       // keys per warp-wide load
+  static constexpr int J = LPK / GP;         // loads per sub-tile (J * GP scores per lane)
+  static constexpr int KT = J * KPS;         // keys per sub-tile
+  static constexpr int ROW = D * 2;          // bytes per key row
+  static constexpr int SK_MIN = 8192 / (2 * ROW);
+  static constexpr int SUB = KT >= SK_MIN ? 1 : SK_MIN / KT;
+  static constexpr int SK = KT * SUB;        // keys per stage tile (>= 8 KB of K + V)
+  static constexpr int TILE = SK * ROW;      // bytes of the K (or V) half of a stage
   static constexpr int STAGE = 2 * TILE;
-  // stages per warp: about 24 KB of K/V in flight per warp, at least 2
-  static constexpr int NS = (24576 / STAGE) < 2 ? 2 : ((24576 / STAGE) > 8 ? 8 : 24576 / STAGE);
-  static constexpr int STAGE_BYTES = kWarps * NS * STAGE;
-  static constexpr int MERGE_BYTES = kWarps * GP * (D + 2) * 4;
-  static constexpr int BAR_OFF = STAGE_BYTES > MERGE_BYTES ? STAGE_BYTES : MERGE_BYTES;
-  static constexpr int PSM_OFF = BAR_OFF + kWarps * NS * 8;
-  static constexpr int SMEM = PSM_OFF + kWarps * (32 + GP) * 4;
+  static constexpr int NS = STAGE >= 16384 ? 2 : 3;
+  static constexpr int BAR_OFF = kWarps * NS * STAGE;
+  static constexpr int ML_OFF = BAR_OFF + kWarps * NS * 8;     // float [kWarps][2*GP]
+  static constexpr int SLOT_OFF = ML_OFF + kWarps * 2 * GP * 4; // int [kWarps]
+  static constexpr int PSM_OFF = SLOT_OFF + kWarps * 4;         // float [kWarps][32+GP]
+  static constexpr int TAB_OFF = (PSM_OFF + kWarps * (32 + GP) * 4 + 15) / 16 * 16;
+  static constexpr int SMEM_MAX = TAB_OFF + (2 * kMaxUnits + 1) * 4;
   static_assert(D == 128 || D == 256, "head_dim");
   static_assert(LPK % GP == 0, "GP must divide the lanes per key");
+  static_assert(GP * D * 4 <= STAGE, "a stage buffer holds one warp's partial output");
 };
 
 __device__ __forceinline__ void unpack8(const uint4& w, float (&f)[8]) {
@@ -57,10 +74,10 @@ __device__ __forceinline__ void unpack8(const uint4& w, float (&f)[8]) {
   f[6] = bf16_lo(w.w); f[7] = bf16_hi(w.w);
 }
 
-// Sum N = W partial values across W lanes (W a power of two, groups aligned)
-// so that lane l ends with the full sum of value (l % W). Each level halves the
-// values a lane keeps: the lane whose bit `w` is set keeps the upper half and
-// sends the lower half to its partner, and the other way round.
+// Sum W partial values across W lanes (W a power of two, groups aligned) so
+// that lane l ends with the full sum of value (l % W). At each level the lane
+// whose bit `w` is set keeps the upper half of its values and sends the lower
+// half to its partner, which does the opposite.
 template <int W>
 __device__ __forceinline__ float transpose_reduce(float (&v)[W], int lane) {
 #pragma unroll
@@ -77,19 +94,11 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[W], int lane) {
   return v[0];
 }
 
-// The cached keys of call row b for KV head j: count n, ring start slot and
-// base pointers. Bad metadata reads nothing and is reported once.
-struct StreamKeys {
-  int n;
-  int start;
-  const uint16_t* kb;
-  const uint16_t* vb;
-};
-
-template <bool PAGED, int D>
-__device__ __forceinline__ StreamKeys stream_keys(const CacheView& c, int b, int j, int Hkv,
-                                                  int max_len, bool report, int* err) {
-  StreamKeys s{0, 0, c.k, c.v};
+// Cached keys of call row b (the same for all its KV heads). Bad metadata is
+// reported (once per row) and yields no keys.
+template <bool PAGED>
+__device__ __forceinline__ int unit_length(const CacheView& c, int b, int max_len, bool report,
+                                           int* err) {
   if constexpr (PAGED) {
     int n = c.seq_len[b];
     const int cap = min(max_len, c.bt_stride * c.P);
@@ -97,48 +106,87 @@ __device__ __forceinline__ StreamKeys stream_keys(const CacheView& c, int b, int
       if (report) raise_error(err, ERR_LENGTH);
       n = n < 0 ? 0 : cap;
     }
-    s.n = n;
+    return n;
   } else {
     const int row = c.stream_rows ? c.stream_rows[b] : b;
     const int head = c.ring_head[b], cnt = c.ring_count[b];
     if (row < 0 || row >= c.n_rows || head < 0 || head >= c.R || cnt < 0 || cnt > c.R) {
       if (report) raise_error(err, ERR_INDEX);
-      return s;
+      return 0;
     }
-    s.n = cnt;
-    s.start = head - cnt < 0 ? head - cnt + c.R : head - cnt;
-    const int64_t off = (static_cast<int64_t>(row) * Hkv + j) * c.R * D;
-    s.kb = c.k + off;
-    s.vb = c.v + off;
+    return cnt;
   }
-  return s;
+}
+
+// Inclusive prefix sum of x[0, n) in shared memory by the whole block.
+__device__ void block_scan_inclusive(int* x, int n) {
+  __shared__ int warp_sum[kWarps];
+  const int t = threadIdx.x;
+  const int per = (n + kThreads - 1) / kThreads;
+  const int lo = min(n, t * per), hi = min(n, lo + per);
+  int sum = 0;
+  for (int i = lo; i < hi; ++i) {
+    sum += x[i];
+    x[i] = sum;
+  }
+  int incl = sum;
+#pragma unroll
+  for (int w = 1; w < 32; w <<= 1) {
+    const int y = __shfl_up_sync(kFull, incl, w);
+    if ((t & 31) >= w) incl += y;
+  }
+  if ((t & 31) == 31) warp_sum[t >> 5] = incl;
+  __syncthreads();
+  int before = incl - sum;
+  for (int w = 0; w < (t >> 5); ++w) before += warp_sum[w];
+  for (int i = lo; i < hi; ++i) x[i] += before;
+  __syncthreads();
+}
+
+// Last unit u with P[u] <= g (P[0] = 0 <= g); its range then contains g.
+__device__ __forceinline__ int unit_of(const int* P, int U, int g) {
+  int lo = 0, hi = U - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (P[mid] <= g) lo = mid; else hi = mid - 1;
+  }
+  return lo;
 }
 
 template <int D, int GP, bool PAGED>
-__global__ void __launch_bounds__(kWarps * 32, 2) decode_split_kernel(const SplitArgs a, int G) {
+__global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const SplitArgs a, int G) {
   using Gm = Geo<D, GP>;
-  constexpr int LPK = Gm::LPK, KPS = Gm::KPS, J = Gm::J, KT = Gm::KT, NS = Gm::NS;
-  extern __shared__ __align__(1024) uint8_t smem[];
-  const int split = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
+  constexpr int LPK = Gm::LPK, KPS = Gm::KPS, J = Gm::J, KT = Gm::KT, SK = Gm::SK;
+  constexpr int SUB = Gm::SUB, NS = Gm::NS;
+  extern __shared__ __align__(16) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const CacheView& c = a.c;
-  const int Hkv = a.Hkv;
+  const int Hkv = a.Hkv, U = a.B * Hkv;
+  const int NC = gridDim.x, cta = blockIdx.x;
+  int* P = reinterpret_cast<int*>(smem + Gm::TAB_OFF);  // [U + 1] tile prefix over units
+  int* N = P + U + 1;                                    // [U] cached keys per unit
 
-  // Caller metadata and the cache itself are not written by the preceding
-  // kernel (the RoPE prologue), so the first tiles are requested before the
-  // dependency wait and overlap it.
-  const StreamKeys sk = stream_keys<PAGED, D>(c, b, j, Hkv, a.max_len,
-                                              split == 0 && threadIdx.x == 0, a.err);
-  const int k0 = split * a.chunk;
-  const int k1 = min(sk.n, k0 + a.chunk);
-  const int ntiles = k1 > k0 ? (k1 - k0 + KT - 1) / KT : 0;
-  const int my_tiles = ntiles > warp ? (ntiles - warp + kWarps - 1) / kWarps : 0;
+  // ---- unit table from caller metadata (not written by the preceding kernel)
+  for (int u = threadIdx.x; u < U; u += kThreads) {
+    const int b = u / Hkv;
+    const int n = unit_length<PAGED>(c, b, a.max_len, cta == 0 && u - b * Hkv == 0, a.err);
+    N[u] = n;
+    P[u + 1] = (n + SK - 1) / SK;
+  }
+  if (threadIdx.x == 0) P[0] = 0;
+  __syncthreads();
+  block_scan_inclusive(P + 1, U);
+  const int T = P[U];
+  const int g0 = static_cast<int>(static_cast<int64_t>(cta) * T / NC);
+  const int g1 = static_cast<int>(static_cast<int64_t>(cta + 1) * T / NC);
+  if (cta == 0)  // the combine locates each unit's segments from this table
+    for (int u = threadIdx.x; u <= U; u += kThreads) a.tiles[u] = P[u];
 
+  // ---- this warp's tiles: g = g0 + warp + kWarps * it
+  const int span = g1 - g0;
+  const int my_n = span > warp ? (span - warp + kWarps - 1) / kWarps : 0;
   uint8_t* wsm = smem + warp * NS * Gm::STAGE;
   const uint32_t bar0 = smem_addr(smem + Gm::BAR_OFF) + warp * NS * 8;
-  float* psm = reinterpret_cast<float*>(smem + Gm::PSM_OFF) + warp * (32 + GP);
-  const int32_t* bt = PAGED ? c.block_table + static_cast<int64_t>(b) * c.bt_stride : nullptr;
-
   if (lane == 0) {
     for (int s = 0; s < NS; ++s) mbar_init(bar0 + 8 * s, 1);
     fence_mbar_init();
@@ -146,17 +194,23 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_split_kernel(const Spli
   __syncwarp();
 
   const uint64_t policy = l2_evict_first_policy();
+  int u_iss = my_n > 0 ? unit_of(P, U, g0 + warp) : 0;
+  // Request tile `it` of this warp into stage it % NS (one lane).
   auto issue = [&](int it) {
-    const int stg = it % NS;
-    const int t0 = k0 + (warp + it * kWarps) * KT;
-    const int cnt = min(KT, k1 - t0);
-    const uint32_t bar = bar0 + 8 * stg;
-    const uint32_t kd = smem_addr(wsm + stg * Gm::STAGE);
+    const int g = g0 + warp + kWarps * it;
+    while (P[u_iss + 1] <= g) ++u_iss;
+    const int u = u_iss;
+    const int b = u / Hkv, j = u - b * Hkv;
+    const int k0 = (g - P[u]) * SK;
+    const int cnt = min(SK, N[u] - k0);
+    const uint32_t bar = bar0 + 8 * (it % NS);
+    const uint32_t kd = smem_addr(wsm + (it % NS) * Gm::STAGE);
     const uint32_t vd = kd + Gm::TILE;
     mbar_arrive_expect_tx(bar, 2u * cnt * Gm::ROW);
     if constexpr (PAGED) {
-      int t = t0, done = 0;
-      while (t < t0 + cnt) {
+      const int32_t* bt = c.block_table + static_cast<int64_t>(b) * c.bt_stride;
+      int t = k0, done = 0;
+      while (t < k0 + cnt) {
         const int pi = t / c.P;
         const int off = t - pi * c.P;
         int pg = bt[pi];
@@ -164,201 +218,247 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_split_kernel(const Spli
           raise_error(a.err, ERR_INDEX);
           pg = 0;
         }
-        const int run = min(c.P - off, t0 + cnt - t);
+        const int run = min(c.P - off, k0 + cnt - t);
         const int64_t src = ((static_cast<int64_t>(pg) * Hkv + j) * c.P + off) * D;
-        bulk_copy_g2s(kd + done * Gm::ROW, sk.kb + src, run * Gm::ROW, bar, policy);
-        bulk_copy_g2s(vd + done * Gm::ROW, sk.vb + src, run * Gm::ROW, bar, policy);
+        bulk_copy_g2s(kd + done * Gm::ROW, c.k + src, run * Gm::ROW, bar, policy);
+        bulk_copy_g2s(vd + done * Gm::ROW, c.v + src, run * Gm::ROW, bar, policy);
         t += run;
         done += run;
       }
     } else {
-      int phys = sk.start + t0;
+      const int row = c.stream_rows ? c.stream_rows[b] : b;
+      const int n = N[u];
+      const int head = c.ring_head[b];
+      const int start = head - n < 0 ? head - n + c.R : head - n;
+      const int64_t base = (static_cast<int64_t>(row) * Hkv + j) * c.R * D;
+      int phys = start + k0;
       if (phys >= c.R) phys -= c.R;
       const int run1 = min(cnt, c.R - phys);
-      bulk_copy_g2s(kd, sk.kb + static_cast<int64_t>(phys) * D, run1 * Gm::ROW, bar, policy);
-      bulk_copy_g2s(vd, sk.vb + static_cast<int64_t>(phys) * D, run1 * Gm::ROW, bar, policy);
+      bulk_copy_g2s(kd, c.k + base + static_cast<int64_t>(phys) * D, run1 * Gm::ROW, bar, policy);
+      bulk_copy_g2s(vd, c.v + base + static_cast<int64_t>(phys) * D, run1 * Gm::ROW, bar, policy);
       if (run1 < cnt) {
-        bulk_copy_g2s(kd + run1 * Gm::ROW, sk.kb, (cnt - run1) * Gm::ROW, bar, policy);
-        bulk_copy_g2s(vd + run1 * Gm::ROW, sk.vb, (cnt - run1) * Gm::ROW, bar, policy);
+        bulk_copy_g2s(kd + run1 * Gm::ROW, c.k + base, (cnt - run1) * Gm::ROW, bar, policy);
+        bulk_copy_g2s(vd + run1 * Gm::ROW, c.v + base, (cnt - run1) * Gm::ROW, bar, policy);
       }
     }
   };
   if (lane == 0) {
-    const int pre = my_tiles < NS ? my_tiles : NS;
+    const int pre = my_n < NS ? my_n : NS;
     for (int it = 0; it < pre; ++it) issue(it);
   }
 
   pdl_wait();  // the rotated, pre-scaled q of this call
   pdl_trigger();
 
-  // This lane's 8 dims of each query head of the group (padding heads are 0).
+  float* ML = reinterpret_cast<float*>(smem + Gm::ML_OFF);
+  int* SLOT = reinterpret_cast<int*>(smem + Gm::SLOT_OFF);
+  float* psm = reinterpret_cast<float*>(smem + Gm::PSM_OFF) + warp * (32 + GP);
   const int dl = (lane % LPK) * 8;
-  float q[GP][8];
-#pragma unroll
-  for (int g = 0; g < GP; ++g) {
-    if (g < G) {
-      const float* src = a.qhat + (static_cast<int64_t>(b) * Hkv * G + j * G + g) * D + dl;
-      const float4 x0 = *reinterpret_cast<const float4*>(src);
-      const float4 x1 = *reinterpret_cast<const float4*>(src + 4);
-      q[g][0] = x0.x; q[g][1] = x0.y; q[g][2] = x0.z; q[g][3] = x0.w;
-      q[g][4] = x1.x; q[g][5] = x1.y; q[g][6] = x1.z; q[g][7] = x1.w;
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) q[g][e] = 0.f;
-    }
-  }
+  const int half = lane / LPK;                         // key of a warp-wide load held by this lane
+  const int key_s = ((lane % LPK) / GP) * KPS + half;  // sub-tile key of this lane's score
 
-  float o[GP][8];
-#pragma unroll
-  for (int g = 0; g < GP; ++g)
-#pragma unroll
-    for (int e = 0; e < 8; ++e) o[g][e] = 0.f;
-  float m_run = -INFINITY, l_run = 0.f;
-  const int half = lane / LPK;                        // key of a warp-wide load held by this lane
-  const int key_s = ((lane % LPK) / GP) * KPS + half; // tile key of this lane's score
+  bool failed = false;
+  int it = 0;
+  int deferred = -1;
+  bool first_seg = true;
+  for (int u = span > 0 ? unit_of(P, U, g0) : U; u < U && P[u] < g1; ++u) {
+    if (P[u + 1] == P[u]) continue;  // a unit with no cached keys
+    const int ge = min(g1, P[u + 1]);
+    const int b = u / Hkv, j = u - b * Hkv;
 
-  for (int it = 0; it < my_tiles; ++it) {
-    const int stg = it % NS;
-    if (!mbar_wait_bounded(bar0 + 8 * stg, (it / NS) & 1)) {
-      if (lane == 0) raise_error(a.err, ERR_TIMEOUT);
-      break;
-    }
-    const int t0 = k0 + (warp + it * kWarps) * KT;
-    const int nvalid = min(KT, k1 - t0);
-    const uint4* Ks = reinterpret_cast<const uint4*>(wsm + stg * Gm::STAGE);
-    const uint4* Vs = Ks + Gm::TILE / 16;
-
-    // scores: J loads of 8 dims, GP heads each, then the transposing reduction
-    float sp[J * GP];
-#pragma unroll
-    for (int jj = 0; jj < J; ++jj) {
-      float kf[8];
-      unpack8(Ks[jj * 32 + lane], kf);
-#pragma unroll
-      for (int g = 0; g < GP; ++g) {
-        float acc = q[g][0] * kf[0];
-#pragma unroll
-        for (int e = 1; e < 8; ++e) acc = fmaf(q[g][e], kf[e], acc);
-        sp[jj * GP + g] = acc;
-      }
-    }
-    float s = transpose_reduce<LPK>(sp, lane);
-    if (key_s >= nvalid) s = -INFINITY;
-
-    // online softmax (base 2): every lane holds one (key, head) score
-    float tmax = s;
-#pragma unroll
-    for (int w = GP; w < 32; w <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, w));
-    const float m_new = fmaxf(m_run, tmax);
-    const float corr = exp2_fast(m_run - m_new);
-    const float p = exp2_fast(s - m_new);
-    l_run = fmaf(l_run, corr, p);
-    m_run = m_new;
-    psm[lane] = p;
-    if (lane < GP) psm[32 + lane] = corr;
-    __syncwarp();
-
+    float q[GP][8];
 #pragma unroll
     for (int g = 0; g < GP; ++g) {
-      const float cr = psm[32 + g];
+      if (g < G) {
+        const float* src = a.qhat + (static_cast<int64_t>(b) * Hkv * G + j * G + g) * D + dl;
+        const float4 x0 = *reinterpret_cast<const float4*>(src);
+        const float4 x1 = *reinterpret_cast<const float4*>(src + 4);
+        q[g][0] = x0.x; q[g][1] = x0.y; q[g][2] = x0.z; q[g][3] = x0.w;
+        q[g][4] = x1.x; q[g][5] = x1.y; q[g][6] = x1.z; q[g][7] = x1.w;
+      } else {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[g][e] *= cr;
-    }
-    if (nvalid == KT) {
-#pragma unroll
-      for (int jj = 0; jj < J; ++jj) {
-        float vf[8];
-        unpack8(Vs[jj * 32 + lane], vf);
-        const float* pp = psm + half * LPK + jj * GP;
-#pragma unroll
-        for (int g = 0; g < GP; ++g) {
-          const float pg = pp[g];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) o[g][e] = fmaf(pg, vf[e], o[g][e]);
-        }
-      }
-    } else {
-#pragma unroll
-      for (int jj = 0; jj < J; ++jj) {
-        if (jj * KPS + half < nvalid) {
-          float vf[8];
-          unpack8(Vs[jj * 32 + lane], vf);
-          const float* pp = psm + half * LPK + jj * GP;
-#pragma unroll
-          for (int g = 0; g < GP; ++g) {
-            const float pg = pp[g];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o[g][e] = fmaf(pg, vf[e], o[g][e]);
-          }
-        }
+        for (int e = 0; e < 8; ++e) q[g][e] = 0.f;
       }
     }
-    __syncwarp();
-    if (lane == 0 && it + NS < my_tiles) {
-      fence_proxy_async_smem();
-      issue(it + NS);
-    }
-  }
-
-  // warp totals: l over the lanes holding the same head; o over the keys of a
-  // warp-wide load held by different lane groups
-#pragma unroll
-  for (int w = GP; w < 32; w <<= 1) l_run += __shfl_xor_sync(kFull, l_run, w);
-#pragma unroll
-  for (int w = LPK; w < 32; w <<= 1)
+    float o[GP][8];
 #pragma unroll
     for (int g = 0; g < GP; ++g)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[g][e] += __shfl_xor_sync(kFull, o[g][e], w);
+      for (int e = 0; e < 8; ++e) o[g][e] = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;
+    int last_stage = -1;
 
-  // merge the warps in shared memory (the stage buffers are idle now)
-  __syncthreads();
-  float* mo = reinterpret_cast<float*>(smem);        // [kWarps][GP][D]
-  float* mm = mo + kWarps * GP * D;                  // [kWarps][GP]
-  float* ml = mm + kWarps * GP;                      // [kWarps][GP]
-  if (lane < LPK) {
+    for (;;) {
+      const int g = g0 + warp + kWarps * it;
+      if (it >= my_n || g >= ge) break;
+      const int stg = it % NS;
+      if (!failed) {
+        // the whole warp agrees on the outcome, so the shuffles below stay converged
+        const bool ok = __all_sync(kFull, mbar_wait_bounded(bar0 + 8 * stg, (it / NS) & 1));
+        if (!ok) {
+          failed = true;
+          if (lane == 0) raise_error(a.err, ERR_TIMEOUT);
+        }
+      }
+      if (!failed) {
+        const int nstage = min(SK, N[u] - (g - P[u]) * SK);
+#pragma unroll 1
+        for (int sb = 0; sb < SUB; ++sb) {
+          const int nvalid = nstage - sb * KT;
+          if (nvalid <= 0) break;
+          const uint4* Ks = reinterpret_cast<const uint4*>(wsm + stg * Gm::STAGE) + sb * (KT * D / 8);
+          const uint4* Vs = Ks + Gm::TILE / 16;
+
+          // scores: J loads of 8 dims for GP heads, then the transposing reduction
+          float sp[J * GP];
 #pragma unroll
-    for (int g = 0; g < GP; ++g) {
-      float* dst = mo + (warp * GP + g) * D + dl;
-      *reinterpret_cast<float4*>(dst) = make_float4(o[g][0], o[g][1], o[g][2], o[g][3]);
-      *reinterpret_cast<float4*>(dst + 4) = make_float4(o[g][4], o[g][5], o[g][6], o[g][7]);
+          for (int jj = 0; jj < J; ++jj) {
+            float kf[8];
+            unpack8(Ks[jj * 32 + lane], kf);
+#pragma unroll
+            for (int h = 0; h < GP; ++h) {
+              float acc = q[h][0] * kf[0];
+#pragma unroll
+              for (int e = 1; e < 8; ++e) acc = fmaf(q[h][e], kf[e], acc);
+              sp[jj * GP + h] = acc;
+            }
+          }
+          float s = transpose_reduce<LPK>(sp, lane);
+          if (key_s >= nvalid) s = -INFINITY;
+
+          // online softmax (base 2): every lane holds one (key, head) score
+          float tmax = s;
+#pragma unroll
+          for (int w = GP; w < 32; w <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, w));
+          const float m_new = fmaxf(m_run, tmax);
+          const float corr = exp2_fast(m_run - m_new);
+          const float p = exp2_fast(s - m_new);
+          l_run = fmaf(l_run, corr, p);
+          m_run = m_new;
+          psm[lane] = p;
+          if (lane < GP) psm[32 + lane] = corr;
+          __syncwarp();
+#pragma unroll
+          for (int h = 0; h < GP; ++h) {
+            const float cr = psm[32 + h];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[h][e] *= cr;
+          }
+          if (nvalid >= KT) {
+#pragma unroll
+            for (int jj = 0; jj < J; ++jj) {
+              float vf[8];
+              unpack8(Vs[jj * 32 + lane], vf);
+              const float* pp = psm + half * LPK + jj * GP;
+#pragma unroll
+              for (int h = 0; h < GP; ++h) {
+                const float ph = pp[h];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[h][e] = fmaf(ph, vf[e], o[h][e]);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < J; ++jj) {
+              if (jj * KPS + half < nvalid) {
+                float vf[8];
+                unpack8(Vs[jj * 32 + lane], vf);
+                const float* pp = psm + half * LPK + jj * GP;
+#pragma unroll
+                for (int h = 0; h < GP; ++h) {
+                  const float ph = pp[h];
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) o[h][e] = fmaf(ph, vf[e], o[h][e]);
+                }
+              }
+            }
+          }
+          __syncwarp();
+        }
+      }
+      last_stage = stg;
+      // Refill this stage with the warp's tile NS ahead. The warp's last tile
+      // of a segment keeps its stage as the merge buffer until the merge is done.
+      if (it + NS < my_n) {
+        if (g + kWarps >= ge) {
+          deferred = it + NS;
+        } else if (lane == 0 && !failed) {
+          fence_proxy_async_smem();
+          issue(it + NS);
+        }
+      }
+      ++it;
     }
-  }
-  if (lane < GP) {
-    mm[warp * GP + lane] = m_run;
-    ml[warp * GP + lane] = l_run;
-  }
-  __syncthreads();
-  float* dst = a.part + ((static_cast<int64_t>(b) * Hkv + j) * a.splits + split) * (GP * (D + 2));
-  for (int e = threadIdx.x; e < GP * D; e += kWarps * 32) {
-    const int g = e / D;
-    float M = -INFINITY;
+
+    // ---- merge the warps' states for this segment
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mm[w * GP + g]);
-    float acc = 0.f;
-    if (M != -INFINITY) {
+    for (int w = GP; w < 32; w <<= 1) l_run += __shfl_xor_sync(kFull, l_run, w);
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) acc = fmaf(exp2_fast(mm[w * GP + g] - M), mo[(w * GP + g) * D + (e - g * D)], acc);
+    for (int w = LPK; w < 32; w <<= 1)
+#pragma unroll
+      for (int h = 0; h < GP; ++h)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[h][e] += __shfl_xor_sync(kFull, o[h][e], w);
+    if (last_stage >= 0 && lane < LPK) {
+      float* os = reinterpret_cast<float*>(wsm + last_stage * Gm::STAGE);
+#pragma unroll
+      for (int h = 0; h < GP; ++h) {
+        *reinterpret_cast<float4*>(os + h * D + dl) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+        *reinterpret_cast<float4*>(os + h * D + dl + 4) = make_float4(o[h][4], o[h][5], o[h][6], o[h][7]);
+      }
     }
-    dst[e] = acc;
-  }
-  if (threadIdx.x < GP) {
-    const int g = threadIdx.x;
-    float M = -INFINITY;
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mm[w * GP + g]);
-    float L = 0.f;
-    if (M != -INFINITY)
-      for (int w = 0; w < kWarps; ++w) L = fmaf(exp2_fast(mm[w * GP + g] - M), ml[w * GP + g], L);
-    dst[GP * D + g] = M;
-    dst[GP * D + GP + g] = L;
+    if (lane < GP) {
+      ML[warp * 2 * GP + lane] = last_stage >= 0 ? m_run : -INFINITY;
+      ML[warp * 2 * GP + GP + lane] = last_stage >= 0 ? l_run : 0.f;
+    }
+    if (lane == 0) SLOT[warp] = last_stage;
+    __syncthreads();
+    const int slot = first_seg ? cta : NC + u;
+    float* dst = a.part + static_cast<int64_t>(slot) * (GP * (D + 2));
+    for (int e = threadIdx.x; e < GP * D; e += kThreads) {
+      const int h = e / D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ML[w * 2 * GP + h]);
+      float acc = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          const int st = SLOT[w];
+          if (st >= 0) {
+            const float* os = reinterpret_cast<const float*>(smem + (w * NS + st) * Gm::STAGE);
+            acc = fmaf(exp2_fast(ML[w * 2 * GP + h] - M), os[e], acc);
+          }
+        }
+      }
+      dst[e] = acc;
+    }
+    if (threadIdx.x < GP) {
+      const int h = threadIdx.x;
+      float M = -INFINITY;
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ML[w * 2 * GP + h]);
+      float L = 0.f;
+      if (M != -INFINITY)
+        for (int w = 0; w < kWarps; ++w) L = fmaf(exp2_fast(ML[w * 2 * GP + h] - M), ML[w * 2 * GP + GP + h], L);
+      dst[GP * D + h] = M;
+      dst[GP * D + GP + h] = L;
+    }
+    __syncthreads();
+    if (deferred >= 0) {
+      if (lane == 0 && !failed) {
+        fence_proxy_async_smem();
+        issue(deferred);
+      }
+      deferred = -1;
+    }
+    first_seg = false;
   }
 }
 
 // ---------------------------------------------------------------- combine
 
-// Threads per head in the combine: TPH lanes, each 4 dims of a DSPLIT-th of D.
 // One CTA per (dim chunk, KV head, stream); the G heads of the group each use
-// TPH consecutive lanes of one warp.
+// TPH consecutive lanes of one warp, 4 dims per lane.
 template <int TPH>
 __device__ __forceinline__ float group_sum(float x) {
 #pragma unroll
@@ -374,7 +474,7 @@ __device__ __forceinline__ float group_max(float x) {
 
 template <int D, int TPH, bool PAGED>
 __global__ void __launch_bounds__(256) decode_combine_kernel(const CombineArgs a, int G, int GP) {
-  extern __shared__ float wsm[];  // [heads in block][splits]: weights of the splits
+  extern __shared__ float wsm[];  // [heads in block][max segments]: merge weights
   const int chunk_d = TPH * 4;
   const int dc = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
   // the block is a whole number of warps; lanes past the G heads repeat the
@@ -387,10 +487,9 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const CombineArgs a
   const CacheView& c = a.c;
 
   // ---- caller inputs (not produced by the split kernel): before the wait
-  int n = 0, wb_slot = -1;
   int64_t wb_off = -1;  // element offset of the new entry's row for KV head j
   if constexpr (PAGED) {
-    n = c.seq_len[b];
+    int n = c.seq_len[b];
     const int cap = min(a.max_len, c.bt_stride * c.P);
     n = n < 0 ? 0 : (n > cap ? cap : n);
     if (a.write_back) {
@@ -404,72 +503,123 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const CombineArgs a
   } else {
     const int row = c.stream_rows ? c.stream_rows[b] : b;
     const int head = c.ring_head[b], cnt = c.ring_count[b];
-    if (!(row < 0 || row >= c.n_rows || head < 0 || head >= c.R || cnt < 0 || cnt > c.R)) {
-      n = cnt;
-      wb_slot = head;
-      wb_off = ((static_cast<int64_t>(row) * Hkv + j) * c.R + wb_slot) * D;
-    }
+    if (!(row < 0 || row >= c.n_rows || head < 0 || head >= c.R || cnt < 0 || cnt > c.R))
+      wb_off = ((static_cast<int64_t>(row) * Hkv + j) * c.R + head) * D;
   }
-  const int S = n > 0 ? (n + a.chunk - 1) / a.chunk : 0;
   const uint2 vw = *reinterpret_cast<const uint2*>(a.v_new + (static_cast<int64_t>(b) * Hkv + j) * D + d4);
   float sig = 1.f;
   if (a.gate) sig = 1.f / (1.f + expf(-bf16_to_f32(a.gate[static_cast<int64_t>(b) * Hq + h])));
 
-  pdl_wait();  // partials of the split kernel
+  pdl_wait();  // partials and the tile table of the split kernel
   pdl_trigger();
 
-  // ---- new token's score (base 2): q_hat (pre-scaled) . k_entry over all D
+  // ---- this unit's segments: CTAs c_lo..c_hi of the split grid
+  const int U = a.B * Hkv, u = b * Hkv + j, NC = a.split_ctas;
+  const int T = a.tiles[U];
+  const int p0 = a.tiles[u], p1 = a.tiles[u + 1];
+  int S = 0, c_lo = 0, first_slot = 0;
+  if (p1 > p0) {
+    // CTA of global tile x: floor(((x + 1) * NC - 1) / T)
+    c_lo = static_cast<int>((static_cast<int64_t>(p0 + 1) * NC - 1) / T);
+    const int c_hi = static_cast<int>((static_cast<int64_t>(p1) * NC - 1) / T);
+    S = c_hi - c_lo + 1;
+    const int begin_lo = static_cast<int>(static_cast<int64_t>(c_lo) * T / NC);
+    first_slot = begin_lo == p0 ? c_lo : NC + u;
+  }
+
+  // ---- loads first: the segments' (m, l) and their first output slices,
+  // q_hat and the new key entry - none depends on another
+  const int stride = GP * (D + 2);
+  auto seg = [&](int k) -> const float* {
+    return a.part + static_cast<int64_t>(k == 0 ? first_slot : c_lo + k) * stride;
+  };
+  // Segment k > 0 is the first segment of split CTA c_lo + k - unless that CTA
+  // got no tiles at all (possible when the call's keys are far below its
+  // planned bound), in which case it wrote nothing and is skipped.
+  auto seg_ok = [&](int k) -> bool {
+    if (k == 0) return true;
+    const int64_t cc = c_lo + k;
+    return cc * T / NC < (cc + 1) * T / NC;
+  };
+  constexpr int kPre = 4;
+  float mk = -INFINITY, lk = 0.f;
+  if (t < S && seg_ok(t)) {
+    const float* pk = seg(t);
+    mk = pk[GP * D + g];
+    lk = pk[GP * D + GP + g];
+  }
+  float4 ov[kPre];
+#pragma unroll
+  for (int x = 0; x < kPre; ++x)
+    ov[x] = x < S && seg_ok(x) ? *reinterpret_cast<const float4*>(seg(x) + g * D + d4)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+  constexpr int NQ = D / (4 * TPH);
   const float* qh = a.qhat + (static_cast<int64_t>(b) * Hq + h) * D;
   const uint16_t* kh = a.khat + (static_cast<int64_t>(b) * Hkv + j) * D;
+  float4 qv[NQ];
+  uint2 kv[NQ];
+#pragma unroll
+  for (int x = 0; x < NQ; ++x) {
+    qv[x] = *reinterpret_cast<const float4*>(qh + (t + x * TPH) * 4);
+    kv[x] = *reinterpret_cast<const uint2*>(kh + (t + x * TPH) * 4);
+  }
+
+  // ---- new token's score (base 2): q_hat (pre-scaled) . k_entry over all D
   float dot = 0.f;
-  for (int d = t * 4; d < D; d += TPH * 4) {
-    const float4 qv = *reinterpret_cast<const float4*>(qh + d);
-    const uint2 kw = *reinterpret_cast<const uint2*>(kh + d);
-    dot = fmaf(qv.x, bf16_lo(kw.x), dot);
-    dot = fmaf(qv.y, bf16_hi(kw.x), dot);
-    dot = fmaf(qv.z, bf16_lo(kw.y), dot);
-    dot = fmaf(qv.w, bf16_hi(kw.y), dot);
+#pragma unroll
+  for (int x = 0; x < NQ; ++x) {
+    dot = fmaf(qv[x].x, bf16_lo(kv[x].x), dot);
+    dot = fmaf(qv[x].y, bf16_hi(kv[x].x), dot);
+    dot = fmaf(qv[x].z, bf16_lo(kv[x].y), dot);
+    dot = fmaf(qv[x].w, bf16_hi(kv[x].y), dot);
   }
   const float s_new = group_sum<TPH>(dot);
 
-  // ---- merge: M over the splits and the new token, then weights and L
-  const int stride = GP * (D + 2);
-  const float* P0 = a.part + (static_cast<int64_t>(b) * Hkv + j) * a.splits * stride;
-  float M = s_new;
-  for (int s = t; s < S; s += TPH) M = fmaxf(M, P0[s * stride + GP * D + g]);
-  M = group_max<TPH>(M);
-  float L = 0.f;
-  for (int s = t; s < S; s += TPH) {
-    const float w = exp2_fast(P0[s * stride + GP * D + g] - M);
-    wsm[gb * a.splits + s] = w;
-    L = fmaf(w, P0[s * stride + GP * D + GP + g], L);
-  }
-  L = group_sum<TPH>(L);
-  __syncwarp();
-  // the weighted sum of the partial outputs: loads issued ahead of the FMAs
+  // ---- merge: M over the segments and the new token, weights, L, outputs
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float* po = P0 + g * D + d4;
-  int s = 0;
-  for (; s + 4 <= S; s += 4) {
-    float4 v[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) v[u] = *reinterpret_cast<const float4*>(po + (s + u) * stride);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float w = wsm[gb * a.splits + s + u];
-      acc.x = fmaf(w, v[u].x, acc.x);
-      acc.y = fmaf(w, v[u].y, acc.y);
-      acc.z = fmaf(w, v[u].z, acc.z);
-      acc.w = fmaf(w, v[u].w, acc.w);
-    }
-  }
-  for (; s < S; ++s) {
-    const float4 v = *reinterpret_cast<const float4*>(po + s * stride);
-    const float w = wsm[gb * a.splits + s];
+  auto fold = [&](float w, const float4& v) {
     acc.x = fmaf(w, v.x, acc.x);
     acc.y = fmaf(w, v.y, acc.y);
     acc.z = fmaf(w, v.z, acc.z);
     acc.w = fmaf(w, v.w, acc.w);
+  };
+  float M, L;
+  if (S <= TPH) {
+    // one segment per lane: weights stay in registers and are broadcast
+    M = group_max<TPH>(fmaxf(s_new, mk));
+    const float w = t < S ? exp2_fast(mk - M) : 0.f;
+    L = group_sum<TPH>(w * lk);
+    const int base = threadIdx.x - t;  // first lane of this head's group
+#pragma unroll
+    for (int x = 0; x < kPre; ++x) {
+      const float wx = __shfl_sync(kFull, w, (base + x) & 31);
+      if (x < S) fold(wx, ov[x]);
+    }
+    for (int k = kPre; k < S; ++k) {
+      const float wk = __shfl_sync(kFull, w, (base + k) & 31);
+      if (seg_ok(k)) fold(wk, *reinterpret_cast<const float4*>(seg(k) + g * D + d4));
+    }
+  } else {
+    M = mk;
+    for (int k = t + TPH; k < S; k += TPH)
+      if (seg_ok(k)) M = fmaxf(M, seg(k)[GP * D + g]);
+    M = group_max<TPH>(fmaxf(M, s_new));
+    L = 0.f;
+    for (int k = t; k < S; k += TPH) {
+      float w = 0.f;
+      if (seg_ok(k)) {
+        const float* pk = seg(k);
+        w = exp2_fast(pk[GP * D + g] - M);
+        L = fmaf(w, pk[GP * D + GP + g], L);
+      }
+      wsm[gb * a.split_ctas + k] = w;
+    }
+    L = group_sum<TPH>(L);
+    __syncwarp();
+#pragma unroll
+    for (int x = 0; x < kPre; ++x) fold(wsm[gb * a.split_ctas + x], ov[x]);
+    for (int k = kPre; k < S; ++k)
+      if (seg_ok(k)) fold(wsm[gb * a.split_ctas + k], *reinterpret_cast<const float4*>(seg(k) + g * D + d4));
   }
   // the new token joins as a length-1 score vector
   const float wn = exp2_fast(s_new - M);
@@ -497,12 +647,12 @@ cudaError_t split_launch(const SplitArgs& a, int G, cudaStream_t s) {
   auto k = decode_split_kernel<D, GP, PAGED>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM_MAX);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid(a.splits, a.Hkv, a.B);
-  return launch_pdl(k, grid, dim3(kWarps * 32), Gm::SMEM, s, a, G);
+  const size_t smem = Gm::TAB_OFF + (2 * a.B * a.Hkv + 1) * sizeof(int);
+  return launch_pdl(k, dim3(a.ctas), dim3(kThreads), smem, s, a, G);
 }
 
 template <int D, int GP>
@@ -512,10 +662,20 @@ cudaError_t split_dispatch_paged(const SplitArgs& a, int G, cudaStream_t s) {
 
 int padded_group(int G) { return G <= 2 ? 2 : (G <= 4 ? 4 : (G <= 8 ? 8 : 0)); }
 
+template <int D>
+int geo_smem_max(int GP) {
+  return GP == 2 ? Geo<D, 2>::SMEM_MAX : GP == 4 ? Geo<D, 4>::SMEM_MAX : GP == 8 ? Geo<D, 8>::SMEM_MAX : 0;
+}
+template <int D>
+int geo_stage_keys(int GP) {
+  return GP == 2 ? Geo<D, 2>::SK : GP == 4 ? Geo<D, 4>::SK : GP == 8 ? Geo<D, 8>::SK : 0;
+}
+
 }  // namespace
 
 cudaError_t launch_decode_split(const SplitArgs& a, int D, int G, cudaStream_t s) {
   const int GP = padded_group(G);
+  if (a.B * a.Hkv > kMaxUnits) return cudaErrorNotSupported;
   if (D == 256) {
     if (GP == 2) return split_dispatch_paged<256, 2>(a, G, s);
     if (GP == 4) return split_dispatch_paged<256, 4>(a, G, s);
@@ -530,20 +690,20 @@ cudaError_t launch_decode_split(const SplitArgs& a, int D, int G, cudaStream_t s
 
 int decode_split_tile_keys(int D, int G) {
   const int GP = padded_group(G);
-  if (GP == 0 || (D != 128 && D != 256)) return 0;
-  return (D / 8 / GP) * (32 / (D / 8));
+  if (GP == 0) return 0;
+  return D == 256 ? geo_stage_keys<256>(GP) : D == 128 ? geo_stage_keys<128>(GP) : 0;
 }
 
 int decode_split_ctas_per_sm(int D, int G) {
   const int GP = padded_group(G);
-  int smem = 0;
-  if (D == 256) smem = GP == 2 ? Geo<256, 2>::SMEM : GP == 4 ? Geo<256, 4>::SMEM : GP == 8 ? Geo<256, 8>::SMEM : 0;
-  if (D == 128) smem = GP == 2 ? Geo<128, 2>::SMEM : GP == 4 ? Geo<128, 4>::SMEM : GP == 8 ? Geo<128, 8>::SMEM : 0;
+  const int smem = GP == 0 ? 0 : D == 256 ? geo_smem_max<256>(GP) : D == 128 ? geo_smem_max<128>(GP) : 0;
   if (smem == 0) return 0;
   // 228 KB of shared memory per SM, 1 KB of it reserved per resident CTA
-  int per_sm = (233472) / (smem + 1024);
+  const int per_sm = 233472 / (smem + 1024);
   return per_sm > 2 ? 2 : per_sm;
 }
+
+int decode_max_units() { return kMaxUnits; }
 
 cudaError_t launch_decode_combine(const CombineArgs& a, int D, int G, cudaStream_t s) {
   const int GP = padded_group(G);
@@ -554,15 +714,14 @@ cudaError_t launch_decode_combine(const CombineArgs& a, int D, int G, cudaStream
   const int dmin = D / 128;  // TPH <= 32
   const int dmax = D / 32;   // TPH >= 8
   dsplit = dsplit < dmin ? dmin : (dsplit > dmax ? dmax : dsplit);
-  // round up to a power of two
   int p2 = 1;
   while (p2 < dsplit) p2 <<= 1;
   dsplit = p2 > dmax ? dmax : p2;
   const int tph = D / 4 / dsplit;
-  dim3 grid(dsplit, a.Hkv, a.B);
   const int threads = (G * tph + 31) / 32 * 32;
+  dim3 grid(dsplit, a.Hkv, a.B);
   dim3 block(threads);
-  const size_t smem = static_cast<size_t>(threads / tph) * a.splits * sizeof(float);
+  const size_t smem = static_cast<size_t>(threads / tph) * a.split_ctas * sizeof(float);
   const bool paged = a.c.paged != 0;
 #define DATTN_COMBINE(DD, TT)                                                                     \
   if (D == DD && tph == TT)                                                                       \

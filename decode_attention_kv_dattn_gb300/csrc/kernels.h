@@ -47,15 +47,18 @@ struct RopeArgs {
   int* err;
 };
 
-// Split-K pass over the cached keys of a decode call.
+// Split-K pass over the cached keys of a decode call (stream-K: the grid of
+// `ctas` CTAs cuts the concatenated tiles of all (stream, KV head) units into
+// equal ranges). Partial slot of a segment: the CTA index for the first
+// segment of a CTA's range, ctas + unit for any later one.
 struct SplitArgs {
   CacheView c;
   int B, Hkv;
-  int chunk;                   // keys per split
-  int splits;                  // S: grid.x
+  int ctas;                    // grid size
   int max_len;                 // host bound on cached length (paged)
   const float* qhat;           // [B, Hq, D]
-  float* part;                 // [B, Hkv, S, G*(D+2)]: o[G][D], m[G], l[G]
+  float* part;                 // [ctas + B*Hkv][GP*(D+2)]: o[GP][D], m[GP], l[GP]
+  int* tiles;                  // [B*Hkv + 1] out: tile prefix over units
   int* err;
 };
 
@@ -63,7 +66,9 @@ struct SplitArgs {
 struct CombineArgs {
   CacheView c;
   int B, Hkv;
-  int chunk, splits, max_len;
+  int split_ctas;              // grid size of the split pass
+  const int* tiles;            // [B*Hkv + 1] from the split pass
+  int max_len;
   const float* qhat;           // [B, Hq, D]
   const uint16_t* khat;        // [B, Hkv, D]
   const uint16_t* v_new;       // [B, Hkv, D]
@@ -95,8 +100,10 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 
 // Resident CTAs per SM of the split kernel for (D, G) (0 if unsupported).
 int decode_split_ctas_per_sm(int D, int G);
-// Keys per tile of the split kernel for (D, G).
+// Keys per stage tile of the split kernel for (D, G).
 int decode_split_tile_keys(int D, int G);
+// Largest number of (stream, KV head) units of one decode call.
+int decode_max_units();
 
 // Launch with programmatic stream serialization: the kernel may begin while
 // its predecessor in the stream finishes; every kernel here waits on the

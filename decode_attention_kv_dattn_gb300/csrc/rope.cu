@@ -18,67 +18,109 @@ namespace dattn {
 
 namespace {
 
-constexpr int kRopeThreads = 64;
+constexpr int kRopeThreads = 64;      // append kernel
+constexpr int kRowThreads = 512;      // prologue: one CTA per token row
+constexpr int kMaxItems = 8;          // pair slots per thread (heads * D/2 <= 512 * 8)
+constexpr int kMaxT = 16;             // verify rows per stream
 
-// Position of verify row `row` = s*T + i: prefix_len[s] + depth(i), walking
-// the parent pointers (parent[i] < i, -1 = root). A bad parent stops the walk
-// and is reported.
-__device__ __forceinline__ int64_t verify_position(const RopeArgs& a, int row, int* err) {
-  const int s = row / a.T;
-  const int i = row - s * a.T;
-  const int32_t* par = a.parent + static_cast<int64_t>(s) * a.T;
-  int depth = 0;
-  int node = i;
-  for (int steps = 0; steps < a.T; ++steps) {
-    const int p = par[node];
-    if (p < 0) break;
-    if (p >= node) {
-      raise_error(err, ERR_INDEX);
-      break;
-    }
-    ++depth;
-    node = p;
-  }
-  return static_cast<int64_t>(a.prefix_len[s]) + depth;
-}
-
-__global__ void __launch_bounds__(kRopeThreads) rope_kernel(const RopeArgs a) {
+// The prologue of a call: one CTA per token row. Work items are "pair slots"
+// of every head (Hq query heads, then Hkv key heads): slot p < r/2 is the
+// rotated pair (p, p + r/2); slot p >= r/2 holds two pass-through dims. All
+// inputs are loaded first; the fp64 cos/sin of each pair index is computed
+// once per row (one thread each) into shared memory meanwhile.
+__global__ void __launch_bounds__(kRowThreads) rope_kernel(const RopeArgs a) {
+  __shared__ float cs_c[128], cs_s[128];
+  __shared__ int64_t pos_s;
+  __shared__ int par_s[kMaxT];
   // The workspace written below may still be read by the previous call.
   pdl_wait();
   pdl_trigger();
-  const int row = blockIdx.y;
-  const int job = blockIdx.x * kRopeThreads + threadIdx.x;
+  const int row = blockIdx.x;
   const int half = a.r / 2;
-  if (job >= half + (a.D - a.r)) return;
-  const int64_t pos = a.parent ? verify_position(a, row, a.err) : a.pos[row];
-  const uint16_t* q = a.q + static_cast<int64_t>(row) * a.Hq * a.D;
-  const uint16_t* k = a.k + static_cast<int64_t>(row) * a.Hkv * a.D;
-  float* qh = a.qhat + static_cast<int64_t>(row) * a.Hq * a.D;
-  uint16_t* kh = a.khat + static_cast<int64_t>(row) * a.Hkv * a.D;
-  if (job < half) {
-    const int i = job;
-    const double angle = __dmul_rn(static_cast<double>(pos), a.inv_freq[i]);
+  const int slots = a.D / 2;
+  const int heads = a.Hq + a.Hkv;
+  const int items = heads * slots;
+
+  // ---- loads of this thread's pair slots (independent of the position)
+  uint32_t xy[kMaxItems];
+#pragma unroll
+  for (int k = 0; k < kMaxItems; ++k) {
+    const int it = threadIdx.x + k * kRowThreads;
+    xy[k] = 0;
+    if (it < items) {
+      const int hh = it / slots, p = it - hh * slots;
+      const uint16_t* src = hh < a.Hq ? a.q + (static_cast<int64_t>(row) * a.Hq + hh) * a.D
+                                      : a.k + (static_cast<int64_t>(row) * a.Hkv + (hh - a.Hq)) * a.D;
+      const int d0 = p < half ? p : a.r + 2 * (p - half);
+      const int d1 = p < half ? p + half : d0 + 1;
+      xy[k] = static_cast<uint32_t>(src[d0]) | (static_cast<uint32_t>(src[d1]) << 16);
+    }
+  }
+  // ---- position of the row
+  if (a.parent) {
+    const int T = a.T;
+    const int s = row / T, i = row - s * T;
+    if (threadIdx.x < T) par_s[threadIdx.x] = a.parent[static_cast<int64_t>(s) * T + threadIdx.x];
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int depth = 0, node = i;
+      for (int steps = 0; steps < T; ++steps) {
+        const int p = par_s[node];
+        if (p < 0) break;
+        if (p >= node) {
+          raise_error(a.err, ERR_INDEX);
+          break;
+        }
+        ++depth;
+        node = p;
+      }
+      pos_s = static_cast<int64_t>(a.prefix_len[s]) + depth;
+    }
+  } else if (threadIdx.x == 0) {
+    pos_s = a.pos[row];
+  }
+  __syncthreads();
+  if (threadIdx.x < half) {
+    const double angle = __dmul_rn(static_cast<double>(pos_s), a.inv_freq[threadIdx.x]);
     double sd, cd;
     sincos(angle, &sd, &cd);
-    const float cf = __double2float_rn(cd);
-    const float sf = __double2float_rn(sd);
-    for (int h = 0; h < a.Hq; ++h) {
-      const float x = bf16_to_f32(q[h * a.D + i]);
-      const float y = bf16_to_f32(q[h * a.D + i + half]);
-      qh[h * a.D + i] = fmaf(x, cf, -y * sf) * a.q_scale;
-      qh[h * a.D + i + half] = fmaf(y, cf, x * sf) * a.q_scale;
+    cs_c[threadIdx.x] = __double2float_rn(cd);
+    cs_s[threadIdx.x] = __double2float_rn(sd);
+  }
+  __syncthreads();
+
+  // ---- rotate and store
+#pragma unroll
+  for (int k = 0; k < kMaxItems; ++k) {
+    const int it = threadIdx.x + k * kRowThreads;
+    if (it >= items) break;
+    const int hh = it / slots, p = it - hh * slots;
+    const int d0 = p < half ? p : a.r + 2 * (p - half);
+    const int d1 = p < half ? p + half : d0 + 1;
+    const float x = bf16_to_f32(static_cast<uint16_t>(xy[k] & 0xffffu));
+    const float y = bf16_to_f32(static_cast<uint16_t>(xy[k] >> 16));
+    if (hh < a.Hq) {
+      float* dst = a.qhat + (static_cast<int64_t>(row) * a.Hq + hh) * a.D;
+      if (p < half) {
+        const float cf = cs_c[p], sf = cs_s[p];
+        dst[d0] = fmaf(x, cf, -y * sf) * a.q_scale;
+        dst[d1] = fmaf(y, cf, x * sf) * a.q_scale;
+      } else {
+        dst[d0] = x * a.q_scale;
+        dst[d1] = y * a.q_scale;
+      }
+    } else {
+      uint16_t* dst = a.khat + (static_cast<int64_t>(row) * a.Hkv + (hh - a.Hq)) * a.D;
+      if (p < half) {
+        const double c64 = cs_c[p], s64 = cs_s[p];
+        const double xd = x, yd = y;
+        dst[d0] = f64_to_bf16(__dsub_rn(__dmul_rn(xd, c64), __dmul_rn(yd, s64)));
+        dst[d1] = f64_to_bf16(__dadd_rn(__dmul_rn(yd, c64), __dmul_rn(xd, s64)));
+      } else {
+        dst[d0] = static_cast<uint16_t>(xy[k] & 0xffffu);
+        dst[d1] = static_cast<uint16_t>(xy[k] >> 16);
+      }
     }
-    const double c64 = cf, s64 = sf;
-    for (int h = 0; h < a.Hkv; ++h) {
-      const double x = bf16_to_f32(k[h * a.D + i]);
-      const double y = bf16_to_f32(k[h * a.D + i + half]);
-      kh[h * a.D + i] = f64_to_bf16(__dsub_rn(__dmul_rn(x, c64), __dmul_rn(y, s64)));
-      kh[h * a.D + i + half] = f64_to_bf16(__dadd_rn(__dmul_rn(y, c64), __dmul_rn(x, s64)));
-    }
-  } else {
-    const int d = a.r + (job - half);
-    for (int h = 0; h < a.Hq; ++h) qh[h * a.D + d] = bf16_to_f32(q[h * a.D + d]) * a.q_scale;
-    for (int h = 0; h < a.Hkv; ++h) kh[h * a.D + d] = k[h * a.D + d];
   }
 }
 
@@ -163,9 +205,9 @@ __global__ void __launch_bounds__(kRopeThreads) append_kernel(const AppendArgs a
 }  // namespace
 
 cudaError_t launch_rope(const RopeArgs& a, cudaStream_t s) {
-  const int jobs = a.r / 2 + (a.D - a.r);
-  dim3 grid((jobs + kRopeThreads - 1) / kRopeThreads, a.rows);
-  return launch_pdl(rope_kernel, grid, dim3(kRopeThreads), 0, s, a);
+  if ((a.Hq + a.Hkv) * (a.D / 2) > kRowThreads * kMaxItems || a.r > 256 || (a.parent && a.T > kMaxT))
+    return cudaErrorNotSupported;
+  return launch_pdl(rope_kernel, dim3(a.rows), dim3(kRowThreads), 0, s, a);
 }
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {

@@ -140,6 +140,19 @@ def test_paged_group_sizes(dattn, oracle, D, Hq, Hkv):
     run_and_check(dattn, oracle, case)
 
 
+def test_lengths_far_below_the_planned_bound(dattn, oracle):
+    """The split grid is sized from the call's bound; when the streams are much
+    shorter, many split CTAs get no keys and the combine must skip them."""
+    case = paged_case(45, 3, 8, 2, 256, 16, [17, 0, 5], gate=True)
+    dc = DeviceCase(case)
+    h = make_handle(dattn, case, max_context=65536)
+    h.decode(0, dc.cache_desc(dattn), dc.q, dc.k_new, dc.v_new, dc.pos, dc.out, gate=dc.gate,
+             max_seq_len=65536)
+    assert h.get_error() == dattn.OK
+    ref, ke, ve = oracle_decode(oracle, case)
+    assert_close(dc.out.cpu().numpy(), ref)
+
+
 # ------------------------------------------------------------------ properties
 
 def test_run_to_run_bit_identity(dattn):
