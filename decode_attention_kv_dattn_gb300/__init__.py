@@ -23,7 +23,7 @@ lib = ctypes.CDLL(LIB_PATH)
 
 # ---------------------------------------------------------------- C types
 
-OK, EINVAL, EXCEEDS, ECUDA, EINDEX, ETIMEOUT, EUNSUPPORTED, ELENGTH = range(8)
+OK, EINVAL, EXCEEDS, ECUDA, EINDEX, ETIMEOUT, EUNSUPPORTED, ELENGTH, ERANGE = range(9)
 CACHE_RING, CACHE_PAGED = 0, 1
 
 _vp = ctypes.c_void_p

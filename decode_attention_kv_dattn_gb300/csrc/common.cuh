@@ -152,4 +152,42 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   return r;
 }
 
+// Inclusive prefix sum of x[0, n) in shared memory by a whole block of NT
+// threads (NT a multiple of 32, at most 1024).
+template <int NT>
+__device__ void block_scan_inclusive(int* x, int n) {
+  __shared__ int warp_sum[NT / 32];
+  const int t = threadIdx.x;
+  const int per = (n + NT - 1) / NT;
+  const int lo = min(n, t * per), hi = min(n, lo + per);
+  int sum = 0;
+  for (int i = lo; i < hi; ++i) {
+    sum += x[i];
+    x[i] = sum;
+  }
+  int incl = sum;
+#pragma unroll
+  for (int w = 1; w < 32; w <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, w);
+    if ((t & 31) >= w) incl += y;
+  }
+  if ((t & 31) == 31) warp_sum[t >> 5] = incl;
+  __syncthreads();
+  int before = incl - sum;
+  for (int w = 0; w < (t >> 5); ++w) before += warp_sum[w];
+  for (int i = lo; i < hi; ++i) x[i] += before;
+  __syncthreads();
+}
+
+// Last unit u in [0, U) with P[u] <= g (P[0] = 0 <= g); its tile range
+// [P[u], P[u + 1]) then contains g.
+__device__ __forceinline__ int unit_of(const int* P, int U, int g) {
+  int lo = 0, hi = U - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (P[mid] <= g) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 }  // namespace dattn

@@ -34,6 +34,8 @@ struct dattn_handle {
   int* tiles = nullptr;    // tile prefix over units, from the split pass
   uint16_t* khat = nullptr;
   float* part = nullptr;
+  float* vpart = nullptr;   // verify partials: [sms + units][G*T][D+4]
+  size_t vpart_slots = 0;
   int* err = nullptr;
 };
 
@@ -122,6 +124,7 @@ const char* dattn_error_string(int code) {
     case DATTN_ETIMEOUT: return "a bounded device wait timed out";
     case DATTN_EUNSUPPORTED: return "shape not supported by this build";
     case DATTN_ELENGTH: return "a stream is longer than the call's bound";
+    case DATTN_ERANGE: return "a cached value lies outside the fp16 range the verify pass computes in";
     default: return "unknown dattn status";
   }
 }
@@ -202,6 +205,13 @@ int dattn_create(const dattn_config* cfg, int device, dattn_t** out) {
     return fail(DATTN_ECUDA);
   const size_t part_floats = h->part_units * h->GP * (D + 2);
   if (cudaMalloc(&h->part, part_floats * sizeof(float)) != cudaSuccess) return fail(DATTN_ECUDA);
+  if (h->max_verify_rows > 0) {
+    if (G * h->max_verify_rows > 128) return fail(DATTN_EUNSUPPORTED);
+    if (static_cast<int64_t>(h->max_streams) * Hkv > kVerifyMaxUnits) return fail(DATTN_EUNSUPPORTED);
+    h->vpart_slots = static_cast<size_t>(h->num_sms) + static_cast<size_t>(h->max_streams) * Hkv;
+    const size_t vfloats = h->vpart_slots * G * h->max_verify_rows * (D + 4);
+    if (cudaMalloc(&h->vpart, vfloats * sizeof(float)) != cudaSuccess) return fail(DATTN_ECUDA);
+  }
   if (cudaMalloc(&h->err, sizeof(int)) != cudaSuccess) return fail(DATTN_ECUDA);
   if (cudaMemset(h->err, 0, sizeof(int)) != cudaSuccess) return fail(DATTN_ECUDA);
   *out = h;
@@ -215,6 +225,7 @@ void dattn_destroy(dattn_t* h) {
   cudaFree(h->qhat);
   cudaFree(h->khat);
   cudaFree(h->part);
+  cudaFree(h->vpart);
   cudaFree(h->tiles);
   cudaFree(h->err);
   delete h;
@@ -232,6 +243,7 @@ int dattn_get_error(dattn_t* h, dattn_stream_t stream) {
   if (cudaStreamSynchronize(s) != cudaSuccess) return DATTN_ECUDA;
   if (bits & ERR_TIMEOUT) return DATTN_ETIMEOUT;
   if (bits & ERR_INDEX) return DATTN_EINDEX;
+  if (bits & ERR_RANGE) return DATTN_ERANGE;
   if (bits & ERR_LENGTH) return DATTN_ELENGTH;
   return DATTN_OK;
 }
@@ -346,11 +358,81 @@ int dattn_decode(dattn_t* h, int layer, const dattn_cache* cache, const dattn_de
 
 int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, const dattn_verify_args* args,
                  dattn_stream_t stream) {
-  (void)cache;
-  (void)args;
-  (void)stream;
-  if (!h || layer < 0 || layer >= static_cast<int>(h->layers.size())) return DATTN_EINVAL;
-  return DATTN_EUNSUPPORTED;
+  if (!h || !args || layer < 0 || layer >= static_cast<int>(h->layers.size())) return DATTN_EINVAL;
+  const dattn_layer_config& L = h->layers[layer];
+  if (L.cache_kind != DATTN_CACHE_PAGED) return DATTN_EUNSUPPORTED;
+  int rc = check_cache(L, cache);
+  if (rc != DATTN_OK) return rc;
+  const int S = args->num_streams, T = args->rows;
+  if (S <= 0 || T <= 0) return DATTN_EINVAL;
+  if (h->max_verify_rows == 0 || T > h->max_verify_rows || S > h->max_streams) return DATTN_EXCEEDS;
+  if (!args->q || !args->k || !args->v || !args->parent || !args->out) return DATTN_EINVAL;
+  if (!aligned16(args->q) || !aligned16(args->k) || !aligned16(args->v) || !aligned16(args->out))
+    return DATTN_EINVAL;
+  const int n_max = args->max_prefix_len > 0 ? args->max_prefix_len : h->max_context;
+  if (n_max > h->max_context) return DATTN_EXCEEDS;
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return DATTN_ECUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  RopeArgs ra{};
+  ra.rows = S * T;
+  ra.Hq = h->Hq;
+  ra.Hkv = h->Hkv;
+  ra.D = h->D;
+  ra.r = L.rotary_dim;
+  ra.q = static_cast<const uint16_t*>(args->q);
+  ra.k = static_cast<const uint16_t*>(args->k);
+  ra.prefix_len = cache->seq_len;
+  ra.parent = args->parent;
+  ra.T = T;
+  ra.inv_freq = h->inv_freq[layer];
+  ra.q_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(h->D)));
+  ra.qhat = h->qhat;
+  ra.khat = h->khat;
+  ra.err = h->err;
+  rc = cuda_status(launch_rope(ra, s));
+  if (rc != DATTN_OK) return rc;
+
+  // one CTA per SM, at least two tiles each for the largest prefix this call may have
+  const int64_t tiles = static_cast<int64_t>(S) * h->Hkv * ((n_max + kVerifyTileKeys - 1) / kVerifyTileKeys);
+  int64_t ctas = (tiles + 1) / 2;
+  if (ctas > h->num_sms) ctas = h->num_sms;
+  if (ctas < 1) ctas = 1;
+  VerifySplitArgs va{};
+  va.c = make_view(h, L, cache);
+  va.S = S;
+  va.T = T;
+  va.Hkv = h->Hkv;
+  va.G = h->G;
+  va.ctas = static_cast<int>(ctas);
+  va.max_len = n_max;
+  va.qhat = h->qhat;
+  va.part = h->vpart;
+  va.tiles = h->tiles;
+  va.err = h->err;
+  rc = cuda_status(launch_verify_split(va, h->D, s));
+  if (rc != DATTN_OK) return rc;
+
+  VerifyCombineArgs vc{};
+  vc.c = va.c;
+  vc.S = S;
+  vc.T = T;
+  vc.Hkv = h->Hkv;
+  vc.G = h->G;
+  vc.split_ctas = va.ctas;
+  vc.tiles = h->tiles;
+  vc.max_len = n_max;
+  vc.qhat = h->qhat;
+  vc.khat = h->khat;
+  vc.v = static_cast<const uint16_t*>(args->v);
+  vc.parent = args->parent;
+  vc.gate = static_cast<const uint16_t*>(args->gate);
+  vc.part = h->vpart;
+  vc.out = args->out;
+  vc.write_back = args->write_back;
+  vc.err = h->err;
+  return cuda_status(launch_verify_combine(vc, h->D, s));
 }
 
 }  // extern "C"

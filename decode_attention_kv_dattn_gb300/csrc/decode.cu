@@ -118,41 +118,6 @@ __device__ __forceinline__ int unit_length(const CacheView& c, int b, int max_le
   }
 }
 
-// Inclusive prefix sum of x[0, n) in shared memory by the whole block.
-__device__ void block_scan_inclusive(int* x, int n) {
-  __shared__ int warp_sum[kWarps];
-  const int t = threadIdx.x;
-  const int per = (n + kThreads - 1) / kThreads;
-  const int lo = min(n, t * per), hi = min(n, lo + per);
-  int sum = 0;
-  for (int i = lo; i < hi; ++i) {
-    sum += x[i];
-    x[i] = sum;
-  }
-  int incl = sum;
-#pragma unroll
-  for (int w = 1; w < 32; w <<= 1) {
-    const int y = __shfl_up_sync(kFull, incl, w);
-    if ((t & 31) >= w) incl += y;
-  }
-  if ((t & 31) == 31) warp_sum[t >> 5] = incl;
-  __syncthreads();
-  int before = incl - sum;
-  for (int w = 0; w < (t >> 5); ++w) before += warp_sum[w];
-  for (int i = lo; i < hi; ++i) x[i] += before;
-  __syncthreads();
-}
-
-// Last unit u with P[u] <= g (P[0] = 0 <= g); its range then contains g.
-__device__ __forceinline__ int unit_of(const int* P, int U, int g) {
-  int lo = 0, hi = U - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (P[mid] <= g) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
 template <int D, int GP, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const SplitArgs a, int G) {
   using Gm = Geo<D, GP>;
@@ -175,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const SplitAr
   }
   if (threadIdx.x == 0) P[0] = 0;
   __syncthreads();
-  block_scan_inclusive(P + 1, U);
+  block_scan_inclusive<kThreads>(P + 1, U);
   const int T = P[U];
   const int g0 = static_cast<int>(static_cast<int64_t>(cta) * T / NC);
   const int g1 = static_cast<int>(static_cast<int64_t>(cta + 1) * T / NC);

@@ -10,7 +10,7 @@
 namespace dattn {
 
 // Sticky device error bits (see dattn_get_error).
-enum : int { ERR_INDEX = 1, ERR_TIMEOUT = 2, ERR_LENGTH = 4 };
+enum : int { ERR_INDEX = 1, ERR_TIMEOUT = 2, ERR_LENGTH = 4, ERR_RANGE = 8 };
 
 // One layer's cache as the kernels see it.
 struct CacheView {
@@ -92,11 +92,49 @@ struct AppendArgs {
   int* err;
 };
 
+// Tensor-core pass of tree verify over each stream's paged prefix (stream-K
+// over (stream, KV head) units, the G*T rows of a unit in one 128-row MMA).
+// Partial slot layout: [ctas + S*Hkv][G*T rows][D + 4] fp32 (o[D], m, l, pad).
+struct VerifySplitArgs {
+  CacheView c;                 // paged; seq_len = prefix lengths
+  int S, T, Hkv, G;
+  int ctas;
+  int max_len;
+  const float* qhat;           // [S*T, Hq, D] pre-scaled, from the RoPE prologue
+  float* part;
+  int* tiles;                  // [S*Hkv + 1] out
+  int* err;
+};
+
+// Tree-window join: merge the prefix segments of each row, score the row's
+// path in the window (its ancestors and itself), gate, store, write back.
+struct VerifyCombineArgs {
+  CacheView c;
+  int S, T, Hkv, G;
+  int split_ctas;
+  const int* tiles;
+  int max_len;
+  const float* qhat;           // [S*T, Hq, D]
+  const uint16_t* khat;        // [S*T, Hkv, D] rotated window keys (bf16 entries)
+  const uint16_t* v;           // [S, T, Hkv, D]
+  const int32_t* parent;       // [S, T]
+  const uint16_t* gate;        // [S, T, Hq] or null
+  const float* part;
+  float* out;                  // [S, T, Hq, D]
+  int write_back;
+  int* err;
+};
+
 // Each returns cudaErrorNotSupported for a shape with no compiled kernel.
 cudaError_t launch_rope(const RopeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_split(const SplitArgs& a, int D, int G, cudaStream_t s);
 cudaError_t launch_decode_combine(const CombineArgs& a, int D, int G, cudaStream_t s);
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
+cudaError_t launch_verify_split(const VerifySplitArgs& a, int D, cudaStream_t s);
+cudaError_t launch_verify_combine(const VerifyCombineArgs& a, int D, cudaStream_t s);
+// Keys per tile of the verify pass and its largest unit count.
+constexpr int kVerifyTileKeys = 64;
+constexpr int kVerifyMaxUnits = 512;
 
 // Resident CTAs per SM of the split kernel for (D, G) (0 if unsupported).
 int decode_split_ctas_per_sm(int D, int G);

@@ -1,0 +1,597 @@
+// Tree verify: S streams x T draft rows, each row under its own tree mask
+// ("TensorFold PR #608": verify rounds take every stream's window together, up
+// to 16 streams of 16 rows). Row i of stream s sits at position
+// prefix_len + depth(i) and attends to the stream's whole paged prefix, its
+// ancestors in the tree and itself.
+//
+// Two passes after the RoPE prologue:
+//  * verify_split_kernel - the prefix, on the 5th-generation tensor cores. The
+//    G*T query rows of one (stream, KV head) unit share every prefix key, so a
+//    unit is one 128-row MMA tile (G*T <= 128): S = Q K^T into tensor memory
+//    (TMEM), an online softmax by four warps (thread t owns row t), then
+//    O += P V accumulated in TMEM. Work is split stream-K over all units'
+//    64-key tiles (one CTA per SM), as in the decode split pass.
+//    Operands are fp16: eight producer warps load bf16 K/V rows, convert them
+//    to fp16 (exact for |x| < 65504) and store them in the 128-byte-swizzled
+//    layout the MMA reads; q and P are rounded to fp16. (fp16 keeps the
+//    error of q and P rounding under the tolerance at every prefix length;
+//    bf16 operands do not at short prefixes.) The accumulator is rescaled
+//    lazily: only when a row's maximum grows by more than 2^8.
+//  * verify_combine_kernel - per (stream, row, KV head): merges the prefix
+//    segments, scores the row's tree path in fp32 and joins it in score
+//    space, applies the gate, stores fp32 and writes the window entries back.
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "tc.cuh"
+
+namespace dattn {
+
+namespace {
+
+constexpr int VM = 128;              // MMA rows (G*T <= VM)
+constexpr int VNK = kVerifyTileKeys; // keys per tile
+constexpr int kSoftWarps = 4;        // softmax warps: TMEM lane quarters 0..3
+constexpr int kProdWarps = 8;        // producer warps
+constexpr int kMmaWarp = kSoftWarps + kProdWarps;
+constexpr int kVThreads = (kMmaWarp + 1) * 32;
+constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold
+
+// A partial row is o[D], m, l, padded to a 16-byte multiple: D + 4 floats.
+template <int D>
+constexpr int row_stride() { return D + 4; }
+
+template <int D>
+struct VGeo {
+  static constexpr int NREG = D / 64;                 // 64-dim (128-byte) regions per row
+  static constexpr int Q_OFF = 0;
+  static constexpr int Q_REG = VM * 128;              // bytes of one Q region
+  static constexpr int KT_REG = VNK * 128;            // bytes of one K (or V) region
+  static constexpr int KT_BYTES = NREG * KT_REG;
+  static constexpr int ST_OFF = Q_OFF + NREG * Q_REG;
+  static constexpr int ST_BYTES = 2 * KT_BYTES;       // K then V
+  static constexpr int P_OFF = ST_OFF + 2 * ST_BYTES;
+  static constexpr int BAR_OFF = P_OFF + VM * 128;
+  static constexpr int NBAR = 12;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8; // tmem slot, abort flag
+  static constexpr int TAB_OFF = MISC_OFF + 16;
+  static constexpr int SMEM = TAB_OFF + (2 * kVerifyMaxUnits + 1) * 4 + 1024;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t S_COL = 0;                // two 64-column score buffers
+  static constexpr uint32_t O_COL = 256;              // D columns of output
+  static_assert(D == 128 || D == 256, "head_dim");
+};
+
+// barrier indices
+enum { B_FULL = 0, B_EMPTY = 2, B_SFULL = 4, B_SFREE = 6, B_PFULL = 8, B_PVDONE = 9, B_QREADY = 10, B_OFREE = 11 };
+
+struct Waiter {
+  uint32_t bars;
+  volatile int* abort;
+  int* err;
+  // Bounded wait; on a timeout (or when another role gave up) every role
+  // leaves its loop and the CTA frees its tensor memory.
+  __device__ __forceinline__ bool wait(int b, uint32_t parity) const {
+    const uint32_t bar = bars + 8 * b;
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+      for (int i = 0; i < 32; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > 2000000000ull) {
+        *abort = 1;
+        raise_error(err, ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+};
+
+__device__ __forceinline__ uint32_t cvt_pair_f16(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// bf16 pair -> fp16 pair (exact below 65504 in magnitude); flags overflow.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, uint32_t& ovf) {
+  ovf |= ((w & 0x7fffu) >= 0x4780u) | (((w >> 16) & 0x7fffu) >= 0x4780u);
+  return cvt_pair_f16(bf16_lo(w), bf16_hi(w));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const VerifySplitArgs a) {
+  using V = VGeo<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const CacheView& c = a.c;
+  const int Hkv = a.Hkv, U = a.S * Hkv, G = a.G, T = a.T, R = G * T, Hq = Hkv * G;
+  const int NC = gridDim.x, cta = blockIdx.x;
+  int* Pt = reinterpret_cast<int*>(smem + V::TAB_OFF);  // [U + 1] tile prefix
+  int* Nn = Pt + U + 1;                                   // [U] prefix keys per unit
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + V::MISC_OFF + 4);
+
+  // ---- unit table (caller metadata only)
+  for (int u = threadIdx.x; u < U; u += kVThreads) {
+    const int s = u / Hkv;
+    int n = c.seq_len[s];
+    const int cap = min(a.max_len, c.bt_stride * c.P);
+    if (n < 0 || n > cap) {
+      if (cta == 0 && u - s * Hkv == 0) raise_error(a.err, ERR_LENGTH);
+      n = n < 0 ? 0 : cap;
+    }
+    Nn[u] = n;
+    Pt[u + 1] = (n + VNK - 1) / VNK;
+  }
+  if (threadIdx.x == 0) {
+    Pt[0] = 0;
+    *abort_flag = 0;
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(sbase + V::BAR_OFF + 8 * (B_FULL + b), kProdWarps);
+      mbar_init(sbase + V::BAR_OFF + 8 * (B_EMPTY + b), 1);
+      mbar_init(sbase + V::BAR_OFF + 8 * (B_SFULL + b), 1);
+      mbar_init(sbase + V::BAR_OFF + 8 * (B_SFREE + b), kSoftWarps);
+    }
+    mbar_init(sbase + V::BAR_OFF + 8 * B_PFULL, kSoftWarps);
+    mbar_init(sbase + V::BAR_OFF + 8 * B_PVDONE, 1);
+    mbar_init(sbase + V::BAR_OFF + 8 * B_QREADY, kSoftWarps);
+    mbar_init(sbase + V::BAR_OFF + 8 * B_OFREE, kSoftWarps);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  block_scan_inclusive<kVThreads>(Pt + 1, U);
+  const int Ttot = Pt[U];
+  const int g0 = static_cast<int>(static_cast<int64_t>(cta) * Ttot / NC);
+  const int g1 = static_cast<int>(static_cast<int64_t>(cta + 1) * Ttot / NC);
+  if (cta == 0)
+    for (int u = threadIdx.x; u <= U; u += kVThreads) a.tiles[u] = Pt[u];
+  if (warp == kMmaWarp) tc::alloc(sbase + V::MISC_OFF, V::TMEM_COLS);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + V::MISC_OFF);
+  pdl_trigger();
+
+  const int ntiles = g1 - g0;
+  const Waiter W{sbase + V::BAR_OFF, abort_flag, a.err};
+
+  if (ntiles > 0 && warp >= kSoftWarps && warp < kMmaWarp) {
+    // ================= producers: bf16 K/V rows -> fp16, swizzled =================
+    const int pt = threadIdx.x - kSoftWarps * 32;         // 0 .. 255
+    constexpr int CPR = D / 8;                            // 16-byte chunks per row
+    constexpr int JOBS = 2 * VNK * CPR / (kProdWarps * 32);  // chunks per thread per tile
+    uint4 buf[JOBS];
+    uint32_t ovf = 0;
+    int u = unit_of(Pt, U, g0);
+    auto load = [&](int k) {
+      const int g = g0 + k;
+      while (Pt[u + 1] <= g) ++u;
+      const int s = u / Hkv, j = u - s * Hkv;
+      const int k0 = (g - Pt[u]) * VNK;
+      const int nvalid = min(VNK, Nn[u] - k0);
+      const int32_t* bt = c.block_table + static_cast<int64_t>(s) * c.bt_stride;
+#pragma unroll
+      for (int x = 0; x < JOBS; ++x) {
+        const int e = pt + x * kProdWarps * 32;
+        const int which = e / (VNK * CPR);
+        const int rem = e - which * (VNK * CPR);
+        const int r = rem / CPR, ch = rem - r * CPR;
+        buf[x] = make_uint4(0u, 0u, 0u, 0u);
+        if (r < nvalid) {
+          const int t = k0 + r;
+          const int pi = t / c.P;
+          int pg = bt[pi];
+          if (pg < 0 || pg >= c.n_rows) {
+            raise_error(a.err, ERR_INDEX);
+            pg = 0;
+          }
+          const int64_t row = (static_cast<int64_t>(pg) * Hkv + j) * c.P + (t - pi * c.P);
+          buf[x] = ld_nc_v4((which ? c.v : c.k) + row * D + ch * 8);
+        }
+      }
+    };
+    load(0);
+    for (int k = 0; k < ntiles; ++k) {
+      const int st = k & 1;
+      if (k >= 2 && !__all_sync(0xffffffffu, W.wait(B_EMPTY + st, ((k >> 1) - 1) & 1))) break;
+      uint8_t* stage = smem + V::ST_OFF + st * V::ST_BYTES;
+#pragma unroll
+      for (int x = 0; x < JOBS; ++x) {
+        const int e = pt + x * kProdWarps * 32;
+        const int which = e / (VNK * CPR);
+        const int rem = e - which * (VNK * CPR);
+        const int r = rem / CPR, ch = rem - r * CPR;
+        uint4 h;
+        h.x = bf16x2_to_f16x2(buf[x].x, ovf);
+        h.y = bf16x2_to_f16x2(buf[x].y, ovf);
+        h.z = bf16x2_to_f16x2(buf[x].z, ovf);
+        h.w = bf16x2_to_f16x2(buf[x].w, ovf);
+        const int off = which * V::KT_BYTES + (ch >> 3) * V::KT_REG + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(stage + off) = h;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sbase + V::BAR_OFF + 8 * (B_FULL + st));
+      if (k + 1 < ntiles) load(k + 1);
+    }
+    if (__any_sync(0xffffffffu, ovf != 0) && lane == 0) raise_error(a.err, ERR_RANGE);
+  } else if (ntiles > 0 && warp == kMmaWarp) {
+    // ================= MMA issue (one thread) =================
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = tc::f16_idesc(VM, VNK, 0, false);
+      constexpr uint32_t idesc_pv = tc::f16_idesc(VM, D, 0, true);
+      bool ok = true;
+      auto issue_qk = [&](int k) -> bool {
+        const int st = k & 1, sb = k & 1;
+        if (!W.wait(B_FULL + st, (k >> 1) & 1)) return false;
+        if (k >= 2 && !W.wait(B_SFREE + sb, ((k >> 1) - 1) & 1)) return false;
+        tc::fence_after();
+        const uint32_t kbase = sbase + V::ST_OFF + st * V::ST_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t da = tc::sw128_desc(sbase + V::Q_OFF + (kk >> 2) * V::Q_REG + (kk & 3) * 32, 16, 1024);
+          const uint64_t db = tc::sw128_desc(kbase + (kk >> 2) * V::KT_REG + (kk & 3) * 32, 16, 1024);
+          tc::mma(tmem + V::S_COL + sb * VNK, da, db, idesc_qk, kk > 0);
+        }
+        tc::commit(sbase + V::BAR_OFF + 8 * (B_SFULL + sb));
+        return true;
+      };
+      int u = unit_of(Pt, U, g0), prev_u = -1, seg = 0;
+      for (int k = 0; k < ntiles && ok; ++k) {
+        const int g = g0 + k;
+        while (Pt[u + 1] <= g) ++u;
+        const bool seg_start = u != prev_u;
+        const bool seg_end = k == ntiles - 1 || g + 1 >= Pt[u + 1];
+        if (seg_start) {
+          if (!W.wait(B_QREADY, seg & 1) || !issue_qk(k)) break;
+        }
+        if (!seg_end && !issue_qk(k + 1)) break;
+        if (!W.wait(B_PFULL, k & 1)) break;
+        if (seg_start && seg > 0 && !W.wait(B_OFREE, (seg - 1) & 1)) break;
+        tc::fence_after();
+        const int st = k & 1;
+        const uint32_t vbase = sbase + V::ST_OFF + st * V::ST_BYTES + V::KT_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < VNK / 16; ++kk) {
+          const uint64_t da = tc::sw128_desc(sbase + V::P_OFF + kk * 32, 16, 1024);
+          const uint64_t db = tc::sw128_desc(vbase + kk * 2048, V::KT_REG, 1024);
+          tc::mma(tmem + V::O_COL, da, db, idesc_pv, !seg_start || kk > 0);
+        }
+        tc::commit(sbase + V::BAR_OFF + 8 * B_PVDONE);
+        tc::commit(sbase + V::BAR_OFF + 8 * (B_EMPTY + st));
+        if (seg_end) ++seg;
+        prev_u = u;
+      }
+    }
+    __syncwarp();
+  } else if (ntiles > 0 && warp < kSoftWarps) {
+    // ================= softmax: thread t owns row t =================
+    pdl_wait();  // q rotated by the prologue
+    const int t = threadIdx.x;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+    uint8_t* Q = smem + V::Q_OFF;
+    uint8_t* Pb = smem + V::P_OFF;
+    int u = unit_of(Pt, U, g0), prev_u = -1, seg = 0;
+    float m_ref = -INFINITY, l = 0.f;
+    for (int k = 0; k < ntiles; ++k) {
+      const int g = g0 + k;
+      while (Pt[u + 1] <= g) ++u;
+      const bool seg_start = u != prev_u;
+      const bool seg_end = k == ntiles - 1 || g + 1 >= Pt[u + 1];
+      if (seg_start) {
+        // this unit's q rows as fp16 in the swizzled K-major layout
+        const int s = u / Hkv, j = u - s * Hkv;
+        const float* src = nullptr;
+        if (t < R) {
+          const int gq = t / T, i = t - gq * T;
+          src = a.qhat + ((static_cast<int64_t>(s) * T + i) * Hq + j * G + gq) * D;
+        }
+#pragma unroll 4
+        for (int ch = 0; ch < D / 8; ++ch) {
+          uint4 h = make_uint4(0u, 0u, 0u, 0u);
+          if (src) {
+            const float4 x0 = *reinterpret_cast<const float4*>(src + ch * 8);
+            const float4 x1 = *reinterpret_cast<const float4*>(src + ch * 8 + 4);
+            h = make_uint4(cvt_pair_f16(x0.x, x0.y), cvt_pair_f16(x0.z, x0.w), cvt_pair_f16(x1.x, x1.y),
+                           cvt_pair_f16(x1.z, x1.w));
+          }
+          *reinterpret_cast<uint4*>(Q + (ch >> 3) * V::Q_REG + t * 128 + (((ch & 7) ^ (t & 7)) << 4)) = h;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sbase + V::BAR_OFF + 8 * B_QREADY);
+        m_ref = -INFINITY;
+        l = 0.f;
+      }
+      const int sb = k & 1;
+      if (!__all_sync(0xffffffffu, W.wait(B_SFULL + sb, (k >> 1) & 1))) break;
+      tc::fence_after();
+      uint32_t sr[64];
+      tc::ld64(tmem + lane_off + V::S_COL + sb * VNK, sr);
+      tc::wait_ld();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sbase + V::BAR_OFF + 8 * (B_SFREE + sb));
+      const int nvalid = min(VNK, Nn[u] - (g - Pt[u]) * VNK);
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int x = 0; x < 64; ++x) {
+        const float sx = x < nvalid ? __uint_as_float(sr[x]) : -INFINITY;
+        sr[x] = __float_as_uint(sx);
+        tmax = fmaxf(tmax, sx);
+      }
+      bool pv_waited = false;
+      if (m_ref == -INFINITY) {
+        m_ref = tmax;
+      } else {
+        const bool need = tmax > m_ref + kRescaleLog2;
+        if (__any_sync(0xffffffffu, need)) {
+          // rescale this warp's rows of O once the last PV has landed
+          if (!__all_sync(0xffffffffu, W.wait(B_PVDONE, (k - 1) & 1))) break;
+          pv_waited = true;
+          tc::fence_after();
+          const float f = need ? exp2_fast(m_ref - tmax) : 1.f;
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tc::ld32(tmem + lane_off + V::O_COL + cc * 32, o);
+            tc::wait_ld();
+#pragma unroll
+            for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * f);
+            tc::st32(tmem + lane_off + V::O_COL + cc * 32, o);
+          }
+          tc::wait_st();
+          if (need) {
+            l *= f;
+            m_ref = tmax;
+          }
+        }
+      }
+      // probabilities in fp16; the row sum uses the same rounded values
+      uint32_t ph[32];
+      float lsum = 0.f;
+#pragma unroll
+      for (int x = 0; x < 32; ++x) {
+        const float p0 = exp2_fast(__uint_as_float(sr[2 * x]) - m_ref);
+        const float p1 = exp2_fast(__uint_as_float(sr[2 * x + 1]) - m_ref);
+        const __half2 h = __floats2half2_rn(p0, p1);
+        lsum += __low2float(h) + __high2float(h);
+        ph[x] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      l += lsum;
+      // the P buffer is free once the previous PV has completed
+      if (k > 0 && !pv_waited && !__all_sync(0xffffffffu, W.wait(B_PVDONE, (k - 1) & 1))) break;
+#pragma unroll
+      for (int x = 0; x < 8; ++x)
+        *reinterpret_cast<uint4*>(Pb + t * 128 + ((x ^ (t & 7)) << 4)) =
+            make_uint4(ph[4 * x], ph[4 * x + 1], ph[4 * x + 2], ph[4 * x + 3]);
+      fence_proxy_async_smem();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sbase + V::BAR_OFF + 8 * B_PFULL);
+      if (seg_end) {
+        if (!__all_sync(0xffffffffu, W.wait(B_PVDONE, k & 1))) break;
+        tc::fence_after();
+        const int slot = seg == 0 ? cta : NC + u;
+        float* dst = a.part + (static_cast<int64_t>(slot) * R + t) * row_stride<D>();
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tc::ld32(tmem + lane_off + V::O_COL + cc * 32, o);
+          tc::wait_ld();
+          if (t < R) {
+#pragma unroll
+            for (int x = 0; x < 32; x += 4)
+              *reinterpret_cast<float4*>(dst + cc * 32 + x) =
+                  make_float4(__uint_as_float(o[x]), __uint_as_float(o[x + 1]), __uint_as_float(o[x + 2]),
+                              __uint_as_float(o[x + 3]));
+          }
+        }
+        if (t < R) {
+          dst[D] = m_ref;
+          dst[D + 1] = l;
+        }
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sbase + V::BAR_OFF + 8 * B_OFREE);
+        ++seg;
+      }
+      prev_u = u;
+    }
+  }
+
+  tc::fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc::fence_after();
+    tc::dealloc(tmem, V::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- combine
+
+template <int D>
+__global__ void __launch_bounds__(256) verify_combine_kernel(const VerifyCombineArgs a) {
+  constexpr int EPL = D / 32;  // dims per lane
+  __shared__ int par_s[16];
+  __shared__ int path_s[16];
+  __shared__ int npath_s;
+  const int i = blockIdx.x, j = blockIdx.y, s = blockIdx.z;
+  const int g = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = a.G, T = a.T, Hkv = a.Hkv, Hq = Hkv * G, R = G * T, h = j * G + g;
+  const int64_t tok = static_cast<int64_t>(s) * T + i;
+  const CacheView& c = a.c;
+
+  // ---- caller inputs: tree, gate, prefix length, write-back target
+  if (threadIdx.x < T) par_s[threadIdx.x] = a.parent[static_cast<int64_t>(s) * T + threadIdx.x];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int np = 0, node = i;
+    path_s[np++] = node;
+    for (int steps = 0; steps < T; ++steps) {
+      const int p = par_s[node];
+      if (p < 0) break;
+      if (p >= node) {
+        raise_error(a.err, ERR_INDEX);
+        break;
+      }
+      node = p;
+      path_s[np++] = node;
+    }
+    npath_s = np;
+  }
+  float sig = 1.f;
+  if (a.gate) sig = 1.f / (1.f + expf(-bf16_to_f32(a.gate[tok * Hq + h])));
+  int n = c.seq_len[s];
+  const int cap = min(a.max_len, c.bt_stride * c.P);
+  n = n < 0 ? 0 : (n > cap ? cap : n);
+  int64_t wb_off = -1;
+  if (a.write_back && g == 0) {
+    const int idx = n + i;
+    const int pi = idx / c.P;
+    const int pg = pi < c.bt_stride ? c.block_table[static_cast<int64_t>(s) * c.bt_stride + pi] : -1;
+    if (pg >= 0 && pg < c.n_rows)
+      wb_off = ((static_cast<int64_t>(pg) * Hkv + j) * c.P + idx % c.P) * D;
+    else if (lane == 0)
+      raise_error(a.err, ERR_INDEX);
+  }
+  __syncthreads();
+  const int np = npath_s;
+
+  pdl_wait();  // prefix partials of the split pass; rotated q and window keys
+  pdl_trigger();
+
+  float q[EPL];
+  {
+    const float* src = a.qhat + (tok * Hq + h) * D + lane * EPL;
+#pragma unroll
+    for (int e = 0; e < EPL; e += 4) {
+      const float4 x = *reinterpret_cast<const float4*>(src + e);
+      q[e] = x.x; q[e + 1] = x.y; q[e + 2] = x.z; q[e + 3] = x.w;
+    }
+  }
+  // ---- scores of the row's tree path (itself and its ancestors), fp32
+  float sw[16];
+  float M = -INFINITY;
+#pragma unroll 1
+  for (int p = 0; p < np; ++p) {
+    const uint16_t* kp = a.khat + ((static_cast<int64_t>(s) * T + path_s[p]) * Hkv + j) * D + lane * EPL;
+    float dot = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; e += 2) {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(kp + e);
+      dot = fmaf(q[e], bf16_lo(w), dot);
+      dot = fmaf(q[e + 1], bf16_hi(w), dot);
+    }
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, w);
+    sw[p] = dot;
+    M = fmaxf(M, dot);
+  }
+  // ---- the prefix segments of this unit (row r = g * T + i)
+  const int U = a.S * Hkv, u = s * Hkv + j, NC = a.split_ctas;
+  const int Ttot = a.tiles[U];
+  const int p0 = a.tiles[u], p1 = a.tiles[u + 1];
+  int S = 0, c_lo = 0, first_slot = 0;
+  if (p1 > p0) {
+    c_lo = static_cast<int>((static_cast<int64_t>(p0 + 1) * NC - 1) / Ttot);
+    const int c_hi = static_cast<int>((static_cast<int64_t>(p1) * NC - 1) / Ttot);
+    S = c_hi - c_lo + 1;
+    first_slot = static_cast<int>(static_cast<int64_t>(c_lo) * Ttot / NC) == p0 ? c_lo : NC + u;
+  }
+  const int r = g * T + i;
+  auto seg_row = [&](int k) -> const float* {
+    const int slot = k == 0 ? first_slot : c_lo + k;
+    return a.part + (static_cast<int64_t>(slot) * R + r) * row_stride<D>();
+  };
+  auto seg_ok = [&](int k) -> bool {
+    if (k == 0) return true;
+    const int64_t cc = c_lo + k;
+    return cc * Ttot / NC < (cc + 1) * Ttot / NC;
+  };
+  for (int k = 0; k < S; ++k)
+    if (seg_ok(k)) M = fmaxf(M, seg_row(k)[D]);
+  float acc[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+  float L = 0.f;
+  for (int k = 0; k < S; ++k) {
+    if (!seg_ok(k)) continue;
+    const float* pr = seg_row(k);
+    const float w = exp2_fast(pr[D] - M);
+    L = fmaf(w, pr[D + 1], L);
+#pragma unroll
+    for (int e = 0; e < EPL; e += 4) {
+      const float4 x = *reinterpret_cast<const float4*>(pr + lane * EPL + e);
+      acc[e] = fmaf(w, x.x, acc[e]);
+      acc[e + 1] = fmaf(w, x.y, acc[e + 1]);
+      acc[e + 2] = fmaf(w, x.z, acc[e + 2]);
+      acc[e + 3] = fmaf(w, x.w, acc[e + 3]);
+    }
+  }
+  // ---- the tree path joins as its own score vector
+#pragma unroll 1
+  for (int p = 0; p < np; ++p) {
+    const float w = exp2_fast(sw[p] - M);
+    L += w;
+    const uint16_t* vp = a.v + ((static_cast<int64_t>(s) * T + path_s[p]) * Hkv + j) * D + lane * EPL;
+#pragma unroll
+    for (int e = 0; e < EPL; e += 2) {
+      const uint32_t x = *reinterpret_cast<const uint32_t*>(vp + e);
+      acc[e] = fmaf(w, bf16_lo(x), acc[e]);
+      acc[e + 1] = fmaf(w, bf16_hi(x), acc[e + 1]);
+    }
+  }
+  const float scale = sig / L;
+  float* dst = a.out + (tok * Hq + h) * D + lane * EPL;
+#pragma unroll
+  for (int e = 0; e < EPL; e += 4)
+    *reinterpret_cast<float4*>(dst + e) =
+        make_float4(acc[e] * scale, acc[e + 1] * scale, acc[e + 2] * scale, acc[e + 3] * scale);
+
+  // ---- write-back of this node's entry at token index prefix_len + i
+  if (wb_off >= 0) {
+    const uint16_t* kh = a.khat + (tok * Hkv + j) * D + lane * EPL;
+    const uint16_t* vv = a.v + (tok * Hkv + j) * D + lane * EPL;
+#pragma unroll
+    for (int e = 0; e < EPL; e += 4) {
+      *reinterpret_cast<uint2*>(c.k + wb_off + lane * EPL + e) = *reinterpret_cast<const uint2*>(kh + e);
+      *reinterpret_cast<uint2*>(c.v + wb_off + lane * EPL + e) = *reinterpret_cast<const uint2*>(vv + e);
+    }
+  }
+}
+
+template <int D>
+cudaError_t verify_split_launch(const VerifySplitArgs& a, cudaStream_t s) {
+  using V = VGeo<D>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(verify_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, V::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  return launch_pdl(verify_split_kernel<D>, dim3(a.ctas), dim3(kVThreads), V::SMEM, s, a);
+}
+
+}  // namespace
+
+cudaError_t launch_verify_split(const VerifySplitArgs& a, int D, cudaStream_t s) {
+  if (a.G * a.T > VM || a.T > 16 || a.S * a.Hkv > kVerifyMaxUnits) return cudaErrorNotSupported;
+  if (D == 256) return verify_split_launch<256>(a, s);
+  if (D == 128) return verify_split_launch<128>(a, s);
+  return cudaErrorNotSupported;
+}
+
+cudaError_t launch_verify_combine(const VerifyCombineArgs& a, int D, cudaStream_t s) {
+  if (a.G > 8 || a.T > 16) return cudaErrorNotSupported;
+  dim3 grid(a.T, a.Hkv, a.S);
+  dim3 block(32 * a.G);
+  if (D == 256) return launch_pdl(verify_combine_kernel<256>, grid, block, 0, s, a);
+  if (D == 128) return launch_pdl(verify_combine_kernel<128>, grid, block, 0, s, a);
+  return cudaErrorNotSupported;
+}
+
+}  // namespace dattn

@@ -66,7 +66,9 @@ enum {
   DATTN_EINDEX = 4,        /* device metadata out of range (from dattn_get_error) */
   DATTN_ETIMEOUT = 5,      /* a bounded device wait gave up (dattn_get_error)     */
   DATTN_EUNSUPPORTED = 6,  /* a shape this build has no kernel for                */
-  DATTN_ELENGTH = 7        /* a stream longer than the call's bound (get_error)   */
+  DATTN_ELENGTH = 7,       /* a stream longer than the call's bound (get_error)   */
+  DATTN_ERANGE = 8         /* verify: a cached K/V value beyond the fp16 range
+                              (|x| >= 65520) the tensor-core pass computes in     */
 };
 
 enum { DATTN_CACHE_RING = 0, DATTN_CACHE_PAGED = 1 };
@@ -180,8 +182,8 @@ DATTN_API int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, cons
                  dattn_stream_t stream);
 
 /* Synchronize `stream`, then return and clear the sticky device error word:
- * DATTN_OK, DATTN_EINDEX, DATTN_ELENGTH or DATTN_ETIMEOUT (the first found in
- * that order of severity: ETIMEOUT, EINDEX, ELENGTH). */
+ * DATTN_OK, DATTN_ETIMEOUT, DATTN_EINDEX, DATTN_ERANGE or DATTN_ELENGTH (the
+ * first found in that order of severity). */
 DATTN_API int dattn_get_error(dattn_t* h, dattn_stream_t stream);
 
 /* Static description of a status code. */
