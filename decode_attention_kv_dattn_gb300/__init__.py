@@ -73,9 +73,12 @@ lib.dattn_error_string.argtypes = [_int]
 lib.dattn_error_string.restype = ctypes.c_char_p
 lib.dattn_destroy.argtypes = [_vp]
 lib.dattn_destroy.restype = None
+lib.dattn_decode_noalloc.argtypes = [ctypes.POINTER(Config), _int, ctypes.POINTER(Cache),
+                                     ctypes.POINTER(DecodeArgs), _vp]
+lib.dattn_decode_noalloc.restype = _int
 
 EXPORTS = ("dattn_create", "dattn_append_kv", "dattn_decode", "dattn_verify",
-           "dattn_get_error", "dattn_error_string", "dattn_destroy")
+           "dattn_get_error", "dattn_error_string", "dattn_destroy", "dattn_decode_noalloc")
 
 
 class DattnError(RuntimeError):
@@ -183,3 +186,14 @@ class Handle:
     def get_error(self, stream=None) -> int:
         """Synchronize the stream; return and clear the sticky device status."""
         return lib.dattn_get_error(self._h, _stream_ptr(stream))
+
+
+def decode_noalloc(config: Config, layer, cache: Cache, q, k_new, v_new, pos, out, gate=None,
+                   max_seq_len=0, write_back=True, stream=None):
+    """Decode without a handle, for callers that cannot allocate device memory:
+    the library's fixed scratch array stands in for a handle's workspace.
+    `config` is a Config structure (for instance Handle.config)."""
+    args = DecodeArgs(q.shape[0], _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(gate), _ptr(pos),
+                      _ptr(out), int(max_seq_len), int(write_back))
+    _check(lib.dattn_decode_noalloc(ctypes.byref(config), layer, ctypes.byref(cache),
+                                    ctypes.byref(args), _stream_ptr(stream)), "dattn_decode_noalloc")

@@ -1,0 +1,209 @@
+// dattn_decode_noalloc: decode attention for callers that cannot allocate
+// device memory.
+//
+// Some callers have no way to call cudaMalloc: code that runs inside a memory
+// budget owned by someone else (an inference server that hands out all device
+// memory from its own pool up front), code that must not allocate while a
+// latency-critical loop runs, or embedding layers that only receive raw device
+// pointers. dattn_create allocates the handle's workspace, so those callers
+// cannot use dattn_decode. This entry point needs no handle: its scratch space
+// (rotated q and k, the split partials, the tile table, the error word and the
+// RoPE frequency table) lives in one fixed-size array in device global memory
+// that the library defines at file scope. The caller passes only its inputs,
+// outputs and cache, exactly as for dattn_decode.
+//
+// The array is created when the library's module is loaded on a device and
+// stays there until the process exits. All calls on a device share it and it
+// keeps the last call's contents; every call rewrites what it reads (and
+// clears its error word first), but two calls that run on the GPU at the same
+// time - on different streams, or not ordered on one stream - race on it.
+//
+// The kernels are the same ones dattn_decode launches; only where their
+// scratch lives differs.
+#include <cmath>
+#include <mutex>
+
+#include "dattn.h"
+#include "kernels.h"
+
+using namespace dattn;
+
+namespace {
+
+// Upper bound of the scratch this entry point may use on one device: 8 MiB.
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct DeviceScratch {
+  bool ready = false;
+  unsigned char* base = nullptr;  // device address of g_noalloc_scratch
+  int sms = 0;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceScratch g_devices[kMaxDevices];
+std::mutex g_mutex;
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+int padded_group(int G) { return G <= 2 ? 2 : (G <= 4 ? 4 : (G <= 8 ? 8 : 0)); }
+
+}  // namespace
+
+extern "C" DATTN_API int dattn_decode_noalloc(const dattn_config* cfg, int layer, const dattn_cache* cache,
+                                              const dattn_decode_args* args, dattn_stream_t stream) {
+  // ---- host checks (nothing is launched when one fails)
+  if (!cfg || !cache || !args || !cfg->layers || layer < 0 || layer >= cfg->num_layers) return DATTN_EINVAL;
+  const int Hq = cfg->num_q_heads, Hkv = cfg->num_kv_heads, D = cfg->head_dim;
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return DATTN_EINVAL;
+  if (D != 128 && D != 256) return DATTN_EUNSUPPORTED;
+  const int G = Hq / Hkv, GP = padded_group(G);
+  if (GP == 0) return DATTN_EUNSUPPORTED;
+  const dattn_layer_config& L = cfg->layers[layer];
+  if (L.rotary_dim < 0 || L.rotary_dim > D || L.rotary_dim % 2 || (L.rotary_dim > 0 && !(L.rope_theta > 0.0)))
+    return DATTN_EINVAL;
+  if (!cache->k || !cache->v || cache->n_rows <= 0) return DATTN_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(cache->k) | reinterpret_cast<uintptr_t>(cache->v)) & 15u) return DATTN_EINVAL;
+  int n_max;
+  if (L.cache_kind == DATTN_CACHE_RING) {
+    if (L.ring_slots <= 0 || !cache->ring_head || !cache->ring_count) return DATTN_EINVAL;
+    n_max = L.ring_slots;
+  } else if (L.cache_kind == DATTN_CACHE_PAGED) {
+    if (L.page_size <= 0 || !cache->block_table || !cache->seq_len || cache->bt_stride <= 0) return DATTN_EINVAL;
+    n_max = args->max_seq_len > 0 ? args->max_seq_len : cfg->max_context;
+    if (n_max <= 0 || n_max > cfg->max_context) return DATTN_EXCEEDS;
+  } else {
+    return DATTN_EINVAL;
+  }
+  const int B = args->num_streams;
+  if (B <= 0) return DATTN_EINVAL;
+  if (!args->q || !args->k_new || !args->v_new || !args->pos || !args->out) return DATTN_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(args->q) | reinterpret_cast<uintptr_t>(args->k_new) |
+       reinterpret_cast<uintptr_t>(args->v_new) | reinterpret_cast<uintptr_t>(args->out)) & 15u)
+    return DATTN_EINVAL;
+  if (static_cast<int64_t>(B) * Hkv > decode_max_units()) return DATTN_EXCEEDS;
+
+  // ---- once per device: the device address of the scratch array
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DATTN_ECUDA;
+  DeviceScratch ds;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceScratch& d = g_devices[dev];
+    if (!d.ready) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return DATTN_ECUDA;
+      int sms = 0;
+      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DATTN_ECUDA;
+      d.base = static_cast<unsigned char*>(p);
+      d.sms = sms;
+      d.ready = true;
+    }
+    ds = d;
+  }
+
+  // ---- the split grid, as dattn_decode plans it
+  const int tile_keys = decode_split_tile_keys(D, G);
+  const int resident = ds.sms * decode_split_ctas_per_sm(D, G);
+  if (tile_keys <= 0 || resident <= 0) return DATTN_EUNSUPPORTED;
+  int64_t ctas = (static_cast<int64_t>(B) * Hkv * ((n_max + tile_keys - 1) / tile_keys) + 3) / 4;
+  if (ctas > resident) ctas = resident;
+  if (ctas < 1) ctas = 1;
+
+  // ---- carve the scratch; reject what does not fit
+  const int half = L.rotary_dim / 2;
+  size_t off = 0;
+  const size_t err_off = off;
+  off = align256(off + sizeof(int));
+  const size_t freq_off = off;
+  off = align256(off + static_cast<size_t>(half) * sizeof(double));
+  const size_t tiles_off = off;
+  off = align256(off + (static_cast<size_t>(B) * Hkv + 1) * sizeof(int));
+  const size_t qhat_off = off;
+  off = align256(off + static_cast<size_t>(B) * Hq * D * sizeof(float));
+  const size_t khat_off = off;
+  off = align256(off + static_cast<size_t>(B) * Hkv * D * sizeof(uint16_t));
+  const size_t part_off = off;
+  off = align256(off + (static_cast<size_t>(ctas) + static_cast<size_t>(B) * Hkv) * GP * (D + 2) * sizeof(float));
+  if (off > kNoAllocScratchBytes) return DATTN_EXCEEDS;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int* err = reinterpret_cast<int*>(ds.base + err_off);
+  double* inv_freq = half > 0 ? reinterpret_cast<double*>(ds.base + freq_off) : nullptr;
+  // The error word accumulates bits, so it starts every call at zero; the
+  // frequency table is rewritten from the host (theta^(-2i/r) in fp64).
+  if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return DATTN_ECUDA;
+  if (half > 0) {
+    double f[128];
+    if (half > 128) return DATTN_EUNSUPPORTED;
+    for (int i = 0; i < half; ++i)
+      f[i] = std::pow(L.rope_theta, -static_cast<double>(2 * i) / static_cast<double>(L.rotary_dim));
+    if (cudaMemcpyAsync(inv_freq, f, half * sizeof(double), cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return DATTN_ECUDA;
+  }
+
+  CacheView cv{};
+  cv.k = static_cast<uint16_t*>(cache->k);
+  cv.v = static_cast<uint16_t*>(cache->v);
+  cv.paged = L.cache_kind == DATTN_CACHE_PAGED;
+  cv.n_rows = cache->n_rows;
+  cv.R = L.ring_slots;
+  cv.P = L.page_size;
+  cv.ring_head = cache->ring_head;
+  cv.ring_count = cache->ring_count;
+  cv.stream_rows = cache->stream_rows;
+  cv.block_table = cache->block_table;
+  cv.bt_stride = cache->bt_stride;
+  cv.seq_len = cache->seq_len;
+
+  RopeArgs ra{};
+  ra.rows = B;
+  ra.Hq = Hq;
+  ra.Hkv = Hkv;
+  ra.D = D;
+  ra.r = L.rotary_dim;
+  ra.q = static_cast<const uint16_t*>(args->q);
+  ra.k = static_cast<const uint16_t*>(args->k_new);
+  ra.pos = args->pos;
+  ra.T = 1;
+  ra.inv_freq = inv_freq;
+  ra.q_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+  ra.qhat = reinterpret_cast<float*>(ds.base + qhat_off);
+  ra.khat = reinterpret_cast<uint16_t*>(ds.base + khat_off);
+  ra.err = err;
+  cudaError_t e = launch_rope(ra, s);
+  if (e != cudaSuccess) return e == cudaErrorNotSupported ? DATTN_EUNSUPPORTED : DATTN_ECUDA;
+
+  SplitArgs sa{};
+  sa.c = cv;
+  sa.B = B;
+  sa.Hkv = Hkv;
+  sa.ctas = static_cast<int>(ctas);
+  sa.max_len = n_max;
+  sa.qhat = ra.qhat;
+  sa.part = reinterpret_cast<float*>(ds.base + part_off);
+  sa.tiles = reinterpret_cast<int*>(ds.base + tiles_off);
+  sa.err = err;
+  e = launch_decode_split(sa, D, G, s);
+  if (e != cudaSuccess) return e == cudaErrorNotSupported ? DATTN_EUNSUPPORTED : DATTN_ECUDA;
+
+  CombineArgs ca{};
+  ca.c = cv;
+  ca.B = B;
+  ca.Hkv = Hkv;
+  ca.split_ctas = sa.ctas;
+  ca.tiles = sa.tiles;
+  ca.max_len = n_max;
+  ca.qhat = ra.qhat;
+  ca.khat = ra.khat;
+  ca.v_new = static_cast<const uint16_t*>(args->v_new);
+  ca.gate = static_cast<const uint16_t*>(args->gate);
+  ca.part = sa.part;
+  ca.out = args->out;
+  ca.write_back = args->write_back;
+  ca.err = err;
+  e = launch_decode_combine(ca, D, G, s);
+  if (e != cudaSuccess) return e == cudaErrorNotSupported ? DATTN_EUNSUPPORTED : DATTN_ECUDA;
+  return DATTN_OK;
+}

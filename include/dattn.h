@@ -192,6 +192,27 @@ DATTN_API const char* dattn_error_string(int code);
 /* Free the workspace and the handle. Safe on NULL. */
 DATTN_API void dattn_destroy(dattn_t* h);
 
+/* Decode for callers that cannot allocate device memory (no counterpart on the
+ * pages: it serves callers whose device memory is owned by someone else, e.g.
+ * a server that hands out its whole pool up front, or code that must not
+ * allocate inside a latency-critical loop). Same operation, layouts and
+ * arguments as dattn_decode for layer `layer` of `cfg`, but no handle: the
+ * scratch space (rotated q/k, split partials, tile table, error word, RoPE
+ * frequencies) lives in one 8 MiB array in device memory that the library
+ * defines at file scope; every GPU that loads the library holds it until the
+ * process exits. Nothing is allocated or freed by this call.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - A call whose scratch would not fit in 8 MiB returns DATTN_EXCEEDS
+ *     (about 2.4 MiB for 64 streams x 8 query heads x head_dim 256).
+ *   - All calls on a device share the array, which keeps the last call's
+ *     contents; each call rewrites what it uses and clears its error word, but
+ *     calls that overlap on the GPU (other streams, or unordered) race.
+ *   - Device-side metadata errors are recorded in the array's error word and
+ *     are not returned; only host-side checks produce the status. */
+DATTN_API int dattn_decode_noalloc(const dattn_config* cfg, int layer, const dattn_cache* cache,
+                                   const dattn_decode_args* args, dattn_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
