@@ -45,12 +45,12 @@ FALLBACK_HBM_GBS = 6800.0
 
 # ---------------------------------------------------------------- accounting
 
-def layer_bytes(kind, B, n_cached, P=16):
-    """Algorithmic bytes of one decode call: the cached K/V read once, plus the
-    call's small inputs and outputs (q, k_new, v_new, gate, out, the written
-    entry, and the index metadata read)."""
-    kv = B * n_cached * 2 * HKV * D * 2
-    io = B * (HQ * D * 2 + 2 * HKV * D * 2 + HQ * 2 + HQ * D * 4 + 2 * HKV * D * 2)
+def layer_bytes(kind, B, n_cached, P=16, Hq=HQ, Hkv=HKV, D=D, gate=True):
+    """Algorithmic bytes of one decode call over B streams of n_cached tokens:
+    the cached K/V read once, plus the call's small inputs and outputs (q,
+    k_new, v_new, gate, out, the written entry, the index metadata read)."""
+    kv = B * n_cached * 2 * Hkv * D * 2
+    io = B * (Hq * D * 2 + 2 * Hkv * D * 2 + (Hq * 2 if gate else 0) + Hq * D * 4 + 2 * Hkv * D * 2)
     if kind == "sliding":
         meta = B * 3 * 4
     else:
@@ -167,7 +167,45 @@ def max_over_ranks(x: float, world: int) -> float:
 
 # ---------------------------------------------------------------- the step
 
-class Step:
+class Workload:
+    """One benchmark step: a fixed list of C-ABI calls over device-resident
+    inputs, captured in one CUDA graph."""
+    flush_l2 = False
+
+    def run_eager(self):
+        for i in range(self.ncalls):
+            self.run_call(i)
+
+    def capture(self):
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.run_eager()  # first calls set kernel attributes outside the capture
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.run_eager()
+        torch.cuda.synchronize()
+
+    def launches_per_step(self):
+        return 3 * self.ncalls
+
+    def pack_inputs(self, tensors, device):
+        """Move the step's per-call inputs into one device buffer (so the
+        end-to-end leg refreshes them with one host-to-device copy)."""
+        total = sum(t.numel() for t in tensors)
+        self.inbuf = torch.empty(total, dtype=torch.bfloat16, device=device)
+        views, off = [], 0
+        for t in tensors:
+            v = self.inbuf[off:off + t.numel()].view(t.shape)
+            v.copy_(t)
+            views.append(v)
+            off += t.numel()
+        return views
+
+
+class Step(Workload):
     def __init__(self, B, context, seed, device="cuda"):
         import decode_attention_kv_dattn_gb300 as dattn
         import synth
@@ -189,55 +227,214 @@ class Step:
                 self.descs.append(dattn.ring_cache(L["k"], L["v"], L["head"], L["count"], L["rows"]))
             else:
                 self.descs.append(dattn.paged_cache(L["k"], L["v"], L["block_table"], L["seq_len"]))
-        # the per-step inputs live in one packed device buffer (so the end-to-end
-        # leg can refresh them with one host-to-device copy) and the outputs in one
-        self.in_elems = [L["q"].numel() + L["k_new"].numel() + L["v_new"].numel() + L["gate"].numel()
-                         for L in self.layers]
-        total = sum(self.in_elems)
-        self.inbuf = torch.empty(total, dtype=torch.bfloat16, device=device)
-        off = 0
-        for L in self.layers:
-            for name in ("q", "k_new", "v_new", "gate"):
-                n = L[name].numel()
-                view = self.inbuf[off:off + n].view(L[name].shape)
-                view.copy_(L[name])
-                L[name] = view
-                off += n
+        names = ("q", "k_new", "v_new", "gate")
+        views = self.pack_inputs([L[n] for L in self.layers for n in names], device)
+        for i, L in enumerate(self.layers):
+            for k, n in enumerate(names):
+                L[n] = views[4 * i + k]
         self.out = torch.empty((len(self.layers), B, HQ, D), dtype=torch.float32, device=device)
         self.graph = None
+        self.ncalls = len(self.layers)
+        total, tokens, per_kind = step_accounting(B, context)
+        self.bytes_step, self.tokens_step = total, tokens
+        self.dominant = [l for l, L in enumerate(self.layers) if L["kind"] == "full"]
+        self.dominant_kv_bytes = per_kind["full"][0]
+        self.others = [l for l, L in enumerate(self.layers) if L["kind"] == "sliding"]
+        self.config = {"workload": "hybrid 28-layer decode step: [sliding x3, full] x7, 8 q / 2 KV heads, "
+                                   f"head_dim 256, {B} streams, context {context}",
+                       "streams": B, "context": context, "sliding_ring_slots": 511,
+                       "full_page_size": 16, "gate": True, "write_back": True}
+        self.kernel = f"decode_split (full layers, {B} streams x {context} tokens)"
 
-    def run_layer(self, l, stream=None):
+    def run_call(self, l, stream=None):
         L = self.layers[l]
         self.h.decode(l, self.descs[l], L["q"], L["k_new"], L["v_new"], L["pos"], self.out[l],
                       gate=L["gate"], max_seq_len=self.context if L["kind"] == "full" else 0,
                       write_back=True, stream=stream)
 
-    def run_eager(self):
-        for l in range(len(self.layers)):
-            self.run_layer(l)
+class DecodeCall(Workload):
+    """One decode call per step: the single sliding layer, the paged batch or
+    a long-context layer."""
 
-    def capture(self):
-        s = torch.cuda.Stream()
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(s):
-            self.run_eager()  # first calls set kernel attributes outside the capture
-        torch.cuda.current_stream().wait_stream(s)
-        torch.cuda.synchronize()
-        self.graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(self.graph):
-            self.run_eager()
-        torch.cuda.synchronize()
+    def __init__(self, name, seed, device="cuda"):
+        import decode_attention_kv_dattn_gb300 as dattn
+        import synth
+        g = torch.Generator(device=device)
+        g.manual_seed(seed)
+        hg = synth.generator(seed)
+        rnd = lambda *sh: torch.randn(*sh, generator=g, device=device).to(torch.bfloat16)
+        if name == "sliding":
+            B, Hq, Hkv, Dh, R = 1, 8, 2, 256, 511
+            start = int(synth.randint(0, R - 1, 1, hg)[0])
+            self.lens = [300]
+            k, v = rnd(B, Hkv, R, Dh), rnd(B, Hkv, R, Dh)
+            head = torch.tensor([(start + 300) % R], dtype=torch.int32, device=device)
+            count = torch.tensor([300], dtype=torch.int32, device=device)
+            layer = {"kind": dattn.CACHE_RING, "ring_slots": R, "rotary_dim": 256, "rope_theta": 1e4}
+            self.desc = dattn.ring_cache(k, v, head, count)
+            self._keep = (k, v, head, count)
+            pos, gate, P, kind = [300], True, 16, "sliding"
+            self.flush_l2 = True
+            self.config = {"workload": "single sliding layer: 1 stream, 8 q / 2 KV heads, head_dim 256, "
+                                       "ring of 511 slots with 300 written, RoPE 256 dims theta 1e4, gate",
+                           "streams": 1, "context": 300}
+        else:
+            if name == "paged":
+                B, Hq, Hkv, Dh, P, r, th, gate = 64, 16, 8, 128, 16, 128, 1e6, False
+                self.lens = [int(x) for x in synth.randint(64, 4096, B, hg)]
+                desc = "paged batched decode: 64 streams, lengths U[64, 4096], 16-token permuted pages, " \
+                       "16 q / 8 KV heads, head_dim 128, RoPE 128 dims theta 1e6, no gate"
+            elif name == "long1m":
+                B, Hq, Hkv, Dh, P, r, th, gate = 1, 8, 2, 256, 64, 64, 5e6, False
+                self.lens = [1 << 20]
+                desc = "long-context decode: 1 stream of 1,048,576 tokens, 64-token pages, 8 q / 2 KV heads, head_dim 256"
+            elif name == "long262k":
+                B, Hq, Hkv, Dh, P, r, th, gate = 8, 8, 2, 256, 64, 64, 5e6, False
+                self.lens = [1 << 18] * 8
+                desc = "long-context decode: 8 streams of 262,144 tokens, 64-token pages, 8 q / 2 KV heads, head_dim 256"
+            else:
+                raise ValueError(name)
+            k, v, bt, seq = synth.paged_device(g, B, Hkv, Dh, P, self.lens, room=1, device=device)
+            layer = {"kind": dattn.CACHE_PAGED, "page_size": P, "rotary_dim": r, "rope_theta": th}
+            self.desc = dattn.paged_cache(k, v, bt, seq)
+            self._keep = (k, v, bt, seq)
+            pos, kind = self.lens, "full"
+            self.config = {"workload": desc, "streams": B, "context": max(self.lens)}
+        self.kind, self.B, self.Hq, self.Hkv, self.D, self.P, self.gate_on = kind, B, Hq, Hkv, Dh, P, gate
+        self.rope = (layer["rotary_dim"], layer["rope_theta"])
+        self.h = dattn.Handle(Hq, Hkv, Dh, [layer], B, max_context=max(self.lens) if kind == "full" else 0)
+        ins = [rnd(B, Hq, Dh), rnd(B, Hkv, Dh), rnd(B, Hkv, Dh)] + ([rnd(B, Hq)] if gate else [])
+        views = self.pack_inputs(ins, device)
+        self.q, self.k_new, self.v_new = views[:3]
+        self.g = views[3] if gate else None
+        self.pos = torch.tensor(pos, dtype=torch.int32, device=device)
+        self.out = torch.empty((B, Hq, Dh), dtype=torch.float32, device=device)
+        self.ncalls = 1
+        self.graph = None
+        kv = io = 0
+        for n in self.lens:
+            a, b_ = layer_bytes(kind, 1, n, P, Hq, Hkv, Dh, gate)
+            kv += a
+            io += b_
+        self.bytes_step, self.tokens_step = kv + io, sum(n + 1 for n in self.lens)
+        self.dominant, self.others, self.dominant_kv_bytes = [0], [], kv
+        self.kernel = "decode_split (" + self.config["workload"].split(":")[0] + ")"
 
-    def launches_per_step(self):
-        return 3 * len(self.layers)
+    def run_call(self, i, stream=None):
+        self.h.decode(0, self.desc, self.q, self.k_new, self.v_new, self.pos, self.out, gate=self.g,
+                      max_seq_len=max(self.lens) if self.kind == "full" else 0, write_back=True,
+                      stream=stream)
+
+    def oracle_sample(self):
+        """A bounded host sample of the call: its first stream (pages gathered)."""
+        u16 = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+        d = {"kind": self.kind, "rope": _Rope(*self.rope), "q": u16(self.q[:1]), "k_new": u16(self.k_new[:1]),
+             "v_new": u16(self.v_new[:1]), "gate": None if self.g is None else u16(self.g[:1]),
+             "pos": self.pos[:1].cpu().numpy(), "Hq": self.Hq, "Hkv": self.Hkv, "D": self.D, "P": self.P}
+        k, v = self._keep[0], self._keep[1]
+        if self.kind == "sliding":
+            d.update(k=u16(k[:1]), v=u16(v[:1]), head=self._keep[2][:1].cpu().numpy(),
+                     count=self._keep[3][:1].cpu().numpy())
+        else:
+            bt = self._keep[2][:1]
+            pages = bt.reshape(-1)
+            pages = pages[pages >= 0]
+            d.update(k=u16(k[pages]), v=u16(v[pages]),
+                     block_table=np.arange(pages.numel(), dtype=np.int32).reshape(1, -1),
+                     seq_len=self._keep[3][:1].cpu().numpy())
+        return [d], "1 stream of the call"
+
+
+class VerifyCall(Workload):
+    """One tree-verify round per step: 16 streams x 16 rows."""
+
+    def __init__(self, seed, device="cuda"):
+        import decode_attention_kv_dattn_gb300 as dattn
+        import synth
+        g = torch.Generator(device=device)
+        g.manual_seed(seed)
+        hg = synth.generator(seed)
+        S, T, Hq, Hkv, Dh, P = 16, 16, 24, 4, 256, 16
+        self.lens = [int(x) for x in synth.randint(512, 8192, S, hg)]
+        parent = np.stack([synth.tree_parents(hg, T) for _ in range(S)])
+        k, v, bt, seq = synth.paged_device(g, S, Hkv, Dh, P, self.lens, room=T, device=device)
+        self._keep = (k, v, bt, seq)
+        self.desc = dattn.paged_cache(k, v, bt, seq)
+        layer = {"kind": dattn.CACHE_PAGED, "page_size": P, "rotary_dim": 64, "rope_theta": 5e6}
+        self.h = dattn.Handle(Hq, Hkv, Dh, [layer], S, max_context=max(self.lens), max_verify_rows=T)
+        rnd = lambda *sh: torch.randn(*sh, generator=g, device=device).to(torch.bfloat16)
+        self.q, self.k, self.v = self.pack_inputs([rnd(S, T, Hq, Dh), rnd(S, T, Hkv, Dh), rnd(S, T, Hkv, Dh)], device)
+        self.parent = torch.from_numpy(parent).to(device)
+        self.out = torch.empty((S, T, Hq, Dh), dtype=torch.float32, device=device)
+        self.ncalls, self.graph = 1, None
+        kv = sum(self.lens) * 2 * Hkv * Dh * 2
+        io = S * T * ((Hq + 2 * Hkv) * Dh * 2 + 4 + Hq * Dh * 4 + 2 * Hkv * Dh * 2) + \
+            sum((n + T + P - 1) // P for n in self.lens) * 4 + S * 4
+        self.bytes_step, self.tokens_step = kv + io, sum(n + T for n in self.lens)
+        self.dominant, self.others, self.dominant_kv_bytes = [0], [], kv
+        self.S, self.T, self.Hq, self.Hkv, self.D, self.P = S, T, Hq, Hkv, Dh, P
+        self.config = {"workload": "tree verify: 16 streams x 16 rows (random best-first trees, depth <= 7), "
+                                   "paged prefixes U[512, 8192], 24 q / 4 KV heads, head_dim 256, "
+                                   "RoPE 64 dims theta 5e6, no gate", "streams": S, "rows": T,
+                       "context": max(self.lens)}
+        self.kernel = "verify_split (tcgen05, 96 rows per KV head)"
+
+    def run_call(self, i, stream=None):
+        self.h.verify(0, self.desc, self.q, self.k, self.v, self.parent, self.out,
+                      max_prefix_len=max(self.lens), write_back=True, stream=stream)
+
+    def oracle_sample(self):
+        u16 = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+        bt = self._keep[2][:1]
+        pages = bt.reshape(-1)
+        pages = pages[pages >= 0]
+        d = {"kind": "verify", "rope": _Rope(64, 5e6), "q": u16(self.q[:1]), "k_new": u16(self.k[:1]),
+             "v_new": u16(self.v[:1]), "parent": self.parent[:1].cpu().numpy(),
+             "k": u16(self._keep[0][pages]), "v": u16(self._keep[1][pages]),
+             "block_table": np.arange(pages.numel(), dtype=np.int32).reshape(1, -1),
+             "seq_len": self._keep[3][:1].cpu().numpy(), "Hq": self.Hq, "Hkv": self.Hkv, "D": self.D,
+             "P": self.P, "T": self.T}
+        return [d], "1 of 16 streams (16 rows)"
+
+
+class _Rope:
+    def __init__(self, rotary_dim, theta):
+        self.rotary_dim, self.theta = rotary_dim, theta
+
+
+WORKLOADS = ("hybrid", "sliding", "paged", "verify", "long1m", "long262k")
+
+
+def make_workload(name, seed, args):
+    if name == "hybrid":
+        return Step(args.streams, args.context, seed)
+    if name == "verify":
+        return VerifyCall(seed)
+    return DecodeCall(name, seed)
 
 
 def time_graph(step, K, W, world):
+    """Device time of K graph replays. Workloads smaller than L2 flush it
+    (a 256 MiB write) before every step; the flush is not timed."""
     for _ in range(W):
         step.graph.replay()
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
+    if step.flush_l2:
+        scrub = torch.empty(64 << 20, dtype=torch.float32, device="cuda")
+        total = 0.0
+        for _ in range(K):
+            scrub.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            step.graph.replay()
+            e1.record()
+            e1.synchronize()
+            total += e0.elapsed_time(e1) / 1e3
+        barrier(world)
+        return total
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record()
@@ -250,16 +447,19 @@ def time_graph(step, K, W, world):
 
 
 def time_layers(step, K):
-    """Per-call device time of each layer (CUDA events on the launch stream
-    around each call: the call's RoPE, split and combine kernels)."""
-    n = len(step.layers)
+    """Per-call device time (CUDA events on the launch stream around each call:
+    the call's RoPE, split and combine kernels)."""
+    n = step.ncalls
     reps = max(3, min(K, 50))
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(n)] for _ in range(reps)]
+    scrub = torch.empty(64 << 20, dtype=torch.float32, device="cuda") if step.flush_l2 else None
     for r in range(reps):
         for l in range(n):
+            if scrub is not None:
+                scrub.zero_()
             ev[r][l][0].record()
-            step.run_layer(l)
+            step.run_call(l)
             ev[r][l][1].record()
     torch.cuda.synchronize()
     per = [statistics.mean(ev[r][l][0].elapsed_time(ev[r][l][1]) for r in range(reps)) / 1e3
@@ -269,7 +469,7 @@ def time_layers(step, K):
 
 def time_e2e(step, K, W, world):
     """Through the public API with host buffers: every step copies its inputs
-    from pinned host memory, replays the 28 calls and reads the outputs back."""
+    from pinned host memory, replays the step's calls and reads the outputs back."""
     host_in = torch.empty(step.inbuf.shape, dtype=step.inbuf.dtype, pin_memory=True)
     host_in.copy_(step.inbuf)
     host_out = torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
@@ -302,7 +502,7 @@ def time_e2e(step, K, W, world):
 # ---------------------------------------------------------------- oracle baseline
 
 def oracle_sample_inputs(step, streams, layers):
-    """Host copies of the sampled streams of the chosen layers, with each
+    """Host copies of the sampled streams of the chosen hybrid layers, with each
     full layer's pages gathered into a compact pool."""
     out = []
     u16 = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
@@ -311,7 +511,7 @@ def oracle_sample_inputs(step, streams, layers):
         L = step.layers[l]
         d = {"kind": L["kind"], "rope": L["rope"], "q": u16(L["q"][sel]), "k_new": u16(L["k_new"][sel]),
              "v_new": u16(L["v_new"][sel]), "gate": u16(L["gate"][sel]),
-             "pos": L["pos"][sel].cpu().numpy()}
+             "pos": L["pos"][sel].cpu().numpy(), "Hq": HQ, "Hkv": HKV, "D": D, "P": 16}
         if L["kind"] == "sliding":
             d.update(k=u16(L["k"][sel]), v=u16(L["v"][sel]), head=L["head"][sel].cpu().numpy(),
                      count=L["count"][sel].cpu().numpy())
@@ -331,40 +531,58 @@ def oracle_pass(o, sample):
         if d["kind"] == "sliding":
             o.decode_ring(d["k"], d["v"], d["head"], d["count"], d["q"], d["k_new"], d["v_new"],
                           d["pos"], r, th, gate=d["gate"])
-        else:
+        elif d["kind"] == "full":
             o.decode_paged(d["k"], d["v"], d["block_table"], d["seq_len"], d["q"], d["k_new"],
                            d["v_new"], d["pos"], r, th, gate=d["gate"])
+        else:
+            o.verify(d["k"], d["v"], d["block_table"], d["seq_len"], d["q"], d["k_new"], d["v_new"],
+                     d["parent"], r, th)
 
 
 def sample_bytes_tokens(sample):
     by = tok = 0
     for d in sample:
-        n = int(d["count"][0]) if d["kind"] == "sliding" else int(d["seq_len"][0])
-        Bs = d["q"].shape[0]
-        kv, io = layer_bytes(d["kind"], Bs, n)
-        by += kv + io
-        tok += Bs * (n + 1)
+        Hq, Hkv, Dh, P = d["Hq"], d["Hkv"], d["D"], d["P"]
+        if d["kind"] == "verify":
+            T = d["T"]
+            for n in d["seq_len"]:
+                n = int(n)
+                by += n * 2 * Hkv * Dh * 2 + T * ((Hq + 2 * Hkv) * Dh * 2 + 4 + Hq * Dh * 4 + 2 * Hkv * Dh * 2)
+                tok += n + T
+            continue
+        lens = d["count"] if d["kind"] == "sliding" else d["seq_len"]
+        for n in lens:
+            kv, io = layer_bytes(d["kind"], 1, int(n), P, Hq, Hkv, Dh, d.get("gate") is not None)
+            by += kv + io
+            tok += int(n) + 1
     return by, tok
 
 
 def cpu_baseline(step, budget_s=15.0):
+    """The fp64 oracle timed on a bounded sample of the workload."""
     import oracle as oracle_pkg
     o = oracle_pkg.get()
-    layers = list(range(28))
-    sample = oracle_sample_inputs(step, [0, 1], layers)
+    if isinstance(step, Step):
+        sample = oracle_sample_inputs(step, [0, 1], list(range(28)))
+        what = f"2 of {step.B} streams x all 28 layers"
+        items = 2 * HKV
+    else:
+        sample, what = step.oracle_sample()
+        items = step.Hkv
     t0 = time.perf_counter()
     oracle_pass(o, sample)
     t1 = time.perf_counter() - t0
-    reps = max(1, int(budget_s / max(t1, 1e-3)) - 1)
+    reps = max(1, min(200, int(budget_s / max(t1, 1e-3)) - 1))
     t0 = time.perf_counter()
     for _ in range(reps):
         oracle_pass(o, sample)
     t = (time.perf_counter() - t0) / reps
     by, tok = sample_bytes_tokens(sample)
-    return {"value": by / t / 1e9, "unit": "GB/s", "tokens_per_s": tok / t,
-            "cores": min(o.hardware_threads(), 2 * HKV), "kind": "oracle",
-            "sample": f"2 of {step.B} streams x all 28 layers (the oracle threads over "
-                      f"(stream, KV head): 4 work items), {reps} passes of {t:.3f} s"}
+    cores = min(o.hardware_threads(), items)
+    return {"value": by / t / 1e9, "unit": "GB/s", "tokens_per_s": tok / t, "cores": cores,
+            "kind": "oracle",
+            "sample": f"{what} (the oracle threads over (stream, KV head): {items} work items), "
+                      f"{reps} passes of {t:.3f} s"}
 
 
 # ---------------------------------------------------------------- arms
@@ -382,7 +600,8 @@ def run_reference(args, world, rank):
     for c in cases:
         x, ca = c.inputs, c.cache
         d = {"kind": "sliding" if c.kind == "ring" else "full", "rope": c.rope, "q": x.q,
-             "k_new": x.k_new, "v_new": x.v_new, "gate": x.gate, "pos": x.pos}
+             "k_new": x.k_new, "v_new": x.v_new, "gate": x.gate, "pos": x.pos,
+             "Hq": HQ, "Hkv": HKV, "D": D, "P": 16}
         if c.kind == "ring":
             d.update(k=ca.k, v=ca.v, head=ca.head, count=ca.count)
         else:
@@ -412,10 +631,9 @@ def run_reference(args, world, rank):
 
 def run_dattn(args, world, rank, local):
     assert torch.cuda.is_available(), "bench.py needs a GPU"
-    B, ctx = args.streams, args.context
-    step = Step(B, ctx, SEED + rank)
+    step = make_workload(args.workload, SEED + rank, args)
     step.capture()
-    bytes_step, tokens_step, per_kind = step_accounting(B, ctx)
+    bytes_step, tokens_step = step.bytes_step, step.tokens_step
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -425,14 +643,11 @@ def run_dattn(args, world, rank, local):
     value = bytes_step * world * args.steps / t / 1e9
     tok_s = tokens_step * world * args.steps / t
 
-    # per-call times of the dominant call (the full layers' split-K pass)
+    # per-call time of the dominant call (the split-K pass over the most bytes)
     per = time_layers(step, args.steps)
-    full = [per[l] for l, L in enumerate(step.layers) if L["kind"] == "full"]
-    slid = [per[l] for l, L in enumerate(step.layers) if L["kind"] == "sliding"]
-    t_full = statistics.mean(full)
-    kv_full = per_kind["full"][0]
+    t_dom = statistics.mean(per[l] for l in step.dominant)
     peak, peak_src = peak_hbm()
-    achieved = kv_full / t_full / 1e9
+    achieved = step.dominant_kv_bytes / t_dom / 1e9
 
     e2e = None
     if not args.no_e2e:
@@ -449,30 +664,31 @@ def run_dattn(args, world, rank, local):
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
         try:
-            traffic = json.load(open(tpath)).get("decode_split_full_layer_bytes")
+            traffic = json.load(open(tpath)).get(args.workload)
         except Exception:
             traffic = None
+    config = dict(step.config)
+    config.update({"l2": ("flushed (256 MiB write) before every step" if step.flush_l2 else
+                          f"inputs larger than L2: {bytes_step / 1e9:.3f} GB per step vs 129 MB L2"),
+                   "timing": f"one CUDA graph of {step.ncalls} call(s) per step, CUDA events",
+                   "parallelism": f"replicas x{world}"})
+    per_call = {"dominant": t_dom * 1e6}
+    if step.others:
+        per_call["others"] = statistics.mean(per[l] for l in step.others) * 1e6
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (bf16 N(0,1) K/V and inputs drawn on the device, seeded)",
-        "config": {"workload": "hybrid 28-layer decode step: [sliding x3, full] x7, 8 q / 2 KV heads, "
-                               f"head_dim 256, {B} streams, context {ctx}",
-                   "streams": B, "context": ctx, "sliding_ring_slots": 511,
-                   "full_page_size": 16, "gate": True, "write_back": True,
-                   "l2": f"inputs larger than L2: {bytes_step / 1e9:.2f} GB per step vs 129 MB L2",
-                   "timing": "one CUDA graph of 28 calls per step, CUDA events",
-                   "parallelism": f"replicas x{world}"},
+        "config": config,
         "attended_kv_tokens_per_s": tok_s,
         "frac_of_peak": value / peak,
         "peak_gbs": peak, "peak_source": peak_src,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "kernel": f"decode_split (full layers, {B} streams x {ctx} tokens)",
-                     "note": "achieved = cached K/V bytes of one full-layer call / that call's "
-                             "CUDA-event time (RoPE + split + combine), of " + peak_src},
-        "per_call_us": {"full": t_full * 1e6, "sliding": statistics.mean(slid) * 1e6},
+                     "frac": achieved / peak, "traffic": traffic, "kernel": step.kernel,
+                     "note": "achieved = cached K/V bytes of one dominant call / that call's "
+                             "CUDA-event time (RoPE + split + combine kernels), peak of " + peak_src},
+        "per_call_us": per_call,
         "cpu_baseline": base,
         "e2e": e2e,
         "gpu_launches": step.launches_per_step() * args.steps,
@@ -492,6 +708,9 @@ def main():
     ap.add_argument("--streams", type=int, default=B_STREAMS,
                     help="streams per GPU (smaller values make short profiling runs)")
     ap.add_argument("--context", type=int, default=CONTEXT)
+    ap.add_argument("--workload", default="hybrid", choices=WORKLOADS,
+                    help="hybrid (default): the 28-layer step; sliding, paged, verify, long1m, "
+                         "long262k: the other workloads, one call per step")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     try:

@@ -10,6 +10,7 @@
 //                  applies the gate, stores fp32 and writes the new entry back.
 // The new entry is written in (3), after (2) has completed: when a ring is
 // full the new entry takes the oldest token's slot, which (2) still reads.
+#include <algorithm>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -35,6 +36,8 @@ struct dattn_handle {
   uint16_t* khat = nullptr;
   float* part = nullptr;
   float* vpart = nullptr;   // verify partials: [sms + units][G*T][D+4]
+  int* counters = nullptr;  // finished segments per (stream, KV head); zero between calls
+  int fused_resident = 0;   // resident one-launch decode CTAs on the whole GPU
   size_t vpart_slots = 0;
   int* err = nullptr;
 };
@@ -175,7 +178,8 @@ int dattn_create(const dattn_config* cfg, int device, dattn_t** out) {
   if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
     return fail(DATTN_ECUDA);
   h->split_resident = h->num_sms * decode_split_ctas_per_sm(D, G);
-  if (h->split_resident <= 0) return fail(DATTN_EUNSUPPORTED);
+  h->fused_resident = h->num_sms * decode_fused_ctas_per_sm(D, G);
+  if (h->split_resident <= 0 || h->fused_resident <= 0) return fail(DATTN_EUNSUPPORTED);
 
   // RoPE inverse frequencies theta^(-2i/r), fp64, one table per layer
   for (const dattn_layer_config& L : h->layers) {
@@ -200,7 +204,12 @@ int dattn_create(const dattn_config* cfg, int device, dattn_t** out) {
   if (cudaMalloc(&h->khat, rows * Hkv * D * sizeof(uint16_t)) != cudaSuccess) return fail(DATTN_ECUDA);
   // Partials: one slot per split CTA plus one per unit.
   if (static_cast<int64_t>(h->max_streams) * Hkv > decode_max_units()) return fail(DATTN_EUNSUPPORTED);
-  h->part_units = static_cast<size_t>(h->split_resident) + static_cast<size_t>(h->max_streams) * Hkv;
+  h->part_units = static_cast<size_t>(std::max(h->split_resident, h->fused_resident)) +
+                  static_cast<size_t>(h->max_streams) * Hkv;
+  if (cudaMalloc(&h->counters, static_cast<size_t>(h->max_streams) * Hkv * sizeof(int)) != cudaSuccess)
+    return fail(DATTN_ECUDA);
+  if (cudaMemset(h->counters, 0, static_cast<size_t>(h->max_streams) * Hkv * sizeof(int)) != cudaSuccess)
+    return fail(DATTN_ECUDA);
   if (cudaMalloc(&h->tiles, (static_cast<size_t>(h->max_streams) * Hkv + 1) * sizeof(int)) != cudaSuccess)
     return fail(DATTN_ECUDA);
   const size_t part_floats = h->part_units * h->GP * (D + 2);
@@ -226,6 +235,7 @@ void dattn_destroy(dattn_t* h) {
   cudaFree(h->khat);
   cudaFree(h->part);
   cudaFree(h->vpart);
+  cudaFree(h->counters);
   cudaFree(h->tiles);
   cudaFree(h->err);
   delete h;
@@ -240,6 +250,10 @@ int dattn_get_error(dattn_t* h, dattn_stream_t stream) {
   if (cudaMemcpyAsync(&bits, h->err, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return DATTN_ECUDA;
   if (cudaMemsetAsync(h->err, 0, sizeof(int), s) != cudaSuccess) return DATTN_ECUDA;
+  // a call that gave up part-way may have left segment counts behind
+  if (bits && cudaMemsetAsync(h->counters, 0, static_cast<size_t>(h->max_streams) * h->Hkv * sizeof(int), s) !=
+                  cudaSuccess)
+    return DATTN_ECUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return DATTN_ECUDA;
   if (bits & ERR_TIMEOUT) return DATTN_ETIMEOUT;
   if (bits & ERR_INDEX) return DATTN_EINDEX;
@@ -305,55 +319,35 @@ int dattn_decode(dattn_t* h, int layer, const dattn_cache* cache, const dattn_de
   if (!guard.ok) return DATTN_ECUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-  RopeArgs ra{};
-  ra.rows = B;
-  ra.Hq = h->Hq;
-  ra.Hkv = h->Hkv;
-  ra.D = h->D;
-  ra.r = L.rotary_dim;
-  ra.q = static_cast<const uint16_t*>(args->q);
-  ra.k = static_cast<const uint16_t*>(args->k_new);
-  ra.pos = args->pos;
-  ra.T = 1;
-  ra.inv_freq = h->inv_freq[layer];
-  ra.q_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(h->D)));
-  ra.qhat = h->qhat;
-  ra.khat = h->khat;
-  ra.err = h->err;
-  rc = cuda_status(launch_rope(ra, s));
-  if (rc != DATTN_OK) return rc;
-
-  const int ctas = plan_split_ctas(h, B * h->Hkv, n_max, decode_split_tile_keys(h->D, h->G));
+  const int ctas = [&] {
+    const int tk = decode_split_tile_keys(h->D, h->G);
+    int64_t c = (static_cast<int64_t>(B) * h->Hkv * ((n_max + tk - 1) / tk) + 3) / 4;
+    if (c > h->fused_resident) c = h->fused_resident;
+    return static_cast<int>(c < 1 ? 1 : c);
+  }();
   if (static_cast<size_t>(ctas) + static_cast<size_t>(B) * h->Hkv > h->part_units) return DATTN_EXCEEDS;
-  SplitArgs sa{};
-  sa.c = make_view(h, L, cache);
-  sa.B = B;
-  sa.Hkv = h->Hkv;
-  sa.ctas = ctas;
-  sa.max_len = n_max;
-  sa.qhat = h->qhat;
-  sa.part = h->part;
-  sa.tiles = h->tiles;
-  sa.err = h->err;
-  rc = cuda_status(launch_decode_split(sa, h->D, h->G, s));
-  if (rc != DATTN_OK) return rc;
-
-  CombineArgs ca{};
-  ca.c = sa.c;
-  ca.B = B;
-  ca.Hkv = h->Hkv;
-  ca.split_ctas = ctas;
-  ca.tiles = h->tiles;
-  ca.max_len = n_max;
-  ca.qhat = h->qhat;
-  ca.khat = h->khat;
-  ca.v_new = static_cast<const uint16_t*>(args->v_new);
-  ca.gate = static_cast<const uint16_t*>(args->gate);
-  ca.part = h->part;
-  ca.out = args->out;
-  ca.write_back = args->write_back;
-  ca.err = h->err;
-  return cuda_status(launch_decode_combine(ca, h->D, h->G, s));
+  FusedArgs fa{};
+  fa.c = make_view(h, L, cache);
+  fa.B = B;
+  fa.Hkv = h->Hkv;
+  fa.G = h->G;
+  fa.ctas = ctas;
+  fa.max_len = n_max;
+  fa.q = static_cast<const uint16_t*>(args->q);
+  fa.k_new = static_cast<const uint16_t*>(args->k_new);
+  fa.v_new = static_cast<const uint16_t*>(args->v_new);
+  fa.gate = static_cast<const uint16_t*>(args->gate);
+  fa.pos = args->pos;
+  fa.inv_freq = h->inv_freq[layer];
+  fa.r = L.rotary_dim;
+  fa.q_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(h->D)));
+  fa.out = args->out;
+  fa.write_back = args->write_back;
+  fa.part = h->part;
+  fa.khat = h->khat;
+  fa.counters = h->counters;
+  fa.err = h->err;
+  return cuda_status(launch_decode_fused(fa, h->D, s));
 }
 
 int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, const dattn_verify_args* args,

@@ -79,6 +79,31 @@ struct CombineArgs {
   int* err;
 };
 
+// One-launch decode (RoPE, split-K pass, combine, gate, store, write-back):
+// stream-K over (stream, KV head) units; the CTA that holds a unit's first
+// tile writes its rotated key entry, the CTA that finishes a unit's last
+// segment (per-unit counter) combines the unit.
+struct FusedArgs {
+  CacheView c;
+  int B, Hkv, G;
+  int ctas;
+  int max_len;
+  const uint16_t* q;           // [B, Hq, D]
+  const uint16_t* k_new;       // [B, Hkv, D]
+  const uint16_t* v_new;       // [B, Hkv, D]
+  const uint16_t* gate;        // [B, Hq] or null
+  const int32_t* pos;          // [B]
+  const double* inv_freq;      // [r / 2]
+  int r;
+  float q_scale;               // log2(e) / sqrt(D)
+  float* out;                  // [B, Hq, D]
+  int write_back;
+  float* part;                 // [ctas + B*Hkv][GP*(D+2)]
+  uint16_t* khat;              // [B*Hkv][D] rotated key entries
+  int* counters;               // [B*Hkv] finished segments; zero between calls
+  int* err;
+};
+
 struct AppendArgs {
   CacheView c;
   int B, Tmax, Hkv, D, r;
@@ -129,6 +154,8 @@ struct VerifyCombineArgs {
 cudaError_t launch_rope(const RopeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_split(const SplitArgs& a, int D, int G, cudaStream_t s);
 cudaError_t launch_decode_combine(const CombineArgs& a, int D, int G, cudaStream_t s);
+cudaError_t launch_decode_fused(const FusedArgs& a, int D, cudaStream_t s);
+int decode_fused_ctas_per_sm(int D, int G);
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_verify_split(const VerifySplitArgs& a, int D, cudaStream_t s);
 cudaError_t launch_verify_combine(const VerifyCombineArgs& a, int D, cudaStream_t s);

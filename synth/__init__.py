@@ -332,3 +332,21 @@ def hybrid_step_device(seed: int, B: int, context: int, device="cuda"):
                      seq_len=torch.full((B,), context, dtype=torch.int32, device=device))
         layers.append(L)
     return layers
+
+
+def paged_device(gen, B, Hkv, D, P, lens, room=1, device="cuda"):
+    """Paged pools drawn on the device (bf16 N(0,1) everywhere), page table
+    from a random permutation; lens is a host list of cached lengths."""
+    lens = [int(n) for n in lens]
+    npages = [(n + room + P - 1) // P for n in lens]
+    total = sum(npages) + 3
+    perm = torch.randperm(total, generator=gen, device=device).to(torch.int32)
+    bt = torch.full((B, max(npages)), -1, dtype=torch.int32, device=device)
+    nxt = 0
+    for b in range(B):
+        bt[b, :npages[b]] = perm[nxt:nxt + npages[b]]
+        nxt += npages[b]
+    k = torch.randn(total, Hkv, P, D, generator=gen, device=device).to(torch.bfloat16)
+    v = torch.randn(total, Hkv, P, D, generator=gen, device=device).to(torch.bfloat16)
+    seq = torch.tensor(lens, dtype=torch.int32, device=device)
+    return k, v, bt, seq
