@@ -188,8 +188,10 @@ class Workload:
             self.run_eager()
         torch.cuda.synchronize()
 
+    launches_per_call = 1   # one-launch decode; verify is three kernels
+
     def launches_per_step(self):
-        return 3 * self.ncalls
+        return self.launches_per_call * self.ncalls
 
     def pack_inputs(self, tensors, device):
         """Move the step's per-call inputs into one device buffer (so the
@@ -347,6 +349,7 @@ class DecodeCall(Workload):
 
 class VerifyCall(Workload):
     """One tree-verify round per step: 16 streams x 16 rows."""
+    launches_per_call = 3
 
     def __init__(self, seed, device="cuda"):
         import decode_attention_kv_dattn_gb300 as dattn
@@ -687,7 +690,7 @@ def run_dattn(args, world, rank, local):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "kernel": step.kernel,
                      "note": "achieved = cached K/V bytes of one dominant call / that call's "
-                             "CUDA-event time (RoPE + split + combine kernels), peak of " + peak_src},
+                             "CUDA-event time (all of the call's kernels), peak of " + peak_src},
         "per_call_us": per_call,
         "cpu_baseline": base,
         "e2e": e2e,

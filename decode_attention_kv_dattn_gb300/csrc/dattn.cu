@@ -27,7 +27,7 @@ struct dattn_handle {
   int Hq = 0, Hkv = 0, D = 0, G = 0, GP = 0;
   int max_streams = 0, max_context = 0, max_verify_rows = 0;
   std::vector<dattn_layer_config> layers;
-  std::vector<double*> inv_freq;  // device, per layer ([r/2] or null)
+  std::vector<uint64_t*> rope_step;  // device, per layer ([r/2] phase steps or null)
   int num_sms = 0;
   int split_resident = 0;  // resident split CTAs on the whole GPU
   size_t part_units = 0;   // capacity of the partials, in segment slots
@@ -181,19 +181,18 @@ int dattn_create(const dattn_config* cfg, int device, dattn_t** out) {
   h->fused_resident = h->num_sms * decode_fused_ctas_per_sm(D, G);
   if (h->split_resident <= 0 || h->fused_resident <= 0) return fail(DATTN_EUNSUPPORTED);
 
-  // RoPE inverse frequencies theta^(-2i/r), fp64, one table per layer
+  // RoPE phase steps (fixed-point turns per position), one table per layer
   for (const dattn_layer_config& L : h->layers) {
-    double* dev = nullptr;
+    uint64_t* dev = nullptr;
     if (L.rotary_dim > 0) {
-      std::vector<double> f(L.rotary_dim / 2);
-      for (int i = 0; i < L.rotary_dim / 2; ++i)
-        f[i] = std::pow(L.rope_theta, -static_cast<double>(2 * i) / static_cast<double>(L.rotary_dim));
-      if (cudaMalloc(&dev, f.size() * sizeof(double)) != cudaSuccess) return fail(DATTN_ECUDA);
-      h->inv_freq.push_back(dev);
-      if (cudaMemcpy(dev, f.data(), f.size() * sizeof(double), cudaMemcpyHostToDevice) != cudaSuccess)
+      std::vector<uint64_t> f(L.rotary_dim / 2);
+      for (int i = 0; i < L.rotary_dim / 2; ++i) f[i] = rope_phase_step(L.rope_theta, L.rotary_dim, i);
+      if (cudaMalloc(&dev, f.size() * sizeof(uint64_t)) != cudaSuccess) return fail(DATTN_ECUDA);
+      h->rope_step.push_back(dev);
+      if (cudaMemcpy(dev, f.data(), f.size() * sizeof(uint64_t), cudaMemcpyHostToDevice) != cudaSuccess)
         return fail(DATTN_ECUDA);
     } else {
-      h->inv_freq.push_back(nullptr);
+      h->rope_step.push_back(nullptr);
     }
   }
 
@@ -230,7 +229,7 @@ int dattn_create(const dattn_config* cfg, int device, dattn_t** out) {
 void dattn_destroy(dattn_t* h) {
   if (!h) return;
   DeviceGuard guard(h->device);
-  for (double* p : h->inv_freq) cudaFree(p);
+  for (uint64_t* p : h->rope_step) cudaFree(p);
   cudaFree(h->qhat);
   cudaFree(h->khat);
   cudaFree(h->part);
@@ -290,7 +289,7 @@ int dattn_append_kv(dattn_t* h, int layer, const dattn_cache* cache, int num_str
   a.k = static_cast<const uint16_t*>(k);
   a.v = static_cast<const uint16_t*>(v);
   a.rotate = rotate;
-  a.inv_freq = h->inv_freq[layer];
+  a.rope_step = h->rope_step[layer];
   a.err = h->err;
   return cuda_status(launch_append(a, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -338,7 +337,7 @@ int dattn_decode(dattn_t* h, int layer, const dattn_cache* cache, const dattn_de
   fa.v_new = static_cast<const uint16_t*>(args->v_new);
   fa.gate = static_cast<const uint16_t*>(args->gate);
   fa.pos = args->pos;
-  fa.inv_freq = h->inv_freq[layer];
+  fa.rope_step = h->rope_step[layer];
   fa.r = L.rotary_dim;
   fa.q_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(h->D)));
   fa.out = args->out;
@@ -380,7 +379,7 @@ int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, const dattn_ve
   ra.prefix_len = cache->seq_len;
   ra.parent = args->parent;
   ra.T = T;
-  ra.inv_freq = h->inv_freq[layer];
+  ra.rope_step = h->rope_step[layer];
   ra.q_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(h->D)));
   ra.qhat = h->qhat;
   ra.khat = h->khat;

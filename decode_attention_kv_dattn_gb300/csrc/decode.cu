@@ -74,6 +74,13 @@ __device__ __forceinline__ void unpack8(const uint4& w, float (&f)[8]) {
   f[6] = bf16_lo(w.w); f[7] = bf16_hi(w.w);
 }
 
+__device__ __forceinline__ void unpack8x2(const uint4& w, float2 (&f)[4]) {
+  f[0] = make_float2(bf16_lo(w.x), bf16_hi(w.x));
+  f[1] = make_float2(bf16_lo(w.y), bf16_hi(w.y));
+  f[2] = make_float2(bf16_lo(w.z), bf16_hi(w.z));
+  f[3] = make_float2(bf16_lo(w.w), bf16_hi(w.w));
+}
+
 // Sum W partial values across W lanes (W a power of two, groups aligned) so
 // that lane l ends with the full sum of value (l % W). At each level the lane
 // whose bit `w` is set keeps the upper half of its values and sends the lower
@@ -608,18 +615,6 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const CombineArgs a
 
 // ---------------------------------------------------------------- one-launch decode
 
-// fp32 cos/sin of pos * inv_freq: the angle is formed in fp64 and reduced
-// modulo 2 pi in fp64 (two-constant Cody-Waite: 2 pi = C1 + C2, C1 the fp64
-// value nearest to 2 pi), then evaluated in fp32. Used for q, whose rotation is
-// not part of the bit-exact entry contract.
-__device__ __forceinline__ void rope_cs_f32(int64_t pos, double inv_freq, float& c, float& s) {
-  const double ang = __dmul_rn(static_cast<double>(pos), inv_freq);
-  const double k = rint(ang * 0.15915494309189535);
-  double red = fma(-k, 6.283185307179586, ang);
-  red = fma(-k, 2.4492935982947064e-16, red);
-  sincosf(static_cast<float>(red), &s, &c);
-}
-
 template <int D, int GP>
 struct FGeo {
   using Gm = Geo<D, GP>;
@@ -631,36 +626,40 @@ struct FGeo {
 };
 
 // Rotate the G query heads of unit (b, j) into qs[GP][D] (fp32, pre-scaled;
-// heads >= G are zero). All threads of the CTA take part.
+// heads >= G are zero). All threads of the CTA take part, one pair at a time,
+// each pair's cos and sin shared by the heads.
 template <int D, int GP>
 __device__ __forceinline__ void fused_rope_q(const FusedArgs& a, int b, int j, float* qs) {
   const int G = a.G, Hq = a.Hkv * G, half = a.r / 2;
   const int64_t pos = a.pos[b];
-  for (int it = threadIdx.x; it < GP * (D / 2); it += kThreads) {
-    const int g = it / (D / 2), p = it - g * (D / 2);
+  const uint16_t* src = a.q + (static_cast<int64_t>(b) * Hq + j * G) * D;
+  for (int p = threadIdx.x; p < D / 2; p += kThreads) {
     const int d0 = p < half ? p : a.r + 2 * (p - half);
     const int d1 = p < half ? p + half : d0 + 1;
-    float o0 = 0.f, o1 = 0.f;
-    if (g < G) {
-      const uint16_t* src = a.q + (static_cast<int64_t>(b) * Hq + j * G + g) * D;
-      const float x = bf16_to_f32(src[d0]), y = bf16_to_f32(src[d1]);
-      if (p < half) {
-        float c, s;
-        rope_cs_f32(pos, a.inv_freq[p], c, s);
-        o0 = fmaf(x, c, -y * s) * a.q_scale;
-        o1 = fmaf(y, c, x * s) * a.q_scale;
-      } else {
-        o0 = x * a.q_scale;
-        o1 = y * a.q_scale;
+    float c = 1.f, s = 0.f;
+    if (p < half) rope_cos_sin(pos, a.rope_step[p], c, s);
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+      float o0 = 0.f, o1 = 0.f;
+      if (g < G) {
+        const float x = bf16_to_f32(src[g * D + d0]), y = bf16_to_f32(src[g * D + d1]);
+        if (p < half) {
+          o0 = fmaf(x, c, -y * s) * a.q_scale;
+          o1 = fmaf(y, c, x * s) * a.q_scale;
+        } else {
+          o0 = x * a.q_scale;
+          o1 = y * a.q_scale;
+        }
       }
+      qs[g * D + d0] = o0;
+      qs[g * D + d1] = o1;
     }
-    qs[g * D + d0] = o0;
-    qs[g * D + d1] = o1;
   }
 }
 
-// The bit-exact K entry of unit (b, j): fp64 angle, fp32-rounded fp64 cos/sin,
-// bf16_RNE(x*c - y*s) evaluated in fp64. Written to the workspace.
+// The bit-exact K entry of unit (b, j): bf16_RNE(x*c - y*s) evaluated in fp64
+// (both products exact, one rounding) with the fp32 cos and sin of
+// rope_cos_sin. Written to the workspace.
 template <int D>
 __device__ __forceinline__ void fused_k_entry(const FusedArgs& a, int b, int j, uint16_t* dst) {
   const int half = a.r / 2;
@@ -670,10 +669,9 @@ __device__ __forceinline__ void fused_k_entry(const FusedArgs& a, int b, int j, 
     const int d0 = p < half ? p : a.r + 2 * (p - half);
     const int d1 = p < half ? p + half : d0 + 1;
     if (p < half) {
-      const double angle = __dmul_rn(static_cast<double>(pos), a.inv_freq[p]);
-      double sd, cd;
-      sincos(angle, &sd, &cd);
-      const double c64 = __double2float_rn(cd), s64 = __double2float_rn(sd);
+      float cf, sf;
+      rope_cos_sin(pos, a.rope_step[p], cf, sf);
+      const double c64 = cf, s64 = sf;
       const double x = bf16_to_f32(src[d0]), y = bf16_to_f32(src[d1]);
       dst[d0] = f64_to_bf16(__dsub_rn(__dmul_rn(x, c64), __dmul_rn(y, s64)));
       dst[d1] = f64_to_bf16(__dadd_rn(__dmul_rn(y, c64), __dmul_rn(x, s64)));
@@ -907,19 +905,20 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fused_kernel(const FusedAr
     fused_rope_q<D, GP>(a, b, j, qs);
     if (P[u] >= g0) fused_k_entry<D>(a, b, j, a.khat + static_cast<int64_t>(u) * D);
     __syncthreads();
-    float q[GP][8];
+    // packed fp32 pairs: the FMAs below are Blackwell's two-wide FFMA2
+    float2 q2[GP][4];
 #pragma unroll
     for (int g = 0; g < GP; ++g) {
       const float4 x0 = *reinterpret_cast<const float4*>(qs + g * D + dl);
       const float4 x1 = *reinterpret_cast<const float4*>(qs + g * D + dl + 4);
-      q[g][0] = x0.x; q[g][1] = x0.y; q[g][2] = x0.z; q[g][3] = x0.w;
-      q[g][4] = x1.x; q[g][5] = x1.y; q[g][6] = x1.z; q[g][7] = x1.w;
+      q2[g][0] = make_float2(x0.x, x0.y); q2[g][1] = make_float2(x0.z, x0.w);
+      q2[g][2] = make_float2(x1.x, x1.y); q2[g][3] = make_float2(x1.z, x1.w);
     }
-    float o[GP][8];
+    float2 o2[GP][4];
 #pragma unroll
     for (int g = 0; g < GP; ++g)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[g][e] = 0.f;
+      for (int e = 0; e < 4; ++e) o2[g][e] = make_float2(0.f, 0.f);
     float m_run = -INFINITY, l_run = 0.f;
     int last_stage = -1;
 
@@ -945,14 +944,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fused_kernel(const FusedAr
           float sp[J * GP];
 #pragma unroll
           for (int jj = 0; jj < J; ++jj) {
-            float kf[8];
-            unpack8(Ks[jj * 32 + lane], kf);
+            float2 k2[4];
+            unpack8x2(Ks[jj * 32 + lane], k2);
 #pragma unroll
             for (int h = 0; h < GP; ++h) {
-              float acc = q[h][0] * kf[0];
-#pragma unroll
-              for (int e = 1; e < 8; ++e) acc = fmaf(q[h][e], kf[e], acc);
-              sp[jj * GP + h] = acc;
+              float2 a2 = __fmul2_rn(q2[h][0], k2[0]);
+              a2 = __ffma2_rn(q2[h][1], k2[1], a2);
+              a2 = __ffma2_rn(q2[h][2], k2[2], a2);
+              a2 = __ffma2_rn(q2[h][3], k2[3], a2);
+              sp[jj * GP + h] = a2.x + a2.y;
             }
           }
           float s = transpose_reduce<LPK>(sp, lane);
@@ -968,37 +968,41 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fused_kernel(const FusedAr
           psm[lane] = p;
           if (lane < GP) psm[32 + lane] = corr;
           __syncwarp();
+          // rescale only when some head's running maximum moved
+          if (__any_sync(kFull, corr != 1.f)) {
 #pragma unroll
-          for (int h = 0; h < GP; ++h) {
-            const float cr = psm[32 + h];
+            for (int h = 0; h < GP; ++h) {
+              const float cr = psm[32 + h];
+              const float2 c2 = make_float2(cr, cr);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o[h][e] *= cr;
+              for (int e = 0; e < 4; ++e) o2[h][e] = __fmul2_rn(o2[h][e], c2);
+            }
           }
           if (nvalid >= KT) {
 #pragma unroll
             for (int jj = 0; jj < J; ++jj) {
-              float vf[8];
-              unpack8(Vs[jj * 32 + lane], vf);
+              float2 v2[4];
+              unpack8x2(Vs[jj * 32 + lane], v2);
               const float* pp = psm + half * LPK + jj * GP;
 #pragma unroll
               for (int h = 0; h < GP; ++h) {
-                const float ph = pp[h];
+                const float2 p2 = make_float2(pp[h], pp[h]);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o[h][e] = fmaf(ph, vf[e], o[h][e]);
+                for (int e = 0; e < 4; ++e) o2[h][e] = __ffma2_rn(p2, v2[e], o2[h][e]);
               }
             }
           } else {
 #pragma unroll
             for (int jj = 0; jj < J; ++jj) {
               if (jj * KPS + half < nvalid) {
-                float vf[8];
-                unpack8(Vs[jj * 32 + lane], vf);
+                float2 v2[4];
+                unpack8x2(Vs[jj * 32 + lane], v2);
                 const float* pp = psm + half * LPK + jj * GP;
 #pragma unroll
                 for (int h = 0; h < GP; ++h) {
-                  const float ph = pp[h];
+                  const float2 p2 = make_float2(pp[h], pp[h]);
 #pragma unroll
-                  for (int e = 0; e < 8; ++e) o[h][e] = fmaf(ph, vf[e], o[h][e]);
+                  for (int e = 0; e < 4; ++e) o2[h][e] = __ffma2_rn(p2, v2[e], o2[h][e]);
                 }
               }
             }
@@ -1026,13 +1030,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fused_kernel(const FusedAr
 #pragma unroll
       for (int h = 0; h < GP; ++h)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[h][e] += __shfl_xor_sync(kFull, o[h][e], w);
+        for (int e = 0; e < 4; ++e) {
+          o2[h][e].x += __shfl_xor_sync(kFull, o2[h][e].x, w);
+          o2[h][e].y += __shfl_xor_sync(kFull, o2[h][e].y, w);
+        }
     if (last_stage >= 0 && lane < LPK) {
       float* os = reinterpret_cast<float*>(wsm + last_stage * Gm::STAGE);
 #pragma unroll
       for (int h = 0; h < GP; ++h) {
-        *reinterpret_cast<float4*>(os + h * D + dl) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
-        *reinterpret_cast<float4*>(os + h * D + dl + 4) = make_float4(o[h][4], o[h][5], o[h][6], o[h][7]);
+        *reinterpret_cast<float4*>(os + h * D + dl) = make_float4(o2[h][0].x, o2[h][0].y, o2[h][1].x, o2[h][1].y);
+        *reinterpret_cast<float4*>(os + h * D + dl + 4) = make_float4(o2[h][2].x, o2[h][2].y, o2[h][3].x, o2[h][3].y);
       }
     }
     if (lane < GP) {

@@ -5,9 +5,18 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cmath>
 #include <utility>
 
 namespace dattn {
+
+// RoPE angle step of pair i of an r-dim rotation with base theta, in 64-bit
+// fixed-point turns per position: rint(2^64 * theta^(-2i/r) / 2pi), the
+// frequency and the division by 2pi each rounded to fp64.
+inline uint64_t rope_phase_step(double theta, int r, int i) {
+  const double inv_freq = std::pow(theta, -static_cast<double>(2 * i) / static_cast<double>(r));
+  return static_cast<uint64_t>(std::llrint(std::ldexp(inv_freq / 6.283185307179586, 64)));
+}
 
 // Sticky device error bits (see dattn_get_error).
 enum : int { ERR_INDEX = 1, ERR_TIMEOUT = 2, ERR_LENGTH = 4, ERR_RANGE = 8 };
@@ -40,7 +49,7 @@ struct RopeArgs {
   const int32_t* prefix_len;   // [rows / T] (verify) or null
   const int32_t* parent;       // [rows] (verify) or null
   int T;
-  const double* inv_freq;      // [r / 2]
+  const uint64_t* rope_step;   // [r / 2] phase steps (rope_phase_step)
   float q_scale;               // log2(e) / sqrt(D)
   float* qhat;                 // [rows, Hq, D]
   uint16_t* khat;              // [rows, Hkv, D]
@@ -93,7 +102,7 @@ struct FusedArgs {
   const uint16_t* v_new;       // [B, Hkv, D]
   const uint16_t* gate;        // [B, Hq] or null
   const int32_t* pos;          // [B]
-  const double* inv_freq;      // [r / 2]
+  const uint64_t* rope_step;   // [r / 2] phase steps (rope_phase_step)
   int r;
   float q_scale;               // log2(e) / sqrt(D)
   float* out;                  // [B, Hq, D]
@@ -113,7 +122,7 @@ struct AppendArgs {
   const uint16_t* k;           // [B, Tmax, Hkv, D]
   const uint16_t* v;
   int rotate;
-  const double* inv_freq;
+  const uint64_t* rope_step;   // [r / 2]
   int* err;
 };
 

@@ -117,7 +117,7 @@ extern "C" DATTN_API int dattn_decode_noalloc(const dattn_config* cfg, int layer
   const size_t err_off = off;
   off = align256(off + sizeof(int));
   const size_t freq_off = off;
-  off = align256(off + static_cast<size_t>(half) * sizeof(double));
+  off = align256(off + static_cast<size_t>(half) * sizeof(uint64_t));
   const size_t tiles_off = off;
   off = align256(off + (static_cast<size_t>(B) * Hkv + 1) * sizeof(int));
   const size_t qhat_off = off;
@@ -130,16 +130,15 @@ extern "C" DATTN_API int dattn_decode_noalloc(const dattn_config* cfg, int layer
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int* err = reinterpret_cast<int*>(ds.base + err_off);
-  double* inv_freq = half > 0 ? reinterpret_cast<double*>(ds.base + freq_off) : nullptr;
+  uint64_t* rope_step = half > 0 ? reinterpret_cast<uint64_t*>(ds.base + freq_off) : nullptr;
   // The error word accumulates bits, so it starts every call at zero; the
-  // frequency table is rewritten from the host (theta^(-2i/r) in fp64).
+  // RoPE phase-step table is rewritten from the host.
   if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return DATTN_ECUDA;
   if (half > 0) {
-    double f[128];
+    uint64_t f[128];
     if (half > 128) return DATTN_EUNSUPPORTED;
-    for (int i = 0; i < half; ++i)
-      f[i] = std::pow(L.rope_theta, -static_cast<double>(2 * i) / static_cast<double>(L.rotary_dim));
-    if (cudaMemcpyAsync(inv_freq, f, half * sizeof(double), cudaMemcpyHostToDevice, s) != cudaSuccess)
+    for (int i = 0; i < half; ++i) f[i] = rope_phase_step(L.rope_theta, L.rotary_dim, i);
+    if (cudaMemcpyAsync(rope_step, f, half * sizeof(uint64_t), cudaMemcpyHostToDevice, s) != cudaSuccess)
       return DATTN_ECUDA;
   }
 
@@ -167,7 +166,7 @@ extern "C" DATTN_API int dattn_decode_noalloc(const dattn_config* cfg, int layer
   ra.k = static_cast<const uint16_t*>(args->k_new);
   ra.pos = args->pos;
   ra.T = 1;
-  ra.inv_freq = inv_freq;
+  ra.rope_step = rope_step;
   ra.q_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
   ra.qhat = reinterpret_cast<float*>(ds.base + qhat_off);
   ra.khat = reinterpret_cast<uint16_t*>(ds.base + khat_off);

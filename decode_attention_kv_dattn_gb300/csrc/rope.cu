@@ -6,11 +6,11 @@
 // pos * theta^(-2i/r) (rotate-half convention); dims >= r pass through.
 //
 // Rounding contract of the K entry (the value stored in the cache and scored
-// for the new token): angle = pos * inv_freq in fp64, with inv_freq computed on
-// the host in fp64; c and s are the fp64 cosine and sine rounded to fp32; the
-// entry is bf16_RNE(x*c - y*s) evaluated in fp64. Each product of a bf16 and an
-// fp32 value is exact in fp64, so the only roundings are the fp64 difference
-// and the final bf16 step. q is rotated in fp32 and pre-scaled by
+// for the new token): c and s are the fp32 cosine and sine that rope_cos_sin
+// derives from the pair's fixed-point phase step (an exact phase, then an fp32
+// polynomial); the entry is bf16_RNE(x*c - y*s) evaluated in fp64. Each
+// product of a bf16 and an fp32 value is exact in fp64, so the only roundings
+// are the fp64 difference and the final bf16 step. q is rotated in fp32 and pre-scaled by
 // log2(e)/sqrt(D) so that the split kernel's scores are in base-2 units.
 #include "common.cuh"
 
@@ -26,7 +26,7 @@ constexpr int kMaxT = 16;             // verify rows per stream
 // The prologue of a call: one CTA per token row. Work items are "pair slots"
 // of every head (Hq query heads, then Hkv key heads): slot p < r/2 is the
 // rotated pair (p, p + r/2); slot p >= r/2 holds two pass-through dims. All
-// inputs are loaded first; the fp64 cos/sin of each pair index is computed
+// inputs are loaded first; the cos/sin of each pair index is computed
 // once per row (one thread each) into shared memory meanwhile.
 __global__ void __launch_bounds__(kRowThreads) rope_kernel(const RopeArgs a) {
   __shared__ float cs_c[128], cs_s[128];
@@ -81,11 +81,10 @@ __global__ void __launch_bounds__(kRowThreads) rope_kernel(const RopeArgs a) {
   }
   __syncthreads();
   if (threadIdx.x < half) {
-    const double angle = __dmul_rn(static_cast<double>(pos_s), a.inv_freq[threadIdx.x]);
-    double sd, cd;
-    sincos(angle, &sd, &cd);
-    cs_c[threadIdx.x] = __double2float_rn(cd);
-    cs_s[threadIdx.x] = __double2float_rn(sd);
+    float cf, sf;
+    rope_cos_sin(pos_s, a.rope_step[threadIdx.x], cf, sf);
+    cs_c[threadIdx.x] = cf;
+    cs_s[threadIdx.x] = sf;
   }
   __syncthreads();
 
@@ -183,10 +182,9 @@ __global__ void __launch_bounds__(kRopeThreads) append_kernel(const AppendArgs a
   for (int job = threadIdx.x; job < half + (a.D - a.r); job += kRopeThreads) {
     if (job < half) {
       const int i = job;
-      const double angle = __dmul_rn(static_cast<double>(pos), a.inv_freq[i]);
-      double sd, cd;
-      sincos(angle, &sd, &cd);
-      const double c64 = __double2float_rn(cd), s64 = __double2float_rn(sd);
+      float cf, sf;
+      rope_cos_sin(pos, a.rope_step[i], cf, sf);
+      const double c64 = cf, s64 = sf;
       for (int h = 0; h < a.Hkv; ++h) {
         const double x = bf16_to_f32(a.k[src0 + h * a.D + i]);
         const double y = bf16_to_f32(a.k[src0 + h * a.D + i + half]);

@@ -157,7 +157,8 @@ typedef struct {
 } dattn_verify_args;
 
 /* Create a handle on `device`: validates the config, uploads per-layer RoPE
- * frequency tables (theta^(-2i/r) in fp64, computed on the host) and
+ * phase-step tables (the angle per position of each pair, theta^(-2i/r), as
+ * 64-bit fixed-point turns, computed on the host) and
  * allocates the workspace for the split-K partials. The handle owns that
  * memory until dattn_destroy. */
 DATTN_API int dattn_create(const dattn_config* cfg, int device, dattn_t** out);

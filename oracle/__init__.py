@@ -42,6 +42,8 @@ class Oracle:
         L = self.lib
         L.oracle_bf16_round.argtypes = [_D]
         L.oracle_bf16_round.restype = ctypes.c_uint16
+        L.oracle_rope_cos_sin.argtypes = [_I, _D, _L, _I, ctypes.POINTER(_D), ctypes.POINTER(_D)]
+        L.oracle_rope_cos_sin.restype = None
         L.oracle_rope_f64.argtypes = [_P, _I, _I, _D, _L, _P]
         L.oracle_rope_bf16.argtypes = [_P, _I, _I, _D, _L, _P]
         L.oracle_decode_ring.argtypes = [_I, _I, _I, _I, _I, _D, _P, _P, _I, _I, _P, _P, _P,
@@ -69,6 +71,11 @@ class Oracle:
     # ---- numbers and RoPE
     def bf16_round(self, t: float) -> int:
         return int(self.lib.oracle_bf16_round(float(t)))
+
+    def rope_cos_sin(self, r, theta, pos, i):
+        c, s = _D(), _D()
+        self.lib.oracle_rope_cos_sin(r, theta, pos, i, ctypes.byref(c), ctypes.byref(s))
+        return c.value, s.value
 
     def rope_f64(self, x, r, theta, pos):
         x = _u16(x)

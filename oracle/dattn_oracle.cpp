@@ -29,7 +29,8 @@
 //  R5 a ring's valid slots are the `count` slots before `head` (cyclically);
 //     the new entry is written at `head`.
 //  R6 the new K entry is bf16_RNE(x*c - y*s) computed in fp64, with c and s
-//     the fp32-rounded cosine and sine of angle = pos * inv_freq (fp64). The
+//     the fp32 cosine and sine of the angle pos * inv_freq given by the fixed
+//     procedure in rope_cos_sin (fixed-point phase, fp32 polynomial). The
 //     new token is scored with that bf16 entry, i.e. exactly the value that is
 //     stored in the cache, so the score-space join equals attention over the
 //     concatenated key matrix.
@@ -92,7 +93,22 @@ uint16_t bf16_round(double t) {
 
 // ---------------------------------------------------------------- RoPE (R1, R6)
 
-// cos and sin of the rotation of pair i at position pos, each rounded to fp32.
+// cos and sin of the rotation of pair i at position pos, as fp32 values, by
+// the fixed procedure of reading R6, which the GPU runs with the same integer
+// and IEEE operations:
+//  1. The angle pos * theta^(-2i/r) is carried as a fraction of a turn in
+//     64-bit fixed point: F = rint(2^64 * fl64(inv_freq / fl64(2 pi))), and
+//     phase = pos * F mod 2^64 (exact wrap-around arithmetic; a negative pos
+//     wraps the same way). Only the top 32 bits of the phase are kept.
+//  2. The phase is split into a quadrant j (the turn rounded to the nearest
+//     quarter) and a remainder rho in [-2^29, 2^29), i.e. [-1/8, 1/8) of a turn;
+//     t = fl32(fl32(rho) * fl32(2 pi / 2^32)) is the remainder in radians.
+//  3. sin t = t + t^3 (S3 + t^2 (S5 + t^2 (S7 + t^2 S9))) and
+//     cos t = 1 + t^2 (C2 + t^2 (C4 + t^2 (C6 + t^2 (C8 + t^2 C10)))), in fp32
+//     with fused multiply-adds, the Taylor coefficients +-1/n! rounded to fp32
+//     (the first omitted terms are below 2e-9 for |t| <= pi/4).
+//  4. (cos, sin) of the angle follow from (cos t, sin t) by the quarter turns j.
+// The results lie within 2.5e-7 of the cosine and sine of the exact angle.
 void rope_cos_sin(int r, double theta, int64_t pos, int i, double* c, double* s) {
 #if ORACLE_MUTATION == 7
   (void)r;
@@ -101,9 +117,44 @@ void rope_cos_sin(int r, double theta, int64_t pos, int i, double* c, double* s)
   const double expo = -static_cast<double>(2 * i) / static_cast<double>(r);
 #endif
   const double inv_freq = std::pow(theta, expo);
-  const double angle = static_cast<double>(pos) * inv_freq;
-  *c = static_cast<double>(static_cast<float>(std::cos(angle)));
-  *s = static_cast<double>(static_cast<float>(std::sin(angle)));
+  const uint64_t F = static_cast<uint64_t>(std::llrint(std::ldexp(inv_freq / 6.283185307179586, 64)));
+  const uint64_t phase = static_cast<uint64_t>(pos) * F;  // mod 2^64
+#if ORACLE_MUTATION == 16
+  // planted: quadrant by truncation, remainder in [0, 1/4) turn (not centred)
+  const uint32_t w = static_cast<uint32_t>(phase >> 32);
+  const int quadrant = static_cast<int>(w >> 30);
+  const int32_t rho = static_cast<int32_t>(w & ((1u << 30) - 1));
+#else
+  const uint32_t w = static_cast<uint32_t>(phase >> 32) + (1u << 29);
+  const int quadrant = static_cast<int>(w >> 30);
+  const int32_t rho = static_cast<int32_t>(w & ((1u << 30) - 1)) - (1 << 29);
+#endif
+  const float t = static_cast<float>(rho) * 1.46291807926715968e-09f;  // 2 pi / 2^32
+  const float t2 = t * t;
+  float sp = std::fmaf(t2, 2.75573192e-06f, -1.98412698e-04f);
+  sp = std::fmaf(t2, sp, 8.33333333e-03f);
+  sp = std::fmaf(t2, sp, -1.66666667e-01f);
+  const float sn = std::fmaf(t * t2, sp, t);
+  float cp = std::fmaf(t2, -2.75573192e-07f, 2.48015873e-05f);
+  cp = std::fmaf(t2, cp, -1.38888889e-03f);
+  cp = std::fmaf(t2, cp, 4.16666667e-02f);
+  cp = std::fmaf(t2, cp, -5.0e-01f);
+  const float cs = std::fmaf(t2, cp, 1.0f);
+  float cf, sf;
+  switch (quadrant) {
+    case 0: cf = cs; sf = sn; break;
+#if ORACLE_MUTATION == 15
+    case 1: cf = sn; sf = -cs; break;  // planted: quarter turns the wrong way
+    case 2: cf = -cs; sf = -sn; break;
+    default: cf = -sn; sf = cs; break;
+#else
+    case 1: cf = -sn; sf = cs; break;
+    case 2: cf = -cs; sf = -sn; break;
+    default: cf = sn; sf = -cs; break;
+#endif
+  }
+  *c = static_cast<double>(cf);
+  *s = static_cast<double>(sf);
 }
 
 // Rotate the bf16 vector x (length D) at position pos. The result is fp64;
@@ -314,6 +365,11 @@ extern "C" {
 // ----- numbers and RoPE, exposed for the pins
 
 uint16_t oracle_bf16_round(double t) { return bf16_round(t); }
+
+// cos and sin of pair i's rotation at pos (rope_cos_sin), for the pins.
+void oracle_rope_cos_sin(int r, double theta, int64_t pos, int i, double* c, double* s) {
+  rope_cos_sin(r, theta, pos, i, c, s);
+}
 
 int oracle_rope_f64(const uint16_t* x, int D, int r, double theta, int64_t pos, double* out) {
   if (D <= 0 || r < 0 || r > D || r % 2) return 1;

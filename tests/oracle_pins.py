@@ -88,8 +88,38 @@ def pin_bf16_rounding_matches_fp32_conversion(o):
 # ------------------------------------------------------------------ RoPE
 
 def _golden_sym(expr: str) -> float:
-    env = {"c": lambda a: f32(math.cos(a)), "s": lambda a: f32(math.sin(a))}
+    env = {"c": lambda a: math.cos(a), "s": lambda a: math.sin(a)}
     return float(eval(expr, {"__builtins__": {}}, env))
+
+
+# The oracle's cos and sin are fp32 values within COS_SIN_TOL of the cosine and
+# sine of the exact angle for |pos| <= 2^21 (fixed-point phase, fp32 Taylor
+# polynomial on [-pi/4, pi/4]); a pair rotated by them is within twice that
+# times the pair's magnitude.
+COS_SIN_TOL = 1.5e-7
+
+
+def pin_rope_cos_sin_accuracy(o):
+    """cos/sin of pos * theta^(-2i/r) against 40-digit values, over both layer
+    types, every quadrant, angles at quarter turns and negative positions."""
+    mpmath = __import__("mpmath")
+    mpmath.mp.dps = 40
+    rng = np.random.default_rng(3)
+    positions = list(range(0, 33)) + [-1, -77, 511, 4095, 8192, 1 << 20, (1 << 21) - 1]
+    positions += [int(p) for p in rng.integers(0, 1 << 21, 24)]
+    for r, theta in ((256, 1e4), (64, 5e6), (2, 1.0)):
+        for pos in positions:
+            for i in range(r // 2):
+                c, s = o.rope_cos_sin(r, theta, pos, i)
+                assert c == f32(c) and s == f32(s), "cos/sin are fp32 values"
+                a = mpmath.mpf(pos) * mpmath.power(mpmath.mpf(theta), mpmath.mpf(-2 * i) / r)
+                close([c, s], [float(mpmath.cos(a)), float(mpmath.sin(a))], COS_SIN_TOL,
+                      f"cos/sin r={r} theta={theta} pos={pos} i={i}")
+    # r = 2, theta irrelevant (frequency 1): angles 0, 1, ..., and near k pi/4
+    for k in range(-9, 10):
+        pos = round(k * math.pi / 4)
+        c, s = o.rope_cos_sin(2, 1.0, pos, 0)
+        close([c, s], [math.cos(pos), math.sin(pos)], COS_SIN_TOL, f"pos {pos}")
 
 
 def pin_rope_golden(o):
@@ -106,7 +136,7 @@ def pin_rope_golden(o):
         for k, e in c["expect"].items():
             want[int(k)] = _golden_sym(e)
         got = o.rope_f64(bf16(x), c["r"], c["theta"], c["pos"])
-        close(got, want, 1e-15, f"rope golden ({c['why']})")
+        close(got, want, 2 * COS_SIN_TOL * max(1.0, np.abs(x).max()), f"rope golden ({c['why']})")
 
 
 def pin_rope_r2_is_complex_multiplication(o):
@@ -114,9 +144,9 @@ def pin_rope_r2_is_complex_multiplication(o):
     x = rand_bf16(2, 11)
     xv = bf16_val(x)
     for pos in (1, 2, 7, 100, 4097, 1 << 20):
-        z = complex(xv[0], xv[1]) * complex(f32(math.cos(pos)), f32(math.sin(pos)))
+        z = complex(xv[0], xv[1]) * complex(math.cos(pos), math.sin(pos))
         got = o.rope_f64(x, 2, 12345.0, pos)
-        close(got, [z.real, z.imag], 1e-15, f"r=2 pos={pos}")
+        close(got, [z.real, z.imag], 2 * COS_SIN_TOL * abs(z), f"r=2 pos={pos}")
 
 
 def pin_rope_norm_and_relative_position(o):
