@@ -36,8 +36,6 @@ struct dattn_handle {
   uint16_t* khat = nullptr;
   float* part = nullptr;
   float* vpart = nullptr;   // verify partials: [sms + units][G*T][D+4]
-  int* counters = nullptr;  // finished segments per (stream, KV head); zero between calls
-  int fused_resident = 0;   // resident one-launch decode CTAs on the whole GPU
   size_t vpart_slots = 0;
   int* err = nullptr;
 };
@@ -46,7 +44,6 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int padded_group(int G) { return G <= 2 ? 2 : (G <= 4 ? 4 : (G <= 8 ? 8 : 0)); }
 
 // Make `dev` current for the duration of a call and restore the caller's.
 struct DeviceGuard {
@@ -139,7 +136,7 @@ int dattn_create(const dattn_config* cfg, int device, dattn_t** out) {
   if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return DATTN_EINVAL;
   if (D != 128 && D != 256) return DATTN_EUNSUPPORTED;
   const int G = Hq / Hkv;
-  if (padded_group(G) == 0) return DATTN_EUNSUPPORTED;
+  if (decode_group_pad(G) == 0) return DATTN_EUNSUPPORTED;
   if (cfg->max_streams <= 0 || cfg->max_context < 0 || cfg->num_layers <= 0 || !cfg->layers)
     return DATTN_EINVAL;
   if (cfg->max_verify_rows < 0 || cfg->max_verify_rows > 16) return DATTN_EINVAL;
@@ -165,7 +162,7 @@ int dattn_create(const dattn_config* cfg, int device, dattn_t** out) {
   h->Hkv = Hkv;
   h->D = D;
   h->G = G;
-  h->GP = padded_group(G);
+  h->GP = decode_group_pad(G);
   h->max_streams = cfg->max_streams;
   h->max_context = cfg->max_context;
   h->max_verify_rows = cfg->max_verify_rows;
@@ -178,8 +175,7 @@ int dattn_create(const dattn_config* cfg, int device, dattn_t** out) {
   if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
     return fail(DATTN_ECUDA);
   h->split_resident = h->num_sms * decode_split_ctas_per_sm(D, G);
-  h->fused_resident = h->num_sms * decode_fused_ctas_per_sm(D, G);
-  if (h->split_resident <= 0 || h->fused_resident <= 0) return fail(DATTN_EUNSUPPORTED);
+  if (h->split_resident <= 0) return fail(DATTN_EUNSUPPORTED);
 
   // RoPE phase steps (fixed-point turns per position), one table per layer
   for (const dattn_layer_config& L : h->layers) {
@@ -203,12 +199,7 @@ int dattn_create(const dattn_config* cfg, int device, dattn_t** out) {
   if (cudaMalloc(&h->khat, rows * Hkv * D * sizeof(uint16_t)) != cudaSuccess) return fail(DATTN_ECUDA);
   // Partials: one slot per split CTA plus one per unit.
   if (static_cast<int64_t>(h->max_streams) * Hkv > decode_max_units()) return fail(DATTN_EUNSUPPORTED);
-  h->part_units = static_cast<size_t>(std::max(h->split_resident, h->fused_resident)) +
-                  static_cast<size_t>(h->max_streams) * Hkv;
-  if (cudaMalloc(&h->counters, static_cast<size_t>(h->max_streams) * Hkv * sizeof(int)) != cudaSuccess)
-    return fail(DATTN_ECUDA);
-  if (cudaMemset(h->counters, 0, static_cast<size_t>(h->max_streams) * Hkv * sizeof(int)) != cudaSuccess)
-    return fail(DATTN_ECUDA);
+  h->part_units = static_cast<size_t>(h->split_resident) + static_cast<size_t>(h->max_streams) * Hkv;
   if (cudaMalloc(&h->tiles, (static_cast<size_t>(h->max_streams) * Hkv + 1) * sizeof(int)) != cudaSuccess)
     return fail(DATTN_ECUDA);
   const size_t part_floats = h->part_units * h->GP * (D + 2);
@@ -234,7 +225,6 @@ void dattn_destroy(dattn_t* h) {
   cudaFree(h->khat);
   cudaFree(h->part);
   cudaFree(h->vpart);
-  cudaFree(h->counters);
   cudaFree(h->tiles);
   cudaFree(h->err);
   delete h;
@@ -249,10 +239,6 @@ int dattn_get_error(dattn_t* h, dattn_stream_t stream) {
   if (cudaMemcpyAsync(&bits, h->err, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return DATTN_ECUDA;
   if (cudaMemsetAsync(h->err, 0, sizeof(int), s) != cudaSuccess) return DATTN_ECUDA;
-  // a call that gave up part-way may have left segment counts behind
-  if (bits && cudaMemsetAsync(h->counters, 0, static_cast<size_t>(h->max_streams) * h->Hkv * sizeof(int), s) !=
-                  cudaSuccess)
-    return DATTN_ECUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return DATTN_ECUDA;
   if (bits & ERR_TIMEOUT) return DATTN_ETIMEOUT;
   if (bits & ERR_INDEX) return DATTN_EINDEX;
@@ -318,35 +304,56 @@ int dattn_decode(dattn_t* h, int layer, const dattn_cache* cache, const dattn_de
   if (!guard.ok) return DATTN_ECUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-  const int ctas = [&] {
-    const int tk = decode_split_tile_keys(h->D, h->G);
-    int64_t c = (static_cast<int64_t>(B) * h->Hkv * ((n_max + tk - 1) / tk) + 3) / 4;
-    if (c > h->fused_resident) c = h->fused_resident;
-    return static_cast<int>(c < 1 ? 1 : c);
-  }();
+  RopeArgs ra{};
+  ra.rows = B;
+  ra.Hq = h->Hq;
+  ra.Hkv = h->Hkv;
+  ra.D = h->D;
+  ra.r = L.rotary_dim;
+  ra.q = static_cast<const uint16_t*>(args->q);
+  ra.k = static_cast<const uint16_t*>(args->k_new);
+  ra.pos = args->pos;
+  ra.T = 1;
+  ra.rope_step = h->rope_step[layer];
+  ra.q_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(h->D)));
+  ra.qhat = h->qhat;
+  ra.khat = h->khat;
+  ra.err = h->err;
+  rc = cuda_status(launch_rope(ra, s));
+  if (rc != DATTN_OK) return rc;
+
+  const int ctas = plan_split_ctas(h, B * h->Hkv, n_max, decode_split_tile_keys(h->D, h->G));
   if (static_cast<size_t>(ctas) + static_cast<size_t>(B) * h->Hkv > h->part_units) return DATTN_EXCEEDS;
-  FusedArgs fa{};
-  fa.c = make_view(h, L, cache);
-  fa.B = B;
-  fa.Hkv = h->Hkv;
-  fa.G = h->G;
-  fa.ctas = ctas;
-  fa.max_len = n_max;
-  fa.q = static_cast<const uint16_t*>(args->q);
-  fa.k_new = static_cast<const uint16_t*>(args->k_new);
-  fa.v_new = static_cast<const uint16_t*>(args->v_new);
-  fa.gate = static_cast<const uint16_t*>(args->gate);
-  fa.pos = args->pos;
-  fa.rope_step = h->rope_step[layer];
-  fa.r = L.rotary_dim;
-  fa.q_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(h->D)));
-  fa.out = args->out;
-  fa.write_back = args->write_back;
-  fa.part = h->part;
-  fa.khat = h->khat;
-  fa.counters = h->counters;
-  fa.err = h->err;
-  return cuda_status(launch_decode_fused(fa, h->D, s));
+  SplitArgs sa{};
+  sa.c = make_view(h, L, cache);
+  if (encode_cache_maps(sa.c, h->Hkv, h->D, &sa.tmap_k, &sa.tmap_v) != cudaSuccess) return DATTN_EUNSUPPORTED;
+  sa.B = B;
+  sa.Hkv = h->Hkv;
+  sa.ctas = ctas;
+  sa.max_len = n_max;
+  sa.qhat = h->qhat;
+  sa.part = h->part;
+  sa.tiles = h->tiles;
+  sa.err = h->err;
+  rc = cuda_status(launch_decode_split(sa, h->D, h->G, s));
+  if (rc != DATTN_OK) return rc;
+
+  CombineArgs ca{};
+  ca.c = sa.c;
+  ca.B = B;
+  ca.Hkv = h->Hkv;
+  ca.split_ctas = ctas;
+  ca.tiles = h->tiles;
+  ca.max_len = n_max;
+  ca.qhat = h->qhat;
+  ca.khat = h->khat;
+  ca.v_new = static_cast<const uint16_t*>(args->v_new);
+  ca.gate = static_cast<const uint16_t*>(args->gate);
+  ca.part = h->part;
+  ca.out = args->out;
+  ca.write_back = args->write_back;
+  ca.err = h->err;
+  return cuda_status(launch_decode_combine(ca, h->D, h->G, s));
 }
 
 int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, const dattn_verify_args* args,

@@ -6,33 +6,49 @@
 // one softmax; nothing cache-sized is copied, and the new K/V entry is written
 // into its slot afterwards. A ring's slots need no reordering (softmax is
 // order-free, cached keys carry their own rotary phase); unwritten slots are
-// masked by never being read. Grouped-query attention shares each KV head's
-// loads among its G query heads ("vllm-omni commits", talker export commit).
-// Splitting the keys over many CTAs and merging their partial softmax states
-// follows "TensorFold PR #608" (the split "shared" kernel plus a merge, the
-// lessons that the grid must fill the GPU and that a merge must not be a chain
-// of dependent loads).
+// masked. Grouped-query attention shares each KV head's loads among its G
+// query heads ("vllm-omni commits", talker export commit). Splitting the keys
+// over many CTAs and merging their partial softmax states follows "TensorFold
+// PR #608" (the split "shared" kernel plus a merge, the lessons that the grid
+// must fill the GPU and that a merge must not be a chain of dependent loads).
 //
 // GB300 design.
-//  * Work split (stream-K). A "unit" is one (stream, KV head); its cached keys
-//    form ceil(n / SK) stage tiles. All units' tiles are laid end to end and the
-//    grid - exactly the CTAs that fit on the GPU at once - cuts that sequence
-//    into equal contiguous ranges, so every CTA moves the same number of bytes
-//    whatever the mix of lengths. Each piece of a unit inside one CTA (a
-//    "segment") leaves one partial softmax state (m, l, o); the combine merges
-//    a unit's segments.
-//  * Loads. Each warp owns a private ring of NS stage buffers. One lane issues
-//    bulk TMA copies (cp.async.bulk global -> shared, completion counted in
-//    transaction bytes on the stage's mbarrier) for the K and V rows of the
-//    warp's tile NS ahead; the ring keeps streaming across segment boundaries.
-//    Pages and ring wrap-around turn into one copy per contiguous run of rows.
-//  * Math. At G flops per byte the KV stream is HBM-bound, so scores and the
-//    value sum run on the FP32 pipes. A lane holds 8 dims (one 16-byte shared
-//    load) of a key; the per-head dot products of J keys are reduced across the
-//    lanes of a key by a transposing butterfly that leaves exactly one
-//    (key, head) score per lane, so the online softmax costs one exp2 per lane
-//    per sub-tile. Probabilities reach all lanes through shared memory.
+//  * Work split (stream-K). A "unit" is one (stream, KV head). Its cached keys
+//    are visited in groups of 16 rows: 16-row runs of a page (a page of P
+//    rows gives ceil(P / 16) groups), or 16-slot blocks of the ring's physical
+//    slots (only the blocks that hold valid slots; softmax does not care about
+//    the order). A stage tile is 256 / D groups (16 KB of K and V). All units'
+//    tiles are laid end to end and the grid - one CTA per SM - cuts that
+//    sequence into equal contiguous ranges, so every CTA moves the same number
+//    of bytes whatever the mix of lengths. Each piece of a unit inside one CTA
+//    (a "segment") leaves one partial softmax state (m, l, o); the combine
+//    merges a unit's segments.
+//  * Loads. Each warp owns a ring of NS stage buffers. One lane issues 2D
+//    tensor TMA copies (boxes of 16 rows x 64 bf16, 128-byte swizzle; one box
+//    per 64 dims of K and of V per group) for the warp's tile NS ahead, with
+//    completion counted in bytes on the stage's mbarrier; the ring keeps
+//    streaming across segment boundaries. Rows a box brings in that are not
+//    valid keys (past a unit's length, past a page, outside a ring's valid
+//    slots, or zero-filled past the pool) are masked: their scores are set to
+//    -inf and their V rows are zeroed in shared memory before use.
+//  * Math on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate).
+//    The KV stream is HBM-bound at G flops per byte; the tensor cores are used
+//    because they cut the instructions per byte about tenfold against fp32
+//    FMAs, which otherwise limit the issue rate. Per group of 16 keys:
+//      S^T (16 keys x 8 cols) = K (16 x D) . Q^T (D x 8 cols)
+//      O^T (D x 8 cols)      += V^T (D x 16) . P^T (16 x 8 cols)
+//    The 8 (or 2 x 8) columns hold each query head twice: once as the bf16
+//    rounding of the pre-scaled rotated q, once as the bf16 rounding of what
+//    is left ("hi" and "lo"), so q keeps 16 significant bits; the two score
+//    columns of a head are added. The probabilities are split into hi and lo
+//    bf16 parts the same way, so the value sum sees 16-bit probabilities; the
+//    two output columns of a head are added at the end. K and V enter the
+//    tensor cores exactly (they are bf16). The score fragment turns into the
+//    PV operand in registers (movmatrix transposes); online softmax in base 2
+//    runs on the score fragment, and the output is rescaled only when some
+//    head's running maximum moved.
 #include "common.cuh"
+#include "mma.cuh"
 
 namespace dattn {
 
@@ -42,64 +58,27 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxUnits = 1024;   // (stream, KV head) units per call
+constexpr int kGroup = 16;        // keys per MMA group
+constexpr int kBoxBytes = kGroup * 128;  // one TMA box: 16 rows x 64 bf16
 
-template <int D, int GP>
+template <int D, int NT>
 struct Geo {
-  static constexpr int LPK = D / 8;          // lanes per key row (16 bytes each)
-  static constexpr int KPS = 32 / LPK;       // keys per warp-wide load
-  static constexpr int J = LPK / GP;         // loads per sub-tile (J * GP scores per lane)
-  static constexpr int KT = J * KPS;         // keys per sub-tile
-  static constexpr int ROW = D * 2;          // bytes per key row
-  static constexpr int SK_MIN = 8192 / (2 * ROW);
-  static constexpr int SUB = KT >= SK_MIN ? 1 : SK_MIN / KT;
-  static constexpr int SK = KT * SUB;        // keys per stage tile (>= 8 KB of K + V)
-  static constexpr int TILE = SK * ROW;      // bytes of the K (or V) half of a stage
-  static constexpr int STAGE = 2 * TILE;
-  static constexpr int NS = STAGE >= 16384 ? 2 : 3;
-  static constexpr int BAR_OFF = kWarps * NS * STAGE;
-  static constexpr int ML_OFF = BAR_OFF + kWarps * NS * 8;     // float [kWarps][2*GP]
-  static constexpr int SLOT_OFF = ML_OFF + kWarps * 2 * GP * 4; // int [kWarps]
-  static constexpr int PSM_OFF = SLOT_OFF + kWarps * 4;         // float [kWarps][32+GP]
-  static constexpr int TAB_OFF = (PSM_OFF + kWarps * (32 + GP) * 4 + 15) / 16 * 16;
-  static constexpr int SMEM_MAX = TAB_OFF + (2 * kMaxUnits + 1) * 4;
+  static constexpr int GP = 4 * NT;                  // heads per partial slot
+  static constexpr int KSTEPS = D / 16;              // MMA k-steps of a score, m-tiles of an output
+  static constexpr int BOXES = D / 64;               // TMA boxes per 16-row group of K (or V)
+  static constexpr int GBYTES = BOXES * kBoxBytes;   // K (or V) bytes of one group
+  static constexpr int KG = 256 / D;                 // groups per stage tile
+  static constexpr int KHALF = KG * GBYTES;          // K part of a stage; V follows
+  static constexpr int STAGE = 2 * KHALF;
+  static constexpr int NS = 3;
+  static constexpr int BAR_OFF = kWarps * NS * STAGE;        // from the 1024-aligned base
+  static constexpr int ML_OFF = BAR_OFF + kWarps * NS * 8;   // float [kWarps][2*GP]
+  static constexpr int SLOT_OFF = ML_OFF + kWarps * 2 * GP * 4;  // int [kWarps]
+  static constexpr int TAB_OFF = (SLOT_OFF + kWarps * 4 + 15) / 16 * 16;
+  static constexpr int SMEM_MAX = 1024 + TAB_OFF + (2 * kMaxUnits + 1) * 4;
   static_assert(D == 128 || D == 256, "head_dim");
-  static_assert(LPK % GP == 0, "GP must divide the lanes per key");
   static_assert(GP * D * 4 <= STAGE, "a stage buffer holds one warp's partial output");
 };
-
-__device__ __forceinline__ void unpack8(const uint4& w, float (&f)[8]) {
-  f[0] = bf16_lo(w.x); f[1] = bf16_hi(w.x);
-  f[2] = bf16_lo(w.y); f[3] = bf16_hi(w.y);
-  f[4] = bf16_lo(w.z); f[5] = bf16_hi(w.z);
-  f[6] = bf16_lo(w.w); f[7] = bf16_hi(w.w);
-}
-
-__device__ __forceinline__ void unpack8x2(const uint4& w, float2 (&f)[4]) {
-  f[0] = make_float2(bf16_lo(w.x), bf16_hi(w.x));
-  f[1] = make_float2(bf16_lo(w.y), bf16_hi(w.y));
-  f[2] = make_float2(bf16_lo(w.z), bf16_hi(w.z));
-  f[3] = make_float2(bf16_lo(w.w), bf16_hi(w.w));
-}
-
-// Sum W partial values across W lanes (W a power of two, groups aligned) so
-// that lane l ends with the full sum of value (l % W). At each level the lane
-// whose bit `w` is set keeps the upper half of its values and sends the lower
-// half to its partner, which does the opposite.
-template <int W>
-__device__ __forceinline__ float transpose_reduce(float (&v)[W], int lane) {
-#pragma unroll
-  for (int w = W / 2; w >= 1; w >>= 1) {
-    const bool upper = (lane & w) != 0;
-#pragma unroll
-    for (int i = 0; i < w; ++i) {
-      const float lo = v[i], hi = v[i + w];
-      const float send = upper ? lo : hi;
-      const float keep = upper ? hi : lo;
-      v[i] = keep + __shfl_xor_sync(kFull, send, w);
-    }
-  }
-  return v[0];
-}
 
 // Cached keys of call row b (the same for all its KV heads). Bad metadata is
 // reported (once per row) and yields no keys.
@@ -125,12 +104,37 @@ __device__ __forceinline__ int unit_length(const CacheView& c, int b, int max_le
   }
 }
 
-template <int D, int GP, bool PAGED>
-__global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const SplitArgs a, int G) {
-  using Gm = Geo<D, GP>;
-  constexpr int LPK = Gm::LPK, KPS = Gm::KPS, J = Gm::J, KT = Gm::KT, SK = Gm::SK;
-  constexpr int SUB = Gm::SUB, NS = Gm::NS;
-  extern __shared__ __align__(16) uint8_t smem[];
+// First 16-slot block of a ring holding `n` valid slots before `head`.
+__device__ __forceinline__ int ring_first_block(int head, int n, int R) {
+  const int start = head - n < 0 ? head - n + R : head - n;
+  return start >> 4;
+}
+
+// 16-row groups of a unit with n cached keys.
+template <bool PAGED>
+__device__ __forceinline__ int unit_groups(const CacheView& c, int b, int n) {
+  if (n <= 0) return 0;
+  if constexpr (PAGED) {
+    const int gpp = (c.P + kGroup - 1) / kGroup;
+    const int full = n / c.P, rest = n - full * c.P;
+    return full * gpp + (rest + kGroup - 1) / kGroup;
+  } else {
+    const int R = c.R, nb = (R + kGroup - 1) / kGroup;
+    if (n >= R) return nb;
+    const int head = c.ring_head[b];
+    const int start = head - n < 0 ? head - n + R : head - n;
+    const int b0 = start >> 4, end = start + n - 1;
+    if (end < R) return (end >> 4) - b0 + 1;
+    return min(nb, nb - b0 + ((end - R) >> 4) + 1);  // wraps past the last slot
+  }
+}
+
+template <int D, int NT, bool PAGED>
+__global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_constant__ SplitArgs a, int G) {
+  using Gm = Geo<D, NT>;
+  constexpr int GP = Gm::GP, KSTEPS = Gm::KSTEPS, BOXES = Gm::BOXES, KG = Gm::KG, NS = Gm::NS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const CacheView& c = a.c;
   const int Hkv = a.Hkv, U = a.B * Hkv;
@@ -143,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const SplitAr
     const int b = u / Hkv;
     const int n = unit_length<PAGED>(c, b, a.max_len, cta == 0 && u - b * Hkv == 0, a.err);
     N[u] = n;
-    P[u + 1] = (n + SK - 1) / SK;
+    P[u + 1] = (unit_groups<PAGED>(c, b, n) + KG - 1) / KG;
   }
   if (threadIdx.x == 0) P[0] = 0;
   __syncthreads();
@@ -158,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const SplitAr
   const int span = g1 - g0;
   const int my_n = span > warp ? (span - warp + kWarps - 1) / kWarps : 0;
   uint8_t* wsm = smem + warp * NS * Gm::STAGE;
+  const uint32_t wsm_a = smem_addr(wsm);
   const uint32_t bar0 = smem_addr(smem + Gm::BAR_OFF) + warp * NS * 8;
   if (lane == 0) {
     for (int s = 0; s < NS; ++s) mbar_init(bar0 + 8 * s, 1);
@@ -173,44 +178,36 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const SplitAr
     while (P[u_iss + 1] <= g) ++u_iss;
     const int u = u_iss;
     const int b = u / Hkv, j = u - b * Hkv;
-    const int k0 = (g - P[u]) * SK;
-    const int cnt = min(SK, N[u] - k0);
+    const int n = N[u];
+    const int gb = (g - P[u]) * KG;
+    const int gn = min(KG, unit_groups<PAGED>(c, b, n) - gb);
     const uint32_t bar = bar0 + 8 * (it % NS);
-    const uint32_t kd = smem_addr(wsm + (it % NS) * Gm::STAGE);
-    const uint32_t vd = kd + Gm::TILE;
-    mbar_arrive_expect_tx(bar, 2u * cnt * Gm::ROW);
-    if constexpr (PAGED) {
-      const int32_t* bt = c.block_table + static_cast<int64_t>(b) * c.bt_stride;
-      int t = k0, done = 0;
-      while (t < k0 + cnt) {
-        const int pi = t / c.P;
-        const int off = t - pi * c.P;
-        int pg = bt[pi];
+    const uint32_t kd = wsm_a + (it % NS) * Gm::STAGE;
+    mbar_arrive_expect_tx(bar, 2u * gn * Gm::GBYTES);
+    for (int kg = 0; kg < gn; ++kg) {
+      const int gi = gb + kg;
+      int row0;
+      if constexpr (PAGED) {
+        const int gpp = (c.P + kGroup - 1) / kGroup;
+        const int pi = gi / gpp;
+        int pg = c.block_table[static_cast<int64_t>(b) * c.bt_stride + pi];
         if (pg < 0 || pg >= c.n_rows) {
           raise_error(a.err, ERR_INDEX);
           pg = 0;
         }
-        const int run = min(c.P - off, k0 + cnt - t);
-        const int64_t src = ((static_cast<int64_t>(pg) * Hkv + j) * c.P + off) * D;
-        bulk_copy_g2s(kd + done * Gm::ROW, c.k + src, run * Gm::ROW, bar, policy);
-        bulk_copy_g2s(vd + done * Gm::ROW, c.v + src, run * Gm::ROW, bar, policy);
-        t += run;
-        done += run;
+        row0 = (pg * Hkv + j) * c.P + (gi - pi * gpp) * kGroup;
+      } else {
+        const int nb = (c.R + kGroup - 1) / kGroup;
+        int pb = ring_first_block(c.ring_head[b], n, c.R) + gi;
+        if (pb >= nb) pb -= nb;
+        const int row = c.stream_rows ? c.stream_rows[b] : b;
+        row0 = (row * Hkv + j) * c.R + pb * kGroup;
       }
-    } else {
-      const int row = c.stream_rows ? c.stream_rows[b] : b;
-      const int n = N[u];
-      const int head = c.ring_head[b];
-      const int start = head - n < 0 ? head - n + c.R : head - n;
-      const int64_t base = (static_cast<int64_t>(row) * Hkv + j) * c.R * D;
-      int phys = start + k0;
-      if (phys >= c.R) phys -= c.R;
-      const int run1 = min(cnt, c.R - phys);
-      bulk_copy_g2s(kd, c.k + base + static_cast<int64_t>(phys) * D, run1 * Gm::ROW, bar, policy);
-      bulk_copy_g2s(vd, c.v + base + static_cast<int64_t>(phys) * D, run1 * Gm::ROW, bar, policy);
-      if (run1 < cnt) {
-        bulk_copy_g2s(kd + run1 * Gm::ROW, c.k + base, (cnt - run1) * Gm::ROW, bar, policy);
-        bulk_copy_g2s(vd + run1 * Gm::ROW, c.v + base, (cnt - run1) * Gm::ROW, bar, policy);
+#pragma unroll
+      for (int x = 0; x < BOXES; ++x) {
+        tma_load_2d(kd + kg * Gm::GBYTES + x * kBoxBytes, &a.tmap_k, 64 * x, row0, bar, policy);
+        tma_load_2d(kd + Gm::KHALF + kg * Gm::GBYTES + x * kBoxBytes, &a.tmap_v, 64 * x, row0, bar,
+                    policy);
       }
     }
   };
@@ -224,10 +221,25 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const SplitAr
 
   float* ML = reinterpret_cast<float*>(smem + Gm::ML_OFF);
   int* SLOT = reinterpret_cast<int*>(smem + Gm::SLOT_OFF);
-  float* psm = reinterpret_cast<float*>(smem + Gm::PSM_OFF) + warp * (32 + GP);
-  const int dl = (lane % LPK) * 8;
-  const int half = lane / LPK;                         // key of a warp-wide load held by this lane
-  const int key_s = ((lane % LPK) / GP) * KPS + half;  // sub-tile key of this lane's score
+
+  // Per-lane ldmatrix offsets inside a group's 2 KB boxes (128-byte swizzle:
+  // the 16-byte chunk index is XORed with the row mod 8). K (scores, A = K):
+  // matrix m = lane / 8 covers rows 8 * (m & 1) + 0..7 and chunk (m >> 1) of
+  // a k-step's pair of chunks. V (outputs, A = V^T, loaded transposed):
+  // matrix m covers rows 8 * (m >> 1) + 0..7 and chunk (m & 1).
+  const int lr = lane & 7, lm = lane >> 3;
+  uint32_t koff[4], voff[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int rk = lr + 8 * (lm & 1), rv = lr + 8 * (lm >> 1);
+    koff[q] = rk * 128 + (((2 * q + (lm >> 1)) ^ lr) << 4);
+    voff[q] = rv * 128 + (((2 * q + (lm & 1)) ^ lr) << 4);
+  }
+  const int fg = lane >> 2, fc = 2 * (lane & 3);  // fragment row group, column pair
+  // heads of this lane's score / output columns (e = 0, 1): hi/lo columns of
+  // one head are lanes l and l ^ 2 (NT == 1) or tiles 0 and 1 (NT == 2)
+  const int hbase = NT == 1 ? 2 * (lane & 1) : fc;
+  const bool lo_lane = NT == 1 && (lane & 2) != 0;
 
   bool failed = false;
   int it = 0;
@@ -237,35 +249,46 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const SplitAr
     if (P[u + 1] == P[u]) continue;  // a unit with no cached keys
     const int ge = min(g1, P[u + 1]);
     const int b = u / Hkv, j = u - b * Hkv;
+    const int n = N[u];
 
-    float q[GP][8];
+    // q^T as B fragments: column n = fg of tile t holds head (hi or lo part)
+    uint32_t qb[KSTEPS][NT][2];
 #pragma unroll
-    for (int g = 0; g < GP; ++g) {
-      if (g < G) {
-        const float* src = a.qhat + (static_cast<int64_t>(b) * Hkv * G + j * G + g) * D + dl;
-        const float4 x0 = *reinterpret_cast<const float4*>(src);
-        const float4 x1 = *reinterpret_cast<const float4*>(src + 4);
-        q[g][0] = x0.x; q[g][1] = x0.y; q[g][2] = x0.z; q[g][3] = x0.w;
-        q[g][4] = x1.x; q[g][5] = x1.y; q[g][6] = x1.z; q[g][7] = x1.w;
-      } else {
+    for (int t = 0; t < NT; ++t) {
+      const int head = NT == 1 ? (fg & 3) : fg;
+      const bool lo = NT == 1 ? fg >= 4 : t == 1;
+      const float* src = a.qhat + (static_cast<int64_t>(b) * Hkv * G + j * G + head) * D + fc;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) q[g][e] = 0.f;
+      for (int ks = 0; ks < KSTEPS; ++ks) {
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          float2 x = make_float2(0.f, 0.f);
+          if (head < G) x = *reinterpret_cast<const float2*>(src + ks * 16 + h2 * 8);
+          uint32_t hi, lw;
+          split_bf16x2(x.x, x.y, hi, lw);
+          qb[ks][t][h2] = lo ? lw : hi;
+        }
       }
     }
-    float o[GP][8];
+    float o[KSTEPS][NT][4];
 #pragma unroll
-    for (int g = 0; g < GP; ++g)
+    for (int mt = 0; mt < KSTEPS; ++mt)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[g][e] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f;
+      for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[mt][t][e] = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     int last_stage = -1;
+    const int ngroups = unit_groups<PAGED>(c, b, n);
+    int ring_b0 = 0;
+    if constexpr (!PAGED) ring_b0 = ring_first_block(c.ring_head[b], n, c.R);
 
     for (;;) {
       const int g = g0 + warp + kWarps * it;
       if (it >= my_n || g >= ge) break;
       const int stg = it % NS;
       if (!failed) {
-        // the whole warp agrees on the outcome, so the shuffles below stay converged
+        // the whole warp agrees on the outcome, so the collectives below stay converged
         const bool ok = __all_sync(kFull, mbar_wait_bounded(bar0 + 8 * stg, (it / NS) & 1));
         if (!ok) {
           failed = true;
@@ -273,80 +296,128 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const SplitAr
         }
       }
       if (!failed) {
-        const int nstage = min(SK, N[u] - (g - P[u]) * SK);
+        const int gb = (g - P[u]) * KG;
+        const int gn = min(KG, ngroups - gb);
 #pragma unroll 1
-        for (int sb = 0; sb < SUB; ++sb) {
-          const int nvalid = nstage - sb * KT;
-          if (nvalid <= 0) break;
-          const uint4* Ks = reinterpret_cast<const uint4*>(wsm + stg * Gm::STAGE) + sb * (KT * D / 8);
-          const uint4* Vs = Ks + Gm::TILE / 16;
-
-          // scores: J loads of 8 dims for GP heads, then the transposing reduction
-          float sp[J * GP];
-#pragma unroll
-          for (int jj = 0; jj < J; ++jj) {
-            float kf[8];
-            unpack8(Ks[jj * 32 + lane], kf);
-#pragma unroll
-            for (int h = 0; h < GP; ++h) {
-              float acc = q[h][0] * kf[0];
-#pragma unroll
-              for (int e = 1; e < 8; ++e) acc = fmaf(q[h][e], kf[e], acc);
-              sp[jj * GP + h] = acc;
-            }
-          }
-          float s = transpose_reduce<LPK>(sp, lane);
-          if (key_s >= nvalid) s = -INFINITY;
-
-          // online softmax (base 2): every lane holds one (key, head) score
-          float tmax = s;
-#pragma unroll
-          for (int w = GP; w < 32; w <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, w));
-          const float m_new = fmaxf(m_run, tmax);
-          const float corr = exp2_fast(m_run - m_new);
-          const float p = exp2_fast(s - m_new);
-          l_run = fmaf(l_run, corr, p);
-          m_run = m_new;
-          psm[lane] = p;
-          if (lane < GP) psm[32 + lane] = corr;
-          __syncwarp();
-#pragma unroll
-          for (int h = 0; h < GP; ++h) {
-            const float cr = psm[32 + h];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o[h][e] *= cr;
-          }
-          if (nvalid >= KT) {
-#pragma unroll
-            for (int jj = 0; jj < J; ++jj) {
-              float vf[8];
-              unpack8(Vs[jj * 32 + lane], vf);
-              const float* pp = psm + half * LPK + jj * GP;
-#pragma unroll
-              for (int h = 0; h < GP; ++h) {
-                const float ph = pp[h];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o[h][e] = fmaf(ph, vf[e], o[h][e]);
-              }
-            }
+        for (int kg = 0; kg < gn; ++kg) {
+          const uint32_t kbase = wsm_a + stg * Gm::STAGE + kg * Gm::GBYTES;
+          const uint32_t vbase = kbase + Gm::KHALF;
+          // ---- which of the group's 16 rows are valid keys
+          const int gi = gb + kg;
+          const int r = lane & 15;
+          bool valid;
+          if constexpr (PAGED) {
+            const int gpp = (c.P + kGroup - 1) / kGroup;
+            const int pi = gi / gpp, off = (gi - pi * gpp) * kGroup + r;
+            valid = off < c.P && pi * c.P + off < n;
           } else {
+            const int nb = (c.R + kGroup - 1) / kGroup;
+            int pb = ring_b0 + gi;
+            if (pb >= nb) pb -= nb;
+            const int slot = pb * kGroup + r;
+            int d = c.ring_head[b] - 1 - slot;
+            if (d < 0) d += c.R;
+            valid = slot < c.R && d < n;
+          }
+          const uint32_t mask = __ballot_sync(kFull, valid) & 0xffffu;
+          if (mask != 0xffffu) {
+            // zero the V rows of invalid keys (their probabilities are 0, but
+            // the rows may hold NaN and 0 * NaN is NaN)
+            uint8_t* vg = wsm + stg * Gm::STAGE + Gm::KHALF + kg * Gm::GBYTES;
+            for (int i = lane; i < kGroup * BOXES * 8; i += 32) {
+              const int row = i / (BOXES * 8), rest = i - row * (BOXES * 8);
+              if (!((mask >> row) & 1u))
+                *reinterpret_cast<uint4*>(vg + (rest >> 3) * kBoxBytes + row * 128 + (rest & 7) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();  // before the stage is refilled by TMA
+            __syncwarp();
+          }
+
+          // ---- scores S^T = K . Q^T (two accumulator chains)
+          float sacc[2][NT][4];
 #pragma unroll
-            for (int jj = 0; jj < J; ++jj) {
-              if (jj * KPS + half < nvalid) {
-                float vf[8];
-                unpack8(Vs[jj * 32 + lane], vf);
-                const float* pp = psm + half * LPK + jj * GP;
+          for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
-                for (int h = 0; h < GP; ++h) {
-                  const float ph = pp[h];
+            for (int t = 0; t < NT; ++t)
 #pragma unroll
-                  for (int e = 0; e < 8; ++e) o[h][e] = fmaf(ph, vf[e], o[h][e]);
-                }
-              }
+              for (int e = 0; e < 4; ++e) sacc[h2][t][e] = 0.f;
+#pragma unroll
+          for (int ks = 0; ks < KSTEPS; ++ks) {
+            uint32_t af[4];
+            ldsm_x4(kbase + (ks >> 2) * kBoxBytes + koff[ks & 3], af);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) mma_bf16(sacc[ks & 1][t], af, qb[ks][t][0], qb[ks][t][1]);
+          }
+          // full scores of heads hbase + e at keys fg (i = e) and fg + 8 (i = 2 + e)
+          float s[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (NT == 1) {
+              const float x = sacc[0][0][i] + sacc[1][0][i];
+              s[i] = x + __shfl_xor_sync(kFull, x, 2);
+            } else {
+              s[i] = (sacc[0][0][i] + sacc[1][0][i]) + (sacc[0][NT - 1][i] + sacc[1][NT - 1][i]);
             }
           }
-          __syncwarp();
+          if (!((mask >> fg) & 1u)) s[0] = s[1] = -INFINITY;
+          if (!((mask >> (fg + 8)) & 1u)) s[2] = s[3] = -INFINITY;
+
+          // ---- online softmax (base 2), per head over the 16 keys
+          float corr[2], p[4];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float mx = fmaxf(s[e], s[2 + e]);
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+            const float m_new = fmaxf(m_run[e], mx);
+            const float ms = m_new == -INFINITY ? 0.f : m_new;
+            corr[e] = exp2_fast(m_run[e] - ms);
+            p[e] = exp2_fast(s[e] - ms);
+            p[2 + e] = exp2_fast(s[2 + e] - ms);
+            l_run[e] = fmaf(l_run[e], corr[e], p[e] + p[2 + e]);
+            m_run[e] = m_new;
+          }
+          if (__any_sync(kFull, corr[0] != 1.f || corr[1] != 1.f)) {
+#pragma unroll
+            for (int mt = 0; mt < KSTEPS; ++mt)
+#pragma unroll
+              for (int t = 0; t < NT; ++t) {
+                o[mt][t][0] *= corr[0];
+                o[mt][t][1] *= corr[1];
+                o[mt][t][2] *= corr[0];
+                o[mt][t][3] *= corr[1];
+              }
+          }
+
+          // ---- P^T as B fragments (hi and lo bf16 parts), via 8x8 transposes
+          uint32_t pb[NT][2];
+          {
+            uint32_t h01, l01, h23, l23;
+            split_bf16x2(p[0], p[1], h01, l01);
+            split_bf16x2(p[2], p[3], h23, l23);
+            if (NT == 1) {
+              pb[0][0] = movm_t(lo_lane ? l01 : h01);
+              pb[0][1] = movm_t(lo_lane ? l23 : h23);
+            } else {
+              pb[0][0] = movm_t(h01);
+              pb[0][1] = movm_t(h23);
+              pb[NT - 1][0] = movm_t(l01);
+              pb[NT - 1][1] = movm_t(l23);
+            }
+          }
+
+          // ---- outputs O^T += V^T . P^T
+#pragma unroll
+          for (int mt = 0; mt < KSTEPS; ++mt) {
+            uint32_t af[4];
+            ldsm_x4_t(vbase + (mt >> 2) * kBoxBytes + voff[mt & 3], af);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) mma_bf16(o[mt][t], af, pb[t][0], pb[t][1]);
+          }
         }
+        __syncwarp();
       }
       last_stage = stg;
       // Refill this stage with the warp's tile NS ahead. The warp's last tile
@@ -362,29 +433,41 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const SplitAr
       ++it;
     }
 
-    // ---- merge the warps' states for this segment
+    // ---- this warp's state: l summed over the lanes of a head, O^T to the
+    // merge buffer as o[head][dim] (hi + lo columns)
 #pragma unroll
-    for (int w = GP; w < 32; w <<= 1) l_run += __shfl_xor_sync(kFull, l_run, w);
-#pragma unroll
-    for (int w = LPK; w < 32; w <<= 1)
-#pragma unroll
-      for (int h = 0; h < GP; ++h)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[h][e] += __shfl_xor_sync(kFull, o[h][e], w);
-    if (last_stage >= 0 && lane < LPK) {
-      float* os = reinterpret_cast<float*>(wsm + last_stage * Gm::STAGE);
-#pragma unroll
-      for (int h = 0; h < GP; ++h) {
-        *reinterpret_cast<float4*>(os + h * D + dl) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
-        *reinterpret_cast<float4*>(os + h * D + dl + 4) = make_float4(o[h][4], o[h][5], o[h][6], o[h][7]);
-      }
+    for (int e = 0; e < 2; ++e) {
+      l_run[e] += __shfl_xor_sync(kFull, l_run[e], 4);
+      l_run[e] += __shfl_xor_sync(kFull, l_run[e], 8);
+      l_run[e] += __shfl_xor_sync(kFull, l_run[e], 16);
     }
-    if (lane < GP) {
-      ML[warp * 2 * GP + lane] = last_stage >= 0 ? m_run : -INFINITY;
-      ML[warp * 2 * GP + GP + lane] = last_stage >= 0 ? l_run : 0.f;
+    if (last_stage >= 0) {
+      float* os = reinterpret_cast<float*>(wsm + last_stage * Gm::STAGE);
+      const bool writer = NT == 2 || !lo_lane;
+#pragma unroll
+      for (int mt = 0; mt < KSTEPS; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float v;
+          if (NT == 1) {
+            v = o[mt][0][i] + __shfl_xor_sync(kFull, o[mt][0][i], 2);
+          } else {
+            v = o[mt][0][i] + o[mt][NT - 1][i];
+          }
+          if (writer) os[(hbase + (i & 1)) * D + mt * 16 + fg + 8 * (i >> 1)] = v;
+        }
+      fence_proxy_async_smem();  // the buffer is refilled by TMA after the merge
+    }
+    if (fg == 0 && (NT == 2 || !lo_lane)) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        ML[warp * 2 * GP + hbase + e] = last_stage >= 0 ? m_run[e] : -INFINITY;
+        ML[warp * 2 * GP + GP + hbase + e] = last_stage >= 0 ? l_run[e] : 0.f;
+      }
     }
     if (lane == 0) SLOT[warp] = last_stage;
     __syncthreads();
+    // ---- merge the warps' states for this segment into its partial slot
     const int slot = first_seg ? cta : NC + u;
     float* dst = a.part + static_cast<int64_t>(slot) * (GP * (D + 2));
     for (int e = threadIdx.x; e < GP * D; e += kThreads) {
@@ -613,617 +696,99 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const CombineArgs a
   }
 }
 
-// ---------------------------------------------------------------- one-launch decode
+// ---------------------------------------------------------------- launch
 
-template <int D, int GP>
-struct FGeo {
-  using Gm = Geo<D, GP>;
-  static constexpr int QS_OFF = Gm::TAB_OFF;                    // float [GP][D]: rotated q of the unit
-  static constexpr int SN_OFF = QS_OFF + GP * D * 4;            // float [GP]: new-token scores
-  static constexpr int FLAG_OFF = SN_OFF + GP * 4;              // int: "this CTA combines"
-  static constexpr int TAB_OFF = (FLAG_OFF + 4 + 15) / 16 * 16;  // int P[U+1], N[U]
-  static constexpr int SMEM_MAX = TAB_OFF + (2 * kMaxUnits + 1) * 4;
-};
-
-// Rotate the G query heads of unit (b, j) into qs[GP][D] (fp32, pre-scaled;
-// heads >= G are zero). All threads of the CTA take part, one pair at a time,
-// each pair's cos and sin shared by the heads.
-template <int D, int GP>
-__device__ __forceinline__ void fused_rope_q(const FusedArgs& a, int b, int j, float* qs) {
-  const int G = a.G, Hq = a.Hkv * G, half = a.r / 2;
-  const int64_t pos = a.pos[b];
-  const uint16_t* src = a.q + (static_cast<int64_t>(b) * Hq + j * G) * D;
-  for (int p = threadIdx.x; p < D / 2; p += kThreads) {
-    const int d0 = p < half ? p : a.r + 2 * (p - half);
-    const int d1 = p < half ? p + half : d0 + 1;
-    float c = 1.f, s = 0.f;
-    if (p < half) rope_cos_sin(pos, a.rope_step[p], c, s);
-#pragma unroll
-    for (int g = 0; g < GP; ++g) {
-      float o0 = 0.f, o1 = 0.f;
-      if (g < G) {
-        const float x = bf16_to_f32(src[g * D + d0]), y = bf16_to_f32(src[g * D + d1]);
-        if (p < half) {
-          o0 = fmaf(x, c, -y * s) * a.q_scale;
-          o1 = fmaf(y, c, x * s) * a.q_scale;
-        } else {
-          o0 = x * a.q_scale;
-          o1 = y * a.q_scale;
-        }
-      }
-      qs[g * D + d0] = o0;
-      qs[g * D + d1] = o1;
-    }
-  }
-}
-
-// The bit-exact K entry of unit (b, j): bf16_RNE(x*c - y*s) evaluated in fp64
-// (both products exact, one rounding) with the fp32 cos and sin of
-// rope_cos_sin. Written to the workspace.
-template <int D>
-__device__ __forceinline__ void fused_k_entry(const FusedArgs& a, int b, int j, uint16_t* dst) {
-  const int half = a.r / 2;
-  const uint16_t* src = a.k_new + (static_cast<int64_t>(b) * a.Hkv + j) * D;
-  const int64_t pos = a.pos[b];
-  for (int p = threadIdx.x; p < D / 2; p += kThreads) {
-    const int d0 = p < half ? p : a.r + 2 * (p - half);
-    const int d1 = p < half ? p + half : d0 + 1;
-    if (p < half) {
-      float cf, sf;
-      rope_cos_sin(pos, a.rope_step[p], cf, sf);
-      const double c64 = cf, s64 = sf;
-      const double x = bf16_to_f32(src[d0]), y = bf16_to_f32(src[d1]);
-      dst[d0] = f64_to_bf16(__dsub_rn(__dmul_rn(x, c64), __dmul_rn(y, s64)));
-      dst[d1] = f64_to_bf16(__dadd_rn(__dmul_rn(y, c64), __dmul_rn(x, s64)));
-    } else {
-      dst[d0] = src[d0];
-      dst[d1] = src[d1];
-    }
-  }
-}
-
-// Number of split CTAs whose ranges hold tiles of the unit spanning global
-// tiles [p0, p1), and the first of them (CTA of tile x: floor(((x+1)NC-1)/T)).
-__device__ __forceinline__ int unit_segments(int p0, int p1, int T, int NC, int& c_lo, int& first_slot, int u) {
-  if (p1 <= p0) return 0;
-  c_lo = static_cast<int>((static_cast<int64_t>(p0 + 1) * NC - 1) / T);
-  const int c_hi = static_cast<int>((static_cast<int64_t>(p1) * NC - 1) / T);
-  first_slot = static_cast<int>(static_cast<int64_t>(c_lo) * T / NC) == p0 ? c_lo : NC + u;
-  int n = 1;
-  for (int c = c_lo + 1; c <= c_hi; ++c)
-    if (static_cast<int64_t>(c) * T / NC < static_cast<int64_t>(c + 1) * T / NC) ++n;
-  return n;
-}
-
-// Combine unit u = (b, j) from its segment partials (none for an empty unit):
-// new-token join in score space, gate, fp32 store, write-back of the entry.
-// All threads of the CTA take part; qs holds the unit's rotated q.
-template <int D, int GP, bool PAGED>
-__device__ void fused_combine(const FusedArgs& a, int u, const int* P, int T, const float* qs, float* sn) {
-  const int Hkv = a.Hkv, G = a.G, Hq = Hkv * G, NC = a.ctas;
-  const int b = u / Hkv, j = u - b * Hkv;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const CacheView& c = a.c;
-  const uint16_t* kh = a.khat + static_cast<int64_t>(u) * D;
-  // new-token scores (base 2), one warp per head
-  for (int g = warp; g < G; g += kWarps) {
-    float dot = 0.f;
-    for (int d = lane; d < D; d += 32) dot = fmaf(qs[g * D + d], bf16_to_f32(kh[d]), dot);
-#pragma unroll
-    for (int w = 16; w >= 1; w >>= 1) dot += __shfl_xor_sync(kFull, dot, w);
-    if (lane == 0) sn[g] = dot;
-  }
-  __syncthreads();
-  int c_lo = 0, first_slot = 0;
-  const int p0 = P[u], p1 = P[u + 1];
-  const int nseg = unit_segments(p0, p1, T, NC, c_lo, first_slot, u);
-  const int c_hi = p1 > p0 ? static_cast<int>((static_cast<int64_t>(p1) * NC - 1) / T) : c_lo - 1;
-  const int stride = GP * (D + 2);
-  (void)nseg;
-  for (int e = threadIdx.x * 4; e < G * D; e += kThreads * 4) {
-    const int g = e / D, d = e - g * D;
-    const int h = j * G + g;
-    float M = sn[g];
-    for (int cc = c_lo; cc <= c_hi; ++cc) {
-      const bool first = cc == c_lo;
-      if (!first && !(static_cast<int64_t>(cc) * T / NC < static_cast<int64_t>(cc + 1) * T / NC)) continue;
-      const float* pk = a.part + static_cast<int64_t>(first ? first_slot : cc) * stride;
-      M = fmaxf(M, pk[GP * D + g]);
-    }
-    float L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int cc = c_lo; cc <= c_hi; ++cc) {
-      const bool first = cc == c_lo;
-      if (!first && !(static_cast<int64_t>(cc) * T / NC < static_cast<int64_t>(cc + 1) * T / NC)) continue;
-      const float* pk = a.part + static_cast<int64_t>(first ? first_slot : cc) * stride;
-      const float w = exp2_fast(pk[GP * D + g] - M);
-      L = fmaf(w, pk[GP * D + GP + g], L);
-      const float4 v = *reinterpret_cast<const float4*>(pk + g * D + d);
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
-    }
-    const float wn = exp2_fast(sn[g] - M);
-    L += wn;
-    const uint2 vw = *reinterpret_cast<const uint2*>(a.v_new + (static_cast<int64_t>(b) * Hkv + j) * D + d);
-    acc.x = fmaf(wn, bf16_lo(vw.x), acc.x);
-    acc.y = fmaf(wn, bf16_hi(vw.x), acc.y);
-    acc.z = fmaf(wn, bf16_lo(vw.y), acc.z);
-    acc.w = fmaf(wn, bf16_hi(vw.y), acc.w);
-    float sig = 1.f;
-    if (a.gate) sig = 1.f / (1.f + expf(-bf16_to_f32(a.gate[static_cast<int64_t>(b) * Hq + h])));
-    const float scale = sig / L;
-    *reinterpret_cast<float4*>(a.out + (static_cast<int64_t>(b) * Hq + h) * D + d) =
-        make_float4(acc.x * scale, acc.y * scale, acc.z * scale, acc.w * scale);
-  }
-  // write-back of the new entry: every segment of this unit has finished reading
-  if (a.write_back) {
-    int64_t wb = -1;
-    if constexpr (PAGED) {
-      const int n = min(max(c.seq_len[b], 0), min(a.max_len, c.bt_stride * c.P));
-      const int pi = n / c.P;
-      const int pg = pi < c.bt_stride ? c.block_table[static_cast<int64_t>(b) * c.bt_stride + pi] : -1;
-      if (pg >= 0 && pg < c.n_rows)
-        wb = ((static_cast<int64_t>(pg) * Hkv + j) * c.P + n % c.P) * D;
-      else if (threadIdx.x == 0)
-        raise_error(a.err, ERR_INDEX);
-    } else {
-      const int row = c.stream_rows ? c.stream_rows[b] : b;
-      const int head = c.ring_head[b], cnt = c.ring_count[b];
-      if (!(row < 0 || row >= c.n_rows || head < 0 || head >= c.R || cnt < 0 || cnt > c.R))
-        wb = ((static_cast<int64_t>(row) * Hkv + j) * c.R + head) * D;
-    }
-    if (wb >= 0) {
-      const uint16_t* vn = a.v_new + (static_cast<int64_t>(b) * Hkv + j) * D;
-      for (int d = threadIdx.x * 4; d < D; d += kThreads * 4) {
-        *reinterpret_cast<uint2*>(c.k + wb + d) = *reinterpret_cast<const uint2*>(kh + d);
-        *reinterpret_cast<uint2*>(c.v + wb + d) = *reinterpret_cast<const uint2*>(vn + d);
-      }
-    }
-  }
-  if (threadIdx.x == 0) a.counters[u] = 0;
-  __syncthreads();
-}
-
-template <int D, int GP, bool PAGED>
-__global__ void __launch_bounds__(kThreads, 2) decode_fused_kernel(const FusedArgs a) {
-  using Gm = Geo<D, GP>;
-  using F = FGeo<D, GP>;
-  constexpr int LPK = Gm::LPK, KPS = Gm::KPS, J = Gm::J, KT = Gm::KT, SK = Gm::SK;
-  constexpr int SUB = Gm::SUB, NS = Gm::NS;
-  extern __shared__ __align__(16) uint8_t smem[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const CacheView& c = a.c;
-  const int Hkv = a.Hkv, U = a.B * Hkv, G = a.G;
-  const int NC = gridDim.x, cta = blockIdx.x;
-  int* P = reinterpret_cast<int*>(smem + F::TAB_OFF);  // [U + 1] tile prefix over units
-  int* N = P + U + 1;                                   // [U] cached keys per unit
-  float* qs = reinterpret_cast<float*>(smem + F::QS_OFF);
-  float* sn = reinterpret_cast<float*>(smem + F::SN_OFF);
-  int* flag = reinterpret_cast<int*>(smem + F::FLAG_OFF);
-
-  // ---- unit table from caller metadata
-  for (int u = threadIdx.x; u < U; u += kThreads) {
-    const int b = u / Hkv;
-    const int n = unit_length<PAGED>(c, b, a.max_len, cta == 0 && u - b * Hkv == 0, a.err);
-    N[u] = n;
-    P[u + 1] = (n + SK - 1) / SK;
-  }
-  if (threadIdx.x == 0) P[0] = 0;
-  __syncthreads();
-  block_scan_inclusive<kThreads>(P + 1, U);
-  const int T = P[U];
-  const int g0 = static_cast<int>(static_cast<int64_t>(cta) * T / NC);
-  const int g1 = static_cast<int>(static_cast<int64_t>(cta + 1) * T / NC);
-  const int span = g1 - g0;
-  const int my_n = span > warp ? (span - warp + kWarps - 1) / kWarps : 0;
-  uint8_t* wsm = smem + warp * NS * Gm::STAGE;
-  const uint32_t bar0 = smem_addr(smem + Gm::BAR_OFF) + warp * NS * 8;
-  if (lane == 0) {
-    for (int s = 0; s < NS; ++s) mbar_init(bar0 + 8 * s, 1);
-    fence_mbar_init();
-  }
-  __syncwarp();
-
-  // The previous call may still be writing the cache (its new entries) and
-  // reading the workspace: everything below waits for it.
-  pdl_wait();
-  pdl_trigger();
-
-  const uint64_t policy = l2_evict_first_policy();
-  int u_iss = my_n > 0 ? unit_of(P, U, g0 + warp) : 0;
-  auto issue = [&](int it) {
-    const int g = g0 + warp + kWarps * it;
-    while (P[u_iss + 1] <= g) ++u_iss;
-    const int u = u_iss;
-    const int b = u / Hkv, j = u - b * Hkv;
-    const int k0 = (g - P[u]) * SK;
-    const int cnt = min(SK, N[u] - k0);
-    const uint32_t bar = bar0 + 8 * (it % NS);
-    const uint32_t kd = smem_addr(wsm + (it % NS) * Gm::STAGE);
-    const uint32_t vd = kd + Gm::TILE;
-    mbar_arrive_expect_tx(bar, 2u * cnt * Gm::ROW);
-    if constexpr (PAGED) {
-      const int32_t* bt = c.block_table + static_cast<int64_t>(b) * c.bt_stride;
-      int t = k0, done = 0;
-      while (t < k0 + cnt) {
-        const int pi = t / c.P;
-        const int off = t - pi * c.P;
-        int pg = bt[pi];
-        if (pg < 0 || pg >= c.n_rows) {
-          raise_error(a.err, ERR_INDEX);
-          pg = 0;
-        }
-        const int run = min(c.P - off, k0 + cnt - t);
-        const int64_t src = ((static_cast<int64_t>(pg) * Hkv + j) * c.P + off) * D;
-        bulk_copy_g2s(kd + done * Gm::ROW, c.k + src, run * Gm::ROW, bar, policy);
-        bulk_copy_g2s(vd + done * Gm::ROW, c.v + src, run * Gm::ROW, bar, policy);
-        t += run;
-        done += run;
-      }
-    } else {
-      const int row = c.stream_rows ? c.stream_rows[b] : b;
-      const int n = N[u];
-      const int head = c.ring_head[b];
-      const int start = head - n < 0 ? head - n + c.R : head - n;
-      const int64_t base = (static_cast<int64_t>(row) * Hkv + j) * c.R * D;
-      int phys = start + k0;
-      if (phys >= c.R) phys -= c.R;
-      const int run1 = min(cnt, c.R - phys);
-      bulk_copy_g2s(kd, c.k + base + static_cast<int64_t>(phys) * D, run1 * Gm::ROW, bar, policy);
-      bulk_copy_g2s(vd, c.v + base + static_cast<int64_t>(phys) * D, run1 * Gm::ROW, bar, policy);
-      if (run1 < cnt) {
-        bulk_copy_g2s(kd + run1 * Gm::ROW, c.k + base, (cnt - run1) * Gm::ROW, bar, policy);
-        bulk_copy_g2s(vd + run1 * Gm::ROW, c.v + base, (cnt - run1) * Gm::ROW, bar, policy);
-      }
-    }
-  };
-  if (lane == 0) {
-    const int pre = my_n < NS ? my_n : NS;
-    for (int it = 0; it < pre; ++it) issue(it);
-  }
-
-  float* ML = reinterpret_cast<float*>(smem + Gm::ML_OFF);
-  int* SLOT = reinterpret_cast<int*>(smem + Gm::SLOT_OFF);
-  float* psm = reinterpret_cast<float*>(smem + Gm::PSM_OFF) + warp * (32 + GP);
-  const int dl = (lane % LPK) * 8;
-  const int half = lane / LPK;
-  const int key_s = ((lane % LPK) / GP) * KPS + half;
-
-  bool failed = false;
-  int it = 0;
-  int deferred = -1;
-  bool first_seg = true;
-  for (int u = span > 0 ? unit_of(P, U, g0) : U; u < U && P[u] < g1; ++u) {
-    if (P[u + 1] == P[u]) continue;  // a unit with no cached keys
-    const int ge = min(g1, P[u + 1]);
-    const int b = u / Hkv, j = u - b * Hkv;
-
-    // the unit's rotated q; the CTA holding the unit's first tile also writes
-    // the unit's K entry (read by whichever CTA combines the unit)
-    fused_rope_q<D, GP>(a, b, j, qs);
-    if (P[u] >= g0) fused_k_entry<D>(a, b, j, a.khat + static_cast<int64_t>(u) * D);
-    __syncthreads();
-    // packed fp32 pairs: the FMAs below are Blackwell's two-wide FFMA2
-    float2 q2[GP][4];
-#pragma unroll
-    for (int g = 0; g < GP; ++g) {
-      const float4 x0 = *reinterpret_cast<const float4*>(qs + g * D + dl);
-      const float4 x1 = *reinterpret_cast<const float4*>(qs + g * D + dl + 4);
-      q2[g][0] = make_float2(x0.x, x0.y); q2[g][1] = make_float2(x0.z, x0.w);
-      q2[g][2] = make_float2(x1.x, x1.y); q2[g][3] = make_float2(x1.z, x1.w);
-    }
-    float2 o2[GP][4];
-#pragma unroll
-    for (int g = 0; g < GP; ++g)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o2[g][e] = make_float2(0.f, 0.f);
-    float m_run = -INFINITY, l_run = 0.f;
-    int last_stage = -1;
-
-    for (;;) {
-      const int g = g0 + warp + kWarps * it;
-      if (it >= my_n || g >= ge) break;
-      const int stg = it % NS;
-      if (!failed) {
-        const bool ok = __all_sync(kFull, mbar_wait_bounded(bar0 + 8 * stg, (it / NS) & 1));
-        if (!ok) {
-          failed = true;
-          if (lane == 0) raise_error(a.err, ERR_TIMEOUT);
-        }
-      }
-      if (!failed) {
-        const int nstage = min(SK, N[u] - (g - P[u]) * SK);
-#pragma unroll 1
-        for (int sb = 0; sb < SUB; ++sb) {
-          const int nvalid = nstage - sb * KT;
-          if (nvalid <= 0) break;
-          const uint4* Ks = reinterpret_cast<const uint4*>(wsm + stg * Gm::STAGE) + sb * (KT * D / 8);
-          const uint4* Vs = Ks + Gm::TILE / 16;
-          float sp[J * GP];
-#pragma unroll
-          for (int jj = 0; jj < J; ++jj) {
-            float2 k2[4];
-            unpack8x2(Ks[jj * 32 + lane], k2);
-#pragma unroll
-            for (int h = 0; h < GP; ++h) {
-              float2 a2 = __fmul2_rn(q2[h][0], k2[0]);
-              a2 = __ffma2_rn(q2[h][1], k2[1], a2);
-              a2 = __ffma2_rn(q2[h][2], k2[2], a2);
-              a2 = __ffma2_rn(q2[h][3], k2[3], a2);
-              sp[jj * GP + h] = a2.x + a2.y;
-            }
-          }
-          float s = transpose_reduce<LPK>(sp, lane);
-          if (key_s >= nvalid) s = -INFINITY;
-          float tmax = s;
-#pragma unroll
-          for (int w = GP; w < 32; w <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, w));
-          const float m_new = fmaxf(m_run, tmax);
-          const float corr = exp2_fast(m_run - m_new);
-          const float p = exp2_fast(s - m_new);
-          l_run = fmaf(l_run, corr, p);
-          m_run = m_new;
-          psm[lane] = p;
-          if (lane < GP) psm[32 + lane] = corr;
-          __syncwarp();
-          // rescale only when some head's running maximum moved
-          if (__any_sync(kFull, corr != 1.f)) {
-#pragma unroll
-            for (int h = 0; h < GP; ++h) {
-              const float cr = psm[32 + h];
-              const float2 c2 = make_float2(cr, cr);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) o2[h][e] = __fmul2_rn(o2[h][e], c2);
-            }
-          }
-          if (nvalid >= KT) {
-#pragma unroll
-            for (int jj = 0; jj < J; ++jj) {
-              float2 v2[4];
-              unpack8x2(Vs[jj * 32 + lane], v2);
-              const float* pp = psm + half * LPK + jj * GP;
-#pragma unroll
-              for (int h = 0; h < GP; ++h) {
-                const float2 p2 = make_float2(pp[h], pp[h]);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) o2[h][e] = __ffma2_rn(p2, v2[e], o2[h][e]);
-              }
-            }
-          } else {
-#pragma unroll
-            for (int jj = 0; jj < J; ++jj) {
-              if (jj * KPS + half < nvalid) {
-                float2 v2[4];
-                unpack8x2(Vs[jj * 32 + lane], v2);
-                const float* pp = psm + half * LPK + jj * GP;
-#pragma unroll
-                for (int h = 0; h < GP; ++h) {
-                  const float2 p2 = make_float2(pp[h], pp[h]);
-#pragma unroll
-                  for (int e = 0; e < 4; ++e) o2[h][e] = __ffma2_rn(p2, v2[e], o2[h][e]);
-                }
-              }
-            }
-          }
-          __syncwarp();
-        }
-      }
-      last_stage = stg;
-      if (it + NS < my_n) {
-        if (g + kWarps >= ge) {
-          deferred = it + NS;
-        } else if (lane == 0 && !failed) {
-          fence_proxy_async_smem();
-          issue(it + NS);
-        }
-      }
-      ++it;
-    }
-
-    // ---- merge the warps' states for this segment into its partial slot
-#pragma unroll
-    for (int w = GP; w < 32; w <<= 1) l_run += __shfl_xor_sync(kFull, l_run, w);
-#pragma unroll
-    for (int w = LPK; w < 32; w <<= 1)
-#pragma unroll
-      for (int h = 0; h < GP; ++h)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          o2[h][e].x += __shfl_xor_sync(kFull, o2[h][e].x, w);
-          o2[h][e].y += __shfl_xor_sync(kFull, o2[h][e].y, w);
-        }
-    if (last_stage >= 0 && lane < LPK) {
-      float* os = reinterpret_cast<float*>(wsm + last_stage * Gm::STAGE);
-#pragma unroll
-      for (int h = 0; h < GP; ++h) {
-        *reinterpret_cast<float4*>(os + h * D + dl) = make_float4(o2[h][0].x, o2[h][0].y, o2[h][1].x, o2[h][1].y);
-        *reinterpret_cast<float4*>(os + h * D + dl + 4) = make_float4(o2[h][2].x, o2[h][2].y, o2[h][3].x, o2[h][3].y);
-      }
-    }
-    if (lane < GP) {
-      ML[warp * 2 * GP + lane] = last_stage >= 0 ? m_run : -INFINITY;
-      ML[warp * 2 * GP + GP + lane] = last_stage >= 0 ? l_run : 0.f;
-    }
-    if (lane == 0) SLOT[warp] = last_stage;
-    __syncthreads();
-    const int slot = first_seg ? cta : NC + u;
-    float* dst = a.part + static_cast<int64_t>(slot) * (GP * (D + 2));
-    for (int e = threadIdx.x; e < GP * D; e += kThreads) {
-      const int h = e / D;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ML[w * 2 * GP + h]);
-      float acc = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          const int st = SLOT[w];
-          if (st >= 0) {
-            const float* os = reinterpret_cast<const float*>(smem + (w * NS + st) * Gm::STAGE);
-            acc = fmaf(exp2_fast(ML[w * 2 * GP + h] - M), os[e], acc);
-          }
-        }
-      }
-      dst[e] = acc;
-    }
-    if (threadIdx.x < GP) {
-      const int h = threadIdx.x;
-      float M = -INFINITY;
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ML[w * 2 * GP + h]);
-      float L = 0.f;
-      if (M != -INFINITY)
-        for (int w = 0; w < kWarps; ++w) L = fmaf(exp2_fast(ML[w * 2 * GP + h] - M), ML[w * 2 * GP + GP + h], L);
-      dst[GP * D + h] = M;
-      dst[GP * D + GP + h] = L;
-    }
-    // count this segment; the CTA finishing the unit's last segment combines it
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      int c_lo = 0, fs = 0;
-      const int nseg = unit_segments(P[u], P[u + 1], T, NC, c_lo, fs, u);
-      *flag = atomicAdd(a.counters + u, 1) == nseg - 1;
-    }
-    __syncthreads();
-    if (deferred >= 0) {
-      if (lane == 0 && !failed) {
-        fence_proxy_async_smem();
-        issue(deferred);
-      }
-      deferred = -1;
-    }
-    if (*flag) {
-      __threadfence();
-      fused_combine<D, GP, PAGED>(a, u, P, T, qs, sn);
-    }
-    first_seg = false;
-  }
-
-  // units with no cached keys have no segments: CTA u % NC combines them
-  for (int u = cta; u < U; u += NC) {
-    if (N[u] != 0) continue;
-    const int b = u / Hkv, j = u - b * Hkv;
-    fused_rope_q<D, GP>(a, b, j, qs);
-    fused_k_entry<D>(a, b, j, a.khat + static_cast<int64_t>(u) * D);
-    __threadfence();
-    __syncthreads();
-    fused_combine<D, GP, PAGED>(a, u, P, T, qs, sn);
-  }
-}
-
-template <int D, int GP, bool PAGED>
-cudaError_t fused_launch(const FusedArgs& a, cudaStream_t s) {
-  using F = FGeo<D, GP>;
-  auto k = decode_fused_kernel<D, GP, PAGED>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, F::SMEM_MAX);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  const size_t smem = F::TAB_OFF + (2 * a.B * a.Hkv + 1) * sizeof(int);
-  return launch_pdl(k, dim3(a.ctas), dim3(kThreads), smem, s, a);
-}
-
-template <int D, int GP>
-cudaError_t fused_dispatch(const FusedArgs& a, cudaStream_t s) {
-  return a.c.paged ? fused_launch<D, GP, true>(a, s) : fused_launch<D, GP, false>(a, s);
-}
-
-template <int D, int GP, bool PAGED>
+template <int D, int NT, bool PAGED>
 cudaError_t split_launch(const SplitArgs& a, int G, cudaStream_t s) {
-  using Gm = Geo<D, GP>;
-  auto k = decode_split_kernel<D, GP, PAGED>;
+  using Gm = Geo<D, NT>;
+  auto k = decode_split_kernel<D, NT, PAGED>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM_MAX);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const size_t smem = Gm::TAB_OFF + (2 * a.B * a.Hkv + 1) * sizeof(int);
+  const size_t smem = 1024 + Gm::TAB_OFF + (2 * a.B * a.Hkv + 1) * sizeof(int);
   return launch_pdl(k, dim3(a.ctas), dim3(kThreads), smem, s, a, G);
 }
 
-template <int D, int GP>
+template <int D, int NT>
 cudaError_t split_dispatch_paged(const SplitArgs& a, int G, cudaStream_t s) {
-  return a.c.paged ? split_launch<D, GP, true>(a, G, s) : split_launch<D, GP, false>(a, G, s);
+  return a.c.paged ? split_launch<D, NT, true>(a, G, s) : split_launch<D, NT, false>(a, G, s);
 }
 
-int padded_group(int G) { return G <= 2 ? 2 : (G <= 4 ? 4 : (G <= 8 ? 8 : 0)); }
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-template <int D>
-int geo_smem_max(int GP) {
-  return GP == 2 ? Geo<D, 2>::SMEM_MAX : GP == 4 ? Geo<D, 4>::SMEM_MAX : GP == 8 ? Geo<D, 8>::SMEM_MAX : 0;
-}
-template <int D>
-int geo_stage_keys(int GP) {
-  return GP == 2 ? Geo<D, 2>::SK : GP == 4 ? Geo<D, 4>::SK : GP == 8 ? Geo<D, 8>::SK : 0;
+// The driver's tensor-map encoder, looked up once through the runtime.
+EncodeTiledFn encode_tiled() {
+  static const EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
 }
 
 }  // namespace
 
+cudaError_t encode_cache_maps(const CacheView& c, int Hkv, int D, CUtensorMap* k, CUtensorMap* v) {
+  const EncodeTiledFn fn = encode_tiled();
+  if (!fn) return cudaErrorNotSupported;
+  const uint64_t rows = static_cast<uint64_t>(c.n_rows) * Hkv * (c.paged ? c.P : c.R);
+  if (rows == 0 || rows > 0x7fffffffull) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), rows};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
+  const cuuint32_t box[2] = {64, kGroup};
+  const cuuint32_t estride[2] = {1, 1};
+  for (int i = 0; i < 2; ++i) {
+    const CUresult r = fn(i ? v : k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, i ? c.v : c.k, dims, strides,
+                          box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t launch_decode_split(const SplitArgs& a, int D, int G, cudaStream_t s) {
-  const int GP = padded_group(G);
+  const int GP = decode_group_pad(G);
   if (a.B * a.Hkv > kMaxUnits) return cudaErrorNotSupported;
   if (D == 256) {
-    if (GP == 2) return split_dispatch_paged<256, 2>(a, G, s);
-    if (GP == 4) return split_dispatch_paged<256, 4>(a, G, s);
-    if (GP == 8) return split_dispatch_paged<256, 8>(a, G, s);
+    if (GP == 4) return split_dispatch_paged<256, 1>(a, G, s);
+    if (GP == 8) return split_dispatch_paged<256, 2>(a, G, s);
   } else if (D == 128) {
-    if (GP == 2) return split_dispatch_paged<128, 2>(a, G, s);
-    if (GP == 4) return split_dispatch_paged<128, 4>(a, G, s);
-    if (GP == 8) return split_dispatch_paged<128, 8>(a, G, s);
+    if (GP == 4) return split_dispatch_paged<128, 1>(a, G, s);
+    if (GP == 8) return split_dispatch_paged<128, 2>(a, G, s);
   }
   return cudaErrorNotSupported;
 }
 
 int decode_split_tile_keys(int D, int G) {
-  const int GP = padded_group(G);
-  if (GP == 0) return 0;
-  return D == 256 ? geo_stage_keys<256>(GP) : D == 128 ? geo_stage_keys<128>(GP) : 0;
+  if (decode_group_pad(G) == 0 || (D != 128 && D != 256)) return 0;
+  return 256 / D * kGroup;
 }
 
 int decode_split_ctas_per_sm(int D, int G) {
-  const int GP = padded_group(G);
-  const int smem = GP == 0 ? 0 : D == 256 ? geo_smem_max<256>(GP) : D == 128 ? geo_smem_max<128>(GP) : 0;
-  if (smem == 0) return 0;
-  // 228 KB of shared memory per SM, 1 KB of it reserved per resident CTA
-  const int per_sm = 233472 / (smem + 1024);
-  return per_sm > 2 ? 2 : per_sm;
-}
-
-int decode_max_units() { return kMaxUnits; }
-
-cudaError_t launch_decode_fused(const FusedArgs& a, int D, cudaStream_t s) {
-  const int GP = padded_group(a.G);
-  if (a.B * a.Hkv > kMaxUnits) return cudaErrorNotSupported;
-  if (D == 256) {
-    if (GP == 2) return fused_dispatch<256, 2>(a, s);
-    if (GP == 4) return fused_dispatch<256, 4>(a, s);
-    if (GP == 8) return fused_dispatch<256, 8>(a, s);
-  } else if (D == 128) {
-    if (GP == 2) return fused_dispatch<128, 2>(a, s);
-    if (GP == 4) return fused_dispatch<128, 4>(a, s);
-    if (GP == 8) return fused_dispatch<128, 8>(a, s);
-  }
-  return cudaErrorNotSupported;
-}
-
-int decode_fused_ctas_per_sm(int D, int G) {
-  const int GP = padded_group(G);
+  const int GP = decode_group_pad(G);
   int smem = 0;
-  if (D == 256) smem = GP == 2 ? FGeo<256, 2>::SMEM_MAX : GP == 4 ? FGeo<256, 4>::SMEM_MAX : GP == 8 ? FGeo<256, 8>::SMEM_MAX : 0;
-  if (D == 128) smem = GP == 2 ? FGeo<128, 2>::SMEM_MAX : GP == 4 ? FGeo<128, 4>::SMEM_MAX : GP == 8 ? FGeo<128, 8>::SMEM_MAX : 0;
+  if (D == 256) smem = GP == 4 ? Geo<256, 1>::SMEM_MAX : GP == 8 ? Geo<256, 2>::SMEM_MAX : 0;
+  if (D == 128) smem = GP == 4 ? Geo<128, 1>::SMEM_MAX : GP == 8 ? Geo<128, 2>::SMEM_MAX : 0;
   if (smem == 0) return 0;
   // 228 KB of shared memory per SM; 1 KB reserved and the static block-scan scratch per CTA
   const int per_sm = 233472 / (smem + 1024 + 64);
   return per_sm > 2 ? 2 : per_sm;
 }
 
+int decode_max_units() { return kMaxUnits; }
+
 cudaError_t launch_decode_combine(const CombineArgs& a, int D, int G, cudaStream_t s) {
-  const int GP = padded_group(G);
+  const int GP = decode_group_pad(G);
   if (GP == 0) return cudaErrorNotSupported;
   // dims per CTA: enough CTAs to spread the partial reads, at most 32 lanes per head
   const int units = a.B * a.Hkv;

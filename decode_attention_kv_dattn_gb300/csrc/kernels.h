@@ -2,6 +2,7 @@
 // translation units. Not part of the public C ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -56,17 +57,24 @@ struct RopeArgs {
   int* err;
 };
 
+// Query heads of a KV group as the decode kernels lay them out: 4 (G <= 4)
+// or 8 (G <= 8); 0 for a group size with no compiled kernel.
+inline int decode_group_pad(int G) { return G <= 0 ? 0 : (G <= 4 ? 4 : (G <= 8 ? 8 : 0)); }
+
 // Split-K pass over the cached keys of a decode call (stream-K: the grid of
 // `ctas` CTAs cuts the concatenated tiles of all (stream, KV head) units into
 // equal ranges). Partial slot of a segment: the CTA index for the first
 // segment of a CTA's range, ctas + unit for any later one.
 struct SplitArgs {
+  CUtensorMap tmap_k;          // the layer's K cache as a 2D [rows, D] bf16 tensor
+  CUtensorMap tmap_v;          // (encode_cache_maps)
   CacheView c;
   int B, Hkv;
   int ctas;                    // grid size
   int max_len;                 // host bound on cached length (paged)
   const float* qhat;           // [B, Hq, D]
   float* part;                 // [ctas + B*Hkv][GP*(D+2)]: o[GP][D], m[GP], l[GP]
+                               // (GP = decode_group_pad(G))
   int* tiles;                  // [B*Hkv + 1] out: tile prefix over units
   int* err;
 };
@@ -85,31 +93,6 @@ struct CombineArgs {
   const float* part;
   float* out;                  // [B, Hq, D]
   int write_back;
-  int* err;
-};
-
-// One-launch decode (RoPE, split-K pass, combine, gate, store, write-back):
-// stream-K over (stream, KV head) units; the CTA that holds a unit's first
-// tile writes its rotated key entry, the CTA that finishes a unit's last
-// segment (per-unit counter) combines the unit.
-struct FusedArgs {
-  CacheView c;
-  int B, Hkv, G;
-  int ctas;
-  int max_len;
-  const uint16_t* q;           // [B, Hq, D]
-  const uint16_t* k_new;       // [B, Hkv, D]
-  const uint16_t* v_new;       // [B, Hkv, D]
-  const uint16_t* gate;        // [B, Hq] or null
-  const int32_t* pos;          // [B]
-  const uint64_t* rope_step;   // [r / 2] phase steps (rope_phase_step)
-  int r;
-  float q_scale;               // log2(e) / sqrt(D)
-  float* out;                  // [B, Hq, D]
-  int write_back;
-  float* part;                 // [ctas + B*Hkv][GP*(D+2)]
-  uint16_t* khat;              // [B*Hkv][D] rotated key entries
-  int* counters;               // [B*Hkv] finished segments; zero between calls
   int* err;
 };
 
@@ -163,8 +146,9 @@ struct VerifyCombineArgs {
 cudaError_t launch_rope(const RopeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_split(const SplitArgs& a, int D, int G, cudaStream_t s);
 cudaError_t launch_decode_combine(const CombineArgs& a, int D, int G, cudaStream_t s);
-cudaError_t launch_decode_fused(const FusedArgs& a, int D, cudaStream_t s);
-int decode_fused_ctas_per_sm(int D, int G);
+// Tensor maps of a cache's K and V for the split pass: [n_rows * Hkv * (R or
+// P), D] bf16 rows, boxes of 16 rows x 64 elements, 128-byte swizzle.
+cudaError_t encode_cache_maps(const CacheView& c, int Hkv, int D, CUtensorMap* k, CUtensorMap* v);
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_verify_split(const VerifySplitArgs& a, int D, cudaStream_t s);
 cudaError_t launch_verify_combine(const VerifyCombineArgs& a, int D, cudaStream_t s);

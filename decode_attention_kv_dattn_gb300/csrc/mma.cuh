@@ -1,0 +1,82 @@
+// Warp-level tensor-core helpers for the decode split pass: shared-memory
+// matrix loads (ldmatrix), in-register 8x8 transposes (movmatrix), the bf16
+// m16n8k16 MMA with fp32 accumulation, bf16x2 packing, and the 2D tiled TMA
+// load from a tensor map.
+//
+// Fragment conventions (PTX ISA, "Matrix fragments for mma.m16n8k16"): with
+// t the lane, g = t / 4 and c = 2 * (t % 4),
+//   A (16 x 16, row):  a0 = (g, c..c+1)    a1 = (g+8, c..c+1)
+//                      a2 = (g, c+8..c+9)  a3 = (g+8, c+8..c+9)
+//   B (16 x 8, col):   b0 = (k = c..c+1, n = g)   b1 = (k = c+8..c+9, n = g)
+//   C (16 x 8):        c0, c1 = (g, c), (g, c+1)  c2, c3 = (g+8, c), (g+8, c+1)
+// Each 32-bit register holds two bf16 values, the lower index in the low half.
+#pragma once
+
+#include <stdint.h>
+
+namespace dattn {
+
+// Four 8x8 b16 matrices; lane l supplies the row address for matrix l / 8.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// The same with each matrix transposed on the way into registers.
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// Transpose an 8x8 b16 matrix held one row-pair fragment per lane.
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// d += A * B, bf16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two floats to bf16 (nearest-even), `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// The float value of the bf16 nearest to x.
+__device__ __forceinline__ float bf16_round_f32(float x) {
+  return __uint_as_float(pack_bf16x2(0.f, x) & 0xffff0000u);
+}
+
+// x as hi + lo, both bf16 (16 significant bits of x in all): returns the two
+// packed pairs for (x0, x1).
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16x2(x0, x1);
+  const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xffff0000u);
+  lo = pack_bf16x2(x0 - h0, x1 - h1);
+}
+
+// Tiled 2D TMA load of the box at element coordinates (x, y) of the tensor
+// map into shared memory; completion counted on the mbarrier in bytes. x times
+// the element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y,
+                                            uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+}  // namespace dattn

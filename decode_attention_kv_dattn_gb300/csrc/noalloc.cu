@@ -47,8 +47,6 @@ std::mutex g_mutex;
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-int padded_group(int G) { return G <= 2 ? 2 : (G <= 4 ? 4 : (G <= 8 ? 8 : 0)); }
-
 }  // namespace
 
 extern "C" DATTN_API int dattn_decode_noalloc(const dattn_config* cfg, int layer, const dattn_cache* cache,
@@ -58,7 +56,7 @@ extern "C" DATTN_API int dattn_decode_noalloc(const dattn_config* cfg, int layer
   const int Hq = cfg->num_q_heads, Hkv = cfg->num_kv_heads, D = cfg->head_dim;
   if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return DATTN_EINVAL;
   if (D != 128 && D != 256) return DATTN_EUNSUPPORTED;
-  const int G = Hq / Hkv, GP = padded_group(G);
+  const int G = Hq / Hkv, GP = decode_group_pad(G);
   if (GP == 0) return DATTN_EUNSUPPORTED;
   const dattn_layer_config& L = cfg->layers[layer];
   if (L.rotary_dim < 0 || L.rotary_dim > D || L.rotary_dim % 2 || (L.rotary_dim > 0 && !(L.rope_theta > 0.0)))
@@ -130,18 +128,6 @@ extern "C" DATTN_API int dattn_decode_noalloc(const dattn_config* cfg, int layer
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int* err = reinterpret_cast<int*>(ds.base + err_off);
-  uint64_t* rope_step = half > 0 ? reinterpret_cast<uint64_t*>(ds.base + freq_off) : nullptr;
-  // The error word accumulates bits, so it starts every call at zero; the
-  // RoPE phase-step table is rewritten from the host.
-  if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return DATTN_ECUDA;
-  if (half > 0) {
-    uint64_t f[128];
-    if (half > 128) return DATTN_EUNSUPPORTED;
-    for (int i = 0; i < half; ++i) f[i] = rope_phase_step(L.rope_theta, L.rotary_dim, i);
-    if (cudaMemcpyAsync(rope_step, f, half * sizeof(uint64_t), cudaMemcpyHostToDevice, s) != cudaSuccess)
-      return DATTN_ECUDA;
-  }
-
   CacheView cv{};
   cv.k = static_cast<uint16_t*>(cache->k);
   cv.v = static_cast<uint16_t*>(cache->v);
@@ -155,6 +141,21 @@ extern "C" DATTN_API int dattn_decode_noalloc(const dattn_config* cfg, int layer
   cv.block_table = cache->block_table;
   cv.bt_stride = cache->bt_stride;
   cv.seq_len = cache->seq_len;
+  // the split pass reads the cache through tensor maps (host-side encoding)
+  SplitArgs sa{};
+  if (encode_cache_maps(cv, Hkv, D, &sa.tmap_k, &sa.tmap_v) != cudaSuccess) return DATTN_EUNSUPPORTED;
+
+  uint64_t* rope_step = half > 0 ? reinterpret_cast<uint64_t*>(ds.base + freq_off) : nullptr;
+  // The error word accumulates bits, so it starts every call at zero; the
+  // RoPE phase-step table is rewritten from the host.
+  if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return DATTN_ECUDA;
+  if (half > 0) {
+    uint64_t f[128];
+    if (half > 128) return DATTN_EUNSUPPORTED;
+    for (int i = 0; i < half; ++i) f[i] = rope_phase_step(L.rope_theta, L.rotary_dim, i);
+    if (cudaMemcpyAsync(rope_step, f, half * sizeof(uint64_t), cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return DATTN_ECUDA;
+  }
 
   RopeArgs ra{};
   ra.rows = B;
@@ -174,7 +175,6 @@ extern "C" DATTN_API int dattn_decode_noalloc(const dattn_config* cfg, int layer
   cudaError_t e = launch_rope(ra, s);
   if (e != cudaSuccess) return e == cudaErrorNotSupported ? DATTN_EUNSUPPORTED : DATTN_ECUDA;
 
-  SplitArgs sa{};
   sa.c = cv;
   sa.B = B;
   sa.Hkv = Hkv;
