@@ -17,10 +17,33 @@
 #include <new>
 #include <vector>
 
+#include <mutex>
+#include <unordered_map>
+
 #include "dattn.h"
 #include "kernels.h"
 
 using namespace dattn;
+
+namespace dattn {
+
+namespace {
+std::mutex g_order_mutex;
+std::unordered_map<void*, const void*> g_last_written;  // stream -> cache K written by its last launch
+}  // namespace
+
+bool prev_launch_writes(void* stream, const void* cache_k) {
+  std::lock_guard<std::mutex> lock(g_order_mutex);
+  const auto it = g_last_written.find(stream);
+  return it != g_last_written.end() && it->second == cache_k;
+}
+
+void record_launch(void* stream, const void* cache_k) {
+  std::lock_guard<std::mutex> lock(g_order_mutex);
+  g_last_written[stream] = cache_k;
+}
+
+}  // namespace dattn
 
 struct dattn_handle {
   int device = 0;
@@ -29,12 +52,17 @@ struct dattn_handle {
   std::vector<dattn_layer_config> layers;
   std::vector<uint64_t*> rope_step;  // device, per layer ([r/2] phase steps or null)
   int num_sms = 0;
-  int split_resident = 0;  // resident split CTAs on the whole GPU
-  size_t part_units = 0;   // capacity of the partials, in segment slots
-  float* qhat = nullptr;
-  int* tiles = nullptr;    // tile prefix over units, from the split pass
-  uint16_t* khat = nullptr;
-  float* part = nullptr;
+  int decode_resident = 0;  // resident decode CTAs on the whole GPU
+  size_t part_units = 0;    // capacity of the decode partials, in segment slots
+  // Decode workspace, two halves used by alternate calls (a call may run while
+  // the one before it finishes): partials [part_units][GP][D+2] and finished
+  // segments per (stream, KV head), zero between calls.
+  float* part[2] = {nullptr, nullptr};
+  int* counters[2] = {nullptr, nullptr};
+  unsigned decode_calls = 0;
+  float* qhat = nullptr;    // verify: rotated q of the window rows
+  int* tiles = nullptr;     // verify: tile prefix over units, from its split pass
+  uint16_t* khat = nullptr; // verify: rotated window keys
   float* vpart = nullptr;   // verify partials: [sms + units][G*T][D+4]
   size_t vpart_slots = 0;
   int* err = nullptr;
@@ -71,12 +99,12 @@ int cuda_status(cudaError_t e) {
   return DATTN_ECUDA;
 }
 
-// Split grid: every resident split CTA, but at least 4 stage tiles (one per
-// warp) per CTA for the largest amount of work this call may have.
-int plan_split_ctas(const dattn_handle* h, int units, int n_max, int tile_keys) {
+// Decode grid: every resident CTA, but at least 4 stage tiles (one per warp)
+// per CTA for the largest amount of work this call may have.
+int plan_decode_ctas(const dattn_handle* h, int units, int n_max, int tile_keys) {
   const int64_t tiles = static_cast<int64_t>(units) * ((n_max + tile_keys - 1) / tile_keys);
   int64_t ctas = (tiles + 3) / 4;
-  if (ctas > h->split_resident) ctas = h->split_resident;
+  if (ctas > h->decode_resident) ctas = h->decode_resident;
   if (ctas < 1) ctas = 1;
   return static_cast<int>(ctas);
 }
@@ -174,8 +202,8 @@ int dattn_create(const dattn_config* cfg, int device, dattn_t** out) {
   };
   if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
     return fail(DATTN_ECUDA);
-  h->split_resident = h->num_sms * decode_split_ctas_per_sm(D, G);
-  if (h->split_resident <= 0) return fail(DATTN_EUNSUPPORTED);
+  h->decode_resident = h->num_sms * decode_ctas_per_sm(D, G);
+  if (h->decode_resident <= 0) return fail(DATTN_EUNSUPPORTED);
 
   // RoPE phase steps (fixed-point turns per position), one table per layer
   for (const dattn_layer_config& L : h->layers) {
@@ -197,13 +225,19 @@ int dattn_create(const dattn_config* cfg, int device, dattn_t** out) {
                       (h->max_verify_rows > 1 ? h->max_verify_rows : 1);
   if (cudaMalloc(&h->qhat, rows * Hq * D * sizeof(float)) != cudaSuccess) return fail(DATTN_ECUDA);
   if (cudaMalloc(&h->khat, rows * Hkv * D * sizeof(uint16_t)) != cudaSuccess) return fail(DATTN_ECUDA);
-  // Partials: one slot per split CTA plus one per unit.
+  // Decode partials: one slot per CTA plus one per unit; per-unit counters.
   if (static_cast<int64_t>(h->max_streams) * Hkv > decode_max_units()) return fail(DATTN_EUNSUPPORTED);
-  h->part_units = static_cast<size_t>(h->split_resident) + static_cast<size_t>(h->max_streams) * Hkv;
+  h->part_units = static_cast<size_t>(h->decode_resident) + static_cast<size_t>(h->max_streams) * Hkv;
+  for (int i = 0; i < 2; ++i) {
+    const size_t nc = static_cast<size_t>(h->max_streams) * Hkv;
+    if (cudaMalloc(&h->counters[i], nc * sizeof(int)) != cudaSuccess) return fail(DATTN_ECUDA);
+    if (cudaMemset(h->counters[i], 0, nc * sizeof(int)) != cudaSuccess) return fail(DATTN_ECUDA);
+  }
   if (cudaMalloc(&h->tiles, (static_cast<size_t>(h->max_streams) * Hkv + 1) * sizeof(int)) != cudaSuccess)
     return fail(DATTN_ECUDA);
   const size_t part_floats = h->part_units * h->GP * (D + 2);
-  if (cudaMalloc(&h->part, part_floats * sizeof(float)) != cudaSuccess) return fail(DATTN_ECUDA);
+  for (int i = 0; i < 2; ++i)
+    if (cudaMalloc(&h->part[i], part_floats * sizeof(float)) != cudaSuccess) return fail(DATTN_ECUDA);
   if (h->max_verify_rows > 0) {
     if (G * h->max_verify_rows > 128) return fail(DATTN_EUNSUPPORTED);
     if (static_cast<int64_t>(h->max_streams) * Hkv > kVerifyMaxUnits) return fail(DATTN_EUNSUPPORTED);
@@ -223,7 +257,10 @@ void dattn_destroy(dattn_t* h) {
   for (uint64_t* p : h->rope_step) cudaFree(p);
   cudaFree(h->qhat);
   cudaFree(h->khat);
-  cudaFree(h->part);
+  for (int i = 0; i < 2; ++i) {
+    cudaFree(h->part[i]);
+    cudaFree(h->counters[i]);
+  }
   cudaFree(h->vpart);
   cudaFree(h->tiles);
   cudaFree(h->err);
@@ -239,6 +276,11 @@ int dattn_get_error(dattn_t* h, dattn_stream_t stream) {
   if (cudaMemcpyAsync(&bits, h->err, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return DATTN_ECUDA;
   if (cudaMemsetAsync(h->err, 0, sizeof(int), s) != cudaSuccess) return DATTN_ECUDA;
+  // a call that gave up waiting still counts its segments; clear them anyway
+  for (int i = 0; i < 2 && bits; ++i)
+    if (cudaMemsetAsync(h->counters[i], 0, static_cast<size_t>(h->max_streams) * h->Hkv * sizeof(int), s) !=
+        cudaSuccess)
+      return DATTN_ECUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return DATTN_ECUDA;
   if (bits & ERR_TIMEOUT) return DATTN_ETIMEOUT;
   if (bits & ERR_INDEX) return DATTN_EINDEX;
@@ -277,7 +319,9 @@ int dattn_append_kv(dattn_t* h, int layer, const dattn_cache* cache, int num_str
   a.rotate = rotate;
   a.rope_step = h->rope_step[layer];
   a.err = h->err;
-  return cuda_status(launch_append(a, reinterpret_cast<cudaStream_t>(stream)));
+  rc = cuda_status(launch_append(a, reinterpret_cast<cudaStream_t>(stream)));
+  if (rc == DATTN_OK) record_launch(stream, cache->k);
+  return rc;
 }
 
 int dattn_decode(dattn_t* h, int layer, const dattn_cache* cache, const dattn_decode_args* args,
@@ -304,56 +348,36 @@ int dattn_decode(dattn_t* h, int layer, const dattn_cache* cache, const dattn_de
   if (!guard.ok) return DATTN_ECUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-  RopeArgs ra{};
-  ra.rows = B;
-  ra.Hq = h->Hq;
-  ra.Hkv = h->Hkv;
-  ra.D = h->D;
-  ra.r = L.rotary_dim;
-  ra.q = static_cast<const uint16_t*>(args->q);
-  ra.k = static_cast<const uint16_t*>(args->k_new);
-  ra.pos = args->pos;
-  ra.T = 1;
-  ra.rope_step = h->rope_step[layer];
-  ra.q_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(h->D)));
-  ra.qhat = h->qhat;
-  ra.khat = h->khat;
-  ra.err = h->err;
-  rc = cuda_status(launch_rope(ra, s));
-  if (rc != DATTN_OK) return rc;
-
-  const int ctas = plan_split_ctas(h, B * h->Hkv, n_max, decode_split_tile_keys(h->D, h->G));
+  const int ctas = plan_decode_ctas(h, B * h->Hkv, n_max, decode_tile_keys(h->D, h->G));
   if (static_cast<size_t>(ctas) + static_cast<size_t>(B) * h->Hkv > h->part_units) return DATTN_EXCEEDS;
-  SplitArgs sa{};
-  sa.c = make_view(h, L, cache);
-  if (encode_cache_maps(sa.c, h->Hkv, h->D, &sa.tmap_k, &sa.tmap_v) != cudaSuccess) return DATTN_EUNSUPPORTED;
-  sa.B = B;
-  sa.Hkv = h->Hkv;
-  sa.ctas = ctas;
-  sa.max_len = n_max;
-  sa.qhat = h->qhat;
-  sa.part = h->part;
-  sa.tiles = h->tiles;
-  sa.err = h->err;
-  rc = cuda_status(launch_decode_split(sa, h->D, h->G, s));
-  if (rc != DATTN_OK) return rc;
-
-  CombineArgs ca{};
-  ca.c = sa.c;
-  ca.B = B;
-  ca.Hkv = h->Hkv;
-  ca.split_ctas = ctas;
-  ca.tiles = h->tiles;
-  ca.max_len = n_max;
-  ca.qhat = h->qhat;
-  ca.khat = h->khat;
-  ca.v_new = static_cast<const uint16_t*>(args->v_new);
-  ca.gate = static_cast<const uint16_t*>(args->gate);
-  ca.part = h->part;
-  ca.out = args->out;
-  ca.write_back = args->write_back;
-  ca.err = h->err;
-  return cuda_status(launch_decode_combine(ca, h->D, h->G, s));
+  DecodeArgs da{};
+  da.c = make_view(h, L, cache);
+  if (encode_cache_maps(da.c, h->Hkv, h->D, &da.tmap_k, &da.tmap_v) != cudaSuccess) return DATTN_EUNSUPPORTED;
+  da.B = B;
+  da.Hkv = h->Hkv;
+  da.G = h->G;
+  da.max_len = n_max;
+  da.q = static_cast<const uint16_t*>(args->q);
+  da.k_new = static_cast<const uint16_t*>(args->k_new);
+  da.v_new = static_cast<const uint16_t*>(args->v_new);
+  da.gate = static_cast<const uint16_t*>(args->gate);
+  da.pos = args->pos;
+  da.rope_step = h->rope_step[layer];
+  da.r = L.rotary_dim;
+  da.q_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(h->D)));
+  da.out = args->out;
+  da.write_back = args->write_back;
+  const unsigned half = h->decode_calls & 1u;
+  da.part = h->part[half];
+  da.counters = h->counters[half];
+  da.err = h->err;
+  da.early = !prev_launch_writes(stream, cache->k);
+  rc = cuda_status(launch_decode(da, h->D, ctas, s));
+  if (rc == DATTN_OK) {
+    record_launch(stream, args->write_back ? cache->k : nullptr);
+    ++h->decode_calls;
+  }
+  return rc;
 }
 
 int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, const dattn_verify_args* args,
@@ -432,7 +456,9 @@ int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, const dattn_ve
   vc.out = args->out;
   vc.write_back = args->write_back;
   vc.err = h->err;
-  return cuda_status(launch_verify_combine(vc, h->D, s));
+  rc = cuda_status(launch_verify_combine(vc, h->D, s));
+  if (rc == DATTN_OK) record_launch(stream, args->write_back ? cache->k : nullptr);
+  return rc;
 }
 
 }  // extern "C"

@@ -1,16 +1,18 @@
-// Decode attention: the split-K pass over the cached keys and the LSE combine
-// that joins the new token in score space.
+// Decode attention in one launch per call: RoPE of the new token, the pass
+// over the cached keys, the join of the new token in score space, the output
+// gate, the fp32 store and the write-back of the new K/V entry.
 //
 // Method ("vllm-omni commits", score-space join commit): the cached keys (n of
 // them) and the new key are scored separately and their score vectors meet in
 // one softmax; nothing cache-sized is copied, and the new K/V entry is written
 // into its slot afterwards. A ring's slots need no reordering (softmax is
 // order-free, cached keys carry their own rotary phase); unwritten slots are
-// masked. Grouped-query attention shares each KV head's loads among its G
-// query heads ("vllm-omni commits", talker export commit). Splitting the keys
+// masked. Per-layer-type RoPE and the head-wise sigmoid gate follow the Spark
+// model commit of the same page; grouped-query attention shares each KV head's
+// loads among its G query heads (talker export commit). Splitting the keys
 // over many CTAs and merging their partial softmax states follows "TensorFold
-// PR #608" (the split "shared" kernel plus a merge, the lessons that the grid
-// must fill the GPU and that a merge must not be a chain of dependent loads).
+// PR #608" (the grid must fill the GPU; a merge must not be a chain of
+// dependent loads).
 //
 // GB300 design.
 //  * Work split (stream-K). A "unit" is one (stream, KV head). Its cached keys
@@ -21,16 +23,24 @@
 //    tiles are laid end to end and the grid - one CTA per SM - cuts that
 //    sequence into equal contiguous ranges, so every CTA moves the same number
 //    of bytes whatever the mix of lengths. Each piece of a unit inside one CTA
-//    (a "segment") leaves one partial softmax state (m, l, o); the combine
-//    merges a unit's segments.
+//    (a "segment") leaves one partial softmax state (m, l, o) in global
+//    memory; the CTA that finishes a unit's last segment (a per-unit counter)
+//    merges them with the new token's score, applies the gate, stores the
+//    output and writes the new entry back - after every read of the cache.
+//  * RoPE. At a segment start the CTA rotates the unit's G query heads (fp32,
+//    pre-scaled by log2(e)/sqrt(D)); the cos/sin of each pair come from an
+//    exact fixed-point phase and an fp32 polynomial (rope_cos_sin). The
+//    combining CTA rotates the new key with the same cos/sin and rounds it to
+//    bf16 from fp64 - the exact entry that is scored and stored.
 //  * Loads. Each warp owns a ring of NS stage buffers. One lane issues 2D
 //    tensor TMA copies (boxes of 16 rows x 64 bf16, 128-byte swizzle; one box
 //    per 64 dims of K and of V per group) for the warp's tile NS ahead, with
 //    completion counted in bytes on the stage's mbarrier; the ring keeps
-//    streaming across segment boundaries. Rows a box brings in that are not
-//    valid keys (past a unit's length, past a page, outside a ring's valid
-//    slots, or zero-filled past the pool) are masked: their scores are set to
-//    -inf and their V rows are zeroed in shared memory before use.
+//    streaming across segment boundaries. The rows of each group and its
+//    valid-row mask (past a unit's length, past a page, outside a ring's valid
+//    slots, or zero-filled past the pool) are worked out by the whole warp for
+//    32 tiles at a time, a window ahead, so that no page-table load sits on the
+//    issue path. Invalid rows get -inf scores and zeroed V rows.
 //  * Math on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate).
 //    The KV stream is HBM-bound at G flops per byte; the tensor cores are used
 //    because they cut the instructions per byte about tenfold against fp32
@@ -38,15 +48,14 @@
 //      S^T (16 keys x 8 cols) = K (16 x D) . Q^T (D x 8 cols)
 //      O^T (D x 8 cols)      += V^T (D x 16) . P^T (16 x 8 cols)
 //    The 8 (or 2 x 8) columns hold each query head twice: once as the bf16
-//    rounding of the pre-scaled rotated q, once as the bf16 rounding of what
-//    is left ("hi" and "lo"), so q keeps 16 significant bits; the two score
-//    columns of a head are added. The probabilities are split into hi and lo
-//    bf16 parts the same way, so the value sum sees 16-bit probabilities; the
-//    two output columns of a head are added at the end. K and V enter the
-//    tensor cores exactly (they are bf16). The score fragment turns into the
-//    PV operand in registers (movmatrix transposes); online softmax in base 2
-//    runs on the score fragment, and the output is rescaled only when some
-//    head's running maximum moved.
+//    rounding of the rotated q, once as the bf16 rounding of what is left
+//    ("hi" and "lo"), so q keeps 16 significant bits; the two score columns of
+//    a head are added. The probabilities are split into hi and lo bf16 parts
+//    the same way, and the two output columns of a head are added at the end.
+//    K and V enter the tensor cores exactly (they are bf16). The score
+//    fragment becomes the PV operand in registers (movmatrix transposes);
+//    online softmax in base 2 runs on the score fragment, and the output is
+//    rescaled only when some head's running maximum moved.
 #include "common.cuh"
 #include "mma.cuh"
 
@@ -57,9 +66,10 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kMaxUnits = 1024;   // (stream, KV head) units per call
-constexpr int kGroup = 16;        // keys per MMA group
+constexpr int kMaxUnits = 1024;          // (stream, KV head) units per call
+constexpr int kGroup = 16;               // keys per MMA group
 constexpr int kBoxBytes = kGroup * 128;  // one TMA box: 16 rows x 64 bf16
+constexpr int kWin = 32;                 // tiles per prefetch window (one per lane)
 
 template <int D, int NT>
 struct Geo {
@@ -71,13 +81,30 @@ struct Geo {
   static constexpr int KHALF = KG * GBYTES;          // K part of a stage; V follows
   static constexpr int STAGE = 2 * KHALF;
   static constexpr int NS = 3;
-  static constexpr int BAR_OFF = kWarps * NS * STAGE;        // from the 1024-aligned base
-  static constexpr int ML_OFF = BAR_OFF + kWarps * NS * 8;   // float [kWarps][2*GP]
-  static constexpr int SLOT_OFF = ML_OFF + kWarps * 2 * GP * 4;  // int [kWarps]
-  static constexpr int TAB_OFF = (SLOT_OFF + kWarps * 4 + 15) / 16 * 16;
+  // offsets from the 1024-byte aligned base of dynamic shared memory
+  static constexpr int BAR_OFF = kWarps * NS * STAGE;
+  static constexpr int ML_OFF = BAR_OFF + kWarps * NS * 8;        // float [kWarps][2*GP]
+  static constexpr int SLOT_OFF = ML_OFF + kWarps * 2 * GP * 4;   // int [kWarps]
+  static constexpr int SN_OFF = SLOT_OFF + kWarps * 4;            // float [GP]: new-token scores
+  static constexpr int FLAG_OFF = SN_OFF + GP * 4;                // int: "this CTA combines"
+  static constexpr int CS_OFF = (FLAG_OFF + 4 + 15) / 16 * 16;    // float2 [D/2]: cos, sin
+  static constexpr int QS_OFF = CS_OFF + D / 2 * 8;               // float [GP][D]: rotated q
+  static constexpr int KH_OFF = QS_OFF + GP * D * 4;              // bf16 [D]: new K entry
+  static constexpr int WROW_OFF = KH_OFF + D * 2;                 // int [kWarps][2][kWin*KG]
+  static constexpr int WMASK_OFF = WROW_OFF + kWarps * 2 * kWin * KG * 4;
+  static constexpr int STEP_OFF = WMASK_OFF + kWarps * 2 * kWin * KG * 4;  // uint64 [D/2]: RoPE steps
+  static constexpr int SIG_OFF = STEP_OFF + D / 2 * 8;            // float [GP]: sigmoid(gate)
+  static constexpr int INBAR_OFF = SIG_OFF + GP * 4;              // 2 mbarriers of the input slots
+  static constexpr int IN_Q = 0;                                  // input slot: q [GP][D] bf16,
+  static constexpr int IN_K = GP * D * 2;                         //   k_new [D], v_new [D]
+  static constexpr int IN_V = IN_K + D * 2;
+  static constexpr int IN_BYTES = IN_V + D * 2;
+  static constexpr int IN_OFF = (INBAR_OFF + 16 + 15) / 16 * 16;  // 2 input slots
+  static constexpr int TAB_OFF = IN_OFF + 2 * IN_BYTES;
   static constexpr int SMEM_MAX = 1024 + TAB_OFF + (2 * kMaxUnits + 1) * 4;
   static_assert(D == 128 || D == 256, "head_dim");
   static_assert(GP * D * 4 <= STAGE, "a stage buffer holds one warp's partial output");
+  static_assert(NS < kWin, "issue runs at most one window ahead");
 };
 
 // Cached keys of call row b (the same for all its KV heads). Bad metadata is
@@ -104,59 +131,267 @@ __device__ __forceinline__ int unit_length(const CacheView& c, int b, int max_le
   }
 }
 
-// First 16-slot block of a ring holding `n` valid slots before `head`.
-__device__ __forceinline__ int ring_first_block(int head, int n, int R) {
-  const int start = head - n < 0 ? head - n + R : head - n;
-  return start >> 4;
+// First slot of a ring holding `n` valid slots before `head`.
+__device__ __forceinline__ int ring_start(int head, int n, int R) {
+  return head - n < 0 ? head - n + R : head - n;
 }
 
-// 16-row groups of a unit with n cached keys.
+// 16-row groups of a unit with n cached keys (`head` is the ring head).
 template <bool PAGED>
-__device__ __forceinline__ int unit_groups(const CacheView& c, int b, int n) {
+__device__ __forceinline__ int unit_groups(const CacheView& c, int head, int n) {
   if (n <= 0) return 0;
   if constexpr (PAGED) {
+    (void)head;
     const int gpp = (c.P + kGroup - 1) / kGroup;
     const int full = n / c.P, rest = n - full * c.P;
     return full * gpp + (rest + kGroup - 1) / kGroup;
   } else {
     const int R = c.R, nb = (R + kGroup - 1) / kGroup;
     if (n >= R) return nb;
-    const int head = c.ring_head[b];
-    const int start = head - n < 0 ? head - n + R : head - n;
+    const int start = ring_start(head, n, R);
     const int b0 = start >> 4, end = start + n - 1;
     if (end < R) return (end >> 4) - b0 + 1;
     return min(nb, nb - b0 + ((end - R) >> 4) + 1);  // wraps past the last slot
   }
 }
 
+// Bits r of the valid rows [lo, hi) of a 16-row group (empty when hi <= lo).
+__device__ __forceinline__ uint32_t row_bits(int lo, int hi) {
+  lo = max(lo, 0);
+  hi = min(hi, kGroup);
+  if (hi <= lo) return 0u;
+  return ((1u << (hi - lo)) - 1u) << lo;
+}
+
+// Number of split CTAs whose ranges hold tiles of the unit spanning global
+// tiles [p0, p1), the first of them (CTA of tile x: floor(((x+1)NC-1)/T)) and
+// the partial slot of its segment.
+__device__ __forceinline__ int unit_segments(int p0, int p1, int T, int NC, int u, int& c_lo,
+                                             int& first_slot) {
+  if (p1 <= p0) return 0;
+  c_lo = static_cast<int>((static_cast<int64_t>(p0 + 1) * NC - 1) / T);
+  const int c_hi = static_cast<int>((static_cast<int64_t>(p1) * NC - 1) / T);
+  first_slot = static_cast<int>(static_cast<int64_t>(c_lo) * T / NC) == p0 ? c_lo : NC + u;
+  int n = 1;
+  for (int cc = c_lo + 1; cc <= c_hi; ++cc)
+    if (static_cast<int64_t>(cc) * T / NC < static_cast<int64_t>(cc + 1) * T / NC) ++n;
+  return n;
+}
+
+// Rotate the G query heads of a unit (src: its q rows [G][D], staged in
+// shared memory) at position pos into qs[GP][D] (fp32, pre-scaled; heads >= G
+// are zero) and keep each pair's cos/sin in cs. One pair per thread at a
+// time; all threads of the CTA take part.
+template <int D, int GP>
+__device__ __forceinline__ void rotate_q(const DecodeArgs& a, const uint16_t* src, int pos,
+                                         const uint64_t* step, float* qs, float2* cs) {
+  const int G = a.G, half = a.r / 2;
+  for (int p = threadIdx.x; p < D / 2; p += kThreads) {
+    const int d0 = p < half ? p : a.r + 2 * (p - half);
+    const int d1 = p < half ? p + half : d0 + 1;
+    float c = 1.f, s = 0.f;
+    if (p < half) rope_cos_sin(pos, step[p], c, s);
+    cs[p] = make_float2(c, s);
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+      float o0 = 0.f, o1 = 0.f;
+      if (g < G) {
+        const float x = bf16_to_f32(src[g * D + d0]), y = bf16_to_f32(src[g * D + d1]);
+        if (p < half) {
+          o0 = fmaf(x, c, -y * s) * a.q_scale;
+          o1 = fmaf(y, c, x * s) * a.q_scale;
+        } else {
+          o0 = x * a.q_scale;
+          o1 = y * a.q_scale;
+        }
+      }
+      qs[g * D + d0] = o0;
+      qs[g * D + d1] = o1;
+    }
+  }
+}
+
+// The new token of unit u = (b, j): its K entry into kh (bf16_RNE of the fp64
+// rotation with the cos/sin in cs - the value that is scored and stored), its
+// scores into sn (base 2, one per head, with the rotated q in qs) and the
+// heads' sigmoid(gate) into sig (gate_g: this thread's head's logit, threads <
+// G). `in` holds the unit's staged k_new and v_new rows. All threads of the
+// CTA take part; ends with a CTA barrier.
+template <int D, int GP>
+__device__ void new_token(const DecodeArgs& a, const float* qs, const float2* cs, const uint8_t* in,
+                          float gate_g, uint16_t* kh, float* sn, float* sig) {
+  using Gm = Geo<D, GP / 4>;
+  const int G = a.G, half = a.r / 2;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint16_t* ksrc = reinterpret_cast<const uint16_t*>(in + Gm::IN_K);
+  if (threadIdx.x < G) sig[threadIdx.x] = a.gate ? 1.f / (1.f + expf(-gate_g)) : 1.f;
+  for (int p = threadIdx.x; p < D / 2; p += kThreads) {
+    const int d0 = p < half ? p : a.r + 2 * (p - half);
+    const int d1 = p < half ? p + half : d0 + 1;
+    if (p < half) {
+      const double c64 = cs[p].x, s64 = cs[p].y;
+      const double x = bf16_to_f32(ksrc[d0]), y = bf16_to_f32(ksrc[d1]);
+      kh[d0] = f64_to_bf16(__dsub_rn(__dmul_rn(x, c64), __dmul_rn(y, s64)));
+      kh[d1] = f64_to_bf16(__dadd_rn(__dmul_rn(y, c64), __dmul_rn(x, s64)));
+    } else {
+      kh[d0] = ksrc[d0];
+      kh[d1] = ksrc[d1];
+    }
+  }
+  __syncthreads();
+  for (int g = warp; g < G; g += kWarps) {
+    float dot = 0.f;
+    for (int d = lane; d < D; d += 32) dot = fmaf(qs[g * D + d], bf16_to_f32(kh[d]), dot);
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) dot += __shfl_xor_sync(kFull, dot, w);
+    if (lane == 0) sn[g] = dot;
+  }
+  __syncthreads();
+}
+
+// Running merge of softmax states (max m, sum l, output slice o) over the
+// dims of one head: starts from the new token (m = its score, l = 1, o = v).
+struct Merge8 {
+  float M, L, o[8];
+  __device__ __forceinline__ void add(float m, float l, const float (&x)[8]) {
+    const float Mn = fmaxf(M, m);
+    const float al = exp2_fast(M - Mn), be = exp2_fast(m - Mn);
+    L = fmaf(L, al, l * be);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = fmaf(o[i], al, x[i] * be);
+    M = Mn;
+  }
+};
+
+// Output and write-back of unit u = (b, j) once all of its segments are done.
+// Each thread takes 8 consecutive dims of one head; `states(g, d, mg)` folds
+// the unit's segment states for head g, dims d..d+7 into mg. Needs new_token
+// (kh, sn, sig) and the staged v_new row in `in`. All threads take part.
+template <int D, int GP, bool PAGED, typename States>
+__device__ void finish_unit(const DecodeArgs& a, int u, const uint8_t* in, const uint16_t* kh,
+                            const float* sn, const float* sig, States states) {
+  using Gm = Geo<D, GP / 4>;
+  const int Hkv = a.Hkv, G = a.G, Hq = Hkv * G;
+  const int b = u / Hkv, j = u - b * Hkv;
+  const CacheView& c = a.c;
+  const uint16_t* vsrc = reinterpret_cast<const uint16_t*>(in + Gm::IN_V);
+  for (int e = threadIdx.x * 8; e < G * D; e += kThreads * 8) {
+    const int g = e / D, d = e - g * D;
+    Merge8 mg;
+    mg.M = sn[g];
+    mg.L = 1.f;
+    const uint4 vw = *reinterpret_cast<const uint4*>(vsrc + d);
+    mg.o[0] = bf16_lo(vw.x); mg.o[1] = bf16_hi(vw.x);
+    mg.o[2] = bf16_lo(vw.y); mg.o[3] = bf16_hi(vw.y);
+    mg.o[4] = bf16_lo(vw.z); mg.o[5] = bf16_hi(vw.z);
+    mg.o[6] = bf16_lo(vw.w); mg.o[7] = bf16_hi(vw.w);
+    states(g, d, mg);
+    const float scale = sig[g] / mg.L;
+    float* dst = a.out + (static_cast<int64_t>(b) * Hq + j * G + g) * D + d;
+    *reinterpret_cast<float4*>(dst) = make_float4(mg.o[0] * scale, mg.o[1] * scale, mg.o[2] * scale, mg.o[3] * scale);
+    *reinterpret_cast<float4*>(dst + 4) = make_float4(mg.o[4] * scale, mg.o[5] * scale, mg.o[6] * scale, mg.o[7] * scale);
+  }
+  // write-back of the new entry: every segment of this unit has finished reading
+  if (a.write_back) {
+    int64_t wb = -1;
+    if constexpr (PAGED) {
+      const int n = min(max(c.seq_len[b], 0), min(a.max_len, c.bt_stride * c.P));
+      const int pi = n / c.P;
+      const int pg = pi < c.bt_stride ? c.block_table[static_cast<int64_t>(b) * c.bt_stride + pi] : -1;
+      if (pg >= 0 && pg < c.n_rows)
+        wb = ((static_cast<int64_t>(pg) * Hkv + j) * c.P + n % c.P) * D;
+      else if (threadIdx.x == 0)
+        raise_error(a.err, ERR_INDEX);
+    } else {
+      const int row = c.stream_rows ? c.stream_rows[b] : b;
+      const int head = c.ring_head[b], cnt = c.ring_count[b];
+      if (!(row < 0 || row >= c.n_rows || head < 0 || head >= c.R || cnt < 0 || cnt > c.R))
+        wb = ((static_cast<int64_t>(row) * Hkv + j) * c.R + head) * D;
+    }
+    if (wb >= 0) {
+      for (int d = threadIdx.x * 8; d < D; d += kThreads * 8) {
+        *reinterpret_cast<uint4*>(c.k + wb + d) = *reinterpret_cast<const uint4*>(kh + d);
+        *reinterpret_cast<uint4*>(c.v + wb + d) = *reinterpret_cast<const uint4*>(vsrc + d);
+      }
+    }
+  }
+  __syncthreads();
+}
+
 template <int D, int NT, bool PAGED>
-__global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_constant__ SplitArgs a, int G) {
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeArgs a) {
   using Gm = Geo<D, NT>;
   constexpr int GP = Gm::GP, KSTEPS = Gm::KSTEPS, BOXES = Gm::BOXES, KG = Gm::KG, NS = Gm::NS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const CacheView& c = a.c;
-  const int Hkv = a.Hkv, U = a.B * Hkv;
+  const int Hkv = a.Hkv, U = a.B * Hkv, G = a.G;
   const int NC = gridDim.x, cta = blockIdx.x;
   int* P = reinterpret_cast<int*>(smem + Gm::TAB_OFF);  // [U + 1] tile prefix over units
   int* N = P + U + 1;                                    // [U] cached keys per unit
+  float* ML = reinterpret_cast<float*>(smem + Gm::ML_OFF);
+  int* SLOT = reinterpret_cast<int*>(smem + Gm::SLOT_OFF);
+  float* sn = reinterpret_cast<float*>(smem + Gm::SN_OFF);
+  int* flag = reinterpret_cast<int*>(smem + Gm::FLAG_OFF);
+  float2* cs = reinterpret_cast<float2*>(smem + Gm::CS_OFF);
+  float* qs = reinterpret_cast<float*>(smem + Gm::QS_OFF);
+  uint16_t* kh = reinterpret_cast<uint16_t*>(smem + Gm::KH_OFF);
+  int* wrow = reinterpret_cast<int*>(smem + Gm::WROW_OFF) + warp * 2 * kWin * KG;
+  int* wmask = reinterpret_cast<int*>(smem + Gm::WMASK_OFF) + warp * 2 * kWin * KG;
+  uint64_t* step = reinterpret_cast<uint64_t*>(smem + Gm::STEP_OFF);
+  float* sig = reinterpret_cast<float*>(smem + Gm::SIG_OFF);
+  const uint32_t inbar = smem_addr(smem + Gm::INBAR_OFF);
+  uint8_t* in_slots = smem + Gm::IN_OFF;
 
-  // ---- unit table from caller metadata (not written by the preceding kernel)
+  // ---- unit table from caller metadata (no kernel of this library writes it)
   for (int u = threadIdx.x; u < U; u += kThreads) {
     const int b = u / Hkv;
     const int n = unit_length<PAGED>(c, b, a.max_len, cta == 0 && u - b * Hkv == 0, a.err);
+    int head = 0;
+    if constexpr (!PAGED) head = n > 0 ? c.ring_head[b] : 0;
     N[u] = n;
-    P[u + 1] = (unit_groups<PAGED>(c, b, n) + KG - 1) / KG;
+    P[u + 1] = (unit_groups<PAGED>(c, head, n) + KG - 1) / KG;
   }
-  if (threadIdx.x == 0) P[0] = 0;
+  if (threadIdx.x == 0) {
+    P[0] = 0;
+    mbar_init(inbar, 1);  // the input slots' barriers, used by the whole CTA
+    mbar_init(inbar + 8, 1);
+    fence_mbar_init();
+  }
   __syncthreads();
   block_scan_inclusive<kThreads>(P + 1, U);
   const int T = P[U];
-  const int g0 = static_cast<int>(static_cast<int64_t>(cta) * T / NC);
-  const int g1 = static_cast<int>(static_cast<int64_t>(cta + 1) * T / NC);
-  if (cta == 0)  // the combine locates each unit's segments from this table
-    for (int u = threadIdx.x; u <= U; u += kThreads) a.tiles[u] = P[u];
+
+  // ---- the split of the tiles over the grid. Pieces: when there are no more
+  // units than CTAs and cutting every unit into s = NC / U equal pieces (one
+  // CTA each) leaves the largest piece within 5/4 of a fair share, CTA
+  // u * s + k takes piece k of unit u - units mostly end inside one CTA and
+  // few partials cross CTAs. Otherwise stream-K: CTA c takes the tiles
+  // [c T / NC, (c + 1) T / NC) of all units laid end to end.
+  int max_tiles = 0;
+  for (int u = threadIdx.x; u < U; u += kThreads) max_tiles = max(max_tiles, P[u + 1] - P[u]);
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) max_tiles = max(max_tiles, __shfl_xor_sync(kFull, max_tiles, w));
+  if (lane == 0) SLOT[warp] = max_tiles;
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) max_tiles = max(max_tiles, SLOT[w]);
+  int pieces = 0;
+  if (U <= NC && T > 0) {
+    const int s = NC / U;
+    if (4 * ((max_tiles + s - 1) / s) <= 5 * ((T + NC - 1) / NC)) pieces = s;
+  }
+  int g0, g1;
+  if (pieces) {
+    const int u = cta / pieces, k = cta - u * pieces;
+    const int t = u < U ? P[u + 1] - P[u] : 0;
+    g0 = u < U ? P[u] + k * t / pieces : 0;
+    g1 = u < U ? P[u] + (k + 1) * t / pieces : 0;
+  } else {
+    g0 = static_cast<int>(static_cast<int64_t>(cta) * T / NC);
+    g1 = static_cast<int>(static_cast<int64_t>(cta + 1) * T / NC);
+  }
 
   // ---- this warp's tiles: g = g0 + warp + kWarps * it
   const int span = g1 - g0;
@@ -168,59 +403,157 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     for (int s = 0; s < NS; ++s) mbar_init(bar0 + 8 * s, 1);
     fence_mbar_init();
   }
-  __syncwarp();
+  for (int p = threadIdx.x; p < a.r / 2; p += kThreads) step[p] = a.rope_step[p];
 
-  const uint64_t policy = l2_evict_first_policy();
-  int u_iss = my_n > 0 ? unit_of(P, U, g0 + warp) : 0;
-  // Request tile `it` of this warp into stage it % NS (one lane).
-  auto issue = [&](int it) {
-    const int g = g0 + warp + kWarps * it;
-    while (P[u_iss + 1] <= g) ++u_iss;
-    const int u = u_iss;
+  // ---- the inputs of this CTA's units, staged ahead in two slots: q, k_new
+  // and v_new rows by bulk copy (thread 0), position and gate logits in
+  // registers (threads < G hold their head's logit)
+  auto next_unit = [&](int u) {  // the next unit with tiles in this CTA's range
+    for (++u; u < U && P[u] < g1; ++u)
+      if (P[u + 1] > P[u]) return u;
+    return U;
+  };
+  int n_staged = 0, n_used = 0;
+  int pos_nxt = 0;
+  float gate_nxt = 0.f;
+  auto stage = [&](int u) {
     const int b = u / Hkv, j = u - b * Hkv;
-    const int n = N[u];
-    const int gb = (g - P[u]) * KG;
-    const int gn = min(KG, unit_groups<PAGED>(c, b, n) - gb);
-    const uint32_t bar = bar0 + 8 * (it % NS);
-    const uint32_t kd = wsm_a + (it % NS) * Gm::STAGE;
-    mbar_arrive_expect_tx(bar, 2u * gn * Gm::GBYTES);
-    for (int kg = 0; kg < gn; ++kg) {
-      const int gi = gb + kg;
-      int row0;
+    if (threadIdx.x == 0) {
+      const uint32_t bar = inbar + 8 * (n_staged & 1);
+      const uint32_t dst = smem_addr(in_slots + (n_staged & 1) * Gm::IN_BYTES);
+      const uint32_t qbytes = G * D * 2;
+      mbar_arrive_expect_tx(bar, qbytes + 4u * D);
+      bulk_copy_g2s(dst + Gm::IN_Q, a.q + (static_cast<int64_t>(b) * Hkv + j) * G * D, qbytes, bar,
+                    l2_evict_first_policy());
+      bulk_copy_g2s(dst + Gm::IN_K, a.k_new + (static_cast<int64_t>(b) * Hkv + j) * D, 2u * D, bar,
+                    l2_evict_first_policy());
+      bulk_copy_g2s(dst + Gm::IN_V, a.v_new + (static_cast<int64_t>(b) * Hkv + j) * D, 2u * D, bar,
+                    l2_evict_first_policy());
+    }
+    pos_nxt = a.pos[b];
+    gate_nxt = (a.gate && threadIdx.x < G) ? bf16_to_f32(a.gate[(static_cast<int64_t>(b) * Hkv + j) * G + threadIdx.x]) : 0.f;
+    ++n_staged;
+  };
+  // wait for the oldest staged unit; its slot
+  auto take = [&](int& pos, float& gate_g) -> const uint8_t* {
+    const int s = n_used & 1;
+    if (!mbar_wait_bounded(inbar + 8 * s, (n_used >> 1) & 1)) raise_error(a.err, ERR_TIMEOUT);
+    pos = pos_nxt;
+    gate_g = gate_nxt;
+    ++n_used;
+    return in_slots + s * Gm::IN_BYTES;
+  };
+  const int u_first = span > 0 ? unit_of(P, U, g0) : U;
+  if (u_first < U) stage(u_first);  // the first unit of a range always has tiles in it
+
+  // Window w of this warp: tiles 32w..32w+31, one per lane. For each group of
+  // the tile: the first tensor row of its TMA boxes and its valid-row mask
+  // (0 = no such group). Stored in half (w & 1) of the warp's window arrays.
+  auto fill = [&](int w) {
+    const int x = w * kWin + lane;
+    int rows[KG], masks[KG];
+#pragma unroll
+    for (int kg = 0; kg < KG; ++kg) rows[kg] = masks[kg] = 0;
+    if (x < my_n) {
+      const int g = g0 + warp + kWarps * x;
+      const int u = unit_of(P, U, g);
+      const int b = u / Hkv, j = u - b * Hkv;
+      const int n = N[u];
       if constexpr (PAGED) {
         const int gpp = (c.P + kGroup - 1) / kGroup;
-        const int pi = gi / gpp;
-        int pg = c.block_table[static_cast<int64_t>(b) * c.bt_stride + pi];
-        if (pg < 0 || pg >= c.n_rows) {
-          raise_error(a.err, ERR_INDEX);
-          pg = 0;
-        }
-        row0 = (pg * Hkv + j) * c.P + (gi - pi * gpp) * kGroup;
-      } else {
-        const int nb = (c.R + kGroup - 1) / kGroup;
-        int pb = ring_first_block(c.ring_head[b], n, c.R) + gi;
-        if (pb >= nb) pb -= nb;
-        const int row = c.stream_rows ? c.stream_rows[b] : b;
-        row0 = (row * Hkv + j) * c.R + pb * kGroup;
-      }
+        const int groups = unit_groups<true>(c, 0, n);
 #pragma unroll
-      for (int x = 0; x < BOXES; ++x) {
-        tma_load_2d(kd + kg * Gm::GBYTES + x * kBoxBytes, &a.tmap_k, 64 * x, row0, bar, policy);
-        tma_load_2d(kd + Gm::KHALF + kg * Gm::GBYTES + x * kBoxBytes, &a.tmap_v, 64 * x, row0, bar,
-                    policy);
+        for (int kg = 0; kg < KG; ++kg) {
+          const int gi = (g - P[u]) * KG + kg;
+          if (gi < groups) {
+            const int pi = gi / gpp, gr = gi - pi * gpp;
+            int pg = c.block_table[static_cast<int64_t>(b) * c.bt_stride + pi];
+            if (pg < 0 || pg >= c.n_rows) {
+              raise_error(a.err, ERR_INDEX);
+              pg = 0;
+            }
+            rows[kg] = (pg * Hkv + j) * c.P + gr * kGroup;
+            masks[kg] = static_cast<int>(row_bits(0, min(c.P - gr * kGroup, n - (pi * c.P + gr * kGroup))));
+          }
+        }
+      } else {
+        const int R = c.R, nb = (R + kGroup - 1) / kGroup;
+        const int head = c.ring_head[b];
+        const int row = c.stream_rows ? c.stream_rows[b] : b;
+        const int groups = unit_groups<false>(c, head, n);
+        const int start = ring_start(head, n, R), end = start + n;  // valid: [start, end) mod R
+#pragma unroll
+        for (int kg = 0; kg < KG; ++kg) {
+          const int gi = (g - P[u]) * KG + kg;
+          if (gi < groups) {
+            int pb = (start >> 4) + gi;
+            if (pb >= nb) pb -= nb;
+            const int s0 = pb * kGroup;
+            rows[kg] = (row * Hkv + j) * R + s0;
+            uint32_t m = row_bits(start - s0, min(end, R) - s0);
+            if (end > R) m |= row_bits(-s0, end - R - s0);
+            masks[kg] = static_cast<int>(m);
+          }
+        }
+      }
+    }
+    int* wr = wrow + (w & 1) * kWin * KG;
+    int* wm = wmask + (w & 1) * kWin * KG;
+#pragma unroll
+    for (int kg = 0; kg < KG; ++kg) {
+      wr[lane * KG + kg] = rows[kg];
+      wm[lane * KG + kg] = masks[kg];
+    }
+    __syncwarp();
+  };
+  fill(0);
+  if (my_n > kWin) fill(1);
+
+  const uint64_t policy = l2_evict_first_policy();
+  // Request tile x of this warp into stage x % NS (one lane).
+  auto issue = [&](int x) {
+    const int* wr = wrow + ((x / kWin) & 1) * kWin * KG + (x % kWin) * KG;
+    const int* wm = wmask + ((x / kWin) & 1) * kWin * KG + (x % kWin) * KG;
+    int gn = 0;
+#pragma unroll
+    for (int kg = 0; kg < KG; ++kg) gn += wm[kg] != 0;
+    const uint32_t bar = bar0 + 8 * (x % NS);
+    const uint32_t kd = wsm_a + (x % NS) * Gm::STAGE;
+    mbar_arrive_expect_tx(bar, 2u * gn * Gm::GBYTES);
+#pragma unroll
+    for (int kg = 0; kg < KG; ++kg) {
+      if (kg < gn) {
+        const int row0 = wr[kg];
+#pragma unroll
+        for (int bx = 0; bx < BOXES; ++bx) {
+          tma_load_2d(kd + kg * Gm::GBYTES + bx * kBoxBytes, &a.tmap_k, 64 * bx, row0, bar, policy);
+          tma_load_2d(kd + Gm::KHALF + kg * Gm::GBYTES + bx * kBoxBytes, &a.tmap_v, 64 * bx, row0, bar,
+                      policy);
+        }
       }
     }
   };
+  // Ordering with the preceding launch on the stream, which may still run:
+  // it may be writing its new entries into its own cache, its outputs and its
+  // partials (the other half of the double-buffered workspace). This call's
+  // inputs, metadata and partials are never written by it. So the pass over
+  // the cache runs before waiting for it when its cache is a different one
+  // (a.early); the outputs and the write-back always come after the wait.
+  // Each CTA waits before it lets the next launch begin, so at most two
+  // calls are ever in flight.
+  bool waited = false;
+  auto wait_prev = [&]() {
+    if (!waited) {
+      pdl_wait();
+      pdl_trigger();
+      waited = true;
+    }
+  };
+  if (!a.early) wait_prev();
   if (lane == 0) {
     const int pre = my_n < NS ? my_n : NS;
-    for (int it = 0; it < pre; ++it) issue(it);
+    for (int x = 0; x < pre; ++x) issue(x);
   }
-
-  pdl_wait();  // the rotated, pre-scaled q of this call
-  pdl_trigger();
-
-  float* ML = reinterpret_cast<float*>(smem + Gm::ML_OFF);
-  int* SLOT = reinterpret_cast<int*>(smem + Gm::SLOT_OFF);
 
   // Per-lane ldmatrix offsets inside a group's 2 KB boxes (128-byte swizzle:
   // the 16-byte chunk index is XORed with the row mod 8). K (scores, A = K):
@@ -236,8 +569,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     voff[q] = rv * 128 + (((2 * q + (lm & 1)) ^ lr) << 4);
   }
   const int fg = lane >> 2, fc = 2 * (lane & 3);  // fragment row group, column pair
-  // heads of this lane's score / output columns (e = 0, 1): hi/lo columns of
-  // one head are lanes l and l ^ 2 (NT == 1) or tiles 0 and 1 (NT == 2)
+  // heads of this lane's score / output columns (e = 0, 1): the hi and lo
+  // columns of one head are lanes l and l ^ 2 (NT == 1) or tiles 0 and 1 (NT == 2)
   const int hbase = NT == 1 ? 2 * (lane & 1) : fc;
   const bool lo_lane = NT == 1 && (lane & 2) != 0;
 
@@ -245,25 +578,32 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
   int it = 0;
   int deferred = -1;
   bool first_seg = true;
-  for (int u = span > 0 ? unit_of(P, U, g0) : U; u < U && P[u] < g1; ++u) {
-    if (P[u + 1] == P[u]) continue;  // a unit with no cached keys
+  for (int u = u_first; u < U; u = next_unit(u)) {
     const int ge = min(g1, P[u + 1]);
-    const int b = u / Hkv, j = u - b * Hkv;
-    const int n = N[u];
 
-    // q^T as B fragments: column n = fg of tile t holds head (hi or lo part)
+    // ---- the unit's staged inputs; stage the next unit's meanwhile
+    int pos_u;
+    float gate_u;
+    const uint8_t* in_u = take(pos_u, gate_u);
+    const int u_nxt = next_unit(u);
+    __syncthreads();  // the slot about to be refilled was last read before this point
+    if (u_nxt < U) stage(u_nxt);
+
+    // ---- the unit's rotated q (all threads), then q^T as B fragments:
+    // column n = fg of tile t holds one head's hi or lo part
+    rotate_q<D, GP>(a, reinterpret_cast<const uint16_t*>(in_u + Gm::IN_Q), pos_u, step, qs, cs);
+    __syncthreads();
     uint32_t qb[KSTEPS][NT][2];
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       const int head = NT == 1 ? (fg & 3) : fg;
       const bool lo = NT == 1 ? fg >= 4 : t == 1;
-      const float* src = a.qhat + (static_cast<int64_t>(b) * Hkv * G + j * G + head) * D + fc;
+      const float* src = qs + head * D + fc;
 #pragma unroll
       for (int ks = 0; ks < KSTEPS; ++ks) {
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
-          float2 x = make_float2(0.f, 0.f);
-          if (head < G) x = *reinterpret_cast<const float2*>(src + ks * 16 + h2 * 8);
+          const float2 x = *reinterpret_cast<const float2*>(src + ks * 16 + h2 * 8);
           uint32_t hi, lw;
           split_bf16x2(x.x, x.y, hi, lw);
           qb[ks][t][h2] = lo ? lw : hi;
@@ -279,13 +619,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         for (int e = 0; e < 4; ++e) o[mt][t][e] = 0.f;
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     int last_stage = -1;
-    const int ngroups = unit_groups<PAGED>(c, b, n);
-    int ring_b0 = 0;
-    if constexpr (!PAGED) ring_b0 = ring_first_block(c.ring_head[b], n, c.R);
 
     for (;;) {
       const int g = g0 + warp + kWarps * it;
       if (it >= my_n || g >= ge) break;
+      // the window after next: its half was last read for tiles now behind
+      if (it >= kWin && (it & (kWin - 1)) == 0 && it + kWin < my_n) fill(it / kWin + 1);
       const int stg = it % NS;
       if (!failed) {
         // the whole warp agrees on the outcome, so the collectives below stay converged
@@ -296,30 +635,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         }
       }
       if (!failed) {
-        const int gb = (g - P[u]) * KG;
-        const int gn = min(KG, ngroups - gb);
-#pragma unroll 1
-        for (int kg = 0; kg < gn; ++kg) {
+        const int* wm = wmask + ((it / kWin) & 1) * kWin * KG + (it % kWin) * KG;
+#pragma unroll
+        for (int kg = 0; kg < KG; ++kg) {
+          const uint32_t mask = static_cast<uint32_t>(wm[kg]);
+          if (mask == 0u) break;  // the unit's last tile has fewer groups
           const uint32_t kbase = wsm_a + stg * Gm::STAGE + kg * Gm::GBYTES;
           const uint32_t vbase = kbase + Gm::KHALF;
-          // ---- which of the group's 16 rows are valid keys
-          const int gi = gb + kg;
-          const int r = lane & 15;
-          bool valid;
-          if constexpr (PAGED) {
-            const int gpp = (c.P + kGroup - 1) / kGroup;
-            const int pi = gi / gpp, off = (gi - pi * gpp) * kGroup + r;
-            valid = off < c.P && pi * c.P + off < n;
-          } else {
-            const int nb = (c.R + kGroup - 1) / kGroup;
-            int pb = ring_b0 + gi;
-            if (pb >= nb) pb -= nb;
-            const int slot = pb * kGroup + r;
-            int d = c.ring_head[b] - 1 - slot;
-            if (d < 0) d += c.R;
-            valid = slot < c.R && d < n;
-          }
-          const uint32_t mask = __ballot_sync(kFull, valid) & 0xffffu;
           if (mask != 0xffffu) {
             // zero the V rows of invalid keys (their probabilities are 0, but
             // the rows may hold NaN and 0 * NaN is NaN)
@@ -426,7 +748,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         if (g + kWarps >= ge) {
           deferred = it + NS;
         } else if (lane == 0 && !failed) {
-          fence_proxy_async_smem();
           issue(it + NS);
         }
       }
@@ -467,241 +788,146 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     }
     if (lane == 0) SLOT[warp] = last_stage;
     __syncthreads();
-    // ---- merge the warps' states for this segment into its partial slot
-    const int slot = first_seg ? cta : NC + u;
-    float* dst = a.part + static_cast<int64_t>(slot) * (GP * (D + 2));
-    for (int e = threadIdx.x; e < GP * D; e += kThreads) {
-      const int h = e / D;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ML[w * 2 * GP + h]);
-      float acc = 0.f;
-      if (M != -INFINITY) {
+    // ---- segment end: how many CTAs hold pieces of this unit, and where
+    // their partials are (candidate k: slot, and whether it holds tiles)
+    int c_lo = 0, first_slot = 0, nseg, S;
+    const int p0 = P[u], p1 = P[u + 1];
+    if (pieces) {
+      nseg = min(pieces, p1 - p0);
+      S = pieces;
+    } else {
+      nseg = unit_segments(p0, p1, T, NC, u, c_lo, first_slot);
+      S = static_cast<int>((static_cast<int64_t>(p1) * NC - 1) / T) - c_lo + 1;
+    }
+    auto cand_slot = [&](int k) { return pieces ? u * pieces + k : (k == 0 ? first_slot : c_lo + k); };
+    auto cand_ok = [&](int k) -> bool {
+      if (k >= S) return false;
+      if (pieces) return (k + 1) * (p1 - p0) / pieces > k * (p1 - p0) / pieces;
+      const int64_t cc = c_lo + k;
+      // candidate k > 0 is the first segment of CTA c_lo + k, unless that CTA got no tiles
+      return k == 0 || cc * T / NC < (cc + 1) * T / NC;
+    };
+    if (nseg == 1) {
+      // the whole unit lies in this CTA: the warps' states go straight into the output
+      new_token<D, GP>(a, qs, cs, in_u, gate_u, kh, sn, sig);
+      wait_prev();
+      finish_unit<D, GP, PAGED>(a, u, in_u, kh, sn, sig, [&](int g, int d, Merge8& mg) {
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
           const int st = SLOT[w];
-          if (st >= 0) {
-            const float* os = reinterpret_cast<const float*>(smem + (w * NS + st) * Gm::STAGE);
-            acc = fmaf(exp2_fast(ML[w * 2 * GP + h] - M), os[e], acc);
+          if (st < 0) continue;
+          const float* os = reinterpret_cast<const float*>(smem + (w * NS + st) * Gm::STAGE) + g * D + d;
+          const float4 x0 = *reinterpret_cast<const float4*>(os);
+          const float4 x1 = *reinterpret_cast<const float4*>(os + 4);
+          const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+          mg.add(ML[w * 2 * GP + g], ML[w * 2 * GP + GP + g], x);
+        }
+      });
+      if (deferred >= 0) {  // the merge buffers are free again
+        if (lane == 0 && !failed) issue(deferred);
+        deferred = -1;
+      }
+    } else {
+      // merge the warps' states into this segment's partial slot
+      const int slot = first_seg ? cta : NC + u;
+      float* dst = a.part + static_cast<int64_t>(slot) * (GP * (D + 2));
+      for (int e = threadIdx.x; e < GP * D; e += kThreads) {
+        const int h = e / D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ML[w * 2 * GP + h]);
+        float acc = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < kWarps; ++w) {
+            const int st = SLOT[w];
+            if (st >= 0) {
+              const float* os = reinterpret_cast<const float*>(smem + (w * NS + st) * Gm::STAGE);
+              acc = fmaf(exp2_fast(ML[w * 2 * GP + h] - M), os[e], acc);
+            }
           }
         }
+        dst[e] = acc;
       }
-      dst[e] = acc;
-    }
-    if (threadIdx.x < GP) {
-      const int h = threadIdx.x;
-      float M = -INFINITY;
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ML[w * 2 * GP + h]);
-      float L = 0.f;
-      if (M != -INFINITY)
-        for (int w = 0; w < kWarps; ++w) L = fmaf(exp2_fast(ML[w * 2 * GP + h] - M), ML[w * 2 * GP + GP + h], L);
-      dst[GP * D + h] = M;
-      dst[GP * D + GP + h] = L;
-    }
-    __syncthreads();
-    if (deferred >= 0) {
-      if (lane == 0 && !failed) {
-        fence_proxy_async_smem();
-        issue(deferred);
+      if (threadIdx.x < GP) {
+        const int h = threadIdx.x;
+        float M = -INFINITY;
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ML[w * 2 * GP + h]);
+        float L = 0.f;
+        if (M != -INFINITY)
+          for (int w = 0; w < kWarps; ++w) L = fmaf(exp2_fast(ML[w * 2 * GP + h] - M), ML[w * 2 * GP + GP + h], L);
+        dst[GP * D + h] = M;
+        dst[GP * D + GP + h] = L;
       }
-      deferred = -1;
+      // the new token's part of a combine, while the partial's stores drain
+      new_token<D, GP>(a, qs, cs, in_u, gate_u, kh, sn, sig);
+      if (deferred >= 0) {  // the merge buffers are free again
+        if (lane == 0 && !failed) issue(deferred);
+        deferred = -1;
+      }
+      // count this segment; the CTA finishing the unit's last segment combines it
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) *flag = atomicAdd(a.counters + u, 1) == nseg - 1;
+      __syncthreads();
+      if (*flag) {
+        __threadfence();
+        wait_prev();
+        const int stride = GP * (D + 2);
+        finish_unit<D, GP, PAGED>(a, u, in_u, kh, sn, sig, [&](int g, int d, Merge8& mg) {
+          for (int k0 = 0; k0 < S; k0 += 4) {
+            float m[4], l[4], x[4][8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int k = k0 + q;
+              const bool ok = cand_ok(k);
+              m[q] = -INFINITY;
+              l[q] = 0.f;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) x[q][i] = 0.f;
+              if (ok) {
+                const float* pk = a.part + static_cast<int64_t>(cand_slot(k)) * stride;
+                m[q] = __ldcg(pk + GP * D + g);
+                l[q] = __ldcg(pk + GP * D + GP + g);
+                const float4 y0 = __ldcg(reinterpret_cast<const float4*>(pk + g * D + d));
+                const float4 y1 = __ldcg(reinterpret_cast<const float4*>(pk + g * D + d + 4));
+                x[q][0] = y0.x; x[q][1] = y0.y; x[q][2] = y0.z; x[q][3] = y0.w;
+                x[q][4] = y1.x; x[q][5] = y1.y; x[q][6] = y1.z; x[q][7] = y1.w;
+              }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) mg.add(m[q], l[q], x[q]);
+          }
+        });
+        if (threadIdx.x == 0) a.counters[u] = 0;
+      }
     }
     first_seg = false;
   }
-}
 
-// ---------------------------------------------------------------- combine
-
-// One CTA per (dim chunk, KV head, stream); the G heads of the group each use
-// TPH consecutive lanes of one warp, 4 dims per lane.
-template <int TPH>
-__device__ __forceinline__ float group_sum(float x) {
-#pragma unroll
-  for (int w = TPH / 2; w >= 1; w >>= 1) x += __shfl_xor_sync(kFull, x, w);
-  return x;
-}
-template <int TPH>
-__device__ __forceinline__ float group_max(float x) {
-#pragma unroll
-  for (int w = TPH / 2; w >= 1; w >>= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, w));
-  return x;
-}
-
-template <int D, int TPH, bool PAGED>
-__global__ void __launch_bounds__(256) decode_combine_kernel(const CombineArgs a, int G, int GP) {
-  extern __shared__ float wsm[];  // [heads in block][max segments]: merge weights
-  const int chunk_d = TPH * 4;
-  const int dc = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
-  // the block is a whole number of warps; lanes past the G heads repeat the
-  // last head's arithmetic (for the shuffles) and store nothing
-  const int gb = threadIdx.x / TPH, t = threadIdx.x % TPH;
-  const bool active = gb < G;
-  const int g = active ? gb : G - 1;
-  const int d4 = dc * chunk_d + t * 4;
-  const int Hkv = a.Hkv, Hq = Hkv * G, h = j * G + g;
-  const CacheView& c = a.c;
-
-  // ---- caller inputs (not produced by the split kernel): before the wait
-  int64_t wb_off = -1;  // element offset of the new entry's row for KV head j
-  if constexpr (PAGED) {
-    int n = c.seq_len[b];
-    const int cap = min(a.max_len, c.bt_stride * c.P);
-    n = n < 0 ? 0 : (n > cap ? cap : n);
-    if (a.write_back) {
-      const int pi = n / c.P;
-      const int pg = pi < c.bt_stride ? c.block_table[static_cast<int64_t>(b) * c.bt_stride + pi] : -1;
-      if (pg >= 0 && pg < c.n_rows)
-        wb_off = ((static_cast<int64_t>(pg) * Hkv + j) * c.P + n % c.P) * D;
-      else if (dc == 0 && threadIdx.x == 0)
-        raise_error(a.err, ERR_INDEX);
-    }
-  } else {
-    const int row = c.stream_rows ? c.stream_rows[b] : b;
-    const int head = c.ring_head[b], cnt = c.ring_count[b];
-    if (!(row < 0 || row >= c.n_rows || head < 0 || head >= c.R || cnt < 0 || cnt > c.R))
-      wb_off = ((static_cast<int64_t>(row) * Hkv + j) * c.R + head) * D;
+  // units with no cached keys have no segments: CTA u % NC finishes them
+  for (int u = cta; u < U; u += NC) {
+    if (P[u + 1] != P[u]) continue;
+    __syncthreads();  // the slots, qs and cs may still be read by the previous combine
+    stage(u);
+    int pos_u;
+    float gate_u;
+    const uint8_t* in_u = take(pos_u, gate_u);
+    rotate_q<D, GP>(a, reinterpret_cast<const uint16_t*>(in_u + Gm::IN_Q), pos_u, step, qs, cs);
+    __syncthreads();
+    new_token<D, GP>(a, qs, cs, in_u, gate_u, kh, sn, sig);
+    wait_prev();
+    finish_unit<D, GP, PAGED>(a, u, in_u, kh, sn, sig, [](int, int, Merge8&) {});
   }
-  const uint2 vw = *reinterpret_cast<const uint2*>(a.v_new + (static_cast<int64_t>(b) * Hkv + j) * D + d4);
-  float sig = 1.f;
-  if (a.gate) sig = 1.f / (1.f + expf(-bf16_to_f32(a.gate[static_cast<int64_t>(b) * Hq + h])));
-
-  pdl_wait();  // partials and the tile table of the split kernel
-  pdl_trigger();
-
-  // ---- this unit's segments: CTAs c_lo..c_hi of the split grid
-  const int U = a.B * Hkv, u = b * Hkv + j, NC = a.split_ctas;
-  const int T = a.tiles[U];
-  const int p0 = a.tiles[u], p1 = a.tiles[u + 1];
-  int S = 0, c_lo = 0, first_slot = 0;
-  if (p1 > p0) {
-    // CTA of global tile x: floor(((x + 1) * NC - 1) / T)
-    c_lo = static_cast<int>((static_cast<int64_t>(p0 + 1) * NC - 1) / T);
-    const int c_hi = static_cast<int>((static_cast<int64_t>(p1) * NC - 1) / T);
-    S = c_hi - c_lo + 1;
-    const int begin_lo = static_cast<int>(static_cast<int64_t>(c_lo) * T / NC);
-    first_slot = begin_lo == p0 ? c_lo : NC + u;
-  }
-
-  // ---- loads first: the segments' (m, l) and their first output slices,
-  // q_hat and the new key entry - none depends on another
-  const int stride = GP * (D + 2);
-  auto seg = [&](int k) -> const float* {
-    return a.part + static_cast<int64_t>(k == 0 ? first_slot : c_lo + k) * stride;
-  };
-  // Segment k > 0 is the first segment of split CTA c_lo + k - unless that CTA
-  // got no tiles at all (possible when the call's keys are far below its
-  // planned bound), in which case it wrote nothing and is skipped.
-  auto seg_ok = [&](int k) -> bool {
-    if (k == 0) return true;
-    const int64_t cc = c_lo + k;
-    return cc * T / NC < (cc + 1) * T / NC;
-  };
-  constexpr int kPre = 4;
-  float mk = -INFINITY, lk = 0.f;
-  if (t < S && seg_ok(t)) {
-    const float* pk = seg(t);
-    mk = pk[GP * D + g];
-    lk = pk[GP * D + GP + g];
-  }
-  float4 ov[kPre];
-#pragma unroll
-  for (int x = 0; x < kPre; ++x)
-    ov[x] = x < S && seg_ok(x) ? *reinterpret_cast<const float4*>(seg(x) + g * D + d4)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-  constexpr int NQ = D / (4 * TPH);
-  const float* qh = a.qhat + (static_cast<int64_t>(b) * Hq + h) * D;
-  const uint16_t* kh = a.khat + (static_cast<int64_t>(b) * Hkv + j) * D;
-  float4 qv[NQ];
-  uint2 kv[NQ];
-#pragma unroll
-  for (int x = 0; x < NQ; ++x) {
-    qv[x] = *reinterpret_cast<const float4*>(qh + (t + x * TPH) * 4);
-    kv[x] = *reinterpret_cast<const uint2*>(kh + (t + x * TPH) * 4);
-  }
-
-  // ---- new token's score (base 2): q_hat (pre-scaled) . k_entry over all D
-  float dot = 0.f;
-#pragma unroll
-  for (int x = 0; x < NQ; ++x) {
-    dot = fmaf(qv[x].x, bf16_lo(kv[x].x), dot);
-    dot = fmaf(qv[x].y, bf16_hi(kv[x].x), dot);
-    dot = fmaf(qv[x].z, bf16_lo(kv[x].y), dot);
-    dot = fmaf(qv[x].w, bf16_hi(kv[x].y), dot);
-  }
-  const float s_new = group_sum<TPH>(dot);
-
-  // ---- merge: M over the segments and the new token, weights, L, outputs
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  auto fold = [&](float w, const float4& v) {
-    acc.x = fmaf(w, v.x, acc.x);
-    acc.y = fmaf(w, v.y, acc.y);
-    acc.z = fmaf(w, v.z, acc.z);
-    acc.w = fmaf(w, v.w, acc.w);
-  };
-  float M, L;
-  if (S <= TPH) {
-    // one segment per lane: weights stay in registers and are broadcast
-    M = group_max<TPH>(fmaxf(s_new, mk));
-    const float w = t < S ? exp2_fast(mk - M) : 0.f;
-    L = group_sum<TPH>(w * lk);
-    const int base = threadIdx.x - t;  // first lane of this head's group
-#pragma unroll
-    for (int x = 0; x < kPre; ++x) {
-      const float wx = __shfl_sync(kFull, w, (base + x) & 31);
-      if (x < S) fold(wx, ov[x]);
-    }
-    for (int k = kPre; k < S; ++k) {
-      const float wk = __shfl_sync(kFull, w, (base + k) & 31);
-      if (seg_ok(k)) fold(wk, *reinterpret_cast<const float4*>(seg(k) + g * D + d4));
-    }
-  } else {
-    M = mk;
-    for (int k = t + TPH; k < S; k += TPH)
-      if (seg_ok(k)) M = fmaxf(M, seg(k)[GP * D + g]);
-    M = group_max<TPH>(fmaxf(M, s_new));
-    L = 0.f;
-    for (int k = t; k < S; k += TPH) {
-      float w = 0.f;
-      if (seg_ok(k)) {
-        const float* pk = seg(k);
-        w = exp2_fast(pk[GP * D + g] - M);
-        L = fmaf(w, pk[GP * D + GP + g], L);
-      }
-      wsm[gb * a.split_ctas + k] = w;
-    }
-    L = group_sum<TPH>(L);
-    __syncwarp();
-#pragma unroll
-    for (int x = 0; x < kPre; ++x) fold(wsm[gb * a.split_ctas + x], ov[x]);
-    for (int k = kPre; k < S; ++k)
-      if (seg_ok(k)) fold(wsm[gb * a.split_ctas + k], *reinterpret_cast<const float4*>(seg(k) + g * D + d4));
-  }
-  // the new token joins as a length-1 score vector
-  const float wn = exp2_fast(s_new - M);
-  L += wn;
-  acc.x = fmaf(wn, bf16_lo(vw.x), acc.x);
-  acc.y = fmaf(wn, bf16_hi(vw.x), acc.y);
-  acc.z = fmaf(wn, bf16_lo(vw.y), acc.z);
-  acc.w = fmaf(wn, bf16_hi(vw.y), acc.w);
-  if (!active) return;
-  const float scale = sig / L;
-  *reinterpret_cast<float4*>(a.out + (static_cast<int64_t>(b) * Hq + h) * D + d4) =
-      make_float4(acc.x * scale, acc.y * scale, acc.z * scale, acc.w * scale);
-
-  // ---- write-back of the new entry, after every read of the cache (the split
-  // kernel has completed): the rotated bf16 key and the value
-  if (a.write_back && g == 0 && wb_off >= 0) {
-    *reinterpret_cast<uint2*>(c.k + wb_off + d4) = *reinterpret_cast<const uint2*>(kh + d4);
-    *reinterpret_cast<uint2*>(c.v + wb_off + d4) = vw;
-  }
+  wait_prev();
 }
 
 // ---------------------------------------------------------------- launch
 
 template <int D, int NT, bool PAGED>
-cudaError_t split_launch(const SplitArgs& a, int G, cudaStream_t s) {
+cudaError_t decode_launch(const DecodeArgs& a, int ctas, cudaStream_t s) {
   using Gm = Geo<D, NT>;
-  auto k = decode_split_kernel<D, NT, PAGED>;
+  auto k = decode_kernel<D, NT, PAGED>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM_MAX);
@@ -709,12 +935,12 @@ cudaError_t split_launch(const SplitArgs& a, int G, cudaStream_t s) {
     attr_set = true;
   }
   const size_t smem = 1024 + Gm::TAB_OFF + (2 * a.B * a.Hkv + 1) * sizeof(int);
-  return launch_pdl(k, dim3(a.ctas), dim3(kThreads), smem, s, a, G);
+  return launch_pdl(k, dim3(ctas), dim3(kThreads), smem, s, a);
 }
 
 template <int D, int NT>
-cudaError_t split_dispatch_paged(const SplitArgs& a, int G, cudaStream_t s) {
-  return a.c.paged ? split_launch<D, NT, true>(a, G, s) : split_launch<D, NT, false>(a, G, s);
+cudaError_t decode_dispatch_paged(const DecodeArgs& a, int ctas, cudaStream_t s) {
+  return a.c.paged ? decode_launch<D, NT, true>(a, ctas, s) : decode_launch<D, NT, false>(a, ctas, s);
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -756,25 +982,26 @@ cudaError_t encode_cache_maps(const CacheView& c, int Hkv, int D, CUtensorMap* k
   return cudaSuccess;
 }
 
-cudaError_t launch_decode_split(const SplitArgs& a, int D, int G, cudaStream_t s) {
-  const int GP = decode_group_pad(G);
+cudaError_t launch_decode(const DecodeArgs& a, int D, int ctas, cudaStream_t s) {
+  const int GP = decode_group_pad(a.G);
   if (a.B * a.Hkv > kMaxUnits) return cudaErrorNotSupported;
+  if (a.r > D || a.r % 2 != 0) return cudaErrorNotSupported;
   if (D == 256) {
-    if (GP == 4) return split_dispatch_paged<256, 1>(a, G, s);
-    if (GP == 8) return split_dispatch_paged<256, 2>(a, G, s);
+    if (GP == 4) return decode_dispatch_paged<256, 1>(a, ctas, s);
+    if (GP == 8) return decode_dispatch_paged<256, 2>(a, ctas, s);
   } else if (D == 128) {
-    if (GP == 4) return split_dispatch_paged<128, 1>(a, G, s);
-    if (GP == 8) return split_dispatch_paged<128, 2>(a, G, s);
+    if (GP == 4) return decode_dispatch_paged<128, 1>(a, ctas, s);
+    if (GP == 8) return decode_dispatch_paged<128, 2>(a, ctas, s);
   }
   return cudaErrorNotSupported;
 }
 
-int decode_split_tile_keys(int D, int G) {
+int decode_tile_keys(int D, int G) {
   if (decode_group_pad(G) == 0 || (D != 128 && D != 256)) return 0;
   return 256 / D * kGroup;
 }
 
-int decode_split_ctas_per_sm(int D, int G) {
+int decode_ctas_per_sm(int D, int G) {
   const int GP = decode_group_pad(G);
   int smem = 0;
   if (D == 256) smem = GP == 4 ? Geo<256, 1>::SMEM_MAX : GP == 8 ? Geo<256, 2>::SMEM_MAX : 0;
@@ -786,37 +1013,5 @@ int decode_split_ctas_per_sm(int D, int G) {
 }
 
 int decode_max_units() { return kMaxUnits; }
-
-cudaError_t launch_decode_combine(const CombineArgs& a, int D, int G, cudaStream_t s) {
-  const int GP = decode_group_pad(G);
-  if (GP == 0) return cudaErrorNotSupported;
-  // dims per CTA: enough CTAs to spread the partial reads, at most 32 lanes per head
-  const int units = a.B * a.Hkv;
-  int dsplit = (152 + units - 1) / units;
-  const int dmin = D / 128;  // TPH <= 32
-  const int dmax = D / 32;   // TPH >= 8
-  dsplit = dsplit < dmin ? dmin : (dsplit > dmax ? dmax : dsplit);
-  int p2 = 1;
-  while (p2 < dsplit) p2 <<= 1;
-  dsplit = p2 > dmax ? dmax : p2;
-  const int tph = D / 4 / dsplit;
-  const int threads = (G * tph + 31) / 32 * 32;
-  dim3 grid(dsplit, a.Hkv, a.B);
-  dim3 block(threads);
-  const size_t smem = static_cast<size_t>(threads / tph) * a.split_ctas * sizeof(float);
-  const bool paged = a.c.paged != 0;
-#define DATTN_COMBINE(DD, TT)                                                                     \
-  if (D == DD && tph == TT)                                                                       \
-    return paged ? launch_pdl(decode_combine_kernel<DD, TT, true>, grid, block, smem, s, a, G, GP) \
-                 : launch_pdl(decode_combine_kernel<DD, TT, false>, grid, block, smem, s, a, G, GP);
-  DATTN_COMBINE(256, 32)
-  DATTN_COMBINE(256, 16)
-  DATTN_COMBINE(256, 8)
-  DATTN_COMBINE(128, 32)
-  DATTN_COMBINE(128, 16)
-  DATTN_COMBINE(128, 8)
-#undef DATTN_COMBINE
-  return cudaErrorNotSupported;
-}
 
 }  // namespace dattn

@@ -57,43 +57,39 @@ struct RopeArgs {
   int* err;
 };
 
-// Query heads of a KV group as the decode kernels lay them out: 4 (G <= 4)
+// Query heads of a KV group as the decode kernel lays them out: 4 (G <= 4)
 // or 8 (G <= 8); 0 for a group size with no compiled kernel.
 inline int decode_group_pad(int G) { return G <= 0 ? 0 : (G <= 4 ? 4 : (G <= 8 ? 8 : 0)); }
 
-// Split-K pass over the cached keys of a decode call (stream-K: the grid of
-// `ctas` CTAs cuts the concatenated tiles of all (stream, KV head) units into
-// equal ranges). Partial slot of a segment: the CTA index for the first
-// segment of a CTA's range, ctas + unit for any later one.
-struct SplitArgs {
+// One decode call (RoPE of the new token, the pass over the cached keys, the
+// join in score space, gate, store, write-back) as one launch. Stream-K: the
+// grid cuts the concatenated tiles of all (stream, KV head) units into equal
+// ranges. Partial slot of a segment: the CTA index for the first segment of a
+// CTA's range, gridDim + unit for any later one; the CTA that finishes a
+// unit's last segment (per-unit counter) combines the unit.
+struct DecodeArgs {
   CUtensorMap tmap_k;          // the layer's K cache as a 2D [rows, D] bf16 tensor
   CUtensorMap tmap_v;          // (encode_cache_maps)
   CacheView c;
-  int B, Hkv;
-  int ctas;                    // grid size
+  int B, Hkv, G;
   int max_len;                 // host bound on cached length (paged)
-  const float* qhat;           // [B, Hq, D]
-  float* part;                 // [ctas + B*Hkv][GP*(D+2)]: o[GP][D], m[GP], l[GP]
-                               // (GP = decode_group_pad(G))
-  int* tiles;                  // [B*Hkv + 1] out: tile prefix over units
-  int* err;
-};
-
-// LSE combine + new-token join + gate + store + write-back.
-struct CombineArgs {
-  CacheView c;
-  int B, Hkv;
-  int split_ctas;              // grid size of the split pass
-  const int* tiles;            // [B*Hkv + 1] from the split pass
-  int max_len;
-  const float* qhat;           // [B, Hq, D]
-  const uint16_t* khat;        // [B, Hkv, D]
+  const uint16_t* q;           // [B, Hq, D]
+  const uint16_t* k_new;       // [B, Hkv, D]
   const uint16_t* v_new;       // [B, Hkv, D]
   const uint16_t* gate;        // [B, Hq] or null
-  const float* part;
+  const int32_t* pos;          // [B]
+  const uint64_t* rope_step;   // [r / 2] phase steps (rope_phase_step)
+  int r;
+  float q_scale;               // log2(e) / sqrt(D)
   float* out;                  // [B, Hq, D]
   int write_back;
+  float* part;                 // [ctas + B*Hkv][GP*(D+2)]: o[GP][D], m[GP], l[GP]
+                               // (GP = decode_group_pad(G))
+  int* counters;               // [B*Hkv] finished segments; zero between calls
   int* err;
+  int early;                   // nonzero: the preceding launch on the stream writes
+                               // no part of this cache, so the first cache loads may
+                               // start before it completes
 };
 
 struct AppendArgs {
@@ -144,10 +140,10 @@ struct VerifyCombineArgs {
 
 // Each returns cudaErrorNotSupported for a shape with no compiled kernel.
 cudaError_t launch_rope(const RopeArgs& a, cudaStream_t s);
-cudaError_t launch_decode_split(const SplitArgs& a, int D, int G, cudaStream_t s);
-cudaError_t launch_decode_combine(const CombineArgs& a, int D, int G, cudaStream_t s);
-// Tensor maps of a cache's K and V for the split pass: [n_rows * Hkv * (R or
-// P), D] bf16 rows, boxes of 16 rows x 64 elements, 128-byte swizzle.
+// Decode with `ctas` CTAs (at most decode_ctas_per_sm per SM).
+cudaError_t launch_decode(const DecodeArgs& a, int D, int ctas, cudaStream_t s);
+// Tensor maps of a cache's K and V for the decode kernel: [n_rows * Hkv * (R
+// or P), D] bf16 rows, boxes of 16 rows x 64 elements, 128-byte swizzle.
 cudaError_t encode_cache_maps(const CacheView& c, int Hkv, int D, CUtensorMap* k, CUtensorMap* v);
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_verify_split(const VerifySplitArgs& a, int D, cudaStream_t s);
@@ -156,12 +152,22 @@ cudaError_t launch_verify_combine(const VerifyCombineArgs& a, int D, cudaStream_
 constexpr int kVerifyTileKeys = 64;
 constexpr int kVerifyMaxUnits = 512;
 
-// Resident CTAs per SM of the split kernel for (D, G) (0 if unsupported).
-int decode_split_ctas_per_sm(int D, int G);
-// Keys per stage tile of the split kernel for (D, G).
-int decode_split_tile_keys(int D, int G);
+// Resident CTAs per SM of the decode kernel for (D, G) (0 if unsupported).
+int decode_ctas_per_sm(int D, int G);
+// Keys per stage tile of the decode kernel for (D, G).
+int decode_tile_keys(int D, int G);
 // Largest number of (stream, KV head) units of one decode call.
 int decode_max_units();
+
+// Launch order per stream, for early cache reads. A kernel launched with
+// programmatic stream serialization may run while the launch before it on the
+// stream finishes; that launch is the only one that can still be writing.
+// True when the last launch recorded on `stream` writes into the cache whose
+// K array is `cache_k`.
+bool prev_launch_writes(void* stream, const void* cache_k);
+// Record a launch made on `stream` that writes into the cache with K array
+// `cache_k` (null: writes no cache).
+void record_launch(void* stream, const void* cache_k);
 
 // Launch with programmatic stream serialization: the kernel may begin while
 // its predecessor in the stream finishes; every kernel here waits on the

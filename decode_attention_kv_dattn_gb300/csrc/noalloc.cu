@@ -7,19 +7,20 @@
 // latency-critical loop runs, or embedding layers that only receive raw device
 // pointers. dattn_create allocates the handle's workspace, so those callers
 // cannot use dattn_decode. This entry point needs no handle: its scratch space
-// (rotated q and k, the split partials, the tile table, the error word and the
-// RoPE frequency table) lives in one fixed-size array in device global memory
+// (the split partials, the per-unit segment counters, the error word and the
+// RoPE phase-step table) lives in one fixed-size array in device global memory
 // that the library defines at file scope. The caller passes only its inputs,
 // outputs and cache, exactly as for dattn_decode.
 //
 // The array is created when the library's module is loaded on a device and
 // stays there until the process exits. All calls on a device share it and it
 // keeps the last call's contents; every call rewrites what it reads (and
-// clears its error word first), but two calls that run on the GPU at the same
-// time - on different streams, or not ordered on one stream - race on it.
+// clears its error word and counters first), but two calls that run on the
+// GPU at the same time - on different streams, or not ordered on one stream -
+// race on it.
 //
-// The kernels are the same ones dattn_decode launches; only where their
-// scratch lives differs.
+// The kernel is the same one dattn_decode launches; only where its scratch
+// lives differs.
 #include <cmath>
 #include <mutex>
 
@@ -101,9 +102,9 @@ extern "C" DATTN_API int dattn_decode_noalloc(const dattn_config* cfg, int layer
     ds = d;
   }
 
-  // ---- the split grid, as dattn_decode plans it
-  const int tile_keys = decode_split_tile_keys(D, G);
-  const int resident = ds.sms * decode_split_ctas_per_sm(D, G);
+  // ---- the grid, as dattn_decode plans it
+  const int tile_keys = decode_tile_keys(D, G);
+  const int resident = ds.sms * decode_ctas_per_sm(D, G);
   if (tile_keys <= 0 || resident <= 0) return DATTN_EUNSUPPORTED;
   int64_t ctas = (static_cast<int64_t>(B) * Hkv * ((n_max + tile_keys - 1) / tile_keys) + 3) / 4;
   if (ctas > resident) ctas = resident;
@@ -116,12 +117,8 @@ extern "C" DATTN_API int dattn_decode_noalloc(const dattn_config* cfg, int layer
   off = align256(off + sizeof(int));
   const size_t freq_off = off;
   off = align256(off + static_cast<size_t>(half) * sizeof(uint64_t));
-  const size_t tiles_off = off;
-  off = align256(off + (static_cast<size_t>(B) * Hkv + 1) * sizeof(int));
-  const size_t qhat_off = off;
-  off = align256(off + static_cast<size_t>(B) * Hq * D * sizeof(float));
-  const size_t khat_off = off;
-  off = align256(off + static_cast<size_t>(B) * Hkv * D * sizeof(uint16_t));
+  const size_t counters_off = off;
+  off = align256(off + static_cast<size_t>(B) * Hkv * sizeof(int));
   const size_t part_off = off;
   off = align256(off + (static_cast<size_t>(ctas) + static_cast<size_t>(B) * Hkv) * GP * (D + 2) * sizeof(float));
   if (off > kNoAllocScratchBytes) return DATTN_EXCEEDS;
@@ -142,13 +139,18 @@ extern "C" DATTN_API int dattn_decode_noalloc(const dattn_config* cfg, int layer
   cv.bt_stride = cache->bt_stride;
   cv.seq_len = cache->seq_len;
   // the split pass reads the cache through tensor maps (host-side encoding)
-  SplitArgs sa{};
-  if (encode_cache_maps(cv, Hkv, D, &sa.tmap_k, &sa.tmap_v) != cudaSuccess) return DATTN_EUNSUPPORTED;
+  // the kernel reads the cache through tensor maps (host-side encoding)
+  DecodeArgs da{};
+  if (encode_cache_maps(cv, Hkv, D, &da.tmap_k, &da.tmap_v) != cudaSuccess) return DATTN_EUNSUPPORTED;
 
   uint64_t* rope_step = half > 0 ? reinterpret_cast<uint64_t*>(ds.base + freq_off) : nullptr;
-  // The error word accumulates bits, so it starts every call at zero; the
-  // RoPE phase-step table is rewritten from the host.
+  // The error word accumulates bits and the segment counters must start at
+  // zero, so both are cleared every call; the RoPE phase-step table is
+  // rewritten from the host.
+  int* counters = reinterpret_cast<int*>(ds.base + counters_off);
   if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return DATTN_ECUDA;
+  if (cudaMemsetAsync(counters, 0, static_cast<size_t>(B) * Hkv * sizeof(int), s) != cudaSuccess)
+    return DATTN_ECUDA;
   if (half > 0) {
     uint64_t f[128];
     if (half > 128) return DATTN_EUNSUPPORTED;
@@ -157,52 +159,27 @@ extern "C" DATTN_API int dattn_decode_noalloc(const dattn_config* cfg, int layer
       return DATTN_ECUDA;
   }
 
-  RopeArgs ra{};
-  ra.rows = B;
-  ra.Hq = Hq;
-  ra.Hkv = Hkv;
-  ra.D = D;
-  ra.r = L.rotary_dim;
-  ra.q = static_cast<const uint16_t*>(args->q);
-  ra.k = static_cast<const uint16_t*>(args->k_new);
-  ra.pos = args->pos;
-  ra.T = 1;
-  ra.rope_step = rope_step;
-  ra.q_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
-  ra.qhat = reinterpret_cast<float*>(ds.base + qhat_off);
-  ra.khat = reinterpret_cast<uint16_t*>(ds.base + khat_off);
-  ra.err = err;
-  cudaError_t e = launch_rope(ra, s);
+  da.c = cv;
+  da.B = B;
+  da.Hkv = Hkv;
+  da.G = G;
+  da.max_len = n_max;
+  da.q = static_cast<const uint16_t*>(args->q);
+  da.k_new = static_cast<const uint16_t*>(args->k_new);
+  da.v_new = static_cast<const uint16_t*>(args->v_new);
+  da.gate = static_cast<const uint16_t*>(args->gate);
+  da.pos = args->pos;
+  da.rope_step = rope_step;
+  da.r = L.rotary_dim;
+  da.q_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+  da.out = args->out;
+  da.write_back = args->write_back;
+  da.part = reinterpret_cast<float*>(ds.base + part_off);
+  da.counters = counters;
+  da.err = err;
+  da.early = !prev_launch_writes(stream, cache->k);
+  const cudaError_t e = launch_decode(da, D, static_cast<int>(ctas), s);
   if (e != cudaSuccess) return e == cudaErrorNotSupported ? DATTN_EUNSUPPORTED : DATTN_ECUDA;
-
-  sa.c = cv;
-  sa.B = B;
-  sa.Hkv = Hkv;
-  sa.ctas = static_cast<int>(ctas);
-  sa.max_len = n_max;
-  sa.qhat = ra.qhat;
-  sa.part = reinterpret_cast<float*>(ds.base + part_off);
-  sa.tiles = reinterpret_cast<int*>(ds.base + tiles_off);
-  sa.err = err;
-  e = launch_decode_split(sa, D, G, s);
-  if (e != cudaSuccess) return e == cudaErrorNotSupported ? DATTN_EUNSUPPORTED : DATTN_ECUDA;
-
-  CombineArgs ca{};
-  ca.c = cv;
-  ca.B = B;
-  ca.Hkv = Hkv;
-  ca.split_ctas = sa.ctas;
-  ca.tiles = sa.tiles;
-  ca.max_len = n_max;
-  ca.qhat = ra.qhat;
-  ca.khat = ra.khat;
-  ca.v_new = static_cast<const uint16_t*>(args->v_new);
-  ca.gate = static_cast<const uint16_t*>(args->gate);
-  ca.part = sa.part;
-  ca.out = args->out;
-  ca.write_back = args->write_back;
-  ca.err = err;
-  e = launch_decode_combine(ca, D, G, s);
-  if (e != cudaSuccess) return e == cudaErrorNotSupported ? DATTN_EUNSUPPORTED : DATTN_ECUDA;
+  record_launch(stream, args->write_back ? cache->k : nullptr);
   return DATTN_OK;
 }

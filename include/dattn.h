@@ -159,8 +159,9 @@ typedef struct {
 /* Create a handle on `device`: validates the config, uploads per-layer RoPE
  * phase-step tables (the angle per position of each pair, theta^(-2i/r), as
  * 64-bit fixed-point turns, computed on the host) and
- * allocates the workspace for the split-K partials. The handle owns that
- * memory until dattn_destroy. */
+ * allocates the workspace: the split-K partials and per-(stream, KV head)
+ * segment counters of decode, and the verify pass's buffers. The handle owns
+ * that memory until dattn_destroy. */
 DATTN_API int dattn_create(const dattn_config* cfg, int device, dattn_t** out);
 
 /* Bulk write (prefill or cache set-up): token t < count[b] of call row b goes
@@ -174,7 +175,15 @@ DATTN_API int dattn_append_kv(dattn_t* h, int layer, const dattn_cache* cache, i
                     const int32_t* count, const void* k, const void* v, int rotate,
                     dattn_stream_t stream);
 
-/* Decode attention for one layer (see dattn_decode_args). */
+/* Decode attention for one layer (see dattn_decode_args). One kernel launch.
+ * Ordering: calls on one handle share its workspace, so they must be ordered
+ * (one stream at a time, or streams joined by events). The launch may begin
+ * while the launch before it on the stream is still running: it then streams
+ * its cache early, but only when that earlier launch (a decode, verify or
+ * append of this library) does not write into the same cache; its outputs and
+ * the write-back always wait for the earlier launch to complete. Inputs (q,
+ * k_new, v_new, gate, pos, cache metadata) must not be produced by the
+ * immediately preceding launch if that launch is one of this library's. */
 DATTN_API int dattn_decode(dattn_t* h, int layer, const dattn_cache* cache, const dattn_decode_args* args,
                  dattn_stream_t stream);
 
@@ -198,16 +207,18 @@ DATTN_API void dattn_destroy(dattn_t* h);
  * a server that hands out its whole pool up front, or code that must not
  * allocate inside a latency-critical loop). Same operation, layouts and
  * arguments as dattn_decode for layer `layer` of `cfg`, but no handle: the
- * scratch space (rotated q/k, split partials, tile table, error word, RoPE
- * frequencies) lives in one 8 MiB array in device memory that the library
+ * scratch space (split partials, per-unit segment counters, error word, RoPE
+ * phase steps) lives in one 8 MiB array in device memory that the library
  * defines at file scope; every GPU that loads the library holds it until the
  * process exits. Nothing is allocated or freed by this call.
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
  *   - A call whose scratch would not fit in 8 MiB returns DATTN_EXCEEDS
- *     (about 2.4 MiB for 64 streams x 8 query heads x head_dim 256).
+ *     (about 1.2 MiB for 64 streams x 2 KV heads x 8 query heads x head_dim
+ *     256 on a 152-SM GPU).
  *   - All calls on a device share the array, which keeps the last call's
- *     contents; each call rewrites what it uses and clears its error word, but
+ *     contents; each call rewrites what it uses and clears its error word and
+ *     counters, but
  *     calls that overlap on the GPU (other streams, or unordered) race.
  *   - Device-side metadata errors are recorded in the array's error word and
  *     are not returned; only host-side checks produce the status. */
