@@ -28,17 +28,6 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
   return static_cast<uint16_t>(u >> 16);
 }
 
-// fp64 -> bf16 in one rounding, nearest even. The value is first narrowed to
-// fp32 toward zero with a sticky bit ("round to odd"); rounding that fp32
-// value to bf16 (8 significant bits, 16 fewer than fp32) then gives the same
-// result as rounding the fp64 value directly.
-__device__ __forceinline__ uint16_t f64_to_bf16(double t) {
-  float f = __double2float_rz(t);
-  uint32_t u = __float_as_uint(f);
-  if (static_cast<double>(f) != t && !isnan(t)) u |= 1u;
-  return f32_to_bf16(__uint_as_float(u));
-}
-
 // ------------------------------------------------------------------ RoPE angle
 
 // cos and sin of one RoPE pair's angle at position pos, as fp32 values.

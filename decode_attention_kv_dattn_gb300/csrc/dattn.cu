@@ -209,7 +209,8 @@ int dattn_create(const dattn_config* cfg, int device, dattn_t** out) {
   for (const dattn_layer_config& L : h->layers) {
     uint64_t* dev = nullptr;
     if (L.rotary_dim > 0) {
-      std::vector<uint64_t> f(L.rotary_dim / 2);
+      // whole 16-byte units: the decode kernel bulk-copies the table
+      std::vector<uint64_t> f((L.rotary_dim / 2 + 1) / 2 * 2, 0);
       for (int i = 0; i < L.rotary_dim / 2; ++i) f[i] = rope_phase_step(L.rope_theta, L.rotary_dim, i);
       if (cudaMalloc(&dev, f.size() * sizeof(uint64_t)) != cudaSuccess) return fail(DATTN_ECUDA);
       h->rope_step.push_back(dev);

@@ -56,6 +56,7 @@
 //    fragment becomes the PV operand in registers (movmatrix transposes);
 //    online softmax in base 2 runs on the score fragment, and the output is
 //    rescaled only when some head's running maximum moved.
+#include "bf16_exact.h"
 #include "common.cuh"
 #include "mma.cuh"
 
@@ -66,7 +67,7 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kMaxUnits = 1024;          // (stream, KV head) units per call
+constexpr int kMaxUnits = 512;           // (stream, KV head) units per call
 constexpr int kGroup = 16;               // keys per MMA group
 constexpr int kBoxBytes = kGroup * 128;  // one TMA box: 16 rows x 64 bf16
 constexpr int kWin = 32;                 // tiles per prefetch window (one per lane)
@@ -101,7 +102,7 @@ struct Geo {
   static constexpr int IN_BYTES = IN_V + D * 2;
   static constexpr int IN_OFF = (INBAR_OFF + 16 + 15) / 16 * 16;  // 2 input slots
   static constexpr int TAB_OFF = IN_OFF + 2 * IN_BYTES;
-  static constexpr int SMEM_MAX = 1024 + TAB_OFF + (2 * kMaxUnits + 1) * 4;
+  static constexpr int SMEM_MAX = 1024 + TAB_OFF + (4 * kMaxUnits + 1) * 4;  // P, N, ring head/row
   static_assert(D == 128 || D == 256, "head_dim");
   static_assert(GP * D * 4 <= STAGE, "a stage buffer holds one warp's partial output");
   static_assert(NS < kWin, "issue runs at most one window ahead");
@@ -211,8 +212,8 @@ __device__ __forceinline__ void rotate_q(const DecodeArgs& a, const uint16_t* sr
   }
 }
 
-// The new token of unit u = (b, j): its K entry into kh (bf16_RNE of the fp64
-// rotation with the cos/sin in cs - the value that is scored and stored), its
+// The new token of unit u = (b, j): its K entry into kh (the bf16 nearest to the
+// exact rotation with the cos/sin in cs - the value that is scored and stored), its
 // scores into sn (base 2, one per head, with the rotated q in qs) and the
 // heads' sigmoid(gate) into sig (gate_g: this thread's head's logit, threads <
 // G). `in` holds the unit's staged k_new and v_new rows. All threads of the
@@ -229,10 +230,10 @@ __device__ void new_token(const DecodeArgs& a, const float* qs, const float2* cs
     const int d0 = p < half ? p : a.r + 2 * (p - half);
     const int d1 = p < half ? p + half : d0 + 1;
     if (p < half) {
-      const double c64 = cs[p].x, s64 = cs[p].y;
-      const double x = bf16_to_f32(ksrc[d0]), y = bf16_to_f32(ksrc[d1]);
-      kh[d0] = f64_to_bf16(__dsub_rn(__dmul_rn(x, c64), __dmul_rn(y, s64)));
-      kh[d1] = f64_to_bf16(__dadd_rn(__dmul_rn(y, c64), __dmul_rn(x, s64)));
+      const uint32_t cb = __float_as_uint(cs[p].x), sb = __float_as_uint(cs[p].y);
+      const uint16_t x = ksrc[d0], y = ksrc[d1];
+      kh[d0] = bf16_dot2_exact(x, cb, y, sb ^ 0x80000000u);  // x c - y s
+      kh[d1] = bf16_dot2_exact(y, cb, x, sb);                // y c + x s
     } else {
       kh[d0] = ksrc[d0];
       kh[d1] = ksrc[d1];
@@ -330,6 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   const int NC = gridDim.x, cta = blockIdx.x;
   int* P = reinterpret_cast<int*>(smem + Gm::TAB_OFF);  // [U + 1] tile prefix over units
   int* N = P + U + 1;                                    // [U] cached keys per unit
+  int* HD = N + U;                                       // [U] ring: head slot
+  int* RW = HD + U;                                      // [U] ring: cache row
   float* ML = reinterpret_cast<float*>(smem + Gm::ML_OFF);
   int* SLOT = reinterpret_cast<int*>(smem + Gm::SLOT_OFF);
   float* sn = reinterpret_cast<float*>(smem + Gm::SN_OFF);
@@ -344,21 +347,30 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   const uint32_t inbar = smem_addr(smem + Gm::INBAR_OFF);
   uint8_t* in_slots = smem + Gm::IN_OFF;
 
+  const uint32_t bar0 = smem_addr(smem + Gm::BAR_OFF) + warp * NS * 8;
+  if (lane == 0) {
+    for (int s = 0; s < NS; ++s) mbar_init(bar0 + 8 * s, 1);  // this warp's stages
+    if (warp == 0) {
+      mbar_init(inbar, 1);  // the input slots, used by the whole CTA
+      mbar_init(inbar + 8, 1);
+    }
+    fence_mbar_init();
+  }
+
   // ---- unit table from caller metadata (no kernel of this library writes it)
   for (int u = threadIdx.x; u < U; u += kThreads) {
     const int b = u / Hkv;
     const int n = unit_length<PAGED>(c, b, a.max_len, cta == 0 && u - b * Hkv == 0, a.err);
     int head = 0;
-    if constexpr (!PAGED) head = n > 0 ? c.ring_head[b] : 0;
+    if constexpr (!PAGED) {
+      head = n > 0 ? c.ring_head[b] : 0;
+      HD[u] = head;
+      RW[u] = c.stream_rows ? c.stream_rows[b] : b;
+    }
     N[u] = n;
     P[u + 1] = (unit_groups<PAGED>(c, head, n) + KG - 1) / KG;
   }
-  if (threadIdx.x == 0) {
-    P[0] = 0;
-    mbar_init(inbar, 1);  // the input slots' barriers, used by the whole CTA
-    mbar_init(inbar + 8, 1);
-    fence_mbar_init();
-  }
+  if (threadIdx.x == 0) P[0] = 0;
   __syncthreads();
   block_scan_inclusive<kThreads>(P + 1, U);
   const int T = P[U];
@@ -398,12 +410,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   const int my_n = span > warp ? (span - warp + kWarps - 1) / kWarps : 0;
   uint8_t* wsm = smem + warp * NS * Gm::STAGE;
   const uint32_t wsm_a = smem_addr(wsm);
-  const uint32_t bar0 = smem_addr(smem + Gm::BAR_OFF) + warp * NS * 8;
-  if (lane == 0) {
-    for (int s = 0; s < NS; ++s) mbar_init(bar0 + 8 * s, 1);
-    fence_mbar_init();
-  }
-  for (int p = threadIdx.x; p < a.r / 2; p += kThreads) step[p] = a.rope_step[p];
 
   // ---- the inputs of this CTA's units, staged ahead in two slots: q, k_new
   // and v_new rows by bulk copy (thread 0), position and gate logits in
@@ -415,14 +421,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   };
   int n_staged = 0, n_used = 0;
   int pos_nxt = 0;
-  float gate_nxt = 0.f;
+  uint16_t gate_nxt = 0;  // raw bf16: converting here would wait for the load
   auto stage = [&](int u) {
     const int b = u / Hkv, j = u - b * Hkv;
     if (threadIdx.x == 0) {
       const uint32_t bar = inbar + 8 * (n_staged & 1);
       const uint32_t dst = smem_addr(in_slots + (n_staged & 1) * Gm::IN_BYTES);
       const uint32_t qbytes = G * D * 2;
-      mbar_arrive_expect_tx(bar, qbytes + 4u * D);
+      // the first staging also brings the layer's RoPE phase steps (the table
+      // is allocated in whole 16-byte units)
+      const uint32_t sbytes = n_staged == 0 ? (static_cast<uint32_t>(a.r / 2) * 8u + 15u) / 16u * 16u : 0u;
+      mbar_arrive_expect_tx(bar, qbytes + 4u * D + sbytes);
+      if (sbytes) bulk_copy_g2s(smem_addr(step), a.rope_step, sbytes, bar, l2_evict_first_policy());
       bulk_copy_g2s(dst + Gm::IN_Q, a.q + (static_cast<int64_t>(b) * Hkv + j) * G * D, qbytes, bar,
                     l2_evict_first_policy());
       bulk_copy_g2s(dst + Gm::IN_K, a.k_new + (static_cast<int64_t>(b) * Hkv + j) * D, 2u * D, bar,
@@ -431,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
                     l2_evict_first_policy());
     }
     pos_nxt = a.pos[b];
-    gate_nxt = (a.gate && threadIdx.x < G) ? bf16_to_f32(a.gate[(static_cast<int64_t>(b) * Hkv + j) * G + threadIdx.x]) : 0.f;
+    gate_nxt = (a.gate && threadIdx.x < G) ? a.gate[(static_cast<int64_t>(b) * Hkv + j) * G + threadIdx.x] : 0;
     ++n_staged;
   };
   // wait for the oldest staged unit; its slot
@@ -439,12 +449,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     const int s = n_used & 1;
     if (!mbar_wait_bounded(inbar + 8 * s, (n_used >> 1) & 1)) raise_error(a.err, ERR_TIMEOUT);
     pos = pos_nxt;
-    gate_g = gate_nxt;
+    gate_g = bf16_to_f32(gate_nxt);
     ++n_used;
     return in_slots + s * Gm::IN_BYTES;
   };
   const int u_first = span > 0 ? unit_of(P, U, g0) : U;
-  if (u_first < U) stage(u_first);  // the first unit of a range always has tiles in it
 
   // Window w of this warp: tiles 32w..32w+31, one per lane. For each group of
   // the tile: the first tensor row of its TMA boxes and its valid-row mask
@@ -478,8 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         }
       } else {
         const int R = c.R, nb = (R + kGroup - 1) / kGroup;
-        const int head = c.ring_head[b];
-        const int row = c.stream_rows ? c.stream_rows[b] : b;
+        const int head = HD[u], row = RW[u];
         const int groups = unit_groups<false>(c, head, n);
         const int start = ring_start(head, n, R), end = start + n;  // valid: [start, end) mod R
 #pragma unroll
@@ -549,6 +557,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       waited = true;
     }
   };
+  // the first unit's inputs go first: behind the tiles they would arrive late
+  if (u_first < U) stage(u_first);  // the first unit of a range always has tiles in it
   if (!a.early) wait_prev();
   if (lane == 0) {
     const int pre = my_n < NS ? my_n : NS;
@@ -593,6 +603,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     // column n = fg of tile t holds one head's hi or lo part
     rotate_q<D, GP>(a, reinterpret_cast<const uint16_t*>(in_u + Gm::IN_Q), pos_u, step, qs, cs);
     __syncthreads();
+    // the new token's K entry and scores now, while the first tiles arrive;
+    // they are used when this CTA finishes the unit
+    new_token<D, GP>(a, qs, cs, in_u, gate_u, kh, sn, sig);
     uint32_t qb[KSTEPS][NT][2];
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
@@ -809,7 +822,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     };
     if (nseg == 1) {
       // the whole unit lies in this CTA: the warps' states go straight into the output
-      new_token<D, GP>(a, qs, cs, in_u, gate_u, kh, sn, sig);
       wait_prev();
       finish_unit<D, GP, PAGED>(a, u, in_u, kh, sn, sig, [&](int g, int d, Merge8& mg) {
 #pragma unroll
@@ -859,8 +871,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         dst[GP * D + h] = M;
         dst[GP * D + GP + h] = L;
       }
-      // the new token's part of a combine, while the partial's stores drain
-      new_token<D, GP>(a, qs, cs, in_u, gate_u, kh, sn, sig);
+      __syncthreads();  // every read of the merge buffers is done
       if (deferred >= 0) {  // the merge buffers are free again
         if (lane == 0 && !failed) issue(deferred);
         deferred = -1;
@@ -934,7 +945,7 @@ cudaError_t decode_launch(const DecodeArgs& a, int ctas, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const size_t smem = 1024 + Gm::TAB_OFF + (2 * a.B * a.Hkv + 1) * sizeof(int);
+  const size_t smem = 1024 + Gm::TAB_OFF + (4 * a.B * a.Hkv + 1) * sizeof(int);
   return launch_pdl(k, dim3(ctas), dim3(kThreads), smem, s, a);
 }
 

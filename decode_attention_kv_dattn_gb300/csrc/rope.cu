@@ -8,10 +8,10 @@
 // Rounding contract of the K entry (the value stored in the cache and scored
 // for the new token): c and s are the fp32 cosine and sine that rope_cos_sin
 // derives from the pair's fixed-point phase step (an exact phase, then an fp32
-// polynomial); the entry is bf16_RNE(x*c - y*s) evaluated in fp64. Each
-// product of a bf16 and an fp32 value is exact in fp64, so the only roundings
-// are the fp64 difference and the final bf16 step. q is rotated in fp32 and pre-scaled by
+// polynomial); the entry is the bf16 nearest to the exact x*c - y*s (ties to
+// even), computed in integer arithmetic (bf16_dot2_exact). q is rotated in fp32 and pre-scaled by
 // log2(e)/sqrt(D) so that the split kernel's scores are in base-2 units.
+#include "bf16_exact.h"
 #include "common.cuh"
 
 namespace dattn {
@@ -111,10 +111,10 @@ __global__ void __launch_bounds__(kRowThreads) rope_kernel(const RopeArgs a) {
     } else {
       uint16_t* dst = a.khat + (static_cast<int64_t>(row) * a.Hkv + (hh - a.Hq)) * a.D;
       if (p < half) {
-        const double c64 = cs_c[p], s64 = cs_s[p];
-        const double xd = x, yd = y;
-        dst[d0] = f64_to_bf16(__dsub_rn(__dmul_rn(xd, c64), __dmul_rn(yd, s64)));
-        dst[d1] = f64_to_bf16(__dadd_rn(__dmul_rn(yd, c64), __dmul_rn(xd, s64)));
+        const uint32_t cb = __float_as_uint(cs_c[p]), sb = __float_as_uint(cs_s[p]);
+        const uint16_t xh = static_cast<uint16_t>(xy[k] & 0xffffu), yh = static_cast<uint16_t>(xy[k] >> 16);
+        dst[d0] = bf16_dot2_exact(xh, cb, yh, sb ^ 0x80000000u);  // x c - y s
+        dst[d1] = bf16_dot2_exact(yh, cb, xh, sb);                // y c + x s
       } else {
         dst[d0] = static_cast<uint16_t>(xy[k] & 0xffffu);
         dst[d1] = static_cast<uint16_t>(xy[k] >> 16);
@@ -184,14 +184,11 @@ __global__ void __launch_bounds__(kRopeThreads) append_kernel(const AppendArgs a
       const int i = job;
       float cf, sf;
       rope_cos_sin(pos, a.rope_step[i], cf, sf);
-      const double c64 = cf, s64 = sf;
+      const uint32_t cb = __float_as_uint(cf), sb = __float_as_uint(sf);
       for (int h = 0; h < a.Hkv; ++h) {
-        const double x = bf16_to_f32(a.k[src0 + h * a.D + i]);
-        const double y = bf16_to_f32(a.k[src0 + h * a.D + i + half]);
-        c.k[dst0 + h * head_stride + i] =
-            f64_to_bf16(__dsub_rn(__dmul_rn(x, c64), __dmul_rn(y, s64)));
-        c.k[dst0 + h * head_stride + i + half] =
-            f64_to_bf16(__dadd_rn(__dmul_rn(y, c64), __dmul_rn(x, s64)));
+        const uint16_t x = a.k[src0 + h * a.D + i], y = a.k[src0 + h * a.D + i + half];
+        c.k[dst0 + h * head_stride + i] = bf16_dot2_exact(x, cb, y, sb ^ 0x80000000u);
+        c.k[dst0 + h * head_stride + i + half] = bf16_dot2_exact(y, cb, x, sb);
       }
     } else {
       const int d = a.r + (job - half);

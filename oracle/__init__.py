@@ -42,6 +42,8 @@ class Oracle:
         L = self.lib
         L.oracle_bf16_round.argtypes = [_D]
         L.oracle_bf16_round.restype = ctypes.c_uint16
+        L.oracle_bf16_dot2.argtypes = [ctypes.c_uint16, ctypes.c_float, ctypes.c_uint16, ctypes.c_float]
+        L.oracle_bf16_dot2.restype = ctypes.c_uint16
         L.oracle_rope_cos_sin.argtypes = [_I, _D, _L, _I, ctypes.POINTER(_D), ctypes.POINTER(_D)]
         L.oracle_rope_cos_sin.restype = None
         L.oracle_rope_f64.argtypes = [_P, _I, _I, _D, _L, _P]
@@ -71,6 +73,10 @@ class Oracle:
     # ---- numbers and RoPE
     def bf16_round(self, t: float) -> int:
         return int(self.lib.oracle_bf16_round(float(t)))
+
+    def bf16_dot2(self, x_bits, c, y_bits, s) -> int:
+        """bf16 bits nearest to the exact x*c + y*s (x, y bf16 bits; c, s fp32)."""
+        return int(self.lib.oracle_bf16_dot2(int(x_bits), float(c), int(y_bits), float(s)))
 
     def rope_cos_sin(self, r, theta, pos, i):
         c, s = _D(), _D()

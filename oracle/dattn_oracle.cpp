@@ -91,6 +91,32 @@ uint16_t bf16_round(double t) {
   return static_cast<uint16_t>(u >> 16);
 }
 
+// Round the exact sum p + q of two fp64 values to the nearest bf16, ties to
+// even (reading R6: no intermediate rounding). hi = fl64(p + q) and the exact
+// error lo (Knuth's TwoSum) give p + q = hi + lo exactly, with |lo| at most
+// half an fp64 ulp of hi. A bf16 rounding tie is an fp64 value, so lo can
+// only matter when hi is exactly on a tie; then it says which side p + q is.
+uint16_t bf16_round_sum(double p, double q) {
+  const double hi = p + q;
+  if (!std::isfinite(hi) || hi == 0.0) return bf16_round(hi);
+  const double bv = hi - p;
+  const double lo = (p - (hi - bv)) + (q - bv);
+  int e2;
+  std::frexp(std::fabs(hi), &e2);
+  int lead = e2 - 1;
+  if (lead < -126) lead = -126;
+  const double spacing = std::ldexp(1.0, lead - 7);
+  const double units = hi / spacing;  // exact: a power-of-two scaling
+  const double below = std::floor(units);
+#if ORACLE_MUTATION == 17
+  (void)below;
+  return bf16_round(hi);  // planted: the fp64-rounded sum decides ties
+#else
+  if (lo == 0.0 || units - below != 0.5) return bf16_round(hi);
+  return bf16_round((below + (lo > 0.0 ? 1.0 : 0.0)) * spacing);
+#endif
+}
+
 // ---------------------------------------------------------------- RoPE (R1, R6)
 
 // cos and sin of the rotation of pair i at position pos, as fp32 values, by
@@ -184,10 +210,20 @@ void rope_rotate(const uint16_t* x, int D, int r, double theta, int64_t pos, dou
 }
 
 // The K entry the layer hands back: the rotated key rounded to bf16 (R6).
+// Each element is x*c - y*s or y*c + x*s with both products exact in fp64;
+// their exact sum is rounded once, to the nearest bf16.
 void rope_entry(const uint16_t* x, int D, int r, double theta, int64_t pos, uint16_t* entry) {
   std::vector<double> tmp(D);
   rope_rotate(x, D, r, theta, pos, tmp.data());
   for (int d = 0; d < D; ++d) entry[d] = bf16_round(tmp[d]);
+  const int half = r / 2;
+  for (int i = 0; i < half; ++i) {
+    double c, s;
+    rope_cos_sin(r, theta, pos, i, &c, &s);
+    const double a = bf16_value(x[i]), b = bf16_value(x[i + half]);
+    entry[i] = bf16_round_sum(a * c, -(b * s));
+    entry[i + half] = bf16_round_sum(b * c, a * s);
+  }
 }
 
 double sigmoid(double g) {
@@ -365,6 +401,11 @@ extern "C" {
 // ----- numbers and RoPE, exposed for the pins
 
 uint16_t oracle_bf16_round(double t) { return bf16_round(t); }
+
+// bf16 nearest to the exact x*c + y*s (x, y bf16 bits; c, s fp32), for the pins.
+uint16_t oracle_bf16_dot2(uint16_t x, float c, uint16_t y, float s) {
+  return bf16_round_sum(bf16_value(x) * static_cast<double>(c), bf16_value(y) * static_cast<double>(s));
+}
 
 // cos and sin of pair i's rotation at pos (rope_cos_sin), for the pins.
 void oracle_rope_cos_sin(int r, double theta, int64_t pos, int i, double* c, double* s) {

@@ -164,6 +164,91 @@ def pin_rope_norm_and_relative_position(o):
             close([other], [base], 1e-4, f"relative position shift {shift}")
 
 
+def _bf16_of_fraction(v):
+    """bf16 bits of the Fraction v rounded to nearest, ties to even (8
+    significant bits, exponent range of fp32, subnormal grid 2^-133)."""
+    from fractions import Fraction
+    if v == 0:
+        return 0
+    sign = 0x8000 if v < 0 else 0
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    spacing = Fraction(2) ** (max(e, -126) - 7)
+    units = a / spacing
+    k = units.numerator // units.denominator
+    rem = units - k
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and k % 2 == 1):
+        k += 1
+    val = k * spacing
+    if val >= Fraction(2) ** 128:
+        return sign | 0x7F80
+    bits = int(np.array([float(val)], np.float32).view(np.uint32)[0]) >> 16
+    return sign | bits
+
+
+def _f32_bits_value(bits):
+    return float(np.array([bits], np.uint32).view(np.float32)[0])
+
+
+def pin_bf16_dot2_exact_against_fractions(o):
+    """The K entry's rounding: the bf16 nearest to the exact x*c + y*s, checked
+    against rational arithmetic on random operands of every scale, products
+    that land on rounding ties, and tiny second products."""
+    from fractions import Fraction
+    rng = np.random.default_rng(21)
+    cases = []
+    for _ in range(3000):
+        xb = int(rng.integers(0, 1 << 16)) & 0xFFFF
+        yb = int(rng.integers(0, 1 << 16)) & 0xFFFF
+        if (xb & 0x7F80) == 0x7F80 or (yb & 0x7F80) == 0x7F80:
+            continue
+        cb = int(rng.integers(0, 1 << 32))
+        sb = int(rng.integers(0, 1 << 32))
+        if (cb & 0x7F800000) == 0x7F800000 or (sb & 0x7F800000) == 0x7F800000:
+            continue
+        cases.append((xb, cb, yb, sb))
+    for _ in range(2000):  # ordinary magnitudes, like rotated N(0,1) keys
+        x = float(rng.standard_normal())
+        y = float(rng.standard_normal())
+        ang = float(rng.uniform(-7, 7))
+        xb = int(np.array([x], np.float32).view(np.uint32)[0]) >> 16
+        yb = int(np.array([y], np.float32).view(np.uint32)[0]) >> 16
+        cb = int(np.array([math.cos(ang)], np.float32).view(np.uint32)[0])
+        sb = int(np.array([math.sin(ang)], np.float32).view(np.uint32)[0])
+        cases.append((xb, cb, yb, sb))
+    # x*c on a bf16 tie, y*s far below it (on either side), or exactly zero
+    for k in range(1, 127, 2):
+        c = 1.0 + k * 2.0 ** -8
+        cb = int(np.array([c], np.float32).view(np.uint32)[0])
+        for yb in (67 << 7, (67 << 7) | 0x8000, 0):
+            cases.append((0x3F80, cb, yb, 0x3F800000))
+    for xb, cb, yb, sb in cases:
+        c, s = _f32_bits_value(cb), _f32_bits_value(sb)
+        want = (_bf16_of_fraction(Fraction(bf16_val(xb)[()]) * Fraction(c) + Fraction(bf16_val(yb)[()]) * Fraction(s))
+                if not (c == 0 and s == 0) else None)
+        got = o.bf16_dot2(xb, c, yb, s)
+        if want is None:
+            continue
+        if want == 0 and got == 0x8000:
+            got = 0  # the sign of an exact zero is IEEE's; only the value is pinned here
+        assert got == want, f"bf16({bf16_val(xb)[()]}*{c} + {bf16_val(yb)[()]}*{s}) = {got:#06x}, want {want:#06x}"
+
+
+def pin_rope_entry_matches_rotation(o):
+    """The K entry is the rotation of the key rounded to bf16: away from bf16
+    rounding ties it equals the fp64 rotation rounded once."""
+    for seed, (r, theta, pos) in enumerate(((256, 1e4, 300), (64, 5e6, 4096), (128, 1e6, 77777))):
+        x = rand_bf16(256, 40 + seed)
+        ent = o.rope_bf16(x, r, theta, pos)
+        rot = o.rope_f64(x, r, theta, pos)
+        want = np.array([o.bf16_round(v) for v in rot], np.uint16)
+        assert np.array_equal(ent, want), f"r={r}: {np.sum(ent != want)} entries differ"
+
+
 def pin_rope_entry_identity(o):
     """At position 0, and with no rotary dims, the K entry is the key itself."""
     x = rand_bf16(256, 14)
