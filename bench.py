@@ -246,7 +246,7 @@ class Step(Workload):
                                    f"head_dim 256, {B} streams, context {context}",
                        "streams": B, "context": context, "sliding_ring_slots": 511,
                        "full_page_size": 16, "gate": True, "write_back": True}
-        self.kernel = f"decode_split (full layers, {B} streams x {context} tokens)"
+        self.kernel = f"decode_kernel (full layers, {B} streams x {context} tokens)"
 
     def run_call(self, l, stream=None):
         L = self.layers[l]
@@ -320,7 +320,7 @@ class DecodeCall(Workload):
             io += b_
         self.bytes_step, self.tokens_step = kv + io, sum(n + 1 for n in self.lens)
         self.dominant, self.others, self.dominant_kv_bytes = [0], [], kv
-        self.kernel = "decode_split (" + self.config["workload"].split(":")[0] + ")"
+        self.kernel = "decode_kernel (" + self.config["workload"].split(":")[0] + ")"
 
     def run_call(self, i, stream=None):
         self.h.decode(0, self.desc, self.q, self.k_new, self.v_new, self.pos, self.out, gate=self.g,
@@ -451,7 +451,7 @@ def time_graph(step, K, W, world):
 
 def time_layers(step, K):
     """Per-call device time (CUDA events on the launch stream around each call:
-    the call's RoPE, split and combine kernels)."""
+    every kernel of the call: one for decode, three for verify)."""
     n = step.ncalls
     reps = max(3, min(K, 50))
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
