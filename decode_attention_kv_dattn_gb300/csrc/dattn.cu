@@ -385,7 +385,8 @@ int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, const dattn_ve
                  dattn_stream_t stream) {
   if (!h || !args || layer < 0 || layer >= static_cast<int>(h->layers.size())) return DATTN_EINVAL;
   const dattn_layer_config& L = h->layers[layer];
-  if (L.cache_kind != DATTN_CACHE_PAGED) return DATTN_EUNSUPPORTED;
+  // the prefix pass reads pages as 16-row groups
+  if (L.cache_kind != DATTN_CACHE_PAGED || L.page_size % 16 != 0) return DATTN_EUNSUPPORTED;
   int rc = check_cache(L, cache);
   if (rc != DATTN_OK) return rc;
   const int S = args->num_streams, T = args->rows;
@@ -399,6 +400,9 @@ int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, const dattn_ve
   DeviceGuard guard(h->device);
   if (!guard.ok) return DATTN_ECUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  VerifySplitArgs va{};
+  va.c = make_view(h, L, cache);
+  if (encode_cache_maps(va.c, h->Hkv, h->D, &va.tmap_k, &va.tmap_v) != cudaSuccess) return DATTN_EUNSUPPORTED;
 
   RopeArgs ra{};
   ra.rows = S * T;
@@ -424,8 +428,6 @@ int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, const dattn_ve
   int64_t ctas = (tiles + 1) / 2;
   if (ctas > h->num_sms) ctas = h->num_sms;
   if (ctas < 1) ctas = 1;
-  VerifySplitArgs va{};
-  va.c = make_view(h, L, cache);
   va.S = S;
   va.T = T;
   va.Hkv = h->Hkv;

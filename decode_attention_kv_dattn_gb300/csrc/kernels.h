@@ -109,7 +109,9 @@ struct AppendArgs {
 // over (stream, KV head) units, the G*T rows of a unit in one 128-row MMA).
 // Partial slot layout: [ctas + S*Hkv][G*T rows][D + 4] fp32 (o[D], m, l, pad).
 struct VerifySplitArgs {
-  CacheView c;                 // paged; seq_len = prefix lengths
+  CUtensorMap tmap_k;          // the layer's K and V caches as 2D [rows, D] bf16
+  CUtensorMap tmap_v;          // tensors (encode_cache_maps)
+  CacheView c;                 // paged, page size a multiple of 16; seq_len = prefix lengths
   int S, T, Hkv, G;
   int ctas;
   int max_len;
@@ -149,7 +151,7 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_verify_split(const VerifySplitArgs& a, int D, cudaStream_t s);
 cudaError_t launch_verify_combine(const VerifyCombineArgs& a, int D, cudaStream_t s);
 // Keys per tile of the verify pass and its largest unit count.
-constexpr int kVerifyTileKeys = 64;
+constexpr int kVerifyTileKeys = 32;
 constexpr int kVerifyMaxUnits = 512;
 
 // Resident CTAs per SM of the decode kernel for (D, G) (0 if unsupported).

@@ -28,6 +28,16 @@ __host__ __device__ constexpr uint32_t f16_idesc(int M, int N, int ab_type, bool
 }
 
 // D[tmem] (+)= A[smem] * B[smem]; issued by one thread.
+// D (tmem) (+)= A (tmem: lane = row, each 32-bit column two consecutive K
+// elements) * B (shared-memory descriptor).
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                       bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate ? 1u : 0u));
+}
+
 __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                     bool accumulate) {
   asm volatile(

@@ -10,10 +10,12 @@
 //    unit is one 128-row MMA tile (G*T <= 128): S = Q K^T into tensor memory
 //    (TMEM), an online softmax by four warps (thread t owns row t), then
 //    O += P V accumulated in TMEM. Work is split stream-K over all units'
-//    64-key tiles (one CTA per SM), as in the decode split pass.
-//    Operands are fp16: eight producer warps load bf16 K/V rows, convert them
-//    to fp16 (exact for |x| < 65504) and store them in the 128-byte-swizzled
-//    layout the MMA reads; q and P are rounded to fp16. (fp16 keeps the
+//    32-key tiles (one CTA per SM); four K/V stages let the TMA warp run up to
+//    three tiles ahead.
+//    Operands are fp16: a TMA warp brings the bf16 K/V rows of each 16-key
+//    group as 2D boxes in the 128-byte-swizzled layout the MMA reads, and
+//    eight producer warps convert them to fp16 in place (exact for |x| < 65504);
+//    q and P are rounded to fp16. (fp16 keeps the
 //    error of q and P rounding under the tolerance at every prefix length;
 //    bf16 operands do not at short prefixes.) The accumulator is rescaled
 //    lazily: only when a row's maximum grows by more than 2^8.
@@ -23,6 +25,7 @@
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "mma.cuh"
 #include "tc.cuh"
 
 namespace dattn {
@@ -31,11 +34,31 @@ namespace {
 
 constexpr int VM = 128;              // MMA rows (G*T <= VM)
 constexpr int VNK = kVerifyTileKeys; // keys per tile
+constexpr int NST = 5;               // K/V stages (TMA runs up to four tiles ahead)
+constexpr int kWin = 32;             // tiles whose page rows the TMA warp resolves at once
 constexpr int kSoftWarps = 4;        // softmax warps: TMEM lane quarters 0..3
 constexpr int kProdWarps = 8;        // producer warps
 constexpr int kMmaWarp = kSoftWarps + kProdWarps;
-constexpr int kVThreads = (kMmaWarp + 1) * 32;
+constexpr int kTmaWarp = kMmaWarp + 1;   // issues the prefix tiles' TMA copies
+constexpr int kPvWarp = kTmaWarp + 1;    // issues the P V MMAs (kMmaWarp issues Q K^T)
+constexpr int kVThreads = (kPvWarp + 1) * 32;
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold
+
+// barrier indices
+// (B_FULL, B_EMPTY, B_LOAD: one per stage; B_SFULL, B_SFREE: one per score
+// buffer; B_PFULL, B_PVDONE: one per probability buffer)
+enum {
+  B_FULL = 0,
+  B_EMPTY = B_FULL + NST,
+  B_LOAD = B_EMPTY + NST,
+  B_SFULL = B_LOAD + NST,
+  B_SFREE = B_SFULL + 2,
+  B_PFULL = B_SFREE + 2,
+  B_PVDONE = B_PFULL + 2,
+  B_QREADY = B_PVDONE + 2,
+  B_OFREE = B_QREADY + 1,
+  B_COUNT = B_OFREE + 1
+};
 
 // A partial row is o[D], m, l, padded to a 16-byte multiple: D + 4 floats.
 template <int D>
@@ -44,26 +67,24 @@ constexpr int row_stride() { return D + 4; }
 template <int D>
 struct VGeo {
   static constexpr int NREG = D / 64;                 // 64-dim (128-byte) regions per row
-  static constexpr int Q_OFF = 0;
-  static constexpr int Q_REG = VM * 128;              // bytes of one Q region
   static constexpr int KT_REG = VNK * 128;            // bytes of one K (or V) region
   static constexpr int KT_BYTES = NREG * KT_REG;
-  static constexpr int ST_OFF = Q_OFF + NREG * Q_REG;
+  static constexpr int ST_OFF = 0;
   static constexpr int ST_BYTES = 2 * KT_BYTES;       // K then V
-  static constexpr int P_OFF = ST_OFF + 2 * ST_BYTES;
-  static constexpr int BAR_OFF = P_OFF + VM * 128;
-  static constexpr int NBAR = 12;
+  static constexpr int P_OFF = ST_OFF + NST * ST_BYTES;
+  static constexpr int BAR_OFF = P_OFF + 2 * VM * 128;  // two P buffers
+  static constexpr int NBAR = B_COUNT;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8; // tmem slot, abort flag
   static constexpr int TAB_OFF = MISC_OFF + 16;
   static constexpr int SMEM = TAB_OFF + (2 * kVerifyMaxUnits + 1) * 4 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t S_COL = 0;                // two 64-column score buffers
+  static constexpr uint32_t S_COL = 0;                // two VNK-column score buffers
+  static constexpr uint32_t Q_COL = 64;               // q rows as the MMA's A: D/2 columns of fp16 pairs
   static constexpr uint32_t O_COL = 256;              // D columns of output
   static_assert(D == 128 || D == 256, "head_dim");
 };
 
-// barrier indices
-enum { B_FULL = 0, B_EMPTY = 2, B_SFULL = 4, B_SFREE = 6, B_PFULL = 8, B_PVDONE = 9, B_QREADY = 10, B_OFREE = 11 };
+
 
 struct Waiter {
   uint32_t bars;
@@ -100,7 +121,7 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, uint32_t& ovf) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const VerifySplitArgs a) {
+__global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid_constant__ VerifySplitArgs a) {
   using V = VGeo<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -129,14 +150,19 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const Verify
   if (threadIdx.x == 0) {
     Pt[0] = 0;
     *abort_flag = 0;
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NST; ++b) {
+      mbar_init(sbase + V::BAR_OFF + 8 * (B_LOAD + b), 1);
       mbar_init(sbase + V::BAR_OFF + 8 * (B_FULL + b), kProdWarps);
       mbar_init(sbase + V::BAR_OFF + 8 * (B_EMPTY + b), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(sbase + V::BAR_OFF + 8 * (B_SFULL + b), 1);
       mbar_init(sbase + V::BAR_OFF + 8 * (B_SFREE + b), kSoftWarps);
     }
-    mbar_init(sbase + V::BAR_OFF + 8 * B_PFULL, kSoftWarps);
-    mbar_init(sbase + V::BAR_OFF + 8 * B_PVDONE, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(sbase + V::BAR_OFF + 8 * (B_PFULL + b), kSoftWarps);
+      mbar_init(sbase + V::BAR_OFF + 8 * (B_PVDONE + b), 1);
+    }
     mbar_init(sbase + V::BAR_OFF + 8 * B_QREADY, kSoftWarps);
     mbar_init(sbase + V::BAR_OFF + 8 * B_OFREE, kSoftWarps);
     fence_mbar_init();
@@ -158,109 +184,170 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const Verify
   const int ntiles = g1 - g0;
   const Waiter W{sbase + V::BAR_OFF, abort_flag, a.err};
 
-  if (ntiles > 0 && warp >= kSoftWarps && warp < kMmaWarp) {
-    // ================= producers: bf16 K/V rows -> fp16, swizzled =================
-    const int pt = threadIdx.x - kSoftWarps * 32;         // 0 .. 255
-    constexpr int CPR = D / 8;                            // 16-byte chunks per row
-    constexpr int JOBS = 2 * VNK * CPR / (kProdWarps * 32);  // chunks per thread per tile
-    uint4 buf[JOBS];
-    uint32_t ovf = 0;
-    int u = unit_of(Pt, U, g0);
-    auto load = [&](int k) {
-      const int g = g0 + k;
-      while (Pt[u + 1] <= g) ++u;
+  if (ntiles > 0 && warp == kTmaWarp) {
+    // ================= TMA: bf16 K/V page rows into the stage, swizzled =================
+    // Each 16-key group of a tile is one box of 16 rows x 64 dims per 64-dim
+    // region of K and of V (a page holds whole groups: its size is a multiple
+    // of 16); the 128-byte swizzle is the layout the MMAs read. Groups past the
+    // prefix are not loaded; the producers zero their rows.
+    // Lane x % 32 reads the page ids of tile x one 32-tile window ahead, so
+    // that no page-table load sits between two tiles' copies; lane 0 issues.
+    constexpr int NG = VNK / 16;
+    const uint64_t policy = l2_evict_first_policy();
+    auto fetch = [&](int x, int (&pg)[NG], int (&off)[NG]) -> int {  // returns the group count
+#pragma unroll
+      for (int gr = 0; gr < NG; ++gr) pg[gr] = off[gr] = 0;
+      if (x >= ntiles) return 0;
+      const int g = g0 + x;
+      const int u = unit_of(Pt, U, g);
       const int s = u / Hkv, j = u - s * Hkv;
       const int k0 = (g - Pt[u]) * VNK;
-      const int nvalid = min(VNK, Nn[u] - k0);
+      const int ng = (min(VNK, Nn[u] - k0) + 15) / 16;
       const int32_t* bt = c.block_table + static_cast<int64_t>(s) * c.bt_stride;
 #pragma unroll
-      for (int x = 0; x < JOBS; ++x) {
-        const int e = pt + x * kProdWarps * 32;
-        const int which = e / (VNK * CPR);
-        const int rem = e - which * (VNK * CPR);
-        const int r = rem / CPR, ch = rem - r * CPR;
-        buf[x] = make_uint4(0u, 0u, 0u, 0u);
-        if (r < nvalid) {
-          const int t = k0 + r;
+      for (int gr = 0; gr < NG; ++gr) {
+        if (gr < ng) {
+          const int t = k0 + gr * 16;
           const int pi = t / c.P;
-          int pg = bt[pi];
-          if (pg < 0 || pg >= c.n_rows) {
-            raise_error(a.err, ERR_INDEX);
-            pg = 0;
-          }
-          const int64_t row = (static_cast<int64_t>(pg) * Hkv + j) * c.P + (t - pi * c.P);
-          buf[x] = ld_nc_v4((which ? c.v : c.k) + row * D + ch * 8);
+          pg[gr] = bt[pi];  // used a window later: the load is not waited for here
+          off[gr] = j * c.P + (t - pi * c.P);
         }
       }
+      return ng;
     };
-    load(0);
+    int pg_c[NG], off_c[NG], pg_n[NG], off_n[NG];
+    int ng_c = fetch(lane, pg_c, off_c);
+    int ng_n = fetch(kWin + lane, pg_n, off_n);
     for (int k = 0; k < ntiles; ++k) {
-      const int st = k & 1;
-      if (k >= 2 && !__all_sync(0xffffffffu, W.wait(B_EMPTY + st, ((k >> 1) - 1) & 1))) break;
+      if (k > 0 && (k & (kWin - 1)) == 0) {
+#pragma unroll
+        for (int gr = 0; gr < NG; ++gr) {
+          pg_c[gr] = pg_n[gr];
+          off_c[gr] = off_n[gr];
+        }
+        ng_c = ng_n;
+        ng_n = fetch(k + kWin + lane, pg_n, off_n);
+      }
+      const int st = k % NST;
+      if (k >= NST && !__all_sync(0xffffffffu, W.wait(B_EMPTY + st, (k / NST - 1) & 1))) break;
+      const int src = k & (kWin - 1);
+      const int ngroups = __shfl_sync(0xffffffffu, ng_c, src);
+      int rows[NG];
+#pragma unroll
+      for (int gr = 0; gr < NG; ++gr) {
+        int pg = __shfl_sync(0xffffffffu, pg_c[gr], src);
+        const int off = __shfl_sync(0xffffffffu, off_c[gr], src);
+        if (gr < ngroups && (pg < 0 || pg >= c.n_rows)) {
+          if (lane == 0) raise_error(a.err, ERR_INDEX);
+          pg = 0;
+        }
+        rows[gr] = pg * Hkv * c.P + off;
+      }
+      if (lane == 0) {
+        const uint32_t bar = sbase + V::BAR_OFF + 8 * (B_LOAD + st);
+        const uint32_t stage = sbase + V::ST_OFF + st * V::ST_BYTES;
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(ngroups) * 2u * V::NREG * 2048u);
+#pragma unroll
+        for (int gr = 0; gr < NG; ++gr) {
+          if (gr < ngroups) {
+#pragma unroll
+            for (int rg = 0; rg < V::NREG; ++rg) {
+              tma_load_2d(stage + rg * V::KT_REG + gr * 2048, &a.tmap_k, 64 * rg, rows[gr], bar, policy);
+              tma_load_2d(stage + V::KT_BYTES + rg * V::KT_REG + gr * 2048, &a.tmap_v, 64 * rg, rows[gr], bar,
+                          policy);
+            }
+          }
+        }
+      }
+      __syncwarp();
+    }
+  } else if (ntiles > 0 && warp >= kSoftWarps && warp < kMmaWarp) {
+    // ================= producers: the staged bf16 rows -> fp16, in place =================
+    const int pt = threadIdx.x - kSoftWarps * 32;         // 0 .. 255
+    constexpr int CPR = D / 8;                            // 16-byte chunks per row
+    constexpr int NCH = 2 * VNK * CPR;                    // chunks of a stage (K and V)
+    uint32_t ovf = 0;
+    int u = unit_of(Pt, U, g0);
+    for (int k = 0; k < ntiles; ++k) {
+      const int st = k % NST;
+      if (!__all_sync(0xffffffffu, W.wait(B_LOAD + st, (k / NST) & 1))) break;
+      const int g = g0 + k;
+      while (Pt[u + 1] <= g) ++u;
+      const int nvalid = min(VNK, Nn[u] - (g - Pt[u]) * VNK);
       uint8_t* stage = smem + V::ST_OFF + st * V::ST_BYTES;
 #pragma unroll
-      for (int x = 0; x < JOBS; ++x) {
-        const int e = pt + x * kProdWarps * 32;
+      for (int e = pt; e < NCH; e += kProdWarps * 32) {
         const int which = e / (VNK * CPR);
         const int rem = e - which * (VNK * CPR);
         const int r = rem / CPR, ch = rem - r * CPR;
-        uint4 h;
-        h.x = bf16x2_to_f16x2(buf[x].x, ovf);
-        h.y = bf16x2_to_f16x2(buf[x].y, ovf);
-        h.z = bf16x2_to_f16x2(buf[x].z, ovf);
-        h.w = bf16x2_to_f16x2(buf[x].w, ovf);
-        const int off = which * V::KT_BYTES + (ch >> 3) * V::KT_REG + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(stage + off) = h;
+        uint4* p = reinterpret_cast<uint4*>(stage + which * V::KT_BYTES + (ch >> 3) * V::KT_REG + r * 128 +
+                                            (((ch & 7) ^ (r & 7)) << 4));
+        uint4 h = make_uint4(0u, 0u, 0u, 0u);
+        if (r < nvalid) {
+          const uint4 w = *p;
+          h.x = bf16x2_to_f16x2(w.x, ovf);
+          h.y = bf16x2_to_f16x2(w.y, ovf);
+          h.z = bf16x2_to_f16x2(w.z, ovf);
+          h.w = bf16x2_to_f16x2(w.w, ovf);
+        }
+        *p = h;
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(sbase + V::BAR_OFF + 8 * (B_FULL + st));
-      if (k + 1 < ntiles) load(k + 1);
     }
     if (__any_sync(0xffffffffu, ovf != 0) && lane == 0) raise_error(a.err, ERR_RANGE);
   } else if (ntiles > 0 && warp == kMmaWarp) {
-    // ================= MMA issue (one thread) =================
+    // ================= Q K^T issue (one thread) =================
     if (lane == 0) {
       constexpr uint32_t idesc_qk = tc::f16_idesc(VM, VNK, 0, false);
-      constexpr uint32_t idesc_pv = tc::f16_idesc(VM, D, 0, true);
-      bool ok = true;
-      auto issue_qk = [&](int k) -> bool {
-        const int st = k & 1, sb = k & 1;
-        if (!W.wait(B_FULL + st, (k >> 1) & 1)) return false;
-        if (k >= 2 && !W.wait(B_SFREE + sb, ((k >> 1) - 1) & 1)) return false;
+      int u = unit_of(Pt, U, g0), prev_u = -1, seg = 0;
+      for (int k = 0; k < ntiles; ++k) {
+        const int g = g0 + k;
+        while (Pt[u + 1] <= g) ++u;
+        if (u != prev_u) {  // this unit's q rows are in place
+          if (!W.wait(B_QREADY, seg & 1)) break;
+          ++seg;
+          prev_u = u;
+        }
+        const int st = k % NST, sb = k & 1;
+        if (!W.wait(B_FULL + st, (k / NST) & 1)) break;
+        if (k >= 2 && !W.wait(B_SFREE + sb, ((k >> 1) - 1) & 1)) break;
         tc::fence_after();
         const uint32_t kbase = sbase + V::ST_OFF + st * V::ST_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t da = tc::sw128_desc(sbase + V::Q_OFF + (kk >> 2) * V::Q_REG + (kk & 3) * 32, 16, 1024);
           const uint64_t db = tc::sw128_desc(kbase + (kk >> 2) * V::KT_REG + (kk & 3) * 32, 16, 1024);
-          tc::mma(tmem + V::S_COL + sb * VNK, da, db, idesc_qk, kk > 0);
+          tc::mma_ts(tmem + V::S_COL + sb * VNK, tmem + V::Q_COL + kk * 8, db, idesc_qk, kk > 0);
         }
         tc::commit(sbase + V::BAR_OFF + 8 * (B_SFULL + sb));
-        return true;
-      };
+      }
+    }
+    __syncwarp();
+  } else if (ntiles > 0 && warp == kPvWarp) {
+    // ================= P V issue (one thread) =================
+    // PV(k) follows QK(k): its P was made from the scores QK(k) wrote. The
+    // stage's K and V are free once PV(k) completes.
+    if (lane == 0) {
+      constexpr uint32_t idesc_pv = tc::f16_idesc(VM, D, 0, true);
       int u = unit_of(Pt, U, g0), prev_u = -1, seg = 0;
-      for (int k = 0; k < ntiles && ok; ++k) {
+      for (int k = 0; k < ntiles; ++k) {
         const int g = g0 + k;
         while (Pt[u + 1] <= g) ++u;
         const bool seg_start = u != prev_u;
         const bool seg_end = k == ntiles - 1 || g + 1 >= Pt[u + 1];
-        if (seg_start) {
-          if (!W.wait(B_QREADY, seg & 1) || !issue_qk(k)) break;
-        }
-        if (!seg_end && !issue_qk(k + 1)) break;
-        if (!W.wait(B_PFULL, k & 1)) break;
+        if (!W.wait(B_PFULL + (k & 1), (k >> 1) & 1)) break;
         if (seg_start && seg > 0 && !W.wait(B_OFREE, (seg - 1) & 1)) break;
         tc::fence_after();
-        const int st = k & 1;
+        const int st = k % NST;
         const uint32_t vbase = sbase + V::ST_OFF + st * V::ST_BYTES + V::KT_BYTES;
 #pragma unroll
         for (int kk = 0; kk < VNK / 16; ++kk) {
-          const uint64_t da = tc::sw128_desc(sbase + V::P_OFF + kk * 32, 16, 1024);
+          const uint64_t da = tc::sw128_desc(sbase + V::P_OFF + (k & 1) * VM * 128 + kk * 32, 16, 1024);
           const uint64_t db = tc::sw128_desc(vbase + kk * 2048, V::KT_REG, 1024);
           tc::mma(tmem + V::O_COL, da, db, idesc_pv, !seg_start || kk > 0);
         }
-        tc::commit(sbase + V::BAR_OFF + 8 * B_PVDONE);
+        tc::commit(sbase + V::BAR_OFF + 8 * (B_PVDONE + (k & 1)));
         tc::commit(sbase + V::BAR_OFF + 8 * (B_EMPTY + st));
         if (seg_end) ++seg;
         prev_u = u;
@@ -272,7 +359,6 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const Verify
     pdl_wait();  // q rotated by the prologue
     const int t = threadIdx.x;
     const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
-    uint8_t* Q = smem + V::Q_OFF;
     uint8_t* Pb = smem + V::P_OFF;
     int u = unit_of(Pt, U, g0), prev_u = -1, seg = 0;
     float m_ref = -INFINITY, l = 0.f;
@@ -282,25 +368,28 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const Verify
       const bool seg_start = u != prev_u;
       const bool seg_end = k == ntiles - 1 || g + 1 >= Pt[u + 1];
       if (seg_start) {
-        // this unit's q rows as fp16 in the swizzled K-major layout
+        // this unit's q rows as fp16 pairs into tensor memory (the QK MMAs'
+        // A operand; the previous unit's QKs are done: its last scores were read)
         const int s = u / Hkv, j = u - s * Hkv;
         const float* src = nullptr;
         if (t < R) {
           const int gq = t / T, i = t - gq * T;
           src = a.qhat + ((static_cast<int64_t>(s) * T + i) * Hq + j * G + gq) * D;
         }
-#pragma unroll 4
-        for (int ch = 0; ch < D / 8; ++ch) {
-          uint4 h = make_uint4(0u, 0u, 0u, 0u);
-          if (src) {
-            const float4 x0 = *reinterpret_cast<const float4*>(src + ch * 8);
-            const float4 x1 = *reinterpret_cast<const float4*>(src + ch * 8 + 4);
-            h = make_uint4(cvt_pair_f16(x0.x, x0.y), cvt_pair_f16(x0.z, x0.w), cvt_pair_f16(x1.x, x1.y),
-                           cvt_pair_f16(x1.z, x1.w));
+#pragma unroll 1
+        for (int c32 = 0; c32 < D / 64; ++c32) {
+          uint32_t qv[32];
+#pragma unroll
+          for (int x = 0; x < 32; x += 2) {
+            float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (src) y = *reinterpret_cast<const float4*>(src + 64 * c32 + 2 * x);
+            qv[x] = cvt_pair_f16(y.x, y.y);
+            qv[x + 1] = cvt_pair_f16(y.z, y.w);
           }
-          *reinterpret_cast<uint4*>(Q + (ch >> 3) * V::Q_REG + t * 128 + (((ch & 7) ^ (t & 7)) << 4)) = h;
+          tc::st32(tmem + lane_off + V::Q_COL + 32 * c32, qv);
         }
-        fence_proxy_async_smem();
+        tc::wait_st();
+        tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(sbase + V::BAR_OFF + 8 * B_QREADY);
         m_ref = -INFINITY;
@@ -309,8 +398,8 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const Verify
       const int sb = k & 1;
       if (!__all_sync(0xffffffffu, W.wait(B_SFULL + sb, (k >> 1) & 1))) break;
       tc::fence_after();
-      uint32_t sr[64];
-      tc::ld64(tmem + lane_off + V::S_COL + sb * VNK, sr);
+      uint32_t sr[VNK];
+      tc::ld32(tmem + lane_off + V::S_COL + sb * VNK, sr);
       tc::wait_ld();
       tc::fence_before();
       __syncwarp();
@@ -318,7 +407,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const Verify
       const int nvalid = min(VNK, Nn[u] - (g - Pt[u]) * VNK);
       float tmax = -INFINITY;
 #pragma unroll
-      for (int x = 0; x < 64; ++x) {
+      for (int x = 0; x < VNK; ++x) {
         const float sx = x < nvalid ? __uint_as_float(sr[x]) : -INFINITY;
         sr[x] = __float_as_uint(sx);
         tmax = fmaxf(tmax, sx);
@@ -330,7 +419,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const Verify
         const bool need = tmax > m_ref + kRescaleLog2;
         if (__any_sync(0xffffffffu, need)) {
           // rescale this warp's rows of O once the last PV has landed
-          if (!__all_sync(0xffffffffu, W.wait(B_PVDONE, (k - 1) & 1))) break;
+          if (!__all_sync(0xffffffffu, W.wait(B_PVDONE + ((k - 1) & 1), ((k - 1) >> 1) & 1))) break;
           pv_waited = true;
           tc::fence_after();
           const float f = need ? exp2_fast(m_ref - tmax) : 1.f;
@@ -351,10 +440,10 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const Verify
         }
       }
       // probabilities in fp16; the row sum uses the same rounded values
-      uint32_t ph[32];
+      uint32_t ph[VNK / 2];
       float lsum = 0.f;
 #pragma unroll
-      for (int x = 0; x < 32; ++x) {
+      for (int x = 0; x < VNK / 2; ++x) {
         const float p0 = exp2_fast(__uint_as_float(sr[2 * x]) - m_ref);
         const float p1 = exp2_fast(__uint_as_float(sr[2 * x + 1]) - m_ref);
         const __half2 h = __floats2half2_rn(p0, p1);
@@ -362,18 +451,20 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const Verify
         ph[x] = *reinterpret_cast<const uint32_t*>(&h);
       }
       l += lsum;
-      // the P buffer is free once the previous PV has completed
-      if (k > 0 && !pv_waited && !__all_sync(0xffffffffu, W.wait(B_PVDONE, (k - 1) & 1))) break;
+      // this tile's P buffer is free once the PV two tiles back has completed
+      // (PVs complete in order: a wait for the previous one covers it)
+      if (k >= 2 && !pv_waited && !__all_sync(0xffffffffu, W.wait(B_PVDONE + (k & 1), ((k >> 1) - 1) & 1))) break;
+      uint8_t* Pk = Pb + (k & 1) * VM * 128;
 #pragma unroll
-      for (int x = 0; x < 8; ++x)
-        *reinterpret_cast<uint4*>(Pb + t * 128 + ((x ^ (t & 7)) << 4)) =
+      for (int x = 0; x < VNK / 8; ++x)
+        *reinterpret_cast<uint4*>(Pk + t * 128 + ((x ^ (t & 7)) << 4)) =
             make_uint4(ph[4 * x], ph[4 * x + 1], ph[4 * x + 2], ph[4 * x + 3]);
       fence_proxy_async_smem();
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(sbase + V::BAR_OFF + 8 * B_PFULL);
+      if (lane == 0) mbar_arrive(sbase + V::BAR_OFF + 8 * (B_PFULL + (k & 1)));
       if (seg_end) {
-        if (!__all_sync(0xffffffffu, W.wait(B_PVDONE, k & 1))) break;
+        if (!__all_sync(0xffffffffu, W.wait(B_PVDONE + (k & 1), (k >> 1) & 1))) break;
         tc::fence_after();
         const int slot = seg == 0 ? cta : NC + u;
         float* dst = a.part + (static_cast<int64_t>(slot) * R + t) * row_stride<D>();
