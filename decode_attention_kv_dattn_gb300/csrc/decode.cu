@@ -71,6 +71,13 @@ constexpr int kMaxUnits = 512;           // (stream, KV head) units per call
 constexpr int kGroup = 16;               // keys per MMA group
 constexpr int kBoxBytes = kGroup * 128;  // one TMA box: 16 rows x 64 bf16
 constexpr int kWin = 32;                 // tiles per prefetch window (one per lane)
+// Fixed cost of one segment of a unit in the stream-K split, in stage tiles of
+// one CTA: a segment boundary takes about as long as streaming this many
+// tiles with all warps.
+#ifndef DATTN_SEGMENT_COST
+#define DATTN_SEGMENT_COST 12
+#endif
+constexpr int kSegmentCost = DATTN_SEGMENT_COST;
 
 template <int D, int NT>
 struct Geo {
@@ -164,18 +171,48 @@ __device__ __forceinline__ uint32_t row_bits(int lo, int hi) {
   return ((1u << (hi - lo)) - 1u) << lo;
 }
 
-// Number of split CTAs whose ranges hold tiles of the unit spanning global
-// tiles [p0, p1), the first of them (CTA of tile x: floor(((x+1)NC-1)/T)) and
-// the partial slot of its segment.
-__device__ __forceinline__ int unit_segments(int p0, int p1, int T, int NC, int u, int& c_lo,
+// The stream-K split runs over weighted positions: unit u starts at
+// P[u] + C u, its first C positions stand for the fixed cost of one segment of
+// it (staging its inputs, RoPE, the new token, the merge and the output), and
+// its tiles follow one position each. CTA c takes the positions
+// [c W / NC, (c + 1) W / NC) of the W = T + C U in all, so a CTA whose range
+// crosses many short units gets fewer tiles.
+struct Split {
+  const int* P;  // [U + 1] tile prefix over units
+  int U, C, NC;
+  int64_t W;
+  __device__ __forceinline__ int64_t bound(int c) const { return static_cast<int64_t>(c) * W / NC; }
+  // first tile at or after weighted position t (T past the end)
+  __device__ int tile_at(int64_t t) const {
+    if (t >= W) return P[U];
+    int lo = 0, hi = U - 1;  // the last unit starting at or before t
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (P[mid] + static_cast<int64_t>(C) * mid <= t) lo = mid; else hi = mid - 1;
+    }
+    const int64_t off = t - (P[lo] + static_cast<int64_t>(C) * lo) - C;
+    return P[lo] + (off > 0 ? static_cast<int>(off) : 0);
+  }
+  // CTA whose range holds tile x of unit u
+  __device__ __forceinline__ int cta_of(int x, int u) const {
+    const int64_t w = x + static_cast<int64_t>(C) * (u + 1);
+    return static_cast<int>(((w + 1) * NC - 1) / W);
+  }
+  __device__ __forceinline__ bool has_tiles_inside(int c) const { return bound(c) < bound(c + 1); }
+};
+
+// Number of CTAs whose ranges hold tiles of unit u (global tiles [p0, p1)),
+// the first of them, the last, and the partial slot of the first one's
+// segment (that CTA's own slot when the unit starts its range).
+__device__ __forceinline__ int unit_segments(const Split& sp, int p0, int p1, int u, int& c_lo, int& c_hi,
                                              int& first_slot) {
   if (p1 <= p0) return 0;
-  c_lo = static_cast<int>((static_cast<int64_t>(p0 + 1) * NC - 1) / T);
-  const int c_hi = static_cast<int>((static_cast<int64_t>(p1) * NC - 1) / T);
-  first_slot = static_cast<int>(static_cast<int64_t>(c_lo) * T / NC) == p0 ? c_lo : NC + u;
+  c_lo = sp.cta_of(p0, u);
+  c_hi = sp.cta_of(p1 - 1, u);
+  first_slot = sp.tile_at(sp.bound(c_lo)) == p0 ? c_lo : sp.NC + u;
   int n = 1;
-  for (int cc = c_lo + 1; cc <= c_hi; ++cc)
-    if (static_cast<int64_t>(cc) * T / NC < static_cast<int64_t>(cc + 1) * T / NC) ++n;
+  // a CTA strictly inside the unit's span holds its tiles iff its range is not empty
+  for (int cc = c_lo + 1; cc <= c_hi; ++cc) n += sp.has_tiles_inside(cc);
   return n;
 }
 
@@ -379,8 +416,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   // units than CTAs and cutting every unit into s = NC / U equal pieces (one
   // CTA each) leaves the largest piece within 5/4 of a fair share, CTA
   // u * s + k takes piece k of unit u - units mostly end inside one CTA and
-  // few partials cross CTAs. Otherwise stream-K: CTA c takes the tiles
-  // [c T / NC, (c + 1) T / NC) of all units laid end to end.
+  // few partials cross CTAs. Otherwise stream-K over the units laid end to
+  // end, each weighted with the fixed cost of a segment (Split).
   int max_tiles = 0;
   for (int u = threadIdx.x; u < U; u += kThreads) max_tiles = max(max_tiles, P[u + 1] - P[u]);
 #pragma unroll
@@ -389,6 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   __syncthreads();
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) max_tiles = max(max_tiles, SLOT[w]);
+  const Split sp{P, U, a.unit_cost, NC, T + static_cast<int64_t>(a.unit_cost) * U};
   int pieces = 0;
   if (U <= NC && T > 0) {
     const int s = NC / U;
@@ -401,8 +439,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     g0 = u < U ? P[u] + k * t / pieces : 0;
     g1 = u < U ? P[u] + (k + 1) * t / pieces : 0;
   } else {
-    g0 = static_cast<int>(static_cast<int64_t>(cta) * T / NC);
-    g1 = static_cast<int>(static_cast<int64_t>(cta + 1) * T / NC);
+    g0 = sp.tile_at(sp.bound(cta));
+    g1 = sp.tile_at(sp.bound(cta + 1));
   }
 
   // ---- this warp's tiles: g = g0 + warp + kWarps * it
@@ -803,22 +841,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     __syncthreads();
     // ---- segment end: how many CTAs hold pieces of this unit, and where
     // their partials are (candidate k: slot, and whether it holds tiles)
-    int c_lo = 0, first_slot = 0, nseg, S;
+    int c_lo = 0, c_hi = 0, first_slot = 0, nseg, S;
     const int p0 = P[u], p1 = P[u + 1];
     if (pieces) {
       nseg = min(pieces, p1 - p0);
       S = pieces;
     } else {
-      nseg = unit_segments(p0, p1, T, NC, u, c_lo, first_slot);
-      S = static_cast<int>((static_cast<int64_t>(p1) * NC - 1) / T) - c_lo + 1;
+      nseg = unit_segments(sp, p0, p1, u, c_lo, c_hi, first_slot);
+      S = c_hi - c_lo + 1;
     }
     auto cand_slot = [&](int k) { return pieces ? u * pieces + k : (k == 0 ? first_slot : c_lo + k); };
     auto cand_ok = [&](int k) -> bool {
       if (k >= S) return false;
       if (pieces) return (k + 1) * (p1 - p0) / pieces > k * (p1 - p0) / pieces;
-      const int64_t cc = c_lo + k;
       // candidate k > 0 is the first segment of CTA c_lo + k, unless that CTA got no tiles
-      return k == 0 || cc * T / NC < (cc + 1) * T / NC;
+      return k == 0 || sp.has_tiles_inside(c_lo + k);
     };
     if (nseg == 1) {
       // the whole unit lies in this CTA: the warps' states go straight into the output
@@ -993,7 +1030,9 @@ cudaError_t encode_cache_maps(const CacheView& c, int Hkv, int D, CUtensorMap* k
   return cudaSuccess;
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, int D, int ctas, cudaStream_t s) {
+cudaError_t launch_decode(const DecodeArgs& args, int D, int ctas, cudaStream_t s) {
+  DecodeArgs a = args;
+  a.unit_cost = kSegmentCost;
   const int GP = decode_group_pad(a.G);
   if (a.B * a.Hkv > kMaxUnits) return cudaErrorNotSupported;
   if (a.r > D || a.r % 2 != 0) return cudaErrorNotSupported;

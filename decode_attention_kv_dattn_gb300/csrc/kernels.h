@@ -90,6 +90,8 @@ struct DecodeArgs {
   int early;                   // nonzero: the preceding launch on the stream writes
                                // no part of this cache, so the first cache loads may
                                // start before it completes
+  int unit_cost;               // fixed cost of one segment of a unit, in stage tiles
+                               // (set by launch_decode)
 };
 
 struct AppendArgs {
