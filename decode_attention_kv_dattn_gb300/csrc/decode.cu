@@ -65,8 +65,9 @@ namespace dattn {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
+constexpr int kWarps = 4;                // streaming warps
+constexpr int kHelper = kWarps;          // the helper warp's index
+constexpr int kThreads = (kWarps + 1) * 32;
 constexpr int kMaxUnits = 512;           // (stream, KV head) units per call
 constexpr int kGroup = 16;               // keys per MMA group
 constexpr int kBoxBytes = kGroup * 128;  // one TMA box: 16 rows x 64 bf16
@@ -78,6 +79,12 @@ constexpr int kWin = 32;                 // tiles per prefetch window (one per l
 #define DATTN_SEGMENT_COST 12
 #endif
 constexpr int kSegmentCost = DATTN_SEGMENT_COST;
+// Largest excess (percent) of the biggest piece over a fair share of the tiles
+// for which the split cuts every unit into equal pieces instead of stream-K.
+#ifndef DATTN_PIECES_SLACK
+#define DATTN_PIECES_SLACK 25
+#endif
+constexpr int kPiecesSlack = DATTN_PIECES_SLACK;
 
 template <int D, int NT>
 struct Geo {
@@ -89,30 +96,41 @@ struct Geo {
   static constexpr int KHALF = KG * GBYTES;          // K part of a stage; V follows
   static constexpr int STAGE = 2 * KHALF;
   static constexpr int NS = 3;
+  // mbarriers: [kWarps][NS] stages, 2 input slots, then the four hand-offs
+  // between the streaming warps and the helper
+  static constexpr int NBAR = kWarps * NS + 2 + 4;
   // offsets from the 1024-byte aligned base of dynamic shared memory
   static constexpr int BAR_OFF = kWarps * NS * STAGE;
-  static constexpr int ML_OFF = BAR_OFF + kWarps * NS * 8;        // float [kWarps][2*GP]
+  static constexpr int INBAR_OFF = BAR_OFF + kWarps * NS * 8;
+  static constexpr int PREP_FULL_OFF = INBAR_OFF + 16;   // q of the next segment is in qs
+  static constexpr int PREP_EMPTY_OFF = INBAR_OFF + 24;  // every streaming warp has read qs
+  static constexpr int MERGE_FULL_OFF = INBAR_OFF + 32;  // every warp's state is in its buffer
+  static constexpr int MERGE_EMPTY_OFF = INBAR_OFF + 40; // the helper has read the states
+  static constexpr int ML_OFF = BAR_OFF + NBAR * 8;               // float [kWarps][2*GP]
   static constexpr int SLOT_OFF = ML_OFF + kWarps * 2 * GP * 4;   // int [kWarps]
-  static constexpr int SN_OFF = SLOT_OFF + kWarps * 4;            // float [GP]: new-token scores
-  static constexpr int FLAG_OFF = SN_OFF + GP * 4;                // int: "this CTA combines"
+  static constexpr int FLAG_OFF = SLOT_OFF + kWarps * 4;          // int: "this CTA combines"
   static constexpr int CS_OFF = (FLAG_OFF + 4 + 15) / 16 * 16;    // float2 [D/2]: cos, sin
   static constexpr int QS_OFF = CS_OFF + D / 2 * 8;               // float [GP][D]: rotated q
-  static constexpr int KH_OFF = QS_OFF + GP * D * 4;              // bf16 [D]: new K entry
-  static constexpr int WROW_OFF = KH_OFF + D * 2;                 // int [kWarps][2][kWin*KG]
+  static constexpr int WROW_OFF = QS_OFF + GP * D * 4;            // int [kWarps][2][kWin*KG]
   static constexpr int WMASK_OFF = WROW_OFF + kWarps * 2 * kWin * KG * 4;
   static constexpr int STEP_OFF = WMASK_OFF + kWarps * 2 * kWin * KG * 4;  // uint64 [D/2]: RoPE steps
-  static constexpr int SIG_OFF = STEP_OFF + D / 2 * 8;            // float [GP]: sigmoid(gate)
-  static constexpr int INBAR_OFF = SIG_OFF + GP * 4;              // 2 mbarriers of the input slots
-  static constexpr int IN_Q = 0;                                  // input slot: q [GP][D] bf16,
-  static constexpr int IN_K = GP * D * 2;                         //   k_new [D], v_new [D]
+  // input slot: q [GP][D] bf16, k_new [D], v_new [D] (one bulk copy each),
+  // then the new token worked out from them: K entry [D] bf16, scores [GP],
+  // sigmoid(gate) [GP]
+  static constexpr int IN_Q = 0;
+  static constexpr int IN_K = GP * D * 2;
   static constexpr int IN_V = IN_K + D * 2;
-  static constexpr int IN_BYTES = IN_V + D * 2;
-  static constexpr int IN_OFF = (INBAR_OFF + 16 + 15) / 16 * 16;  // 2 input slots
+  static constexpr int IN_KH = IN_V + D * 2;
+  static constexpr int IN_SN = IN_KH + D * 2;
+  static constexpr int IN_SIG = IN_SN + GP * 4;
+  static constexpr int IN_BYTES = (IN_SIG + GP * 4 + 15) / 16 * 16;
+  static constexpr int IN_OFF = (STEP_OFF + D / 2 * 8 + 15) / 16 * 16;  // 2 input slots
   static constexpr int TAB_OFF = IN_OFF + 2 * IN_BYTES;
   static constexpr int SMEM_MAX = 1024 + TAB_OFF + (4 * kMaxUnits + 1) * 4;  // P, N, ring head/row
   static_assert(D == 128 || D == 256, "head_dim");
   static_assert(GP * D * 4 <= STAGE, "a stage buffer holds one warp's partial output");
   static_assert(NS < kWin, "issue runs at most one window ahead");
+  static_assert(SMEM_MAX <= 232448, "shared memory per CTA");
 };
 
 // Cached keys of call row b (the same for all its KV heads). Bad metadata is
@@ -216,15 +234,22 @@ __device__ __forceinline__ int unit_segments(const Split& sp, int p0, int p1, in
   return n;
 }
 
-// Rotate the G query heads of a unit (src: its q rows [G][D], staged in
-// shared memory) at position pos into qs[GP][D] (fp32, pre-scaled; heads >= G
-// are zero) and keep each pair's cos/sin in cs. One pair per thread at a
-// time; all threads of the CTA take part.
-template <int D, int GP>
-__device__ __forceinline__ void rotate_q(const DecodeArgs& a, const uint16_t* src, int pos,
-                                         const uint64_t* step, float* qs, float2* cs) {
+// Work on one unit's inputs and outputs is done by a team: the helper warp
+// (NTH = 32, t = lane) for segment ends in the middle of a CTA's range, or the
+// whole CTA (NTH = kThreads, t = threadIdx.x) for its last one.
+template <int NTH>
+__device__ __forceinline__ void team_sync() {
+  if constexpr (NTH == 32) __syncwarp(); else __syncthreads();
+}
+
+// Rotate the G query heads of a unit (src: its staged q rows [G][D]) at
+// position pos into qs[GP][D] (fp32, pre-scaled; heads >= G are zero) and keep
+// each pair's cos/sin in cs.
+template <int D, int GP, int NTH>
+__device__ __forceinline__ void prep_q(const DecodeArgs& a, const uint16_t* src, int pos, const uint64_t* step,
+                                       float* qs, float2* cs, int t) {
   const int G = a.G, half = a.r / 2;
-  for (int p = threadIdx.x; p < D / 2; p += kThreads) {
+  for (int p = t; p < D / 2; p += NTH) {
     const int d0 = p < half ? p : a.r + 2 * (p - half);
     const int d1 = p < half ? p + half : d0 + 1;
     float c = 1.f, s = 0.f;
@@ -249,42 +274,44 @@ __device__ __forceinline__ void rotate_q(const DecodeArgs& a, const uint16_t* sr
   }
 }
 
-// The new token of unit u = (b, j): its K entry into kh (the bf16 nearest to the
-// exact rotation with the cos/sin in cs - the value that is scored and stored), its
-// scores into sn (base 2, one per head, with the rotated q in qs) and the
-// heads' sigmoid(gate) into sig (gate_g: this thread's head's logit, threads <
-// G). `in` holds the unit's staged k_new and v_new rows. All threads of the
-// CTA take part; ends with a CTA barrier.
-template <int D, int GP>
-__device__ void new_token(const DecodeArgs& a, const float* qs, const float2* cs, const uint8_t* in,
-                          float gate_g, uint16_t* kh, float* sn, float* sig) {
+// The new token of a unit from its input slot: its K entry (the bf16 nearest
+// to the exact rotation with the cos/sin in cs - the value that is scored and
+// stored), its score per head (base 2, with the rotated q in qs) and the
+// heads' sigmoid(gate) (gate_raw: the bf16 logit of head t, for t < G), all
+// into the slot. Starts after cs and qs are complete for the team; ends with a
+// team barrier.
+template <int D, int GP, int NTH>
+__device__ __forceinline__ void prep_token(const DecodeArgs& a, const float* qs, const float2* cs, uint8_t* slot,
+                                           uint16_t gate_raw, int t) {
   using Gm = Geo<D, GP / 4>;
   const int G = a.G, half = a.r / 2;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint16_t* ksrc = reinterpret_cast<const uint16_t*>(in + Gm::IN_K);
-  if (threadIdx.x < G) sig[threadIdx.x] = a.gate ? 1.f / (1.f + expf(-gate_g)) : 1.f;
-  for (int p = threadIdx.x; p < D / 2; p += kThreads) {
-    const int d0 = p < half ? p : a.r + 2 * (p - half);
-    const int d1 = p < half ? p + half : d0 + 1;
-    if (p < half) {
-      const uint32_t cb = __float_as_uint(cs[p].x), sb = __float_as_uint(cs[p].y);
-      const uint16_t x = ksrc[d0], y = ksrc[d1];
-      kh[d0] = bf16_dot2_exact(x, cb, y, sb ^ 0x80000000u);  // x c - y s
-      kh[d1] = bf16_dot2_exact(y, cb, x, sb);                // y c + x s
-    } else {
-      kh[d0] = ksrc[d0];
-      kh[d1] = ksrc[d1];
+  const uint16_t* ksrc = reinterpret_cast<const uint16_t*>(slot + Gm::IN_K);
+  uint16_t* kh = reinterpret_cast<uint16_t*>(slot + Gm::IN_KH);
+  float* sn = reinterpret_cast<float*>(slot + Gm::IN_SN);
+  float* sig = reinterpret_cast<float*>(slot + Gm::IN_SIG);
+  if (t < G) sig[t] = a.gate ? 1.f / (1.f + expf(-bf16_to_f32(gate_raw))) : 1.f;
+  for (int e = t; e < D; e += NTH) {
+    uint16_t v = ksrc[e];
+    if (e < half) {
+      const float2 q = cs[e];  // x c - y s with x = k[e], y = k[e + half]
+      v = bf16_dot2_exact(ksrc[e], __float_as_uint(q.x), ksrc[e + half], __float_as_uint(q.y) ^ 0x80000000u);
+    } else if (e < a.r) {
+      const float2 q = cs[e - half];  // y c + x s with y = k[e], x = k[e - half]
+      v = bf16_dot2_exact(ksrc[e], __float_as_uint(q.x), ksrc[e - half], __float_as_uint(q.y));
     }
+    kh[e] = v;
   }
-  __syncthreads();
-  for (int g = warp; g < G; g += kWarps) {
+  team_sync<NTH>();
+  constexpr int W = NTH / 32;
+  const int w = t >> 5, lane = t & 31;
+  for (int g = w; g < G; g += W) {
     float dot = 0.f;
     for (int d = lane; d < D; d += 32) dot = fmaf(qs[g * D + d], bf16_to_f32(kh[d]), dot);
 #pragma unroll
-    for (int w = 16; w >= 1; w >>= 1) dot += __shfl_xor_sync(kFull, dot, w);
+    for (int o = 16; o >= 1; o >>= 1) dot += __shfl_xor_sync(kFull, dot, o);
     if (lane == 0) sn[g] = dot;
   }
-  __syncthreads();
+  team_sync<NTH>();
 }
 
 // Running merge of softmax states (max m, sum l, output slice o) over the
@@ -303,17 +330,20 @@ struct Merge8 {
 
 // Output and write-back of unit u = (b, j) once all of its segments are done.
 // Each thread takes 8 consecutive dims of one head; `states(g, d, mg)` folds
-// the unit's segment states for head g, dims d..d+7 into mg. Needs new_token
-// (kh, sn, sig) and the staged v_new row in `in`. All threads take part.
-template <int D, int GP, bool PAGED, typename States>
-__device__ void finish_unit(const DecodeArgs& a, int u, const uint8_t* in, const uint16_t* kh,
-                            const float* sn, const float* sig, States states) {
+// the unit's segment states for head g, dims d..d+7 into mg. Needs the new
+// token in the unit's input slot. No barrier at the end.
+template <int D, int GP, bool PAGED, int NTH, typename States>
+__device__ __forceinline__ void finish_unit(const DecodeArgs& a, int u, const uint8_t* slot, int t,
+                                            States states) {
   using Gm = Geo<D, GP / 4>;
   const int Hkv = a.Hkv, G = a.G, Hq = Hkv * G;
   const int b = u / Hkv, j = u - b * Hkv;
   const CacheView& c = a.c;
-  const uint16_t* vsrc = reinterpret_cast<const uint16_t*>(in + Gm::IN_V);
-  for (int e = threadIdx.x * 8; e < G * D; e += kThreads * 8) {
+  const uint16_t* vsrc = reinterpret_cast<const uint16_t*>(slot + Gm::IN_V);
+  const uint16_t* kh = reinterpret_cast<const uint16_t*>(slot + Gm::IN_KH);
+  const float* sn = reinterpret_cast<const float*>(slot + Gm::IN_SN);
+  const float* sig = reinterpret_cast<const float*>(slot + Gm::IN_SIG);
+  for (int e = t * 8; e < G * D; e += NTH * 8) {
     const int g = e / D, d = e - g * D;
     Merge8 mg;
     mg.M = sn[g];
@@ -338,7 +368,7 @@ __device__ void finish_unit(const DecodeArgs& a, int u, const uint8_t* in, const
       const int pg = pi < c.bt_stride ? c.block_table[static_cast<int64_t>(b) * c.bt_stride + pi] : -1;
       if (pg >= 0 && pg < c.n_rows)
         wb = ((static_cast<int64_t>(pg) * Hkv + j) * c.P + n % c.P) * D;
-      else if (threadIdx.x == 0)
+      else if (t == 0)
         raise_error(a.err, ERR_INDEX);
     } else {
       const int row = c.stream_rows ? c.stream_rows[b] : b;
@@ -347,13 +377,190 @@ __device__ void finish_unit(const DecodeArgs& a, int u, const uint8_t* in, const
         wb = ((static_cast<int64_t>(row) * Hkv + j) * c.R + head) * D;
     }
     if (wb >= 0) {
-      for (int d = threadIdx.x * 8; d < D; d += kThreads * 8) {
+      for (int d = t * 8; d < D; d += NTH * 8) {
         *reinterpret_cast<uint4*>(c.k + wb + d) = *reinterpret_cast<const uint4*>(kh + d);
         *reinterpret_cast<uint4*>(c.v + wb + d) = *reinterpret_cast<const uint4*>(vsrc + d);
       }
     }
   }
-  __syncthreads();
+}
+
+// The streaming warps' states of one segment (merge buffers: warp w's stage
+// SLOT[w], or none when SLOT[w] < 0) folded into mg for head g, dims d..d+7.
+template <int D, int NT>
+__device__ __forceinline__ void fold_warps(const uint8_t* smem, const float* ML, const int* SLOT, int g, int d,
+                                           Merge8& mg) {
+  using Gm = Geo<D, NT>;
+  constexpr int GP = Gm::GP;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const int st = SLOT[w];
+    if (st < 0) continue;
+    const float* os = reinterpret_cast<const float*>(smem + (w * Gm::NS + st) * Gm::STAGE) + g * D + d;
+    const float4 x0 = *reinterpret_cast<const float4*>(os);
+    const float4 x1 = *reinterpret_cast<const float4*>(os + 4);
+    const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+    mg.add(ML[w * 2 * GP + g], ML[w * 2 * GP + GP + g], x);
+  }
+}
+
+// The streaming warps' states of one segment merged into the partial slot
+// dst: o[GP][D] (relative to the merged maximum), then m[GP], l[GP]. No
+// barrier at the end.
+template <int D, int NT, int NTH>
+__device__ __forceinline__ void write_partial(const uint8_t* smem, const float* ML, const int* SLOT, float* dst,
+                                              int t) {
+  using Gm = Geo<D, NT>;
+  constexpr int GP = Gm::GP;
+  for (int e = t * 8; e < GP * D; e += NTH * 8) {
+    const int h = e / D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w)
+      if (SLOT[w] >= 0) M = fmaxf(M, ML[w * 2 * GP + h]);
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const int st = SLOT[w];
+        if (st < 0) continue;
+        const float f = exp2_fast(ML[w * 2 * GP + h] - M);
+        const float* os = reinterpret_cast<const float*>(smem + (w * Gm::NS + st) * Gm::STAGE) + e;
+        const float4 x0 = *reinterpret_cast<const float4*>(os);
+        const float4 x1 = *reinterpret_cast<const float4*>(os + 4);
+        acc[0] = fmaf(f, x0.x, acc[0]); acc[1] = fmaf(f, x0.y, acc[1]);
+        acc[2] = fmaf(f, x0.z, acc[2]); acc[3] = fmaf(f, x0.w, acc[3]);
+        acc[4] = fmaf(f, x1.x, acc[4]); acc[5] = fmaf(f, x1.y, acc[5]);
+        acc[6] = fmaf(f, x1.z, acc[6]); acc[7] = fmaf(f, x1.w, acc[7]);
+      }
+    }
+    *reinterpret_cast<float4*>(dst + e) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    *reinterpret_cast<float4*>(dst + e + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+  for (int h = t; h < GP; h += NTH) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w)
+      if (SLOT[w] >= 0) M = fmaxf(M, ML[w * 2 * GP + h]);
+    float L = 0.f;
+    if (M != -INFINITY)
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w)
+        if (SLOT[w] >= 0) L = fmaf(exp2_fast(ML[w * 2 * GP + h] - M), ML[w * 2 * GP + GP + h], L);
+    dst[GP * D + h] = M;
+    dst[GP * D + GP + h] = L;
+  }
+}
+
+// Bulk copies (issued by the calling thread) of unit u's q, k_new and v_new
+// rows into input slot n & 1, counted on that slot's mbarrier; the first
+// staging of a CTA (n == 0) also brings the layer's RoPE phase steps (the
+// table is allocated in whole 16-byte units).
+template <int D, int GP>
+__device__ __forceinline__ void issue_stage(const DecodeArgs& a, int u, int n, uint32_t inbar, uint8_t* in_slots,
+                                            uint64_t* step) {
+  using Gm = Geo<D, GP / 4>;
+  const int Hkv = a.Hkv, G = a.G;
+  const int b = u / Hkv, j = u - b * Hkv;
+  const uint32_t bar = inbar + 8 * (n & 1);
+  const uint32_t dst = smem_addr(in_slots + (n & 1) * Gm::IN_BYTES);
+  const uint32_t qbytes = static_cast<uint32_t>(G) * D * 2;
+  const uint32_t sbytes = n == 0 ? (static_cast<uint32_t>(a.r / 2) * 8u + 15u) / 16u * 16u : 0u;
+  const uint64_t pol = l2_evict_first_policy();
+  mbar_arrive_expect_tx(bar, qbytes + 4u * D + sbytes);
+  if (sbytes) bulk_copy_g2s(smem_addr(step), a.rope_step, sbytes, bar, pol);
+  bulk_copy_g2s(dst + Gm::IN_Q, a.q + (static_cast<int64_t>(b) * Hkv + j) * G * D, qbytes, bar, pol);
+  bulk_copy_g2s(dst + Gm::IN_K, a.k_new + (static_cast<int64_t>(b) * Hkv + j) * D, 2u * D, bar, pol);
+  bulk_copy_g2s(dst + Gm::IN_V, a.v_new + (static_cast<int64_t>(b) * Hkv + j) * D, 2u * D, bar, pol);
+}
+
+// End of one segment of unit u, whose streaming warps' states are in their
+// merge buffers. When the unit lies wholly in this CTA, its output and
+// write-back follow from those states; otherwise they are merged into the
+// segment's partial slot, and the CTA finishing the unit's last segment (a
+// per-unit counter) merges all of its partials. `release()` runs once the
+// merge buffers have been read; `wait_prev()` before the first output store.
+template <int D, int NT, bool PAGED, int NTH, typename WaitPrev, typename Release>
+__device__ void end_segment(const DecodeArgs& a, const Split& sp, int pieces, int u, bool first_seg, int cta,
+                            const uint8_t* smem, const float* ML, const int* SLOT, const uint8_t* slot, int* flag,
+                            int t, WaitPrev wait_prev, Release release) {
+  using Gm = Geo<D, NT>;
+  constexpr int GP = Gm::GP;
+  const int NC = sp.NC, p0 = sp.P[u], p1 = sp.P[u + 1];
+  int c_lo = 0, c_hi = 0, first_slot = 0, nseg, S;
+  if (pieces) {
+    nseg = min(pieces, p1 - p0);
+    S = pieces;
+  } else {
+    nseg = unit_segments(sp, p0, p1, u, c_lo, c_hi, first_slot);
+    S = c_hi - c_lo + 1;
+  }
+  if (nseg == 1) {
+    // the whole unit lies in this CTA: the warps' states go straight into the output
+    wait_prev();
+    finish_unit<D, GP, PAGED, NTH>(a, u, slot, t, [&](int g, int d, Merge8& mg) {
+      fold_warps<D, NT>(smem, ML, SLOT, g, d, mg);
+    });
+    team_sync<NTH>();
+    release();
+    return;
+  }
+  const int pslot = first_seg ? cta : NC + u;
+  write_partial<D, NT, NTH>(smem, ML, SLOT, a.part + static_cast<int64_t>(pslot) * (GP * (D + 2)), t);
+  __threadfence();
+  team_sync<NTH>();
+  release();
+  // count this segment; the team finishing the unit's last segment combines it
+  int last;
+  if constexpr (NTH == 32) {
+    last = t == 0 ? atomicAdd(a.counters + u, 1) == nseg - 1 : 0;
+    last = __shfl_sync(kFull, last, 0);
+  } else {
+    if (t == 0) *flag = atomicAdd(a.counters + u, 1) == nseg - 1;
+    __syncthreads();
+    last = *flag;
+  }
+  if (!last) return;
+  __threadfence();
+  wait_prev();
+  // candidate k: the partial slot of the k-th CTA of the unit's span, and
+  // whether it holds tiles of the unit
+  auto cand_slot = [&](int k) { return pieces ? u * pieces + k : (k == 0 ? first_slot : c_lo + k); };
+  auto cand_ok = [&](int k) -> bool {
+    if (k >= S) return false;
+    if (pieces) return (k + 1) * (p1 - p0) / pieces > k * (p1 - p0) / pieces;
+    // candidate k > 0 is the first segment of CTA c_lo + k, unless that CTA got no tiles
+    return k == 0 || sp.has_tiles_inside(c_lo + k);
+  };
+  const int stride = GP * (D + 2);
+  finish_unit<D, GP, PAGED, NTH>(a, u, slot, t, [&](int g, int d, Merge8& mg) {
+    for (int k0 = 0; k0 < S; k0 += 4) {
+      float m[4], l[4], x[4][8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int k = k0 + q;
+        m[q] = -INFINITY;
+        l[q] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[q][i] = 0.f;
+        if (cand_ok(k)) {
+          const float* pk = a.part + static_cast<int64_t>(cand_slot(k)) * stride;
+          m[q] = __ldcg(pk + GP * D + g);
+          l[q] = __ldcg(pk + GP * D + GP + g);
+          const float4 y0 = __ldcg(reinterpret_cast<const float4*>(pk + g * D + d));
+          const float4 y1 = __ldcg(reinterpret_cast<const float4*>(pk + g * D + d + 4));
+          x[q][0] = y0.x; x[q][1] = y0.y; x[q][2] = y0.z; x[q][3] = y0.w;
+          x[q][4] = y1.x; x[q][5] = y1.y; x[q][6] = y1.z; x[q][7] = y1.w;
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) mg.add(m[q], l[q], x[q]);
+    }
+  });
+  if (t == 0) a.counters[u] = 0;
+  team_sync<NTH>();
 }
 
 template <int D, int NT, bool PAGED>
@@ -361,10 +568,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   using Gm = Geo<D, NT>;
   constexpr int GP = Gm::GP, KSTEPS = Gm::KSTEPS, BOXES = Gm::BOXES, KG = Gm::KG, NS = Gm::NS;
   extern __shared__ uint8_t smem_raw[];
+  __shared__ int warp_max[kThreads / 32];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const CacheView& c = a.c;
-  const int Hkv = a.Hkv, U = a.B * Hkv, G = a.G;
+  const int Hkv = a.Hkv, U = a.B * Hkv;
   const int NC = gridDim.x, cta = blockIdx.x;
   int* P = reinterpret_cast<int*>(smem + Gm::TAB_OFF);  // [U + 1] tile prefix over units
   int* N = P + U + 1;                                    // [U] cached keys per unit
@@ -372,29 +580,32 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   int* RW = HD + U;                                      // [U] ring: cache row
   float* ML = reinterpret_cast<float*>(smem + Gm::ML_OFF);
   int* SLOT = reinterpret_cast<int*>(smem + Gm::SLOT_OFF);
-  float* sn = reinterpret_cast<float*>(smem + Gm::SN_OFF);
   int* flag = reinterpret_cast<int*>(smem + Gm::FLAG_OFF);
   float2* cs = reinterpret_cast<float2*>(smem + Gm::CS_OFF);
   float* qs = reinterpret_cast<float*>(smem + Gm::QS_OFF);
-  uint16_t* kh = reinterpret_cast<uint16_t*>(smem + Gm::KH_OFF);
-  int* wrow = reinterpret_cast<int*>(smem + Gm::WROW_OFF) + warp * 2 * kWin * KG;
-  int* wmask = reinterpret_cast<int*>(smem + Gm::WMASK_OFF) + warp * 2 * kWin * KG;
   uint64_t* step = reinterpret_cast<uint64_t*>(smem + Gm::STEP_OFF);
-  float* sig = reinterpret_cast<float*>(smem + Gm::SIG_OFF);
-  const uint32_t inbar = smem_addr(smem + Gm::INBAR_OFF);
   uint8_t* in_slots = smem + Gm::IN_OFF;
+  const uint32_t stage_bars = smem_addr(smem + Gm::BAR_OFF);
+  const uint32_t inbar = smem_addr(smem + Gm::INBAR_OFF);
+  const uint32_t prep_full = smem_addr(smem + Gm::PREP_FULL_OFF);
+  const uint32_t prep_empty = smem_addr(smem + Gm::PREP_EMPTY_OFF);
+  const uint32_t merge_full = smem_addr(smem + Gm::MERGE_FULL_OFF);
+  const uint32_t merge_empty = smem_addr(smem + Gm::MERGE_EMPTY_OFF);
 
-  const uint32_t bar0 = smem_addr(smem + Gm::BAR_OFF) + warp * NS * 8;
-  if (lane == 0) {
-    for (int s = 0; s < NS; ++s) mbar_init(bar0 + 8 * s, 1);  // this warp's stages
-    if (warp == 0) {
-      mbar_init(inbar, 1);  // the input slots, used by the whole CTA
-      mbar_init(inbar + 8, 1);
-    }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kWarps * NS; ++i) mbar_init(stage_bars + 8 * i, 1);
+    mbar_init(inbar, 1);  // the input slots
+    mbar_init(inbar + 8, 1);
+    mbar_init(prep_full, 1);
+    mbar_init(prep_empty, kWarps);
+    mbar_init(merge_full, kWarps);
+    mbar_init(merge_empty, 1);
     fence_mbar_init();
   }
 
-  // ---- unit table from caller metadata (no kernel of this library writes it)
+  // ---- unit table from caller metadata (no kernel of this library writes
+  // it): tiles per unit, then their prefix sum
+  int max_tiles = 0;
   for (int u = threadIdx.x; u < U; u += kThreads) {
     const int b = u / Hkv;
     const int n = unit_length<PAGED>(c, b, a.max_len, cta == 0 && u - b * Hkv == 0, a.err);
@@ -405,32 +616,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       RW[u] = c.stream_rows ? c.stream_rows[b] : b;
     }
     N[u] = n;
-    P[u + 1] = (unit_groups<PAGED>(c, head, n) + KG - 1) / KG;
+    const int tiles = (unit_groups<PAGED>(c, head, n) + KG - 1) / KG;
+    P[u + 1] = tiles;
+    max_tiles = max(max_tiles, tiles);
   }
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) max_tiles = max(max_tiles, __shfl_xor_sync(kFull, max_tiles, w));
+  if (lane == 0) warp_max[warp] = max_tiles;
   if (threadIdx.x == 0) P[0] = 0;
   __syncthreads();
   block_scan_inclusive<kThreads>(P + 1, U);
   const int T = P[U];
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) max_tiles = max(max_tiles, warp_max[w]);
 
   // ---- the split of the tiles over the grid. Pieces: when there are no more
   // units than CTAs and cutting every unit into s = NC / U equal pieces (one
-  // CTA each) leaves the largest piece within 5/4 of a fair share, CTA
-  // u * s + k takes piece k of unit u - units mostly end inside one CTA and
-  // few partials cross CTAs. Otherwise stream-K over the units laid end to
+  // CTA each) leaves the largest piece within kPiecesSlack of a fair share,
+  // CTA u * s + k takes piece k of unit u - units mostly end inside one CTA
+  // and few partials cross CTAs. Otherwise stream-K over the units laid end to
   // end, each weighted with the fixed cost of a segment (Split).
-  int max_tiles = 0;
-  for (int u = threadIdx.x; u < U; u += kThreads) max_tiles = max(max_tiles, P[u + 1] - P[u]);
-#pragma unroll
-  for (int w = 16; w >= 1; w >>= 1) max_tiles = max(max_tiles, __shfl_xor_sync(kFull, max_tiles, w));
-  if (lane == 0) SLOT[warp] = max_tiles;
-  __syncthreads();
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) max_tiles = max(max_tiles, SLOT[w]);
   const Split sp{P, U, a.unit_cost, NC, T + static_cast<int64_t>(a.unit_cost) * U};
   int pieces = 0;
   if (U <= NC && T > 0) {
     const int s = NC / U;
-    if (4 * ((max_tiles + s - 1) / s) <= 5 * ((T + NC - 1) / NC)) pieces = s;
+    if (100 * ((max_tiles + s - 1) / s) <= (100 + kPiecesSlack) * ((T + NC - 1) / NC)) pieces = s;
   }
   int g0, g1;
   if (pieces) {
@@ -442,143 +652,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     g0 = sp.tile_at(sp.bound(cta));
     g1 = sp.tile_at(sp.bound(cta + 1));
   }
-
-  // ---- this warp's tiles: g = g0 + warp + kWarps * it
   const int span = g1 - g0;
-  const int my_n = span > warp ? (span - warp + kWarps - 1) / kWarps : 0;
-  uint8_t* wsm = smem + warp * NS * Gm::STAGE;
-  const uint32_t wsm_a = smem_addr(wsm);
-
-  // ---- the inputs of this CTA's units, staged ahead in two slots: q, k_new
-  // and v_new rows by bulk copy (thread 0), position and gate logits in
-  // registers (threads < G hold their head's logit)
+  // this CTA's units (segments), in order
   auto next_unit = [&](int u) {  // the next unit with tiles in this CTA's range
     for (++u; u < U && P[u] < g1; ++u)
       if (P[u + 1] > P[u]) return u;
     return U;
   };
-  int n_staged = 0, n_used = 0;
-  int pos_nxt = 0;
-  uint16_t gate_nxt = 0;  // raw bf16: converting here would wait for the load
-  auto stage = [&](int u) {
-    const int b = u / Hkv, j = u - b * Hkv;
-    if (threadIdx.x == 0) {
-      const uint32_t bar = inbar + 8 * (n_staged & 1);
-      const uint32_t dst = smem_addr(in_slots + (n_staged & 1) * Gm::IN_BYTES);
-      const uint32_t qbytes = G * D * 2;
-      // the first staging also brings the layer's RoPE phase steps (the table
-      // is allocated in whole 16-byte units)
-      const uint32_t sbytes = n_staged == 0 ? (static_cast<uint32_t>(a.r / 2) * 8u + 15u) / 16u * 16u : 0u;
-      mbar_arrive_expect_tx(bar, qbytes + 4u * D + sbytes);
-      if (sbytes) bulk_copy_g2s(smem_addr(step), a.rope_step, sbytes, bar, l2_evict_first_policy());
-      bulk_copy_g2s(dst + Gm::IN_Q, a.q + (static_cast<int64_t>(b) * Hkv + j) * G * D, qbytes, bar,
-                    l2_evict_first_policy());
-      bulk_copy_g2s(dst + Gm::IN_K, a.k_new + (static_cast<int64_t>(b) * Hkv + j) * D, 2u * D, bar,
-                    l2_evict_first_policy());
-      bulk_copy_g2s(dst + Gm::IN_V, a.v_new + (static_cast<int64_t>(b) * Hkv + j) * D, 2u * D, bar,
-                    l2_evict_first_policy());
-    }
-    pos_nxt = a.pos[b];
-    gate_nxt = (a.gate && threadIdx.x < G) ? a.gate[(static_cast<int64_t>(b) * Hkv + j) * G + threadIdx.x] : 0;
-    ++n_staged;
-  };
-  // wait for the oldest staged unit; its slot
-  auto take = [&](int& pos, float& gate_g) -> const uint8_t* {
-    const int s = n_used & 1;
-    if (!mbar_wait_bounded(inbar + 8 * s, (n_used >> 1) & 1)) raise_error(a.err, ERR_TIMEOUT);
-    pos = pos_nxt;
-    gate_g = bf16_to_f32(gate_nxt);
-    ++n_used;
-    return in_slots + s * Gm::IN_BYTES;
-  };
-  const int u_first = span > 0 ? unit_of(P, U, g0) : U;
+  const int u_first = span > 0 ? unit_of(P, U, g0) : U;  // the first unit of a range has tiles in it
+  int n_segs = 0, u_last = U;
+  for (int u = u_first; u < U; u = next_unit(u)) {
+    u_last = u;
+    ++n_segs;
+  }
 
-  // Window w of this warp: tiles 32w..32w+31, one per lane. For each group of
-  // the tile: the first tensor row of its TMA boxes and its valid-row mask
-  // (0 = no such group). Stored in half (w & 1) of the warp's window arrays.
-  auto fill = [&](int w) {
-    const int x = w * kWin + lane;
-    int rows[KG], masks[KG];
-#pragma unroll
-    for (int kg = 0; kg < KG; ++kg) rows[kg] = masks[kg] = 0;
-    if (x < my_n) {
-      const int g = g0 + warp + kWarps * x;
-      const int u = unit_of(P, U, g);
-      const int b = u / Hkv, j = u - b * Hkv;
-      const int n = N[u];
-      if constexpr (PAGED) {
-        const int gpp = (c.P + kGroup - 1) / kGroup;
-        const int groups = unit_groups<true>(c, 0, n);
-#pragma unroll
-        for (int kg = 0; kg < KG; ++kg) {
-          const int gi = (g - P[u]) * KG + kg;
-          if (gi < groups) {
-            const int pi = gi / gpp, gr = gi - pi * gpp;
-            int pg = c.block_table[static_cast<int64_t>(b) * c.bt_stride + pi];
-            if (pg < 0 || pg >= c.n_rows) {
-              raise_error(a.err, ERR_INDEX);
-              pg = 0;
-            }
-            rows[kg] = (pg * Hkv + j) * c.P + gr * kGroup;
-            masks[kg] = static_cast<int>(row_bits(0, min(c.P - gr * kGroup, n - (pi * c.P + gr * kGroup))));
-          }
-        }
-      } else {
-        const int R = c.R, nb = (R + kGroup - 1) / kGroup;
-        const int head = HD[u], row = RW[u];
-        const int groups = unit_groups<false>(c, head, n);
-        const int start = ring_start(head, n, R), end = start + n;  // valid: [start, end) mod R
-#pragma unroll
-        for (int kg = 0; kg < KG; ++kg) {
-          const int gi = (g - P[u]) * KG + kg;
-          if (gi < groups) {
-            int pb = (start >> 4) + gi;
-            if (pb >= nb) pb -= nb;
-            const int s0 = pb * kGroup;
-            rows[kg] = (row * Hkv + j) * R + s0;
-            uint32_t m = row_bits(start - s0, min(end, R) - s0);
-            if (end > R) m |= row_bits(-s0, end - R - s0);
-            masks[kg] = static_cast<int>(m);
-          }
-        }
-      }
-    }
-    int* wr = wrow + (w & 1) * kWin * KG;
-    int* wm = wmask + (w & 1) * kWin * KG;
-#pragma unroll
-    for (int kg = 0; kg < KG; ++kg) {
-      wr[lane * KG + kg] = rows[kg];
-      wm[lane * KG + kg] = masks[kg];
-    }
-    __syncwarp();
-  };
-  fill(0);
-  if (my_n > kWin) fill(1);
-
-  const uint64_t policy = l2_evict_first_policy();
-  // Request tile x of this warp into stage x % NS (one lane).
-  auto issue = [&](int x) {
-    const int* wr = wrow + ((x / kWin) & 1) * kWin * KG + (x % kWin) * KG;
-    const int* wm = wmask + ((x / kWin) & 1) * kWin * KG + (x % kWin) * KG;
-    int gn = 0;
-#pragma unroll
-    for (int kg = 0; kg < KG; ++kg) gn += wm[kg] != 0;
-    const uint32_t bar = bar0 + 8 * (x % NS);
-    const uint32_t kd = wsm_a + (x % NS) * Gm::STAGE;
-    mbar_arrive_expect_tx(bar, 2u * gn * Gm::GBYTES);
-#pragma unroll
-    for (int kg = 0; kg < KG; ++kg) {
-      if (kg < gn) {
-        const int row0 = wr[kg];
-#pragma unroll
-        for (int bx = 0; bx < BOXES; ++bx) {
-          tma_load_2d(kd + kg * Gm::GBYTES + bx * kBoxBytes, &a.tmap_k, 64 * bx, row0, bar, policy);
-          tma_load_2d(kd + Gm::KHALF + kg * Gm::GBYTES + bx * kBoxBytes, &a.tmap_v, 64 * bx, row0, bar,
-                      policy);
-        }
-      }
-    }
-  };
   // Ordering with the preceding launch on the stream, which may still run:
   // it may be writing its new entries into its own cache, its outputs and its
   // partials (the other half of the double-buffered workspace). This call's
@@ -595,377 +682,454 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       waited = true;
     }
   };
-  // the first unit's inputs go first: behind the tiles they would arrive late
-  if (u_first < U) stage(u_first);  // the first unit of a range always has tiles in it
   if (!a.early) wait_prev();
-  if (lane == 0) {
-    const int pre = my_n < NS ? my_n : NS;
-    for (int x = 0; x < pre; ++x) issue(x);
-  }
 
-  // Per-lane ldmatrix offsets inside a group's 2 KB boxes (128-byte swizzle:
-  // the 16-byte chunk index is XORed with the row mod 8). K (scores, A = K):
-  // matrix m = lane / 8 covers rows 8 * (m & 1) + 0..7 and chunk (m >> 1) of
-  // a k-step's pair of chunks. V (outputs, A = V^T, loaded transposed):
-  // matrix m covers rows 8 * (m >> 1) + 0..7 and chunk (m & 1).
-  const int lr = lane & 7, lm = lane >> 3;
-  uint32_t koff[4], voff[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int rk = lr + 8 * (lm & 1), rv = lr + 8 * (lm >> 1);
-    koff[q] = rk * 128 + (((2 * q + (lm >> 1)) ^ lr) << 4);
-    voff[q] = rv * 128 + (((2 * q + (lm & 1)) ^ lr) << 4);
-  }
-  const int fg = lane >> 2, fc = 2 * (lane & 3);  // fragment row group, column pair
-  // heads of this lane's score / output columns (e = 0, 1): the hi and lo
-  // columns of one head are lanes l and l ^ 2 (NT == 1) or tiles 0 and 1 (NT == 2)
-  const int hbase = NT == 1 ? 2 * (lane & 1) : fc;
-  const bool lo_lane = NT == 1 && (lane & 2) != 0;
+  if (warp != kHelper) {
+    // ================= streaming warp: tiles g = g0 + warp + kWarps * it
+    const int my_n = span > warp ? (span - warp + kWarps - 1) / kWarps : 0;
+    uint8_t* wsm = smem + warp * NS * Gm::STAGE;
+    const uint32_t wsm_a = smem_addr(wsm);
+    const uint32_t bar0 = stage_bars + warp * NS * 8;
+    int* wrow = reinterpret_cast<int*>(smem + Gm::WROW_OFF) + warp * 2 * kWin * KG;
+    int* wmask = reinterpret_cast<int*>(smem + Gm::WMASK_OFF) + warp * 2 * kWin * KG;
 
-  bool failed = false;
-  int it = 0;
-  int deferred = -1;
-  bool first_seg = true;
-  for (int u = u_first; u < U; u = next_unit(u)) {
-    const int ge = min(g1, P[u + 1]);
-
-    // ---- the unit's staged inputs; stage the next unit's meanwhile
-    int pos_u;
-    float gate_u;
-    const uint8_t* in_u = take(pos_u, gate_u);
-    const int u_nxt = next_unit(u);
-    __syncthreads();  // the slot about to be refilled was last read before this point
-    if (u_nxt < U) stage(u_nxt);
-
-    // ---- the unit's rotated q (all threads), then q^T as B fragments:
-    // column n = fg of tile t holds one head's hi or lo part
-    rotate_q<D, GP>(a, reinterpret_cast<const uint16_t*>(in_u + Gm::IN_Q), pos_u, step, qs, cs);
-    __syncthreads();
-    // the new token's K entry and scores now, while the first tiles arrive;
-    // they are used when this CTA finishes the unit
-    new_token<D, GP>(a, qs, cs, in_u, gate_u, kh, sn, sig);
-    uint32_t qb[KSTEPS][NT][2];
+    // Window w of this warp: tiles 32w..32w+31, one per lane. For each group of
+    // the tile: the first tensor row of its TMA boxes and its valid-row mask
+    // (0 = no such group). Stored in half (w & 1) of the warp's window arrays.
+    auto fill = [&](int w) {
+      const int x = w * kWin + lane;
+      int rows[KG], masks[KG];
 #pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      const int head = NT == 1 ? (fg & 3) : fg;
-      const bool lo = NT == 1 ? fg >= 4 : t == 1;
-      const float* src = qs + head * D + fc;
+      for (int kg = 0; kg < KG; ++kg) rows[kg] = masks[kg] = 0;
+      if (x < my_n) {
+        const int g = g0 + warp + kWarps * x;
+        const int u = unit_of(P, U, g);
+        const int b = u / Hkv, j = u - b * Hkv;
+        const int n = N[u];
+        if constexpr (PAGED) {
+          const int gpp = (c.P + kGroup - 1) / kGroup;
+          const int groups = unit_groups<true>(c, 0, n);
 #pragma unroll
-      for (int ks = 0; ks < KSTEPS; ++ks) {
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const float2 x = *reinterpret_cast<const float2*>(src + ks * 16 + h2 * 8);
-          uint32_t hi, lw;
-          split_bf16x2(x.x, x.y, hi, lw);
-          qb[ks][t][h2] = lo ? lw : hi;
-        }
-      }
-    }
-    float o[KSTEPS][NT][4];
-#pragma unroll
-    for (int mt = 0; mt < KSTEPS; ++mt)
-#pragma unroll
-      for (int t = 0; t < NT; ++t)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o[mt][t][e] = 0.f;
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-    int last_stage = -1;
-
-    for (;;) {
-      const int g = g0 + warp + kWarps * it;
-      if (it >= my_n || g >= ge) break;
-      // the window after next: its half was last read for tiles now behind
-      if (it >= kWin && (it & (kWin - 1)) == 0 && it + kWin < my_n) fill(it / kWin + 1);
-      const int stg = it % NS;
-      if (!failed) {
-        // the whole warp agrees on the outcome, so the collectives below stay converged
-        const bool ok = __all_sync(kFull, mbar_wait_bounded(bar0 + 8 * stg, (it / NS) & 1));
-        if (!ok) {
-          failed = true;
-          if (lane == 0) raise_error(a.err, ERR_TIMEOUT);
-        }
-      }
-      if (!failed) {
-        const int* wm = wmask + ((it / kWin) & 1) * kWin * KG + (it % kWin) * KG;
-#pragma unroll
-        for (int kg = 0; kg < KG; ++kg) {
-          const uint32_t mask = static_cast<uint32_t>(wm[kg]);
-          if (mask == 0u) break;  // the unit's last tile has fewer groups
-          const uint32_t kbase = wsm_a + stg * Gm::STAGE + kg * Gm::GBYTES;
-          const uint32_t vbase = kbase + Gm::KHALF;
-          if (mask != 0xffffu) {
-            // zero the V rows of invalid keys (their probabilities are 0, but
-            // the rows may hold NaN and 0 * NaN is NaN)
-            uint8_t* vg = wsm + stg * Gm::STAGE + Gm::KHALF + kg * Gm::GBYTES;
-            for (int i = lane; i < kGroup * BOXES * 8; i += 32) {
-              const int row = i / (BOXES * 8), rest = i - row * (BOXES * 8);
-              if (!((mask >> row) & 1u))
-                *reinterpret_cast<uint4*>(vg + (rest >> 3) * kBoxBytes + row * 128 + (rest & 7) * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
-            }
-            fence_proxy_async_smem();  // before the stage is refilled by TMA
-            __syncwarp();
-          }
-
-          // ---- scores S^T = K . Q^T (two accumulator chains)
-          float sacc[2][NT][4];
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2)
-#pragma unroll
-            for (int t = 0; t < NT; ++t)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) sacc[h2][t][e] = 0.f;
-#pragma unroll
-          for (int ks = 0; ks < KSTEPS; ++ks) {
-            uint32_t af[4];
-            ldsm_x4(kbase + (ks >> 2) * kBoxBytes + koff[ks & 3], af);
-#pragma unroll
-            for (int t = 0; t < NT; ++t) mma_bf16(sacc[ks & 1][t], af, qb[ks][t][0], qb[ks][t][1]);
-          }
-          // full scores of heads hbase + e at keys fg (i = e) and fg + 8 (i = 2 + e)
-          float s[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            if (NT == 1) {
-              const float x = sacc[0][0][i] + sacc[1][0][i];
-              s[i] = x + __shfl_xor_sync(kFull, x, 2);
-            } else {
-              s[i] = (sacc[0][0][i] + sacc[1][0][i]) + (sacc[0][NT - 1][i] + sacc[1][NT - 1][i]);
-            }
-          }
-          if (!((mask >> fg) & 1u)) s[0] = s[1] = -INFINITY;
-          if (!((mask >> (fg + 8)) & 1u)) s[2] = s[3] = -INFINITY;
-
-          // ---- online softmax (base 2), per head over the 16 keys
-          float corr[2], p[4];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            float mx = fmaxf(s[e], s[2 + e]);
-            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
-            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
-            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
-            const float m_new = fmaxf(m_run[e], mx);
-            const float ms = m_new == -INFINITY ? 0.f : m_new;
-            corr[e] = exp2_fast(m_run[e] - ms);
-            p[e] = exp2_fast(s[e] - ms);
-            p[2 + e] = exp2_fast(s[2 + e] - ms);
-            l_run[e] = fmaf(l_run[e], corr[e], p[e] + p[2 + e]);
-            m_run[e] = m_new;
-          }
-          if (__any_sync(kFull, corr[0] != 1.f || corr[1] != 1.f)) {
-#pragma unroll
-            for (int mt = 0; mt < KSTEPS; ++mt)
-#pragma unroll
-              for (int t = 0; t < NT; ++t) {
-                o[mt][t][0] *= corr[0];
-                o[mt][t][1] *= corr[1];
-                o[mt][t][2] *= corr[0];
-                o[mt][t][3] *= corr[1];
+          for (int kg = 0; kg < KG; ++kg) {
+            const int gi = (g - P[u]) * KG + kg;
+            if (gi < groups) {
+              const int pi = gi / gpp, gr = gi - pi * gpp;
+              int pg = c.block_table[static_cast<int64_t>(b) * c.bt_stride + pi];
+              if (pg < 0 || pg >= c.n_rows) {
+                raise_error(a.err, ERR_INDEX);
+                pg = 0;
               }
-          }
-
-          // ---- P^T as B fragments (hi and lo bf16 parts), via 8x8 transposes
-          uint32_t pb[NT][2];
-          {
-            uint32_t h01, l01, h23, l23;
-            split_bf16x2(p[0], p[1], h01, l01);
-            split_bf16x2(p[2], p[3], h23, l23);
-            if (NT == 1) {
-              pb[0][0] = movm_t(lo_lane ? l01 : h01);
-              pb[0][1] = movm_t(lo_lane ? l23 : h23);
-            } else {
-              pb[0][0] = movm_t(h01);
-              pb[0][1] = movm_t(h23);
-              pb[NT - 1][0] = movm_t(l01);
-              pb[NT - 1][1] = movm_t(l23);
+              rows[kg] = (pg * Hkv + j) * c.P + gr * kGroup;
+              masks[kg] = static_cast<int>(row_bits(0, min(c.P - gr * kGroup, n - (pi * c.P + gr * kGroup))));
             }
           }
-
-          // ---- outputs O^T += V^T . P^T
+        } else {
+          const int R = c.R, nb = (R + kGroup - 1) / kGroup;
+          const int head = HD[u], row = RW[u];
+          const int groups = unit_groups<false>(c, head, n);
+          const int start = ring_start(head, n, R), end = start + n;  // valid: [start, end) mod R
 #pragma unroll
-          for (int mt = 0; mt < KSTEPS; ++mt) {
-            uint32_t af[4];
-            ldsm_x4_t(vbase + (mt >> 2) * kBoxBytes + voff[mt & 3], af);
-#pragma unroll
-            for (int t = 0; t < NT; ++t) mma_bf16(o[mt][t], af, pb[t][0], pb[t][1]);
+          for (int kg = 0; kg < KG; ++kg) {
+            const int gi = (g - P[u]) * KG + kg;
+            if (gi < groups) {
+              int pb = (start >> 4) + gi;
+              if (pb >= nb) pb -= nb;
+              const int s0 = pb * kGroup;
+              rows[kg] = (row * Hkv + j) * R + s0;
+              uint32_t m = row_bits(start - s0, min(end, R) - s0);
+              if (end > R) m |= row_bits(-s0, end - R - s0);
+              masks[kg] = static_cast<int>(m);
+            }
           }
         }
-        __syncwarp();
       }
-      last_stage = stg;
-      // Refill this stage with the warp's tile NS ahead. The warp's last tile
-      // of a segment keeps its stage as the merge buffer until the merge is done.
-      if (it + NS < my_n) {
-        if (g + kWarps >= ge) {
-          deferred = it + NS;
-        } else if (lane == 0 && !failed) {
-          issue(it + NS);
+      int* wr = wrow + (w & 1) * kWin * KG;
+      int* wm = wmask + (w & 1) * kWin * KG;
+#pragma unroll
+      for (int kg = 0; kg < KG; ++kg) {
+        wr[lane * KG + kg] = rows[kg];
+        wm[lane * KG + kg] = masks[kg];
+      }
+      __syncwarp();
+    };
+    fill(0);
+    if (my_n > kWin) fill(1);
+
+    const uint64_t policy = l2_evict_first_policy();
+    // Request tile x of this warp into stage x % NS (one lane).
+    auto issue = [&](int x) {
+      const int* wr = wrow + ((x / kWin) & 1) * kWin * KG + (x % kWin) * KG;
+      const int* wm = wmask + ((x / kWin) & 1) * kWin * KG + (x % kWin) * KG;
+      int gn = 0;
+#pragma unroll
+      for (int kg = 0; kg < KG; ++kg) gn += wm[kg] != 0;
+      const uint32_t bar = bar0 + 8 * (x % NS);
+      const uint32_t kd = wsm_a + (x % NS) * Gm::STAGE;
+      mbar_arrive_expect_tx(bar, 2u * gn * Gm::GBYTES);
+#pragma unroll
+      for (int kg = 0; kg < KG; ++kg) {
+        if (kg < gn) {
+          const int row0 = wr[kg];
+#pragma unroll
+          for (int bx = 0; bx < BOXES; ++bx) {
+            tma_load_2d(kd + kg * Gm::GBYTES + bx * kBoxBytes, &a.tmap_k, 64 * bx, row0, bar, policy);
+            tma_load_2d(kd + Gm::KHALF + kg * Gm::GBYTES + bx * kBoxBytes, &a.tmap_v, 64 * bx, row0, bar,
+                        policy);
+          }
         }
       }
-      ++it;
+    };
+    if (lane == 0) {
+      const int pre = my_n < NS ? my_n : NS;
+      for (int x = 0; x < pre; ++x) issue(x);
     }
 
-    // ---- this warp's state: l summed over the lanes of a head, O^T to the
-    // merge buffer as o[head][dim] (hi + lo columns)
+    // Per-lane ldmatrix offsets inside a group's 2 KB boxes (128-byte swizzle:
+    // the 16-byte chunk index is XORed with the row mod 8). K (scores, A = K):
+    // matrix m = lane / 8 covers rows 8 * (m & 1) + 0..7 and chunk (m >> 1) of
+    // a k-step's pair of chunks. V (outputs, A = V^T, loaded transposed):
+    // matrix m covers rows 8 * (m >> 1) + 0..7 and chunk (m & 1).
+    const int lr = lane & 7, lm = lane >> 3;
+    uint32_t koff[4], voff[4];
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      l_run[e] += __shfl_xor_sync(kFull, l_run[e], 4);
-      l_run[e] += __shfl_xor_sync(kFull, l_run[e], 8);
-      l_run[e] += __shfl_xor_sync(kFull, l_run[e], 16);
+    for (int q = 0; q < 4; ++q) {
+      const int rk = lr + 8 * (lm & 1), rv = lr + 8 * (lm >> 1);
+      koff[q] = rk * 128 + (((2 * q + (lm >> 1)) ^ lr) << 4);
+      voff[q] = rv * 128 + (((2 * q + (lm & 1)) ^ lr) << 4);
     }
-    if (last_stage >= 0) {
-      float* os = reinterpret_cast<float*>(wsm + last_stage * Gm::STAGE);
-      const bool writer = NT == 2 || !lo_lane;
+    const int fg = lane >> 2, fc = 2 * (lane & 3);  // fragment row group, column pair
+    // heads of this lane's score / output columns (e = 0, 1): the hi and lo
+    // columns of one head are lanes l and l ^ 2 (NT == 1) or tiles 0 and 1 (NT == 2)
+    const int hbase = NT == 1 ? 2 * (lane & 1) : fc;
+    const bool lo_lane = NT == 1 && (lane & 2) != 0;
+
+    bool failed = false;
+    auto check = [&](bool ok) {  // the whole warp agrees, so its collectives stay converged
+      if (!failed && !__all_sync(kFull, ok)) {
+        failed = true;
+        if (lane == 0) raise_error(a.err, ERR_TIMEOUT);
+      }
+    };
+    int it = 0;
+    int held = -1;  // tile whose stage still holds the previous segment's merge buffer
+    int seg = 0;
+    for (int u = u_first; u < U; u = next_unit(u), ++seg) {
+      const int ge = min(g1, P[u + 1]);
+
+      // ---- the unit's rotated q from the helper, as B fragments: column n =
+      // fg of tile t holds one head's hi or lo part
+      if (!failed) check(mbar_wait_bounded(prep_full, seg & 1));
+      uint32_t qb[KSTEPS][NT][2];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const int head = NT == 1 ? (fg & 3) : fg;
+        const bool lo = NT == 1 ? fg >= 4 : t == 1;
+        const float* src = qs + head * D + fc;
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks) {
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const float2 x = *reinterpret_cast<const float2*>(src + ks * 16 + h2 * 8);
+            uint32_t hi, lw;
+            split_bf16x2(x.x, x.y, hi, lw);
+            qb[ks][t][h2] = lo ? lw : hi;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(prep_empty);
+
+      float o[KSTEPS][NT][4];
 #pragma unroll
       for (int mt = 0; mt < KSTEPS; ++mt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float v;
-          if (NT == 1) {
-            v = o[mt][0][i] + __shfl_xor_sync(kFull, o[mt][0][i], 2);
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[mt][t][e] = 0.f;
+      float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+      int last_stage = -1, pend = -1;
+
+      for (;;) {
+        const int g = g0 + warp + kWarps * it;
+        if (it >= my_n || g >= ge) break;
+        // the window after next: its half was last read for tiles now behind
+        if (it >= kWin && (it & (kWin - 1)) == 0 && it + kWin < my_n) fill(it / kWin + 1);
+        // the previous segment's merge buffer streams again once the helper has read it
+        if (held >= 0) {
+          bool ready;
+          if (held == it) {
+            if (!failed) check(mbar_wait_bounded(merge_empty, (seg - 1) & 1));
+            ready = true;
           } else {
-            v = o[mt][0][i] + o[mt][NT - 1][i];
+            ready = __shfl_sync(kFull, mbar_test_wait(merge_empty, (seg - 1) & 1) ? 1 : 0, 0) != 0;
           }
-          if (writer) os[(hbase + (i & 1)) * D + mt * 16 + fg + 8 * (i >> 1)] = v;
+          if (ready) {
+            if (lane == 0 && !failed) issue(held);
+            held = -1;
+          }
         }
-      fence_proxy_async_smem();  // the buffer is refilled by TMA after the merge
-    }
-    if (fg == 0 && (NT == 2 || !lo_lane)) {
+        const int stg = it % NS;
+        if (!failed) check(mbar_wait_bounded(bar0 + 8 * stg, (it / NS) & 1));
+        if (!failed) {
+          const int* wm = wmask + ((it / kWin) & 1) * kWin * KG + (it % kWin) * KG;
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        ML[warp * 2 * GP + hbase + e] = last_stage >= 0 ? m_run[e] : -INFINITY;
-        ML[warp * 2 * GP + GP + hbase + e] = last_stage >= 0 ? l_run[e] : 0.f;
-      }
-    }
-    if (lane == 0) SLOT[warp] = last_stage;
-    __syncthreads();
-    // ---- segment end: how many CTAs hold pieces of this unit, and where
-    // their partials are (candidate k: slot, and whether it holds tiles)
-    int c_lo = 0, c_hi = 0, first_slot = 0, nseg, S;
-    const int p0 = P[u], p1 = P[u + 1];
-    if (pieces) {
-      nseg = min(pieces, p1 - p0);
-      S = pieces;
-    } else {
-      nseg = unit_segments(sp, p0, p1, u, c_lo, c_hi, first_slot);
-      S = c_hi - c_lo + 1;
-    }
-    auto cand_slot = [&](int k) { return pieces ? u * pieces + k : (k == 0 ? first_slot : c_lo + k); };
-    auto cand_ok = [&](int k) -> bool {
-      if (k >= S) return false;
-      if (pieces) return (k + 1) * (p1 - p0) / pieces > k * (p1 - p0) / pieces;
-      // candidate k > 0 is the first segment of CTA c_lo + k, unless that CTA got no tiles
-      return k == 0 || sp.has_tiles_inside(c_lo + k);
-    };
-    if (nseg == 1) {
-      // the whole unit lies in this CTA: the warps' states go straight into the output
-      wait_prev();
-      finish_unit<D, GP, PAGED>(a, u, in_u, kh, sn, sig, [&](int g, int d, Merge8& mg) {
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          const int st = SLOT[w];
-          if (st < 0) continue;
-          const float* os = reinterpret_cast<const float*>(smem + (w * NS + st) * Gm::STAGE) + g * D + d;
-          const float4 x0 = *reinterpret_cast<const float4*>(os);
-          const float4 x1 = *reinterpret_cast<const float4*>(os + 4);
-          const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-          mg.add(ML[w * 2 * GP + g], ML[w * 2 * GP + GP + g], x);
-        }
-      });
-      if (deferred >= 0) {  // the merge buffers are free again
-        if (lane == 0 && !failed) issue(deferred);
-        deferred = -1;
-      }
-    } else {
-      // merge the warps' states into this segment's partial slot
-      const int slot = first_seg ? cta : NC + u;
-      float* dst = a.part + static_cast<int64_t>(slot) * (GP * (D + 2));
-      for (int e = threadIdx.x; e < GP * D; e += kThreads) {
-        const int h = e / D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ML[w * 2 * GP + h]);
-        float acc = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-          for (int w = 0; w < kWarps; ++w) {
-            const int st = SLOT[w];
-            if (st >= 0) {
-              const float* os = reinterpret_cast<const float*>(smem + (w * NS + st) * Gm::STAGE);
-              acc = fmaf(exp2_fast(ML[w * 2 * GP + h] - M), os[e], acc);
+          for (int kg = 0; kg < KG; ++kg) {
+            const uint32_t mask = static_cast<uint32_t>(wm[kg]);
+            if (mask == 0u) break;  // the unit's last tile has fewer groups
+            const uint32_t kbase = wsm_a + stg * Gm::STAGE + kg * Gm::GBYTES;
+            const uint32_t vbase = kbase + Gm::KHALF;
+            if (mask != 0xffffu) {
+              // zero the V rows of invalid keys (their probabilities are 0, but
+              // the rows may hold NaN and 0 * NaN is NaN)
+              uint8_t* vg = wsm + stg * Gm::STAGE + Gm::KHALF + kg * Gm::GBYTES;
+              for (int i = lane; i < kGroup * BOXES * 8; i += 32) {
+                const int row = i / (BOXES * 8), rest = i - row * (BOXES * 8);
+                if (!((mask >> row) & 1u))
+                  *reinterpret_cast<uint4*>(vg + (rest >> 3) * kBoxBytes + row * 128 + (rest & 7) * 16) =
+                      make_uint4(0u, 0u, 0u, 0u);
+              }
+              fence_proxy_async_smem();  // before the stage is refilled by TMA
+              __syncwarp();
             }
-          }
-        }
-        dst[e] = acc;
-      }
-      if (threadIdx.x < GP) {
-        const int h = threadIdx.x;
-        float M = -INFINITY;
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ML[w * 2 * GP + h]);
-        float L = 0.f;
-        if (M != -INFINITY)
-          for (int w = 0; w < kWarps; ++w) L = fmaf(exp2_fast(ML[w * 2 * GP + h] - M), ML[w * 2 * GP + GP + h], L);
-        dst[GP * D + h] = M;
-        dst[GP * D + GP + h] = L;
-      }
-      __syncthreads();  // every read of the merge buffers is done
-      if (deferred >= 0) {  // the merge buffers are free again
-        if (lane == 0 && !failed) issue(deferred);
-        deferred = -1;
-      }
-      // count this segment; the CTA finishing the unit's last segment combines it
-      __threadfence();
-      __syncthreads();
-      if (threadIdx.x == 0) *flag = atomicAdd(a.counters + u, 1) == nseg - 1;
-      __syncthreads();
-      if (*flag) {
-        __threadfence();
-        wait_prev();
-        const int stride = GP * (D + 2);
-        finish_unit<D, GP, PAGED>(a, u, in_u, kh, sn, sig, [&](int g, int d, Merge8& mg) {
-          for (int k0 = 0; k0 < S; k0 += 4) {
-            float m[4], l[4], x[4][8];
+
+            // ---- scores S^T = K . Q^T (two accumulator chains)
+            float sacc[2][NT][4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int k = k0 + q;
-              const bool ok = cand_ok(k);
-              m[q] = -INFINITY;
-              l[q] = 0.f;
+            for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
-              for (int i = 0; i < 8; ++i) x[q][i] = 0.f;
-              if (ok) {
-                const float* pk = a.part + static_cast<int64_t>(cand_slot(k)) * stride;
-                m[q] = __ldcg(pk + GP * D + g);
-                l[q] = __ldcg(pk + GP * D + GP + g);
-                const float4 y0 = __ldcg(reinterpret_cast<const float4*>(pk + g * D + d));
-                const float4 y1 = __ldcg(reinterpret_cast<const float4*>(pk + g * D + d + 4));
-                x[q][0] = y0.x; x[q][1] = y0.y; x[q][2] = y0.z; x[q][3] = y0.w;
-                x[q][4] = y1.x; x[q][5] = y1.y; x[q][6] = y1.z; x[q][7] = y1.w;
+              for (int t = 0; t < NT; ++t)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sacc[h2][t][e] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < KSTEPS; ++ks) {
+              uint32_t af[4];
+              ldsm_x4(kbase + (ks >> 2) * kBoxBytes + koff[ks & 3], af);
+#pragma unroll
+              for (int t = 0; t < NT; ++t) mma_bf16(sacc[ks & 1][t], af, qb[ks][t][0], qb[ks][t][1]);
+            }
+            // full scores of heads hbase + e at keys fg (i = e) and fg + 8 (i = 2 + e)
+            float s[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              if (NT == 1) {
+                const float x = sacc[0][0][i] + sacc[1][0][i];
+                s[i] = x + __shfl_xor_sync(kFull, x, 2);
+              } else {
+                s[i] = (sacc[0][0][i] + sacc[1][0][i]) + (sacc[0][NT - 1][i] + sacc[1][NT - 1][i]);
               }
             }
+            if (!((mask >> fg) & 1u)) s[0] = s[1] = -INFINITY;
+            if (!((mask >> (fg + 8)) & 1u)) s[2] = s[3] = -INFINITY;
+
+            // ---- online softmax (base 2), per head over the 16 keys
+            float corr[2], p[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) mg.add(m[q], l[q], x[q]);
+            for (int e = 0; e < 2; ++e) {
+              float mx = fmaxf(s[e], s[2 + e]);
+              mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+              mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+              mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+              const float m_new = fmaxf(m_run[e], mx);
+              const float ms = m_new == -INFINITY ? 0.f : m_new;
+              corr[e] = exp2_fast(m_run[e] - ms);
+              p[e] = exp2_fast(s[e] - ms);
+              p[2 + e] = exp2_fast(s[2 + e] - ms);
+              l_run[e] = fmaf(l_run[e], corr[e], p[e] + p[2 + e]);
+              m_run[e] = m_new;
+            }
+            if (__any_sync(kFull, corr[0] != 1.f || corr[1] != 1.f)) {
+#pragma unroll
+              for (int mt = 0; mt < KSTEPS; ++mt)
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                  o[mt][t][0] *= corr[0];
+                  o[mt][t][1] *= corr[1];
+                  o[mt][t][2] *= corr[0];
+                  o[mt][t][3] *= corr[1];
+                }
+            }
+
+            // ---- P^T as B fragments (hi and lo bf16 parts), via 8x8 transposes
+            uint32_t pb[NT][2];
+            {
+              uint32_t h01, l01, h23, l23;
+              split_bf16x2(p[0], p[1], h01, l01);
+              split_bf16x2(p[2], p[3], h23, l23);
+              if (NT == 1) {
+                pb[0][0] = movm_t(lo_lane ? l01 : h01);
+                pb[0][1] = movm_t(lo_lane ? l23 : h23);
+              } else {
+                pb[0][0] = movm_t(h01);
+                pb[0][1] = movm_t(h23);
+                pb[NT - 1][0] = movm_t(l01);
+                pb[NT - 1][1] = movm_t(l23);
+              }
+            }
+
+            // ---- outputs O^T += V^T . P^T
+#pragma unroll
+            for (int mt = 0; mt < KSTEPS; ++mt) {
+              uint32_t af[4];
+              ldsm_x4_t(vbase + (mt >> 2) * kBoxBytes + voff[mt & 3], af);
+#pragma unroll
+              for (int t = 0; t < NT; ++t) mma_bf16(o[mt][t], af, pb[t][0], pb[t][1]);
+            }
           }
-        });
-        if (threadIdx.x == 0) a.counters[u] = 0;
+          __syncwarp();
+        }
+
+        last_stage = stg;
+        // Refill this stage with the warp's tile NS ahead. The warp's last tile
+        // of a segment keeps its stage as the merge buffer until the helper
+        // (or the CTA) has read it.
+        if (it + NS < my_n) {
+          if (g + kWarps >= ge) {
+            pend = it + NS;
+          } else if (lane == 0 && !failed) {
+            issue(it + NS);
+          }
+        }
+        ++it;
       }
+
+      // ---- this warp's state: l summed over the lanes of a head, O^T to the
+      // merge buffer as o[head][dim] (hi + lo columns). The previous
+      // segment's buffers must have been read first (ML and SLOT are reused).
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        l_run[e] += __shfl_xor_sync(kFull, l_run[e], 4);
+        l_run[e] += __shfl_xor_sync(kFull, l_run[e], 8);
+        l_run[e] += __shfl_xor_sync(kFull, l_run[e], 16);
+      }
+      if (seg > 0) {
+        if (!failed) check(mbar_wait_bounded(merge_empty, (seg - 1) & 1));
+        if (held >= 0) {
+          if (lane == 0 && !failed) issue(held);
+          held = -1;
+        }
+      }
+      held = pend;
+      if (last_stage >= 0) {
+        float* os = reinterpret_cast<float*>(wsm + last_stage * Gm::STAGE);
+        const bool writer = NT == 2 || !lo_lane;
+#pragma unroll
+        for (int mt = 0; mt < KSTEPS; ++mt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float v;
+            if (NT == 1) {
+              v = o[mt][0][i] + __shfl_xor_sync(kFull, o[mt][0][i], 2);
+            } else {
+              v = o[mt][0][i] + o[mt][NT - 1][i];
+            }
+            if (writer) os[(hbase + (i & 1)) * D + mt * 16 + fg + 8 * (i >> 1)] = v;
+          }
+        fence_proxy_async_smem();  // the buffer is refilled by TMA after the merge
+      }
+      if (fg == 0 && (NT == 2 || !lo_lane)) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          ML[warp * 2 * GP + hbase + e] = last_stage >= 0 ? m_run[e] : -INFINITY;
+          ML[warp * 2 * GP + GP + hbase + e] = last_stage >= 0 ? l_run[e] : 0.f;
+        }
+      }
+      if (lane == 0) SLOT[warp] = last_stage;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(merge_full);
     }
-    first_seg = false;
+  } else {
+    // ================= helper warp: the units' inputs, RoPE and new token one
+    // segment ahead; the end of every segment but the CTA's last
+    bool failed = false;
+    auto check = [&](bool ok) {
+      if (!failed && !__all_sync(kFull, ok)) {
+        failed = true;
+        if (lane == 0) raise_error(a.err, ERR_TIMEOUT);
+      }
+    };
+    int n_st = 0;  // units staged so far; unit k of this CTA uses input slot k & 1
+    int pos_s[2] = {0, 0};
+    uint16_t gate_s[2] = {0, 0};  // raw bf16: converting here would wait for the load
+    auto stage = [&](int u) {
+      const int b = u / Hkv, j = u - b * Hkv, sl = n_st & 1;
+      __syncwarp();  // every lane's reads of the slot come first
+      if (lane == 0) issue_stage<D, GP>(a, u, n_st, inbar, in_slots, step);
+      const int pv = a.pos[b];
+      const uint16_t gv = (a.gate && lane < a.G) ? a.gate[(static_cast<int64_t>(b) * Hkv + j) * a.G + lane] : 0;
+      if (sl == 0) {
+        pos_s[0] = pv;
+        gate_s[0] = gv;
+      } else {
+        pos_s[1] = pv;
+        gate_s[1] = gv;
+      }
+      ++n_st;
+    };
+    // rotated q of the CTA's k-th unit into qs (then PREP_FULL), its new token into its slot
+    auto prep = [&](int k) {
+      const int sl = k & 1;
+      if (!failed) check(mbar_wait_bounded(inbar + 8 * sl, (k >> 1) & 1));
+      uint8_t* slot = in_slots + sl * Gm::IN_BYTES;
+      prep_q<D, GP, 32>(a, reinterpret_cast<const uint16_t*>(slot + Gm::IN_Q), sl ? pos_s[1] : pos_s[0], step,
+                        qs, cs, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(prep_full);
+      prep_token<D, GP, 32>(a, qs, cs, slot, sl ? gate_s[1] : gate_s[0], lane);
+    };
+    if (u_first < U) {
+      stage(u_first);
+      const int u1 = next_unit(u_first);
+      if (u1 < U) stage(u1);
+      prep(0);
+    }
+    int seg = 0;
+    for (int u = u_first; u < U; ++seg) {
+      const int un = next_unit(u);
+      if (un >= U) break;  // the CTA's last segment is ended by the whole CTA
+      // the next unit's q, once every streaming warp has read this one's
+      if (!failed) check(mbar_wait_bounded(prep_empty, seg & 1));
+      prep(seg + 1);
+      // this segment's end
+      if (!failed) check(mbar_wait_bounded(merge_full, seg & 1));
+      end_segment<D, NT, PAGED, 32>(a, sp, pieces, u, seg == 0, cta, smem, ML, SLOT,
+                                    in_slots + (seg & 1) * Gm::IN_BYTES, flag, lane, wait_prev, [&] {
+                                      fence_proxy_async_smem();
+                                      __syncwarp();
+                                      if (lane == 0) mbar_arrive(merge_empty);
+                                    });
+      // its slot is free: the unit after next
+      const int unn = next_unit(un);
+      if (unn < U) stage(unn);
+      u = un;
+    }
   }
 
-  // units with no cached keys have no segments: CTA u % NC finishes them
+  // ---- the CTA's last segment, ended by all threads
+  __syncthreads();
+  if (u_last < U) {
+    const int sl = n_segs - 1;
+    end_segment<D, NT, PAGED, kThreads>(a, sp, pieces, u_last, sl == 0, cta, smem, ML, SLOT,
+                                        in_slots + (sl & 1) * Gm::IN_BYTES, flag, threadIdx.x, wait_prev, [] {});
+  }
+
+  // ---- units with no cached keys have no segments: CTA u % NC finishes them
+  int n = n_segs;
   for (int u = cta; u < U; u += NC) {
     if (P[u + 1] != P[u]) continue;
-    __syncthreads();  // the slots, qs and cs may still be read by the previous combine
-    stage(u);
-    int pos_u;
-    float gate_u;
-    const uint8_t* in_u = take(pos_u, gate_u);
-    rotate_q<D, GP>(a, reinterpret_cast<const uint16_t*>(in_u + Gm::IN_Q), pos_u, step, qs, cs);
+    __syncthreads();  // the slot, qs and cs may still be read
+    const int b = u / Hkv, j = u - b * Hkv;
+    if (threadIdx.x == 0) issue_stage<D, GP>(a, u, n, inbar, in_slots, step);
+    const int pos = a.pos[b];
+    const uint16_t gr =
+        (a.gate && threadIdx.x < a.G) ? a.gate[(static_cast<int64_t>(b) * Hkv + j) * a.G + threadIdx.x] : 0;
+    if (!mbar_wait_bounded(inbar + 8 * (n & 1), (n >> 1) & 1)) raise_error(a.err, ERR_TIMEOUT);
+    uint8_t* slot = in_slots + (n & 1) * Gm::IN_BYTES;
+    prep_q<D, GP, kThreads>(a, reinterpret_cast<const uint16_t*>(slot + Gm::IN_Q), pos, step, qs, cs, threadIdx.x);
     __syncthreads();
-    new_token<D, GP>(a, qs, cs, in_u, gate_u, kh, sn, sig);
+    prep_token<D, GP, kThreads>(a, qs, cs, slot, gr, threadIdx.x);
     wait_prev();
-    finish_unit<D, GP, PAGED>(a, u, in_u, kh, sn, sig, [](int, int, Merge8&) {});
+    finish_unit<D, GP, PAGED, kThreads>(a, u, slot, threadIdx.x, [](int, int, Merge8&) {});
+    ++n;
   }
   wait_prev();
 }
