@@ -138,4 +138,55 @@ DATTN_HD uint16_t bf16_dot2_exact(uint16_t xb, uint32_t cb, uint16_t yb, uint32_
   return static_cast<uint16_t>(sign | (biased << 7) | (q & 0x7fu));
 }
 
+// fp32 operations that the compiler may not fuse or reorder.
+#if defined(__CUDA_ARCH__)
+DATTN_HD float f32_mul(float a, float b) { return __fmul_rn(a, b); }
+DATTN_HD float f32_add(float a, float b) { return __fadd_rn(a, b); }
+DATTN_HD float f32_fma(float a, float b, float c) { return __fmaf_rn(a, b, c); }
+DATTN_HD uint32_t f32_bits(float x) { return __float_as_uint(x); }
+DATTN_HD float f32_of(uint32_t b) { return __uint_as_float(b); }
+#else
+DATTN_HD float f32_mul(float a, float b) { return a * b; }  // built without contraction
+DATTN_HD float f32_add(float a, float b) { return a + b; }
+DATTN_HD float f32_fma(float a, float b, float c) { return __builtin_fmaf(a, b, c); }
+DATTN_HD uint32_t f32_bits(float x) { uint32_t b; __builtin_memcpy(&b, &x, 4); return b; }
+DATTN_HD float f32_of(uint32_t b) { float x; __builtin_memcpy(&x, &b, 4); return x; }
+#endif
+
+// The same result as bf16_dot2_exact, mostly from fp32 arithmetic. Each product
+// is split into its fp32 rounding and the exact error of that rounding (an
+// FMA), the two roundings are added with the exact error of that sum
+// (TwoSum), and the three error terms are added on top: the fp32 value v so
+// obtained is within one unit in its last place of the exact sum, as long as
+// no term is subnormal and v is not much smaller than the products (then the
+// rounding errors of the error terms stay far below that unit). bf16 rounding
+// only changes at the midpoints between bf16 values - fp32 patterns whose low
+// 16 bits are 0x8000 - so when v is at least 3 units away from one, v and
+// the exact sum round to the same bf16 value. All other cases (near a
+// midpoint, cancellation, tiny or huge magnitudes, non-finite inputs) take
+// the integer routine.
+DATTN_HD uint16_t bf16_dot2(uint16_t xb, uint32_t cb, uint16_t yb, uint32_t sb) {
+  const float x = f32_of(static_cast<uint32_t>(xb) << 16), y = f32_of(static_cast<uint32_t>(yb) << 16);
+  const float c = f32_of(cb), s = f32_of(sb);
+  const float ph = f32_mul(x, c), qh = f32_mul(y, s);
+  const float pl = f32_fma(x, c, -ph), ql = f32_fma(y, s, -qh);
+  const float sh = f32_add(ph, qh);
+  // TwoSum: e1 = (ph + qh) - sh exactly
+  const float bv = f32_add(sh, -ph);
+  const float av = f32_add(sh, -bv);
+  const float e1 = f32_add(f32_add(ph, -av), f32_add(qh, -bv));
+  const float r = f32_add(f32_add(e1, pl), ql);
+  const float v = f32_add(sh, r);
+  const uint32_t vb = f32_bits(v);
+  const uint32_t ev = (vb >> 23) & 0xffu;
+  const uint32_t ep = (f32_bits(ph) >> 23) & 0xffu, eq = (f32_bits(qh) >> 23) & 0xffu;
+  const uint32_t em = ep > eq ? ep : eq;  // exponent of the larger product
+  const uint32_t low = vb & 0xffffu;
+  // finite, normal products in [2^-60, 2^120), v within 2^-16 of the larger
+  // one, and not within 2 units of a bf16 midpoint
+  const bool ok = em >= 67u && em < 247u && ev + 16u >= em && ev >= 27u && (low < 0x7ffdu || low > 0x8003u);
+  if (ok) return static_cast<uint16_t>((vb + 0x8000u) >> 16);
+  return bf16_dot2_exact(xb, cb, yb, sb);
+}
+
 }  // namespace dattn

@@ -181,6 +181,11 @@ __device__ __forceinline__ void pdl_trigger() {
 
 // ------------------------------------------------------------------ loads
 
+// Bring the 128-byte line holding p into L2 (no register result).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   uint4 r;
   asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"

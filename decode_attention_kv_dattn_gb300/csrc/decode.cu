@@ -72,6 +72,7 @@ constexpr int kMaxUnits = 512;           // (stream, KV head) units per call
 constexpr int kGroup = 16;               // keys per MMA group
 constexpr int kBoxBytes = kGroup * 128;  // one TMA box: 16 rows x 64 bf16
 constexpr int kWin = 32;                 // tiles per prefetch window (one per lane)
+constexpr int64_t kPrefetchLines = 1 << 15;  // largest page table (128-byte lines) put in L2 at start
 // Fixed cost of one segment of a unit in the stream-K split, in stage tiles of
 // one CTA: a segment boundary takes about as long as streaming this many
 // tiles with all warps.
@@ -294,10 +295,10 @@ __device__ __forceinline__ void prep_token(const DecodeArgs& a, const float* qs,
     uint16_t v = ksrc[e];
     if (e < half) {
       const float2 q = cs[e];  // x c - y s with x = k[e], y = k[e + half]
-      v = bf16_dot2_exact(ksrc[e], __float_as_uint(q.x), ksrc[e + half], __float_as_uint(q.y) ^ 0x80000000u);
+      v = bf16_dot2(ksrc[e], __float_as_uint(q.x), ksrc[e + half], __float_as_uint(q.y) ^ 0x80000000u);
     } else if (e < a.r) {
       const float2 q = cs[e - half];  // y c + x s with y = k[e], x = k[e - half]
-      v = bf16_dot2_exact(ksrc[e], __float_as_uint(q.x), ksrc[e - half], __float_as_uint(q.y));
+      v = bf16_dot2(ksrc[e], __float_as_uint(q.x), ksrc[e - half], __float_as_uint(q.y));
     }
     kh[e] = v;
   }
@@ -592,6 +593,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   const uint32_t merge_full = smem_addr(smem + Gm::MERGE_FULL_OFF);
   const uint32_t merge_empty = smem_addr(smem + Gm::MERGE_EMPTY_OFF);
 
+  if (threadIdx.x == 32) {
+    prefetch_tmap(&a.tmap_k);
+    prefetch_tmap(&a.tmap_v);
+  }
+  if constexpr (PAGED) {
+    // the page table into L2 (each CTA a share of its lines), for the window
+    // fills that read it once the split is known
+    const int64_t lines = (static_cast<int64_t>(a.B) * c.bt_stride + 31) / 32;
+    if (lines <= kPrefetchLines)
+      for (int64_t i = static_cast<int64_t>(cta) * kThreads + threadIdx.x; i < lines;
+           i += static_cast<int64_t>(NC) * kThreads)
+        prefetch_l2(c.block_table + i * 32);
+  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < kWarps * NS; ++i) mbar_init(stage_bars + 8 * i, 1);
     mbar_init(inbar, 1);  // the input slots
@@ -752,8 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       }
       __syncwarp();
     };
-    fill(0);
-    if (my_n > kWin) fill(1);
+    fill(0);  // window 1 is filled once the first tiles are requested
 
     const uint64_t policy = l2_evict_first_policy();
     // Request tile x of this warp into stage x % NS (one lane).
@@ -852,8 +865,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       for (;;) {
         const int g = g0 + warp + kWarps * it;
         if (it >= my_n || g >= ge) break;
-        // the window after next: its half was last read for tiles now behind
-        if (it >= kWin && (it & (kWin - 1)) == 0 && it + kWin < my_n) fill(it / kWin + 1);
+        // the next window: its half was last read for tiles now behind
+        if ((it & (kWin - 1)) == 0 && it + kWin < my_n) fill(it / kWin + 1);
         // the previous segment's merge buffer streams again once the helper has read it
         if (held >= 0) {
           bool ready;

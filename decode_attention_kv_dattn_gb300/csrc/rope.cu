@@ -9,8 +9,9 @@
 // for the new token): c and s are the fp32 cosine and sine that rope_cos_sin
 // derives from the pair's fixed-point phase step (an exact phase, then an fp32
 // polynomial); the entry is the bf16 nearest to the exact x*c - y*s (ties to
-// even), computed in integer arithmetic (bf16_dot2_exact). q is rotated in fp32 and pre-scaled by
-// log2(e)/sqrt(D) so that the split kernel's scores are in base-2 units.
+// even), from fp32 error terms or, near a bf16 midpoint, in integers
+// (bf16_dot2). q is rotated in fp32 and pre-scaled by log2(e)/sqrt(D) so that
+// the split kernel's scores are in base-2 units.
 #include "bf16_exact.h"
 #include "common.cuh"
 
@@ -113,8 +114,8 @@ __global__ void __launch_bounds__(kRowThreads) rope_kernel(const RopeArgs a) {
       if (p < half) {
         const uint32_t cb = __float_as_uint(cs_c[p]), sb = __float_as_uint(cs_s[p]);
         const uint16_t xh = static_cast<uint16_t>(xy[k] & 0xffffu), yh = static_cast<uint16_t>(xy[k] >> 16);
-        dst[d0] = bf16_dot2_exact(xh, cb, yh, sb ^ 0x80000000u);  // x c - y s
-        dst[d1] = bf16_dot2_exact(yh, cb, xh, sb);                // y c + x s
+        dst[d0] = bf16_dot2(xh, cb, yh, sb ^ 0x80000000u);  // x c - y s
+        dst[d1] = bf16_dot2(yh, cb, xh, sb);                // y c + x s
       } else {
         dst[d0] = static_cast<uint16_t>(xy[k] & 0xffffu);
         dst[d1] = static_cast<uint16_t>(xy[k] >> 16);
@@ -187,8 +188,8 @@ __global__ void __launch_bounds__(kRopeThreads) append_kernel(const AppendArgs a
       const uint32_t cb = __float_as_uint(cf), sb = __float_as_uint(sf);
       for (int h = 0; h < a.Hkv; ++h) {
         const uint16_t x = a.k[src0 + h * a.D + i], y = a.k[src0 + h * a.D + i + half];
-        c.k[dst0 + h * head_stride + i] = bf16_dot2_exact(x, cb, y, sb ^ 0x80000000u);
-        c.k[dst0 + h * head_stride + i + half] = bf16_dot2_exact(y, cb, x, sb);
+        c.k[dst0 + h * head_stride + i] = bf16_dot2(x, cb, y, sb ^ 0x80000000u);
+        c.k[dst0 + h * head_stride + i + half] = bf16_dot2(y, cb, x, sb);
       }
     } else {
       const int d = a.r + (job - half);
