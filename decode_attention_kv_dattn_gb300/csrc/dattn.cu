@@ -402,7 +402,6 @@ int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, const dattn_ve
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   VerifySplitArgs va{};
   va.c = make_view(h, L, cache);
-  if (encode_cache_maps(va.c, h->Hkv, h->D, &va.tmap_k, &va.tmap_v) != cudaSuccess) return DATTN_EUNSUPPORTED;
 
   RopeArgs ra{};
   ra.rows = S * T;

@@ -111,8 +111,6 @@ struct AppendArgs {
 // over (stream, KV head) units, the G*T rows of a unit in one 128-row MMA).
 // Partial slot layout: [ctas + S*Hkv][G*T rows][D + 4] fp32 (o[D], m, l, pad).
 struct VerifySplitArgs {
-  CUtensorMap tmap_k;          // the layer's K and V caches as 2D [rows, D] bf16
-  CUtensorMap tmap_v;          // tensors (encode_cache_maps)
   CacheView c;                 // paged, page size a multiple of 16; seq_len = prefix lengths
   int S, T, Hkv, G;
   int ctas;

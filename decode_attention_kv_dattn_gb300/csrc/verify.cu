@@ -10,12 +10,15 @@
 //    unit is one 128-row MMA tile (G*T <= 128): S = Q K^T into tensor memory
 //    (TMEM), an online softmax by four warps (thread t owns row t), then
 //    O += P V accumulated in TMEM. Work is split stream-K over all units'
-//    32-key tiles (one CTA per SM); four K/V stages let the TMA warp run up to
-//    three tiles ahead.
+//    32-key tiles (one CTA per SM).
 //    Operands are fp16: a TMA warp brings the bf16 K/V rows of each 16-key
-//    group as 2D boxes in the 128-byte-swizzled layout the MMA reads, and
-//    eight producer warps convert them to fp16 in place (exact for |x| < 65504);
-//    q and P are rounded to fp16. (fp16 keeps the
+//    group (contiguous within a page) by one bulk copy each into one of three
+//    row-major bf16 stages, and eight producer warps convert each tile into
+//    one of three fp16 operand buffers in the 128-byte-swizzled layout the
+//    MMAs read (exact for |x| < 65504).
+//    A stage is refilled as soon as it is converted, so the copies in flight
+//    do not wait for the tile's MMAs; an operand buffer is held from its
+//    conversion until its PV completes. q and P are rounded to fp16. (fp16 keeps the
 //    error of q and P rounding under the tolerance at every prefix length;
 //    bf16 operands do not at short prefixes.) The accumulator is rescaled
 //    lazily: only when a row's maximum grows by more than 2^8.
@@ -34,7 +37,8 @@ namespace {
 
 constexpr int VM = 128;              // MMA rows (G*T <= VM)
 constexpr int VNK = kVerifyTileKeys; // keys per tile
-constexpr int NST = 5;               // K/V stages (TMA runs up to four tiles ahead)
+constexpr int NST = 3;               // bf16 K/V stages the TMA fills (released once converted)
+constexpr int NWB = 3;               // fp16 operand buffers (released once their PV completes)
 constexpr int kWin = 32;             // tiles whose page rows the TMA warp resolves at once
 constexpr int kSoftWarps = 4;        // softmax warps: TMEM lane quarters 0..3
 constexpr int kProdWarps = 8;        // producer warps
@@ -45,15 +49,16 @@ constexpr int kVThreads = (kPvWarp + 1) * 32;
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold
 
 // barrier indices
-// (B_FULL, B_EMPTY, B_LOAD: one per stage; B_SFULL, B_SFREE: one per score
-// buffer; B_PFULL, B_PVDONE: one per probability buffer)
+// (B_LOAD, B_EMPTY: one per bf16 stage; B_FULL, B_WFREE: one per fp16 operand
+// buffer; B_SFULL: one per score buffer; B_PFULL, B_PVDONE: one per
+// probability buffer)
 enum {
-  B_FULL = 0,
-  B_EMPTY = B_FULL + NST,
-  B_LOAD = B_EMPTY + NST,
-  B_SFULL = B_LOAD + NST,
-  B_SFREE = B_SFULL + 2,
-  B_PFULL = B_SFREE + 2,
+  B_LOAD = 0,
+  B_EMPTY = B_LOAD + NST,
+  B_FULL = B_EMPTY + NST,
+  B_WFREE = B_FULL + NWB,
+  B_SFULL = B_WFREE + NWB,
+  B_PFULL = B_SFULL + 2,
   B_PVDONE = B_PFULL + 2,
   B_QREADY = B_PVDONE + 2,
   B_OFREE = B_QREADY + 1,
@@ -69,17 +74,23 @@ struct VGeo {
   static constexpr int NREG = D / 64;                 // 64-dim (128-byte) regions per row
   static constexpr int KT_REG = VNK * 128;            // bytes of one K (or V) region
   static constexpr int KT_BYTES = NREG * KT_REG;
-  static constexpr int ST_OFF = 0;
+  static constexpr int ST_OFF = 0;                    // NST bf16 stages as the TMA wrote them
   static constexpr int ST_BYTES = 2 * KT_BYTES;       // K then V
-  static constexpr int P_OFF = ST_OFF + NST * ST_BYTES;
-  static constexpr int BAR_OFF = P_OFF + 2 * VM * 128;  // two P buffers
+  static constexpr int WB_OFF = ST_OFF + NST * ST_BYTES;  // NWB fp16 operand buffers, same layout
+  static constexpr int BAR_OFF = WB_OFF + NWB * ST_BYTES;
   static constexpr int NBAR = B_COUNT;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8; // tmem slot, abort flag
   static constexpr int TAB_OFF = MISC_OFF + 16;
   static constexpr int SMEM = TAB_OFF + (2 * kVerifyMaxUnits + 1) * 4 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t S_COL = 0;                // two VNK-column score buffers
-  static constexpr uint32_t Q_COL = 64;               // q rows as the MMA's A: D/2 columns of fp16 pairs
+  // Two score buffers, each SCH accumulators of VNK columns: Q K^T runs as SCH
+  // independent chains over the k-steps (a single chain of 16 small MMAs
+  // waits on itself), summed when the scores are read. P of the tile is then
+  // written over the buffer's first VNK/2 columns, the A operand of P V.
+  static constexpr int SCH = 2;
+  static constexpr uint32_t S_COL = 0;
+  static constexpr uint32_t S_BUF = SCH * VNK;        // columns per score buffer
+  static constexpr uint32_t Q_COL = 2 * S_BUF;        // q rows as the MMA's A: D/2 columns of fp16 pairs
   static constexpr uint32_t O_COL = 256;              // D columns of output
   static_assert(D == 128 || D == 256, "head_dim");
 };
@@ -114,11 +125,6 @@ __device__ __forceinline__ uint32_t cvt_pair_f16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// bf16 pair -> fp16 pair (exact below 65504 in magnitude); flags overflow.
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, uint32_t& ovf) {
-  ovf |= ((w & 0x7fffu) >= 0x4780u) | (((w >> 16) & 0x7fffu) >= 0x4780u);
-  return cvt_pair_f16(bf16_lo(w), bf16_hi(w));
-}
 
 template <int D>
 __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid_constant__ VerifySplitArgs a) {
@@ -152,12 +158,14 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
     *abort_flag = 0;
     for (int b = 0; b < NST; ++b) {
       mbar_init(sbase + V::BAR_OFF + 8 * (B_LOAD + b), 1);
+      mbar_init(sbase + V::BAR_OFF + 8 * (B_EMPTY + b), kProdWarps);
+    }
+    for (int b = 0; b < NWB; ++b) {
       mbar_init(sbase + V::BAR_OFF + 8 * (B_FULL + b), kProdWarps);
-      mbar_init(sbase + V::BAR_OFF + 8 * (B_EMPTY + b), 1);
+      mbar_init(sbase + V::BAR_OFF + 8 * (B_WFREE + b), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(sbase + V::BAR_OFF + 8 * (B_SFULL + b), 1);
-      mbar_init(sbase + V::BAR_OFF + 8 * (B_SFREE + b), kSoftWarps);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(sbase + V::BAR_OFF + 8 * (B_PFULL + b), kSoftWarps);
@@ -185,10 +193,10 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
   const Waiter W{sbase + V::BAR_OFF, abort_flag, a.err};
 
   if (ntiles > 0 && warp == kTmaWarp) {
-    // ================= TMA: bf16 K/V page rows into the stage, swizzled =================
-    // Each 16-key group of a tile is one box of 16 rows x 64 dims per 64-dim
-    // region of K and of V (a page holds whole groups: its size is a multiple
-    // of 16); the 128-byte swizzle is the layout the MMAs read. Groups past the
+    // ================= TMA: bf16 K/V page rows into the stage =================
+    // Each 16-key group of a tile is 16 consecutive rows of one page (its size
+    // is a multiple of 16): one contiguous bulk copy each for K and V, stored
+    // row-major; the producers lay them out for the MMAs. Groups past the
     // prefix are not loaded; the producers zero their rows.
     // Lane x % 32 reads the page ids of tile x one 32-tile window ahead, so
     // that no page-table load sits between two tiles' copies; lane 0 issues.
@@ -244,59 +252,84 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
         rows[gr] = pg * Hkv * c.P + off;
       }
       if (lane == 0) {
+        // one bulk copy per 16-key group of K and of V: 16 consecutive rows of
+        // a page (8 KB at D = 256), row-major into the stage
         const uint32_t bar = sbase + V::BAR_OFF + 8 * (B_LOAD + st);
         const uint32_t stage = sbase + V::ST_OFF + st * V::ST_BYTES;
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(ngroups) * 2u * V::NREG * 2048u);
+        constexpr uint32_t GB = 16u * D * 2u;  // bytes of one group
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(ngroups) * 2u * GB);
 #pragma unroll
         for (int gr = 0; gr < NG; ++gr) {
           if (gr < ngroups) {
-#pragma unroll
-            for (int rg = 0; rg < V::NREG; ++rg) {
-              tma_load_2d(stage + rg * V::KT_REG + gr * 2048, &a.tmap_k, 64 * rg, rows[gr], bar, policy);
-              tma_load_2d(stage + V::KT_BYTES + rg * V::KT_REG + gr * 2048, &a.tmap_v, 64 * rg, rows[gr], bar,
-                          policy);
-            }
+            const int64_t e0 = static_cast<int64_t>(rows[gr]) * D;
+            bulk_copy_g2s(stage + gr * GB, c.k + e0, GB, bar, policy);
+            bulk_copy_g2s(stage + V::KT_BYTES + gr * GB, c.v + e0, GB, bar, policy);
           }
         }
       }
       __syncwarp();
     }
   } else if (ntiles > 0 && warp >= kSoftWarps && warp < kMmaWarp) {
-    // ================= producers: the staged bf16 rows -> fp16, in place =================
+    // ================= producers: a staged bf16 tile -> fp16 operand buffer k % NWB =================
+    // (row-major bf16 in, the MMAs' 128-byte-swizzled fp16 layout out)
+    // The stage goes back to the TMA as soon as it is read; the operand buffer
+    // is free again once the PV NWB tiles back has completed.
     const int pt = threadIdx.x - kSoftWarps * 32;         // 0 .. 255
     constexpr int CPR = D / 8;                            // 16-byte chunks per row
     constexpr int NCH = 2 * VNK * CPR;                    // chunks of a stage (K and V)
-    uint32_t ovf = 0;
+    constexpr int PER = NCH / (kProdWarps * 32);          // chunks per thread
+    static_assert(NCH % (kProdWarps * 32) == 0, "whole chunks per thread");
+    // this thread's chunks (the same positions in every tile): byte offset in
+    // the row-major stage, in the swizzled operand buffer, and key row
+    int soff[PER], coff[PER], crow[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = pt + i * kProdWarps * 32;
+      const int which = e / (VNK * CPR);
+      const int rem = e - which * (VNK * CPR);
+      const int r = rem / CPR, ch = rem - r * CPR;
+      soff[i] = which * V::KT_BYTES + r * (D * 2) + ch * 16;
+      coff[i] = which * V::KT_BYTES + (ch >> 3) * V::KT_REG + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+      crow[i] = r;
+    }
+    uint32_t mag = 0;  // largest |x| seen, per 16-bit half (bf16 bit patterns)
     int u = unit_of(Pt, U, g0);
     for (int k = 0; k < ntiles; ++k) {
-      const int st = k % NST;
+      const int st = k % NST, wb = k % NWB;
       if (!__all_sync(0xffffffffu, W.wait(B_LOAD + st, (k / NST) & 1))) break;
+      if (k >= NWB && !__all_sync(0xffffffffu, W.wait(B_WFREE + wb, (k / NWB - 1) & 1))) break;
       const int g = g0 + k;
       while (Pt[u + 1] <= g) ++u;
       const int nvalid = min(VNK, Nn[u] - (g - Pt[u]) * VNK);
-      uint8_t* stage = smem + V::ST_OFF + st * V::ST_BYTES;
+      const uint8_t* stage = smem + V::ST_OFF + st * V::ST_BYTES;
+      uint8_t* obuf = smem + V::WB_OFF + wb * V::ST_BYTES;
+      // all loads first, then the conversions and stores (rows past the prefix become zeros)
+      uint4 w[PER];
 #pragma unroll
-      for (int e = pt; e < NCH; e += kProdWarps * 32) {
-        const int which = e / (VNK * CPR);
-        const int rem = e - which * (VNK * CPR);
-        const int r = rem / CPR, ch = rem - r * CPR;
-        uint4* p = reinterpret_cast<uint4*>(stage + which * V::KT_BYTES + (ch >> 3) * V::KT_REG + r * 128 +
-                                            (((ch & 7) ^ (r & 7)) << 4));
-        uint4 h = make_uint4(0u, 0u, 0u, 0u);
-        if (r < nvalid) {
-          const uint4 w = *p;
-          h.x = bf16x2_to_f16x2(w.x, ovf);
-          h.y = bf16x2_to_f16x2(w.y, ovf);
-          h.z = bf16x2_to_f16x2(w.z, ovf);
-          h.w = bf16x2_to_f16x2(w.w, ovf);
-        }
-        *p = h;
+      for (int i = 0; i < PER; ++i)
+        w[i] = crow[i] < nvalid ? *reinterpret_cast<const uint4*>(stage + soff[i]) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        mag = __vmaxu2(mag, w[i].x & 0x7fff7fffu);
+        mag = __vmaxu2(mag, w[i].y & 0x7fff7fffu);
+        mag = __vmaxu2(mag, w[i].z & 0x7fff7fffu);
+        mag = __vmaxu2(mag, w[i].w & 0x7fff7fffu);
+        const uint4 h = make_uint4(cvt_pair_f16(bf16_lo(w[i].x), bf16_hi(w[i].x)),
+                                   cvt_pair_f16(bf16_lo(w[i].y), bf16_hi(w[i].y)),
+                                   cvt_pair_f16(bf16_lo(w[i].z), bf16_hi(w[i].z)),
+                                   cvt_pair_f16(bf16_lo(w[i].w), bf16_hi(w[i].w)));
+        *reinterpret_cast<uint4*>(obuf + coff[i]) = h;
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(sbase + V::BAR_OFF + 8 * (B_FULL + st));
+      if (lane == 0) {
+        mbar_arrive(sbase + V::BAR_OFF + 8 * (B_FULL + wb));
+        mbar_arrive(sbase + V::BAR_OFF + 8 * (B_EMPTY + st));
+      }
     }
-    if (__any_sync(0xffffffffu, ovf != 0) && lane == 0) raise_error(a.err, ERR_RANGE);
+    // fp16 holds bf16 values below 65504 in magnitude exactly (bf16 0x4780 = 65536)
+    const bool ovf = (mag & 0xffffu) >= 0x4780u || (mag >> 16) >= 0x4780u;
+    if (__any_sync(0xffffffffu, ovf) && lane == 0) raise_error(a.err, ERR_RANGE);
   } else if (ntiles > 0 && warp == kMmaWarp) {
     // ================= Q K^T issue (one thread) =================
     if (lane == 0) {
@@ -310,15 +343,17 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
           ++seg;
           prev_u = u;
         }
-        const int st = k % NST, sb = k & 1;
-        if (!W.wait(B_FULL + st, (k / NST) & 1)) break;
-        if (k >= 2 && !W.wait(B_SFREE + sb, ((k >> 1) - 1) & 1)) break;
+        const int sb = k & 1, wb = k % NWB;
+        if (!W.wait(B_FULL + wb, (k / NWB) & 1)) break;
+        // the score buffer (and the P in it) is free once PV two tiles back has completed
+        if (k >= 2 && !W.wait(B_PVDONE + sb, ((k >> 1) - 1) & 1)) break;
         tc::fence_after();
-        const uint32_t kbase = sbase + V::ST_OFF + st * V::ST_BYTES;
+        const uint32_t kbase = sbase + V::WB_OFF + wb * V::ST_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t db = tc::sw128_desc(kbase + (kk >> 2) * V::KT_REG + (kk & 3) * 32, 16, 1024);
-          tc::mma_ts(tmem + V::S_COL + sb * VNK, tmem + V::Q_COL + kk * 8, db, idesc_qk, kk > 0);
+          tc::mma_ts(tmem + V::S_COL + sb * V::S_BUF + (kk % V::SCH) * VNK, tmem + V::Q_COL + kk * 8, db, idesc_qk,
+                     kk >= V::SCH);
         }
         tc::commit(sbase + V::BAR_OFF + 8 * (B_SFULL + sb));
       }
@@ -327,7 +362,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
   } else if (ntiles > 0 && warp == kPvWarp) {
     // ================= P V issue (one thread) =================
     // PV(k) follows QK(k): its P was made from the scores QK(k) wrote. The
-    // stage's K and V are free once PV(k) completes.
+    // operand buffer's K and V are free once PV(k) completes.
     if (lane == 0) {
       constexpr uint32_t idesc_pv = tc::f16_idesc(VM, D, 0, true);
       int u = unit_of(Pt, U, g0), prev_u = -1, seg = 0;
@@ -339,16 +374,15 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
         if (!W.wait(B_PFULL + (k & 1), (k >> 1) & 1)) break;
         if (seg_start && seg > 0 && !W.wait(B_OFREE, (seg - 1) & 1)) break;
         tc::fence_after();
-        const int st = k % NST;
-        const uint32_t vbase = sbase + V::ST_OFF + st * V::ST_BYTES + V::KT_BYTES;
+        const uint32_t vbase = sbase + V::WB_OFF + (k % NWB) * V::ST_BYTES + V::KT_BYTES;
 #pragma unroll
         for (int kk = 0; kk < VNK / 16; ++kk) {
-          const uint64_t da = tc::sw128_desc(sbase + V::P_OFF + (k & 1) * VM * 128 + kk * 32, 16, 1024);
           const uint64_t db = tc::sw128_desc(vbase + kk * 2048, V::KT_REG, 1024);
-          tc::mma(tmem + V::O_COL, da, db, idesc_pv, !seg_start || kk > 0);
+          tc::mma_ts(tmem + V::O_COL, tmem + V::S_COL + (k & 1) * V::S_BUF + kk * 8, db, idesc_pv,
+                     !seg_start || kk > 0);
         }
         tc::commit(sbase + V::BAR_OFF + 8 * (B_PVDONE + (k & 1)));
-        tc::commit(sbase + V::BAR_OFF + 8 * (B_EMPTY + st));
+        tc::commit(sbase + V::BAR_OFF + 8 * (B_WFREE + k % NWB));
         if (seg_end) ++seg;
         prev_u = u;
       }
@@ -359,7 +393,6 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
     pdl_wait();  // q rotated by the prologue
     const int t = threadIdx.x;
     const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
-    uint8_t* Pb = smem + V::P_OFF;
     int u = unit_of(Pt, U, g0), prev_u = -1, seg = 0;
     float m_ref = -INFINITY, l = 0.f;
     for (int k = 0; k < ntiles; ++k) {
@@ -399,11 +432,15 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
       if (!__all_sync(0xffffffffu, W.wait(B_SFULL + sb, (k >> 1) & 1))) break;
       tc::fence_after();
       uint32_t sr[VNK];
-      tc::ld32(tmem + lane_off + V::S_COL + sb * VNK, sr);
-      tc::wait_ld();
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sbase + V::BAR_OFF + 8 * (B_SFREE + sb));
+      {
+        static_assert(V::SCH == 2 && VNK == 32, "two 32-column score accumulators");
+        uint32_t s2[VNK];
+        tc::ld32(tmem + lane_off + V::S_COL + sb * V::S_BUF, sr);
+        tc::ld32(tmem + lane_off + V::S_COL + sb * V::S_BUF + VNK, s2);
+        tc::wait_ld();
+#pragma unroll
+        for (int x = 0; x < VNK; ++x) sr[x] = __float_as_uint(__uint_as_float(sr[x]) + __uint_as_float(s2[x]));
+      }
       const int nvalid = min(VNK, Nn[u] - (g - Pt[u]) * VNK);
       float tmax = -INFINITY;
 #pragma unroll
@@ -412,7 +449,6 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
         sr[x] = __float_as_uint(sx);
         tmax = fmaxf(tmax, sx);
       }
-      bool pv_waited = false;
       if (m_ref == -INFINITY) {
         m_ref = tmax;
       } else {
@@ -420,7 +456,6 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
         if (__any_sync(0xffffffffu, need)) {
           // rescale this warp's rows of O once the last PV has landed
           if (!__all_sync(0xffffffffu, W.wait(B_PVDONE + ((k - 1) & 1), ((k - 1) >> 1) & 1))) break;
-          pv_waited = true;
           tc::fence_after();
           const float f = need ? exp2_fast(m_ref - tmax) : 1.f;
 #pragma unroll 1
@@ -451,15 +486,11 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
         ph[x] = *reinterpret_cast<const uint32_t*>(&h);
       }
       l += lsum;
-      // this tile's P buffer is free once the PV two tiles back has completed
-      // (PVs complete in order: a wait for the previous one covers it)
-      if (k >= 2 && !pv_waited && !__all_sync(0xffffffffu, W.wait(B_PVDONE + (k & 1), ((k >> 1) - 1) & 1))) break;
-      uint8_t* Pk = Pb + (k & 1) * VM * 128;
-#pragma unroll
-      for (int x = 0; x < VNK / 8; ++x)
-        *reinterpret_cast<uint4*>(Pk + t * 128 + ((x ^ (t & 7)) << 4)) =
-            make_uint4(ph[4 * x], ph[4 * x + 1], ph[4 * x + 2], ph[4 * x + 3]);
-      fence_proxy_async_smem();
+      // row t of P (fp16 pairs) over this tile's scores, where PV reads its A
+      // operand (the scores were read above; the PV two tiles back that read
+      // this buffer's P completed before QK(k) was issued)
+      tc::st16(tmem + lane_off + V::S_COL + sb * V::S_BUF, ph);
+      tc::wait_st();
       tc::fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(sbase + V::BAR_OFF + 8 * (B_PFULL + (k & 1)));
