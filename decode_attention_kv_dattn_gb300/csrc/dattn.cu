@@ -234,7 +234,7 @@ int dattn_create(const dattn_config* cfg, int device, dattn_t** out) {
     if (cudaMalloc(&h->counters[i], nc * sizeof(int)) != cudaSuccess) return fail(DATTN_ECUDA);
     if (cudaMemset(h->counters[i], 0, nc * sizeof(int)) != cudaSuccess) return fail(DATTN_ECUDA);
   }
-  if (cudaMalloc(&h->tiles, (static_cast<size_t>(h->max_streams) * Hkv + 1) * sizeof(int)) != cudaSuccess)
+  if (cudaMalloc(&h->tiles, (4 * static_cast<size_t>(h->max_streams) * Hkv + 1) * sizeof(int)) != cudaSuccess)
     return fail(DATTN_ECUDA);
   const size_t part_floats = h->part_units * h->GP * (D + 2);
   for (int i = 0; i < 2; ++i)

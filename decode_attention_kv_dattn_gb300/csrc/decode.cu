@@ -190,51 +190,6 @@ __device__ __forceinline__ uint32_t row_bits(int lo, int hi) {
   return ((1u << (hi - lo)) - 1u) << lo;
 }
 
-// The stream-K split runs over weighted positions: unit u starts at
-// P[u] + C u, its first C positions stand for the fixed cost of one segment of
-// it (staging its inputs, RoPE, the new token, the merge and the output), and
-// its tiles follow one position each. CTA c takes the positions
-// [c W / NC, (c + 1) W / NC) of the W = T + C U in all, so a CTA whose range
-// crosses many short units gets fewer tiles.
-struct Split {
-  const int* P;  // [U + 1] tile prefix over units
-  int U, C, NC;
-  int64_t W;
-  __device__ __forceinline__ int64_t bound(int c) const { return static_cast<int64_t>(c) * W / NC; }
-  // first tile at or after weighted position t (T past the end)
-  __device__ int tile_at(int64_t t) const {
-    if (t >= W) return P[U];
-    int lo = 0, hi = U - 1;  // the last unit starting at or before t
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (P[mid] + static_cast<int64_t>(C) * mid <= t) lo = mid; else hi = mid - 1;
-    }
-    const int64_t off = t - (P[lo] + static_cast<int64_t>(C) * lo) - C;
-    return P[lo] + (off > 0 ? static_cast<int>(off) : 0);
-  }
-  // CTA whose range holds tile x of unit u
-  __device__ __forceinline__ int cta_of(int x, int u) const {
-    const int64_t w = x + static_cast<int64_t>(C) * (u + 1);
-    return static_cast<int>(((w + 1) * NC - 1) / W);
-  }
-  __device__ __forceinline__ bool has_tiles_inside(int c) const { return bound(c) < bound(c + 1); }
-};
-
-// Number of CTAs whose ranges hold tiles of unit u (global tiles [p0, p1)),
-// the first of them, the last, and the partial slot of the first one's
-// segment (that CTA's own slot when the unit starts its range).
-__device__ __forceinline__ int unit_segments(const Split& sp, int p0, int p1, int u, int& c_lo, int& c_hi,
-                                             int& first_slot) {
-  if (p1 <= p0) return 0;
-  c_lo = sp.cta_of(p0, u);
-  c_hi = sp.cta_of(p1 - 1, u);
-  first_slot = sp.tile_at(sp.bound(c_lo)) == p0 ? c_lo : sp.NC + u;
-  int n = 1;
-  // a CTA strictly inside the unit's span holds its tiles iff its range is not empty
-  for (int cc = c_lo + 1; cc <= c_hi; ++cc) n += sp.has_tiles_inside(cc);
-  return n;
-}
-
 // Work on one unit's inputs and outputs is done by a team: the helper warp
 // (NTH = 32, t = lane) for segment ends in the middle of a CTA's range, or the
 // whole CTA (NTH = kThreads, t = threadIdx.x) for its last one.

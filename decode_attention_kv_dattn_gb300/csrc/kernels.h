@@ -117,7 +117,9 @@ struct VerifySplitArgs {
   int max_len;
   const float* qhat;           // [S*T, Hq, D] pre-scaled, from the RoPE prologue
   float* part;
-  int* tiles;                  // [S*Hkv + 1] out
+  int* tiles;                  // out, U = S*Hkv: [U + 1] tile prefix over units, then per
+                               // unit the first CTA of its span [U], the span's length [U]
+                               // and the partial slot of its first segment [U]
   int* err;
 };
 
@@ -127,7 +129,7 @@ struct VerifyCombineArgs {
   CacheView c;
   int S, T, Hkv, G;
   int split_ctas;
-  const int* tiles;
+  const int* tiles;            // written by the split pass (VerifySplitArgs::tiles)
   int max_len;
   const float* qhat;           // [S*T, Hq, D]
   const uint16_t* khat;        // [S*T, Hkv, D] rotated window keys (bf16 entries)
@@ -152,6 +154,8 @@ cudaError_t launch_verify_split(const VerifySplitArgs& a, int D, cudaStream_t s)
 cudaError_t launch_verify_combine(const VerifyCombineArgs& a, int D, cudaStream_t s);
 // Keys per tile of the verify pass and its largest unit count.
 constexpr int kVerifyTileKeys = 32;
+// Fixed cost of one unit segment of the verify pass's split, in tiles.
+constexpr int kVerifySegmentCost = 8;
 constexpr int kVerifyMaxUnits = 512;
 
 // Resident CTAs per SM of the decode kernel for (D, G) (0 if unsupported).

@@ -39,6 +39,7 @@ constexpr int VM = 128;              // MMA rows (G*T <= VM)
 constexpr int VNK = kVerifyTileKeys; // keys per tile
 constexpr int NST = 3;               // bf16 K/V stages the TMA fills (released once converted)
 constexpr int NWB = 3;               // fp16 operand buffers (released once their PV completes)
+constexpr int NSB = 4;               // score buffers in tensor memory (each later holds its tile's P)
 constexpr int kWin = 32;             // tiles whose page rows the TMA warp resolves at once
 constexpr int kSoftWarps = 4;        // softmax warps: TMEM lane quarters 0..3
 constexpr int kProdWarps = 8;        // producer warps
@@ -50,7 +51,8 @@ constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold
 
 // barrier indices
 // (B_LOAD, B_EMPTY: one per bf16 stage; B_FULL, B_WFREE: one per fp16 operand
-// buffer; B_SFULL: one per score buffer; B_PFULL, B_PVDONE: one per
+// buffer; B_SFULL, B_PFULL, B_SDONE: one per score buffer (its scores are in,
+// its P is in, its PV has completed); B_PVDONE: PV(k) completed, by k & 1; one per
 // probability buffer)
 enum {
   B_LOAD = 0,
@@ -58,8 +60,9 @@ enum {
   B_FULL = B_EMPTY + NST,
   B_WFREE = B_FULL + NWB,
   B_SFULL = B_WFREE + NWB,
-  B_PFULL = B_SFULL + 2,
-  B_PVDONE = B_PFULL + 2,
+  B_PFULL = B_SFULL + NSB,
+  B_SDONE = B_PFULL + NSB,
+  B_PVDONE = B_SDONE + NSB,
   B_QREADY = B_PVDONE + 2,
   B_OFREE = B_QREADY + 1,
   B_COUNT = B_OFREE + 1
@@ -83,14 +86,11 @@ struct VGeo {
   static constexpr int TAB_OFF = MISC_OFF + 16;
   static constexpr int SMEM = TAB_OFF + (2 * kVerifyMaxUnits + 1) * 4 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
-  // Two score buffers, each SCH accumulators of VNK columns: Q K^T runs as SCH
-  // independent chains over the k-steps (a single chain of 16 small MMAs
-  // waits on itself), summed when the scores are read. P of the tile is then
-  // written over the buffer's first VNK/2 columns, the A operand of P V.
-  static constexpr int SCH = 2;
+  // NSB score buffers of VNK columns; P of a tile is written over its scores
+  // once they are read (the buffer's first VNK/2 columns, the A operand of P V)
   static constexpr uint32_t S_COL = 0;
-  static constexpr uint32_t S_BUF = SCH * VNK;        // columns per score buffer
-  static constexpr uint32_t Q_COL = 2 * S_BUF;        // q rows as the MMA's A: D/2 columns of fp16 pairs
+  static constexpr uint32_t S_BUF = VNK;              // columns per score buffer
+  static constexpr uint32_t Q_COL = NSB * S_BUF;      // q rows as the MMA's A: D/2 columns of fp16 pairs
   static constexpr uint32_t O_COL = 256;              // D columns of output
   static_assert(D == 128 || D == 256, "head_dim");
 };
@@ -164,13 +164,12 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
       mbar_init(sbase + V::BAR_OFF + 8 * (B_FULL + b), kProdWarps);
       mbar_init(sbase + V::BAR_OFF + 8 * (B_WFREE + b), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NSB; ++b) {
       mbar_init(sbase + V::BAR_OFF + 8 * (B_SFULL + b), 1);
-    }
-    for (int b = 0; b < 2; ++b) {
       mbar_init(sbase + V::BAR_OFF + 8 * (B_PFULL + b), kSoftWarps);
-      mbar_init(sbase + V::BAR_OFF + 8 * (B_PVDONE + b), 1);
+      mbar_init(sbase + V::BAR_OFF + 8 * (B_SDONE + b), 1);
     }
+    for (int b = 0; b < 2; ++b) mbar_init(sbase + V::BAR_OFF + 8 * (B_PVDONE + b), 1);
     mbar_init(sbase + V::BAR_OFF + 8 * B_QREADY, kSoftWarps);
     mbar_init(sbase + V::BAR_OFF + 8 * B_OFREE, kSoftWarps);
     fence_mbar_init();
@@ -178,10 +177,24 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
   __syncthreads();
   block_scan_inclusive<kVThreads>(Pt + 1, U);
   const int Ttot = Pt[U];
-  const int g0 = static_cast<int>(static_cast<int64_t>(cta) * Ttot / NC);
-  const int g1 = static_cast<int>(static_cast<int64_t>(cta + 1) * Ttot / NC);
-  if (cta == 0)
+  // stream-K over the units' tiles, each unit weighted with the fixed cost of
+  // one segment of it (at a segment end the whole tile pipeline drains, the
+  // partial output leaves tensor memory and the next unit's q comes in)
+  const Split sp{Pt, U, kVerifySegmentCost, NC, Ttot + static_cast<int64_t>(kVerifySegmentCost) * U};
+  const int g0 = sp.tile_at(sp.bound(cta));
+  const int g1 = sp.tile_at(sp.bound(cta + 1));
+  if (cta == 0) {
+    // for the combine: the tile prefix, then per unit the first CTA of its
+    // span, the span's length and the partial slot of its first segment
     for (int u = threadIdx.x; u <= U; u += kVThreads) a.tiles[u] = Pt[u];
+    for (int u = threadIdx.x; u < U; u += kVThreads) {
+      int c_lo = 0, c_hi = -1, first_slot = 0;
+      unit_segments(sp, Pt[u], Pt[u + 1], u, c_lo, c_hi, first_slot);
+      a.tiles[U + 1 + u] = c_lo;
+      a.tiles[2 * U + 1 + u] = c_hi - c_lo + 1;
+      a.tiles[3 * U + 1 + u] = first_slot;
+    }
+  }
   if (warp == kMmaWarp) tc::alloc(sbase + V::MISC_OFF, V::TMEM_COLS);
   tc::fence_before();
   __syncthreads();
@@ -343,17 +356,16 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
           ++seg;
           prev_u = u;
         }
-        const int sb = k & 1, wb = k % NWB;
+        const int sb = k % NSB, wb = k % NWB;
         if (!W.wait(B_FULL + wb, (k / NWB) & 1)) break;
-        // the score buffer (and the P in it) is free once PV two tiles back has completed
-        if (k >= 2 && !W.wait(B_PVDONE + sb, ((k >> 1) - 1) & 1)) break;
+        // the score buffer (and the P in it) is free once the PV NSB tiles back has completed
+        if (k >= NSB && !W.wait(B_SDONE + sb, (k / NSB - 1) & 1)) break;
         tc::fence_after();
         const uint32_t kbase = sbase + V::WB_OFF + wb * V::ST_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t db = tc::sw128_desc(kbase + (kk >> 2) * V::KT_REG + (kk & 3) * 32, 16, 1024);
-          tc::mma_ts(tmem + V::S_COL + sb * V::S_BUF + (kk % V::SCH) * VNK, tmem + V::Q_COL + kk * 8, db, idesc_qk,
-                     kk >= V::SCH);
+          tc::mma_ts(tmem + V::S_COL + sb * V::S_BUF, tmem + V::Q_COL + kk * 8, db, idesc_qk, kk > 0);
         }
         tc::commit(sbase + V::BAR_OFF + 8 * (B_SFULL + sb));
       }
@@ -371,17 +383,18 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
         while (Pt[u + 1] <= g) ++u;
         const bool seg_start = u != prev_u;
         const bool seg_end = k == ntiles - 1 || g + 1 >= Pt[u + 1];
-        if (!W.wait(B_PFULL + (k & 1), (k >> 1) & 1)) break;
+        if (!W.wait(B_PFULL + k % NSB, (k / NSB) & 1)) break;
         if (seg_start && seg > 0 && !W.wait(B_OFREE, (seg - 1) & 1)) break;
         tc::fence_after();
         const uint32_t vbase = sbase + V::WB_OFF + (k % NWB) * V::ST_BYTES + V::KT_BYTES;
 #pragma unroll
         for (int kk = 0; kk < VNK / 16; ++kk) {
           const uint64_t db = tc::sw128_desc(vbase + kk * 2048, V::KT_REG, 1024);
-          tc::mma_ts(tmem + V::O_COL, tmem + V::S_COL + (k & 1) * V::S_BUF + kk * 8, db, idesc_pv,
+          tc::mma_ts(tmem + V::O_COL, tmem + V::S_COL + (k % NSB) * V::S_BUF + kk * 8, db, idesc_pv,
                      !seg_start || kk > 0);
         }
         tc::commit(sbase + V::BAR_OFF + 8 * (B_PVDONE + (k & 1)));
+        tc::commit(sbase + V::BAR_OFF + 8 * (B_SDONE + k % NSB));
         tc::commit(sbase + V::BAR_OFF + 8 * (B_WFREE + k % NWB));
         if (seg_end) ++seg;
         prev_u = u;
@@ -428,19 +441,13 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
         m_ref = -INFINITY;
         l = 0.f;
       }
-      const int sb = k & 1;
-      if (!__all_sync(0xffffffffu, W.wait(B_SFULL + sb, (k >> 1) & 1))) break;
+      const int sb = k % NSB;
+      if (!__all_sync(0xffffffffu, W.wait(B_SFULL + sb, (k / NSB) & 1))) break;
       tc::fence_after();
       uint32_t sr[VNK];
-      {
-        static_assert(V::SCH == 2 && VNK == 32, "two 32-column score accumulators");
-        uint32_t s2[VNK];
-        tc::ld32(tmem + lane_off + V::S_COL + sb * V::S_BUF, sr);
-        tc::ld32(tmem + lane_off + V::S_COL + sb * V::S_BUF + VNK, s2);
-        tc::wait_ld();
-#pragma unroll
-        for (int x = 0; x < VNK; ++x) sr[x] = __float_as_uint(__uint_as_float(sr[x]) + __uint_as_float(s2[x]));
-      }
+      static_assert(VNK == 32, "one 32-column score read per row");
+      tc::ld32(tmem + lane_off + V::S_COL + sb * V::S_BUF, sr);
+      tc::wait_ld();
       const int nvalid = min(VNK, Nn[u] - (g - Pt[u]) * VNK);
       float tmax = -INFINITY;
 #pragma unroll
@@ -487,13 +494,13 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
       }
       l += lsum;
       // row t of P (fp16 pairs) over this tile's scores, where PV reads its A
-      // operand (the scores were read above; the PV two tiles back that read
+      // operand (the scores were read above; the PV NSB tiles back that read
       // this buffer's P completed before QK(k) was issued)
       tc::st16(tmem + lane_off + V::S_COL + sb * V::S_BUF, ph);
       tc::wait_st();
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(sbase + V::BAR_OFF + 8 * (B_PFULL + (k & 1)));
+      if (lane == 0) mbar_arrive(sbase + V::BAR_OFF + 8 * (B_PFULL + sb));
       if (seg_end) {
         if (!__all_sync(0xffffffffu, W.wait(B_PVDONE + (k & 1), (k >> 1) & 1))) break;
         tc::fence_after();
@@ -616,23 +623,17 @@ __global__ void __launch_bounds__(256) verify_combine_kernel(const VerifyCombine
   // ---- the prefix segments of this unit (row r = g * T + i)
   const int U = a.S * Hkv, u = s * Hkv + j, NC = a.split_ctas;
   const int Ttot = a.tiles[U];
-  const int p0 = a.tiles[u], p1 = a.tiles[u + 1];
-  int S = 0, c_lo = 0, first_slot = 0;
-  if (p1 > p0) {
-    c_lo = static_cast<int>((static_cast<int64_t>(p0 + 1) * NC - 1) / Ttot);
-    const int c_hi = static_cast<int>((static_cast<int64_t>(p1) * NC - 1) / Ttot);
-    S = c_hi - c_lo + 1;
-    first_slot = static_cast<int>(static_cast<int64_t>(c_lo) * Ttot / NC) == p0 ? c_lo : NC + u;
-  }
+  const int c_lo = a.tiles[U + 1 + u], S = a.tiles[2 * U + 1 + u], first_slot = a.tiles[3 * U + 1 + u];
+  const int64_t W = Ttot + static_cast<int64_t>(kVerifySegmentCost) * U;  // the split's weighted length
   const int r = g * T + i;
   auto seg_row = [&](int k) -> const float* {
     const int slot = k == 0 ? first_slot : c_lo + k;
     return a.part + (static_cast<int64_t>(slot) * R + r) * row_stride<D>();
   };
-  auto seg_ok = [&](int k) -> bool {
+  auto seg_ok = [&](int k) -> bool {  // a CTA strictly inside the span holds tiles iff its range is not empty
     if (k == 0) return true;
     const int64_t cc = c_lo + k;
-    return cc * Ttot / NC < (cc + 1) * Ttot / NC;
+    return cc * W / NC < (cc + 1) * W / NC;
   };
   for (int k = 0; k < S; ++k)
     if (seg_ok(k)) M = fmaxf(M, seg_row(k)[D]);
