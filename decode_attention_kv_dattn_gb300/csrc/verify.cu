@@ -200,7 +200,6 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + V::MISC_OFF);
-  pdl_trigger();
 
   const int ntiles = g1 - g0;
   const Waiter W{sbase + V::BAR_OFF, abort_flag, a.err};
@@ -404,6 +403,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
   } else if (ntiles > 0 && warp < kSoftWarps) {
     // ================= softmax: thread t owns row t =================
     pdl_wait();  // q rotated by the prologue
+    pdl_trigger();
     const int t = threadIdx.x;
     const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
     int u = unit_of(Pt, U, g0), prev_u = -1, seg = 0;
@@ -538,6 +538,11 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
     tc::fence_after();
     tc::dealloc(tmem, V::TMEM_COLS);
   }
+  // The combine may begin once every CTA of this pass has triggered, and each
+  // one does so only after the prologue has completed: so the combine reads the
+  // rotated q and window keys before waiting for this pass.
+  pdl_wait();
+  pdl_trigger();
 }
 
 // ---------------------------------------------------------------- combine
@@ -590,9 +595,9 @@ __global__ void __launch_bounds__(256) verify_combine_kernel(const VerifyCombine
   __syncthreads();
   const int np = npath_s;
 
-  pdl_wait();  // prefix partials of the split pass; rotated q and window keys
-  pdl_trigger();
-
+  // ---- before waiting for the prefix pass (the prologue it waited for has
+  // completed): the row's tree path - itself and its ancestors - scored in
+  // fp32 and joined as a softmax state (M, L, acc) of its own
   float q[EPL];
   {
     const float* src = a.qhat + (tok * Hq + h) * D + lane * EPL;
@@ -602,7 +607,6 @@ __global__ void __launch_bounds__(256) verify_combine_kernel(const VerifyCombine
       q[e] = x.x; q[e + 1] = x.y; q[e + 2] = x.z; q[e + 3] = x.w;
     }
   }
-  // ---- scores of the row's tree path (itself and its ancestors), fp32
   float sw[16];
   float M = -INFINITY;
 #pragma unroll 1
@@ -620,42 +624,10 @@ __global__ void __launch_bounds__(256) verify_combine_kernel(const VerifyCombine
     sw[p] = dot;
     M = fmaxf(M, dot);
   }
-  // ---- the prefix segments of this unit (row r = g * T + i)
-  const int U = a.S * Hkv, u = s * Hkv + j, NC = a.split_ctas;
-  const int Ttot = a.tiles[U];
-  const int c_lo = a.tiles[U + 1 + u], S = a.tiles[2 * U + 1 + u], first_slot = a.tiles[3 * U + 1 + u];
-  const int64_t W = Ttot + static_cast<int64_t>(kVerifySegmentCost) * U;  // the split's weighted length
-  const int r = g * T + i;
-  auto seg_row = [&](int k) -> const float* {
-    const int slot = k == 0 ? first_slot : c_lo + k;
-    return a.part + (static_cast<int64_t>(slot) * R + r) * row_stride<D>();
-  };
-  auto seg_ok = [&](int k) -> bool {  // a CTA strictly inside the span holds tiles iff its range is not empty
-    if (k == 0) return true;
-    const int64_t cc = c_lo + k;
-    return cc * W / NC < (cc + 1) * W / NC;
-  };
-  for (int k = 0; k < S; ++k)
-    if (seg_ok(k)) M = fmaxf(M, seg_row(k)[D]);
   float acc[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-  float L = 0.f;
-  for (int k = 0; k < S; ++k) {
-    if (!seg_ok(k)) continue;
-    const float* pr = seg_row(k);
-    const float w = exp2_fast(pr[D] - M);
-    L = fmaf(w, pr[D + 1], L);
-#pragma unroll
-    for (int e = 0; e < EPL; e += 4) {
-      const float4 x = *reinterpret_cast<const float4*>(pr + lane * EPL + e);
-      acc[e] = fmaf(w, x.x, acc[e]);
-      acc[e + 1] = fmaf(w, x.y, acc[e + 1]);
-      acc[e + 2] = fmaf(w, x.z, acc[e + 2]);
-      acc[e + 3] = fmaf(w, x.w, acc[e + 3]);
-    }
-  }
-  // ---- the tree path joins as its own score vector
+  float L = 0.f;  // relative to M
 #pragma unroll 1
   for (int p = 0; p < np; ++p) {
     const float w = exp2_fast(sw[p] - M);
@@ -667,6 +639,61 @@ __global__ void __launch_bounds__(256) verify_combine_kernel(const VerifyCombine
       acc[e] = fmaf(w, bf16_lo(x), acc[e]);
       acc[e + 1] = fmaf(w, bf16_hi(x), acc[e + 1]);
     }
+  }
+
+  pdl_wait();  // the prefix partials and their layout
+  pdl_trigger();
+
+  // ---- the prefix segments of this unit (row r = g * T + i), merged online
+  const int U = a.S * Hkv, u = s * Hkv + j, NC = a.split_ctas;
+  const int Ttot = a.tiles[U];
+  const int c_lo = a.tiles[U + 1 + u], S = a.tiles[2 * U + 1 + u], first_slot = a.tiles[3 * U + 1 + u];
+  const int64_t W = Ttot + static_cast<int64_t>(kVerifySegmentCost) * U;  // the split's weighted length
+  const int r = g * T + i;
+  auto seg_row = [&](int k) -> const float* {
+    const int slot = k == 0 ? first_slot : c_lo + k;
+    return a.part + (static_cast<int64_t>(slot) * R + r) * row_stride<D>();
+  };
+  auto seg_ok = [&](int k) -> bool {  // a CTA strictly inside the span holds tiles iff its range is not empty
+    if (k >= S) return false;
+    if (k == 0) return true;
+    const int64_t cc = c_lo + k;
+    return cc * W / NC < (cc + 1) * W / NC;
+  };
+  constexpr int SB = 2;  // segments whose loads go out together
+  for (int k0 = 0; k0 < S; k0 += SB) {
+    float mk[SB], lk[SB], ok[SB][EPL];
+#pragma unroll
+    for (int b = 0; b < SB; ++b) {
+      mk[b] = -INFINITY;
+      lk[b] = 0.f;
+      if (seg_ok(k0 + b)) {
+        const float* pr = seg_row(k0 + b);
+        mk[b] = __ldcg(pr + D);
+        lk[b] = __ldcg(pr + D + 1);
+#pragma unroll
+        for (int e = 0; e < EPL; e += 4) {
+          const float4 x = __ldcg(reinterpret_cast<const float4*>(pr + lane * EPL + e));
+          ok[b][e] = x.x; ok[b][e + 1] = x.y; ok[b][e + 2] = x.z; ok[b][e + 3] = x.w;
+        }
+      }
+    }
+    float Mn = M;
+#pragma unroll
+    for (int b = 0; b < SB; ++b) Mn = fmaxf(Mn, mk[b]);
+    const float f = exp2_fast(M - Mn);  // M is finite: the row's own score is in it
+    L *= f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] *= f;
+#pragma unroll
+    for (int b = 0; b < SB; ++b) {
+      if (mk[b] == -INFINITY) continue;
+      const float w = exp2_fast(mk[b] - Mn);
+      L = fmaf(w, lk[b], L);
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[e] = fmaf(w, ok[b][e], acc[e]);
+    }
+    M = Mn;
   }
   const float scale = sig / L;
   float* dst = a.out + (tok * Hq + h) * D + lane * EPL;
