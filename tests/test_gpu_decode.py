@@ -140,6 +140,30 @@ def test_paged_group_sizes(dattn, oracle, D, Hq, Hkv):
     run_and_check(dattn, oracle, case)
 
 
+def test_many_short_units_per_cta(dattn, oracle):
+    """512 (stream, KV head) units, most of them a few keys long (some empty)
+    and a few long ones: the weighted split gives some CTAs dozens of unit
+    segments, each prepared and ended by the helper warp while the streaming
+    warps go on."""
+    rng = np.random.default_rng(7)
+    lens = [int(x) for x in rng.integers(0, 40, 256)]
+    for b in (3, 100, 200):
+        lens[b] = 3000
+    for b in (5, 6, 50):
+        lens[b] = 0
+    case = paged_case(61, len(lens), 4, 2, 128, 16, lens, gate=True, rope=(128, 1e6))
+    run_and_check(dattn, oracle, case)
+
+
+def test_many_short_ring_units(dattn, oracle):
+    """The same on ring caches: 256 streams x 2 KV heads, short and empty rings."""
+    rng = np.random.default_rng(8)
+    counts = [int(x) for x in rng.integers(0, 30, 256)]
+    counts[10] = 63
+    case = ring_case(62, 256, 8, 2, 256, 63, counts)
+    run_and_check(dattn, oracle, case)
+
+
 def test_lengths_far_below_the_planned_bound(dattn, oracle):
     """The split grid is sized from the call's bound; when the streams are much
     shorter, many split CTAs get no keys and the combine must skip them."""
