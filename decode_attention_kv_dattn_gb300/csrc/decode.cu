@@ -32,9 +32,10 @@
 //    exact fixed-point phase and an fp32 polynomial (rope_cos_sin). The
 //    combining CTA rotates the new key with the same cos/sin and rounds it to
 //    bf16 from fp64 - the exact entry that is scored and stored.
-//  * Loads. Each warp owns a ring of NS stage buffers. One lane issues 2D
-//    tensor TMA copies (boxes of 16 rows x 64 bf16, 128-byte swizzle; one box
-//    per 64 dims of K and of V per group) for the warp's tile NS ahead, with
+//  * Loads. Each warp owns a ring of NS stage buffers. One lane issues tensor
+//    TMA copies (16 rows of a group, 128-byte swizzle: one 3D box for both
+//    64-dim regions at D = 128, one 2D box per region at D = 256) for the
+//    warp's tile NS ahead, with
 //    completion counted in bytes on the stage's mbarrier; the ring keeps
 //    streaming across segment boundaries. The rows of each group and its
 //    valid-row mask (past a unit's length, past a page, outside a ring's valid
@@ -86,6 +87,11 @@ constexpr int kSegmentCost = DATTN_SEGMENT_COST;
 #define DATTN_PIECES_SLACK 25
 #endif
 constexpr int kPiecesSlack = DATTN_PIECES_SLACK;
+// TMA boxes per 16-row group: at D = 128 one 3D box takes both 64-dim regions
+// (measured faster); at D = 256 one 2D box per region (the single 8 KB box
+// measured slower on the 16-token-page and ring layers of the hybrid step).
+template <int D>
+constexpr bool kGroupBox = D == 128;
 
 template <int D, int NT>
 struct Geo {
@@ -738,11 +744,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       for (int kg = 0; kg < KG; ++kg) {
         if (kg < gn) {
           const int row0 = wr[kg];
+          if constexpr (kGroupBox<D>) {
+            // one box per group: 16 rows x both 64-dim regions
+            tma_load_3d(kd + kg * Gm::GBYTES, &a.tmap_k, 0, row0, 0, bar, policy);
+            tma_load_3d(kd + Gm::KHALF + kg * Gm::GBYTES, &a.tmap_v, 0, row0, 0, bar, policy);
+          } else {
+            // one box per 64-dim region of the group
 #pragma unroll
-          for (int bx = 0; bx < BOXES; ++bx) {
-            tma_load_2d(kd + kg * Gm::GBYTES + bx * kBoxBytes, &a.tmap_k, 64 * bx, row0, bar, policy);
-            tma_load_2d(kd + Gm::KHALF + kg * Gm::GBYTES + bx * kBoxBytes, &a.tmap_v, 64 * bx, row0, bar,
-                        policy);
+            for (int bx = 0; bx < BOXES; ++bx) {
+              tma_load_2d(kd + kg * Gm::GBYTES + bx * kBoxBytes, &a.tmap_k, 64 * bx, row0, bar, policy);
+              tma_load_2d(kd + Gm::KHALF + kg * Gm::GBYTES + bx * kBoxBytes, &a.tmap_v, 64 * bx, row0, bar,
+                          policy);
+            }
           }
         }
       }
@@ -1149,12 +1162,19 @@ cudaError_t encode_cache_maps(const CacheView& c, int Hkv, int D, CUtensorMap* k
   if (!fn) return cudaErrorNotSupported;
   const uint64_t rows = static_cast<uint64_t>(c.n_rows) * Hkv * (c.paged ? c.P : c.R);
   if (rows == 0 || rows > 0x7fffffffull) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), rows};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
-  const cuuint32_t box[2] = {64, kGroup};
-  const cuuint32_t estride[2] = {1, 1};
+  // D = 128: a 3D view of the [rows, D] bf16 cache, (64 dims, row, 64-dim
+  // region), so that one box brings a 16-row group as its regions of 16 rows x
+  // 128 bytes one after the other; D = 256: the 2D [rows, D] view, one box
+  // per region. Either way the 128-byte-swizzled layout the MMAs read.
+  const bool group_box = D == 128 ? kGroupBox<128> : kGroupBox<256>;
+  const cuuint32_t rank = group_box ? 3 : 2;
+  const cuuint64_t dims[3] = {group_box ? 64u : static_cast<cuuint64_t>(D), rows,
+                              static_cast<cuuint64_t>(D / 64)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, 128};
+  const cuuint32_t box[3] = {64, kGroup, static_cast<cuuint32_t>(D / 64)};
+  const cuuint32_t estride[3] = {1, 1, 1};
   for (int i = 0; i < 2; ++i) {
-    const CUresult r = fn(i ? v : k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, i ? c.v : c.k, dims, strides,
+    const CUresult r = fn(i ? v : k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, i ? c.v : c.k, dims, strides,
                           box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;

@@ -146,8 +146,10 @@ struct VerifyCombineArgs {
 cudaError_t launch_rope(const RopeArgs& a, cudaStream_t s);
 // Decode with `ctas` CTAs (at most decode_ctas_per_sm per SM).
 cudaError_t launch_decode(const DecodeArgs& a, int D, int ctas, cudaStream_t s);
-// Tensor maps of a cache's K and V for the decode kernel: [n_rows * Hkv * (R
-// or P), D] bf16 rows, boxes of 16 rows x 64 elements, 128-byte swizzle.
+// Tensor maps of a cache's K and V for the decode kernel over its [n_rows *
+// Hkv * (R or P), D] bf16 rows, 128-byte swizzle: at D = 128 seen as (64 dims,
+// row, 2 regions) with one box per 16-row group; at D = 256 as [rows, D] with
+// boxes of 16 rows x 64 dims.
 cudaError_t encode_cache_maps(const CacheView& c, int Hkv, int D, CUtensorMap* k, CUtensorMap* v);
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_verify_split(const VerifySplitArgs& a, int D, cudaStream_t s);
