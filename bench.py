@@ -472,33 +472,69 @@ def time_layers(step, K):
 
 def time_e2e(step, K, W, world):
     """Through the public API with host buffers: every step copies its inputs
-    from pinned host memory, replays the step's calls and reads the outputs back."""
+    from pinned host memory, replays the step's calls and reads the outputs
+    back. The copies run on a second stream through two device staging
+    buffers each way, so step k's upload and step k-1's download overlap the
+    calls of steps k-1 and k; events order each step's calls after its own
+    inputs have arrived and each download after its own outputs exist. The
+    timed region runs from the first upload to the last download."""
+    main = torch.cuda.current_stream()
+    cs = torch.cuda.Stream()
     host_in = torch.empty(step.inbuf.shape, dtype=step.inbuf.dtype, pin_memory=True)
     host_in.copy_(step.inbuf)
-    host_out = torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
-    s = torch.cuda.current_stream()
+    host_out = [torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True) for _ in range(2)]
+    in_stage = [torch.empty_like(step.inbuf) for _ in range(2)]
+    out_stage = [torch.empty_like(step.out) for _ in range(2)]
+    ev = {n: [torch.cuda.Event() for _ in range(2)] for n in ("in", "in_free", "out", "out_free")}
 
-    def one():
-        step.inbuf.copy_(host_in, non_blocking=True)
+    def upload(k):
+        with torch.cuda.stream(cs):
+            if k >= 2:
+                cs.wait_event(ev["in_free"][k % 2])
+            in_stage[k % 2].copy_(host_in, non_blocking=True)
+            ev["in"][k % 2].record(cs)
+
+    def compute(k):
+        main.wait_event(ev["in"][k % 2])
+        step.inbuf.copy_(in_stage[k % 2])
+        ev["in_free"][k % 2].record(main)
         step.graph.replay()
-        host_out.copy_(step.out, non_blocking=True)
+        if k >= 2:
+            main.wait_event(ev["out_free"][k % 2])
+        out_stage[k % 2].copy_(step.out)
+        ev["out"][k % 2].record(main)
 
-    for _ in range(W):
-        one()
+    def download(k):
+        with torch.cuda.stream(cs):
+            cs.wait_event(ev["out"][k % 2])
+            host_out[k % 2].copy_(out_stage[k % 2], non_blocking=True)
+            ev["out_free"][k % 2].record(cs)
+
+    def run(n, start_event=None):
+        if start_event is not None:
+            cs.wait_event(start_event)
+        upload(0)
+        for k in range(n):
+            if k + 1 < n:
+                upload(k + 1)
+            compute(k)
+            download(k)
+        main.wait_stream(cs)
+
+    run(W)
     torch.cuda.synchronize()
     barrier(world)
     t0 = time.perf_counter()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(s)
-    for _ in range(K):
-        one()
-    e1.record(s)
+    e0.record(main)
+    run(K, e0)
+    e1.record(main)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     barrier(world)
     h2d = host_in.numel() * host_in.element_size()
-    d2h = host_out.numel() * host_out.element_size()
+    d2h = host_out[0].numel() * host_out[0].element_size()
     return max(e0.elapsed_time(e1) / 1e3, wall), h2d, d2h
 
 
