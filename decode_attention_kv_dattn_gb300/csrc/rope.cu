@@ -27,15 +27,16 @@ constexpr int kMaxT = 16;             // verify rows per stream
 // The prologue of a call: one CTA per token row. Work items are "pair slots"
 // of every head (Hq query heads, then Hkv key heads): slot p < r/2 is the
 // rotated pair (p, p + r/2); slot p >= r/2 holds two pass-through dims. All
-// inputs are loaded first; the cos/sin of each pair index is computed
-// once per row (one thread each) into shared memory meanwhile.
+// inputs are loaded first, before waiting for the preceding launch; the
+// cos/sin of each pair index is computed once per row (one thread each) into
+// shared memory meanwhile.
 __global__ void __launch_bounds__(kRowThreads) rope_kernel(const RopeArgs a) {
   __shared__ float cs_c[128], cs_s[128];
   __shared__ int64_t pos_s;
   __shared__ int par_s[kMaxT];
-  // The workspace written below may still be read by the previous call.
-  pdl_wait();
-  pdl_trigger();
+  // Everything up to the stores reads caller inputs only, so it runs while the
+  // previous launch finishes; the workspace written below may still be read
+  // by it, so the stores wait.
   const int row = blockIdx.x;
   const int half = a.r / 2;
   const int slots = a.D / 2;
@@ -88,6 +89,9 @@ __global__ void __launch_bounds__(kRowThreads) rope_kernel(const RopeArgs a) {
     cs_s[threadIdx.x] = sf;
   }
   __syncthreads();
+
+  pdl_wait();
+  pdl_trigger();
 
   // ---- rotate and store
 #pragma unroll
