@@ -61,6 +61,7 @@ struct dattn_handle {
   int* counters[2] = {nullptr, nullptr};
   unsigned decode_calls = 0;
   float* qhat = nullptr;    // verify: rotated q of the window rows
+  uint16_t* qhat16 = nullptr;  // the same rounded to fp16 (the tensor-core pass's operand)
   int* tiles = nullptr;     // verify: tile prefix over units, from its split pass
   uint16_t* khat = nullptr; // verify: rotated window keys
   float* vpart = nullptr;   // verify partials: [sms + units][G*T][D+4]
@@ -225,6 +226,7 @@ int dattn_create(const dattn_config* cfg, int device, dattn_t** out) {
   const size_t rows = static_cast<size_t>(h->max_streams) *
                       (h->max_verify_rows > 1 ? h->max_verify_rows : 1);
   if (cudaMalloc(&h->qhat, rows * Hq * D * sizeof(float)) != cudaSuccess) return fail(DATTN_ECUDA);
+  if (cudaMalloc(&h->qhat16, rows * Hq * D * sizeof(uint16_t)) != cudaSuccess) return fail(DATTN_ECUDA);
   if (cudaMalloc(&h->khat, rows * Hkv * D * sizeof(uint16_t)) != cudaSuccess) return fail(DATTN_ECUDA);
   // Decode partials: one slot per CTA plus one per unit; per-unit counters.
   if (static_cast<int64_t>(h->max_streams) * Hkv > decode_max_units()) return fail(DATTN_EUNSUPPORTED);
@@ -257,6 +259,7 @@ void dattn_destroy(dattn_t* h) {
   DeviceGuard guard(h->device);
   for (uint64_t* p : h->rope_step) cudaFree(p);
   cudaFree(h->qhat);
+  cudaFree(h->qhat16);
   cudaFree(h->khat);
   for (int i = 0; i < 2; ++i) {
     cudaFree(h->part[i]);
@@ -417,6 +420,7 @@ int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, const dattn_ve
   ra.rope_step = h->rope_step[layer];
   ra.q_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(h->D)));
   ra.qhat = h->qhat;
+  ra.qhat16 = h->qhat16;
   ra.khat = h->khat;
   ra.err = h->err;
   rc = cuda_status(launch_rope(ra, s));
@@ -433,7 +437,7 @@ int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, const dattn_ve
   va.G = h->G;
   va.ctas = static_cast<int>(ctas);
   va.max_len = n_max;
-  va.qhat = h->qhat;
+  va.qhat16 = h->qhat16;
   va.part = h->vpart;
   va.tiles = h->tiles;
   va.err = h->err;

@@ -53,6 +53,7 @@ struct RopeArgs {
   const uint64_t* rope_step;   // [r / 2] phase steps (rope_phase_step)
   float q_scale;               // log2(e) / sqrt(D)
   float* qhat;                 // [rows, Hq, D]
+  uint16_t* qhat16;            // [rows, Hq, D] the same values rounded to fp16 (bits), or null
   uint16_t* khat;              // [rows, Hkv, D]
   int* err;
 };
@@ -115,7 +116,7 @@ struct VerifySplitArgs {
   int S, T, Hkv, G;
   int ctas;
   int max_len;
-  const float* qhat;           // [S*T, Hq, D] pre-scaled, from the RoPE prologue
+  const uint16_t* qhat16;      // [S*T, Hq, D] pre-scaled q rounded to fp16 (bits), from the RoPE prologue
   float* part;
   int* tiles;                  // out, U = S*Hkv: [U + 1] tile prefix over units, then per
                                // unit the first CTA of its span [U], the span's length [U]

@@ -11,7 +11,10 @@
 // polynomial); the entry is the bf16 nearest to the exact x*c - y*s (ties to
 // even), from fp32 error terms or, near a bf16 midpoint, in integers
 // (bf16_dot2). q is rotated in fp32 and pre-scaled by log2(e)/sqrt(D) so that
-// the split kernel's scores are in base-2 units.
+// the split kernel's scores are in base-2 units; the tensor-core pass reads
+// it rounded to fp16, which is written beside it.
+#include <cuda_fp16.h>
+
 #include "bf16_exact.h"
 #include "common.cuh"
 
@@ -104,14 +107,21 @@ __global__ void __launch_bounds__(kRowThreads) rope_kernel(const RopeArgs a) {
     const float x = bf16_to_f32(static_cast<uint16_t>(xy[k] & 0xffffu));
     const float y = bf16_to_f32(static_cast<uint16_t>(xy[k] >> 16));
     if (hh < a.Hq) {
-      float* dst = a.qhat + (static_cast<int64_t>(row) * a.Hq + hh) * a.D;
+      const int64_t o = (static_cast<int64_t>(row) * a.Hq + hh) * a.D;
+      float v0, v1;
       if (p < half) {
         const float cf = cs_c[p], sf = cs_s[p];
-        dst[d0] = fmaf(x, cf, -y * sf) * a.q_scale;
-        dst[d1] = fmaf(y, cf, x * sf) * a.q_scale;
+        v0 = fmaf(x, cf, -y * sf) * a.q_scale;
+        v1 = fmaf(y, cf, x * sf) * a.q_scale;
       } else {
-        dst[d0] = x * a.q_scale;
-        dst[d1] = y * a.q_scale;
+        v0 = x * a.q_scale;
+        v1 = y * a.q_scale;
+      }
+      a.qhat[o + d0] = v0;
+      a.qhat[o + d1] = v1;
+      if (a.qhat16) {  // the tensor-core pass's operand: the same values, rounded to nearest fp16
+        a.qhat16[o + d0] = __half_as_ushort(__float2half_rn(v0));
+        a.qhat16[o + d1] = __half_as_ushort(__float2half_rn(v1));
       }
     } else {
       uint16_t* dst = a.khat + (static_cast<int64_t>(row) * a.Hkv + (hh - a.Hq)) * a.D;

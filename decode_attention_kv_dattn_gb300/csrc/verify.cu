@@ -417,20 +417,22 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
         // this unit's q rows as fp16 pairs into tensor memory (the QK MMAs'
         // A operand; the previous unit's QKs are done: its last scores were read)
         const int s = u / Hkv, j = u - s * Hkv;
-        const float* src = nullptr;
+        const uint16_t* src = nullptr;
         if (t < R) {
           const int gq = t / T, i = t - gq * T;
-          src = a.qhat + ((static_cast<int64_t>(s) * T + i) * Hq + j * G + gq) * D;
+          src = a.qhat16 + ((static_cast<int64_t>(s) * T + i) * Hq + j * G + gq) * D;
         }
 #pragma unroll 1
         for (int c32 = 0; c32 < D / 64; ++c32) {
-          uint32_t qv[32];
+          uint32_t qv[32];  // fp16 pairs, the lower dim in the low half
 #pragma unroll
-          for (int x = 0; x < 32; x += 2) {
-            float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (src) y = *reinterpret_cast<const float4*>(src + 64 * c32 + 2 * x);
-            qv[x] = cvt_pair_f16(y.x, y.y);
-            qv[x + 1] = cvt_pair_f16(y.z, y.w);
+          for (int x = 0; x < 32; x += 4) {
+            uint4 y = make_uint4(0u, 0u, 0u, 0u);
+            if (src) y = *reinterpret_cast<const uint4*>(src + 64 * c32 + 2 * x);
+            qv[x] = y.x;
+            qv[x + 1] = y.y;
+            qv[x + 2] = y.z;
+            qv[x + 3] = y.w;
           }
           tc::st32(tmem + lane_off + V::Q_COL + 32 * c32, qv);
         }
