@@ -77,7 +77,7 @@ def peak_hbm():
     try:
         with open(path) as f:
             return float(json.load(f)["hbm_gbs"]), "measured"
-    except Exception:
+    except (OSError, ValueError, KeyError, TypeError):
         return FALLBACK_HBM_GBS, "fallback"
 
 
@@ -100,7 +100,7 @@ class ClockSampler:
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except Exception:
+        except OSError:
             self.proc = None
 
     def stop(self):
@@ -109,7 +109,7 @@ class ClockSampler:
         self.proc.terminate()
         try:
             out, _ = self.proc.communicate(timeout=5)
-        except Exception:
+        except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
         sm, smax, reasons = [], [], set()
@@ -703,8 +703,9 @@ def run_dattn(args, world, rank, local):
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
         try:
-            traffic = json.load(open(tpath)).get(args.workload)
-        except Exception:
+            with open(tpath) as f:
+                traffic = json.load(f).get(args.workload)
+        except (OSError, ValueError, AttributeError):
             traffic = None
     config = dict(step.config)
     config.update({"l2": ("flushed (256 MiB write) before every step" if step.flush_l2 else

@@ -1121,12 +1121,9 @@ template <int D, int NT, bool PAGED>
 cudaError_t decode_launch(const DecodeArgs& a, int ctas, cudaStream_t s) {
   using Gm = Geo<D, NT>;
   auto k = decode_kernel<D, NT, PAGED>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM_MAX);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> opted{0};
+  const cudaError_t e = opt_in_smem(k, Gm::SMEM_MAX, opted);
+  if (e != cudaSuccess) return e;
   const size_t smem = 1024 + Gm::TAB_OFF + (4 * a.B * a.Hkv + 1) * sizeof(int);
   return launch_pdl(k, dim3(ctas), dim3(kThreads), smem, s, a);
 }

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <cmath>
 #include <utility>
 
@@ -177,6 +178,21 @@ bool prev_launch_writes(void* stream, const void* cache_k);
 // Record a launch made on `stream` that writes into the cache with K array
 // `cache_k` (null: writes no cache).
 void record_launch(void* stream, const void* cache_k);
+
+// Raise `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per device (`done` holds one bit per device id below 64; the
+// call is idempotent, so racing threads at worst repeat it).
+template <typename Kernel>
+cudaError_t opt_in_smem(Kernel kernel, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0ull;
+  if (bit != 0ull && (done.load(std::memory_order_acquire) & bit) != 0ull) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0ull) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 // Launch with programmatic stream serialization: the kernel may begin while
 // its predecessor in the stream finishes; every kernel here waits on the

@@ -719,12 +719,9 @@ __global__ void __launch_bounds__(256) verify_combine_kernel(const VerifyCombine
 template <int D>
 cudaError_t verify_split_launch(const VerifySplitArgs& a, cudaStream_t s) {
   using V = VGeo<D>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(verify_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, V::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> opted{0};
+  const cudaError_t e = opt_in_smem(verify_split_kernel<D>, V::SMEM, opted);
+  if (e != cudaSuccess) return e;
   return launch_pdl(verify_split_kernel<D>, dim3(a.ctas), dim3(kVThreads), V::SMEM, s, a);
 }
 
