@@ -151,7 +151,7 @@ const char* dattn_error_string(int code) {
     case DATTN_ECUDA: return "CUDA runtime error";
     case DATTN_EINDEX: return "device metadata out of range (page id, ring slot, tree parent)";
     case DATTN_ETIMEOUT: return "a bounded device wait timed out";
-    case DATTN_EUNSUPPORTED: return "shape not supported by this build";
+    case DATTN_EUNSUPPORTED: return "shape not supported: no compiled kernel for it";
     case DATTN_ELENGTH: return "a stream is longer than the call's bound";
     case DATTN_ERANGE: return "a cached value lies outside the fp16 range the verify pass computes in";
     default: return "unknown dattn status";

@@ -65,7 +65,7 @@ enum {
   DATTN_ECUDA = 3,         /* a CUDA runtime call failed                          */
   DATTN_EINDEX = 4,        /* device metadata out of range (from dattn_get_error) */
   DATTN_ETIMEOUT = 5,      /* a bounded device wait gave up (dattn_get_error)     */
-  DATTN_EUNSUPPORTED = 6,  /* a shape this build has no kernel for                */
+  DATTN_EUNSUPPORTED = 6,  /* a shape with no compiled kernel                     */
   DATTN_ELENGTH = 7,       /* a stream longer than the call's bound (get_error)   */
   DATTN_ERANGE = 8         /* verify: a cached K/V value beyond the fp16 range
                               (|x| >= 65520) the tensor-core pass computes in     */
