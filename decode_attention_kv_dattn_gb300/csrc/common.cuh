@@ -223,7 +223,7 @@ __device__ void block_scan_inclusive(int* x, int n) {
 
 // Last unit u in [0, U) with P[u] <= g (P[0] = 0 <= g); its tile range
 // [P[u], P[u + 1]) then contains g.
-__device__ __forceinline__ int unit_of(const int* P, int U, int g) {
+__host__ __device__ __forceinline__ int unit_of(const int* P, int U, int g) {
   int lo = 0, hi = U - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -244,9 +244,9 @@ struct Split {
   const int* P;  // [U + 1] tile prefix over units
   int U, C, NC;
   int64_t W;
-  __device__ __forceinline__ int64_t bound(int c) const { return static_cast<int64_t>(c) * W / NC; }
+  __host__ __device__ __forceinline__ int64_t bound(int c) const { return static_cast<int64_t>(c) * W / NC; }
   // first tile at or after weighted position t (T past the end)
-  __device__ __forceinline__ int tile_at(int64_t t) const {
+  __host__ __device__ __forceinline__ int tile_at(int64_t t) const {
     if (t >= W) return P[U];
     int lo = 0, hi = U - 1;  // the last unit starting at or before t
     while (lo < hi) {
@@ -257,17 +257,17 @@ struct Split {
     return P[lo] + (off > 0 ? static_cast<int>(off) : 0);
   }
   // CTA whose range holds tile x of unit u
-  __device__ __forceinline__ int cta_of(int x, int u) const {
+  __host__ __device__ __forceinline__ int cta_of(int x, int u) const {
     const int64_t w = x + static_cast<int64_t>(C) * (u + 1);
     return static_cast<int>(((w + 1) * NC - 1) / W);
   }
-  __device__ __forceinline__ bool has_tiles_inside(int c) const { return bound(c) < bound(c + 1); }
+  __host__ __device__ __forceinline__ bool has_tiles_inside(int c) const { return bound(c) < bound(c + 1); }
 };
 
 // Number of CTAs whose ranges hold tiles of unit u (global tiles [p0, p1)),
 // the first of them, the last, and the partial slot of the first one's
 // segment (that CTA's own slot when the unit starts its range).
-__device__ __forceinline__ int unit_segments(const Split& sp, int p0, int p1, int u, int& c_lo, int& c_hi,
+__host__ __device__ __forceinline__ int unit_segments(const Split& sp, int p0, int p1, int u, int& c_lo, int& c_hi,
                                              int& first_slot) {
   if (p1 <= p0) return 0;
   c_lo = sp.cta_of(p0, u);
