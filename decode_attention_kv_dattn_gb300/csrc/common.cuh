@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include "kernels.h"
+#include "rope_angle.h"
 
 namespace dattn {
 
@@ -29,38 +30,8 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
 }
 
 // ------------------------------------------------------------------ RoPE angle
-
-// cos and sin of one RoPE pair's angle at position pos, as fp32 values.
-// step = rint(2^64 * inv_freq / 2pi) is the pair's angle per position in
-// 64-bit fixed-point turns, so pos * step mod 2^64 is the phase, exactly. Its
-// top 32 bits split into a quadrant j (nearest quarter turn) and a remainder
-// in [-1/8, 1/8) turn; cos and sin of the remainder t come from their Taylor
-// series through t^10 and t^9 in fp32 (coefficients +-1/n!, first omitted
-// terms below 2e-9 on [-pi/4, pi/4]) and are turned by j quarter turns. Every
-// step is an integer or a correctly rounded fp32 operation (no contraction),
-// so the result is the same on any IEEE machine: within 1.5e-7 of the exact
-// values for |pos| <= 2^21, and no fp64 work.
-__device__ __forceinline__ void rope_cos_sin(int64_t pos, uint64_t step, float& c, float& s) {
-  const uint64_t phase = static_cast<uint64_t>(pos) * step;
-  const uint32_t w = static_cast<uint32_t>(phase >> 32) + (1u << 29);
-  const uint32_t quad = w >> 30;
-  const int32_t rho = static_cast<int32_t>(w & 0x3fffffffu) - (1 << 29);
-  const float t = __fmul_rn(__int2float_rn(rho), 1.46291807926715968e-09f);  // 2 pi / 2^32
-  const float t2 = __fmul_rn(t, t);
-  float sp = __fmaf_rn(t2, 2.75573192e-06f, -1.98412698e-04f);
-  sp = __fmaf_rn(t2, sp, 8.33333333e-03f);
-  sp = __fmaf_rn(t2, sp, -1.66666667e-01f);
-  const float sn = __fmaf_rn(__fmul_rn(t, t2), sp, t);
-  float cp = __fmaf_rn(t2, -2.75573192e-07f, 2.48015873e-05f);
-  cp = __fmaf_rn(t2, cp, -1.38888889e-03f);
-  cp = __fmaf_rn(t2, cp, 4.16666667e-02f);
-  cp = __fmaf_rn(t2, cp, -5.0e-01f);
-  const float cs = __fmaf_rn(t2, cp, 1.0f);
-  const float a = (quad & 1u) ? sn : cs;  // |cos| of the angle
-  const float b = (quad & 1u) ? cs : sn;  // |sin| of the angle
-  c = (quad == 1u || quad == 2u) ? -a : a;
-  s = (quad >= 2u) ? -b : b;
-}
+// rope_cos_sin: rope_angle.h (plain C++ apart from the qualifiers, so that the
+// host test suite builds the same routine).
 
 // 2^x with the hardware approximation (MUFU.EX2); exact 0 for -inf.
 __device__ __forceinline__ float exp2_fast(float x) {
