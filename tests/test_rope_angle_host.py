@@ -8,7 +8,9 @@ integer or correctly rounded fp32 operation, compiled without contraction), and
 the phase (pos * step mod 2^64, an exact integer) is turned into an angle in
 Python integers and fp64 (error ~1e-16), so the check is independent of the
 routine's own arithmetic. A planted mistake in the series or the quadrant logic
-moves some value by far more than the bound.
+moves some value by far more than the bound. A second test checks that the host
+library's per-pair steps (kernels.h: rope_phase_step) are that definition, bit
+for bit.
 """
 import math
 import os
@@ -107,3 +109,41 @@ def test_rope_cos_sin_within_bound(tmp_path):
         if err > worst[0]:
             worst = (err, (p, st, c, s, ec, es))
     assert worst[0] <= BOUND, f"max error {worst[0]:.3e} at {worst[1]}"
+
+
+STEP_SHIM = r'''
+#include <cstdio>
+#include "kernels.h"
+// stdin: "theta r i" per line; stdout: the library's phase step.
+int main() {
+  double theta;
+  int r, i;
+  while (std::scanf("%lf %d %d", &theta, &r, &i) == 3)
+    std::printf("%llu\n", static_cast<unsigned long long>(dattn::rope_phase_step(theta, r, i)));
+  return 0;
+}
+'''
+
+
+def test_library_phase_steps_match_the_definition(tmp_path):
+    """The host library's per-pair steps (kernels.h: rope_phase_step) are
+    rint(2^64 theta^(-2i/r) / 2 pi) as defined above, bit for bit."""
+    gxx = shutil.which("g++") or shutil.which("c++")
+    cuda_inc = "/usr/local/cuda/include"
+    if gxx is None or not os.path.isdir(cuda_inc):
+        pytest.skip("no host C++ compiler or CUDA headers")
+    src = tmp_path / "step_shim.cpp"
+    src.write_text(STEP_SHIM)
+    exe = tmp_path / "step_shim"
+    r = subprocess.run([gxx, "-O2", "-std=c++17", "-I", CSRC, "-I", cuda_inc, "-o", str(exe), str(src)],
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-4000:]
+    cases = [(theta, rd, i) for rd in (2, 32, 64, 128, 256) for theta in (1e4, 1e6, 5e6, 1.5e5)
+             for i in range(rd // 2)]
+    r = subprocess.run([str(exe)], input="".join(f"{t!r} {rd} {i}\n" for t, rd, i in cases),
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    got = [int(x) for x in r.stdout.split()]
+    want = [phase_step(t, rd, i) for t, rd, i in cases]
+    bad = [(c, g, w) for c, g, w in zip(cases, got, want) if g != w]
+    assert len(got) == len(cases) and not bad, bad[:5]
