@@ -41,6 +41,9 @@ CONTEXT = 4096
 HQ, HKV, D = 8, 2, 256
 SEED = 1
 FALLBACK_HBM_GBS = 6800.0
+# Steps that move less than this are timed with L2 flushed before each step
+# (a 256 MiB write, untimed); larger ones stream far more than the 129 MB L2.
+L2_SAFE_BYTES = 1 << 30
 
 
 # ---------------------------------------------------------------- accounting
@@ -79,6 +82,39 @@ def peak_hbm():
             return float(json.load(f)["hbm_gbs"]), "measured"
     except (OSError, ValueError, KeyError, TypeError):
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sources_sha():
+    """sha256 of the library's CUDA sources (csrc/), to tell whether a
+    recorded ncu capture still describes the kernels that run."""
+    import hashlib
+    d = os.path.join(ROOT, "decode_attention_kv_dattn_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(d)):
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch of the workload's dominant kernel from an ncu
+    capture (dram__bytes_read.sum + dram__bytes_write.sum), as recorded in
+    profiles/dram_traffic.md, or None when no capture matches the current
+    kernel sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    sha = kernel_sources_sha()
+    for line in lines:
+        p = [x.strip() for x in line.strip().strip("|").split("|")]
+        if len(p) >= 3 and p[0] == workload and p[2] == sha:
+            try:
+                return int(p[1])
+            except ValueError:
+                return None
+    return None
 
 
 # ---------------------------------------------------------------- clocks
@@ -239,6 +275,7 @@ class Step(Workload):
         self.ncalls = len(self.layers)
         total, tokens, per_kind = step_accounting(B, context)
         self.bytes_step, self.tokens_step = total, tokens
+        self.flush_l2 = total < L2_SAFE_BYTES
         self.dominant = [l for l, L in enumerate(self.layers) if L["kind"] == "full"]
         self.dominant_kv_bytes = per_kind["full"][0]
         self.others = [l for l, L in enumerate(self.layers) if L["kind"] == "sliding"]
@@ -294,6 +331,12 @@ class DecodeCall(Workload):
                 B, Hq, Hkv, Dh, P, r, th, gate = 8, 8, 2, 256, 64, 64, 5e6, False
                 self.lens = [1 << 18] * 8
                 desc = "long-context decode: 8 streams of 262,144 tokens, 64-token pages, 8 q / 2 KV heads, head_dim 256"
+            elif name.startswith("long128k_b"):
+                B = int(name[len("long128k_b"):])
+                Hq, Hkv, Dh, P, r, th, gate = 8, 2, 256, 64, 64, 5e6, False
+                self.lens = [1 << 17] * B
+                desc = (f"long-context decode: {B} stream(s) of 131,072 tokens, 64-token pages, "
+                        "8 q / 2 KV heads, head_dim 256")
             else:
                 raise ValueError(name)
             k, v, bt, seq = synth.paged_device(g, B, Hkv, Dh, P, self.lens, room=1, device=device)
@@ -302,6 +345,7 @@ class DecodeCall(Workload):
             self._keep = (k, v, bt, seq)
             pos, kind = self.lens, "full"
             self.config = {"workload": desc, "streams": B, "context": max(self.lens)}
+            self.flush_l2 = sum(self.lens) * 2 * Hkv * Dh * 2 < L2_SAFE_BYTES
         self.kind, self.B, self.Hq, self.Hkv, self.D, self.P, self.gate_on = kind, B, Hq, Hkv, Dh, P, gate
         self.rope = (layer["rotary_dim"], layer["rope_theta"])
         self.h = dattn.Handle(Hq, Hkv, Dh, [layer], B, max_context=max(self.lens) if kind == "full" else 0)
@@ -447,6 +491,56 @@ def time_graph(step, K, W, world):
     torch.cuda.synchronize()
     barrier(world)
     return e0.elapsed_time(e1) / 1e3
+
+
+# Every configuration of the method's workloads, timed in the same run as the
+# headline: name -> constructor. The hybrid grid covers batch 1/8/64 at
+# context 1024 and 4096; the long-context set adds 128k tokens at batch 1/8/64.
+SURVEY = [
+    ("sliding", lambda: DecodeCall("sliding", SEED)),
+    ("paged", lambda: DecodeCall("paged", SEED)),
+    ("verify", lambda: VerifyCall(SEED)),
+    ("long1m", lambda: DecodeCall("long1m", SEED)),
+    ("long262k", lambda: DecodeCall("long262k", SEED)),
+    ("long128k_b1", lambda: DecodeCall("long128k_b1", SEED)),
+    ("long128k_b8", lambda: DecodeCall("long128k_b8", SEED)),
+    ("long128k_b64", lambda: DecodeCall("long128k_b64", SEED)),
+    ("hybrid_b1_c1024", lambda: Step(1, 1024, SEED)),
+    ("hybrid_b1_c4096", lambda: Step(1, 4096, SEED)),
+    ("hybrid_b8_c1024", lambda: Step(8, 1024, SEED)),
+    ("hybrid_b8_c4096", lambda: Step(8, 4096, SEED)),
+    ("hybrid_b64_c1024", lambda: Step(64, 1024, SEED)),
+]
+
+
+def survey_workloads(peak, steps=10, warmup=3, names=None):
+    """Each workload of SURVEY built, captured and timed like the headline:
+    its step throughput (GB/s, fraction of the HBM peak, attended KV tokens/s)
+    and the roofline of its dominant call (cached K/V bytes / that call's
+    CUDA-event time). Device memory is released between workloads."""
+    out = {}
+    for name, make in SURVEY:
+        if names is not None and name not in names:
+            continue
+        step = make()
+        step.capture()
+        t = time_graph(step, steps, warmup, 1)
+        per = time_layers(step, steps)
+        t_dom = statistics.mean(per[l] for l in step.dominant)
+        achieved = step.dominant_kv_bytes / t_dom / 1e9
+        v = step.bytes_step * steps / t / 1e9
+        entry = {"value": v, "unit": "GB/s", "frac": v / peak,
+                 "attended_kv_tokens_per_s": step.tokens_step * steps / t,
+                 "us_per_step": t / steps * 1e6,
+                 "l2": "flushed before each step" if step.flush_l2 else "step larger than L2",
+                 "roofline": {"bound": "hbm", "kernel": step.kernel, "achieved": achieved, "peak": peak,
+                              "unit": "GB/s", "frac": achieved / peak, "us_per_call": t_dom * 1e6},
+                 "config": step.config}
+        out[name] = entry
+        del step
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
 
 
 def time_layers(step, K):
@@ -598,13 +692,17 @@ def sample_bytes_tokens(sample):
 
 
 def cpu_baseline(step, budget_s=15.0):
-    """The fp64 oracle timed on a bounded sample of the workload."""
+    """The fp64 oracle timed on a bounded sample of the workload. The oracle
+    threads over (stream, KV head) items; the hybrid step's sample takes
+    enough streams to give every host thread one item."""
     import oracle as oracle_pkg
     o = oracle_pkg.get()
+    hw = o.hardware_threads()
     if isinstance(step, Step):
-        sample = oracle_sample_inputs(step, [0, 1], list(range(28)))
-        what = f"2 of {step.B} streams x all 28 layers"
-        items = 2 * HKV
+        ns = max(1, min(step.B, -(-hw // HKV)))
+        sample = oracle_sample_inputs(step, list(range(ns)), list(range(28)))
+        what = f"{ns} of {step.B} streams x all 28 layers"
+        items = ns * HKV
     else:
         sample, what = step.oracle_sample()
         items = step.Hkv
@@ -617,11 +715,10 @@ def cpu_baseline(step, budget_s=15.0):
         oracle_pass(o, sample)
     t = (time.perf_counter() - t0) / reps
     by, tok = sample_bytes_tokens(sample)
-    cores = min(o.hardware_threads(), items)
-    return {"value": by / t / 1e9, "unit": "GB/s", "tokens_per_s": tok / t, "cores": cores,
-            "kind": "oracle",
-            "sample": f"{what} (the oracle threads over (stream, KV head): {items} work items), "
-                      f"{reps} passes of {t:.3f} s"}
+    return {"value": by / t / 1e9, "unit": "GB/s", "tokens_per_s": tok / t, "cores": hw,
+            "threads_used": min(hw, items), "kind": "oracle",
+            "sample": f"{what} (the oracle threads over (stream, KV head): {items} work items on "
+                      f"{min(hw, items)} of the host's {hw} hardware threads), {reps} passes of {t:.3f} s"}
 
 
 # ---------------------------------------------------------------- arms
@@ -633,8 +730,11 @@ def run_reference(args, world, rank):
     import oracle as oracle_pkg
     import synth
     o = oracle_pkg.get()
-    # one stream of the workload's first four layers (3 sliding + 1 full) per step
-    cases = [synth.hybrid_layer(SEED, l, 1, CONTEXT) for l in range(4)]
+    hw = o.hardware_threads()
+    # the workload's first four layers (3 sliding + 1 full) per step, with
+    # enough streams that every host thread has a (stream, KV head) item
+    ns = max(1, min(B_STREAMS, -(-hw // HKV)))
+    cases = [synth.hybrid_layer(SEED, l, ns, CONTEXT) for l in range(4)]
     sample = []
     for c in cases:
         x, ca = c.inputs, c.cache
@@ -659,11 +759,11 @@ def run_reference(args, world, rank):
             "ms_per_step": t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": "hybrid 28-layer decode step (8 q / 2 KV heads, head_dim 256), "
-                                   "sampled: 1 stream x layers 0-3 (3 sliding + 1 full) at context 4096",
+                                   f"sampled: {ns} stream(s) x layers 0-3 (3 sliding + 1 full) at context 4096",
                        "context": CONTEXT},
             "attended_kv_tokens_per_s": tok * args.steps / t,
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": min(o.hardware_threads(), HKV), "kind": "oracle",
-                             "sample": "1 stream x layers 0-3 per step"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": hw, "threads_used": min(hw, ns * HKV),
+                             "kind": "oracle", "sample": f"{ns} stream(s) x layers 0-3 per step"},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -697,16 +797,14 @@ def run_dattn(args, world, rank, local):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     base = cpu_baseline(step) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    surveyed = None
+    if rank == 0 and world == 1 and args.workload == "hybrid" and not args.no_survey:
+        peak0, _ = peak_hbm()
+        del step.graph
+        surveyed = survey_workloads(peak0)
     if rank != 0:
         return
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
-        try:
-            with open(tpath) as f:
-                traffic = json.load(f).get(args.workload)
-        except (OSError, ValueError, AttributeError):
-            traffic = None
+    traffic = recorded_traffic(args.workload)
     config = dict(step.config)
     config.update({"l2": ("flushed (256 MiB write) before every step" if step.flush_l2 else
                           f"inputs larger than L2: {bytes_step / 1e9:.3f} GB per step vs 129 MB L2"),
@@ -733,6 +831,7 @@ def run_dattn(args, world, rank, local):
         "e2e": e2e,
         "gpu_launches": step.launches_per_step() * args.steps,
         "clocks": clk,
+        "workloads": surveyed,
     }
     print(json.dumps(line), flush=True)
 
@@ -745,6 +844,8 @@ def main():
     ap.add_argument("--impl", default="dattn", choices=["dattn", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
+    ap.add_argument("--no-survey", action="store_true",
+                    help="skip timing the other workloads (reported under \"workloads\")")
     ap.add_argument("--streams", type=int, default=B_STREAMS,
                     help="streams per GPU (smaller values make short profiling runs)")
     ap.add_argument("--context", type=int, default=CONTEXT)

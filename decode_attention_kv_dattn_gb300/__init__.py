@@ -76,9 +76,13 @@ lib.dattn_destroy.restype = None
 lib.dattn_decode_noalloc.argtypes = [ctypes.POINTER(Config), _int, ctypes.POINTER(Cache),
                                      ctypes.POINTER(DecodeArgs), _vp]
 lib.dattn_decode_noalloc.restype = _int
+lib.dattn_debug_config.argtypes = [_vp, _int, ctypes.c_uint]
+lib.dattn_debug_config.restype = _int
+DEBUG_WITHHOLD_Q = 1
 
 EXPORTS = ("dattn_create", "dattn_append_kv", "dattn_decode", "dattn_verify",
-           "dattn_get_error", "dattn_error_string", "dattn_destroy", "dattn_decode_noalloc")
+           "dattn_get_error", "dattn_error_string", "dattn_destroy", "dattn_decode_noalloc",
+           "dattn_debug_config")
 
 
 class DattnError(RuntimeError):
@@ -182,6 +186,11 @@ class Handle:
                           _ptr(gate), _ptr(out), int(max_prefix_len), int(write_back))
         _check(lib.dattn_verify(self._h, layer, ctypes.byref(cache), ctypes.byref(args),
                                 _stream_ptr(stream)), "dattn_verify")
+
+    def debug_config(self, flags=0, wait_limit_us=0):
+        """Testing aid: the limit of the device's bounded waits and fault
+        injection on the host's side of the wait (see dattn_debug_config)."""
+        _check(lib.dattn_debug_config(self._h, int(flags), int(wait_limit_us)), "dattn_debug_config")
 
     def get_error(self, stream=None) -> int:
         """Synchronize the stream; return and clear the sticky device status."""

@@ -1,15 +1,13 @@
-// Host side of the dattn C ABI: argument checks, the split-K plan, the
-// workspace, and the launch sequence of each call.
+// Host side of the dattn C ABI: argument checks, the workspace, the split
+// plan and the launches of each call.
 //
-// A decode call is three launches on the caller's stream, each a programmatic
-// dependent of the previous one:
-//   1. rope      - rotates q (fp32, pre-scaled) and k (bf16 entry) at pos;
-//   2. split     - S CTAs per (stream, KV head) stream the cached K/V through
-//                  shared memory and leave partial softmax states (m, l, o);
-//   3. combine   - merges the partials, joins the new token in score space,
-//                  applies the gate, stores fp32 and writes the new entry back.
-// The new entry is written in (3), after (2) has completed: when a ring is
-// full the new entry takes the oldest token's slot, which (2) still reads.
+// A decode call is one kernel launch (decode_kernel): RoPE of the new token,
+// the pass over the cached keys, the join in score space, the gate, the fp32
+// store and the write-back of the new entry, which comes after every read of
+// the cache (when a ring is full the new entry takes the oldest slot). A
+// verify call is three launches (the RoPE prologue, the tensor-core pass over
+// the prefix, the combine with the tree part), each a programmatic dependent
+// of the one before.
 #include <algorithm>
 #include <cmath>
 #include <cstdlib>
@@ -67,6 +65,8 @@ struct dattn_handle {
   float* vpart = nullptr;   // verify partials: [sms + units][G*T][D+4]
   size_t vpart_slots = 0;
   int* err = nullptr;
+  uint64_t wait_ns = kDefaultWaitNs;  // limit of the kernels' bounded waits
+  int debug_flags = 0;                // dattn_debug_config
 };
 
 namespace {
@@ -98,16 +98,6 @@ int cuda_status(cudaError_t e) {
     return DATTN_EUNSUPPORTED;
   }
   return DATTN_ECUDA;
-}
-
-// Decode grid: every resident CTA, but at least 4 stage tiles (one per warp)
-// per CTA for the largest amount of work this call may have.
-int plan_decode_ctas(const dattn_handle* h, int units, int n_max, int tile_keys) {
-  const int64_t tiles = static_cast<int64_t>(units) * ((n_max + tile_keys - 1) / tile_keys);
-  int64_t ctas = (tiles + 3) / 4;
-  if (ctas > h->decode_resident) ctas = h->decode_resident;
-  if (ctas < 1) ctas = 1;
-  return static_cast<int>(ctas);
 }
 
 CacheView make_view(const dattn_handle* h, const dattn_layer_config& L, const dattn_cache* c) {
@@ -271,6 +261,13 @@ void dattn_destroy(dattn_t* h) {
   delete h;
 }
 
+int dattn_debug_config(dattn_t* h, int flags, unsigned wait_limit_us) {
+  if (!h || (flags & ~DATTN_DEBUG_WITHHOLD_Q) != 0) return DATTN_EINVAL;
+  h->debug_flags = (flags & DATTN_DEBUG_WITHHOLD_Q) ? kDebugWithholdQ : 0;
+  h->wait_ns = wait_limit_us ? static_cast<uint64_t>(wait_limit_us) * 1000ull : kDefaultWaitNs;
+  return DATTN_OK;
+}
+
 int dattn_get_error(dattn_t* h, dattn_stream_t stream) {
   if (!h) return DATTN_EINVAL;
   DeviceGuard guard(h->device);
@@ -352,7 +349,7 @@ int dattn_decode(dattn_t* h, int layer, const dattn_cache* cache, const dattn_de
   if (!guard.ok) return DATTN_ECUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-  const int ctas = plan_decode_ctas(h, B * h->Hkv, n_max, decode_tile_keys(h->D, h->G));
+  const int ctas = plan_decode_ctas(h->decode_resident, B * h->Hkv, n_max, decode_tile_keys(h->D, h->G));
   if (static_cast<size_t>(ctas) + static_cast<size_t>(B) * h->Hkv > h->part_units) return DATTN_EXCEEDS;
   DecodeArgs da{};
   da.c = make_view(h, L, cache);
@@ -376,6 +373,8 @@ int dattn_decode(dattn_t* h, int layer, const dattn_cache* cache, const dattn_de
   da.counters = h->counters[half];
   da.err = h->err;
   da.early = !prev_launch_writes(stream, cache->k);
+  da.wait_ns = h->wait_ns;
+  da.debug_flags = h->debug_flags;
   rc = cuda_status(launch_decode(da, h->D, ctas, s));
   if (rc == DATTN_OK) {
     record_launch(stream, args->write_back ? cache->k : nullptr);

@@ -27,11 +27,12 @@
 //    memory; the CTA that finishes a unit's last segment (a per-unit counter)
 //    merges them with the new token's score, applies the gate, stores the
 //    output and writes the new entry back - after every read of the cache.
-//  * RoPE. At a segment start the CTA rotates the unit's G query heads (fp32,
-//    pre-scaled by log2(e)/sqrt(D)); the cos/sin of each pair come from an
-//    exact fixed-point phase and an fp32 polynomial (rope_cos_sin). The
-//    combining CTA rotates the new key with the same cos/sin and rounds it to
-//    bf16 from fp64 - the exact entry that is scored and stored.
+//  * RoPE. A helper warp rotates each unit's G query heads one segment ahead
+//    (fp32, pre-scaled by log2(e)/sqrt(D)); the cos/sin of each pair come from
+//    an exact fixed-point phase and an fp32 polynomial (rope_cos_sin). It
+//    rotates the new key with the same cos/sin and rounds it to the bf16
+//    nearest the exact rotation (fp32 error terms, an integer fallback near a
+//    bf16 midpoint: bf16_dot2) - the entry that is scored and stored.
 //  * Loads. Each warp owns a ring of NS stage buffers. One lane issues tensor
 //    TMA copies (16 rows of a group, 128-byte swizzle: one 3D box for both
 //    64-dim regions at D = 128, one 2D box per region at D = 256) for the
@@ -730,8 +731,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     fill(0);  // window 1 is filled once the first tiles are requested
 
     const uint64_t policy = l2_evict_first_policy();
+    // Stages with copies in flight (bit st, kept by the issuing lane) and the
+    // parity of each stage's next wait (bit 8 + st): a warp that gave up
+    // waiting still lets its copies land before the CTA exits.
+    uint32_t copies = 0;
     // Request tile x of this warp into stage x % NS (one lane).
     auto issue = [&](int x) {
+      copies |= 1u << (x % NS);
       const int* wr = wrow + ((x / kWin) & 1) * kWin * KG + (x % kWin) * KG;
       const int* wm = wmask + ((x / kWin) & 1) * kWin * KG + (x % kWin) * KG;
       int gn = 0;
@@ -799,7 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 
       // ---- the unit's rotated q from the helper, as B fragments: column n =
       // fg of tile t holds one head's hi or lo part
-      if (!failed) check(mbar_wait_bounded(prep_full, seg & 1));
+      if (!failed) check(mbar_wait_bounded(prep_full, seg & 1, a.wait_ns));
       uint32_t qb[KSTEPS][NT][2];
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
@@ -839,7 +845,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         if (held >= 0) {
           bool ready;
           if (held == it) {
-            if (!failed) check(mbar_wait_bounded(merge_empty, (seg - 1) & 1));
+            if (!failed) check(mbar_wait_bounded(merge_empty, (seg - 1) & 1, a.wait_ns));
             ready = true;
           } else {
             ready = __shfl_sync(kFull, mbar_test_wait(merge_empty, (seg - 1) & 1) ? 1 : 0, 0) != 0;
@@ -850,7 +856,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           }
         }
         const int stg = it % NS;
-        if (!failed) check(mbar_wait_bounded(bar0 + 8 * stg, (it / NS) & 1));
+        if (!failed) {
+          check(mbar_wait_bounded(bar0 + 8 * stg, (it / NS) & 1, a.wait_ns));
+          copies &= ~(1u << stg);
+          copies ^= 0x100u << stg;
+        }
         if (!failed) {
           const int* wm = wmask + ((it / kWin) & 1) * kWin * KG + (it % kWin) * KG;
 #pragma unroll
@@ -983,7 +993,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         l_run[e] += __shfl_xor_sync(kFull, l_run[e], 16);
       }
       if (seg > 0) {
-        if (!failed) check(mbar_wait_bounded(merge_empty, (seg - 1) & 1));
+        if (!failed) check(mbar_wait_bounded(merge_empty, (seg - 1) & 1, a.wait_ns));
         if (held >= 0) {
           if (lane == 0 && !failed) issue(held);
           held = -1;
@@ -1018,6 +1028,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       __syncwarp();
       if (lane == 0) mbar_arrive(merge_full);
     }
+    // copies still in flight exist only after a wait gave up: let them land
+    if (lane == 0)
+      for (int st = 0; st < NS; ++st)
+        if ((copies >> st) & 1u) mbar_wait_bounded(bar0 + 8 * st, (copies >> (8 + st)) & 1u, a.wait_ns);
+    __syncwarp();
   } else {
     // ================= helper warp: the units' inputs, RoPE and new token one
     // segment ahead; the end of every segment but the CTA's last
@@ -1049,12 +1064,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     // rotated q of the CTA's k-th unit into qs (then PREP_FULL), its new token into its slot
     auto prep = [&](int k) {
       const int sl = k & 1;
-      if (!failed) check(mbar_wait_bounded(inbar + 8 * sl, (k >> 1) & 1));
+      if (!failed) check(mbar_wait_bounded(inbar + 8 * sl, (k >> 1) & 1, a.wait_ns));
       uint8_t* slot = in_slots + sl * Gm::IN_BYTES;
       prep_q<D, GP, 32>(a, reinterpret_cast<const uint16_t*>(slot + Gm::IN_Q), sl ? pos_s[1] : pos_s[0], step,
                         qs, cs, lane);
       __syncwarp();
-      if (lane == 0) mbar_arrive(prep_full);
+      // (a testing aid can withhold the first unit's q, so that every
+      // streaming warp's bounded wait for it runs out)
+      if (lane == 0 && !(k == 0 && (a.debug_flags & kDebugWithholdQ))) mbar_arrive(prep_full);
       prep_token<D, GP, 32>(a, qs, cs, slot, sl ? gate_s[1] : gate_s[0], lane);
     };
     if (u_first < U) {
@@ -1068,10 +1085,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       const int un = next_unit(u);
       if (un >= U) break;  // the CTA's last segment is ended by the whole CTA
       // the next unit's q, once every streaming warp has read this one's
-      if (!failed) check(mbar_wait_bounded(prep_empty, seg & 1));
+      if (!failed) check(mbar_wait_bounded(prep_empty, seg & 1, a.wait_ns));
       prep(seg + 1);
       // this segment's end
-      if (!failed) check(mbar_wait_bounded(merge_full, seg & 1));
+      if (!failed) check(mbar_wait_bounded(merge_full, seg & 1, a.wait_ns));
       end_segment<D, NT, PAGED, 32>(a, sp, pieces, u, seg == 0, cta, smem, ML, SLOT,
                                     in_slots + (seg & 1) * Gm::IN_BYTES, flag, lane, wait_prev, [&] {
                                       fence_proxy_async_smem();
@@ -1103,7 +1120,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     const int pos = a.pos[b];
     const uint16_t gr =
         (a.gate && threadIdx.x < a.G) ? a.gate[(static_cast<int64_t>(b) * Hkv + j) * a.G + threadIdx.x] : 0;
-    if (!mbar_wait_bounded(inbar + 8 * (n & 1), (n >> 1) & 1)) raise_error(a.err, ERR_TIMEOUT);
+    if (!mbar_wait_bounded(inbar + 8 * (n & 1), (n >> 1) & 1, a.wait_ns)) raise_error(a.err, ERR_TIMEOUT);
     uint8_t* slot = in_slots + (n & 1) * Gm::IN_BYTES;
     prep_q<D, GP, kThreads>(a, reinterpret_cast<const uint16_t*>(slot + Gm::IN_Q), pos, step, qs, cs, threadIdx.x);
     __syncthreads();
@@ -1118,19 +1135,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 // ---------------------------------------------------------------- launch
 
 template <int D, int NT, bool PAGED>
-cudaError_t decode_launch(const DecodeArgs& a, int ctas, cudaStream_t s) {
+cudaError_t decode_launch(const DecodeArgs& a, int ctas, cudaStream_t s, bool pdl) {
   using Gm = Geo<D, NT>;
   auto k = decode_kernel<D, NT, PAGED>;
   static std::atomic<uint64_t> opted{0};
   const cudaError_t e = opt_in_smem(k, Gm::SMEM_MAX, opted);
   if (e != cudaSuccess) return e;
   const size_t smem = 1024 + Gm::TAB_OFF + (4 * a.B * a.Hkv + 1) * sizeof(int);
+  if (!pdl) {
+    k<<<ctas, kThreads, smem, s>>>(a);
+    return cudaGetLastError();
+  }
   return launch_pdl(k, dim3(ctas), dim3(kThreads), smem, s, a);
 }
 
 template <int D, int NT>
-cudaError_t decode_dispatch_paged(const DecodeArgs& a, int ctas, cudaStream_t s) {
-  return a.c.paged ? decode_launch<D, NT, true>(a, ctas, s) : decode_launch<D, NT, false>(a, ctas, s);
+cudaError_t decode_dispatch_paged(const DecodeArgs& a, int ctas, cudaStream_t s, bool pdl) {
+  return a.c.paged ? decode_launch<D, NT, true>(a, ctas, s, pdl) : decode_launch<D, NT, false>(a, ctas, s, pdl);
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -1179,18 +1200,19 @@ cudaError_t encode_cache_maps(const CacheView& c, int Hkv, int D, CUtensorMap* k
   return cudaSuccess;
 }
 
-cudaError_t launch_decode(const DecodeArgs& args, int D, int ctas, cudaStream_t s) {
+cudaError_t launch_decode(const DecodeArgs& args, int D, int ctas, cudaStream_t s, bool pdl) {
   DecodeArgs a = args;
   a.unit_cost = kSegmentCost;
+  if (a.wait_ns == 0) a.wait_ns = kDefaultWaitNs;
   const int GP = decode_group_pad(a.G);
   if (a.B * a.Hkv > kMaxUnits) return cudaErrorNotSupported;
   if (a.r > D || a.r % 2 != 0) return cudaErrorNotSupported;
   if (D == 256) {
-    if (GP == 4) return decode_dispatch_paged<256, 1>(a, ctas, s);
-    if (GP == 8) return decode_dispatch_paged<256, 2>(a, ctas, s);
+    if (GP == 4) return decode_dispatch_paged<256, 1>(a, ctas, s, pdl);
+    if (GP == 8) return decode_dispatch_paged<256, 2>(a, ctas, s, pdl);
   } else if (D == 128) {
-    if (GP == 4) return decode_dispatch_paged<128, 1>(a, ctas, s);
-    if (GP == 8) return decode_dispatch_paged<128, 2>(a, ctas, s);
+    if (GP == 4) return decode_dispatch_paged<128, 1>(a, ctas, s, pdl);
+    if (GP == 8) return decode_dispatch_paged<128, 2>(a, ctas, s, pdl);
   }
   return cudaErrorNotSupported;
 }

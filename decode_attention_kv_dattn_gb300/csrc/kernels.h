@@ -23,6 +23,12 @@ inline uint64_t rope_phase_step(double theta, int r, int i) {
 // Sticky device error bits (see dattn_get_error).
 enum : int { ERR_INDEX = 1, ERR_TIMEOUT = 2, ERR_LENGTH = 4, ERR_RANGE = 8 };
 
+// Limit of a bounded device wait unless the handle sets another (2 s).
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+// Testing aid (dattn_debug_config): the decode kernel's helper warp withholds
+// the first unit's rotated query, so the streaming warps' waits run out.
+constexpr int kDebugWithholdQ = 1;
+
 // One layer's cache as the kernels see it.
 struct CacheView {
   uint16_t* k;                 // ring [n_rows, Hkv, R, D] / paged [pages, Hkv, P, D]
@@ -94,6 +100,8 @@ struct DecodeArgs {
                                // start before it completes
   int unit_cost;               // fixed cost of one segment of a unit, in stage tiles
                                // (set by launch_decode)
+  uint64_t wait_ns;            // limit of every bounded wait (0 = kDefaultWaitNs)
+  int debug_flags;             // kDebugWithholdQ: see dattn_debug_config
 };
 
 struct AppendArgs {
@@ -144,10 +152,23 @@ struct VerifyCombineArgs {
   int* err;
 };
 
+// Decode grid: every resident CTA (`resident` on the whole GPU), but at
+// least 4 stage tiles (one per streaming warp) per CTA for the largest amount
+// of work the call may have: `units` units of up to `n_max` keys each.
+inline int plan_decode_ctas(int resident, int units, int n_max, int tile_keys) {
+  const int64_t tiles = static_cast<int64_t>(units) * ((n_max + tile_keys - 1) / tile_keys);
+  int64_t ctas = (tiles + 3) / 4;
+  if (ctas > resident) ctas = resident;
+  if (ctas < 1) ctas = 1;
+  return static_cast<int>(ctas);
+}
+
 // Each returns cudaErrorNotSupported for a shape with no compiled kernel.
 cudaError_t launch_rope(const RopeArgs& a, cudaStream_t s);
-// Decode with `ctas` CTAs (at most decode_ctas_per_sm per SM).
-cudaError_t launch_decode(const DecodeArgs& a, int D, int ctas, cudaStream_t s);
+// Decode with `ctas` CTAs (at most decode_ctas_per_sm per SM). With pdl the
+// launch is a programmatic dependent of the previous one on the stream;
+// without, it starts once everything before it on the stream has completed.
+cudaError_t launch_decode(const DecodeArgs& a, int D, int ctas, cudaStream_t s, bool pdl = true);
 // Tensor maps of a cache's K and V for the decode kernel over its [n_rows *
 // Hkv * (R or P), D] bf16 rows, 128-byte swizzle: at D = 128 seen as (64 dims,
 // row, 2 regions) with one box per 16-row group; at D = 256 as [rows, D] with

@@ -14,13 +14,17 @@
 //
 // The array is created when the library's module is loaded on a device and
 // stays there until the process exits. All calls on a device share it and it
-// keeps the last call's contents; every call rewrites what it reads (and
-// clears its error word and counters first), but two calls that run on the
-// GPU at the same time - on different streams, or not ordered on one stream -
-// race on it.
+// keeps the last call's contents. Every call starts with a small set-up kernel
+// that clears the error word and the segment counters (the decode kernel
+// needs them at zero) and writes the layer's RoPE phase steps, which it
+// receives by value in its kernel parameters - no host buffer has to outlive
+// the call. Two calls that run on the GPU at the same time - on different
+// streams, or not ordered on one stream - race on the array.
 //
-// The kernel is the same one dattn_decode launches; only where its scratch
-// lives differs.
+// The decode kernel is the same one dattn_decode launches; only where its
+// scratch lives differs, and it is launched as an ordinary (not a
+// programmatic-dependent) launch, so it starts after the set-up kernel has
+// completed.
 #include <cmath>
 #include <mutex>
 
@@ -47,6 +51,24 @@ DeviceScratch g_devices[kMaxDevices];
 std::mutex g_mutex;
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+constexpr int kMaxPhaseSteps = 128;  // r / 2 for r <= 256
+
+// Everything the set-up kernel writes, passed by value.
+struct NoAllocSetup {
+  uint64_t step[kMaxPhaseSteps];  // RoPE phase steps of the layer
+  uint64_t* step_dst;
+  int half;                       // r / 2
+  int* err;
+  int* counters;
+  int n_counters;
+};
+
+__global__ void __launch_bounds__(256) noalloc_setup_kernel(const __grid_constant__ NoAllocSetup p) {
+  for (int i = threadIdx.x; i < p.half; i += blockDim.x) p.step_dst[i] = p.step[i];
+  for (int i = threadIdx.x; i < p.n_counters; i += blockDim.x) p.counters[i] = 0;
+  if (threadIdx.x == 0) *p.err = 0;
+}
 
 }  // namespace
 
@@ -106,12 +128,11 @@ extern "C" DATTN_API int dattn_decode_noalloc(const dattn_config* cfg, int layer
   const int tile_keys = decode_tile_keys(D, G);
   const int resident = ds.sms * decode_ctas_per_sm(D, G);
   if (tile_keys <= 0 || resident <= 0) return DATTN_EUNSUPPORTED;
-  int64_t ctas = (static_cast<int64_t>(B) * Hkv * ((n_max + tile_keys - 1) / tile_keys) + 3) / 4;
-  if (ctas > resident) ctas = resident;
-  if (ctas < 1) ctas = 1;
+  const int ctas = plan_decode_ctas(resident, B * Hkv, n_max, tile_keys);
 
   // ---- carve the scratch; reject what does not fit
   const int half = L.rotary_dim / 2;
+  if (half > kMaxPhaseSteps) return DATTN_EUNSUPPORTED;
   size_t off = 0;
   const size_t err_off = off;
   off = align256(off + sizeof(int));
@@ -138,26 +159,24 @@ extern "C" DATTN_API int dattn_decode_noalloc(const dattn_config* cfg, int layer
   cv.block_table = cache->block_table;
   cv.bt_stride = cache->bt_stride;
   cv.seq_len = cache->seq_len;
-  // the split pass reads the cache through tensor maps (host-side encoding)
   // the kernel reads the cache through tensor maps (host-side encoding)
   DecodeArgs da{};
   if (encode_cache_maps(cv, Hkv, D, &da.tmap_k, &da.tmap_v) != cudaSuccess) return DATTN_EUNSUPPORTED;
 
   uint64_t* rope_step = half > 0 ? reinterpret_cast<uint64_t*>(ds.base + freq_off) : nullptr;
-  // The error word accumulates bits and the segment counters must start at
-  // zero, so both are cleared every call; the RoPE phase-step table is
-  // rewritten from the host.
   int* counters = reinterpret_cast<int*>(ds.base + counters_off);
-  if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return DATTN_ECUDA;
-  if (cudaMemsetAsync(counters, 0, static_cast<size_t>(B) * Hkv * sizeof(int), s) != cudaSuccess)
-    return DATTN_ECUDA;
-  if (half > 0) {
-    uint64_t f[128];
-    if (half > 128) return DATTN_EUNSUPPORTED;
-    for (int i = 0; i < half; ++i) f[i] = rope_phase_step(L.rope_theta, L.rotary_dim, i);
-    if (cudaMemcpyAsync(rope_step, f, half * sizeof(uint64_t), cudaMemcpyHostToDevice, s) != cudaSuccess)
-      return DATTN_ECUDA;
-  }
+  // The error word accumulates bits and the segment counters must start at
+  // zero, so both are cleared every call, and the RoPE phase steps are
+  // rewritten, by one set-up kernel that holds the steps in its parameters.
+  NoAllocSetup setup{};
+  for (int i = 0; i < half; ++i) setup.step[i] = rope_phase_step(L.rope_theta, L.rotary_dim, i);
+  setup.step_dst = rope_step;
+  setup.half = half;
+  setup.err = err;
+  setup.counters = counters;
+  setup.n_counters = B * Hkv;
+  noalloc_setup_kernel<<<1, 256, 0, s>>>(setup);
+  if (cudaGetLastError() != cudaSuccess) return DATTN_ECUDA;
 
   da.c = cv;
   da.B = B;
@@ -178,7 +197,7 @@ extern "C" DATTN_API int dattn_decode_noalloc(const dattn_config* cfg, int layer
   da.counters = counters;
   da.err = err;
   da.early = !prev_launch_writes(stream, cache->k);
-  const cudaError_t e = launch_decode(da, D, static_cast<int>(ctas), s);
+  const cudaError_t e = launch_decode(da, D, ctas, s, /*pdl=*/false);
   if (e != cudaSuccess) return e == cudaErrorNotSupported ? DATTN_EUNSUPPORTED : DATTN_ECUDA;
   record_launch(stream, args->write_back ? cache->k : nullptr);
   return DATTN_OK;

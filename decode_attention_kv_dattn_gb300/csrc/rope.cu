@@ -146,7 +146,8 @@ __global__ void __launch_bounds__(kRopeThreads) append_kernel(const AppendArgs a
   const int t = blockIdx.x, b = blockIdx.y;
   const CacheView& c = a.c;
   const int cnt = a.count[b];
-  if (cnt < 0 || cnt > a.Tmax) {
+  // a ring row takes at most R tokens per call, so no slot is written twice
+  if (cnt < 0 || cnt > a.Tmax || (!c.paged && cnt > c.R)) {
     if (t == 0 && threadIdx.x == 0) raise_error(a.err, ERR_INDEX);
     return;
   }

@@ -167,9 +167,10 @@ DATTN_API int dattn_create(const dattn_config* cfg, int device, dattn_t** out);
 /* Bulk write (prefill or cache set-up): token t < count[b] of call row b goes
  * to cache index start_index[b] + t (ring: slot (start_index[b] + t) mod R of
  * row stream_rows[b]; paged: offset idx % P of page block_table[b][idx / P]).
- * k, v = [B, max_tokens, Hkv, D] bf16. When rotate != 0 the key is turned at
- * position start_pos[b] + t and rounded to bf16 (nearest-even, from fp64) -
- * the same entry decode writes back. start_index, start_pos, count: [B]. */
+ * k, v = [B, max_tokens, Hkv, D] bf16. A ring row takes at most R tokens per
+ * call (count[b] > R is reported as DATTN_EINDEX and writes nothing for b). When rotate != 0 the key is turned at
+ * position start_pos[b] + t and rounded to the bf16 nearest the exact
+ * rotation (ties to even) - the same entry decode writes back. start_index, start_pos, count: [B]. */
 DATTN_API int dattn_append_kv(dattn_t* h, int layer, const dattn_cache* cache, int num_streams,
                     int max_tokens, const int32_t* start_index, const int32_t* start_pos,
                     const int32_t* count, const void* k, const void* v, int rotate,
@@ -196,6 +197,22 @@ DATTN_API int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, cons
  * first found in that order of severity). */
 DATTN_API int dattn_get_error(dattn_t* h, dattn_stream_t stream);
 
+/* Testing aid for the failure path (no counterpart on the pages): every
+ * device wait of the library is bounded, and one that runs out ends the call
+ * with DATTN_ETIMEOUT from dattn_get_error instead of hanging the GPU.
+ *   wait_limit_us - limit of the handle's bounded waits in microseconds for
+ *                   its later decode calls (0 = the default, 2 s).
+ *   flags         - DATTN_DEBUG_WITHHOLD_Q: in each later decode call, the
+ *                   kernel's helper warp withholds every CTA's first rotated
+ *                   query, so the streaming warps' waits for it run out after
+ *                   the limit. The call still completes (the copies it issued
+ *                   land before it exits) and the context stays usable; the
+ *                   output and any write-back of that call are undefined.
+ *                   0 restores normal operation.
+ * Returns DATTN_EINVAL for a null handle or an unknown flag. */
+enum { DATTN_DEBUG_WITHHOLD_Q = 1 };
+DATTN_API int dattn_debug_config(dattn_t* h, int flags, unsigned wait_limit_us);
+
 /* Static description of a status code. */
 DATTN_API const char* dattn_error_string(int code);
 
@@ -217,11 +234,14 @@ DATTN_API void dattn_destroy(dattn_t* h);
  *     (about 1.2 MiB for 64 streams x 2 KV heads x 8 query heads x head_dim
  *     256 on a 152-SM GPU).
  *   - All calls on a device share the array, which keeps the last call's
- *     contents; each call rewrites what it uses and clears its error word and
- *     counters, but
- *     calls that overlap on the GPU (other streams, or unordered) race.
- *   - Device-side metadata errors are recorded in the array's error word and
- *     are not returned; only host-side checks produce the status. */
+ *     contents. Each call first runs a small set-up kernel that clears the
+ *     error word and the segment counters and writes the RoPE phase steps
+ *     (passed by value), then the decode kernel; calls that overlap on the
+ *     GPU (other streams, or unordered) race on the array.
+ *   - Device-side metadata errors (a page id outside the pool, a ring head
+ *     outside [0, R), a length above the bound) are recorded in the array's
+ *     error word and are not returned; only host-side checks produce the
+ *     status. The output of a call with such metadata is undefined. */
 DATTN_API int dattn_decode_noalloc(const dattn_config* cfg, int layer, const dattn_cache* cache,
                                    const dattn_decode_args* args, dattn_stream_t stream);
 

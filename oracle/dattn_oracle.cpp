@@ -627,7 +627,8 @@ int oracle_verify(int S, int T, int Hq, int Hkv, int D, int r, double theta,
 // ----- bulk append. Token t (< count[b]) of call row b goes to cache index
 // start_index[b] + t and, when rotate != 0, is rotated at position
 // start_pos[b] + t. k/v are [B, Tmax, Hkv, D]. The caches are updated in place.
-// Ring: index i of row stream_rows[b] is slot i mod R of [n_rows, Hkv, R, D].
+// Ring: index i of row stream_rows[b] is slot i mod R of [n_rows, Hkv, R, D];
+// a call writes at most R tokens per ring row.
 int oracle_append_ring(int B, int Tmax, int Hkv, int D, int r, double theta,
                        uint16_t* k_ring, uint16_t* v_ring, int n_rows, int R,
                        const int32_t* stream_rows, const int32_t* start_index,
@@ -637,11 +638,17 @@ int oracle_append_ring(int B, int Tmax, int Hkv, int D, int r, double theta,
   std::vector<uint16_t> entry(D);
   for (int b = 0; b < B; ++b) {
     const int row = stream_rows ? stream_rows[b] : b;
-    if (row < 0 || row >= n_rows || count[b] < 0 || count[b] > Tmax || start_index[b] < 0) return 2;
+    // at most one ring's worth per call: each slot is written at most once
+    if (row < 0 || row >= n_rows || count[b] < 0 || count[b] > Tmax || count[b] > R || start_index[b] < 0)
+      return 2;
     for (int t = 0; t < count[b]; ++t)
       for (int j = 0; j < Hkv; ++j) {
         const size_t src = ((static_cast<size_t>(b) * Tmax + t) * Hkv + j) * D;
+#if ORACLE_MUTATION == 18
+        const int slot = (start_index[b] + t + 1) % R;  // planted: slot off by one
+#else
         const int slot = (start_index[b] + t) % R;
+#endif
         const size_t dst = ((static_cast<size_t>(row) * Hkv + j) * R + slot) * D;
         if (rotate)
           rope_entry(k + src, D, r, theta, start_pos[b] + t, entry.data());

@@ -249,6 +249,108 @@ def pin_rope_entry_matches_rotation(o):
         assert np.array_equal(ent, want), f"r={r}: {np.sum(ent != want)} entries differ"
 
 
+def _mpf_fraction(x):
+    """The exact rational value of an mpmath number (a binary float)."""
+    from fractions import Fraction
+    sign, man, exp, _ = x._mpf_
+    f = Fraction(int(man)) * (Fraction(2) ** exp if exp >= 0 else Fraction(1, 2 ** (-exp)))
+    return -f if sign else f
+
+
+def _bf16_midpoint_distance(v):
+    """|v| minus its nearest bf16 rounding boundary (a midpoint between two
+    neighbouring bf16 values), as a float; v is a Fraction."""
+    from fractions import Fraction
+    a = abs(v)
+    if a == 0:
+        return float("inf")
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    spacing = Fraction(2) ** (max(e, -126) - 7)
+    units = a / spacing
+    frac = units - units.numerator // units.denominator
+    return float(abs(frac - Fraction(1, 2)) * spacing)
+
+
+def pin_rope_entry_is_rounded_exact_rotation(o):
+    """The K entry against its plain definition: the bf16 nearest (ties to
+    even) to the exact rotation x cos(a) - y sin(a), y cos(a) + x sin(a) with
+    a = pos * theta^(-2i/r), cos and sin to 40 digits (mpmath), the rounding in
+    rational arithmetic. The oracle turns by fp32 cos/sin within COS_SIN_TOL of
+    the exact ones, so an element may differ only where the exact value lies
+    within (|x| + |y|) * COS_SIN_TOL of a bf16 rounding boundary; those
+    exceptions are counted and must stay rare. Covers both layer types and the
+    paged batch's RoPE (r = 256, theta 1e4; r = 64, theta 5e6; r = 128, theta
+    1e6), positions up to 2^21 - 1 and negative ones; dims >= r pass through."""
+    mpmath = __import__("mpmath")
+    mpmath.mp.dps = 40
+    rng = np.random.default_rng(17)
+    D = 256
+    positions = [0, 1, 2, 3, 7, 299, 300, 511, 4095, 4096, 65535, -5, (1 << 21) - 1]
+    positions += [int(p) for p in rng.integers(0, 1 << 21, 12)]
+    checked = near = 0
+    for cfg, (r, theta) in enumerate(((256, 1e4), (64, 5e6), (128, 1e6))):
+        half = r // 2
+        inv = [mpmath.power(mpmath.mpf(theta), mpmath.mpf(-2 * i) / r) for i in range(half)]
+        for n, pos in enumerate(positions):
+            x = rand_bf16(D, 1000 + 100 * cfg + n)
+            xv = bf16_val(x)
+            ent = o.rope_bf16(x, r, theta, pos)
+            assert np.array_equal(ent[r:], x[r:]), f"r={r}: dims past r must pass through"
+            for i in range(half):
+                a = mpmath.mpf(pos) * inv[i]
+                c, s = mpmath.cos(a), mpmath.sin(a)
+                px, py = mpmath.mpf(float(xv[i])), mpmath.mpf(float(xv[i + half]))
+                bound = (abs(float(xv[i])) + abs(float(xv[i + half]))) * COS_SIN_TOL
+                for d, exact in ((i, px * c - py * s), (i + half, py * c + px * s)):
+                    v = _mpf_fraction(exact)
+                    checked += 1
+                    if _bf16_midpoint_distance(v) <= bound:
+                        near += 1  # within the cos/sin error of a rounding boundary
+                        continue
+                    want = _bf16_of_fraction(v)
+                    got = int(ent[d])
+                    if want == 0 and got == 0x8000:
+                        got = 0
+                    assert got == want, (f"r={r} theta={theta} pos={pos} dim {d}: entry {got:#06x}, "
+                                         f"exact rotation rounds to {want:#06x}")
+    assert near <= max(3, checked // 200), f"{near} of {checked} elements near a rounding boundary"
+
+
+def pin_append_ring_places_entries(o):
+    """Bulk append into rings, against a hand-derived slot layout. R = 5 slots,
+    three ring rows, call rows mapped to ring rows 2 and 0. Call row 0 writes
+    tokens 0..3 at indices 3..6, i.e. slots 3, 4, 0, 1 of ring row 2; call row 1
+    writes tokens 0..4 at indices 7..11, i.e. slots 2, 3, 4, 0, 1 of ring row 0
+    (a whole ring, wrapping). Keys are turned at start_pos + t (or copied when
+    rotate is off); every other slot keeps its NaN."""
+    Hkv, D, R, n_rows = 2, 8, 5, 3
+    Kr = np.full((n_rows, Hkv, R, D), NAN, np.uint16)
+    Vr = Kr.copy()
+    k = rand_bf16((2, 5, Hkv, D), 950)
+    v = rand_bf16((2, 5, Hkv, D), 951)
+    where = {(2, 3): (0, 0), (2, 4): (0, 1), (2, 0): (0, 2), (2, 1): (0, 3),
+             (0, 2): (1, 0), (0, 3): (1, 1), (0, 4): (1, 2), (0, 0): (1, 3), (0, 1): (1, 4)}
+    start_pos = [10, 0]
+    for rotate in (True, False):
+        Ko, Vo = o.append_ring(Kr, Vr, [3, 7], start_pos, [4, 5], k, v, 8, 1e4, rotate=rotate,
+                               stream_rows=[2, 0])
+        for row in range(n_rows):
+            for slot in range(R):
+                if (row, slot) not in where:
+                    assert np.all(Ko[row, :, slot] == NAN) and np.all(Vo[row, :, slot] == NAN), \
+                        f"slot ({row}, {slot}) was written"
+                    continue
+                b, t = where[(row, slot)]
+                for j in range(Hkv):
+                    want_k = o.rope_bf16(k[b, t, j], 8, 1e4, start_pos[b] + t) if rotate else k[b, t, j]
+                    assert np.array_equal(Ko[row, j, slot], want_k), f"K at ({row}, {slot}) rotate={rotate}"
+                    assert np.array_equal(Vo[row, j, slot], v[b, t, j]), f"V at ({row}, {slot})"
+
+
 def pin_rope_entry_identity(o):
     """At position 0, and with no rotary dims, the K entry is the key itself."""
     x = rand_bf16(256, 14)

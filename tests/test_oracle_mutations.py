@@ -7,7 +7,8 @@ pairs, frequencies over the wrong width, a wrong score scale, a tree depth off
 by one, a missing tree mask, a page offset off by one, sigmoid(-g), values
 taken from keys, truncation instead of rounding, quarter turns of the RoPE
 phase taken the wrong way, an uncentred phase remainder, the K entry rounded
-from the fp64-rounded sum instead of the exact one. If one of them passed every
+from the fp64-rounded sum instead of the exact one, a ring append slot off by
+one. If one of them passed every
 pin, the pins would not be sharp enough to trust the oracle.
 """
 import pytest
@@ -15,7 +16,7 @@ import pytest
 import oracle as oracle_pkg
 from oracle_pins import ALL_PINS
 
-MUTATIONS = list(range(1, 18))
+MUTATIONS = list(range(1, 19))
 
 
 @pytest.mark.parametrize("mutation", MUTATIONS)

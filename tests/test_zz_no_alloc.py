@@ -41,9 +41,30 @@ def test_noalloc_matches_decode_on_two_calls_in_a_row():
         assert_close(out.cpu().numpy(), ref.cpu().numpy(), "noalloc vs decode")
 
 
+def test_noalloc_write_back_matches_the_oracle(oracle):
+    """With write-back on, the noalloc call stores the oracle's K/V entries bit
+    for bit (only the new tokens' slots change) and its outputs match the
+    oracle, on a ring layer and a paged layer, two calls in a row."""
+    import decode_attention_kv_dattn_gb300 as dattn
+    from gpu_util import check_write_back, host_u16, oracle_decode
+    for case in (synth.single_sliding_layer(0), synth.paged_batched(2, B=8)):
+        dc = DeviceCase(case)
+        h = make_handle(dattn, case)  # only its config is used: no workspace is touched
+        dattn.decode_noalloc(h.config, 0, dc.cache_desc(dattn), dc.q, dc.k_new, dc.v_new, dc.pos, dc.out,
+                             gate=dc.gate, write_back=True)
+        torch.cuda.synchronize()
+        ref, ke, ve = oracle_decode(oracle, case)
+        assert_close(dc.out.cpu().numpy(), ref, "noalloc vs oracle")
+        check_write_back(case, host_u16(dc.k), host_u16(dc.v), ke, ve)
+        h.close()
+
+
 def test_noalloc_rejects_what_does_not_fit():
-    """256 streams of 32 query heads at head_dim 256 need 8 MiB of rotated
-    queries alone: the call is refused before anything is launched."""
+    """256 streams x 4 KV heads are 1024 (stream, KV head) units, more than one
+    decode call takes (512): the call is refused with DATTN_EXCEEDS before
+    anything is launched. Within that limit the largest call's scratch - split
+    partials for 152 CTAs + 512 units of 8 heads x (256 + 2) floats, 5.4 MB -
+    fits the 8 MiB array."""
     import decode_attention_kv_dattn_gb300 as dattn
     B, Hq, Hkv, D, P = 256, 32, 4, 256, 16
     layers = (dattn.LayerConfig * 1)(dattn.LayerConfig(dattn.CACHE_PAGED, 0, P, 64, 5e6))
