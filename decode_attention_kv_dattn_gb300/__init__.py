@@ -120,15 +120,21 @@ def _stream_ptr(stream):
 # ---------------------------------------------------------------- cache descriptors
 
 def ring_cache(k, v, ring_head, ring_count, stream_rows=None) -> Cache:
-    """k, v: [rows, Hkv, R, D] bf16; ring_head, ring_count (, stream_rows): [B] int32."""
-    return Cache(_ptr(k), _ptr(v), k.shape[0], _ptr(ring_head), _ptr(ring_count),
-                 _ptr(stream_rows), None, 0, None)
+    """k, v: [rows, Hkv, R, D] bf16; ring_head, ring_count (, stream_rows): [B] int32.
+    The descriptor holds the tensors it points to, so they live as long as it does."""
+    c = Cache(_ptr(k), _ptr(v), k.shape[0], _ptr(ring_head), _ptr(ring_count),
+              _ptr(stream_rows), None, 0, None)
+    c._tensors = (k, v, ring_head, ring_count, stream_rows)
+    return c
 
 
 def paged_cache(k, v, block_table, seq_len) -> Cache:
-    """k, v: [pages, Hkv, P, D] bf16; block_table [B, max_pages] int32; seq_len [B] int32."""
-    return Cache(_ptr(k), _ptr(v), k.shape[0], None, None, None, _ptr(block_table),
-                 block_table.shape[1], _ptr(seq_len))
+    """k, v: [pages, Hkv, P, D] bf16; block_table [B, max_pages] int32; seq_len [B] int32.
+    The descriptor holds the tensors it points to, so they live as long as it does."""
+    c = Cache(_ptr(k), _ptr(v), k.shape[0], None, None, None, _ptr(block_table),
+              block_table.shape[1], _ptr(seq_len))
+    c._tensors = (k, v, block_table, seq_len)
+    return c
 
 
 # ---------------------------------------------------------------- handle

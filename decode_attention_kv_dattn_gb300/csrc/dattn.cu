@@ -11,6 +11,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdlib>
+#include <cstdio>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -59,7 +60,8 @@ struct dattn_handle {
   int* counters[2] = {nullptr, nullptr};
   unsigned decode_calls = 0;
   float* qhat = nullptr;    // verify: rotated q of the window rows
-  uint16_t* qhat16 = nullptr;  // the same rounded to fp16 (the tensor-core pass's operand)
+  uint16_t* qhl = nullptr;  // the same as bf16 hi and lo planes (the tensor-core pass's operand)
+  int qhl_rows = 0;         // rows of one plane
   int* tiles = nullptr;     // verify: tile prefix over units, from its split pass
   uint16_t* khat = nullptr; // verify: rotated window keys
   float* vpart = nullptr;   // verify partials: [sms + units][G*T][D+4]
@@ -91,8 +93,12 @@ struct DeviceGuard {
   }
 };
 
-int cuda_status(cudaError_t e) {
+// With DATTN_VERBOSE set in the environment, a failed launch names its CUDA
+// error on stderr (the status code alone says only DATTN_ECUDA).
+int cuda_status(cudaError_t e, const char* what = "launch") {
   if (e == cudaSuccess) return DATTN_OK;
+  static const bool verbose = std::getenv("DATTN_VERBOSE") != nullptr;
+  if (verbose) std::fprintf(stderr, "dattn: %s: %s (%s)\n", what, cudaGetErrorName(e), cudaGetErrorString(e));
   if (e == cudaErrorNotSupported) {
     cudaGetLastError();
     return DATTN_EUNSUPPORTED;
@@ -143,7 +149,7 @@ const char* dattn_error_string(int code) {
     case DATTN_ETIMEOUT: return "a bounded device wait timed out";
     case DATTN_EUNSUPPORTED: return "shape not supported: no compiled kernel for it";
     case DATTN_ELENGTH: return "a stream is longer than the call's bound";
-    case DATTN_ERANGE: return "a cached value lies outside the fp16 range the verify pass computes in";
+    case DATTN_ERANGE: return "a cached value lies outside the fp16 range the verify pass forms P V in";
     default: return "unknown dattn status";
   }
 }
@@ -216,7 +222,8 @@ int dattn_create(const dattn_config* cfg, int device, dattn_t** out) {
   const size_t rows = static_cast<size_t>(h->max_streams) *
                       (h->max_verify_rows > 1 ? h->max_verify_rows : 1);
   if (cudaMalloc(&h->qhat, rows * Hq * D * sizeof(float)) != cudaSuccess) return fail(DATTN_ECUDA);
-  if (cudaMalloc(&h->qhat16, rows * Hq * D * sizeof(uint16_t)) != cudaSuccess) return fail(DATTN_ECUDA);
+  h->qhl_rows = static_cast<int>(rows);
+  if (cudaMalloc(&h->qhl, 2 * rows * Hq * D * sizeof(uint16_t)) != cudaSuccess) return fail(DATTN_ECUDA);
   if (cudaMalloc(&h->khat, rows * Hkv * D * sizeof(uint16_t)) != cudaSuccess) return fail(DATTN_ECUDA);
   // Decode partials: one slot per CTA plus one per unit; per-unit counters.
   if (static_cast<int64_t>(h->max_streams) * Hkv > decode_max_units()) return fail(DATTN_EUNSUPPORTED);
@@ -232,7 +239,7 @@ int dattn_create(const dattn_config* cfg, int device, dattn_t** out) {
   for (int i = 0; i < 2; ++i)
     if (cudaMalloc(&h->part[i], part_floats * sizeof(float)) != cudaSuccess) return fail(DATTN_ECUDA);
   if (h->max_verify_rows > 0) {
-    if (G * h->max_verify_rows > 128) return fail(DATTN_EUNSUPPORTED);
+    if (G * h->max_verify_rows > kVerifyMaxRows) return fail(DATTN_EUNSUPPORTED);
     if (static_cast<int64_t>(h->max_streams) * Hkv > kVerifyMaxUnits) return fail(DATTN_EUNSUPPORTED);
     h->vpart_slots = static_cast<size_t>(h->num_sms) + static_cast<size_t>(h->max_streams) * Hkv;
     const size_t vfloats = h->vpart_slots * G * h->max_verify_rows * (D + 4);
@@ -249,7 +256,7 @@ void dattn_destroy(dattn_t* h) {
   DeviceGuard guard(h->device);
   for (uint64_t* p : h->rope_step) cudaFree(p);
   cudaFree(h->qhat);
-  cudaFree(h->qhat16);
+  cudaFree(h->qhl);
   cudaFree(h->khat);
   for (int i = 0; i < 2; ++i) {
     cudaFree(h->part[i]);
@@ -320,7 +327,7 @@ int dattn_append_kv(dattn_t* h, int layer, const dattn_cache* cache, int num_str
   a.rotate = rotate;
   a.rope_step = h->rope_step[layer];
   a.err = h->err;
-  rc = cuda_status(launch_append(a, reinterpret_cast<cudaStream_t>(stream)));
+  rc = cuda_status(launch_append(a, reinterpret_cast<cudaStream_t>(stream)), "append");
   if (rc == DATTN_OK) record_launch(stream, cache->k);
   return rc;
 }
@@ -375,7 +382,7 @@ int dattn_decode(dattn_t* h, int layer, const dattn_cache* cache, const dattn_de
   da.early = !prev_launch_writes(stream, cache->k);
   da.wait_ns = h->wait_ns;
   da.debug_flags = h->debug_flags;
-  rc = cuda_status(launch_decode(da, h->D, ctas, s));
+  rc = cuda_status(launch_decode(da, h->D, ctas, s), "decode");
   if (rc == DATTN_OK) {
     record_launch(stream, args->write_back ? cache->k : nullptr);
     ++h->decode_calls;
@@ -404,6 +411,21 @@ int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, const dattn_ve
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   VerifySplitArgs va{};
   va.c = make_view(h, L, cache);
+  // one CTA per SM, at least one tile each for the largest prefix this call may have
+  const int64_t tiles = static_cast<int64_t>(S) * h->Hkv * ((n_max + kVerifyTileKeys - 1) / kVerifyTileKeys);
+  int64_t ctas = tiles;
+  if (ctas > h->num_sms) ctas = h->num_sms;
+  if (ctas < 1) ctas = 1;
+  va.S = S;
+  va.T = T;
+  va.Hkv = h->Hkv;
+  va.G = h->G;
+  va.qhl = h->qhl;
+  va.ctas = static_cast<int>(ctas);
+  va.max_len = n_max;
+  if (encode_verify_maps(va.c, h->Hkv, h->D, h->qhl, h->qhl_rows, h->Hq, h->G, S, T, &va.tmap_k, &va.tmap_v,
+                         &va.tmap_q) != cudaSuccess)
+    return DATTN_EUNSUPPORTED;
 
   RopeArgs ra{};
   ra.rows = S * T;
@@ -419,28 +441,17 @@ int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, const dattn_ve
   ra.rope_step = h->rope_step[layer];
   ra.q_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(h->D)));
   ra.qhat = h->qhat;
-  ra.qhat16 = h->qhat16;
+  ra.qhl = h->qhl;
+  ra.qhl_rows = h->qhl_rows;
   ra.khat = h->khat;
   ra.err = h->err;
-  rc = cuda_status(launch_rope(ra, s));
+  rc = cuda_status(launch_rope(ra, s), "verify prologue");
   if (rc != DATTN_OK) return rc;
 
-  // one CTA per SM, at least two tiles each for the largest prefix this call may have
-  const int64_t tiles = static_cast<int64_t>(S) * h->Hkv * ((n_max + kVerifyTileKeys - 1) / kVerifyTileKeys);
-  int64_t ctas = (tiles + 1) / 2;
-  if (ctas > h->num_sms) ctas = h->num_sms;
-  if (ctas < 1) ctas = 1;
-  va.S = S;
-  va.T = T;
-  va.Hkv = h->Hkv;
-  va.G = h->G;
-  va.ctas = static_cast<int>(ctas);
-  va.max_len = n_max;
-  va.qhat16 = h->qhat16;
   va.part = h->vpart;
   va.tiles = h->tiles;
   va.err = h->err;
-  rc = cuda_status(launch_verify_split(va, h->D, s));
+  rc = cuda_status(launch_verify_split(va, h->D, s), "verify pass");
   if (rc != DATTN_OK) return rc;
 
   VerifyCombineArgs vc{};
@@ -461,7 +472,7 @@ int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, const dattn_ve
   vc.out = args->out;
   vc.write_back = args->write_back;
   vc.err = h->err;
-  rc = cuda_status(launch_verify_combine(vc, h->D, s));
+  rc = cuda_status(launch_verify_combine(vc, h->D, s), "verify combine");
   if (rc == DATTN_OK) record_launch(stream, args->write_back ? cache->k : nullptr);
   return rc;
 }

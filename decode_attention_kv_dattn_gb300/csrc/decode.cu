@@ -1200,6 +1200,46 @@ cudaError_t encode_cache_maps(const CacheView& c, int Hkv, int D, CUtensorMap* k
   return cudaSuccess;
 }
 
+cudaError_t encode_verify_maps(const CacheView& c, int Hkv, int D, const uint16_t* qhl, int qhl_rows, int Hq,
+                               int G, int S, int T, CUtensorMap* k, CUtensorMap* v, CUtensorMap* q) {
+  const EncodeTiledFn fn = encode_tiled();
+  if (!fn) return cudaErrorNotSupported;
+  const uint64_t rows = static_cast<uint64_t>(c.n_rows) * Hkv * (c.paged ? c.P : c.R);
+  if (rows == 0 || rows > 0x7fffffffull) return cudaErrorNotSupported;
+  {
+    // K: 2D [rows, D], one box = 16 rows x 64 dims
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), rows};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
+    const cuuint32_t box[2] = {64, kGroup};
+    const cuuint32_t estride[2] = {1, 1};
+    const CUresult r = fn(k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.k, dims, strides, box, estride,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  {
+    // V: 3D (64 dims, row, 64-dim region), one box = a 16-row group, every region
+    const cuuint64_t dims[3] = {64, rows, static_cast<cuuint64_t>(D / 64)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, 128};
+    const cuuint32_t box[3] = {64, kGroup, static_cast<cuuint32_t>(D / 64)};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    const CUresult r = fn(v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, c.v, dims, strides, box, estride,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq),
+                              static_cast<cuuint64_t>(S) * T, 2};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hq) * D * 2,
+                                 static_cast<cuuint64_t>(qhl_rows) * Hq * D * 2};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(T), 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  const CUresult r = fn(q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(qhl), dims, strides, box,
+                        estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t launch_decode(const DecodeArgs& args, int D, int ctas, cudaStream_t s, bool pdl) {
   DecodeArgs a = args;
   a.unit_cost = kSegmentCost;

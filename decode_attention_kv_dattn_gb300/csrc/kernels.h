@@ -60,7 +60,9 @@ struct RopeArgs {
   const uint64_t* rope_step;   // [r / 2] phase steps (rope_phase_step)
   float q_scale;               // log2(e) / sqrt(D)
   float* qhat;                 // [rows, Hq, D]
-  uint16_t* qhat16;            // [rows, Hq, D] the same values rounded to fp16 (bits), or null
+  uint16_t* qhl;               // [2][qhl_rows, Hq, D]: the same values as bf16 hi, then the
+                               // bf16 rounding of what is left (lo), or null
+  int qhl_rows;                // rows of one plane of qhl (its capacity)
   uint16_t* khat;              // [rows, Hkv, D]
   int* err;
 };
@@ -118,14 +120,19 @@ struct AppendArgs {
 };
 
 // Tensor-core pass of tree verify over each stream's paged prefix (stream-K
-// over (stream, KV head) units, the G*T rows of a unit in one 128-row MMA).
-// Partial slot layout: [ctas + S*Hkv][G*T rows][D + 4] fp32 (o[D], m, l, pad).
+// over (stream, KV head) units and their 128-key tiles; the G*T rows of a
+// unit are one 128-row MMA tile).
+// Partial slot layout: [ctas + S*Hkv][G*T rows][D + 4] fp32 (o[D], m, l, pad),
+// row g * T + i for query head g of the group and tree node i.
 struct VerifySplitArgs {
+  CUtensorMap tmap_k;          // the layer's K pool as [rows, D] bf16, boxes of 16 rows x 64 dims
+  CUtensorMap tmap_v;          // its V pool as (64 dims, rows, D/64 regions), boxes of (64, 16, D/64)
+  CUtensorMap tmap_q;          // q hi/lo as (D, Hq, S*T, 2) bf16, boxes of (64, G, T, 1)
   CacheView c;                 // paged, page size a multiple of 16; seq_len = prefix lengths
   int S, T, Hkv, G;
+  const uint16_t* qhl;         // [2][qhl_rows, Hq, D]: q as bf16 hi (the first plane) and lo
   int ctas;
   int max_len;
-  const uint16_t* qhat16;      // [S*T, Hq, D] pre-scaled q rounded to fp16 (bits), from the RoPE prologue
   float* part;
   int* tiles;                  // out, U = S*Hkv: [U + 1] tile prefix over units, then per
                                // unit the first CTA of its span [U], the span's length [U]
@@ -178,10 +185,19 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_verify_split(const VerifySplitArgs& a, int D, cudaStream_t s);
 cudaError_t launch_verify_combine(const VerifyCombineArgs& a, int D, cudaStream_t s);
 // Keys per tile of the verify pass and its largest unit count.
-constexpr int kVerifyTileKeys = 32;
+constexpr int kVerifyTileKeys = 128;
 // Fixed cost of one unit segment of the verify pass's split, in tiles.
-constexpr int kVerifySegmentCost = 8;
+constexpr int kVerifySegmentCost = 2;
 constexpr int kVerifyMaxUnits = 512;
+// Most rows (G * T) of a verify unit: one 128-row MMA tile.
+constexpr int kVerifyMaxRows = 128;
+// Tensor maps of the verify pass: the K pool as [rows, D] bf16 with boxes of
+// 16 rows x 64 dims, the V pool as (64, rows, D/64) with boxes of (64, 16,
+// D/64) (a 16-row group, all dims), and q hi/lo (qhl, planes of qhl_rows
+// rows) as (D, Hq, S*T, 2) bf16 with boxes of (64, G, T, 1); all 128-byte
+// swizzled.
+cudaError_t encode_verify_maps(const CacheView& c, int Hkv, int D, const uint16_t* qhl, int qhl_rows, int Hq,
+                               int G, int S, int T, CUtensorMap* k, CUtensorMap* v, CUtensorMap* q);
 
 // Resident CTAs per SM of the decode kernel for (D, G) (0 if unsupported).
 int decode_ctas_per_sm(int D, int G);

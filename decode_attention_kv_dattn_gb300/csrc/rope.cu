@@ -12,7 +12,7 @@
 // even), from fp32 error terms or, near a bf16 midpoint, in integers
 // (bf16_dot2). q is rotated in fp32 and pre-scaled by log2(e)/sqrt(D) so that
 // the split kernel's scores are in base-2 units; the tensor-core pass reads
-// it rounded to fp16, which is written beside it.
+// it as two bf16 terms (hi + lo, 16 significant bits), written beside it.
 #include <cuda_fp16.h>
 
 #include "bf16_exact.h"
@@ -119,9 +119,15 @@ __global__ void __launch_bounds__(kRowThreads) rope_kernel(const RopeArgs a) {
       }
       a.qhat[o + d0] = v0;
       a.qhat[o + d1] = v1;
-      if (a.qhat16) {  // the tensor-core pass's operand: the same values, rounded to nearest fp16
-        a.qhat16[o + d0] = __half_as_ushort(__float2half_rn(v0));
-        a.qhat16[o + d1] = __half_as_ushort(__float2half_rn(v1));
+      if (a.qhl) {
+        // the tensor-core pass's operand: each value as two bf16 terms, the
+        // nearest bf16 and the nearest bf16 to what is left
+        const uint16_t h0 = f32_to_bf16(v0), h1 = f32_to_bf16(v1);
+        const int64_t plane = static_cast<int64_t>(a.qhl_rows) * a.Hq * a.D;
+        a.qhl[o + d0] = h0;
+        a.qhl[o + d1] = h1;
+        a.qhl[plane + o + d0] = f32_to_bf16(v0 - bf16_to_f32(h0));
+        a.qhl[plane + o + d1] = f32_to_bf16(v1 - bf16_to_f32(h1));
       }
     } else {
       uint16_t* dst = a.khat + (static_cast<int64_t>(row) * a.Hkv + (hh - a.Hq)) * a.D;

@@ -27,6 +27,12 @@ __host__ __device__ constexpr uint32_t f16_idesc(int M, int N, int ab_type, bool
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// The same with either operand's major-ness chosen: a_mn_major / b_mn_major
+// say that A (M x K) / B (N x K) is stored M- / N-contiguous.
+__host__ __device__ constexpr uint32_t f16_idesc_ab(int M, int N, int ab_type, bool a_mn_major, bool b_mn_major) {
+  return f16_idesc(M, N, ab_type, b_mn_major) | (a_mn_major ? (1u << 15) : 0u);
+}
+
 // D[tmem] (+)= A[smem] * B[smem]; issued by one thread.
 // D (tmem) (+)= A (tmem: lane = row, each 32-bit column two consecutive K
 // elements) * B (shared-memory descriptor).

@@ -4,24 +4,32 @@
 // prefix_len + depth(i) and attends to the stream's whole paged prefix, its
 // ancestors in the tree and itself.
 //
-// Two passes after the RoPE prologue:
+// Three launches, each a programmatic dependent of the one before:
+//  * rope_kernel (rope.cu) - every row's q rotated (fp32 for the combine, and
+//    as two bf16 terms hi + lo for the tensor-core pass) and the window keys'
+//    bf16 entries.
 //  * verify_split_kernel - the prefix, on the 5th-generation tensor cores. The
-//    G*T query rows of one (stream, KV head) unit share every prefix key, so a
-//    unit is one 128-row MMA tile (G*T <= 128): S = Q K^T into tensor memory
-//    (TMEM), an online softmax by four warps (thread t owns row t), then
-//    O += P V accumulated in TMEM. Work is split stream-K over all units'
-//    32-key tiles (one CTA per SM).
-//    Operands are fp16: a TMA warp brings the bf16 K/V rows of each 16-key
-//    group (contiguous within a page) by one bulk copy each into one of three
-//    row-major bf16 stages, and eight producer warps convert each tile into
-//    one of three fp16 operand buffers in the 128-byte-swizzled layout the
-//    MMAs read (exact for |x| < 65504).
-//    A stage is refilled as soon as it is converted, so the copies in flight
-//    do not wait for the tile's MMAs; an operand buffer is held from its
-//    conversion until its PV completes. q and P are rounded to fp16. (fp16 keeps the
-//    error of q and P rounding under the tolerance at every prefix length;
-//    bf16 operands do not at short prefixes.) The accumulator is rescaled
-//    lazily: only when a row's maximum grows by more than 2^8.
+//    G*T rows of one (stream, KV head) unit share every prefix key, so a unit
+//    is one 128-row MMA tile, and the keys come 128 per tile:
+//        S (rows x 128 keys) = q_hi K^T + q_lo K^T     (bf16; q_hi in TMEM,
+//                                                       q_lo in shared memory)
+//        O (rows x D)       += P V                     (fp16; P in shared memory)
+//    K enters exactly as it is stored (bf16) and q keeps 16 significant bits
+//    as two bf16 terms: one rounding of q to 8 or 11 bits breaks the tolerance
+//    once the softmax is peaked. Each softmax thread owns
+//    one row (one TMEM lane): its running maximum, the lazy rescale of its
+//    output row (only when the tile maximum passes the reference by more than
+//    2^8, base 2) and its row sum stay in the thread. The scores leave tensor
+//    memory as soon as the softmax threads hold them, so the next tile's
+//    Q K^T runs while this tile's probabilities are formed.
+//    Loads: the TMA unit lands K by tensor-map boxes of 16 keys x 64 dims and
+//    V by one box per 16-key page group (all dims), 128-byte swizzled, in a
+//    ring of 16 KB chunks in the order the MMAs consume them. K is used as it
+//    lands; four converter warps turn each V chunk from bf16 into fp16 in
+//    place (exact below 65504 in magnitude, which they check: P is fp16, and
+//    bf16 probabilities would break the tolerance) and zero the V rows of keys
+//    outside the prefix (their probability is 0, but 0 x NaN is NaN). Work is
+//    split stream-K over all units' 128-key tiles.
 //  * verify_combine_kernel - per (stream, row, KV head): merges the prefix
 //    segments, scores the row's tree path in fp32 and joins it in score
 //    space, applies the gate, stores fp32 and writes the window entries back.
@@ -35,67 +43,93 @@ namespace dattn {
 
 namespace {
 
-constexpr int VM = 128;              // MMA rows (G*T <= VM)
-constexpr int VNK = kVerifyTileKeys; // keys per tile
-constexpr int NST = 3;               // bf16 K/V stages the TMA fills (released once converted)
-constexpr int NWB = 3;               // fp16 operand buffers (released once their PV completes)
-constexpr int NSB = 4;               // score buffers in tensor memory (each later holds its tile's P)
-constexpr int kWin = 32;             // tiles whose page rows the TMA warp resolves at once
-constexpr int kSoftWarps = 4;        // softmax warps: TMEM lane quarters 0..3
-constexpr int kProdWarps = 8;        // producer warps
-constexpr int kMmaWarp = kSoftWarps + kProdWarps;
-constexpr int kTmaWarp = kMmaWarp + 1;   // issues the prefix tiles' TMA copies
-constexpr int kPvWarp = kTmaWarp + 1;    // issues the P V MMAs (kMmaWarp issues Q K^T)
-constexpr int kVThreads = (kPvWarp + 1) * 32;
-constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold
+constexpr int KT = 128;                    // keys per tile: the Q K^T MMAs' N
+constexpr int VM = 128;                    // MMA rows (G*T <= VM)
+constexpr int kChunk = 16384;              // bytes of one ring chunk
+constexpr int kMaxChunks = 12;
+constexpr int kSoftWarps = 8;              // warps 0..7: TMEM lane quarter w % 4 (one row per
+                                           // lane), keys [64 (w / 4), 64 (w / 4) + 64) of the tile
+constexpr int kTmaWarp = 8;                // issues the K and q_lo TMA copies
+constexpr int kMmaWarp = 9;                // issues the MMAs (one thread)
+constexpr int kConv0 = 10, kConvWarps = 4; // V: bf16 -> fp16 in place
+constexpr int kTmaVWarp = 14;              // issues the V TMA copies
+constexpr int kVThreads = (kTmaVWarp + 1) * 32;
+constexpr float kRescaleLog2 = 8.f;        // lazy rescale threshold (base 2)
+constexpr int kTileRing = 8;               // tiles whose group rows and masks are kept
+constexpr int kSmemLimit = 232448 - 64;    // dynamic shared memory per CTA (the static block-scan
+                                           // scratch, 48 bytes, takes from the same 227 KB)
+static_assert(kVerifyTileKeys == KT, "tile size shared with the host split");
 
 // barrier indices
-// (B_LOAD, B_EMPTY: one per bf16 stage; B_FULL, B_WFREE: one per fp16 operand
-// buffer; B_SFULL, B_PFULL, B_SDONE: one per score buffer (its scores are in,
-// its P is in, its PV has completed); B_PVDONE: PV(k) completed, by k & 1; one per
-// probability buffer)
 enum {
-  B_LOAD = 0,
-  B_EMPTY = B_LOAD + NST,
-  B_FULL = B_EMPTY + NST,
-  B_WFREE = B_FULL + NWB,
-  B_SFULL = B_WFREE + NWB,
-  B_PFULL = B_SFULL + NSB,
-  B_SDONE = B_PFULL + NSB,
-  B_PVDONE = B_SDONE + NSB,
-  B_QREADY = B_PVDONE + 2,
-  B_OFREE = B_QREADY + 1,
-  B_COUNT = B_OFREE + 1
+  B_FULL = 0,                  // [kMaxChunks] chunk landed (TMA transaction bytes)
+  B_CONV = kMaxChunks,         // [kMaxChunks] V chunk converted (one arrival per converter warp)
+  B_FREE = 2 * kMaxChunks,     // [kMaxChunks] the MMAs reading the chunk completed
+                               // (slots [0, CK) form the K ring, [CK, CK + CV) the V ring)
+  B_QLO = 3 * kMaxChunks,      // the segment's q_lo rows landed in shared memory
+  B_QHI,                       // the segment's q_hi rows are in TMEM (softmax warps)
+  B_QFREE,                     // the segment's Q K^T MMAs completed (q may be replaced)
+  B_SFULL,                     // Q K^T of the tile completed
+  B_SFREE,                     // the softmax warps hold the tile's scores (S may be rewritten)
+  B_PFULL,                     // P of the tile written to shared memory (softmax warps)
+  B_PVDONE,                    // P V of the tile completed (P and O free)
+  B_OFREE,                     // the segment's output has been read out of TMEM
+  B_FINAL,                     // every MMA of the CTA completed (before TMEM is freed)
+  B_COUNT
 };
 
 // A partial row is o[D], m, l, padded to a 16-byte multiple: D + 4 floats.
 template <int D>
 constexpr int row_stride() { return D + 4; }
 
-template <int D>
-struct VGeo {
-  static constexpr int NREG = D / 64;                 // 64-dim (128-byte) regions per row
-  static constexpr int KT_REG = VNK * 128;            // bytes of one K (or V) region
-  static constexpr int KT_BYTES = NREG * KT_REG;
-  static constexpr int ST_OFF = 0;                    // NST bf16 stages as the TMA wrote them
-  static constexpr int ST_BYTES = 2 * KT_BYTES;       // K then V
-  static constexpr int WB_OFF = ST_OFF + NST * ST_BYTES;  // NWB fp16 operand buffers, same layout
-  static constexpr int BAR_OFF = WB_OFF + NWB * ST_BYTES;
-  static constexpr int NBAR = B_COUNT;
-  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8; // tmem slot, abort flag
-  static constexpr int TAB_OFF = MISC_OFF + 16;
-  static constexpr int SMEM = TAB_OFF + (2 * kVerifyMaxUnits + 1) * 4 + 1024;
-  static constexpr uint32_t TMEM_COLS = 512;
-  // NSB score buffers of VNK columns; P of a tile is written over its scores
-  // once they are read (the buffer's first VNK/2 columns, the A operand of P V)
-  static constexpr uint32_t S_COL = 0;
-  static constexpr uint32_t S_BUF = VNK;              // columns per score buffer
-  static constexpr uint32_t Q_COL = NSB * S_BUF;      // q rows as the MMA's A: D/2 columns of fp16 pairs
-  static constexpr uint32_t O_COL = 256;              // D columns of output
-  static_assert(D == 128 || D == 256, "head_dim");
+// Shared-memory layout of one CTA for U units; the host computes the same to
+// size the launch.
+struct VLayout {
+  int qlo_off;   // q_lo (A of the second Q K^T MMA): [D/64 regions][128 rows][128 B]
+  int p_off;     // P (A of P V): [2 key regions of 64][128 rows][128 B]
+  int ring_off;  // chunks: the K ring (ck), then the V ring (cv)
+  int chunks;
+  int ck, cv;
+  int bar_off;
+  int misc_off;  // 32 bytes: tmem base (+0), the abort flag (+16)
+  int xch_off;   // float XMAX[2 tile parities][2 halves][128], XL[2 halves][128]: the two key
+                 // halves of a row meet here
+  int trow_off;  // int TROW[kTileRing][8], TMASK[kTileRing][8], VMASK[kTileRing][8]
+  int tab_off;   // int PT[U + 1], NK[U]
+  int total;     // bytes, plus 1024 for the alignment of the base
 };
 
+__host__ __device__ inline VLayout verify_layout(int D, int U) {
+  VLayout L;
+  L.qlo_off = 0;
+  L.p_off = (D / 64) * VM * 128;
+  L.ring_off = L.p_off + (KT / 64) * VM * 128;
+  const int tail = B_COUNT * 8 + 32 + 6 * 128 * 4 + 3 * kTileRing * 8 * 4 + (2 * U + 1) * 4;
+  const int c = (kSmemLimit - 1024 - L.ring_off - tail) / kChunk;
+  L.chunks = c > kMaxChunks ? kMaxChunks : c;
+  // The K ring holds at least a whole tile's K (D/64 chunks): its copy warp
+  // issues a new segment's q_lo rows only after that segment's first K tile,
+  // whose Q K^T needs them.
+  L.ck = L.chunks / 2 < D / 64 ? D / 64 : L.chunks / 2;
+  L.cv = L.chunks - L.ck;
+  L.bar_off = L.ring_off + L.chunks * kChunk;
+  L.misc_off = L.bar_off + B_COUNT * 8;
+  L.xch_off = L.misc_off + 32;
+  L.trow_off = L.xch_off + 6 * 128 * 4;
+  L.tab_off = L.trow_off + 3 * kTileRing * 8 * 4;
+  L.total = L.tab_off + (2 * U + 1) * 4 + 1024;
+  return L;
+}
 
+// TMEM columns: q_hi (D/2 columns of bf16 pairs, the A operand of Q K^T), the
+// scores of a tile (128), the output (D).
+template <int D>
+struct VCols {
+  static constexpr uint32_t Q = 0;
+  static constexpr uint32_t S = D / 2;
+  static constexpr uint32_t O = D / 2 + KT;
+  static constexpr uint32_t TOTAL = D / 2 + KT + D;  // 512 at D = 256, 320 at 128
+};
 
 struct Waiter {
   uint32_t bars;
@@ -111,7 +145,7 @@ struct Waiter {
       for (int i = 0; i < 32; ++i)
         if (mbar_try_wait(bar, parity)) return true;
       if (*abort) return false;
-      if (global_timer_ns() - t0 > 2000000000ull) {
+      if (global_timer_ns() - t0 > kDefaultWaitNs) {
         *abort = 1;
         raise_error(err, ERR_TIMEOUT);
         return false;
@@ -125,10 +159,24 @@ __device__ __forceinline__ uint32_t cvt_pair_f16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// 16 bytes of 8 bf16 values turned into 8 fp16 values in place (exact below
+// 65504 in magnitude); `mag` keeps the largest magnitude seen per 16-bit half.
+__device__ __forceinline__ void convert16(uint8_t* p, uint32_t& mag) {
+  const uint4 w = *reinterpret_cast<const uint4*>(p);
+  mag = __vmaxu2(mag, w.x & 0x7fff7fffu);
+  mag = __vmaxu2(mag, w.y & 0x7fff7fffu);
+  mag = __vmaxu2(mag, w.z & 0x7fff7fffu);
+  mag = __vmaxu2(mag, w.w & 0x7fff7fffu);
+  *reinterpret_cast<uint4*>(p) =
+      make_uint4(cvt_pair_f16(bf16_lo(w.x), bf16_hi(w.x)), cvt_pair_f16(bf16_lo(w.y), bf16_hi(w.y)),
+                 cvt_pair_f16(bf16_lo(w.z), bf16_hi(w.z)), cvt_pair_f16(bf16_lo(w.w), bf16_hi(w.w)));
+}
 
 template <int D>
 __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid_constant__ VerifySplitArgs a) {
-  using V = VGeo<D>;
+  constexpr int NREG = D / 64;        // 64-dim regions: K chunks per tile
+  constexpr int GPV = 8 / NREG;       // 16-key page groups per V chunk
+  using Col = VCols<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -137,9 +185,15 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
   const CacheView& c = a.c;
   const int Hkv = a.Hkv, U = a.S * Hkv, G = a.G, T = a.T, R = G * T, Hq = Hkv * G;
   const int NC = gridDim.x, cta = blockIdx.x;
-  int* Pt = reinterpret_cast<int*>(smem + V::TAB_OFF);  // [U + 1] tile prefix
-  int* Nn = Pt + U + 1;                                   // [U] prefix keys per unit
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + V::MISC_OFF + 4);
+  const VLayout L = verify_layout(D, U);
+  const int CK = L.ck, CV = L.cv;
+  int* PT = reinterpret_cast<int*>(smem + L.tab_off);   // [U + 1] tile prefix
+  int* NK = PT + U + 1;                                   // [U] prefix keys per unit
+  int* TROW = reinterpret_cast<int*>(smem + L.trow_off);  // [kTileRing][8] first tensor row of each group
+  int* TMASK = TROW + kTileRing * 8;                      // [kTileRing][8] valid rows of each group
+  int* VMASK = TMASK + kTileRing * 8;                     // the same, written by the V copy warp
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 16);
+  const uint32_t bars = sbase + L.bar_off;
 
   // ---- unit table (caller metadata only)
   for (int u = threadIdx.x; u < U; u += kVThreads) {
@@ -150,370 +204,413 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
       if (cta == 0 && u - s * Hkv == 0) raise_error(a.err, ERR_LENGTH);
       n = n < 0 ? 0 : cap;
     }
-    Nn[u] = n;
-    Pt[u + 1] = (n + VNK - 1) / VNK;
+    NK[u] = n;
+    PT[u + 1] = (n + KT - 1) / KT;
   }
   if (threadIdx.x == 0) {
-    Pt[0] = 0;
+    PT[0] = 0;
     *abort_flag = 0;
-    for (int b = 0; b < NST; ++b) {
-      mbar_init(sbase + V::BAR_OFF + 8 * (B_LOAD + b), 1);
-      mbar_init(sbase + V::BAR_OFF + 8 * (B_EMPTY + b), kProdWarps);
+    for (int b = 0; b < kMaxChunks; ++b) {
+      mbar_init(bars + 8 * (B_FULL + b), 1);
+      mbar_init(bars + 8 * (B_CONV + b), kConvWarps);
+      mbar_init(bars + 8 * (B_FREE + b), 1);
     }
-    for (int b = 0; b < NWB; ++b) {
-      mbar_init(sbase + V::BAR_OFF + 8 * (B_FULL + b), kProdWarps);
-      mbar_init(sbase + V::BAR_OFF + 8 * (B_WFREE + b), 1);
-    }
-    for (int b = 0; b < NSB; ++b) {
-      mbar_init(sbase + V::BAR_OFF + 8 * (B_SFULL + b), 1);
-      mbar_init(sbase + V::BAR_OFF + 8 * (B_PFULL + b), kSoftWarps);
-      mbar_init(sbase + V::BAR_OFF + 8 * (B_SDONE + b), 1);
-    }
-    for (int b = 0; b < 2; ++b) mbar_init(sbase + V::BAR_OFF + 8 * (B_PVDONE + b), 1);
-    mbar_init(sbase + V::BAR_OFF + 8 * B_QREADY, kSoftWarps);
-    mbar_init(sbase + V::BAR_OFF + 8 * B_OFREE, kSoftWarps);
+    mbar_init(bars + 8 * B_QLO, 1);
+    mbar_init(bars + 8 * B_QHI, kSoftWarps);
+    mbar_init(bars + 8 * B_QFREE, 1);
+    mbar_init(bars + 8 * B_SFULL, 1);
+    mbar_init(bars + 8 * B_SFREE, kSoftWarps);
+    mbar_init(bars + 8 * B_PFULL, kSoftWarps);
+    mbar_init(bars + 8 * B_PVDONE, 1);
+    mbar_init(bars + 8 * B_OFREE, kSoftWarps);
+    mbar_init(bars + 8 * B_FINAL, 1);
     fence_mbar_init();
   }
+  if (threadIdx.x == kTmaWarp * 32) {
+    prefetch_tmap(&a.tmap_k);
+    prefetch_tmap(&a.tmap_v);
+    prefetch_tmap(&a.tmap_q);
+  }
   __syncthreads();
-  block_scan_inclusive<kVThreads>(Pt + 1, U);
-  const int Ttot = Pt[U];
+  block_scan_inclusive<kVThreads>(PT + 1, U);
+  const int Ttot = PT[U];
   // stream-K over the units' tiles, each unit weighted with the fixed cost of
-  // one segment of it (at a segment end the whole tile pipeline drains, the
-  // partial output leaves tensor memory and the next unit's q comes in)
-  const Split sp{Pt, U, kVerifySegmentCost, NC, Ttot + static_cast<int64_t>(kVerifySegmentCost) * U};
+  // one segment of it (its q rows come in, the pipeline refills, its partial
+  // output leaves tensor memory)
+  const Split sp{PT, U, kVerifySegmentCost, NC, Ttot + static_cast<int64_t>(kVerifySegmentCost) * U};
   const int g0 = sp.tile_at(sp.bound(cta));
   const int g1 = sp.tile_at(sp.bound(cta + 1));
   if (cta == 0) {
     // for the combine: the tile prefix, then per unit the first CTA of its
     // span, the span's length and the partial slot of its first segment
-    for (int u = threadIdx.x; u <= U; u += kVThreads) a.tiles[u] = Pt[u];
+    for (int u = threadIdx.x; u <= U; u += kVThreads) a.tiles[u] = PT[u];
     for (int u = threadIdx.x; u < U; u += kVThreads) {
       int c_lo = 0, c_hi = -1, first_slot = 0;
-      unit_segments(sp, Pt[u], Pt[u + 1], u, c_lo, c_hi, first_slot);
+      unit_segments(sp, PT[u], PT[u + 1], u, c_lo, c_hi, first_slot);
       a.tiles[U + 1 + u] = c_lo;
       a.tiles[2 * U + 1 + u] = c_hi - c_lo + 1;
       a.tiles[3 * U + 1 + u] = first_slot;
     }
   }
-  if (warp == kMmaWarp) tc::alloc(sbase + V::MISC_OFF, V::TMEM_COLS);
+  const int nt = g1 - g0;
+  if (nt > 0 && warp == kMmaWarp) tc::alloc(sbase + L.misc_off, Col::TOTAL > 256 ? 512 : 256);
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + V::MISC_OFF);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L.misc_off);
+  const Waiter W{bars, abort_flag, a.err};
+  // the unit of CTA tile k (global tile g0 + k), from the unit of an earlier tile
+  auto unit_at = [&](int k, int u) {
+    while (PT[u + 1] <= g0 + k) ++u;
+    return u;
+  };
+  const int u_first = nt > 0 ? unit_of(PT, U, g0) : 0;
 
-  const int ntiles = g1 - g0;
-  const Waiter W{sbase + V::BAR_OFF, abort_flag, a.err};
-
-  if (ntiles > 0 && warp == kTmaWarp) {
-    // ================= TMA: bf16 K/V page rows into the stage =================
-    // Each 16-key group of a tile is 16 consecutive rows of one page (its size
-    // is a multiple of 16): one contiguous bulk copy each for K and V, stored
-    // row-major; the producers lay them out for the MMAs. Groups past the
-    // prefix are not loaded; the producers zero their rows.
-    // Lane x % 32 reads the page ids of tile x one 32-tile window ahead, so
-    // that no page-table load sits between two tiles' copies; lane 0 issues.
-    constexpr int NG = VNK / 16;
+  // lane gi < 8 of a copy warp: first tensor row and valid rows of group gi
+  // of tile k of unit u (one page-table load)
+  auto group_of = [&](int k, int u, int& row, int& mask) {
+    row = mask = 0;
+    if (lane >= 8 || k >= nt) return;
+    const int s = u / Hkv, j = u - s * Hkv;
+    const int t0 = ((g0 + k) - PT[u]) * KT + lane * 16;
+    const int valid = min(16, NK[u] - t0);
+    if (valid <= 0) return;
+    int pg = c.block_table[static_cast<int64_t>(s) * c.bt_stride + t0 / c.P];
+    if (pg < 0 || pg >= c.n_rows) {
+      raise_error(a.err, ERR_INDEX);
+      pg = 0;
+    }
+    row = (pg * Hkv + j) * c.P + t0 % c.P;
+    mask = static_cast<int>((1u << valid) - 1u);
+  };
+  if (nt > 0 && (warp == kTmaWarp || warp == kTmaVWarp)) {
+    // ================= TMA: K (and each segment's q_lo rows) or V, one warp each =================
+    // Each tile's group rows are worked out one tile ahead, so that no
+    // page-table load waits on the issue path.
+    const bool is_v = warp == kTmaVWarp;
+    const int nring = is_v ? CV : CK, ring0 = is_v ? CK : 0;
+    int* MASKS = is_v ? VMASK : TMASK;
     const uint64_t policy = l2_evict_first_policy();
-    auto fetch = [&](int x, int (&pg)[NG], int (&off)[NG]) -> int {  // returns the group count
+    int u = u_first, seg = -1, issued = 0;
+    int nrow, nmask;
+    group_of(0, u, nrow, nmask);
+    bool waited = false, ok = true;
+    for (int k = 0; k < nt && ok; ++k) {
+      const int e = (k % kTileRing) * 8;
+      const int un = unit_at(k, u);
+      const bool new_seg = un != u || k == 0;
+      u = un;
+      int rows[8];
 #pragma unroll
-      for (int gr = 0; gr < NG; ++gr) pg[gr] = off[gr] = 0;
-      if (x >= ntiles) return 0;
-      const int g = g0 + x;
-      const int u = unit_of(Pt, U, g);
-      const int s = u / Hkv, j = u - s * Hkv;
-      const int k0 = (g - Pt[u]) * VNK;
-      const int ng = (min(VNK, Nn[u] - k0) + 15) / 16;
-      const int32_t* bt = c.block_table + static_cast<int64_t>(s) * c.bt_stride;
-#pragma unroll
-      for (int gr = 0; gr < NG; ++gr) {
-        if (gr < ng) {
-          const int t = k0 + gr * 16;
-          const int pi = t / c.P;
-          pg[gr] = bt[pi];  // used a window later: the load is not waited for here
-          off[gr] = j * c.P + (t - pi * c.P);
-        }
-      }
-      return ng;
-    };
-    int pg_c[NG], off_c[NG], pg_n[NG], off_n[NG];
-    int ng_c = fetch(lane, pg_c, off_c);
-    int ng_n = fetch(kWin + lane, pg_n, off_n);
-    for (int k = 0; k < ntiles; ++k) {
-      if (k > 0 && (k & (kWin - 1)) == 0) {
-#pragma unroll
-        for (int gr = 0; gr < NG; ++gr) {
-          pg_c[gr] = pg_n[gr];
-          off_c[gr] = off_n[gr];
-        }
-        ng_c = ng_n;
-        ng_n = fetch(k + kWin + lane, pg_n, off_n);
-      }
-      const int st = k % NST;
-      if (k >= NST && !__all_sync(0xffffffffu, W.wait(B_EMPTY + st, (k / NST - 1) & 1))) break;
-      const int src = k & (kWin - 1);
-      const int ngroups = __shfl_sync(0xffffffffu, ng_c, src);
-      int rows[NG];
-#pragma unroll
-      for (int gr = 0; gr < NG; ++gr) {
-        int pg = __shfl_sync(0xffffffffu, pg_c[gr], src);
-        const int off = __shfl_sync(0xffffffffu, off_c[gr], src);
-        if (gr < ngroups && (pg < 0 || pg >= c.n_rows)) {
-          if (lane == 0) raise_error(a.err, ERR_INDEX);
-          pg = 0;
-        }
-        rows[gr] = pg * Hkv * c.P + off;
-      }
+      for (int gi = 0; gi < 8; ++gi) rows[gi] = __shfl_sync(0xffffffffu, nrow, gi);
+      if (lane < 8) MASKS[e + lane] = nmask;
+      if (!is_v && lane < 8) TROW[e + lane] = nrow;
+      __syncwarp();
+      if (k + 1 < nt) group_of(k + 1, unit_at(k + 1, u), nrow, nmask);
       if (lane == 0) {
-        // one bulk copy per 16-key group of K and of V: 16 consecutive rows of
-        // a page (8 KB at D = 256), row-major into the stage
-        const uint32_t bar = sbase + V::BAR_OFF + 8 * (B_LOAD + st);
-        const uint32_t stage = sbase + V::ST_OFF + st * V::ST_BYTES;
-        constexpr uint32_t GB = 16u * D * 2u;  // bytes of one group
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(ngroups) * 2u * GB);
-#pragma unroll
-        for (int gr = 0; gr < NG; ++gr) {
-          if (gr < ngroups) {
-            const int64_t e0 = static_cast<int64_t>(rows[gr]) * D;
-            bulk_copy_g2s(stage + gr * GB, c.k + e0, GB, bar, policy);
-            bulk_copy_g2s(stage + V::KT_BYTES + gr * GB, c.v + e0, GB, bar, policy);
+        // K(k): one chunk per 64-dim region, one box per loaded group;
+        // V(k): one chunk per GPV groups, one box per loaded group (all dims)
+        for (int ch = 0; ch < NREG && ok; ++ch) {
+          const int idx = k * NREG + ch, slot = ring0 + idx % nring;
+          if (idx >= nring && !W.wait(B_FREE + slot, ((idx / nring) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          const uint32_t dst = sbase + L.ring_off + slot * kChunk;
+          const uint32_t bar = bars + 8 * (B_FULL + slot);
+          if (!is_v) {
+            int n = 0;
+            for (int gi = 0; gi < 8; ++gi) n += MASKS[e + gi] != 0;
+            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n) * 2048u);
+            for (int gi = 0; gi < 8; ++gi)
+              if (MASKS[e + gi] != 0) tma_load_2d(dst + gi * 2048, &a.tmap_k, 64 * ch, rows[gi], bar, policy);
+          } else {
+            int n = 0;
+            for (int gg = 0; gg < GPV; ++gg) n += MASKS[e + ch * GPV + gg] != 0;
+            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n) * NREG * 2048u);
+            for (int gg = 0; gg < GPV; ++gg)
+              if (MASKS[e + ch * GPV + gg] != 0)
+                tma_load_3d(dst + gg * NREG * 2048, &a.tmap_v, 0, rows[ch * GPV + gg], 0, bar, policy);
+          }
+          issued = idx + 1;
+        }
+        if (ok && new_seg && !is_v) {
+          // the segment's q_lo rows once its previous segment's Q K^T
+          // completed; the first ones once the prologue that writes them has
+          if (!waited) {
+            pdl_wait();
+            waited = true;
+          }
+          ++seg;
+          if (seg > 0 && !W.wait(B_QFREE, (seg - 1) & 1)) ok = false;
+          if (ok) {
+            const int s = u / Hkv, j = u - s * Hkv;
+            const uint32_t bar = bars + 8 * B_QLO;
+            mbar_arrive_expect_tx(bar, NREG * static_cast<uint32_t>(R) * 128u);
+            for (int rr = 0; rr < NREG; ++rr)
+              tma_load_4d(sbase + L.qlo_off + rr * VM * 128, &a.tmap_q, 64 * rr, j * G, s * T, 1, bar, policy);
           }
         }
       }
-      __syncwarp();
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     }
-  } else if (ntiles > 0 && warp >= kSoftWarps && warp < kMmaWarp) {
-    // ================= producers: a staged bf16 tile -> fp16 operand buffer k % NWB =================
-    // (row-major bf16 in, the MMAs' 128-byte-swizzled fp16 layout out)
-    // The stage goes back to the TMA as soon as it is read; the operand buffer
-    // is free again once the PV NWB tiles back has completed.
-    const int pt = threadIdx.x - kSoftWarps * 32;         // 0 .. 255
-    constexpr int CPR = D / 8;                            // 16-byte chunks per row
-    constexpr int NCH = 2 * VNK * CPR;                    // chunks of a stage (K and V)
-    constexpr int PER = NCH / (kProdWarps * 32);          // chunks per thread
-    static_assert(NCH % (kProdWarps * 32) == 0, "whole chunks per thread");
-    // this thread's chunks (the same positions in every tile): byte offset in
-    // the row-major stage, in the swizzled operand buffer, and key row
-    int soff[PER], coff[PER], crow[PER];
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      const int e = pt + i * kProdWarps * 32;
-      const int which = e / (VNK * CPR);
-      const int rem = e - which * (VNK * CPR);
-      const int r = rem / CPR, ch = rem - r * CPR;
-      soff[i] = which * V::KT_BYTES + r * (D * 2) + ch * 16;
-      coff[i] = which * V::KT_BYTES + (ch >> 3) * V::KT_REG + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-      crow[i] = r;
+    // Copies still in flight exist only when a role gave up: let the latest
+    // copy into every chunk and the last q copy land before the CTA exits.
+    if (lane == 0 && *abort_flag) {
+      for (int idx = max(0, issued - nring); idx < issued; ++idx)
+        mbar_wait_bounded(bars + 8 * (B_FULL + ring0 + idx % nring), (idx / nring) & 1);
+      if (!is_v && seg >= 0) mbar_wait_bounded(bars + 8 * B_QLO, seg & 1);
     }
-    uint32_t mag = 0;  // largest |x| seen, per 16-bit half (bf16 bit patterns)
-    int u = unit_of(Pt, U, g0);
-    for (int k = 0; k < ntiles; ++k) {
-      const int st = k % NST, wb = k % NWB;
-      if (!__all_sync(0xffffffffu, W.wait(B_LOAD + st, (k / NST) & 1))) break;
-      if (k >= NWB && !__all_sync(0xffffffffu, W.wait(B_WFREE + wb, (k / NWB - 1) & 1))) break;
-      const int g = g0 + k;
-      while (Pt[u + 1] <= g) ++u;
-      const int nvalid = min(VNK, Nn[u] - (g - Pt[u]) * VNK);
-      const uint8_t* stage = smem + V::ST_OFF + st * V::ST_BYTES;
-      uint8_t* obuf = smem + V::WB_OFF + wb * V::ST_BYTES;
-      // all loads first, then the conversions and stores (rows past the prefix become zeros)
-      uint4 w[PER];
+    __syncwarp();
+  } else if (nt > 0 && warp >= kConv0 && warp < kConv0 + kConvWarps) {
+    // ================= converters: each landed V chunk bf16 -> fp16 in place =================
+    const int ct = threadIdx.x - kConv0 * 32;  // 0 .. 127
+    uint32_t mag = 0;
+    bool ok = true;
+    for (int k = 0; k < nt && ok; ++k) {
+      const int e = (k % kTileRing) * 8;
+      for (int ch = 0; ch < NREG; ++ch) {
+        const int idx = k * NREG + ch, slot = CK + idx % CV;
+        if (!__all_sync(0xffffffffu, W.wait(B_FULL + slot, (idx / CV) & 1))) {
+          ok = false;
+          break;
+        }
+        uint8_t* base = smem + L.ring_off + slot * kChunk;
 #pragma unroll
-      for (int i = 0; i < PER; ++i)
-        w[i] = crow[i] < nvalid ? *reinterpret_cast<const uint4*>(stage + soff[i]) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-      for (int i = 0; i < PER; ++i) {
-        mag = __vmaxu2(mag, w[i].x & 0x7fff7fffu);
-        mag = __vmaxu2(mag, w[i].y & 0x7fff7fffu);
-        mag = __vmaxu2(mag, w[i].z & 0x7fff7fffu);
-        mag = __vmaxu2(mag, w[i].w & 0x7fff7fffu);
-        const uint4 h = make_uint4(cvt_pair_f16(bf16_lo(w[i].x), bf16_hi(w[i].x)),
-                                   cvt_pair_f16(bf16_lo(w[i].y), bf16_hi(w[i].y)),
-                                   cvt_pair_f16(bf16_lo(w[i].z), bf16_hi(w[i].z)),
-                                   cvt_pair_f16(bf16_lo(w[i].w), bf16_hi(w[i].w)));
-        *reinterpret_cast<uint4*>(obuf + coff[i]) = h;
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(sbase + V::BAR_OFF + 8 * (B_FULL + wb));
-        mbar_arrive(sbase + V::BAR_OFF + 8 * (B_EMPTY + st));
+        for (int i = 0; i < kChunk / 16 / 128; ++i) {
+          // [group][region][16 rows][128 B]: rows outside the prefix become 0
+          const int p = ct + i * 128;
+          const int gg = p / (NREG * 128), row = (p >> 3) & 15;
+          if ((VMASK[e + ch * GPV + gg] >> row) & 1)
+            convert16(base + p * 16, mag);
+          else
+            *reinterpret_cast<uint4*>(base + p * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars + 8 * (B_CONV + slot));
       }
     }
     // fp16 holds bf16 values below 65504 in magnitude exactly (bf16 0x4780 = 65536)
     const bool ovf = (mag & 0xffffu) >= 0x4780u || (mag >> 16) >= 0x4780u;
     if (__any_sync(0xffffffffu, ovf) && lane == 0) raise_error(a.err, ERR_RANGE);
-  } else if (ntiles > 0 && warp == kMmaWarp) {
-    // ================= Q K^T issue (one thread) =================
+  } else if (nt > 0 && warp == kMmaWarp) {
+    // ================= MMA issue (one thread) =================
+    // Order: Q K^T(0), then for each tile k >= 1 Q K^T(k) and P V(k - 1), then
+    // P V(n - 1): a tile's scores are formed into probabilities while the
+    // next tile's Q K^T runs.
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = tc::f16_idesc(VM, VNK, 0, false);
-      int u = unit_of(Pt, U, g0), prev_u = -1, seg = 0;
-      for (int k = 0; k < ntiles; ++k) {
-        const int g = g0 + k;
-        while (Pt[u + 1] <= g) ++u;
-        if (u != prev_u) {  // this unit's q rows are in place
-          if (!W.wait(B_QREADY, seg & 1)) break;
+      constexpr uint32_t idesc_qk = tc::f16_idesc(VM, KT, 1, false);  // bf16; B = K: K-major
+      constexpr uint32_t idesc_pv = tc::f16_idesc(VM, D, 0, true);    // B = V: D-contiguous
+      int u = u_first, seg = -1;
+      auto qk = [&](int k) -> bool {
+        const int un = unit_at(k, u);
+        const bool seg_first = un != u || k == 0;
+        u = un;
+        const bool seg_last = k == nt - 1 || g0 + k + 1 >= PT[u + 1];
+        if (seg_first) {
           ++seg;
-          prev_u = u;
+          if (!W.wait(B_QLO, seg & 1) || !W.wait(B_QHI, seg & 1)) return false;
         }
-        const int sb = k % NSB, wb = k % NWB;
-        if (!W.wait(B_FULL + wb, (k / NWB) & 1)) break;
-        // the score buffer (and the P in it) is free once the PV NSB tiles back has completed
-        if (k >= NSB && !W.wait(B_SDONE + sb, (k / NSB - 1) & 1)) break;
-        tc::fence_after();
-        const uint32_t kbase = sbase + V::WB_OFF + wb * V::ST_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t db = tc::sw128_desc(kbase + (kk >> 2) * V::KT_REG + (kk & 3) * 32, 16, 1024);
-          tc::mma_ts(tmem + V::S_COL + sb * V::S_BUF, tmem + V::Q_COL + kk * 8, db, idesc_qk, kk > 0);
-        }
-        tc::commit(sbase + V::BAR_OFF + 8 * (B_SFULL + sb));
-      }
-    }
-    __syncwarp();
-  } else if (ntiles > 0 && warp == kPvWarp) {
-    // ================= P V issue (one thread) =================
-    // PV(k) follows QK(k): its P was made from the scores QK(k) wrote. The
-    // operand buffer's K and V are free once PV(k) completes.
-    if (lane == 0) {
-      constexpr uint32_t idesc_pv = tc::f16_idesc(VM, D, 0, true);
-      int u = unit_of(Pt, U, g0), prev_u = -1, seg = 0;
-      for (int k = 0; k < ntiles; ++k) {
-        const int g = g0 + k;
-        while (Pt[u + 1] <= g) ++u;
-        const bool seg_start = u != prev_u;
-        const bool seg_end = k == ntiles - 1 || g + 1 >= Pt[u + 1];
-        if (!W.wait(B_PFULL + k % NSB, (k / NSB) & 1)) break;
-        if (seg_start && seg > 0 && !W.wait(B_OFREE, (seg - 1) & 1)) break;
-        tc::fence_after();
-        const uint32_t vbase = sbase + V::WB_OFF + (k % NWB) * V::ST_BYTES + V::KT_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < VNK / 16; ++kk) {
-          const uint64_t db = tc::sw128_desc(vbase + kk * 2048, V::KT_REG, 1024);
-          tc::mma_ts(tmem + V::O_COL, tmem + V::S_COL + (k % NSB) * V::S_BUF + kk * 8, db, idesc_pv,
-                     !seg_start || kk > 0);
-        }
-        tc::commit(sbase + V::BAR_OFF + 8 * (B_PVDONE + (k & 1)));
-        tc::commit(sbase + V::BAR_OFF + 8 * (B_SDONE + k % NSB));
-        tc::commit(sbase + V::BAR_OFF + 8 * (B_WFREE + k % NWB));
-        if (seg_end) ++seg;
-        prev_u = u;
-      }
-    }
-    __syncwarp();
-  } else if (ntiles > 0 && warp < kSoftWarps) {
-    // ================= softmax: thread t owns row t =================
-    pdl_wait();  // q rotated by the prologue
-    pdl_trigger();
-    const int t = threadIdx.x;
-    const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
-    int u = unit_of(Pt, U, g0), prev_u = -1, seg = 0;
-    float m_ref = -INFINITY, l = 0.f;
-    for (int k = 0; k < ntiles; ++k) {
-      const int g = g0 + k;
-      while (Pt[u + 1] <= g) ++u;
-      const bool seg_start = u != prev_u;
-      const bool seg_end = k == ntiles - 1 || g + 1 >= Pt[u + 1];
-      if (seg_start) {
-        // this unit's q rows as fp16 pairs into tensor memory (the QK MMAs'
-        // A operand; the previous unit's QKs are done: its last scores were read)
-        const int s = u / Hkv, j = u - s * Hkv;
-        const uint16_t* src = nullptr;
-        if (t < R) {
-          const int gq = t / T, i = t - gq * T;
-          src = a.qhat16 + ((static_cast<int64_t>(s) * T + i) * Hq + j * G + gq) * D;
-        }
-#pragma unroll 1
-        for (int c32 = 0; c32 < D / 64; ++c32) {
-          uint32_t qv[32];  // fp16 pairs, the lower dim in the low half
-#pragma unroll
-          for (int x = 0; x < 32; x += 4) {
-            uint4 y = make_uint4(0u, 0u, 0u, 0u);
-            if (src) y = *reinterpret_cast<const uint4*>(src + 64 * c32 + 2 * x);
-            qv[x] = y.x;
-            qv[x + 1] = y.y;
-            qv[x + 2] = y.z;
-            qv[x + 3] = y.w;
-          }
-          tc::st32(tmem + lane_off + V::Q_COL + 32 * c32, qv);
-        }
-        tc::wait_st();
-        tc::fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sbase + V::BAR_OFF + 8 * B_QREADY);
-        m_ref = -INFINITY;
-        l = 0.f;
-      }
-      const int sb = k % NSB;
-      if (!__all_sync(0xffffffffu, W.wait(B_SFULL + sb, (k / NSB) & 1))) break;
-      tc::fence_after();
-      uint32_t sr[VNK];
-      static_assert(VNK == 32, "one 32-column score read per row");
-      tc::ld32(tmem + lane_off + V::S_COL + sb * V::S_BUF, sr);
-      tc::wait_ld();
-      const int nvalid = min(VNK, Nn[u] - (g - Pt[u]) * VNK);
-      float tmax = -INFINITY;
-#pragma unroll
-      for (int x = 0; x < VNK; ++x) {
-        const float sx = x < nvalid ? __uint_as_float(sr[x]) : -INFINITY;
-        sr[x] = __float_as_uint(sx);
-        tmax = fmaxf(tmax, sx);
-      }
-      if (m_ref == -INFINITY) {
-        m_ref = tmax;
-      } else {
-        const bool need = tmax > m_ref + kRescaleLog2;
-        if (__any_sync(0xffffffffu, need)) {
-          // rescale this warp's rows of O once the last PV has landed
-          if (!__all_sync(0xffffffffu, W.wait(B_PVDONE + ((k - 1) & 1), ((k - 1) >> 1) & 1))) break;
+        // S is free once the softmax warps hold the previous tile's scores
+        if (k > 0 && !W.wait(B_SFREE, (k - 1) & 1)) return false;
+        for (int ch = 0; ch < NREG; ++ch) {
+          const int idx = k * NREG + ch, slot = idx % CK;
+          if (!W.wait(B_FULL + slot, (idx / CK) & 1)) return false;  // K is used as it landed
           tc::fence_after();
-          const float f = need ? exp2_fast(m_ref - tmax) : 1.f;
-#pragma unroll 1
-          for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t o[32];
-            tc::ld32(tmem + lane_off + V::O_COL + cc * 32, o);
-            tc::wait_ld();
+          const uint32_t kc = sbase + L.ring_off + slot * kChunk;
+          const uint32_t qc = sbase + L.qlo_off + ch * VM * 128;
 #pragma unroll
-            for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * f);
-            tc::st32(tmem + lane_off + V::O_COL + cc * 32, o);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t kdesc = tc::sw128_desc(kc + kk * 32, 16, 1024);
+            tc::mma_ts(tmem + Col::S, tmem + Col::Q + (4 * ch + kk) * 8, kdesc, idesc_qk, ch > 0 || kk > 0);
+            tc::mma(tmem + Col::S, tc::sw128_desc(qc + kk * 32, 16, 1024), kdesc, idesc_qk, true);
           }
-          tc::wait_st();
-          if (need) {
-            l *= f;
-            m_ref = tmax;
-          }
+          tc::commit(bars + 8 * (B_FREE + slot));
         }
-      }
-      // probabilities in fp16; the row sum uses the same rounded values
-      uint32_t ph[VNK / 2];
-      float lsum = 0.f;
+        tc::commit(bars + 8 * B_SFULL);
+        if (seg_last) tc::commit(bars + 8 * B_QFREE);
+        return true;
+      };
+      int pv_u = u_first, pv_seg = -1;
+      auto pv = [&](int k) -> bool {
+        const int un = unit_at(k, pv_u);
+        const bool seg_first = un != pv_u || k == 0;
+        pv_u = un;
+        if (seg_first) ++pv_seg;
+        if (!W.wait(B_PFULL, k & 1)) return false;
+        if (seg_first && pv_seg > 0 && !W.wait(B_OFREE, (pv_seg - 1) & 1)) return false;
+        for (int ch = 0; ch < NREG; ++ch) {
+          const int idx = k * NREG + ch, slot = CK + idx % CV;
+          if (!W.wait(B_CONV + slot, (idx / CV) & 1)) return false;
+          tc::fence_after();
+          const uint32_t vc = sbase + L.ring_off + slot * kChunk;
 #pragma unroll
-      for (int x = 0; x < VNK / 2; ++x) {
-        const float p0 = exp2_fast(__uint_as_float(sr[2 * x]) - m_ref);
-        const float p1 = exp2_fast(__uint_as_float(sr[2 * x + 1]) - m_ref);
-        const __half2 h = __floats2half2_rn(p0, p1);
-        lsum += __low2float(h) + __high2float(h);
-        ph[x] = *reinterpret_cast<const uint32_t*>(&h);
+          for (int gg = 0; gg < GPV; ++gg) {
+            const int grp = ch * GPV + gg;  // 16-key group of the tile
+            const uint64_t pdesc = tc::sw128_desc(sbase + L.p_off + (grp >> 2) * VM * 128 + (grp & 3) * 32, 16, 1024);
+            tc::mma(tmem + Col::O, pdesc, tc::sw128_desc(vc + gg * NREG * 2048, 2048, 1024), idesc_pv,
+                    !(seg_first && grp == 0));
+          }
+          tc::commit(bars + 8 * (B_FREE + slot));
+        }
+        tc::commit(bars + 8 * B_PVDONE);
+        return true;
+      };
+      bool ok = qk(0);
+      for (int k = 1; k < nt && ok; ++k) ok = qk(k) && pv(k - 1);
+      if (ok) pv(nt - 1);
+      // every MMA issued has completed before the tensor memory is freed
+      tc::commit(bars + 8 * B_FINAL);
+      if (!mbar_wait_bounded(bars + 8 * B_FINAL, 0)) raise_error(a.err, ERR_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (nt > 0 && warp < kSoftWarps) {
+    // ================= softmax: row t = 32 (w % 4) + lane, keys of half w / 4 =================
+    const int q4 = warp & 3, kh = warp >> 2;
+    const int t = 32 * q4 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
+    float* XMAX = reinterpret_cast<float*>(smem + L.xch_off);  // [2][2][128]
+    float* XL = XMAX + 512;                                     // [2][128]
+    // the two warps of a lane quarter (the two key halves of its rows) meet
+    auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(1 + q4) : "memory"); };
+    // unit u's q_hi rows into TMEM (the A operand of the first Q K^T MMA of
+    // every 16 dims; rows past R are zero); each key half writes half the dims
+    auto load_qhi = [&](int u) {
+      const int s = u / Hkv, j = u - s * Hkv;
+      const uint16_t* src = nullptr;
+      if (t < R) {
+        const int i = t / G, g = t - i * G;  // rows as the q_lo box lays them out: i * G + g
+        src = a.qhl + ((static_cast<int64_t>(s) * T + i) * Hq + j * G + g) * D;
       }
-      l += lsum;
-      // row t of P (fp16 pairs) over this tile's scores, where PV reads its A
-      // operand (the scores were read above; the PV NSB tiles back that read
-      // this buffer's P completed before QK(k) was issued)
-      tc::st16(tmem + lane_off + V::S_COL + sb * V::S_BUF, ph);
+#pragma unroll 1
+      for (int c32 = kh * (D / 128); c32 < (kh + 1) * (D / 128); ++c32) {
+        uint32_t qv[32];  // bf16 pairs, the lower dim in the low half
+#pragma unroll
+        for (int x = 0; x < 32; x += 4) {
+          uint4 y = make_uint4(0u, 0u, 0u, 0u);
+          if (src) y = *reinterpret_cast<const uint4*>(src + 64 * c32 + 2 * x);
+          qv[x] = y.x;
+          qv[x + 1] = y.y;
+          qv[x + 2] = y.z;
+          qv[x + 3] = y.w;
+        }
+        tc::st32(tmem + lane_off + Col::Q + 32 * c32, qv);
+      }
       tc::wait_st();
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(sbase + V::BAR_OFF + 8 * (B_PFULL + sb));
-      if (seg_end) {
-        if (!__all_sync(0xffffffffu, W.wait(B_PVDONE + (k & 1), (k >> 1) & 1))) break;
+      if (lane == 0) mbar_arrive(bars + 8 * B_QHI);
+    };
+    pdl_wait();  // q is written by the prologue
+    load_qhi(u_first);
+    int u = u_first, seg = -1;
+    float m_ref = -INFINITY, l = 0.f;  // l: this half's share of the row sum
+    uint8_t* pbase = smem + L.p_off + kh * VM * 128;  // P's key region of this half
+    for (int k = 0; k < nt; ++k) {
+      const int un = unit_at(k, u);
+      const bool seg_first = un != u || k == 0;
+      u = un;
+      const bool seg_last = k == nt - 1 || g0 + k + 1 >= PT[u + 1];
+      if (seg_first) {
+        ++seg;
+        m_ref = -INFINITY;
+        l = 0.f;
+      }
+      if (!__all_sync(0xffffffffu, W.wait(B_SFULL, k & 1))) break;
+      tc::fence_after();
+      // this row's scores of the half-tile, then S is free for the next Q K^T
+      float sv[64];
+      tc::ld64(tmem + lane_off + Col::S + 64 * kh, *reinterpret_cast<uint32_t(*)[64]>(sv));
+      tc::wait_ld();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + 8 * B_SFREE);
+      // the next unit's q_hi, as soon as this segment's Q K^T completed
+      // (already true: it completed before this tile's scores were read)
+      if (seg_last && k + 1 < nt) {
+        if (!__all_sync(0xffffffffu, W.wait(B_QFREE, seg & 1))) break;
+        load_qhi(unit_at(k + 1, u));
+      }
+      // (the tile's group masks were written before its first copy was issued)
+      const int e = (k % kTileRing) * 8 + 4 * kh;
+      const uint32_t km0 = t < R ? static_cast<uint32_t>(TMASK[e]) | (static_cast<uint32_t>(TMASK[e + 1]) << 16) : 0u;
+      const uint32_t km1 = t < R ? static_cast<uint32_t>(TMASK[e + 2]) | (static_cast<uint32_t>(TMASK[e + 3]) << 16) : 0u;
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int x = 0; x < 64; ++x) {
+        if (!(((x < 32 ? km0 : km1) >> (x & 31)) & 1u)) sv[x] = -INFINITY;
+        mx[x & 3] = fmaxf(mx[x & 3], sv[x]);
+      }
+      // (two buffers by tile parity: a half may start the next tile while its
+      // partner still reads this one's)
+      float* xm = XMAX + (k & 1) * 256;
+      xm[kh * 128 + t] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      pair_sync();
+      const float tmax = fmaxf(xm[t], xm[128 + t]);
+      const bool need = tmax > m_ref + kRescaleLog2;
+      const float f = need ? exp2_fast(m_ref - tmax) : 1.f;  // 0 when the reference was -inf
+      if (need) {
+        l *= f;
+        m_ref = tmax;
+      }
+      // P and O are free, and O complete, once the previous tile's P V completed
+      if (k > 0 && !__all_sync(0xffffffffu, W.wait(B_PVDONE, (k - 1) & 1))) break;
+      tc::fence_after();
+      // Rows whose reference moved rescale their output so far (this half of
+      // its columns). The TMEM loads and stores are warp-wide, so the warp
+      // takes them together (factor 1 for the other rows).
+      if (!seg_first && __any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+        for (int cc = kh * (D / 64); cc < (kh + 1) * (D / 64); ++cc) {
+          uint32_t o[32];
+          tc::ld32(tmem + lane_off + Col::O + cc * 32, o);
+          tc::wait_ld();
+#pragma unroll
+          for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * f);
+          tc::st32(tmem + lane_off + Col::O + cc * 32, o);
+        }
+        tc::wait_st();
+      }
+      // probabilities in fp16 into P (row t, this half's 64 keys: one 128-byte
+      // row, 16-byte chunks of 8 keys swizzled by the row); the row sum uses
+      // the same rounded values
+      float ls[2] = {0.f, 0.f};
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        uint32_t w4[4];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const float s0 = sv[8 * c8 + 2 * x], s1 = sv[8 * c8 + 2 * x + 1];
+          const float p0 = s0 == -INFINITY ? 0.f : exp2_fast(s0 - m_ref);
+          const float p1 = s1 == -INFINITY ? 0.f : exp2_fast(s1 - m_ref);
+          const __half2 hp = __floats2half2_rn(p0, p1);
+          ls[x & 1] += __low2float(hp) + __high2float(hp);
+          w4[x] = *reinterpret_cast<const uint32_t*>(&hp);
+        }
+        *reinterpret_cast<uint4*>(pbase + t * 128 + ((c8 ^ (t & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      }
+      l += ls[0] + ls[1];
+      fence_proxy_async_smem();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + 8 * B_PFULL);
+      if (seg_last) {
+        // ---- the segment's partial state: o (relative to the reference), m, l
+        if (!__all_sync(0xffffffffu, W.wait(B_PVDONE, k & 1))) break;
         tc::fence_after();
         const int slot = seg == 0 ? cta : NC + u;
-        float* dst = a.part + (static_cast<int64_t>(slot) * R + t) * row_stride<D>();
+        float* dst = nullptr;
+        if (t < R) {
+          const int i = t / G, g = t - i * G;
+          dst = a.part + (static_cast<int64_t>(slot) * R + g * T + i) * row_stride<D>();
+        }
 #pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = kh * (D / 64); cc < (kh + 1) * (D / 64); ++cc) {
           uint32_t o[32];
-          tc::ld32(tmem + lane_off + V::O_COL + cc * 32, o);
+          tc::ld32(tmem + lane_off + Col::O + cc * 32, o);
           tc::wait_ld();
-          if (t < R) {
+          if (dst) {
 #pragma unroll
             for (int x = 0; x < 32; x += 4)
               *reinterpret_cast<float4*>(dst + cc * 32 + x) =
@@ -521,28 +618,28 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
                               __uint_as_float(o[x + 3]));
           }
         }
-        if (t < R) {
+        XL[kh * 128 + t] = l;
+        pair_sync();
+        if (dst && kh == 0) {
           dst[D] = m_ref;
-          dst[D + 1] = l;
+          dst[D + 1] = XL[t] + XL[128 + t];
         }
         tc::fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(sbase + V::BAR_OFF + 8 * B_OFREE);
-        ++seg;
+        if (lane == 0) mbar_arrive(bars + 8 * B_OFREE);
       }
-      prev_u = u;
     }
   }
 
   tc::fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (nt > 0 && warp == kMmaWarp) {
     tc::fence_after();
-    tc::dealloc(tmem, V::TMEM_COLS);
+    tc::dealloc(tmem, Col::TOTAL > 256 ? 512 : 256);
   }
   // The combine may begin once every CTA of this pass has triggered, and each
-  // one does so only after the prologue has completed: so the combine reads the
-  // rotated q and window keys before waiting for this pass.
+  // one does so only after the prologue has completed: so the combine reads
+  // the rotated q and window keys before waiting for this pass.
   pdl_wait();
   pdl_trigger();
 }
@@ -718,11 +815,12 @@ __global__ void __launch_bounds__(256) verify_combine_kernel(const VerifyCombine
 
 template <int D>
 cudaError_t verify_split_launch(const VerifySplitArgs& a, cudaStream_t s) {
-  using V = VGeo<D>;
   static std::atomic<uint64_t> opted{0};
-  const cudaError_t e = opt_in_smem(verify_split_kernel<D>, V::SMEM, opted);
+  const cudaError_t e = opt_in_smem(verify_split_kernel<D>, kSmemLimit, opted);
   if (e != cudaSuccess) return e;
-  return launch_pdl(verify_split_kernel<D>, dim3(a.ctas), dim3(kVThreads), V::SMEM, s, a);
+  const VLayout L = verify_layout(D, a.S * a.Hkv);
+  if (L.cv < 2 || L.total > kSmemLimit) return cudaErrorNotSupported;
+  return launch_pdl(verify_split_kernel<D>, dim3(a.ctas), dim3(kVThreads), static_cast<size_t>(L.total), s, a);
 }
 
 }  // namespace

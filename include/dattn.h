@@ -67,8 +67,9 @@ enum {
   DATTN_ETIMEOUT = 5,      /* a bounded device wait gave up (dattn_get_error)     */
   DATTN_EUNSUPPORTED = 6,  /* a shape with no compiled kernel                     */
   DATTN_ELENGTH = 7,       /* a stream longer than the call's bound (get_error)   */
-  DATTN_ERANGE = 8         /* verify: a cached K/V value beyond the fp16 range
-                              (|x| >= 65520) the tensor-core pass computes in     */
+  DATTN_ERANGE = 8         /* verify: a cached V value beyond the fp16 range
+                              (|x| >= 65520) in which the tensor-core pass forms
+                              P V (from dattn_get_error)                          */
 };
 
 enum { DATTN_CACHE_RING = 0, DATTN_CACHE_PAGED = 1 };

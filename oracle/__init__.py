@@ -33,6 +33,20 @@ def _i32(a):
     return None if a is None else np.ascontiguousarray(a, dtype=np.int32)
 
 
+def _norm(qk_norm):
+    """QK-norm arguments: qk_norm = (q weights, k weights, eps) as bf16 [D]
+    arrays and a float, or None for a layer without QK-norm."""
+    if qk_norm is None:
+        return (None, None, 0.0)
+    qw, kw, eps = qk_norm
+    global _keep_norm
+    _keep_norm = (_u16(qw), _u16(kw))
+    return (_ptr(_keep_norm[0]), _ptr(_keep_norm[1]), float(eps))
+
+
+_keep_norm = None
+
+
 class Oracle:
     """One loaded build of the oracle (mutation 0 is the real one)."""
 
@@ -48,18 +62,21 @@ class Oracle:
         L.oracle_rope_cos_sin.restype = None
         L.oracle_rope_f64.argtypes = [_P, _I, _I, _D, _L, _P]
         L.oracle_rope_bf16.argtypes = [_P, _I, _I, _D, _L, _P]
+        N3 = [_P, _P, _D]  # QK-norm: q weight, k weight (bf16 [D] or null), eps
         L.oracle_decode_ring.argtypes = [_I, _I, _I, _I, _I, _D, _P, _P, _I, _I, _P, _P, _P,
-                                         _P, _P, _P, _P, _P, _P, _P, _P, _I]
+                                         _P, _P, _P, _P, _P, _P, _P, _P, _I] + N3
         L.oracle_decode_paged.argtypes = [_I, _I, _I, _I, _I, _D, _P, _P, _I, _I, _P, _I, _P,
-                                          _P, _P, _P, _P, _P, _P, _P, _P, _I]
+                                          _P, _P, _P, _P, _P, _P, _P, _P, _I] + N3
         L.oracle_decode_concat.argtypes = [_I, _I, _I, _I, _I, _D, _P, _P, _I, _P, _P, _P, _P,
-                                           _P, _P, _P, _I]
+                                           _P, _P, _P, _I] + N3
         L.oracle_verify.argtypes = [_I, _I, _I, _I, _I, _I, _D, _P, _P, _I, _I, _P, _I, _P,
-                                    _P, _P, _P, _P, _P, _P, _P, _I]
+                                    _P, _P, _P, _P, _P, _P, _P, _I] + N3
         L.oracle_append_ring.argtypes = [_I, _I, _I, _I, _I, _D, _P, _P, _I, _I, _P, _P, _P,
-                                         _P, _P, _P, _I]
+                                         _P, _P, _P, _I, _P, _D]
         L.oracle_append_paged.argtypes = [_I, _I, _I, _I, _I, _D, _P, _P, _I, _I, _P, _I, _P,
-                                          _P, _P, _P, _P, _I]
+                                          _P, _P, _P, _P, _I, _P, _D]
+        L.oracle_qk_norm.argtypes = [_P, _P, _I, _D, _P]
+        L.oracle_qk_norm.restype = None
         for f in ("oracle_rope_f64", "oracle_rope_bf16", "oracle_decode_ring",
                   "oracle_decode_paged", "oracle_decode_concat", "oracle_verify",
                   "oracle_append_ring", "oracle_append_paged", "oracle_hardware_threads"):
@@ -89,6 +106,13 @@ class Oracle:
         self._check(self.lib.oracle_rope_f64(_ptr(x), x.shape[-1], r, theta, pos, _ptr(out)), "rope")
         return out
 
+    def qk_norm(self, x, w, eps):
+        """QK-norm of one bf16 head vector x with bf16 weights w: bf16 bits."""
+        x, w = _u16(x), _u16(w)
+        out = np.empty(x.shape[-1], np.uint16)
+        self.lib.oracle_qk_norm(_ptr(x), _ptr(w), x.shape[-1], float(eps), _ptr(out))
+        return out
+
     def rope_bf16(self, x, r, theta, pos):
         x = _u16(x)
         out = np.empty(x.shape[-1], np.uint16)
@@ -97,7 +121,7 @@ class Oracle:
 
     # ---- decode
     def decode_ring(self, k_ring, v_ring, ring_head, ring_count, q, k_new, v_new, pos,
-                    r, theta, gate=None, stream_rows=None, n_threads=0):
+                    r, theta, gate=None, stream_rows=None, n_threads=0, qk_norm=None):
         """k_ring/v_ring [rows, Hkv, R, D]; q [B, Hq, D]; k_new/v_new [B, Hkv, D].
         Returns (out [B,Hq,D] f64, k_entry [B,Hkv,D] u16, v_entry [B,Hkv,D] u16)."""
         k_ring, v_ring, q, k_new, v_new = map(_u16, (k_ring, v_ring, q, k_new, v_new))
@@ -111,12 +135,12 @@ class Oracle:
         rc = self.lib.oracle_decode_ring(B, Hq, Hkv, D, r, theta, _ptr(k_ring), _ptr(v_ring),
                                          n_rows, R, _ptr(sr), _ptr(hd), _ptr(ct), _ptr(q),
                                          _ptr(k_new), _ptr(v_new), _ptr(gate), _ptr(ps),
-                                         _ptr(out), _ptr(ke), _ptr(ve), n_threads)
+                                         _ptr(out), _ptr(ke), _ptr(ve), n_threads, *_norm(qk_norm))
         self._check(rc, "decode_ring")
         return out, ke, ve
 
     def decode_paged(self, k_pages, v_pages, block_table, seq_len, q, k_new, v_new, pos,
-                     r, theta, gate=None, n_threads=0):
+                     r, theta, gate=None, n_threads=0, qk_norm=None):
         """k_pages/v_pages [num_pages, Hkv, P, D]; block_table [B, max_pages]."""
         k_pages, v_pages, q, k_new, v_new = map(_u16, (k_pages, v_pages, q, k_new, v_new))
         gate = None if gate is None else _u16(gate)
@@ -130,12 +154,13 @@ class Oracle:
         rc = self.lib.oracle_decode_paged(B, Hq, Hkv, D, r, theta, _ptr(k_pages), _ptr(v_pages),
                                           num_pages, P, _ptr(bt), bt.shape[1], _ptr(sl),
                                           _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(gate),
-                                          _ptr(ps), _ptr(out), _ptr(ke), _ptr(ve), n_threads)
+                                          _ptr(ps), _ptr(out), _ptr(ke), _ptr(ve), n_threads,
+                                          *_norm(qk_norm))
         self._check(rc, "decode_paged")
         return out, ke, ve
 
     def decode_concat(self, k_chrono, v_chrono, count, q, k_new, v_new, pos, r, theta,
-                      gate=None, n_threads=0):
+                      gate=None, n_threads=0, qk_norm=None):
         """Key-space twin: k_chrono/v_chrono [B, Hkv, cap, D] oldest first."""
         k_chrono, v_chrono, q, k_new, v_new = map(_u16, (k_chrono, v_chrono, q, k_new, v_new))
         gate = None if gate is None else _u16(gate)
@@ -146,13 +171,13 @@ class Oracle:
         rc = self.lib.oracle_decode_concat(B, Hq, Hkv, D, r, theta, _ptr(k_chrono),
                                            _ptr(v_chrono), cap, _ptr(ct), _ptr(q), _ptr(k_new),
                                            _ptr(v_new), _ptr(gate), _ptr(ps), _ptr(out),
-                                           n_threads)
+                                           n_threads, *_norm(qk_norm))
         self._check(rc, "decode_concat")
         return out
 
     # ---- verify
     def verify(self, k_pages, v_pages, block_table, prefix_len, q, k, v, parent, r, theta,
-               gate=None, n_threads=0):
+               gate=None, n_threads=0, qk_norm=None):
         """q [S,T,Hq,D]; k/v [S,T,Hkv,D]; parent [S,T]. Returns (out f64, k_entry u16)."""
         k_pages, v_pages, q, k, v = map(_u16, (k_pages, v_pages, q, k, v))
         gate = None if gate is None else _u16(gate)
@@ -165,13 +190,13 @@ class Oracle:
         rc = self.lib.oracle_verify(S, T, Hq, Hkv, D, r, theta, _ptr(k_pages), _ptr(v_pages),
                                     num_pages, P, _ptr(bt), bt.shape[1], _ptr(pl), _ptr(q),
                                     _ptr(k), _ptr(v), _ptr(pa), _ptr(gate), _ptr(out), _ptr(ke),
-                                    n_threads)
+                                    n_threads, *_norm(qk_norm))
         self._check(rc, "verify")
         return out, ke
 
     # ---- append (returns updated copies)
     def append_ring(self, k_ring, v_ring, start_index, start_pos, count, k, v, r, theta,
-                    rotate=True, stream_rows=None):
+                    rotate=True, stream_rows=None, qk_norm=None):
         kr, vr = _u16(k_ring).copy(), _u16(v_ring).copy()
         k, v = _u16(k), _u16(v)
         n_rows, Hkv, R, D = kr.shape
@@ -179,12 +204,12 @@ class Oracle:
         rc = self.lib.oracle_append_ring(B, Tmax, Hkv, D, r, theta, _ptr(kr), _ptr(vr), n_rows, R,
                                          _ptr(_i32(stream_rows)), _ptr(_i32(start_index)),
                                          _ptr(_i32(start_pos)), _ptr(_i32(count)), _ptr(k),
-                                         _ptr(v), int(rotate))
+                                         _ptr(v), int(rotate), *_norm(qk_norm)[1:])
         self._check(rc, "append_ring")
         return kr, vr
 
     def append_paged(self, k_pages, v_pages, block_table, start_index, start_pos, count, k, v,
-                     r, theta, rotate=True):
+                     r, theta, rotate=True, qk_norm=None):
         kp, vp = _u16(k_pages).copy(), _u16(v_pages).copy()
         k, v = _u16(k), _u16(v)
         num_pages, Hkv, P, D = kp.shape
@@ -193,7 +218,8 @@ class Oracle:
         rc = self.lib.oracle_append_paged(B, Tmax, Hkv, D, r, theta, _ptr(kp), _ptr(vp),
                                           num_pages, P, _ptr(bt), bt.shape[1],
                                           _ptr(_i32(start_index)), _ptr(_i32(start_pos)),
-                                          _ptr(_i32(count)), _ptr(k), _ptr(v), int(rotate))
+                                          _ptr(_i32(count)), _ptr(k), _ptr(v), int(rotate),
+                                          *_norm(qk_norm)[1:])
         self._check(rc, "append_paged")
         return kp, vp
 

@@ -226,6 +226,44 @@ void rope_entry(const uint16_t* x, int D, int r, double theta, int64_t pos, uint
   }
 }
 
+// ---------------------------------------------------------------- QK-norm
+
+// Per-head RMS norm applied to q and to the new key before RoPE ("pega-omni
+// PR #4", the talker kernels: RoPE with QK-norm). Reading (the pages give no
+// formula): each head vector x of length D becomes
+//   y_d = w_d * x_d / sqrt(mean(x^2) + eps),
+// the exact value rounded once to bf16 (the layer's type), with one weight
+// vector w (bf16, [D]) per layer for q and one for k; RoPE then turns y.
+void qk_norm(const uint16_t* x, const uint16_t* w, int D, double eps, uint16_t* y) {
+  double ss = 0.0;
+  for (int d = 0; d < D; ++d) ss += bf16_value(x[d]) * bf16_value(x[d]);
+#if ORACLE_MUTATION == 19
+  const double inv = 1.0 / (std::sqrt(ss / D) + eps);  // planted: eps outside the root
+#elif ORACLE_MUTATION == 20
+  const double inv = 1.0 / std::sqrt(ss + eps);  // planted: sum instead of mean
+#else
+  const double inv = 1.0 / std::sqrt(ss / D + eps);
+#endif
+  for (int d = 0; d < D; ++d) y[d] = bf16_round(bf16_value(w[d]) * bf16_value(x[d]) * inv);
+}
+
+// The vector RoPE turns: x itself, or its QK-norm when the layer has one.
+const uint16_t* normed(const uint16_t* x, const uint16_t* w, int D, double eps, std::vector<uint16_t>& buf) {
+  if (!w) return x;
+  buf.resize(D);
+  qk_norm(x, w, D, eps, buf.data());
+  return buf.data();
+}
+
+// A layer's rotation: RoPE dims and base, and its QK-norm weights (or null).
+struct Rot {
+  int r;
+  double theta;
+  const uint16_t* qn;
+  const uint16_t* kn;
+  double eps;
+};
+
 double sigmoid(double g) {
 #if ORACLE_MUTATION == 12
   return 1.0 / (1.0 + std::exp(g));  // planted: sigmoid(-g)
@@ -363,11 +401,14 @@ struct DecodeTail {
 
 // Shared per-(stream, KV head) step of every decode form once the list of
 // valid cached rows is known: rotate, score in score space, gate, entries.
-void decode_one(int b, int j, int Hq, int Hkv, int D, int r, double theta,
+void decode_one(int b, int j, int Hq, int Hkv, int D, const Rot& rot,
                 const std::vector<const uint16_t*>& ck, const std::vector<const uint16_t*>& cv,
                 const DecodeTail& a) {
+  const int r = rot.r;
+  const double theta = rot.theta;
   const int64_t pos = a.pos[b];
-  const uint16_t* kn = a.k_new + (static_cast<size_t>(b) * Hkv + j) * D;
+  std::vector<uint16_t> kbuf, qbuf;
+  const uint16_t* kn = normed(a.k_new + (static_cast<size_t>(b) * Hkv + j) * D, rot.kn, D, rot.eps, kbuf);
   const uint16_t* vn = a.v_new + (static_cast<size_t>(b) * Hkv + j) * D;
   std::vector<uint16_t> entry(D);
   rope_entry(kn, D, r, theta, pos, entry.data());
@@ -378,7 +419,8 @@ void decode_one(int b, int j, int Hq, int Hkv, int D, int r, double theta,
   std::vector<double> qhat(D);
   for (int h = 0; h < Hq; ++h) {
     if (kv_head_of(h, Hq, Hkv) != j) continue;
-    rope_rotate(a.q + (static_cast<size_t>(b) * Hq + h) * D, D, r, theta, pos, qhat.data());
+    rope_rotate(normed(a.q + (static_cast<size_t>(b) * Hq + h) * D, rot.qn, D, rot.eps, qbuf), D, r, theta, pos,
+                qhat.data());
     double* o = a.out + (static_cast<size_t>(b) * Hq + h) * D;
     attend_score_space(qhat.data(), D, ck, cv, {kent.data()}, {vn}, o);
 #if ORACLE_MUTATION != 4
@@ -418,6 +460,11 @@ int oracle_rope_f64(const uint16_t* x, int D, int r, double theta, int64_t pos, 
   return 0;
 }
 
+// QK-norm of one head vector (qk_norm), for the pins.
+void oracle_qk_norm(const uint16_t* x, const uint16_t* w, int D, double eps, uint16_t* y) {
+  qk_norm(x, w, D, eps, y);
+}
+
 int oracle_rope_bf16(const uint16_t* x, int D, int r, double theta, int64_t pos, uint16_t* out) {
   if (D <= 0 || r < 0 || r > D || r % 2) return 1;
   rope_entry(x, D, r, theta, pos, out);
@@ -432,8 +479,10 @@ int oracle_decode_ring(int B, int Hq, int Hkv, int D, int r, double theta,
                        const int32_t* stream_rows, const int32_t* ring_head,
                        const int32_t* ring_count, const uint16_t* q, const uint16_t* k_new,
                        const uint16_t* v_new, const uint16_t* gate, const int32_t* pos,
-                       double* out, uint16_t* k_entry, uint16_t* v_entry, int n_threads) {
+                       double* out, uint16_t* k_entry, uint16_t* v_entry, int n_threads,
+                       const uint16_t* q_norm, const uint16_t* k_norm, double norm_eps) {
   if (!shape_ok(Hq, Hkv, D, r) || R <= 0) return 1;
+  const Rot rot{r, theta, q_norm, k_norm, norm_eps};
   for (int b = 0; b < B; ++b) {
     const int row = stream_rows ? stream_rows[b] : b;
     if (row < 0 || row >= n_rows) return 2;
@@ -454,7 +503,7 @@ int oracle_decode_ring(int B, int Hq, int Hkv, int D, int r, double theta,
       ck.push_back(k_ring + (base + slot) * D);
       cv.push_back(v_ring + (base + slot) * D);
     }
-    decode_one(b, j, Hq, Hkv, D, r, theta, ck, cv, tail);
+    decode_one(b, j, Hq, Hkv, D, rot, ck, cv, tail);
   });
   return 0;
 }
@@ -467,8 +516,10 @@ int oracle_decode_paged(int B, int Hq, int Hkv, int D, int r, double theta,
                         const int32_t* block_table, int bt_stride, const int32_t* seq_len,
                         const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
                         const uint16_t* gate, const int32_t* pos, double* out,
-                        uint16_t* k_entry, uint16_t* v_entry, int n_threads) {
+                        uint16_t* k_entry, uint16_t* v_entry, int n_threads,
+                        const uint16_t* q_norm, const uint16_t* k_norm, double norm_eps) {
   if (!shape_ok(Hq, Hkv, D, r) || P <= 0) return 1;
+  const Rot rot{r, theta, q_norm, k_norm, norm_eps};
   for (int b = 0; b < B; ++b) {
     if (seq_len[b] < 0 || (seq_len[b] + P - 1) / P > bt_stride) return 2;
     for (int t = 0; t < seq_len[b]; t += P) {
@@ -491,7 +542,7 @@ int oracle_decode_paged(int B, int Hq, int Hkv, int D, int r, double theta,
       ck.push_back(k_pages + row);
       cv.push_back(v_pages + row);
     }
-    decode_one(b, j, Hq, Hkv, D, r, theta, ck, cv, tail);
+    decode_one(b, j, Hq, Hkv, D, rot, ck, cv, tail);
   });
   return 0;
 }
@@ -504,7 +555,8 @@ int oracle_decode_concat(int B, int Hq, int Hkv, int D, int r, double theta,
                          const uint16_t* k_chrono, const uint16_t* v_chrono, int cap,
                          const int32_t* count, const uint16_t* q, const uint16_t* k_new,
                          const uint16_t* v_new, const uint16_t* gate, const int32_t* pos,
-                         double* out, int n_threads) {
+                         double* out, int n_threads, const uint16_t* q_norm, const uint16_t* k_norm,
+                         double norm_eps) {
   if (!shape_ok(Hq, Hkv, D, r)) return 1;
   for (int b = 0; b < B; ++b)
     if (count[b] < 0 || count[b] > cap) return 2;
@@ -520,15 +572,16 @@ int oracle_decode_concat(int B, int Hq, int Hkv, int D, int r, double theta,
           K[t * D + d] = bf16_value(k_chrono[(base + t) * D + d]);
           V[t * D + d] = bf16_value(v_chrono[(base + t) * D + d]);
         }
-      std::vector<uint16_t> entry(D);
+      std::vector<uint16_t> entry(D), kbuf, qbuf;
       const size_t nb = (static_cast<size_t>(b) * Hkv + j) * D;
-      rope_entry(k_new + nb, D, r, theta, pos[b], entry.data());
+      rope_entry(normed(k_new + nb, k_norm, D, norm_eps, kbuf), D, r, theta, pos[b], entry.data());
       for (int d = 0; d < D; ++d) {
         K[(rows - 1) * D + d] = bf16_value(entry[d]);
         V[(rows - 1) * D + d] = bf16_value(v_new[nb + d]);
       }
       std::vector<double> qhat(D);
-      rope_rotate(q + (static_cast<size_t>(b) * Hq + h) * D, D, r, theta, pos[b], qhat.data());
+      rope_rotate(normed(q + (static_cast<size_t>(b) * Hq + h) * D, q_norm, D, norm_eps, qbuf), D, r, theta, pos[b],
+                  qhat.data());
       double* o = out + (static_cast<size_t>(b) * Hq + h) * D;
       attend_key_matrix(qhat.data(), D, K, V, rows, o);
       if (gate) {
@@ -551,7 +604,8 @@ int oracle_verify(int S, int T, int Hq, int Hkv, int D, int r, double theta,
                   const int32_t* block_table, int bt_stride, const int32_t* prefix_len,
                   const uint16_t* q, const uint16_t* k, const uint16_t* v,
                   const int32_t* parent, const uint16_t* gate, double* out,
-                  uint16_t* k_entry, int n_threads) {
+                  uint16_t* k_entry, int n_threads, const uint16_t* q_norm, const uint16_t* k_norm,
+                  double norm_eps) {
   if (!shape_ok(Hq, Hkv, D, r) || P <= 0 || T <= 0) return 1;
   for (int s = 0; s < S; ++s) {
     if (prefix_len[s] < 0 || (prefix_len[s] + P - 1) / P > bt_stride) return 2;
@@ -583,7 +637,9 @@ int oracle_verify(int S, int T, int Hq, int Hkv, int D, int r, double theta,
     std::vector<double> entd(static_cast<size_t>(T) * D);
     for (int i = 0; i < T; ++i) {
       const size_t src = ((static_cast<size_t>(s) * T + i) * Hkv + j) * D;
-      rope_entry(k + src, D, r, theta, prefix_len[s] + depth[i], ent.data() + static_cast<size_t>(i) * D);
+      std::vector<uint16_t> kbuf;
+      rope_entry(normed(k + src, k_norm, D, norm_eps, kbuf), D, r, theta, prefix_len[s] + depth[i],
+                 ent.data() + static_cast<size_t>(i) * D);
       for (int d = 0; d < D; ++d) entd[static_cast<size_t>(i) * D + d] = bf16_value(ent[static_cast<size_t>(i) * D + d]);
       if (k_entry) std::memcpy(k_entry + src, ent.data() + static_cast<size_t>(i) * D, D * 2);
     }
@@ -611,7 +667,9 @@ int oracle_verify(int S, int T, int Hq, int Hkv, int D, int r, double theta,
       for (int h = 0; h < Hq; ++h) {
         if (kv_head_of(h, Hq, Hkv) != j) continue;
         const size_t qi = (static_cast<size_t>(s) * T + i) * Hq + h;
-        rope_rotate(q + qi * D, D, r, theta, prefix_len[s] + depth[i], qhat.data());
+        std::vector<uint16_t> qbuf;
+        rope_rotate(normed(q + qi * D, q_norm, D, norm_eps, qbuf), D, r, theta, prefix_len[s] + depth[i],
+                    qhat.data());
         double* o = out + qi * D;
         attend_score_space(qhat.data(), D, ck, cv, ek, ev, o);
         if (gate) {
@@ -633,9 +691,10 @@ int oracle_append_ring(int B, int Tmax, int Hkv, int D, int r, double theta,
                        uint16_t* k_ring, uint16_t* v_ring, int n_rows, int R,
                        const int32_t* stream_rows, const int32_t* start_index,
                        const int32_t* start_pos, const int32_t* count,
-                       const uint16_t* k, const uint16_t* v, int rotate) {
+                       const uint16_t* k, const uint16_t* v, int rotate, const uint16_t* k_norm,
+                       double norm_eps) {
   if (D <= 0 || r < 0 || r > D || r % 2 || R <= 0) return 1;
-  std::vector<uint16_t> entry(D);
+  std::vector<uint16_t> entry(D), kbuf;
   for (int b = 0; b < B; ++b) {
     const int row = stream_rows ? stream_rows[b] : b;
     // at most one ring's worth per call: each slot is written at most once
@@ -651,7 +710,7 @@ int oracle_append_ring(int B, int Tmax, int Hkv, int D, int r, double theta,
 #endif
         const size_t dst = ((static_cast<size_t>(row) * Hkv + j) * R + slot) * D;
         if (rotate)
-          rope_entry(k + src, D, r, theta, start_pos[b] + t, entry.data());
+          rope_entry(normed(k + src, k_norm, D, norm_eps, kbuf), D, r, theta, start_pos[b] + t, entry.data());
         else
           std::memcpy(entry.data(), k + src, D * 2);
         std::memcpy(k_ring + dst, entry.data(), D * 2);
@@ -666,9 +725,10 @@ int oracle_append_paged(int B, int Tmax, int Hkv, int D, int r, double theta,
                         uint16_t* k_pages, uint16_t* v_pages, int num_pages, int P,
                         const int32_t* block_table, int bt_stride, const int32_t* start_index,
                         const int32_t* start_pos, const int32_t* count,
-                        const uint16_t* k, const uint16_t* v, int rotate) {
+                        const uint16_t* k, const uint16_t* v, int rotate, const uint16_t* k_norm,
+                        double norm_eps) {
   if (D <= 0 || r < 0 || r > D || r % 2 || P <= 0) return 1;
-  std::vector<uint16_t> entry(D);
+  std::vector<uint16_t> entry(D), kbuf;
   for (int b = 0; b < B; ++b) {
     if (count[b] < 0 || count[b] > Tmax || start_index[b] < 0) return 2;
     if (count[b] > 0 && (start_index[b] + count[b] - 1) / P >= bt_stride) return 2;
@@ -680,7 +740,7 @@ int oracle_append_paged(int B, int Tmax, int Hkv, int D, int r, double theta,
         const size_t src = ((static_cast<size_t>(b) * Tmax + t) * Hkv + j) * D;
         const size_t dst = ((static_cast<size_t>(pg) * Hkv + j) * P + idx % P) * D;
         if (rotate)
-          rope_entry(k + src, D, r, theta, start_pos[b] + t, entry.data());
+          rope_entry(normed(k + src, k_norm, D, norm_eps, kbuf), D, r, theta, start_pos[b] + t, entry.data());
         else
           std::memcpy(entry.data(), k + src, D * 2);
         std::memcpy(k_pages + dst, entry.data(), D * 2);

@@ -47,7 +47,8 @@ def test_append_ring(dattn, oracle, rotate, D, Hkv, r, theta):
     layer = {"kind": dattn.CACHE_RING, "ring_slots": R, "rotary_dim": r, "rope_theta": theta}
     h = dattn.Handle(Hkv * 2, Hkv, D, [layer], B)
     zeros = torch.zeros(B, dtype=torch.int32, device="cuda")
-    desc = dattn.ring_cache(kd, vd, zeros, zeros, dev(stream_rows))
+    rows_d = dev(stream_rows)  # the descriptor holds raw pointers: keep the tensors alive
+    desc = dattn.ring_cache(kd, vd, zeros, zeros, rows_d)
     h.append_kv(0, desc, dev(k), dev(v), dev(start_index), dev(count), start_pos=dev(start_pos),
                 rotate=rotate)
     assert h.get_error() == dattn.OK
@@ -85,7 +86,8 @@ def test_append_paged(dattn, oracle, rotate, D, Hkv, P, r, theta):
     layer = {"kind": dattn.CACHE_PAGED, "page_size": P, "rotary_dim": r, "rope_theta": theta}
     h = dattn.Handle(Hkv * 2, Hkv, D, [layer], B, max_context=int(bt.shape[1] * P))
     seq = torch.zeros(B, dtype=torch.int32, device="cuda")
-    desc = dattn.paged_cache(kd, vd, dev(bt), seq)
+    bt_d = dev(bt)
+    desc = dattn.paged_cache(kd, vd, bt_d, seq)
     h.append_kv(0, desc, dev(k), dev(v), dev(starts), dev(count), start_pos=dev(start_pos), rotate=rotate)
     assert h.get_error() == dattn.OK
     Ko, Vo = oracle.append_paged(Kp, Vp, bt, starts, start_pos, count, k, v, r, theta, rotate=rotate)
@@ -110,7 +112,8 @@ def test_append_then_decode_equals_oracle(dattn, oracle):
     layer = {"kind": dattn.CACHE_RING, "ring_slots": R, "rotary_dim": 256, "rope_theta": 1e4}
     h = dattn.Handle(Hq, Hkv, D, [layer], B)
     head = ((start + n) % R).astype(np.int32)
-    desc = dattn.ring_cache(kd, vd, dev(head), dev(count))
+    head_d, count_d = dev(head), dev(count)
+    desc = dattn.ring_cache(kd, vd, head_d, count_d)
     h.append_kv(0, desc, dev(k), dev(v), dev(start), dev(count), start_pos=dev(pos0))
     Ko, Vo = oracle.append_ring(Kr, Vr, start, pos0, count, k, v, 256, 1e4)
     x = synth.decode_inputs(gen, B, Hq, Hkv, D, [n, n], gate=True)

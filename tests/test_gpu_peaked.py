@@ -4,7 +4,7 @@ Synthetic N(0, 1) queries and keys at head_dim 256 give scores of standard
 deviation about 1: a nearly flat softmax. These cases make it peaked, where
 the kernels' precision choices matter - decode's hi/lo bf16 split of q and of
 the probabilities and its rescale only when a running maximum moves; verify's
-fp16 q and P and its lazy rescale (threshold 2^8 in base-2 units):
+hi/lo bf16 q, fp16 P and its lazy rescale (threshold 2^8 in base-2 units):
   * q scaled by 8 and by 32 (exact in bf16);
   * one cached key equal to a multiple of a head's rotated query, placed early,
     mid-stream and as the last key, so that the running maximum jumps by far
@@ -169,8 +169,9 @@ def run_verify(dattn, oracle, case, expect=None):
              "rope_theta": case.rope.theta}
     h = dattn.Handle(case.Hq, case.Hkv, case.D, [layer], S, max_context=int(c.seq_len.max()) or 1,
                      max_verify_rows=T)
-    h.verify(0, dattn.paged_cache(dev(c.k), dev(c.v), dev(c.block_table), dev(c.seq_len)), dev(case.q),
-             dev(case.k), dev(case.v), dev(case.parent), out, write_back=False)
+    keep = [dev(c.k), dev(c.v), dev(c.block_table), dev(c.seq_len)]  # the descriptor holds raw pointers
+    h.verify(0, dattn.paged_cache(*keep), dev(case.q), dev(case.k), dev(case.v), dev(case.parent), out,
+             write_back=False)
     status = h.get_error()
     h.close()
     if expect is not None:
@@ -180,6 +181,13 @@ def run_verify(dattn, oracle, case, expect=None):
     ref, _ = oracle.verify(c.k, c.v, c.block_table, c.seq_len, case.q, case.k, case.v, case.parent,
                            case.rope.rotary_dim, case.rope.theta)
     return assert_close(out.cpu().numpy(), ref, "peaked verify")
+
+
+@pytest.mark.parametrize("scale", [8.0, 32.0])
+def test_verify_scaled_queries(dattn, oracle, scale):
+    case = verify_case(600, 4, 16, [3000, 700, 64, 1500])
+    case.q = to_bf16(bf16_val(case.q) * scale)
+    run_verify(dattn, oracle, case)
 
 
 def test_verify_dominant_prefix_keys(dattn, oracle):
@@ -221,13 +229,23 @@ def test_verify_tiny_values_stay_within_tolerance(dattn, oracle):
     run_verify(dattn, oracle, case)
 
 
-@pytest.mark.parametrize("which", ["k", "v"])
-def test_verify_value_beyond_fp16_is_reported(dattn, which):
-    """A cached K or V value of 65536 (a bf16 number beyond fp16's range) is
-    reported as DATTN_ERANGE; nothing faults."""
+def test_verify_value_beyond_fp16_is_reported(dattn):
+    """A cached V value of 65536 (a bf16 number beyond fp16's range, in which
+    the tensor-core pass forms P V) is reported as DATTN_ERANGE; nothing
+    faults."""
     import decode_attention_kv_dattn_gb300 as d
     case = verify_case(604, 2, 8, [500, 40])
     c = case.cache
-    pool = c.k if which == "k" else c.v
-    pool[c.block_table[0, 17 // c.P], 1, 17 % c.P, 5] = 0x4780  # 65536
+    c.v[c.block_table[0, 17 // c.P], 1, 17 % c.P, 5] = 0x4780  # 65536
     run_verify(dattn, None, case, expect=d.ERANGE)
+
+
+def test_verify_large_cached_keys(dattn, oracle):
+    """Keys enter the tensor cores as stored (bf16): a cached key element of
+    65536 (beyond fp16's range) is scored exactly and the rows it dominates
+    match the oracle."""
+    case = verify_case(605, 2, 8, [500, 40])
+    c = case.cache
+    c.k[c.block_table[0, 17 // c.P], 1, 17 % c.P, 5] = 0x4780  # 65536
+    c.k[c.block_table[1, 3 // c.P], 0, 3 % c.P, 9] = 0xC780   # -65536
+    run_verify(dattn, oracle, case)
