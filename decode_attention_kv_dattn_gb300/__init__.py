@@ -10,6 +10,7 @@ importing this package fails if libdattn.so has not been built (run
 import ctypes
 import os
 
+import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -32,7 +33,23 @@ _int = ctypes.c_int
 
 class LayerConfig(ctypes.Structure):
     _fields_ = [("cache_kind", _int), ("ring_slots", _int), ("page_size", _int),
-                ("rotary_dim", _int), ("rope_theta", ctypes.c_double)]
+                ("rotary_dim", _int), ("rope_theta", ctypes.c_double),
+                ("q_norm_weight", _vp), ("k_norm_weight", _vp), ("norm_eps", ctypes.c_double)]
+
+
+def _host_bf16(w, D, what):
+    """QK-norm weights as a contiguous host array of D bf16 bit patterns
+    (numpy uint16, or a CPU bfloat16 tensor), or None."""
+    if w is None:
+        return None
+    if isinstance(w, torch.Tensor):
+        if w.is_cuda or w.dtype != torch.bfloat16:
+            raise TypeError(f"{what}: a CPU bfloat16 tensor or a uint16 numpy array")
+        w = w.contiguous().view(torch.int16).numpy().view(np.uint16)
+    w = np.ascontiguousarray(w, dtype=np.uint16)
+    if w.shape != (D,):
+        raise ValueError(f"{what}: shape {w.shape}, expected ({D},)")
+    return w
 
 
 class Config(ctypes.Structure):
@@ -147,9 +164,21 @@ class Handle:
         if device is None:
             device = torch.cuda.current_device()
         self.device = device
-        self._layers = (LayerConfig * len(layers))(*[
-            LayerConfig(l["kind"], l.get("ring_slots", 0), l.get("page_size", 0),
-                        l.get("rotary_dim", 0), float(l.get("rope_theta", 0.0))) for l in layers])
+        # QK-norm weights (layer keys "q_norm", "k_norm", "norm_eps"): host
+        # arrays the config points at, kept alive with it (dattn_create copies
+        # them; decode_noalloc reads them on every call)
+        self._norm_keep = []
+        cfgs = []
+        for l in layers:
+            qn = _host_bf16(l.get("q_norm"), head_dim, "q_norm")
+            kn = _host_bf16(l.get("k_norm"), head_dim, "k_norm")
+            self._norm_keep += [qn, kn]
+            cfgs.append(LayerConfig(l["kind"], l.get("ring_slots", 0), l.get("page_size", 0),
+                                    l.get("rotary_dim", 0), float(l.get("rope_theta", 0.0)),
+                                    None if qn is None else qn.ctypes.data,
+                                    None if kn is None else kn.ctypes.data,
+                                    float(l.get("norm_eps", 0.0))))
+        self._layers = (LayerConfig * len(layers))(*cfgs)
         self.config = Config(num_q_heads, num_kv_heads, head_dim, max_streams, max_context,
                              max_verify_rows, len(layers), self._layers)
         h = _vp()

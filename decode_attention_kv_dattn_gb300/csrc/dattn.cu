@@ -50,6 +50,7 @@ struct dattn_handle {
   int max_streams = 0, max_context = 0, max_verify_rows = 0;
   std::vector<dattn_layer_config> layers;
   std::vector<uint64_t*> rope_step;  // device, per layer ([r/2] phase steps or null)
+  std::vector<uint16_t*> q_norm, k_norm;  // device, per layer ([D] QK-norm weights or null)
   int num_sms = 0;
   int decode_resident = 0;  // resident decode CTAs on the whole GPU
   size_t part_units = 0;    // capacity of the decode partials, in segment slots
@@ -176,6 +177,7 @@ int dattn_create(const dattn_config* cfg, int device, dattn_t** out) {
     }
     if (L.rotary_dim < 0 || L.rotary_dim > D || L.rotary_dim % 2) return DATTN_EINVAL;
     if (L.rotary_dim > 0 && !(L.rope_theta > 0.0)) return DATTN_EINVAL;
+    if ((L.q_norm_weight || L.k_norm_weight) && !(L.norm_eps >= 0.0)) return DATTN_EINVAL;
   }
   DeviceGuard guard(device);
   if (!guard.ok) return DATTN_ECUDA;
@@ -218,6 +220,24 @@ int dattn_create(const dattn_config* cfg, int device, dattn_t** out) {
     }
   }
 
+  // QK-norm weights, one [D] copy per layer and side; the handle keeps no
+  // host pointer of the caller's
+  for (dattn_layer_config& L : h->layers) {
+    for (int side = 0; side < 2; ++side) {
+      const uint16_t* src = side == 0 ? L.q_norm_weight : L.k_norm_weight;
+      uint16_t* dev = nullptr;
+      if (src) {
+        if (cudaMalloc(&dev, D * sizeof(uint16_t)) != cudaSuccess) return fail(DATTN_ECUDA);
+        (side == 0 ? h->q_norm : h->k_norm).push_back(dev);
+        if (cudaMemcpy(dev, src, D * sizeof(uint16_t), cudaMemcpyHostToDevice) != cudaSuccess)
+          return fail(DATTN_ECUDA);
+      } else {
+        (side == 0 ? h->q_norm : h->k_norm).push_back(nullptr);
+      }
+    }
+    L.q_norm_weight = L.k_norm_weight = nullptr;
+  }
+
   // Workspace. Rows of rotated q/k: one per stream (decode) or per verify row.
   const size_t rows = static_cast<size_t>(h->max_streams) *
                       (h->max_verify_rows > 1 ? h->max_verify_rows : 1);
@@ -255,6 +275,8 @@ void dattn_destroy(dattn_t* h) {
   if (!h) return;
   DeviceGuard guard(h->device);
   for (uint64_t* p : h->rope_step) cudaFree(p);
+  for (uint16_t* p : h->q_norm) cudaFree(p);
+  for (uint16_t* p : h->k_norm) cudaFree(p);
   cudaFree(h->qhat);
   cudaFree(h->qhl);
   cudaFree(h->khat);
@@ -327,6 +349,8 @@ int dattn_append_kv(dattn_t* h, int layer, const dattn_cache* cache, int num_str
   a.rotate = rotate;
   a.rope_step = h->rope_step[layer];
   a.err = h->err;
+  a.k_norm = h->k_norm[layer];
+  a.norm_eps = L.norm_eps;
   rc = cuda_status(launch_append(a, reinterpret_cast<cudaStream_t>(stream)), "append");
   if (rc == DATTN_OK) record_launch(stream, cache->k);
   return rc;
@@ -382,6 +406,9 @@ int dattn_decode(dattn_t* h, int layer, const dattn_cache* cache, const dattn_de
   da.early = !prev_launch_writes(stream, cache->k);
   da.wait_ns = h->wait_ns;
   da.debug_flags = h->debug_flags;
+  da.q_norm = h->q_norm[layer];
+  da.k_norm = h->k_norm[layer];
+  da.norm_eps = L.norm_eps;
   rc = cuda_status(launch_decode(da, h->D, ctas, s), "decode");
   if (rc == DATTN_OK) {
     record_launch(stream, args->write_back ? cache->k : nullptr);
@@ -445,6 +472,9 @@ int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, const dattn_ve
   ra.qhl_rows = h->qhl_rows;
   ra.khat = h->khat;
   ra.err = h->err;
+  ra.q_norm = h->q_norm[layer];
+  ra.k_norm = h->k_norm[layer];
+  ra.norm_eps = L.norm_eps;
   rc = cuda_status(launch_rope(ra, s), "verify prologue");
   if (rc != DATTN_OK) return rc;
 

@@ -60,6 +60,7 @@
 //    rescaled only when some head's running maximum moved.
 #include "bf16_exact.h"
 #include "common.cuh"
+#include "qk_norm.cuh"
 #include "mma.cuh"
 
 namespace dattn {
@@ -203,6 +204,24 @@ __device__ __forceinline__ uint32_t row_bits(int lo, int hi) {
 template <int NTH>
 __device__ __forceinline__ void team_sync() {
   if constexpr (NTH == 32) __syncwarp(); else __syncthreads();
+}
+
+// QK-norm of a unit's staged rows in place, before they are rotated: its G
+// query rows (weights a.q_norm) and its new key (a.k_norm), one warp per row.
+// Ends with a team barrier.
+template <int D, int NTH>
+__device__ __forceinline__ void norm_staged(const DecodeArgs& a, uint16_t* q, uint16_t* k, int t) {
+  constexpr int W = NTH / 32;
+  const int w = t >> 5, lane = t & 31;
+  for (int row = w; row <= a.G; row += W) {
+    const uint16_t* wt = row < a.G ? a.q_norm : a.k_norm;
+    if (!wt) continue;
+    uint16_t* x = row < a.G ? q + row * D : k;
+    const double inv = qk_norm_inv(x, D, a.norm_eps, lane);
+    for (int d = lane; d < D; d += 32) x[d] = qk_norm_apply(x[d], wt[d], inv);
+  }
+  fence_proxy_async_smem();  // the slot is refilled by bulk copies later
+  team_sync<NTH>();
 }
 
 // Rotate the G query heads of a unit (src: its staged q rows [G][D]) at
@@ -1066,6 +1085,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       const int sl = k & 1;
       if (!failed) check(mbar_wait_bounded(inbar + 8 * sl, (k >> 1) & 1, a.wait_ns));
       uint8_t* slot = in_slots + sl * Gm::IN_BYTES;
+      if (a.q_norm || a.k_norm)
+        norm_staged<D, 32>(a, reinterpret_cast<uint16_t*>(slot + Gm::IN_Q),
+                           reinterpret_cast<uint16_t*>(slot + Gm::IN_K), lane);
       prep_q<D, GP, 32>(a, reinterpret_cast<const uint16_t*>(slot + Gm::IN_Q), sl ? pos_s[1] : pos_s[0], step,
                         qs, cs, lane);
       __syncwarp();
@@ -1122,6 +1144,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         (a.gate && threadIdx.x < a.G) ? a.gate[(static_cast<int64_t>(b) * Hkv + j) * a.G + threadIdx.x] : 0;
     if (!mbar_wait_bounded(inbar + 8 * (n & 1), (n >> 1) & 1, a.wait_ns)) raise_error(a.err, ERR_TIMEOUT);
     uint8_t* slot = in_slots + (n & 1) * Gm::IN_BYTES;
+    if (a.q_norm || a.k_norm)
+      norm_staged<D, kThreads>(a, reinterpret_cast<uint16_t*>(slot + Gm::IN_Q),
+                               reinterpret_cast<uint16_t*>(slot + Gm::IN_K), threadIdx.x);
     prep_q<D, GP, kThreads>(a, reinterpret_cast<const uint16_t*>(slot + Gm::IN_Q), pos, step, qs, cs, threadIdx.x);
     __syncthreads();
     prep_token<D, GP, kThreads>(a, qs, cs, slot, gr, threadIdx.x);

@@ -65,6 +65,9 @@ struct RopeArgs {
   int qhl_rows;                // rows of one plane of qhl (its capacity)
   uint16_t* khat;              // [rows, Hkv, D]
   int* err;
+  const uint16_t* q_norm;      // [D] QK-norm weights, or null
+  const uint16_t* k_norm;
+  double norm_eps;
 };
 
 // Query heads of a KV group as the decode kernel lays them out: 4 (G <= 4)
@@ -104,6 +107,9 @@ struct DecodeArgs {
                                // (set by launch_decode)
   uint64_t wait_ns;            // limit of every bounded wait (0 = kDefaultWaitNs)
   int debug_flags;             // kDebugWithholdQ: see dattn_debug_config
+  const uint16_t* q_norm;      // [D] QK-norm weights of the queries, or null
+  const uint16_t* k_norm;      // [D] of the new key, or null
+  double norm_eps;
 };
 
 struct AppendArgs {
@@ -117,6 +123,8 @@ struct AppendArgs {
   int rotate;
   const uint64_t* rope_step;   // [r / 2]
   int* err;
+  const uint16_t* k_norm;      // [D] QK-norm weights of the keys (with rotate), or null
+  double norm_eps;
 };
 
 // Tensor-core pass of tree verify over each stream's paged prefix (stream-K

@@ -8,7 +8,7 @@
 // pointers. dattn_create allocates the handle's workspace, so those callers
 // cannot use dattn_decode. This entry point needs no handle: its scratch space
 // (the split partials, the per-unit segment counters, the error word and the
-// RoPE phase-step table) lives in one fixed-size array in device global memory
+// RoPE phase-step table and the layer's QK-norm weights) lives in one fixed-size array in device global memory
 // that the library defines at file scope. The caller passes only its inputs,
 // outputs and cache, exactly as for dattn_decode.
 //
@@ -16,8 +16,8 @@
 // stays there until the process exits. All calls on a device share it and it
 // keeps the last call's contents. Every call starts with a small set-up kernel
 // that clears the error word and the segment counters (the decode kernel
-// needs them at zero) and writes the layer's RoPE phase steps, which it
-// receives by value in its kernel parameters - no host buffer has to outlive
+// needs them at zero) and writes the layer's RoPE phase steps and QK-norm
+// weights, which it receives by value in its kernel parameters - no host buffer has to outlive
 // the call. Two calls that run on the GPU at the same time - on different
 // streams, or not ordered on one stream - race on the array.
 //
@@ -53,11 +53,15 @@ std::mutex g_mutex;
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 constexpr int kMaxPhaseSteps = 128;  // r / 2 for r <= 256
+constexpr int kMaxHeadDim = 256;
 
 // Everything the set-up kernel writes, passed by value.
 struct NoAllocSetup {
   uint64_t step[kMaxPhaseSteps];  // RoPE phase steps of the layer
   uint64_t* step_dst;
+  uint16_t norm[2][kMaxHeadDim];  // QK-norm weights (queries, keys)
+  uint16_t* norm_dst[2];          // or null for a side without a norm
+  int D;
   int half;                       // r / 2
   int* err;
   int* counters;
@@ -66,6 +70,9 @@ struct NoAllocSetup {
 
 __global__ void __launch_bounds__(256) noalloc_setup_kernel(const __grid_constant__ NoAllocSetup p) {
   for (int i = threadIdx.x; i < p.half; i += blockDim.x) p.step_dst[i] = p.step[i];
+  for (int side = 0; side < 2; ++side)
+    if (p.norm_dst[side])
+      for (int i = threadIdx.x; i < p.D; i += blockDim.x) p.norm_dst[side][i] = p.norm[side][i];
   for (int i = threadIdx.x; i < p.n_counters; i += blockDim.x) p.counters[i] = 0;
   if (threadIdx.x == 0) *p.err = 0;
 }
@@ -84,6 +91,7 @@ extern "C" DATTN_API int dattn_decode_noalloc(const dattn_config* cfg, int layer
   const dattn_layer_config& L = cfg->layers[layer];
   if (L.rotary_dim < 0 || L.rotary_dim > D || L.rotary_dim % 2 || (L.rotary_dim > 0 && !(L.rope_theta > 0.0)))
     return DATTN_EINVAL;
+  if ((L.q_norm_weight || L.k_norm_weight) && !(L.norm_eps >= 0.0)) return DATTN_EINVAL;
   if (!cache->k || !cache->v || cache->n_rows <= 0) return DATTN_EINVAL;
   if ((reinterpret_cast<uintptr_t>(cache->k) | reinterpret_cast<uintptr_t>(cache->v)) & 15u) return DATTN_EINVAL;
   int n_max;
@@ -138,6 +146,8 @@ extern "C" DATTN_API int dattn_decode_noalloc(const dattn_config* cfg, int layer
   off = align256(off + sizeof(int));
   const size_t freq_off = off;
   off = align256(off + static_cast<size_t>(half) * sizeof(uint64_t));
+  const size_t norm_off = off;
+  off = align256(off + 2 * static_cast<size_t>(D) * sizeof(uint16_t));
   const size_t counters_off = off;
   off = align256(off + static_cast<size_t>(B) * Hkv * sizeof(int));
   const size_t part_off = off;
@@ -171,6 +181,15 @@ extern "C" DATTN_API int dattn_decode_noalloc(const dattn_config* cfg, int layer
   NoAllocSetup setup{};
   for (int i = 0; i < half; ++i) setup.step[i] = rope_phase_step(L.rope_theta, L.rotary_dim, i);
   setup.step_dst = rope_step;
+  uint16_t* norm_dev[2] = {nullptr, nullptr};
+  for (int side = 0; side < 2; ++side) {
+    const uint16_t* w = side == 0 ? L.q_norm_weight : L.k_norm_weight;
+    if (!w) continue;
+    for (int i = 0; i < D; ++i) setup.norm[side][i] = w[i];
+    norm_dev[side] = reinterpret_cast<uint16_t*>(ds.base + norm_off) + side * D;
+    setup.norm_dst[side] = norm_dev[side];
+  }
+  setup.D = D;
   setup.half = half;
   setup.err = err;
   setup.counters = counters;
@@ -197,6 +216,9 @@ extern "C" DATTN_API int dattn_decode_noalloc(const dattn_config* cfg, int layer
   da.counters = counters;
   da.err = err;
   da.early = !prev_launch_writes(stream, cache->k);
+  da.q_norm = norm_dev[0];
+  da.k_norm = norm_dev[1];
+  da.norm_eps = L.norm_eps;
   const cudaError_t e = launch_decode(da, D, ctas, s, /*pdl=*/false);
   if (e != cudaSuccess) return e == cudaErrorNotSupported ? DATTN_EUNSUPPORTED : DATTN_ECUDA;
   record_launch(stream, args->write_back ? cache->k : nullptr);

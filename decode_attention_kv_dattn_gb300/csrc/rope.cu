@@ -17,26 +17,31 @@
 
 #include "bf16_exact.h"
 #include "common.cuh"
+#include "qk_norm.cuh"
 
 namespace dattn {
 
 namespace {
 
 constexpr int kRopeThreads = 64;      // append kernel
+constexpr int kMaxAppendHeads = 64;   // Hkv of the append kernel
 constexpr int kRowThreads = 512;      // prologue: one CTA per token row
 constexpr int kMaxItems = 8;          // pair slots per thread (heads * D/2 <= 512 * 8)
 constexpr int kMaxT = 16;             // verify rows per stream
+constexpr int kMaxHeads = 64;         // Hq + Hkv of the prologue (heads * D/2 <= 512 * 8)
 
 // The prologue of a call: one CTA per token row. Work items are "pair slots"
 // of every head (Hq query heads, then Hkv key heads): slot p < r/2 is the
 // rotated pair (p, p + r/2); slot p >= r/2 holds two pass-through dims. All
 // inputs are loaded first, before waiting for the preceding launch; the
 // cos/sin of each pair index is computed once per row (one thread each) into
-// shared memory meanwhile.
+// shared memory meanwhile. With QK-norm each head's scale comes first (one
+// warp per head) and the pair slots hold the normalised bf16 values.
 __global__ void __launch_bounds__(kRowThreads) rope_kernel(const RopeArgs a) {
   __shared__ float cs_c[128], cs_s[128];
   __shared__ int64_t pos_s;
   __shared__ int par_s[kMaxT];
+  __shared__ double inv_s[kMaxHeads];
   // Everything up to the stores reads caller inputs only, so it runs while the
   // previous launch finishes; the workspace written below may still be read
   // by it, so the stores wait.
@@ -45,6 +50,22 @@ __global__ void __launch_bounds__(kRowThreads) rope_kernel(const RopeArgs a) {
   const int slots = a.D / 2;
   const int heads = a.Hq + a.Hkv;
   const int items = heads * slots;
+
+  auto head_src = [&](int hh) {
+    return hh < a.Hq ? a.q + (static_cast<int64_t>(row) * a.Hq + hh) * a.D
+                     : a.k + (static_cast<int64_t>(row) * a.Hkv + (hh - a.Hq)) * a.D;
+  };
+  auto head_norm = [&](int hh) { return hh < a.Hq ? a.q_norm : a.k_norm; };
+  const bool norm = a.q_norm || a.k_norm;
+  if (norm) {
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int hh = w; hh < heads; hh += kRowThreads / 32)
+      if (head_norm(hh)) {
+        const double inv = qk_norm_inv(head_src(hh), a.D, a.norm_eps, lane);
+        if (lane == 0) inv_s[hh] = inv;
+      }
+    __syncthreads();
+  }
 
   // ---- loads of this thread's pair slots (independent of the position)
   uint32_t xy[kMaxItems];
@@ -58,7 +79,15 @@ __global__ void __launch_bounds__(kRowThreads) rope_kernel(const RopeArgs a) {
                                       : a.k + (static_cast<int64_t>(row) * a.Hkv + (hh - a.Hq)) * a.D;
       const int d0 = p < half ? p : a.r + 2 * (p - half);
       const int d1 = p < half ? p + half : d0 + 1;
-      xy[k] = static_cast<uint32_t>(src[d0]) | (static_cast<uint32_t>(src[d1]) << 16);
+      uint16_t x = src[d0], y = src[d1];
+      if (norm) {
+        const uint16_t* wt = head_norm(hh);
+        if (wt) {
+          x = qk_norm_apply(x, wt[d0], inv_s[hh]);
+          y = qk_norm_apply(y, wt[d1], inv_s[hh]);
+        }
+      }
+      xy[k] = static_cast<uint32_t>(x) | (static_cast<uint32_t>(y) << 16);
     }
   }
   // ---- position of the row
@@ -185,13 +214,30 @@ __global__ void __launch_bounds__(kRopeThreads) append_kernel(const AppendArgs a
     head_stride = static_cast<int64_t>(c.R) * a.D;
   }
   const int64_t src0 = (static_cast<int64_t>(b) * a.Tmax + t) * a.Hkv * a.D;
-  // V: plain copy, 16 bytes per thread-step.
+  // V: plain copy, 16 bytes per thread-step.  (Every return above is taken by
+  // the whole CTA.)
   for (int e = threadIdx.x; e < a.Hkv * a.D / 8; e += kRopeThreads) {
     const int h = e / (a.D / 8), d8 = e % (a.D / 8);
     const uint4 w = *reinterpret_cast<const uint4*>(a.v + src0 + h * a.D + d8 * 8);
     *reinterpret_cast<uint4*>(c.v + dst0 + h * head_stride + d8 * 8) = w;
   }
-  if (!a.rotate || a.r == 0) {
+  // K: the QK-norm scale of each head first (one warp per head)
+  __shared__ double inv_s[kMaxAppendHeads];
+  const uint16_t* kn = a.rotate ? a.k_norm : nullptr;
+  if (kn) {
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int h = w; h < a.Hkv; h += kRopeThreads / 32) {
+      const double inv = qk_norm_inv(a.k + src0 + h * a.D, a.D, a.norm_eps, lane);
+      if (lane == 0) inv_s[h] = inv;
+    }
+    __syncthreads();
+  }
+  // one cached K value: the input, or its QK-norm
+  auto kval = [&](int h, int d) {
+    const uint16_t x = a.k[src0 + h * a.D + d];
+    return kn ? qk_norm_apply(x, kn[d], inv_s[h]) : x;
+  };
+  if (!a.rotate || (a.r == 0 && !kn)) {
     for (int e = threadIdx.x; e < a.Hkv * a.D / 8; e += kRopeThreads) {
       const int h = e / (a.D / 8), d8 = e % (a.D / 8);
       const uint4 w = *reinterpret_cast<const uint4*>(a.k + src0 + h * a.D + d8 * 8);
@@ -208,13 +254,13 @@ __global__ void __launch_bounds__(kRopeThreads) append_kernel(const AppendArgs a
       rope_cos_sin(pos, a.rope_step[i], cf, sf);
       const uint32_t cb = __float_as_uint(cf), sb = __float_as_uint(sf);
       for (int h = 0; h < a.Hkv; ++h) {
-        const uint16_t x = a.k[src0 + h * a.D + i], y = a.k[src0 + h * a.D + i + half];
+        const uint16_t x = kval(h, i), y = kval(h, i + half);
         c.k[dst0 + h * head_stride + i] = bf16_dot2(x, cb, y, sb ^ 0x80000000u);
         c.k[dst0 + h * head_stride + i + half] = bf16_dot2(y, cb, x, sb);
       }
     } else {
       const int d = a.r + (job - half);
-      for (int h = 0; h < a.Hkv; ++h) c.k[dst0 + h * head_stride + d] = a.k[src0 + h * a.D + d];
+      for (int h = 0; h < a.Hkv; ++h) c.k[dst0 + h * head_stride + d] = kval(h, d);
     }
   }
 }
@@ -222,12 +268,14 @@ __global__ void __launch_bounds__(kRopeThreads) append_kernel(const AppendArgs a
 }  // namespace
 
 cudaError_t launch_rope(const RopeArgs& a, cudaStream_t s) {
-  if ((a.Hq + a.Hkv) * (a.D / 2) > kRowThreads * kMaxItems || a.r > 256 || (a.parent && a.T > kMaxT))
+  if ((a.Hq + a.Hkv) * (a.D / 2) > kRowThreads * kMaxItems || a.Hq + a.Hkv > kMaxHeads || a.r > 256 ||
+      (a.parent && a.T > kMaxT))
     return cudaErrorNotSupported;
   return launch_pdl(rope_kernel, dim3(a.rows), dim3(kRowThreads), 0, s, a);
 }
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
+  if (a.Hkv > kMaxAppendHeads) return cudaErrorNotSupported;
   dim3 grid(a.Tmax, a.B);
   return launch_pdl(append_kernel, grid, dim3(kRopeThreads), 0, s, a);
 }

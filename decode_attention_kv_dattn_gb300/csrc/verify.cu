@@ -22,14 +22,17 @@
 //    2^8, base 2) and its row sum stay in the thread. The scores leave tensor
 //    memory as soon as the softmax threads hold them, so the next tile's
 //    Q K^T runs while this tile's probabilities are formed.
-//    Loads: the TMA unit lands K by tensor-map boxes of 16 keys x 64 dims and
-//    V by one box per 16-key page group (all dims), 128-byte swizzled, in a
-//    ring of 16 KB chunks in the order the MMAs consume them. K is used as it
-//    lands; four converter warps turn each V chunk from bf16 into fp16 in
-//    place (exact below 65504 in magnitude, which they check: P is fp16, and
-//    bf16 probabilities would break the tolerance) and zero the V rows of keys
-//    outside the prefix (their probability is 0, but 0 x NaN is NaN). Work is
-//    split stream-K over all units' 128-key tiles.
+//    Loads: the TMA unit lands K by tensor-map boxes of 16 keys x 64 dims
+//    into a ring of 64-dim tile regions, and V by one box per 16-key page
+//    group (all dims) into a ring of page-group slots, 128-byte swizzled, in
+//    the order the MMAs consume them. K is used as it lands; four converter
+//    warps turn each V slot from bf16 into fp16 in place (exact below 65504 in
+//    magnitude, which they check: P is fp16, and bf16 probabilities would
+//    break the tolerance) and zero the V rows of keys outside the prefix
+//    (their probability is 0, but 0 x NaN is NaN). The q_lo and P operand
+//    regions hold only the rows in use, which leaves the rings the room to
+//    keep a tile in flight behind the one being consumed. Work is split
+//    stream-K over all units' 128-key tiles.
 //  * verify_combine_kernel - per (stream, row, KV head): merges the prefix
 //    segments, scores the row's tree path in fp32 and joins it in score
 //    space, applies the gate, stores fp32 and writes the window entries back.
@@ -45,8 +48,10 @@ namespace {
 
 constexpr int KT = 128;                    // keys per tile: the Q K^T MMAs' N
 constexpr int VM = 128;                    // MMA rows (G*T <= VM)
-constexpr int kChunk = 16384;              // bytes of one ring chunk
-constexpr int kMaxChunks = 12;
+constexpr int kKChunk = 16384;             // bytes of one K ring slot: one 64-dim region of a tile
+constexpr int kMaxK = 8;                   // K ring slots
+constexpr int kKExtra = 0;                 // K slots beyond one tile's regions, when they fit
+constexpr int kMaxV = 24;                  // V ring slots: one 16-key page group (all dims) each
 constexpr int kSoftWarps = 8;              // warps 0..7: TMEM lane quarter w % 4 (one row per
                                            // lane), keys [64 (w / 4), 64 (w / 4) + 64) of the tile
 constexpr int kTmaWarp = 8;                // issues the K and q_lo TMA copies
@@ -62,11 +67,12 @@ static_assert(kVerifyTileKeys == KT, "tile size shared with the host split");
 
 // barrier indices
 enum {
-  B_FULL = 0,                  // [kMaxChunks] chunk landed (TMA transaction bytes)
-  B_CONV = kMaxChunks,         // [kMaxChunks] V chunk converted (one arrival per converter warp)
-  B_FREE = 2 * kMaxChunks,     // [kMaxChunks] the MMAs reading the chunk completed
-                               // (slots [0, CK) form the K ring, [CK, CK + CV) the V ring)
-  B_QLO = 3 * kMaxChunks,      // the segment's q_lo rows landed in shared memory
+  B_KFULL = 0,                 // [kMaxK] K slot landed (TMA transaction bytes)
+  B_KFREE = kMaxK,             // [kMaxK] the Q K^T MMAs reading the K slot completed
+  B_VFULL = 2 * kMaxK,         // [kMaxV] V slot landed
+  B_VCONV = 2 * kMaxK + kMaxV, // [kMaxV] V slot converted (one arrival per converter warp)
+  B_VFREE = 2 * kMaxK + 2 * kMaxV,  // [kMaxV] the P V MMA reading the V slot completed
+  B_QLO = 2 * kMaxK + 3 * kMaxV,    // the segment's q_lo rows landed in shared memory
   B_QHI,                       // the segment's q_hi rows are in TMEM (softmax warps)
   B_QFREE,                     // the segment's Q K^T MMAs completed (q may be replaced)
   B_SFULL,                     // Q K^T of the tile completed
@@ -82,13 +88,16 @@ enum {
 template <int D>
 constexpr int row_stride() { return D + 4; }
 
-// Shared-memory layout of one CTA for U units; the host computes the same to
-// size the launch.
+// Shared-memory layout of one CTA for U units of R rows; the host computes the
+// same to size the launch. An MMA operand region (64 dims or 64 keys of every
+// row, 128 B per row) holds only the R rows rounded up to a core group of 8;
+// the M = 128 MMAs read rows past that from whatever follows, and those rows'
+// results are never used.
 struct VLayout {
-  int qlo_off;   // q_lo (A of the second Q K^T MMA): [D/64 regions][128 rows][128 B]
-  int p_off;     // P (A of P V): [2 key regions of 64][128 rows][128 B]
-  int ring_off;  // chunks: the K ring (ck), then the V ring (cv)
-  int chunks;
+  int rb;        // bytes of one operand region: 128 * round8(R)
+  int qlo_off;   // q_lo (A of the second Q K^T MMA): [D/64 regions][rows][128 B]
+  int p_off;     // P (A of P V): [2 key regions of 64][rows][128 B]
+  int ring_off;  // the K ring (ck slots of kKChunk), then the V ring (cv slots of 32 D bytes)
   int ck, cv;
   int bar_off;
   int misc_off;  // 32 bytes: tmem base (+0), the abort flag (+16)
@@ -99,20 +108,22 @@ struct VLayout {
   int total;     // bytes, plus 1024 for the alignment of the base
 };
 
-__host__ __device__ inline VLayout verify_layout(int D, int U) {
+__host__ __device__ inline VLayout verify_layout(int D, int U, int R) {
   VLayout L;
+  L.rb = ((R + 7) / 8) * 1024;
   L.qlo_off = 0;
-  L.p_off = (D / 64) * VM * 128;
-  L.ring_off = L.p_off + (KT / 64) * VM * 128;
+  L.p_off = (D / 64) * L.rb;
+  L.ring_off = L.p_off + (KT / 64) * L.rb;
   const int tail = B_COUNT * 8 + 32 + 6 * 128 * 4 + 3 * kTileRing * 8 * 4 + (2 * U + 1) * 4;
-  const int c = (kSmemLimit - 1024 - L.ring_off - tail) / kChunk;
-  L.chunks = c > kMaxChunks ? kMaxChunks : c;
-  // The K ring holds at least a whole tile's K (D/64 chunks): its copy warp
+  const int room = kSmemLimit - 1024 - L.ring_off - tail;
+  // The K ring holds at least a whole tile's K (D/64 slots): its copy warp
   // issues a new segment's q_lo rows only after that segment's first K tile,
-  // whose Q K^T needs them.
-  L.ck = L.chunks / 2 < D / 64 ? D / 64 : L.chunks / 2;
-  L.cv = L.chunks - L.ck;
-  L.bar_off = L.ring_off + L.chunks * kChunk;
+  // whose Q K^T needs them. The V ring takes the rest.
+  L.ck = D / 64 + kKExtra;
+  if ((room - L.ck * kKChunk) / (32 * D) < 8) L.ck = D / 64;
+  L.cv = (room - L.ck * kKChunk) / (32 * D);
+  if (L.cv > kMaxV) L.cv = kMaxV;
+  L.bar_off = L.ring_off + L.ck * kKChunk + L.cv * 32 * D;
   L.misc_off = L.bar_off + B_COUNT * 8;
   L.xch_off = L.misc_off + 32;
   L.trow_off = L.xch_off + 6 * 128 * 4;
@@ -175,7 +186,7 @@ __device__ __forceinline__ void convert16(uint8_t* p, uint32_t& mag) {
 template <int D>
 __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid_constant__ VerifySplitArgs a) {
   constexpr int NREG = D / 64;        // 64-dim regions: K chunks per tile
-  constexpr int GPV = 8 / NREG;       // 16-key page groups per V chunk
+  constexpr int VG = 32 * D;          // bytes of one V slot: 16 keys x D dims
   using Col = VCols<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -185,8 +196,9 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
   const CacheView& c = a.c;
   const int Hkv = a.Hkv, U = a.S * Hkv, G = a.G, T = a.T, R = G * T, Hq = Hkv * G;
   const int NC = gridDim.x, cta = blockIdx.x;
-  const VLayout L = verify_layout(D, U);
-  const int CK = L.ck, CV = L.cv;
+  const VLayout L = verify_layout(D, U, R);
+  const int CK = L.ck, CV = L.cv, R8 = L.rb / 128;
+  const uint32_t vring = sbase + L.ring_off + CK * kKChunk;
   int* PT = reinterpret_cast<int*>(smem + L.tab_off);   // [U + 1] tile prefix
   int* NK = PT + U + 1;                                   // [U] prefix keys per unit
   int* TROW = reinterpret_cast<int*>(smem + L.trow_off);  // [kTileRing][8] first tensor row of each group
@@ -210,10 +222,14 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
   if (threadIdx.x == 0) {
     PT[0] = 0;
     *abort_flag = 0;
-    for (int b = 0; b < kMaxChunks; ++b) {
-      mbar_init(bars + 8 * (B_FULL + b), 1);
-      mbar_init(bars + 8 * (B_CONV + b), kConvWarps);
-      mbar_init(bars + 8 * (B_FREE + b), 1);
+    for (int b = 0; b < kMaxK; ++b) {
+      mbar_init(bars + 8 * (B_KFULL + b), 1);
+      mbar_init(bars + 8 * (B_KFREE + b), 1);
+    }
+    for (int b = 0; b < kMaxV; ++b) {
+      mbar_init(bars + 8 * (B_VFULL + b), 1);
+      mbar_init(bars + 8 * (B_VCONV + b), kConvWarps);
+      mbar_init(bars + 8 * (B_VFREE + b), 1);
     }
     mbar_init(bars + 8 * B_QLO, 1);
     mbar_init(bars + 8 * B_QHI, kSoftWarps);
@@ -270,7 +286,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
   // of tile k of unit u (one page-table load)
   auto group_of = [&](int k, int u, int& row, int& mask) {
     row = mask = 0;
-    if (lane >= 8 || k >= nt) return;
+    if (lane >= 8 || k < 0 || k >= nt) return;
     const int s = u / Hkv, j = u - s * Hkv;
     const int t0 = ((g0 + k) - PT[u]) * KT + lane * 16;
     const int valid = min(16, NK[u] - t0);
@@ -288,12 +304,15 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
     // Each tile's group rows are worked out one tile ahead, so that no
     // page-table load waits on the issue path.
     const bool is_v = warp == kTmaVWarp;
-    const int nring = is_v ? CV : CK, ring0 = is_v ? CK : 0;
+    const int nring = is_v ? CV : CK;
+    const int b_full = is_v ? B_VFULL : B_KFULL, b_free = is_v ? B_VFREE : B_KFREE;
     int* MASKS = is_v ? VMASK : TMASK;
     const uint64_t policy = l2_evict_first_policy();
     int u = u_first, seg = -1, issued = 0;
     int nrow, nmask;
     group_of(0, u, nrow, nmask);
+    // The next tile's page-table loads are issued after this tile's copies,
+    // so their latency falls inside the waits for free slots.
     bool waited = false, ok = true;
     for (int k = 0; k < nt && ok; ++k) {
       const int e = (k % kTileRing) * 8;
@@ -306,31 +325,28 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
       if (lane < 8) MASKS[e + lane] = nmask;
       if (!is_v && lane < 8) TROW[e + lane] = nrow;
       __syncwarp();
-      if (k + 1 < nt) group_of(k + 1, unit_at(k + 1, u), nrow, nmask);
       if (lane == 0) {
-        // K(k): one chunk per 64-dim region, one box per loaded group;
-        // V(k): one chunk per GPV groups, one box per loaded group (all dims)
-        for (int ch = 0; ch < NREG && ok; ++ch) {
-          const int idx = k * NREG + ch, slot = ring0 + idx % nring;
-          if (idx >= nring && !W.wait(B_FREE + slot, ((idx / nring) - 1) & 1)) {
+        // K(k): one slot per 64-dim region, one box per loaded group;
+        // V(k): one slot per 16-key group, one box (all dims) when it has keys
+        const int per_tile = is_v ? 8 : NREG;
+        for (int ch = 0; ch < per_tile && ok; ++ch) {
+          const int idx = k * per_tile + ch, slot = idx % nring;
+          if (idx >= nring && !W.wait(b_free + slot, ((idx / nring) - 1) & 1)) {
             ok = false;
             break;
           }
-          const uint32_t dst = sbase + L.ring_off + slot * kChunk;
-          const uint32_t bar = bars + 8 * (B_FULL + slot);
+          const uint32_t bar = bars + 8 * (b_full + slot);
           if (!is_v) {
+            const uint32_t dst = sbase + L.ring_off + slot * kKChunk;
             int n = 0;
             for (int gi = 0; gi < 8; ++gi) n += MASKS[e + gi] != 0;
             mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n) * 2048u);
             for (int gi = 0; gi < 8; ++gi)
               if (MASKS[e + gi] != 0) tma_load_2d(dst + gi * 2048, &a.tmap_k, 64 * ch, rows[gi], bar, policy);
           } else {
-            int n = 0;
-            for (int gg = 0; gg < GPV; ++gg) n += MASKS[e + ch * GPV + gg] != 0;
-            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n) * NREG * 2048u);
-            for (int gg = 0; gg < GPV; ++gg)
-              if (MASKS[e + ch * GPV + gg] != 0)
-                tma_load_3d(dst + gg * NREG * 2048, &a.tmap_v, 0, rows[ch * GPV + gg], 0, bar, policy);
+            const bool any = MASKS[e + ch] != 0;
+            mbar_arrive_expect_tx(bar, any ? static_cast<uint32_t>(VG) : 0u);
+            if (any) tma_load_3d(vring + slot * VG, &a.tmap_v, 0, rows[ch], 0, bar, policy);
           }
           issued = idx + 1;
         }
@@ -348,17 +364,18 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
             const uint32_t bar = bars + 8 * B_QLO;
             mbar_arrive_expect_tx(bar, NREG * static_cast<uint32_t>(R) * 128u);
             for (int rr = 0; rr < NREG; ++rr)
-              tma_load_4d(sbase + L.qlo_off + rr * VM * 128, &a.tmap_q, 64 * rr, j * G, s * T, 1, bar, policy);
+              tma_load_4d(sbase + L.qlo_off + rr * L.rb, &a.tmap_q, 64 * rr, j * G, s * T, 1, bar, policy);
           }
         }
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (k + 1 < nt) group_of(k + 1, unit_at(k + 1, u), nrow, nmask);
     }
     // Copies still in flight exist only when a role gave up: let the latest
-    // copy into every chunk and the last q copy land before the CTA exits.
+    // copy into every slot and the last q copy land before the CTA exits.
     if (lane == 0 && *abort_flag) {
       for (int idx = max(0, issued - nring); idx < issued; ++idx)
-        mbar_wait_bounded(bars + 8 * (B_FULL + ring0 + idx % nring), (idx / nring) & 1);
+        mbar_wait_bounded(bars + 8 * (b_full + idx % nring), (idx / nring) & 1);
       if (!is_v && seg >= 0) mbar_wait_bounded(bars + 8 * B_QLO, seg & 1);
     }
     __syncwarp();
@@ -369,26 +386,26 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
     bool ok = true;
     for (int k = 0; k < nt && ok; ++k) {
       const int e = (k % kTileRing) * 8;
-      for (int ch = 0; ch < NREG; ++ch) {
-        const int idx = k * NREG + ch, slot = CK + idx % CV;
-        if (!__all_sync(0xffffffffu, W.wait(B_FULL + slot, (idx / CV) & 1))) {
+      for (int gi = 0; gi < 8; ++gi) {
+        const int idx = k * 8 + gi, slot = idx % CV;
+        if (!__all_sync(0xffffffffu, W.wait(B_VFULL + slot, (idx / CV) & 1))) {
           ok = false;
           break;
         }
-        uint8_t* base = smem + L.ring_off + slot * kChunk;
+        uint8_t* base = smem + L.ring_off + CK * kKChunk + slot * VG;
+        const uint32_t vmask = static_cast<uint32_t>(VMASK[e + gi]);
 #pragma unroll
-        for (int i = 0; i < kChunk / 16 / 128; ++i) {
-          // [group][region][16 rows][128 B]: rows outside the prefix become 0
+        for (int i = 0; i < VG / 16 / 128; ++i) {
+          // [region][16 rows][128 B]: rows outside the prefix become 0
           const int p = ct + i * 128;
-          const int gg = p / (NREG * 128), row = (p >> 3) & 15;
-          if ((VMASK[e + ch * GPV + gg] >> row) & 1)
+          if ((vmask >> ((p >> 3) & 15)) & 1)
             convert16(base + p * 16, mag);
           else
             *reinterpret_cast<uint4*>(base + p * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bars + 8 * (B_CONV + slot));
+        if (lane == 0) mbar_arrive(bars + 8 * (B_VCONV + slot));
       }
     }
     // fp16 holds bf16 values below 65504 in magnitude exactly (bf16 0x4780 = 65536)
@@ -416,17 +433,17 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
         if (k > 0 && !W.wait(B_SFREE, (k - 1) & 1)) return false;
         for (int ch = 0; ch < NREG; ++ch) {
           const int idx = k * NREG + ch, slot = idx % CK;
-          if (!W.wait(B_FULL + slot, (idx / CK) & 1)) return false;  // K is used as it landed
+          if (!W.wait(B_KFULL + slot, (idx / CK) & 1)) return false;  // K is used as it landed
           tc::fence_after();
-          const uint32_t kc = sbase + L.ring_off + slot * kChunk;
-          const uint32_t qc = sbase + L.qlo_off + ch * VM * 128;
+          const uint32_t kc = sbase + L.ring_off + slot * kKChunk;
+          const uint32_t qc = sbase + L.qlo_off + ch * L.rb;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t kdesc = tc::sw128_desc(kc + kk * 32, 16, 1024);
             tc::mma_ts(tmem + Col::S, tmem + Col::Q + (4 * ch + kk) * 8, kdesc, idesc_qk, ch > 0 || kk > 0);
             tc::mma(tmem + Col::S, tc::sw128_desc(qc + kk * 32, 16, 1024), kdesc, idesc_qk, true);
           }
-          tc::commit(bars + 8 * (B_FREE + slot));
+          tc::commit(bars + 8 * (B_KFREE + slot));
         }
         tc::commit(bars + 8 * B_SFULL);
         if (seg_last) tc::commit(bars + 8 * B_QFREE);
@@ -440,19 +457,14 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
         if (seg_first) ++pv_seg;
         if (!W.wait(B_PFULL, k & 1)) return false;
         if (seg_first && pv_seg > 0 && !W.wait(B_OFREE, (pv_seg - 1) & 1)) return false;
-        for (int ch = 0; ch < NREG; ++ch) {
-          const int idx = k * NREG + ch, slot = CK + idx % CV;
-          if (!W.wait(B_CONV + slot, (idx / CV) & 1)) return false;
+        for (int grp = 0; grp < 8; ++grp) {  // 16-key group of the tile
+          const int idx = k * 8 + grp, slot = idx % CV;
+          if (!W.wait(B_VCONV + slot, (idx / CV) & 1)) return false;
           tc::fence_after();
-          const uint32_t vc = sbase + L.ring_off + slot * kChunk;
-#pragma unroll
-          for (int gg = 0; gg < GPV; ++gg) {
-            const int grp = ch * GPV + gg;  // 16-key group of the tile
-            const uint64_t pdesc = tc::sw128_desc(sbase + L.p_off + (grp >> 2) * VM * 128 + (grp & 3) * 32, 16, 1024);
-            tc::mma(tmem + Col::O, pdesc, tc::sw128_desc(vc + gg * NREG * 2048, 2048, 1024), idesc_pv,
-                    !(seg_first && grp == 0));
-          }
-          tc::commit(bars + 8 * (B_FREE + slot));
+          const uint64_t pdesc = tc::sw128_desc(sbase + L.p_off + (grp >> 2) * L.rb + (grp & 3) * 32, 16, 1024);
+          tc::mma(tmem + Col::O, pdesc, tc::sw128_desc(vring + slot * VG, 2048, 1024), idesc_pv,
+                  !(seg_first && grp == 0));
+          tc::commit(bars + 8 * (B_VFREE + slot));
         }
         tc::commit(bars + 8 * B_PVDONE);
         return true;
@@ -506,7 +518,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
     load_qhi(u_first);
     int u = u_first, seg = -1;
     float m_ref = -INFINITY, l = 0.f;  // l: this half's share of the row sum
-    uint8_t* pbase = smem + L.p_off + kh * VM * 128;  // P's key region of this half
+    uint8_t* pbase = smem + L.p_off + kh * L.rb;  // P's key region of this half
     for (int k = 0; k < nt; ++k) {
       const int un = unit_at(k, u);
       const bool seg_first = un != u || k == 0;
@@ -588,7 +600,8 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
           ls[x & 1] += __low2float(hp) + __high2float(hp);
           w4[x] = *reinterpret_cast<const uint32_t*>(&hp);
         }
-        *reinterpret_cast<uint4*>(pbase + t * 128 + ((c8 ^ (t & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        if (t < R8)  // (the region holds R8 rows)
+          *reinterpret_cast<uint4*>(pbase + t * 128 + ((c8 ^ (t & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
       }
       l += ls[0] + ls[1];
       fence_proxy_async_smem();
@@ -818,8 +831,8 @@ cudaError_t verify_split_launch(const VerifySplitArgs& a, cudaStream_t s) {
   static std::atomic<uint64_t> opted{0};
   const cudaError_t e = opt_in_smem(verify_split_kernel<D>, kSmemLimit, opted);
   if (e != cudaSuccess) return e;
-  const VLayout L = verify_layout(D, a.S * a.Hkv);
-  if (L.cv < 2 || L.total > kSmemLimit) return cudaErrorNotSupported;
+  const VLayout L = verify_layout(D, a.S * a.Hkv, a.G * a.T);
+  if (L.cv < 4 || L.total > kSmemLimit) return cudaErrorNotSupported;
   return launch_pdl(verify_split_kernel<D>, dim3(a.ctas), dim3(kVThreads), static_cast<size_t>(L.total), s, a);
 }
 

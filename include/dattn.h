@@ -85,6 +85,15 @@ typedef struct {
   int rotary_dim;     /* r: RoPE turns dims [0, r) in pairs (i, i + r/2); even,
                          <= head_dim; 0 = no rotation                            */
   double rope_theta;  /* base of the inverse frequencies theta^(-2i/r)           */
+  /* QK-norm before RoPE ("pega-omni PR #4", talker kernels: RoPE with QK-norm),
+   * per head: y_d = w_d x_d / sqrt(mean(x^2) + eps), rounded once to bf16 (ties
+   * to even), then RoPE turns y. HOST pointers to [head_dim] bf16 weights,
+   * copied by dattn_create (dattn_decode_noalloc copies them on each call);
+   * NULL = no norm for that side. The key side applies to the new token of
+   * decode, the window rows of verify and dattn_append_kv with rotate != 0. */
+  const uint16_t* q_norm_weight;
+  const uint16_t* k_norm_weight;
+  double norm_eps;    /* eps (>= 0) of both norms                               */
 } dattn_layer_config;
 
 typedef struct {

@@ -35,12 +35,13 @@ def _i32(a):
 
 def _norm(qk_norm):
     """QK-norm arguments: qk_norm = (q weights, k weights, eps) as bf16 [D]
-    arrays and a float, or None for a layer without QK-norm."""
+    arrays (either may be None: no norm on that side) and a float, or None
+    for a layer without QK-norm."""
     if qk_norm is None:
         return (None, None, 0.0)
     qw, kw, eps = qk_norm
     global _keep_norm
-    _keep_norm = (_u16(qw), _u16(kw))
+    _keep_norm = tuple(None if w is None else _u16(w) for w in (qw, kw))
     return (_ptr(_keep_norm[0]), _ptr(_keep_norm[1]), float(eps))
 
 

@@ -42,12 +42,18 @@ def assert_close(gpu, ref, what=""):
     return float(d.max(initial=0.0))
 
 
-def layer_dict(case):
+def layer_dict(case, qk_norm=None):
+    """The case's layer for dattn.Handle; qk_norm = (q weights, k weights, eps)
+    (bf16 bits [D] each, either may be None) adds a QK-norm."""
     if case.kind == "ring":
-        return {"kind": 0, "ring_slots": case.cache.R, "rotary_dim": case.rope.rotary_dim,
-                "rope_theta": case.rope.theta}
-    return {"kind": 1, "page_size": case.cache.P, "rotary_dim": case.rope.rotary_dim,
-            "rope_theta": case.rope.theta}
+        d = {"kind": 0, "ring_slots": case.cache.R, "rotary_dim": case.rope.rotary_dim,
+             "rope_theta": case.rope.theta}
+    else:
+        d = {"kind": 1, "page_size": case.cache.P, "rotary_dim": case.rope.rotary_dim,
+             "rope_theta": case.rope.theta}
+    if qk_norm is not None:
+        d.update(q_norm=qk_norm[0], k_norm=qk_norm[1], norm_eps=qk_norm[2])
+    return d
 
 
 class DeviceCase:
@@ -79,16 +85,16 @@ class DeviceCase:
         return dattn.paged_cache(self.k, self.v, self.bt, self.seq)
 
 
-def make_handle(dattn, case, max_streams=None, max_context=None, max_verify_rows=0):
+def make_handle(dattn, case, max_streams=None, max_context=None, max_verify_rows=0, qk_norm=None):
     B = case.inputs.q.shape[0] if hasattr(case, "inputs") else case.q.shape[0]
     if max_context is None:
         max_context = int(case.cache.seq_len.max()) if case.kind == "paged" else 0
-    return dattn.Handle(case.Hq, case.Hkv, case.D, [layer_dict(case)],
+    return dattn.Handle(case.Hq, case.Hkv, case.D, [layer_dict(case, qk_norm)],
                         max_streams or B, max_context=max_context,
                         max_verify_rows=max_verify_rows)
 
 
-def oracle_decode(oracle, case, streams=None):
+def oracle_decode(oracle, case, streams=None, qk_norm=None):
     """Oracle output and entries for the case (optionally a subset of streams)."""
     c, x = case.cache, case.inputs
     sel = slice(None) if streams is None else np.asarray(streams)
@@ -97,9 +103,10 @@ def oracle_decode(oracle, case, streams=None):
     if case.kind == "ring":
         return oracle.decode_ring(c.k, c.v, c.head[sel], c.count[sel], x.q[sel], x.k_new[sel],
                                   x.v_new[sel], x.pos[sel], r, th, gate=gate,
-                                  stream_rows=c.stream_rows[sel])
+                                  stream_rows=c.stream_rows[sel], qk_norm=qk_norm)
     return oracle.decode_paged(c.k, c.v, c.block_table[sel], c.seq_len[sel], x.q[sel],
-                               x.k_new[sel], x.v_new[sel], x.pos[sel], r, th, gate=gate)
+                               x.k_new[sel], x.v_new[sel], x.pos[sel], r, th, gate=gate,
+                               qk_norm=qk_norm)
 
 
 def entry_slots(case):

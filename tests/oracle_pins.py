@@ -709,4 +709,108 @@ def pin_append_places_rotated_entries(o):
     assert np.sum(Ko != NAN) == written and np.sum(Vo != NAN) == written
 
 
+# ------------------------------------------------------------------ QK-norm
+# "pega-omni PR #4", talker kernels: RoPE with QK-norm. Reading (the page
+# gives no formula): y = bf16(w * x / sqrt(mean(x^2) + eps)), per head.
+
+def pin_qk_norm_closed_forms(o):
+    """Vectors whose norm is known in closed form: a constant vector c maps to
+    sign(c) * w (eps = 0); ones with eps = 3 map to w / 2; a single nonzero
+    entry a maps to sign(a) * sqrt(D) * w there and 0 elsewhere."""
+    D = 256
+    w = bf16(np.linspace(-1.5, 2.0, D).astype(np.float32).round(2))
+    wv = bf16_val(w)
+    for c in (1.0, 3.0, -2.0, 0.375):
+        y = o.qk_norm(bf16(np.full(D, c)), w, 0.0)
+        assert np.array_equal(bf16_val(y), np.sign(c) * wv), f"constant {c}"
+    y = o.qk_norm(bf16(np.ones(D)), w, 3.0)
+    assert np.array_equal(bf16_val(y), wv / 2), "eps inside the root"
+    x = np.zeros(D, np.float32)
+    x[5] = -0.75
+    y = bf16_val(o.qk_norm(bf16(x), w, 0.0))
+    want = np.zeros(D)
+    want[5] = -math.sqrt(D) * wv[5]  # sqrt(256) = 16: exact
+    assert np.array_equal(y, want), "single entry"
+
+
+def pin_qk_norm_scale_invariance(o):
+    """With eps = 0 the norm does not see a power-of-two scale of its input
+    (every step scales exactly), bit for bit."""
+    D = 128
+    x = rand_bf16(D, 1201)
+    w = rand_bf16(D, 1202)
+    base = o.qk_norm(x, w, 0.0)
+    for k in (-20, -3, 5, 30):
+        xs = bf16(bf16_val(x) * 2.0 ** k)
+        assert np.array_equal(o.qk_norm(xs, w, 0.0), base), f"scale 2^{k}"
+
+
+def pin_qk_norm_is_rounded_exact_value(o):
+    """Each element is the bf16 nearest (ties to even) to the exact
+    w_d x_d / sqrt(mean(x^2) + eps), the root to 50 digits (mpmath) and the
+    rounding in rational arithmetic; elements whose exact value lies within
+    2^-40 of a rounding boundary (relative) are skipped and must be rare."""
+    from fractions import Fraction
+    mpmath = __import__("mpmath")
+    mpmath.mp.dps = 50
+    skipped = checked = 0
+    for n, (D, eps, scale) in enumerate(((256, 1e-6, 1.0), (128, 1e-5, 1e-3), (256, 0.5, 4.0), (64, 0.0, 30.0))):
+        x = bf16(bf16_val(rand_bf16(D, 1300 + n)) * scale)
+        w = rand_bf16(D, 1400 + n)
+        y = o.qk_norm(x, w, eps)
+        xv, wv = bf16_val(x), bf16_val(w)
+        ss = sum(mpmath.mpf(float(v)) ** 2 for v in xv)
+        inv = 1 / mpmath.sqrt(ss / D + mpmath.mpf(eps))
+        for d in range(D):
+            exact = _mpf_fraction(mpmath.mpf(float(wv[d])) * mpmath.mpf(float(xv[d])) * inv)
+            if exact != 0 and _bf16_midpoint_distance(exact) < abs(float(exact)) * 2.0 ** -40:
+                skipped += 1
+                continue
+            checked += 1
+            assert int(y[d]) == _bf16_of_fraction(exact), f"case {n}, element {d}"
+    assert skipped <= 2 and checked > 600, (skipped, checked)
+
+
+def pin_qk_norm_applies_before_rope_to_q_and_new_keys(o):
+    """With QK-norm, decode, verify and append equal the same calls without
+    it on inputs normalised beforehand: the norm acts on q and on the new
+    keys (not on cached entries or V), before RoPE."""
+    Hq, Hkv, D, R, P = 4, 2, 16, 5, 4
+    eps = 1e-3
+    wq, wk = rand_bf16(D, 1501), rand_bf16(D, 1502)
+    nq = lambda a: np.stack([o.qk_norm(r, wq, eps) for r in a.reshape(-1, D)]).reshape(a.shape)
+    nk = lambda a: np.stack([o.qk_norm(r, wk, eps) for r in a.reshape(-1, D)]).reshape(a.shape)
+    norm = (wq, wk, eps)
+    # ring decode
+    Kr = rand_bf16((2, Hkv, R, D), 1503)
+    Vr = rand_bf16((2, Hkv, R, D), 1504)
+    q = rand_bf16((2, Hq, D), 1505)
+    kn = rand_bf16((2, Hkv, D), 1506)
+    vn = rand_bf16((2, Hkv, D), 1507)
+    a = o.decode_ring(Kr, Vr, [2, 4], [3, 5], q, kn, vn, [9, 40], 16, 1e4, qk_norm=norm)
+    b = o.decode_ring(Kr, Vr, [2, 4], [3, 5], nq(q), nk(kn), vn, [9, 40], 16, 1e4)
+    assert all(np.array_equal(x, y) for x, y in zip(a, b)), "ring decode"
+    a = o.decode_ring(Kr, Vr, [2, 4], [3, 5], q, kn, vn, [9, 40], 16, 1e4, qk_norm=(None, wk, eps))
+    b = o.decode_ring(Kr, Vr, [2, 4], [3, 5], q, nk(kn), vn, [9, 40], 16, 1e4)
+    assert all(np.array_equal(x, y) for x, y in zip(a, b)), "ring decode, keys only"
+    # verify
+    S, T = 1, 4
+    Kp, Vp, bt = _prefix_pool(S, Hkv, D, P, [6], T + 1, 1510)
+    qv = rand_bf16((S, T, Hq, D), 1511)
+    kv = rand_bf16((S, T, Hkv, D), 1512)
+    vv = rand_bf16((S, T, Hkv, D), 1513)
+    parent = np.array([[-1, 0, 0, 2]], np.int32)
+    a = o.verify(Kp, Vp, bt, [6], qv, kv, vv, parent, 16, 5e6, qk_norm=norm)
+    b = o.verify(Kp, Vp, bt, [6], nq(qv), nk(kv), vv, parent, 16, 5e6)
+    assert all(np.array_equal(x, y) for x, y in zip(a, b)), "verify"
+    # append (rotate on: normalised then turned; rotate off: stored as given)
+    Ka, Va = o.append_paged(Kp, Vp, bt, [6], [6], [3], kv[:, :3], vv[:, :3], 16, 5e6, qk_norm=norm)
+    Kb, Vb = o.append_paged(Kp, Vp, bt, [6], [6], [3], nk(kv[:, :3]), vv[:, :3], 16, 5e6)
+    assert np.array_equal(Ka, Kb) and np.array_equal(Va, Vb), "append"
+    Ka, _ = o.append_paged(Kp, Vp, bt, [6], [6], [3], kv[:, :3], vv[:, :3], 16, 5e6, rotate=False,
+                           qk_norm=norm)
+    Kb, _ = o.append_paged(Kp, Vp, bt, [6], [6], [3], kv[:, :3], vv[:, :3], 16, 5e6, rotate=False)
+    assert np.array_equal(Ka, Kb), "append without rotation stores the keys as given"
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -21,7 +21,7 @@ def dattn():
     return d
 
 
-def run_verify(dattn, oracle, case: synth.VerifyCase, write_back=True):
+def run_verify(dattn, oracle, case: synth.VerifyCase, write_back=True, qk_norm=None):
     c = case.cache
     S, T = case.q.shape[:2]
     k_pool, v_pool = dev(c.k), dev(c.v)
@@ -31,13 +31,16 @@ def run_verify(dattn, oracle, case: synth.VerifyCase, write_back=True):
     out = torch.full((S, T, case.Hq, case.D), float("nan"), device="cuda")
     layer = {"kind": dattn.CACHE_PAGED, "page_size": c.P, "rotary_dim": case.rope.rotary_dim,
              "rope_theta": case.rope.theta}
+    if qk_norm is not None:
+        layer.update(q_norm=qk_norm[0], k_norm=qk_norm[1], norm_eps=qk_norm[2])
     h = dattn.Handle(case.Hq, case.Hkv, case.D, [layer], S, max_context=int(c.seq_len.max()) or 1,
                      max_verify_rows=T)
     h.verify(0, dattn.paged_cache(k_pool, v_pool, bt, seq), q, k, v, par, out, gate=gate,
              write_back=write_back)
     assert h.get_error() == dattn.OK
     ref, ke = oracle.verify(c.k, c.v, c.block_table, c.seq_len, case.q, case.k, case.v,
-                            case.parent, case.rope.rotary_dim, case.rope.theta, gate=case.gate)
+                            case.parent, case.rope.rotary_dim, case.rope.theta, gate=case.gate,
+                            qk_norm=qk_norm)
     err = assert_close(out.cpu().numpy(), ref, "verify")
     if write_back:
         kexp, vexp = c.k.copy(), c.v.copy()

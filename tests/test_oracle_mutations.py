@@ -8,7 +8,8 @@ by one, a missing tree mask, a page offset off by one, sigmoid(-g), values
 taken from keys, truncation instead of rounding, quarter turns of the RoPE
 phase taken the wrong way, an uncentred phase remainder, the K entry rounded
 from the fp64-rounded sum instead of the exact one, a ring append slot off by
-one. If one of them passed every
+one, the QK-norm eps outside the root, the QK-norm sum of squares not divided
+by D. If one of them passed every
 pin, the pins would not be sharp enough to trust the oracle.
 """
 import pytest
@@ -16,7 +17,7 @@ import pytest
 import oracle as oracle_pkg
 from oracle_pins import ALL_PINS
 
-MUTATIONS = list(range(1, 19))
+MUTATIONS = list(range(1, 21))
 
 
 @pytest.mark.parametrize("mutation", MUTATIONS)

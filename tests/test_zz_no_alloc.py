@@ -9,6 +9,7 @@ first one's leftover scratch) must each match dattn_decode on the same inputs.
 """
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
@@ -55,6 +56,28 @@ def test_noalloc_write_back_matches_the_oracle(oracle):
         torch.cuda.synchronize()
         ref, ke, ve = oracle_decode(oracle, case)
         assert_close(dc.out.cpu().numpy(), ref, "noalloc vs oracle")
+        check_write_back(case, host_u16(dc.k), host_u16(dc.v), ke, ve)
+        h.close()
+
+
+def test_noalloc_with_qk_norm_matches_the_oracle(oracle):
+    """A layer with QK-norm: the set-up kernel copies the weights from its
+    parameters into the scratch array; outputs and written-back entries match
+    the oracle's."""
+    import decode_attention_kv_dattn_gb300 as dattn
+    from gpu_util import check_write_back, host_u16, oracle_decode
+    gen = torch.Generator().manual_seed(31)
+    for case in (synth.single_sliding_layer(1), synth.paged_batched(3, B=8)):
+        D = case.D
+        w = lambda: (1.0 + 0.25 * torch.randn(D, generator=gen)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        norm = (w(), w(), 1e-6)
+        dc = DeviceCase(case)
+        h = make_handle(dattn, case, qk_norm=norm)
+        dattn.decode_noalloc(h.config, 0, dc.cache_desc(dattn), dc.q, dc.k_new, dc.v_new, dc.pos, dc.out,
+                             gate=dc.gate, write_back=True)
+        torch.cuda.synchronize()
+        ref, ke, ve = oracle_decode(oracle, case, qk_norm=norm)
+        assert_close(dc.out.cpu().numpy(), ref, "noalloc with QK-norm vs oracle")
         check_write_back(case, host_u16(dc.k), host_u16(dc.v), ke, ve)
         h.close()
 
