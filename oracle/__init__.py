@@ -71,7 +71,13 @@ class Oracle:
         L.oracle_decode_concat.argtypes = [_I, _I, _I, _I, _I, _D, _P, _P, _I, _P, _P, _P, _P,
                                            _P, _P, _P, _I] + N3
         L.oracle_verify.argtypes = [_I, _I, _I, _I, _I, _I, _D, _P, _P, _I, _I, _P, _I, _P,
-                                    _P, _P, _P, _P, _P, _P, _P, _I] + N3
+                                    _P, _P, _P, _P, _P, _P, _P, _P, _I] + N3
+        L.oracle_verify_ring.argtypes = [_I, _I, _I, _I, _I, _I, _D, _P, _P, _I, _I, _P, _P, _P,
+                                         _P, _P, _P, _P, _P, _P, _P, _P, _I] + N3
+        L.oracle_commit_ring.argtypes = [_I, _I, _I, _I, _I, _D, _P, _P, _I, _I, _P, _P, _P,
+                                         _P, _P, _P, _P, _P, _P, _D]
+        L.oracle_commit_paged.argtypes = [_I, _I, _I, _I, _I, _D, _P, _P, _I, _I, _P, _I, _P, _P,
+                                          _P, _P, _P, _P, _P, _P, _D]
         L.oracle_append_ring.argtypes = [_I, _I, _I, _I, _I, _D, _P, _P, _I, _I, _P, _P, _P,
                                          _P, _P, _P, _I, _P, _D]
         L.oracle_append_paged.argtypes = [_I, _I, _I, _I, _I, _D, _P, _P, _I, _I, _P, _I, _P,
@@ -80,6 +86,7 @@ class Oracle:
         L.oracle_qk_norm.restype = None
         for f in ("oracle_rope_f64", "oracle_rope_bf16", "oracle_decode_ring",
                   "oracle_decode_paged", "oracle_decode_concat", "oracle_verify",
+                  "oracle_verify_ring", "oracle_commit_ring", "oracle_commit_paged",
                   "oracle_append_ring", "oracle_append_paged", "oracle_hardware_threads"):
             getattr(L, f).restype = _I
 
@@ -178,8 +185,9 @@ class Oracle:
 
     # ---- verify
     def verify(self, k_pages, v_pages, block_table, prefix_len, q, k, v, parent, r, theta,
-               gate=None, n_threads=0, qk_norm=None):
-        """q [S,T,Hq,D]; k/v [S,T,Hkv,D]; parent [S,T]. Returns (out f64, k_entry u16)."""
+               gate=None, n_threads=0, qk_norm=None, pos=None):
+        """q [S,T,Hq,D]; k/v [S,T,Hkv,D]; parent [S,T]; pos [S] root positions
+        (default prefix_len). Returns (out f64, k_entry u16)."""
         k_pages, v_pages, q, k, v = map(_u16, (k_pages, v_pages, q, k, v))
         gate = None if gate is None else _u16(gate)
         num_pages, Hkv, P, D = k_pages.shape
@@ -188,12 +196,62 @@ class Oracle:
         out = np.empty((S, T, Hq, D), np.float64)
         ke = np.empty((S, T, Hkv, D), np.uint16)
         pl, pa = _i32(prefix_len), _i32(parent)
+        ps = _i32(pos)
         rc = self.lib.oracle_verify(S, T, Hq, Hkv, D, r, theta, _ptr(k_pages), _ptr(v_pages),
-                                    num_pages, P, _ptr(bt), bt.shape[1], _ptr(pl), _ptr(q),
+                                    num_pages, P, _ptr(bt), bt.shape[1], _ptr(pl), _ptr(ps), _ptr(q),
                                     _ptr(k), _ptr(v), _ptr(pa), _ptr(gate), _ptr(out), _ptr(ke),
                                     n_threads, *_norm(qk_norm))
         self._check(rc, "verify")
         return out, ke
+
+    def verify_ring(self, k_ring, v_ring, ring_head, ring_count, pos, q, k, v, parent, r, theta,
+                    gate=None, stream_rows=None, n_threads=0, qk_norm=None):
+        """Tree verify over ring (sliding) layers: k_ring/v_ring [rows, Hkv, R, D];
+        pos [S] root positions. Returns (out f64, k_entry u16)."""
+        k_ring, v_ring, q, k, v = map(_u16, (k_ring, v_ring, q, k, v))
+        gate = None if gate is None else _u16(gate)
+        n_rows, Hkv, R, D = k_ring.shape
+        S, T, Hq, _ = q.shape
+        out = np.empty((S, T, Hq, D), np.float64)
+        ke = np.empty((S, T, Hkv, D), np.uint16)
+        sr, hd, ct, ps, pa = map(_i32, (stream_rows, ring_head, ring_count, pos, parent))
+        rc = self.lib.oracle_verify_ring(S, T, Hq, Hkv, D, r, theta, _ptr(k_ring), _ptr(v_ring), n_rows, R,
+                                         _ptr(sr), _ptr(hd), _ptr(ct), _ptr(ps), _ptr(q), _ptr(k), _ptr(v),
+                                         _ptr(pa), _ptr(gate), _ptr(out), _ptr(ke), n_threads,
+                                         *_norm(qk_norm))
+        self._check(rc, "verify_ring")
+        return out, ke
+
+    # ---- commit of accepted paths (returns updated copies and the status:
+    # 0, or 3 when some stream's list was not a path and was skipped)
+    def commit_ring(self, k_ring, v_ring, ring_head, pos, k, v, parent, accepted, num_accepted,
+                    r, theta, stream_rows=None, qk_norm=None):
+        kr, vr = _u16(k_ring).copy(), _u16(v_ring).copy()
+        k, v = _u16(k), _u16(v)
+        n_rows, Hkv, R, D = kr.shape
+        S, T = k.shape[:2]
+        rc = self.lib.oracle_commit_ring(S, T, Hkv, D, r, theta, _ptr(kr), _ptr(vr), n_rows, R,
+                                         _ptr(_i32(stream_rows)), _ptr(_i32(ring_head)), _ptr(_i32(pos)),
+                                         _ptr(k), _ptr(v), _ptr(_i32(parent)), _ptr(_i32(accepted)),
+                                         _ptr(_i32(num_accepted)), *_norm(qk_norm)[1:])
+        if rc not in (0, 3):
+            self._check(rc, "commit_ring")
+        return kr, vr, rc
+
+    def commit_paged(self, k_pages, v_pages, block_table, seq_len, pos, k, v, parent, accepted,
+                     num_accepted, r, theta, qk_norm=None):
+        kp, vp = _u16(k_pages).copy(), _u16(v_pages).copy()
+        k, v = _u16(k), _u16(v)
+        num_pages, Hkv, P, D = kp.shape
+        S, T = k.shape[:2]
+        bt = _i32(block_table)
+        rc = self.lib.oracle_commit_paged(S, T, Hkv, D, r, theta, _ptr(kp), _ptr(vp), num_pages, P, _ptr(bt),
+                                          bt.shape[1], _ptr(_i32(seq_len)), _ptr(_i32(pos)), _ptr(k), _ptr(v),
+                                          _ptr(_i32(parent)), _ptr(_i32(accepted)),
+                                          _ptr(_i32(num_accepted)), *_norm(qk_norm)[1:])
+        if rc not in (0, 3):
+            self._check(rc, "commit_paged")
+        return kp, vp, rc
 
     # ---- append (returns updated copies)
     def append_ring(self, k_ring, v_ring, start_index, start_pos, count, k, v, r, theta,

@@ -593,16 +593,98 @@ int oracle_decode_concat(int B, int Hq, int Hkv, int D, int r, double theta,
   return 0;
 }
 
-// ----- tree verify: S streams, T rows each. q [S,T,Hq,D], k/v [S,T,Hkv,D]
-// (k not yet rotated), parent [S,T] (parent[i] < i, -1 = root), prefix in
-// paged leases with prefix_len[s] tokens. Row i sits at position
-// prefix_len + depth(i); it attends to the whole prefix, its ancestors and
+}  // extern "C"
+
+namespace {
+
+// ----- tree verify: S streams x T rows. Row i of stream s sits at position
+// pos0[s] + depth(i) (depth 0 for a root); it attends to the cached entries
+// its layer keeps for that depth, to its ancestors in the tree and to
 // itself, each window key rotated at its own position. out [S,T,Hq,D];
 // k_entry [S,T,Hkv,D] receives every window key's bf16 entry.
+// ("TensorFold PR #608": verify windows under tree masks; a row equals the
+// plain decode of its root-to-node path.)
+
+// One (stream, KV head) of a verify call. cached(d, ck, cv) lists the cached
+// rows a row at depth d attends to.
+template <typename Cached>
+void verify_unit(int s, int j, int T, int Hq, int Hkv, int D, const Rot& rot, int64_t pos0,
+                 const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* parent,
+                 const uint16_t* gate, double* out, uint16_t* k_entry, Cached cached) {
+  const int32_t* par = parent + static_cast<size_t>(s) * T;
+  // depth of each node by walking to its root
+  std::vector<int> depth(T);
+  for (int i = 0; i < T; ++i) {
+    int dpt = 0;
+    for (int a = par[i]; a >= 0; a = par[a]) ++dpt;
+#if ORACLE_MUTATION == 9
+    depth[i] = dpt + 1;  // planted: depth counted from 1
+#else
+    depth[i] = dpt;
+#endif
+  }
+  // rotated bf16 entries of the window keys, each at its own position
+  std::vector<uint16_t> ent(static_cast<size_t>(T) * D);
+  std::vector<double> entd(static_cast<size_t>(T) * D);
+  for (int i = 0; i < T; ++i) {
+    const size_t src = ((static_cast<size_t>(s) * T + i) * Hkv + j) * D;
+    std::vector<uint16_t> kbuf;
+    rope_entry(normed(k + src, rot.kn, D, rot.eps, kbuf), D, rot.r, rot.theta, pos0 + depth[i],
+               ent.data() + static_cast<size_t>(i) * D);
+    for (int d = 0; d < D; ++d) entd[static_cast<size_t>(i) * D + d] = bf16_value(ent[static_cast<size_t>(i) * D + d]);
+    if (k_entry) std::memcpy(k_entry + src, ent.data() + static_cast<size_t>(i) * D, D * 2);
+  }
+  std::vector<double> qhat(D);
+  for (int i = 0; i < T; ++i) {
+    std::vector<const uint16_t*> ck, cv;
+    cached(depth[i], ck, cv);
+    // the row's tree path: itself and its ancestors
+    std::vector<const double*> ek;
+    std::vector<const uint16_t*> ev;
+#if ORACLE_MUTATION == 10
+    for (int a = 0; a < T; ++a) {  // planted: no tree mask
+#else
+    for (int a = i; a >= 0; a = par[a]) {
+#endif
+      ek.push_back(entd.data() + static_cast<size_t>(a) * D);
+      ev.push_back(v + ((static_cast<size_t>(s) * T + a) * Hkv + j) * D);
+    }
+    for (int h = 0; h < Hq; ++h) {
+      if (kv_head_of(h, Hq, Hkv) != j) continue;
+      const size_t qi = (static_cast<size_t>(s) * T + i) * Hq + h;
+      std::vector<uint16_t> qbuf;
+      rope_rotate(normed(q + qi * D, rot.qn, D, rot.eps, qbuf), D, rot.r, rot.theta, pos0 + depth[i],
+                  qhat.data());
+      double* o = out + qi * D;
+      attend_score_space(qhat.data(), D, ck, cv, ek, ev, o);
+      if (gate) {
+        const double g = sigmoid(bf16_value(gate[qi]));
+        for (int d = 0; d < D; ++d) o[d] *= g;
+      }
+    }
+  }
+}
+
+bool parents_ok(int S, int T, const int32_t* parent) {
+  for (int s = 0; s < S; ++s)
+    for (int i = 0; i < T; ++i) {
+      const int pa = parent[static_cast<size_t>(s) * T + i];
+      if (pa < -1 || pa >= i) return false;
+    }
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+// Paged layer: a row at any depth attends to the stream's whole prefix of
+// prefix_len[s] tokens; the window's root sits at pos[s], or at prefix_len[s]
+// when pos is null.
 int oracle_verify(int S, int T, int Hq, int Hkv, int D, int r, double theta,
                   const uint16_t* k_pages, const uint16_t* v_pages, int num_pages, int P,
                   const int32_t* block_table, int bt_stride, const int32_t* prefix_len,
-                  const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                  const int32_t* pos, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                   const int32_t* parent, const uint16_t* gate, double* out,
                   uint16_t* k_entry, int n_threads, const uint16_t* q_norm, const uint16_t* k_norm,
                   double norm_eps) {
@@ -613,71 +695,67 @@ int oracle_verify(int S, int T, int Hq, int Hkv, int D, int r, double theta,
       const int pg = block_table[static_cast<size_t>(s) * bt_stride + t / P];
       if (pg < 0 || pg >= num_pages) return 2;
     }
-    for (int i = 0; i < T; ++i) {
-      const int pa = parent[static_cast<size_t>(s) * T + i];
-      if (pa < -1 || pa >= i) return 3;
-    }
   }
+  if (!parents_ok(S, T, parent)) return 3;
+  const Rot rot{r, theta, q_norm, k_norm, norm_eps};
   parallel_for(S * Hkv, n_threads, [&](int item) {
     const int s = item / Hkv, j = item % Hkv;
-    const int32_t* par = parent + static_cast<size_t>(s) * T;
-    // depth of each node by walking to its root
-    std::vector<int> depth(T);
-    for (int i = 0; i < T; ++i) {
-      int dpt = 0;
-      for (int a = par[i]; a >= 0; a = par[a]) ++dpt;
-#if ORACLE_MUTATION == 9
-      depth[i] = dpt + 1;  // planted: depth counted from 1
-#else
-      depth[i] = dpt;
-#endif
-    }
-    // rotated bf16 entries of the window keys, each at its own position
-    std::vector<uint16_t> ent(static_cast<size_t>(T) * D);
-    std::vector<double> entd(static_cast<size_t>(T) * D);
-    for (int i = 0; i < T; ++i) {
-      const size_t src = ((static_cast<size_t>(s) * T + i) * Hkv + j) * D;
-      std::vector<uint16_t> kbuf;
-      rope_entry(normed(k + src, k_norm, D, norm_eps, kbuf), D, r, theta, prefix_len[s] + depth[i],
-                 ent.data() + static_cast<size_t>(i) * D);
-      for (int d = 0; d < D; ++d) entd[static_cast<size_t>(i) * D + d] = bf16_value(ent[static_cast<size_t>(i) * D + d]);
-      if (k_entry) std::memcpy(k_entry + src, ent.data() + static_cast<size_t>(i) * D, D * 2);
-    }
-    // the prefix rows
-    std::vector<const uint16_t*> ck, cv;
+    std::vector<const uint16_t*> pk, pv;
     for (int t = 0; t < prefix_len[s]; ++t) {
       const int pg = block_table[static_cast<size_t>(s) * bt_stride + t / P];
       const size_t row = ((static_cast<size_t>(pg) * Hkv + j) * P + t % P) * D;
-      ck.push_back(k_pages + row);
-      cv.push_back(v_pages + row);
+      pk.push_back(k_pages + row);
+      pv.push_back(v_pages + row);
     }
-    std::vector<double> qhat(D);
-    for (int i = 0; i < T; ++i) {
-      // the row's tree path: itself and its ancestors
-      std::vector<const double*> ek;
-      std::vector<const uint16_t*> ev;
-#if ORACLE_MUTATION == 10
-      for (int a = 0; a < T; ++a) {  // planted: no tree mask
+    const int64_t pos0 = pos ? pos[s] : prefix_len[s];
+    verify_unit(s, j, T, Hq, Hkv, D, rot, pos0, q, k, v, parent, gate, out, k_entry,
+                [&](int, std::vector<const uint16_t*>& ck, std::vector<const uint16_t*>& cv) {
+                  ck = pk;
+                  cv = pv;
+                });
+  });
+  return 0;
+}
+
+// Ring (sliding-window) layer: ring row stream_rows[s] (identity if null)
+// holds ring_count[s] valid entries, the slots before ring_head[s]. A row at
+// depth d attends to the newest min(count, R - d) of them: what the ring
+// holds after its d ancestors were appended, the window keeping R cached
+// tokens - the entries the plain decode of its path would see.
+int oracle_verify_ring(int S, int T, int Hq, int Hkv, int D, int r, double theta,
+                       const uint16_t* k_ring, const uint16_t* v_ring, int n_rows, int R,
+                       const int32_t* stream_rows, const int32_t* ring_head, const int32_t* ring_count,
+                       const int32_t* pos, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                       const int32_t* parent, const uint16_t* gate, double* out, uint16_t* k_entry,
+                       int n_threads, const uint16_t* q_norm, const uint16_t* k_norm, double norm_eps) {
+  if (!shape_ok(Hq, Hkv, D, r) || R <= 0 || T <= 0) return 1;
+  for (int s = 0; s < S; ++s) {
+    const int row = stream_rows ? stream_rows[s] : s;
+    if (row < 0 || row >= n_rows) return 2;
+    if (ring_head[s] < 0 || ring_head[s] >= R || ring_count[s] < 0 || ring_count[s] > R) return 2;
+  }
+  if (!parents_ok(S, T, parent)) return 3;
+  const Rot rot{r, theta, q_norm, k_norm, norm_eps};
+  parallel_for(S * Hkv, n_threads, [&](int item) {
+    const int s = item / Hkv, j = item % Hkv;
+    const int row = stream_rows ? stream_rows[s] : s;
+    const size_t base = (static_cast<size_t>(row) * Hkv + j) * R;
+    verify_unit(s, j, T, Hq, Hkv, D, rot, pos[s], q, k, v, parent, gate, out, k_entry,
+                [&](int d, std::vector<const uint16_t*>& ck, std::vector<const uint16_t*>& cv) {
+#if ORACLE_MUTATION == 21
+                  const int keep = ring_count[s];  // planted: the path's entries drop nothing
+                  (void)d;
 #else
-      for (int a = i; a >= 0; a = par[a]) {
+                  const int keep = std::min(ring_count[s], std::max(0, R - d));
 #endif
-        ek.push_back(entd.data() + static_cast<size_t>(a) * D);
-        ev.push_back(v + ((static_cast<size_t>(s) * T + a) * Hkv + j) * D);
-      }
-      for (int h = 0; h < Hq; ++h) {
-        if (kv_head_of(h, Hq, Hkv) != j) continue;
-        const size_t qi = (static_cast<size_t>(s) * T + i) * Hq + h;
-        std::vector<uint16_t> qbuf;
-        rope_rotate(normed(q + qi * D, q_norm, D, norm_eps, qbuf), D, r, theta, prefix_len[s] + depth[i],
-                    qhat.data());
-        double* o = out + qi * D;
-        attend_score_space(qhat.data(), D, ck, cv, ek, ev, o);
-        if (gate) {
-          const double g = sigmoid(bf16_value(gate[qi]));
-          for (int d = 0; d < D; ++d) o[d] *= g;
-        }
-      }
-    }
+                  ck.clear();
+                  cv.clear();
+                  for (int i = 0; i < keep; ++i) {  // newest first
+                    const int slot = ((ring_head[s] - 1 - i) % R + R) % R;
+                    ck.push_back(k_ring + (base + slot) * D);
+                    cv.push_back(v_ring + (base + slot) * D);
+                  }
+                });
   });
   return 0;
 }
@@ -749,6 +827,90 @@ int oracle_append_paged(int B, int Tmax, int Hkv, int D, int r, double theta,
     }
   }
   return 0;
+}
+
+// ----- commit of the accepted verify paths ("TensorFold PR #608": a verify
+// round commits only each stream's accepted path). accepted [S, T] lists the
+// accepted nodes of stream s root first, num_accepted[s] of them; they must
+// form a path from a root (accepted[0] a root, each next node a child of the
+// one before). Node accepted[s][d] goes to cache index start + d - ring: slot
+// (ring_head[s] + d) mod R of ring row stream_rows[s]; paged: token
+// seq_len[s] + d - with its key rotated at pos[s] + d: the entry that the
+// verify row of that node and the plain decode of its path use. k, v are the
+// verify call's window inputs [S, T, Hkv, D]. A stream whose list is not such
+// a path is left unchanged, and the call then returns 3.
+}  // extern "C"
+
+namespace {
+bool path_ok(int T, const int32_t* par, const int32_t* acc, int n) {
+  if (n < 0 || n > T) return false;
+  for (int d = 0; d < n; ++d) {
+    const int a = acc[d];
+    if (a < 0 || a >= T || par[a] != (d == 0 ? -1 : acc[d - 1])) return false;
+  }
+  return true;
+}
+
+// the accepted nodes' k and v rows gathered into [S, T, Hkv, D]; counts[s] =
+// the path length, or 0 for a stream whose list is not a path
+bool gather_paths(int S, int T, int Hkv, int D, const uint16_t* k, const uint16_t* v,
+                  const int32_t* parent, const int32_t* accepted, const int32_t* num_accepted,
+                  std::vector<uint16_t>& kg, std::vector<uint16_t>& vg, std::vector<int32_t>& counts) {
+  const size_t row = static_cast<size_t>(Hkv) * D;
+  kg.assign(static_cast<size_t>(S) * T * row, 0);
+  vg.assign(kg.size(), 0);
+  counts.assign(S, 0);
+  bool all_ok = true;
+  for (int s = 0; s < S; ++s) {
+    const int32_t* acc = accepted + static_cast<size_t>(s) * T;
+    if (!path_ok(T, parent + static_cast<size_t>(s) * T, acc, num_accepted[s])) {
+      all_ok = false;
+      continue;
+    }
+    counts[s] = num_accepted[s];
+    for (int d = 0; d < counts[s]; ++d) {
+#if ORACLE_MUTATION == 22
+      const size_t src = (static_cast<size_t>(s) * T + d) * row;  // planted: the first nodes, not the path's
+#else
+      const size_t src = (static_cast<size_t>(s) * T + acc[d]) * row;
+#endif
+      const size_t dst = (static_cast<size_t>(s) * T + d) * row;
+      std::memcpy(&kg[dst], k + src, row * 2);
+      std::memcpy(&vg[dst], v + src, row * 2);
+    }
+  }
+  return all_ok;
+}
+}  // namespace
+
+extern "C" {
+
+int oracle_commit_ring(int S, int T, int Hkv, int D, int r, double theta, uint16_t* k_ring,
+                       uint16_t* v_ring, int n_rows, int R, const int32_t* stream_rows,
+                       const int32_t* ring_head, const int32_t* pos, const uint16_t* k,
+                       const uint16_t* v, const int32_t* parent, const int32_t* accepted,
+                       const int32_t* num_accepted, const uint16_t* k_norm, double norm_eps) {
+  std::vector<uint16_t> kg, vg;
+  std::vector<int32_t> counts;
+  const bool ok = gather_paths(S, T, Hkv, D, k, v, parent, accepted, num_accepted, kg, vg, counts);
+  const int rc = oracle_append_ring(S, T, Hkv, D, r, theta, k_ring, v_ring, n_rows, R, stream_rows, ring_head,
+                                    pos, counts.data(), kg.data(), vg.data(), 1, k_norm, norm_eps);
+  return rc != 0 ? rc : (ok ? 0 : 3);
+}
+
+int oracle_commit_paged(int S, int T, int Hkv, int D, int r, double theta, uint16_t* k_pages,
+                        uint16_t* v_pages, int num_pages, int P, const int32_t* block_table,
+                        int bt_stride, const int32_t* seq_len, const int32_t* pos,
+                        const uint16_t* k, const uint16_t* v, const int32_t* parent,
+                        const int32_t* accepted, const int32_t* num_accepted,
+                        const uint16_t* k_norm, double norm_eps) {
+  std::vector<uint16_t> kg, vg;
+  std::vector<int32_t> counts;
+  const bool ok = gather_paths(S, T, Hkv, D, k, v, parent, accepted, num_accepted, kg, vg, counts);
+  const int rc = oracle_append_paged(S, T, Hkv, D, r, theta, k_pages, v_pages, num_pages, P, block_table,
+                                     bt_stride, seq_len, pos, counts.data(), kg.data(), vg.data(), 1, k_norm,
+                                     norm_eps);
+  return rc != 0 ? rc : (ok ? 0 : 3);
 }
 
 int oracle_hardware_threads(void) {

@@ -709,6 +709,103 @@ def pin_append_places_rotated_entries(o):
     assert np.sum(Ko != NAN) == written and np.sum(Vo != NAN) == written
 
 
+def _path(parent_row, i):
+    """Root-first list of node i's ancestors (without i)."""
+    out = []
+    a = parent_row[i]
+    while a >= 0:
+        out.append(int(a))
+        a = parent_row[a]
+    return out[::-1]
+
+
+def pin_ring_verify_row_equals_decode_of_its_path(o):
+    """Verify over a ring (sliding) layer: each row equals the plain ring
+    decode of its token after its root-to-parent path was appended to the ring
+    (so the ring drops its oldest entries as it fills), for full and partly
+    filled rings, and its window entry equals that decode's entry."""
+    S, T, Hq, Hkv, D, R = 3, 7, 4, 2, 16, 9
+    r, theta = 16, 1e4
+    parent = np.array([[-1, 0, 1, 2, 3, 4, 5], [-1, 0, 0, 1, 3, 4, 2], [-1, 0, 1, 1, 0, 4, 5]], np.int32)
+    Kr = rand_bf16((4, Hkv, R, D), 1601)
+    Vr = rand_bf16((4, Hkv, R, D), 1602)
+    rows = np.array([2, 0, 3], np.int32)
+    head = np.array([4, 0, 8], np.int32)
+    count = np.array([R, R - 2, 3], np.int32)
+    pos = np.array([50, 7, 3], np.int32)
+    q = rand_bf16((S, T, Hq, D), 1603)
+    k = rand_bf16((S, T, Hkv, D), 1604)
+    v = rand_bf16((S, T, Hkv, D), 1605)
+    g = rand_bf16((S, T, Hq), 1606)
+    out, ke = o.verify_ring(Kr, Vr, head, count, pos, q, k, v, parent, r, theta, gate=g, stream_rows=rows)
+    for s in range(S):
+        for i in range(T):
+            path = _path(parent[s], i)
+            d = len(path)
+            Ks, Vs = Kr, Vr
+            if d:
+                kp = k[s, path][None]
+                vp = v[s, path][None]
+                Ks, Vs = o.append_ring(Kr, Vr, [head[s]], [pos[s]], [d], kp, vp, r, theta,
+                                       stream_rows=rows[s:s + 1])
+            dec, kent, _ = o.decode_ring(Ks, Vs, [(head[s] + d) % R], [min(count[s] + d, R)], q[s, i][None],
+                                         k[s, i][None], v[s, i][None], [pos[s] + d], r, theta,
+                                         gate=g[s, i][None], stream_rows=rows[s:s + 1])
+            close(out[s, i], dec[0], 1e-12, f"ring verify row {s},{i}")
+            assert np.array_equal(ke[s, i], kent[0]), "window entry differs from the decode entry"
+
+
+def pin_commit_equals_serial_decode_write_backs(o):
+    """Committing an accepted path writes the same cache as decoding the
+    path's tokens one after another with write-back, on ring and paged
+    layers; a list that is not a path from a root leaves its stream alone."""
+    S, T, Hq, Hkv, D, R, P = 3, 6, 4, 2, 16, 7, 4
+    r, theta = 16, 5e6
+    parent = np.array([[-1, 0, 0, 1, 3, 2], [-1, 0, 1, 2, 3, 4], [-1, 0, 0, 2, 2, 4]], np.int32)
+    accepted = np.full((S, T), -1, np.int32)
+    acc = [[0, 2, 5], [0, 1, 2, 3, 4, 5], [0, 2, 4, 5]]
+    for s, a in enumerate(acc):
+        accepted[s, :len(a)] = a
+    num = np.array([3, 6, 4], np.int32)
+    k = rand_bf16((S, T, Hkv, D), 1701)
+    v = rand_bf16((S, T, Hkv, D), 1702)
+    q = rand_bf16((S, 1, Hq, D), 1703)
+    # ring
+    Kr = rand_bf16((S, Hkv, R, D), 1704)
+    Vr = rand_bf16((S, Hkv, R, D), 1705)
+    head = np.array([5, 0, 2], np.int32)
+    pos = np.array([30, 0, 12], np.int32)
+    Kc, Vc, rc = o.commit_ring(Kr, Vr, head, pos, k, v, parent, accepted, num, r, theta)
+    assert rc == 0
+    Ks, Vs = Kr.copy(), Vr.copy()
+    for s in range(S):
+        for d, a in enumerate(acc[s]):
+            _, ke, ve = o.decode_ring(Ks, Vs, [(head[s] + d) % R], [R], q[s], k[s, a][None], v[s, a][None],
+                                      [pos[s] + d], r, theta, stream_rows=[s])
+            Ks[s, :, (head[s] + d) % R] = ke[0]
+            Vs[s, :, (head[s] + d) % R] = ve[0]
+    assert np.array_equal(Kc, Ks) and np.array_equal(Vc, Vs), "ring commit"
+    # paged
+    Kp, Vp, bt = _prefix_pool(S, Hkv, D, P, [5, 0, 9], T + 1, 1706)
+    seq = np.array([5, 0, 9], np.int32)
+    Kc, Vc, rc = o.commit_paged(Kp, Vp, bt, seq, seq, k, v, parent, accepted, num, r, theta)
+    assert rc == 0
+    Ks, Vs = Kp.copy(), Vp.copy()
+    for s in range(S):
+        for d, a in enumerate(acc[s]):
+            t = seq[s] + d
+            _, ke, ve = o.decode_paged(Ks, Vs, bt[s:s + 1], [t], q[s], k[s, a][None], v[s, a][None], [t],
+                                       r, theta)
+            Ks[bt[s, t // P], :, t % P] = ke[0]
+            Vs[bt[s, t // P], :, t % P] = ve[0]
+    assert np.array_equal(Kc, Ks) and np.array_equal(Vc, Vs), "paged commit"
+    # a broken path (node 3's parent is 2, not 1) leaves stream 2 alone
+    bad = accepted.copy()
+    bad[2, :3] = [0, 1, 3]
+    Kc, Vc, rc = o.commit_ring(Kr, Vr, head, pos, k, v, parent, bad, np.array([0, 0, 3], np.int32), r, theta)
+    assert rc == 3 and np.array_equal(Kc, Kr) and np.array_equal(Vc, Vr), "broken path"
+
+
 # ------------------------------------------------------------------ QK-norm
 # "pega-omni PR #4", talker kernels: RoPE with QK-norm. Reading (the page
 # gives no formula): y = bf16(w * x / sqrt(mean(x^2) + eps)), per head.
