@@ -72,7 +72,7 @@ class DecodeArgs(ctypes.Structure):
 class VerifyArgs(ctypes.Structure):
     _fields_ = [("num_streams", _int), ("rows", _int), ("q", _vp), ("k", _vp), ("v", _vp),
                 ("parent", _vp), ("gate", _vp), ("out", _vp), ("max_prefix_len", _int),
-                ("write_back", _int)]
+                ("write_back", _int), ("pos", _vp)]
 
 
 lib.dattn_create.argtypes = [ctypes.POINTER(Config), _int, ctypes.POINTER(_vp)]
@@ -84,6 +84,8 @@ lib.dattn_decode.argtypes = [_vp, _int, ctypes.POINTER(Cache), ctypes.POINTER(De
 lib.dattn_decode.restype = _int
 lib.dattn_verify.argtypes = [_vp, _int, ctypes.POINTER(Cache), ctypes.POINTER(VerifyArgs), _vp]
 lib.dattn_verify.restype = _int
+lib.dattn_commit.argtypes = [_vp, _int, ctypes.POINTER(Cache), _int, _int, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+lib.dattn_commit.restype = _int
 lib.dattn_get_error.argtypes = [_vp, _vp]
 lib.dattn_get_error.restype = _int
 lib.dattn_error_string.argtypes = [_int]
@@ -97,7 +99,7 @@ lib.dattn_debug_config.argtypes = [_vp, _int, ctypes.c_uint]
 lib.dattn_debug_config.restype = _int
 DEBUG_WITHHOLD_Q = 1
 
-EXPORTS = ("dattn_create", "dattn_append_kv", "dattn_decode", "dattn_verify",
+EXPORTS = ("dattn_create", "dattn_append_kv", "dattn_decode", "dattn_verify", "dattn_commit",
            "dattn_get_error", "dattn_error_string", "dattn_destroy", "dattn_decode_noalloc",
            "dattn_debug_config")
 
@@ -214,13 +216,22 @@ class Handle:
                                 _stream_ptr(stream)), "dattn_decode")
 
     def verify(self, layer, cache: Cache, q, k, v, parent, out, gate=None, max_prefix_len=0,
-               write_back=True, stream=None):
+               write_back=True, pos=None, stream=None):
         """q [S, T, Hq, D], k/v [S, T, Hkv, D] bf16; parent [S, T] int32; out [S, T, Hq, D]
-        fp32; gate [S, T, Hq] bf16 or None. The prefix length is the cache's seq_len."""
+        fp32; gate [S, T, Hq] bf16 or None; pos [S] int32 root positions (default: the
+        cache's seq_len; ring layers need it and take write_back=False)."""
         args = VerifyArgs(q.shape[0], q.shape[1], _ptr(q), _ptr(k), _ptr(v), _ptr(parent),
-                          _ptr(gate), _ptr(out), int(max_prefix_len), int(write_back))
+                          _ptr(gate), _ptr(out), int(max_prefix_len), int(write_back), _ptr(pos))
         _check(lib.dattn_verify(self._h, layer, ctypes.byref(cache), ctypes.byref(args),
                                 _stream_ptr(stream)), "dattn_verify")
+
+    def commit(self, layer, cache: Cache, k, v, parent, accepted, num_accepted, pos, stream=None):
+        """Write each stream's accepted path (accepted [S, T] int32 node indices root
+        first, num_accepted [S]) at the cache's next indices, rotated at pos + d;
+        k, v, parent as given to the verify call."""
+        _check(lib.dattn_commit(self._h, layer, ctypes.byref(cache), k.shape[0], k.shape[1], _ptr(k),
+                                _ptr(v), _ptr(parent), _ptr(accepted), _ptr(num_accepted), _ptr(pos),
+                                _stream_ptr(stream)), "dattn_commit")
 
     def debug_config(self, flags=0, wait_limit_us=0):
         """Testing aid: the limit of the device's bounded waits and fault

@@ -356,6 +356,45 @@ int dattn_append_kv(dattn_t* h, int layer, const dattn_cache* cache, int num_str
   return rc;
 }
 
+int dattn_commit(dattn_t* h, int layer, const dattn_cache* cache, int num_streams, int rows, const void* k,
+                 const void* v, const int32_t* parent, const int32_t* accepted, const int32_t* num_accepted,
+                 const int32_t* pos, dattn_stream_t stream) {
+  if (!h || layer < 0 || layer >= static_cast<int>(h->layers.size())) return DATTN_EINVAL;
+  const dattn_layer_config& L = h->layers[layer];
+  int rc = check_cache(L, cache);
+  if (rc != DATTN_OK) return rc;
+  if (num_streams <= 0 || rows <= 0 || !k || !v || !parent || !accepted || !num_accepted) return DATTN_EINVAL;
+  if (L.rotary_dim > 0 && !pos) return DATTN_EINVAL;
+  if (!aligned16(k) || !aligned16(v)) return DATTN_EINVAL;
+  if (rows > 16) return DATTN_EXCEEDS;
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return DATTN_ECUDA;
+  // a gathered append: node accepted[b][d] to cache index start + d, rotated
+  // at pos[b] + d, where start is the ring head or the prefix length
+  AppendArgs a{};
+  a.c = make_view(h, L, cache);
+  a.B = num_streams;
+  a.Tmax = rows;
+  a.Hkv = h->Hkv;
+  a.D = h->D;
+  a.r = L.rotary_dim;
+  a.start_index = L.cache_kind == DATTN_CACHE_RING ? cache->ring_head : cache->seq_len;
+  a.start_pos = pos;
+  a.count = num_accepted;
+  a.k = static_cast<const uint16_t*>(k);
+  a.v = static_cast<const uint16_t*>(v);
+  a.rotate = 1;
+  a.rope_step = h->rope_step[layer];
+  a.err = h->err;
+  a.k_norm = h->k_norm[layer];
+  a.norm_eps = L.norm_eps;
+  a.gather = accepted;
+  a.parent = parent;
+  rc = cuda_status(launch_append(a, reinterpret_cast<cudaStream_t>(stream)), "commit");
+  if (rc == DATTN_OK) record_launch(stream, cache->k);
+  return rc;
+}
+
 int dattn_decode(dattn_t* h, int layer, const dattn_cache* cache, const dattn_decode_args* args,
                  dattn_stream_t stream) {
   if (!h || !args || layer < 0 || layer >= static_cast<int>(h->layers.size())) return DATTN_EINVAL;
@@ -421,8 +460,9 @@ int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, const dattn_ve
                  dattn_stream_t stream) {
   if (!h || !args || layer < 0 || layer >= static_cast<int>(h->layers.size())) return DATTN_EINVAL;
   const dattn_layer_config& L = h->layers[layer];
+  const bool ring = L.cache_kind == DATTN_CACHE_RING;
   // the prefix pass reads pages as 16-row groups
-  if (L.cache_kind != DATTN_CACHE_PAGED || L.page_size % 16 != 0) return DATTN_EUNSUPPORTED;
+  if (!ring && L.page_size % 16 != 0) return DATTN_EUNSUPPORTED;
   int rc = check_cache(L, cache);
   if (rc != DATTN_OK) return rc;
   const int S = args->num_streams, T = args->rows;
@@ -431,8 +471,15 @@ int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, const dattn_ve
   if (!args->q || !args->k || !args->v || !args->parent || !args->out) return DATTN_EINVAL;
   if (!aligned16(args->q) || !aligned16(args->k) || !aligned16(args->v) || !aligned16(args->out))
     return DATTN_EINVAL;
-  const int n_max = args->max_prefix_len > 0 ? args->max_prefix_len : h->max_context;
-  if (n_max > h->max_context) return DATTN_EXCEEDS;
+  // ring layers: the root positions are the caller's, and nothing is written
+  if (ring && (!args->pos || args->write_back)) return DATTN_EINVAL;
+  int n_max;
+  if (ring) {
+    n_max = L.ring_slots;
+  } else {
+    n_max = args->max_prefix_len > 0 ? args->max_prefix_len : h->max_context;
+    if (n_max > h->max_context) return DATTN_EXCEEDS;
+  }
   DeviceGuard guard(h->device);
   if (!guard.ok) return DATTN_ECUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -447,6 +494,7 @@ int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, const dattn_ve
   va.T = T;
   va.Hkv = h->Hkv;
   va.G = h->G;
+  va.parent = args->parent;
   va.qhl = h->qhl;
   va.ctas = static_cast<int>(ctas);
   va.max_len = n_max;
@@ -462,7 +510,7 @@ int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, const dattn_ve
   ra.r = L.rotary_dim;
   ra.q = static_cast<const uint16_t*>(args->q);
   ra.k = static_cast<const uint16_t*>(args->k);
-  ra.prefix_len = cache->seq_len;
+  ra.prefix_len = args->pos ? args->pos : cache->seq_len;  // the roots' positions
   ra.parent = args->parent;
   ra.T = T;
   ra.rope_step = h->rope_step[layer];

@@ -125,6 +125,11 @@ struct AppendArgs {
   int* err;
   const uint16_t* k_norm;      // [D] QK-norm weights of the keys (with rotate), or null
   double norm_eps;
+  // commit of verify paths: token t of row b is source row gather[b * Tmax + t]
+  // of k/v ([B, Tmax, Hkv, D]), and the row's first count[b] entries of gather
+  // must form a path from a root under parent [B, Tmax]; null for a plain append
+  const int32_t* gather;
+  const int32_t* parent;
 };
 
 // Tensor-core pass of tree verify over each stream's paged prefix (stream-K
@@ -136,8 +141,11 @@ struct VerifySplitArgs {
   CUtensorMap tmap_k;          // the layer's K pool as [rows, D] bf16, boxes of 16 rows x 64 dims
   CUtensorMap tmap_v;          // its V pool as (64 dims, rows, D/64 regions), boxes of (64, 16, D/64)
   CUtensorMap tmap_q;          // q hi/lo as (D, Hq, S*T, 2) bf16, boxes of (64, G, T, 1)
-  CacheView c;                 // paged, page size a multiple of 16; seq_len = prefix lengths
+  CacheView c;                 // paged (page size a multiple of 16; seq_len = prefix lengths)
+                               // or ring (all R slots scanned, the valid ones kept)
   int S, T, Hkv, G;
+  const int32_t* parent;       // [S, T] (ring layers: a row's depth sets how many of the
+                               // oldest entries its path pushed out)
   const uint16_t* qhl;         // [2][qhl_rows, Hq, D]: q as bf16 hi (the first plane) and lo
   int ctas;
   int max_len;

@@ -187,6 +187,21 @@ __global__ void __launch_bounds__(kRopeThreads) append_kernel(const AppendArgs a
     return;
   }
   if (t >= cnt) return;
+  int src_t = t;
+  if (a.gather) {
+    // the row's accepted nodes must form a path from a root: else nothing of
+    // the row is written
+    const int32_t* acc = a.gather + static_cast<int64_t>(b) * a.Tmax;
+    const int32_t* par = a.parent + static_cast<int64_t>(b) * a.Tmax;
+    for (int d = 0; d < cnt; ++d) {
+      const int node = acc[d];
+      if (node < 0 || node >= a.Tmax || par[node] != (d == 0 ? -1 : acc[d - 1])) {
+        if (t == 0 && threadIdx.x == 0) raise_error(a.err, ERR_INDEX);
+        return;
+      }
+    }
+    src_t = acc[t];
+  }
   const int64_t idx = static_cast<int64_t>(a.start_index[b]) + t;
   if (idx < 0) {
     if (threadIdx.x == 0) raise_error(a.err, ERR_INDEX);
@@ -213,7 +228,7 @@ __global__ void __launch_bounds__(kRopeThreads) append_kernel(const AppendArgs a
     dst0 = (static_cast<int64_t>(row) * a.Hkv * c.R + idx % c.R) * a.D;
     head_stride = static_cast<int64_t>(c.R) * a.D;
   }
-  const int64_t src0 = (static_cast<int64_t>(b) * a.Tmax + t) * a.Hkv * a.D;
+  const int64_t src0 = (static_cast<int64_t>(b) * a.Tmax + src_t) * a.Hkv * a.D;
   // V: plain copy, 16 bytes per thread-step.  (Every return above is taken by
   // the whole CTA.)
   for (int e = threadIdx.x; e < a.Hkv * a.D / 8; e += kRopeThreads) {

@@ -210,11 +210,22 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
   // ---- unit table (caller metadata only)
   for (int u = threadIdx.x; u < U; u += kVThreads) {
     const int s = u / Hkv;
-    int n = c.seq_len[s];
-    const int cap = min(a.max_len, c.bt_stride * c.P);
-    if (n < 0 || n > cap) {
-      if (cta == 0 && u - s * Hkv == 0) raise_error(a.err, ERR_LENGTH);
-      n = n < 0 ? 0 : cap;
+    int n;
+    if (c.paged) {
+      n = c.seq_len[s];
+      const int cap = min(a.max_len, c.bt_stride * c.P);
+      if (n < 0 || n > cap) {
+        if (cta == 0 && u - s * Hkv == 0) raise_error(a.err, ERR_LENGTH);
+        n = n < 0 ? 0 : cap;
+      }
+    } else {
+      // a ring: every slot is scanned (the valid ones are masked in), none
+      // when the ring is empty or its metadata is out of range
+      const int cnt = c.ring_count[s], hd = c.ring_head[s];
+      const int row = c.stream_rows ? c.stream_rows[s] : s;
+      const bool bad = cnt < 0 || cnt > c.R || hd < 0 || hd >= c.R || row < 0 || row >= c.n_rows;
+      if (bad && cta == 0 && u - s * Hkv == 0) raise_error(a.err, ERR_INDEX);
+      n = (bad || cnt == 0) ? 0 : c.R;
     }
     NK[u] = n;
     PT[u + 1] = (n + KT - 1) / KT;
@@ -291,6 +302,20 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
     const int t0 = ((g0 + k) - PT[u]) * KT + lane * 16;
     const int valid = min(16, NK[u] - t0);
     if (valid <= 0) return;
+    if (!c.paged) {
+      // slots t0 .. t0 + 15 of the ring; slot x is valid when it is one of
+      // the `count` slots before `head`
+      const int cnt = c.ring_count[s], hd = c.ring_head[s];
+      const int rrow = c.stream_rows ? c.stream_rows[s] : s;
+      uint32_t m = 0;
+      for (int b = 0; b < valid; ++b) {
+        const int age = ((t0 + b - hd + cnt) % c.R + c.R) % c.R;  // 0 = the oldest valid slot
+        if (age < cnt) m |= 1u << b;
+      }
+      row = (rrow * Hkv + j) * c.R + t0;
+      mask = static_cast<int>(m);
+      return;
+    }
     int pg = c.block_table[static_cast<int64_t>(s) * c.bt_stride + t0 / c.P];
     if (pg < 0 || pg >= c.n_rows) {
       raise_error(a.err, ERR_INDEX);
@@ -518,6 +543,10 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
     load_qhi(u_first);
     int u = u_first, seg = -1;
     float m_ref = -INFINITY, l = 0.f;  // l: this half's share of the row sum
+    // Ring layers: a row at depth d sees the newest min(count, R - d) entries,
+    // what its path's d entries leave of the ring: `drop` of its oldest valid
+    // slots (those at age < drop from `oldest`) are masked for this row.
+    int drop = 0, oldest = 0;
     uint8_t* pbase = smem + L.p_off + kh * L.rb;  // P's key region of this half
     for (int k = 0; k < nt; ++k) {
       const int un = unit_at(k, u);
@@ -528,6 +557,19 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
         ++seg;
         m_ref = -INFINITY;
         l = 0.f;
+        if (!c.paged && t < R) {
+          const int s = u / Hkv, i = t / G;
+          int depth = 0, node = i;
+          for (int steps = 0; steps < T; ++steps) {
+            const int p = a.parent[s * T + node];
+            if (p < 0 || p >= node) break;  // (a bad parent is reported by the prologue)
+            ++depth;
+            node = p;
+          }
+          const int cnt = c.ring_count[s];
+          drop = max(0, cnt - c.R + depth);
+          oldest = ((c.ring_head[s] - cnt) % c.R + c.R) % c.R;
+        }
       }
       if (!__all_sync(0xffffffffu, W.wait(B_SFULL, k & 1))) break;
       tc::fence_after();
@@ -549,6 +591,15 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
       const uint32_t km0 = t < R ? static_cast<uint32_t>(TMASK[e]) | (static_cast<uint32_t>(TMASK[e + 1]) << 16) : 0u;
       const uint32_t km1 = t < R ? static_cast<uint32_t>(TMASK[e + 2]) | (static_cast<uint32_t>(TMASK[e + 3]) << 16) : 0u;
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (drop > 0) {
+        // the masked slots are [oldest, oldest + drop) cyclically: as sv
+        // indices [lo, hi), and [0, hi2) for the part that wraps to slot 0
+        const int key0 = ((g0 + k) - PT[u]) * KT + 64 * kh;  // ring slot of sv[0]
+        const int lo = oldest - key0, hi = lo + drop, hi2 = hi - c.R;
+#pragma unroll
+        for (int x = 0; x < 64; ++x)
+          if ((x >= lo && x < hi) || x < hi2) sv[x] = -INFINITY;
+      }
 #pragma unroll
       for (int x = 0; x < 64; ++x) {
         if (!(((x < 32 ? km0 : km1) >> (x & 31)) & 1u)) sv[x] = -INFINITY;
@@ -691,11 +742,11 @@ __global__ void __launch_bounds__(256) verify_combine_kernel(const VerifyCombine
   }
   float sig = 1.f;
   if (a.gate) sig = 1.f / (1.f + expf(-bf16_to_f32(a.gate[tok * Hq + h])));
-  int n = c.seq_len[s];
-  const int cap = min(a.max_len, c.bt_stride * c.P);
-  n = n < 0 ? 0 : (n > cap ? cap : n);
   int64_t wb_off = -1;
-  if (a.write_back && g == 0) {
+  if (a.write_back && c.paged && g == 0) {  // (ring layers commit the accepted path instead)
+    int n = c.seq_len[s];
+    const int cap = min(a.max_len, c.bt_stride * c.P);
+    n = n < 0 ? 0 : (n > cap ? cap : n);
     const int idx = n + i;
     const int pi = idx / c.P;
     const int pg = pi < c.bt_stride ? c.block_table[static_cast<int64_t>(s) * c.bt_stride + pi] : -1;

@@ -148,10 +148,16 @@ typedef struct {
                             the new token's slot after every read of the cache   */
 } dattn_decode_args;
 
-/* One verify round: S streams x T rows. Row i of stream s sits at position
- * seq_len[s] + depth(i); it attends to the stream's whole paged prefix
- * (seq_len[s] tokens), to its ancestors in the tree and to itself, each
- * window key rotated at its own position. */
+/* One verify round: S streams x T rows ("TensorFold PR #608": verify windows
+ * under tree masks). Row i of stream s sits at position pos[s] + depth(i)
+ * (depth 0 for a root); it attends to its ancestors in the tree, to itself -
+ * each window key rotated at its own position - and to the stream's cache:
+ *   paged layer: the whole prefix of seq_len[s] tokens;
+ *   ring layer : the newest min(ring_count[s], R - depth(i)) entries of its
+ *                ring, what the ring holds once the row's ancestors have been
+ *                appended (a verify row equals the plain decode of its path).
+ * Ring layers are never written by verify: dattn_commit writes the accepted
+ * path. */
 typedef struct {
   int num_streams;       /* S                                                     */
   int rows;              /* T, 1 <= T <= max_verify_rows                          */
@@ -162,8 +168,11 @@ typedef struct {
   const void* gate;      /* [S, T, Hq] bf16 or NULL                               */
   float* out;            /* [S, T, Hq, D] fp32                                    */
   int max_prefix_len;    /* host bound on seq_len[s] (0 = max_context)            */
-  int write_back;        /* nonzero: window entry i goes to token index
-                            seq_len[s] + i (node order)                           */
+  int write_back;        /* paged layers: nonzero writes window entry i to token
+                            index seq_len[s] + i (node order). Ring layers: must
+                            be 0 (DATTN_EINVAL otherwise)                         */
+  const int32_t* pos;    /* [S] position of the window's root, or NULL for
+                            seq_len[s] (paged layers only: ring layers need it)   */
 } dattn_verify_args;
 
 /* Create a handle on `device`: validates the config, uploads per-layer RoPE
@@ -198,9 +207,29 @@ DATTN_API int dattn_append_kv(dattn_t* h, int layer, const dattn_cache* cache, i
 DATTN_API int dattn_decode(dattn_t* h, int layer, const dattn_cache* cache, const dattn_decode_args* args,
                  dattn_stream_t stream);
 
-/* Tree verify for one paged layer (see dattn_verify_args). */
+/* Tree verify for one layer, ring or paged (see dattn_verify_args). Three
+ * launches. Shape limits: G * T <= 128 query rows per KV head and
+ * num_streams * Hkv <= 512 (checked at dattn_create: DATTN_EUNSUPPORTED); a
+ * paged layer's page size is a multiple of 16. */
 DATTN_API int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, const dattn_verify_args* args,
                  dattn_stream_t stream);
+
+/* Commit of a verify round ("TensorFold PR #608": a round commits only each
+ * stream's accepted path). accepted [S, T] lists stream s's accepted nodes
+ * root first, num_accepted[s] (0..T) of them; they must form a path from a
+ * root (accepted[0] has parent -1, each next node is a child of the one
+ * before). Node accepted[s][d] is written at cache index start + d - ring:
+ * slot (ring_head[s] + d) mod R of ring row stream_rows[s]; paged: token index
+ * seq_len[s] + d - with its key normalised (QK-norm) and rotated at
+ * pos[s] + d: the same bf16 entry that verify scored for that node and that
+ * a decode of the path would write. k, v, parent: the verify call's window
+ * inputs [S, T, Hkv, D] and [S, T]; pos [S]: the root positions. A stream
+ * whose list is not such a path writes nothing and is reported as
+ * DATTN_EINDEX (dattn_get_error). The caller then advances ring head/count
+ * or seq_len by num_accepted[s]. One launch. */
+DATTN_API int dattn_commit(dattn_t* h, int layer, const dattn_cache* cache, int num_streams, int rows,
+                           const void* k, const void* v, const int32_t* parent, const int32_t* accepted,
+                           const int32_t* num_accepted, const int32_t* pos, dattn_stream_t stream);
 
 /* Synchronize `stream`, then return and clear the sticky device error word:
  * DATTN_OK, DATTN_ETIMEOUT, DATTN_EINDEX, DATTN_ERANGE or DATTN_ELENGTH (the
