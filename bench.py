@@ -41,9 +41,10 @@ CONTEXT = 4096
 HQ, HKV, D = 8, 2, 256
 SEED = 1
 FALLBACK_HBM_GBS = 6800.0
-# Steps that move less than this are timed with L2 flushed before each step
-# (a 256 MiB write, untimed); larger ones stream far more than the 129 MB L2.
-L2_SAFE_BYTES = 1 << 30
+# Steps that move less than twice the 129 MB L2 are timed one at a time with
+# L2 flushed before each (a 256 MiB write, untimed); larger ones stream more
+# than twice the L2 per step and run back to back.
+L2_SAFE_BYTES = 2 * 129 * 10**6
 
 
 # ---------------------------------------------------------------- accounting
@@ -444,12 +445,78 @@ class VerifyCall(Workload):
         return [d], "1 of 16 streams (16 rows)"
 
 
+class VerifyRingCall(Workload):
+    """One speculative round on a sliding layer per step: tree verify of 16
+    streams x 16 rows over full rings, then the commit of each stream's
+    accepted path."""
+    launches_per_call = 4
+
+    def __init__(self, seed, device="cuda"):
+        import decode_attention_kv_dattn_gb300 as dattn
+        import synth
+        g = torch.Generator(device=device)
+        g.manual_seed(seed)
+        hg = synth.generator(seed)
+        S, T, Hq, Hkv, Dh, R = 16, 16, 8, 2, 256, 511
+        rnd = lambda *sh: torch.randn(*sh, generator=g, device=device).to(torch.bfloat16)
+        k, v = rnd(S, Hkv, R, Dh), rnd(S, Hkv, R, Dh)
+        head = torch.from_numpy(synth.randint(0, R - 1, S, hg)).to(device)
+        count = torch.full((S,), R, dtype=torch.int32, device=device)
+        parent = np.stack([synth.tree_parents(hg, T) for _ in range(S)])
+        # each stream accepts the path to a random node
+        acc = np.full((S, T), -1, np.int32)
+        num = np.zeros(S, np.int32)
+        for s in range(S):
+            node, path = int(synth.randint(0, T - 1, 1, hg)[0]), []
+            while node >= 0:
+                path.append(node)
+                node = int(parent[s, node])
+            acc[s, :len(path)] = path[::-1]
+            num[s] = len(path)
+        self.lens = [R] * S
+        self._keep = (k, v, head, count)
+        self.desc = dattn.ring_cache(k, v, head, count)
+        layer = {"kind": dattn.CACHE_RING, "ring_slots": R, "rotary_dim": 256, "rope_theta": 1e4}
+        self.h = dattn.Handle(Hq, Hkv, Dh, [layer], S, max_verify_rows=T)
+        self.q, self.k, self.v = self.pack_inputs([rnd(S, T, Hq, Dh), rnd(S, T, Hkv, Dh), rnd(S, T, Hkv, Dh)], device)
+        self.parent = torch.from_numpy(parent).to(device)
+        self.acc, self.num = torch.from_numpy(acc).to(device), torch.from_numpy(num).to(device)
+        self.pos = torch.from_numpy((synth.randint(0, 100000, S, hg) + R).astype(np.int32)).to(device)
+        self.out = torch.empty((S, T, Hq, Dh), dtype=torch.float32, device=device)
+        self.ncalls, self.graph = 1, None
+        kv = S * R * 2 * Hkv * Dh * 2
+        io = S * T * ((Hq + 2 * Hkv) * Dh * 2 + 4 + Hq * Dh * 4) + int(num.sum()) * 2 * Hkv * Dh * 2 + S * 16
+        self.bytes_step, self.tokens_step = kv + io, S * (R + T)
+        self.flush_l2 = True
+        self.dominant, self.others, self.dominant_kv_bytes = [0], [], kv
+        self.S, self.T, self.Hq, self.Hkv, self.D, self.R = S, T, Hq, Hkv, Dh, R
+        self.config = {"workload": "sliding-layer verify round: 16 streams x 16 rows (random best-first trees, "
+                                   "depth <= 7) over full rings of 511 slots, 8 q / 2 KV heads, head_dim 256, "
+                                   "RoPE 256 dims theta 1e4, then the commit of each stream's accepted path",
+                       "streams": S, "rows": T, "context": R}
+        self.kernel = "verify_split (tcgen05, ring layer, 64 rows per KV head) + combine + commit"
+
+    def run_call(self, i, stream=None):
+        self.h.verify(0, self.desc, self.q, self.k, self.v, self.parent, self.out, write_back=False,
+                      pos=self.pos, stream=stream)
+        self.h.commit(0, self.desc, self.k, self.v, self.parent, self.acc, self.num, self.pos, stream=stream)
+
+    def oracle_sample(self):
+        u16 = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+        d = {"kind": "verify_ring", "rope": _Rope(256, 1e4), "q": u16(self.q[:1]), "k_new": u16(self.k[:1]),
+             "v_new": u16(self.v[:1]), "parent": self.parent[:1].cpu().numpy(), "k": u16(self._keep[0][:1]),
+             "v": u16(self._keep[1][:1]), "head": self._keep[2][:1].cpu().numpy(),
+             "count": self._keep[3][:1].cpu().numpy(), "pos": self.pos[:1].cpu().numpy(), "Hq": self.Hq,
+             "Hkv": self.Hkv, "D": self.D, "P": 16, "T": self.T}
+        return [d], "1 of 16 streams (16 rows, verify only)"
+
+
 class _Rope:
     def __init__(self, rotary_dim, theta):
         self.rotary_dim, self.theta = rotary_dim, theta
 
 
-WORKLOADS = ("hybrid", "sliding", "paged", "verify", "long1m", "long262k")
+WORKLOADS = ("hybrid", "sliding", "paged", "verify", "verify_sliding", "long1m", "long262k")
 
 
 def make_workload(name, seed, args):
@@ -457,6 +524,8 @@ def make_workload(name, seed, args):
         return Step(args.streams, args.context, seed)
     if name == "verify":
         return VerifyCall(seed)
+    if name == "verify_sliding":
+        return VerifyRingCall(seed)
     return DecodeCall(name, seed)
 
 
@@ -500,6 +569,7 @@ SURVEY = [
     ("sliding", lambda: DecodeCall("sliding", SEED)),
     ("paged", lambda: DecodeCall("paged", SEED)),
     ("verify", lambda: VerifyCall(SEED)),
+    ("verify_sliding", lambda: VerifyRingCall(SEED)),
     ("long1m", lambda: DecodeCall("long1m", SEED)),
     ("long262k", lambda: DecodeCall("long262k", SEED)),
     ("long128k_b1", lambda: DecodeCall("long128k_b1", SEED)),
@@ -667,6 +737,9 @@ def oracle_pass(o, sample):
         elif d["kind"] == "full":
             o.decode_paged(d["k"], d["v"], d["block_table"], d["seq_len"], d["q"], d["k_new"],
                            d["v_new"], d["pos"], r, th, gate=d["gate"])
+        elif d["kind"] == "verify_ring":
+            o.verify_ring(d["k"], d["v"], d["head"], d["count"], d["pos"], d["q"], d["k_new"], d["v_new"],
+                          d["parent"], r, th)
         else:
             o.verify(d["k"], d["v"], d["block_table"], d["seq_len"], d["q"], d["k_new"], d["v_new"],
                      d["parent"], r, th)
@@ -676,9 +749,9 @@ def sample_bytes_tokens(sample):
     by = tok = 0
     for d in sample:
         Hq, Hkv, Dh, P = d["Hq"], d["Hkv"], d["D"], d["P"]
-        if d["kind"] == "verify":
+        if d["kind"] in ("verify", "verify_ring"):
             T = d["T"]
-            for n in d["seq_len"]:
+            for n in (d["count"] if d["kind"] == "verify_ring" else d["seq_len"]):
                 n = int(n)
                 by += n * 2 * Hkv * Dh * 2 + T * ((Hq + 2 * Hkv) * Dh * 2 + 4 + Hq * Dh * 4 + 2 * Hkv * Dh * 2)
                 tok += n + T

@@ -82,11 +82,16 @@ class Oracle:
                                          _P, _P, _P, _I, _P, _D]
         L.oracle_append_paged.argtypes = [_I, _I, _I, _I, _I, _D, _P, _P, _I, _I, _P, _I, _P,
                                           _P, _P, _P, _P, _I, _P, _D]
+        L.oracle_prefill_ring.argtypes = [_I, _I, _I, _I, _I, _I, _D, _P, _P, _I, _I, _P, _P, _P, _P, _P,
+                                          _P, _P, _P, _P, _P] + N3
+        L.oracle_prefill_paged.argtypes = [_I, _I, _I, _I, _I, _I, _D, _P, _P, _I, _I, _P, _I, _P, _P, _P,
+                                           _P, _P, _P, _P, _P] + N3
         L.oracle_qk_norm.argtypes = [_P, _P, _I, _D, _P]
         L.oracle_qk_norm.restype = None
         for f in ("oracle_rope_f64", "oracle_rope_bf16", "oracle_decode_ring",
                   "oracle_decode_paged", "oracle_decode_concat", "oracle_verify",
                   "oracle_verify_ring", "oracle_commit_ring", "oracle_commit_paged",
+                  "oracle_prefill_ring", "oracle_prefill_paged",
                   "oracle_append_ring", "oracle_append_paged", "oracle_hardware_threads"):
             getattr(L, f).restype = _I
 
@@ -252,6 +257,38 @@ class Oracle:
         if rc not in (0, 3):
             self._check(rc, "commit_paged")
         return kp, vp, rc
+
+    # ---- ragged prefill (returns out and updated copies of the pools)
+    def prefill_ring(self, k_ring, v_ring, ring_head, ring_count, count, start_pos, q, k, v, r, theta,
+                     gate=None, stream_rows=None, qk_norm=None):
+        kr, vr = _u16(k_ring).copy(), _u16(v_ring).copy()
+        q, k, v = _u16(q), _u16(k), _u16(v)
+        gate = None if gate is None else _u16(gate)
+        n_rows, Hkv, R, D = kr.shape
+        S, Tmax, Hq, _ = q.shape
+        out = np.full((S, Tmax, Hq, D), np.nan)
+        rc = self.lib.oracle_prefill_ring(S, Tmax, Hq, Hkv, D, r, theta, _ptr(kr), _ptr(vr), n_rows, R,
+                                          _ptr(_i32(stream_rows)), _ptr(_i32(ring_head)), _ptr(_i32(ring_count)),
+                                          _ptr(_i32(count)), _ptr(_i32(start_pos)), _ptr(q), _ptr(k), _ptr(v),
+                                          _ptr(gate), _ptr(out), *_norm(qk_norm))
+        self._check(rc, "prefill_ring")
+        return out, kr, vr
+
+    def prefill_paged(self, k_pages, v_pages, block_table, seq_len, count, start_pos, q, k, v, r, theta,
+                      gate=None, qk_norm=None):
+        kp, vp = _u16(k_pages).copy(), _u16(v_pages).copy()
+        q, k, v = _u16(q), _u16(k), _u16(v)
+        gate = None if gate is None else _u16(gate)
+        num_pages, Hkv, P, D = kp.shape
+        S, Tmax, Hq, _ = q.shape
+        bt = _i32(block_table)
+        out = np.full((S, Tmax, Hq, D), np.nan)
+        rc = self.lib.oracle_prefill_paged(S, Tmax, Hq, Hkv, D, r, theta, _ptr(kp), _ptr(vp), num_pages, P,
+                                           _ptr(bt), bt.shape[1], _ptr(_i32(seq_len)), _ptr(_i32(count)),
+                                           _ptr(_i32(start_pos)), _ptr(q), _ptr(k), _ptr(v), _ptr(gate),
+                                           _ptr(out), *_norm(qk_norm))
+        self._check(rc, "prefill_paged")
+        return out, kp, vp
 
     # ---- append (returns updated copies)
     def append_ring(self, k_ring, v_ring, start_index, start_pos, count, k, v, r, theta,

@@ -913,6 +913,81 @@ int oracle_commit_paged(int S, int T, int Hkv, int D, int r, double theta, uint1
   return rc != 0 ? rc : (ok ? 0 : 3);
 }
 
+// ----- ragged prefill: stream s brings count[s] new tokens (q [S, Tmax, Hq, D],
+// k, v [S, Tmax, Hkv, D], gate [S, Tmax, Hq] or null), token t at position
+// start_pos[s] + t. Read as the plain definition: the tokens are decoded one
+// after another, each one joined to the cache in score space and its entry
+// written back before the next (ring: slot head + t, the ring keeping its
+// newest R entries; paged: token index seq_len[s] + t), so token t attends to
+// the cache and to new tokens 0..t. out [S, Tmax, Hq, D] gets rows t <
+// count[s]; the caches are updated in place.
+int oracle_prefill_ring(int S, int Tmax, int Hq, int Hkv, int D, int r, double theta, uint16_t* k_ring,
+                        uint16_t* v_ring, int n_rows, int R, const int32_t* stream_rows, const int32_t* ring_head,
+                        const int32_t* ring_count, const int32_t* count, const int32_t* start_pos,
+                        const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* gate, double* out,
+                        const uint16_t* q_norm, const uint16_t* k_norm, double norm_eps) {
+  for (int s = 0; s < S; ++s)
+    if (count[s] < 0 || count[s] > Tmax) return 2;
+  const size_t qrow = static_cast<size_t>(Hq) * D, kvrow = static_cast<size_t>(Hkv) * D;
+  std::vector<uint16_t> ke(kvrow), ve(kvrow);
+  for (int s = 0; s < S; ++s) {
+    const int row = stream_rows ? stream_rows[s] : s;
+    int head = ring_head[s], cnt = ring_count[s];
+    for (int t = 0; t < count[s]; ++t) {
+      const size_t tok = static_cast<size_t>(s) * Tmax + t;
+#if ORACLE_MUTATION == 23
+      const int32_t pos = start_pos[s] + t + 1;  // planted: positions shifted by one
+#else
+      const int32_t pos = start_pos[s] + t;
+#endif
+      const int rc = oracle_decode_ring(1, Hq, Hkv, D, r, theta, k_ring, v_ring, n_rows, R, &row, &head, &cnt,
+                                        q + tok * qrow, k + tok * kvrow, v + tok * kvrow,
+                                        gate ? gate + tok * Hq : nullptr, &pos, out + tok * qrow, ke.data(),
+                                        ve.data(), 1, q_norm, k_norm, norm_eps);
+      if (rc != 0) return rc;
+      for (int j = 0; j < Hkv; ++j) {
+        const size_t dst = ((static_cast<size_t>(row) * Hkv + j) * R + head) * D;
+        std::memcpy(k_ring + dst, ke.data() + static_cast<size_t>(j) * D, D * 2);
+        std::memcpy(v_ring + dst, ve.data() + static_cast<size_t>(j) * D, D * 2);
+      }
+      head = (head + 1) % R;
+      cnt = std::min(cnt + 1, R);
+    }
+  }
+  return 0;
+}
+
+int oracle_prefill_paged(int S, int Tmax, int Hq, int Hkv, int D, int r, double theta, uint16_t* k_pages,
+                         uint16_t* v_pages, int num_pages, int P, const int32_t* block_table, int bt_stride,
+                         const int32_t* seq_len, const int32_t* count, const int32_t* start_pos,
+                         const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* gate,
+                         double* out, const uint16_t* q_norm, const uint16_t* k_norm, double norm_eps) {
+  for (int s = 0; s < S; ++s)
+    if (count[s] < 0 || count[s] > Tmax) return 2;
+  const size_t qrow = static_cast<size_t>(Hq) * D, kvrow = static_cast<size_t>(Hkv) * D;
+  std::vector<uint16_t> ke(kvrow), ve(kvrow);
+  for (int s = 0; s < S; ++s) {
+    const int32_t* bt = block_table + static_cast<size_t>(s) * bt_stride;
+    for (int t = 0; t < count[s]; ++t) {
+      const size_t tok = static_cast<size_t>(s) * Tmax + t;
+      const int32_t pos = start_pos[s] + t, n = seq_len[s] + t;
+      const int idx = n / P;
+      if (idx >= bt_stride || bt[idx] < 0 || bt[idx] >= num_pages) return 2;
+      const int rc = oracle_decode_paged(1, Hq, Hkv, D, r, theta, k_pages, v_pages, num_pages, P, bt, bt_stride,
+                                         &n, q + tok * qrow, k + tok * kvrow, v + tok * kvrow,
+                                         gate ? gate + tok * Hq : nullptr, &pos, out + tok * qrow, ke.data(),
+                                         ve.data(), 1, q_norm, k_norm, norm_eps);
+      if (rc != 0) return rc;
+      for (int j = 0; j < Hkv; ++j) {
+        const size_t dst = ((static_cast<size_t>(bt[idx]) * Hkv + j) * P + n % P) * D;
+        std::memcpy(k_pages + dst, ke.data() + static_cast<size_t>(j) * D, D * 2);
+        std::memcpy(v_pages + dst, ve.data() + static_cast<size_t>(j) * D, D * 2);
+      }
+    }
+  }
+  return 0;
+}
+
 int oracle_hardware_threads(void) {
   return static_cast<int>(std::thread::hardware_concurrency());
 }

@@ -806,6 +806,84 @@ def pin_commit_equals_serial_decode_write_backs(o):
     assert rc == 3 and np.array_equal(Kc, Kr) and np.array_equal(Vc, Vr), "broken path"
 
 
+def pin_prefill_one_token_is_decode_with_write_back(o):
+    """A prefill of one token is one decode step that writes its entry back."""
+    Hq, Hkv, D, R = 4, 2, 16, 6
+    Kr = rand_bf16((2, Hkv, R, D), 1801)
+    Vr = rand_bf16((2, Hkv, R, D), 1802)
+    q = rand_bf16((1, 1, Hq, D), 1803)
+    k = rand_bf16((1, 1, Hkv, D), 1804)
+    v = rand_bf16((1, 1, Hkv, D), 1805)
+    out, Kp, Vp = o.prefill_ring(Kr, Vr, [4], [5], [1], [77], q, k, v, 16, 1e4, stream_rows=[1])
+    dec, ke, ve = o.decode_ring(Kr, Vr, [4], [5], q[0], k[0], v[0], [77], 16, 1e4, stream_rows=[1])
+    close(out[0, 0], dec[0], 0.0, "one token")
+    Kd, Vd = Kr.copy(), Vr.copy()
+    Kd[1, :, 4], Vd[1, :, 4] = ke[0], ve[0]
+    assert np.array_equal(Kp, Kd) and np.array_equal(Vp, Vd), "its entry written at the head"
+
+
+def pin_prefill_in_two_parts_equals_one(o):
+    """Prefilling tokens [0, a) and then [a, n) - the second call starting
+    where the first one left the cache - equals prefilling [0, n): outputs and
+    caches, ring (the ring wraps and drops its oldest entries) and paged."""
+    S, Hq, Hkv, D, R, P, n = 2, 4, 2, 16, 7, 4, 9
+    q = rand_bf16((S, n, Hq, D), 1901)
+    k = rand_bf16((S, n, Hkv, D), 1902)
+    v = rand_bf16((S, n, Hkv, D), 1903)
+    cnt = np.array([n, 6], np.int32)
+    Kr = rand_bf16((S, Hkv, R, D), 1904)
+    Vr = rand_bf16((S, Hkv, R, D), 1905)
+    head, rc_, pos = np.array([3, 0], np.int32), np.array([R, 2], np.int32), np.array([40, 2], np.int32)
+    out, Kf, Vf = o.prefill_ring(Kr, Vr, head, rc_, cnt, pos, q, k, v, 16, 1e4)
+    a = 4
+    c1 = np.minimum(cnt, a).astype(np.int32)
+    o1, K1, V1 = o.prefill_ring(Kr, Vr, head, rc_, c1, pos, q[:, :a], k[:, :a], v[:, :a], 16, 1e4)
+    o2, K2, V2 = o.prefill_ring(K1, V1, (head + c1) % R, np.minimum(rc_ + c1, R), cnt - c1, pos + c1,
+                                q[:, a:], k[:, a:], v[:, a:], 16, 1e4)
+    for s in range(S):
+        close(out[s, :c1[s]], o1[s, :c1[s]], 0.0, "first part")
+        close(out[s, a:cnt[s]], o2[s, :cnt[s] - a], 0.0, "second part")
+    assert np.array_equal(Kf, K2) and np.array_equal(Vf, V2), "ring after both parts"
+    Kp, Vp, bt = _prefix_pool(S, Hkv, D, P, [5, 0], n + 1, 1906)
+    seq = np.array([5, 0], np.int32)
+    out, Kf, Vf = o.prefill_paged(Kp, Vp, bt, seq, cnt, seq, q, k, v, 16, 5e6)
+    o1, K1, V1 = o.prefill_paged(Kp, Vp, bt, seq, c1, seq, q[:, :a], k[:, :a], v[:, :a], 16, 5e6)
+    o2, K2, V2 = o.prefill_paged(K1, V1, bt, seq + c1, cnt - c1, seq + c1, q[:, a:], k[:, a:], v[:, a:], 16, 5e6)
+    for s in range(S):
+        close(out[s, :c1[s]], o1[s, :c1[s]], 0.0, "first part (paged)")
+        close(out[s, a:cnt[s]], o2[s, :cnt[s] - a], 0.0, "second part (paged)")
+    assert np.array_equal(Kf, K2) and np.array_equal(Vf, V2), "pages after both parts"
+
+
+def pin_prefill_equals_chain_verify_then_commit(o):
+    """Prefill (serial decodes) and tree verify over a chain followed by the
+    commit of the whole chain give the same outputs and caches, on ring and
+    paged layers: two independent routes to the same attention."""
+    S, T, Hq, Hkv, D, R, P = 2, 6, 4, 2, 16, 8, 4
+    q = rand_bf16((S, T, Hq, D), 2001)
+    k = rand_bf16((S, T, Hkv, D), 2002)
+    v = rand_bf16((S, T, Hkv, D), 2003)
+    g = rand_bf16((S, T, Hq), 2004)
+    chain = np.stack([np.arange(-1, T - 1, dtype=np.int32)] * S)
+    acc = np.stack([np.arange(T, dtype=np.int32)] * S)
+    full = np.array([T, T], np.int32)
+    Kr = rand_bf16((S, Hkv, R, D), 2005)
+    Vr = rand_bf16((S, Hkv, R, D), 2006)
+    head, cnt, pos = np.array([5, 1], np.int32), np.array([R, 3], np.int32), np.array([100, 3], np.int32)
+    out, Kf, Vf = o.prefill_ring(Kr, Vr, head, cnt, full, pos, q, k, v, 16, 1e4, gate=g)
+    ver, _ = o.verify_ring(Kr, Vr, head, cnt, pos, q, k, v, chain, 16, 1e4, gate=g)
+    Kc, Vc, rc = o.commit_ring(Kr, Vr, head, pos, k, v, chain, acc, full, 16, 1e4)
+    close(out, ver, 1e-12, "ring: prefill vs chain verify")
+    assert rc == 0 and np.array_equal(Kf, Kc) and np.array_equal(Vf, Vc), "ring: prefill vs commit"
+    Kp, Vp, bt = _prefix_pool(S, Hkv, D, P, [7, 2], T + 1, 2007)
+    seq = np.array([7, 2], np.int32)
+    out, Kf, Vf = o.prefill_paged(Kp, Vp, bt, seq, full, seq, q, k, v, 16, 5e6, gate=g)
+    ver, _ = o.verify(Kp, Vp, bt, seq, q, k, v, chain, 16, 5e6, gate=g)
+    Kc, Vc, rc = o.commit_paged(Kp, Vp, bt, seq, seq, k, v, chain, acc, full, 16, 5e6)
+    close(out, ver, 1e-12, "paged: prefill vs chain verify")
+    assert rc == 0 and np.array_equal(Kf, Kc) and np.array_equal(Vf, Vc), "paged: prefill vs commit"
+
+
 # ------------------------------------------------------------------ QK-norm
 # "pega-omni PR #4", talker kernels: RoPE with QK-norm. Reading (the page
 # gives no formula): y = bf16(w * x / sqrt(mean(x^2) + eps)), per head.
