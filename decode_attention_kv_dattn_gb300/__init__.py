@@ -86,6 +86,8 @@ lib.dattn_verify.argtypes = [_vp, _int, ctypes.POINTER(Cache), ctypes.POINTER(Ve
 lib.dattn_verify.restype = _int
 lib.dattn_commit.argtypes = [_vp, _int, ctypes.POINTER(Cache), _int, _int, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
 lib.dattn_commit.restype = _int
+lib.dattn_prefill.argtypes = [_vp, _int, ctypes.POINTER(Cache), _int, _int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+lib.dattn_prefill.restype = _int
 lib.dattn_get_error.argtypes = [_vp, _vp]
 lib.dattn_get_error.restype = _int
 lib.dattn_error_string.argtypes = [_int]
@@ -99,7 +101,7 @@ lib.dattn_debug_config.argtypes = [_vp, _int, ctypes.c_uint]
 lib.dattn_debug_config.restype = _int
 DEBUG_WITHHOLD_Q = 1
 
-EXPORTS = ("dattn_create", "dattn_append_kv", "dattn_decode", "dattn_verify", "dattn_commit",
+EXPORTS = ("dattn_create", "dattn_append_kv", "dattn_decode", "dattn_verify", "dattn_commit", "dattn_prefill",
            "dattn_get_error", "dattn_error_string", "dattn_destroy", "dattn_decode_noalloc",
            "dattn_debug_config")
 
@@ -232,6 +234,13 @@ class Handle:
         _check(lib.dattn_commit(self._h, layer, ctypes.byref(cache), k.shape[0], k.shape[1], _ptr(k),
                                 _ptr(v), _ptr(parent), _ptr(accepted), _ptr(num_accepted), _ptr(pos),
                                 _stream_ptr(stream)), "dattn_commit")
+
+    def prefill(self, layer, cache: Cache, q, k, v, count, start_pos, out, gate=None, stream=None):
+        """Ragged prefill: q [S, T, Hq, D], k/v [S, T, Hkv, D] bf16, count/start_pos [S] int32,
+        out [S, T, Hq, D] fp32 (rows t < count written), gate [S, T, Hq] bf16 or None."""
+        _check(lib.dattn_prefill(self._h, layer, ctypes.byref(cache), q.shape[0], q.shape[1], _ptr(q), _ptr(k),
+                                 _ptr(v), _ptr(gate), _ptr(count), _ptr(start_pos), _ptr(out),
+                                 _stream_ptr(stream)), "dattn_prefill")
 
     def debug_config(self, flags=0, wait_limit_us=0):
         """Testing aid: the limit of the device's bounded waits and fault

@@ -66,6 +66,8 @@ struct dattn_handle {
   int* tiles = nullptr;     // verify: tile prefix over units, from its split pass
   uint16_t* khat = nullptr; // verify: rotated window keys
   float* vpart = nullptr;   // verify partials: [sms + units][G*T][D+4]
+  int32_t* chain = nullptr;    // prefill: chain-tree parents of a chunk, [S][Tc]
+  int32_t* pmeta = nullptr;    // prefill chunk state: 5 arrays of [max_streams]
   size_t vpart_slots = 0;
   int* err = nullptr;
   uint64_t wait_ns = kDefaultWaitNs;  // limit of the kernels' bounded waits
@@ -134,6 +136,99 @@ int check_cache(const dattn_layer_config& L, const dattn_cache* c) {
     if (!c->block_table || !c->seq_len || c->bt_stride <= 0) return DATTN_EINVAL;
   }
   return DATTN_OK;
+}
+
+// One pass of the verify pipeline (three launches): the RoPE prologue, the
+// tensor-core pass over the cache and the tree-window join. Shared by
+// dattn_verify and by the chunks of dattn_prefill.
+struct VerifyRound {
+  CacheView c;
+  int S, T, n_max;
+  const uint16_t *q, *k, *v, *gate;
+  const int32_t* parent;
+  const int32_t* pos;          // [S] root positions
+  float* out;
+  int write_back;
+  int in_T, row0;              // caller rows: s * in_T + row0 + i
+  const int32_t* rows_valid;   // or null
+  bool after_plain_launch;     // the launch before wrote what the prologue reads early
+};
+
+int verify_round(dattn_t* h, int layer, const VerifyRound& r, cudaStream_t s) {
+  const dattn_layer_config& L = h->layers[layer];
+  VerifySplitArgs va{};
+  va.c = r.c;
+  // one CTA per SM, at least one tile each for the largest prefix this call may have
+  const int64_t tiles = static_cast<int64_t>(r.S) * h->Hkv * ((r.n_max + kVerifyTileKeys - 1) / kVerifyTileKeys);
+  int64_t ctas = tiles;
+  if (ctas > h->num_sms) ctas = h->num_sms;
+  if (ctas < 1) ctas = 1;
+  va.S = r.S;
+  va.T = r.T;
+  va.Hkv = h->Hkv;
+  va.G = h->G;
+  va.parent = r.parent;
+  va.qhl = h->qhl;
+  va.ctas = static_cast<int>(ctas);
+  va.max_len = r.n_max;
+  if (encode_verify_maps(va.c, h->Hkv, h->D, h->qhl, h->qhl_rows, h->Hq, h->G, r.S, r.T, &va.tmap_k, &va.tmap_v,
+                         &va.tmap_q) != cudaSuccess)
+    return DATTN_EUNSUPPORTED;
+
+  RopeArgs ra{};
+  ra.rows = r.S * r.T;
+  ra.Hq = h->Hq;
+  ra.Hkv = h->Hkv;
+  ra.D = h->D;
+  ra.r = L.rotary_dim;
+  ra.q = r.q;
+  ra.k = r.k;
+  ra.prefix_len = r.pos;
+  ra.parent = r.parent;
+  ra.T = r.T;
+  ra.rope_step = h->rope_step[layer];
+  ra.q_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(h->D)));
+  ra.qhat = h->qhat;
+  ra.qhl = h->qhl;
+  ra.qhl_rows = h->qhl_rows;
+  ra.khat = h->khat;
+  ra.err = h->err;
+  ra.q_norm = h->q_norm[layer];
+  ra.k_norm = h->k_norm[layer];
+  ra.norm_eps = L.norm_eps;
+  ra.in_T = r.in_T;
+  ra.row0 = r.row0;
+  int rc = cuda_status(launch_rope(ra, s, !r.after_plain_launch), "verify prologue");
+  if (rc != DATTN_OK) return rc;
+
+  va.part = h->vpart;
+  va.tiles = h->tiles;
+  va.err = h->err;
+  rc = cuda_status(launch_verify_split(va, h->D, s), "verify pass");
+  if (rc != DATTN_OK) return rc;
+
+  VerifyCombineArgs vc{};
+  vc.c = va.c;
+  vc.S = r.S;
+  vc.T = r.T;
+  vc.Hkv = h->Hkv;
+  vc.G = h->G;
+  vc.split_ctas = va.ctas;
+  vc.tiles = h->tiles;
+  vc.max_len = r.n_max;
+  vc.qhat = h->qhat;
+  vc.khat = h->khat;
+  vc.v = r.v;
+  vc.parent = r.parent;
+  vc.gate = r.gate;
+  vc.part = h->vpart;
+  vc.out = r.out;
+  vc.write_back = r.write_back;
+  vc.err = h->err;
+  vc.in_T = r.in_T;
+  vc.row0 = r.row0;
+  vc.rows_valid = r.rows_valid;
+  return cuda_status(launch_verify_combine(vc, h->D, s), "verify combine");
 }
 
 }  // namespace
@@ -264,6 +359,12 @@ int dattn_create(const dattn_config* cfg, int device, dattn_t** out) {
     h->vpart_slots = static_cast<size_t>(h->num_sms) + static_cast<size_t>(h->max_streams) * Hkv;
     const size_t vfloats = h->vpart_slots * G * h->max_verify_rows * (D + 4);
     if (cudaMalloc(&h->vpart, vfloats * sizeof(float)) != cudaSuccess) return fail(DATTN_ECUDA);
+    // prefill: chain trees (written per chunk: parent of row i is i - 1) and
+    // the chunk state
+    const size_t nchain = static_cast<size_t>(h->max_streams) * h->max_verify_rows;
+    if (cudaMalloc(&h->chain, nchain * sizeof(int32_t)) != cudaSuccess) return fail(DATTN_ECUDA);
+    if (cudaMalloc(&h->pmeta, 5 * static_cast<size_t>(h->max_streams) * sizeof(int32_t)) != cudaSuccess)
+      return fail(DATTN_ECUDA);
   }
   if (cudaMalloc(&h->err, sizeof(int)) != cudaSuccess) return fail(DATTN_ECUDA);
   if (cudaMemset(h->err, 0, sizeof(int)) != cudaSuccess) return fail(DATTN_ECUDA);
@@ -278,6 +379,8 @@ void dattn_destroy(dattn_t* h) {
   for (uint16_t* p : h->q_norm) cudaFree(p);
   for (uint16_t* p : h->k_norm) cudaFree(p);
   cudaFree(h->qhat);
+  cudaFree(h->chain);
+  cudaFree(h->pmeta);
   cudaFree(h->qhl);
   cudaFree(h->khat);
   for (int i = 0; i < 2; ++i) {
@@ -351,6 +454,7 @@ int dattn_append_kv(dattn_t* h, int layer, const dattn_cache* cache, int num_str
   a.err = h->err;
   a.k_norm = h->k_norm[layer];
   a.norm_eps = L.norm_eps;
+  a.in_T = max_tokens;
   rc = cuda_status(launch_append(a, reinterpret_cast<cudaStream_t>(stream)), "append");
   if (rc == DATTN_OK) record_launch(stream, cache->k);
   return rc;
@@ -390,6 +494,7 @@ int dattn_commit(dattn_t* h, int layer, const dattn_cache* cache, int num_stream
   a.norm_eps = L.norm_eps;
   a.gather = accepted;
   a.parent = parent;
+  a.in_T = rows;
   rc = cuda_status(launch_append(a, reinterpret_cast<cudaStream_t>(stream)), "commit");
   if (rc == DATTN_OK) record_launch(stream, cache->k);
   return rc;
@@ -482,77 +587,125 @@ int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, const dattn_ve
   }
   DeviceGuard guard(h->device);
   if (!guard.ok) return DATTN_ECUDA;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  VerifySplitArgs va{};
-  va.c = make_view(h, L, cache);
-  // one CTA per SM, at least one tile each for the largest prefix this call may have
-  const int64_t tiles = static_cast<int64_t>(S) * h->Hkv * ((n_max + kVerifyTileKeys - 1) / kVerifyTileKeys);
-  int64_t ctas = tiles;
-  if (ctas > h->num_sms) ctas = h->num_sms;
-  if (ctas < 1) ctas = 1;
-  va.S = S;
-  va.T = T;
-  va.Hkv = h->Hkv;
-  va.G = h->G;
-  va.parent = args->parent;
-  va.qhl = h->qhl;
-  va.ctas = static_cast<int>(ctas);
-  va.max_len = n_max;
-  if (encode_verify_maps(va.c, h->Hkv, h->D, h->qhl, h->qhl_rows, h->Hq, h->G, S, T, &va.tmap_k, &va.tmap_v,
-                         &va.tmap_q) != cudaSuccess)
-    return DATTN_EUNSUPPORTED;
-
-  RopeArgs ra{};
-  ra.rows = S * T;
-  ra.Hq = h->Hq;
-  ra.Hkv = h->Hkv;
-  ra.D = h->D;
-  ra.r = L.rotary_dim;
-  ra.q = static_cast<const uint16_t*>(args->q);
-  ra.k = static_cast<const uint16_t*>(args->k);
-  ra.prefix_len = args->pos ? args->pos : cache->seq_len;  // the roots' positions
-  ra.parent = args->parent;
-  ra.T = T;
-  ra.rope_step = h->rope_step[layer];
-  ra.q_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(h->D)));
-  ra.qhat = h->qhat;
-  ra.qhl = h->qhl;
-  ra.qhl_rows = h->qhl_rows;
-  ra.khat = h->khat;
-  ra.err = h->err;
-  ra.q_norm = h->q_norm[layer];
-  ra.k_norm = h->k_norm[layer];
-  ra.norm_eps = L.norm_eps;
-  rc = cuda_status(launch_rope(ra, s), "verify prologue");
-  if (rc != DATTN_OK) return rc;
-
-  va.part = h->vpart;
-  va.tiles = h->tiles;
-  va.err = h->err;
-  rc = cuda_status(launch_verify_split(va, h->D, s), "verify pass");
-  if (rc != DATTN_OK) return rc;
-
-  VerifyCombineArgs vc{};
-  vc.c = va.c;
-  vc.S = S;
-  vc.T = T;
-  vc.Hkv = h->Hkv;
-  vc.G = h->G;
-  vc.split_ctas = va.ctas;
-  vc.tiles = h->tiles;
-  vc.max_len = n_max;
-  vc.qhat = h->qhat;
-  vc.khat = h->khat;
-  vc.v = static_cast<const uint16_t*>(args->v);
-  vc.parent = args->parent;
-  vc.gate = static_cast<const uint16_t*>(args->gate);
-  vc.part = h->vpart;
-  vc.out = args->out;
-  vc.write_back = args->write_back;
-  vc.err = h->err;
-  rc = cuda_status(launch_verify_combine(vc, h->D, s), "verify combine");
+  VerifyRound vr{};
+  vr.c = make_view(h, L, cache);
+  vr.S = S;
+  vr.T = T;
+  vr.n_max = n_max;
+  vr.q = static_cast<const uint16_t*>(args->q);
+  vr.k = static_cast<const uint16_t*>(args->k);
+  vr.v = static_cast<const uint16_t*>(args->v);
+  vr.gate = static_cast<const uint16_t*>(args->gate);
+  vr.parent = args->parent;
+  vr.pos = args->pos ? args->pos : cache->seq_len;  // the roots' positions
+  vr.out = args->out;
+  vr.write_back = args->write_back;
+  vr.in_T = T;
+  rc = verify_round(h, layer, vr, reinterpret_cast<cudaStream_t>(stream));
   if (rc == DATTN_OK) record_launch(stream, args->write_back ? cache->k : nullptr);
   return rc;
+}
+
+int dattn_prefill(dattn_t* h, int layer, const dattn_cache* cache, int num_streams, int max_tokens,
+                  const void* q, const void* k, const void* v, const void* gate, const int32_t* count,
+                  const int32_t* start_pos, float* out, dattn_stream_t stream) {
+  if (!h || layer < 0 || layer >= static_cast<int>(h->layers.size())) return DATTN_EINVAL;
+  const dattn_layer_config& L = h->layers[layer];
+  const bool ring = L.cache_kind == DATTN_CACHE_RING;
+  if (!ring && L.page_size % 16 != 0) return DATTN_EUNSUPPORTED;
+  int rc = check_cache(L, cache);
+  if (rc != DATTN_OK) return rc;
+  const int S = num_streams;
+  if (S <= 0 || max_tokens < 0 || !q || !k || !v || !count || !out) return DATTN_EINVAL;
+  if (L.rotary_dim > 0 && !start_pos) return DATTN_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return DATTN_EINVAL;
+  if (S > h->max_streams || h->max_verify_rows == 0) return DATTN_EXCEEDS;
+  if (max_tokens == 0) return DATTN_OK;
+  // chunk rows: the verify workspace's rows, at most 128 query rows per KV
+  // head, and no more than a ring holds
+  int Tc = std::min(h->max_verify_rows, kVerifyMaxRows / h->G);
+  if (ring) Tc = std::min(Tc, L.ring_slots);
+  const int n_max = ring ? L.ring_slots : h->max_context;
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return DATTN_ECUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const CacheView base = make_view(h, L, cache);
+  int32_t* seq_c = h->pmeta;
+  int32_t* head_c = seq_c + h->max_streams;
+  int32_t* cnt_c = head_c + h->max_streams;
+  int32_t* pos_c = cnt_c + h->max_streams;
+  int32_t* n_c = pos_c + h->max_streams;
+  for (int row0 = 0; row0 < max_tokens; row0 += Tc) {
+    // the cache as this chunk sees it: the caller's plus the earlier chunks'
+    // tokens (the library never changes the caller's metadata)
+    PrefillMetaArgs m{};
+    m.c = base;
+    m.count = count;
+    m.start_pos = start_pos;
+    m.S = S;
+    m.Tmax = max_tokens;
+    m.row0 = row0;
+    m.Tc = Tc;
+    m.seq_c = seq_c;
+    m.head_c = head_c;
+    m.cnt_c = cnt_c;
+    m.pos_c = pos_c;
+    m.n_c = n_c;
+    m.chain = h->chain;
+    m.err = h->err;
+    rc = cuda_status(launch_prefill_meta(m, s), "prefill chunk state");
+    if (rc != DATTN_OK) return rc;
+    CacheView cv = base;
+    if (ring) {
+      cv.ring_head = head_c;
+      cv.ring_count = cnt_c;
+    } else {
+      cv.seq_len = seq_c;
+    }
+    // the chunk's rows as chain trees through the verify pass ...
+    VerifyRound vr{};
+    vr.c = cv;
+    vr.S = S;
+    vr.T = Tc;
+    vr.n_max = n_max;
+    vr.q = static_cast<const uint16_t*>(q);
+    vr.k = static_cast<const uint16_t*>(k);
+    vr.v = static_cast<const uint16_t*>(v);
+    vr.gate = static_cast<const uint16_t*>(gate);
+    vr.parent = h->chain;
+    vr.pos = pos_c;
+    vr.out = out;
+    vr.in_T = max_tokens;
+    vr.row0 = row0;
+    vr.rows_valid = n_c;
+    vr.after_plain_launch = true;
+    rc = verify_round(h, layer, vr, s);
+    if (rc != DATTN_OK) return rc;
+    // ... and their entries into the cache before the next chunk
+    AppendArgs a{};
+    a.c = cv;
+    a.B = S;
+    a.Tmax = Tc;
+    a.Hkv = h->Hkv;
+    a.D = h->D;
+    a.r = L.rotary_dim;
+    a.start_index = ring ? head_c : seq_c;
+    a.start_pos = pos_c;
+    a.count = n_c;
+    a.k = static_cast<const uint16_t*>(k);
+    a.v = static_cast<const uint16_t*>(v);
+    a.rotate = 1;
+    a.rope_step = h->rope_step[layer];
+    a.err = h->err;
+    a.k_norm = h->k_norm[layer];
+    a.norm_eps = L.norm_eps;
+    a.in_T = max_tokens;
+    a.row0 = row0;
+    rc = cuda_status(launch_append(a, s), "prefill commit");
+    if (rc != DATTN_OK) return rc;
+  }
+  record_launch(stream, cache->k);
+  return DATTN_OK;
 }
 
 }  // extern "C"

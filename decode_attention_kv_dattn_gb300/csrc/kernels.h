@@ -68,6 +68,10 @@ struct RopeArgs {
   const uint16_t* q_norm;      // [D] QK-norm weights, or null
   const uint16_t* k_norm;
   double norm_eps;
+  // Row r = s * T + i reads the caller's q/k row s * in_T + row0 + i (a
+  // prefill chunk of a longer array; rows past in_T read as zero). Verify:
+  // in_T = T, row0 = 0.
+  int in_T, row0;
 };
 
 // Query heads of a KV group as the decode kernel lays them out: 4 (G <= 4)
@@ -125,6 +129,9 @@ struct AppendArgs {
   int* err;
   const uint16_t* k_norm;      // [D] QK-norm weights of the keys (with rotate), or null
   double norm_eps;
+  // source rows: b * in_T + row0 + t of k/v (in_T = Tmax, row0 = 0 but for
+  // prefill chunks)
+  int in_T, row0;
   // commit of verify paths: token t of row b is source row gather[b * Tmax + t]
   // of k/v ([B, Tmax, Hkv, D]), and the row's first count[b] entries of gather
   // must form a path from a root under parent [B, Tmax]; null for a plain append
@@ -156,6 +163,24 @@ struct VerifySplitArgs {
   int* err;
 };
 
+// Ragged prefill in chunks of Tc tokens: the cache state a chunk starts from
+// (the caller's plus the min(count, row0) tokens of earlier chunks) and the
+// chunk's token count and root position, per stream, into scratch arrays.
+struct PrefillMetaArgs {
+  CacheView c;                 // the caller's cache metadata
+  const int32_t* count;        // [S] new tokens of each stream (0..Tmax)
+  const int32_t* start_pos;    // [S] position of each stream's token 0
+  int S, Tmax, row0, Tc;
+  int32_t* seq_c;              // paged: seq_len + m
+  int32_t* head_c;             // ring: (head + m) mod R
+  int32_t* cnt_c;              // ring: min(count + m, R)
+  int32_t* pos_c;              // start_pos + row0
+  int32_t* n_c;                // tokens of this chunk: clamp(count - row0, 0, Tc)
+  int32_t* chain;              // [S, Tc] chain-tree parents: i - 1
+  int* err;
+};
+cudaError_t launch_prefill_meta(const PrefillMetaArgs& a, cudaStream_t s);
+
 // Tree-window join: merge the prefix segments of each row, score the row's
 // path in the window (its ancestors and itself), gate, store, write back.
 struct VerifyCombineArgs {
@@ -173,6 +198,10 @@ struct VerifyCombineArgs {
   float* out;                  // [S, T, Hq, D]
   int write_back;
   int* err;
+  // caller rows of v, gate and out: s * in_T + row0 + i (see RopeArgs); with
+  // rows_valid, only rows i < rows_valid[s] are stored (prefill chunks)
+  int in_T, row0;
+  const int32_t* rows_valid;
 };
 
 // Decode grid: every resident CTA (`resident` on the whole GPU), but at
@@ -187,7 +216,7 @@ inline int plan_decode_ctas(int resident, int units, int n_max, int tile_keys) {
 }
 
 // Each returns cudaErrorNotSupported for a shape with no compiled kernel.
-cudaError_t launch_rope(const RopeArgs& a, cudaStream_t s);
+cudaError_t launch_rope(const RopeArgs& a, cudaStream_t s, bool pdl = true);
 // Decode with `ctas` CTAs (at most decode_ctas_per_sm per SM). With pdl the
 // launch is a programmatic dependent of the previous one on the stream;
 // without, it starts once everything before it on the stream has completed.

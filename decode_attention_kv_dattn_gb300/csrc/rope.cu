@@ -51,16 +51,22 @@ __global__ void __launch_bounds__(kRowThreads) rope_kernel(const RopeArgs a) {
   const int heads = a.Hq + a.Hkv;
   const int items = heads * slots;
 
+  // the caller's row of this token (a prefill chunk reads a window of a
+  // longer array; rows past its end read as zero)
+  const int T_ = a.T > 0 ? a.T : 1;
+  const int rs = row / T_, ri = row - rs * T_;
+  const bool src_ok = a.row0 + ri < a.in_T;
+  const int64_t src_row = static_cast<int64_t>(rs) * a.in_T + a.row0 + ri;
   auto head_src = [&](int hh) {
-    return hh < a.Hq ? a.q + (static_cast<int64_t>(row) * a.Hq + hh) * a.D
-                     : a.k + (static_cast<int64_t>(row) * a.Hkv + (hh - a.Hq)) * a.D;
+    return hh < a.Hq ? a.q + (src_row * a.Hq + hh) * a.D
+                     : a.k + (src_row * a.Hkv + (hh - a.Hq)) * a.D;
   };
   auto head_norm = [&](int hh) { return hh < a.Hq ? a.q_norm : a.k_norm; };
   const bool norm = a.q_norm || a.k_norm;
   if (norm) {
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int hh = w; hh < heads; hh += kRowThreads / 32)
-      if (head_norm(hh)) {
+      if (head_norm(hh) && src_ok) {
         const double inv = qk_norm_inv(head_src(hh), a.D, a.norm_eps, lane);
         if (lane == 0) inv_s[hh] = inv;
       }
@@ -73,10 +79,9 @@ __global__ void __launch_bounds__(kRowThreads) rope_kernel(const RopeArgs a) {
   for (int k = 0; k < kMaxItems; ++k) {
     const int it = threadIdx.x + k * kRowThreads;
     xy[k] = 0;
-    if (it < items) {
+    if (it < items && src_ok) {
       const int hh = it / slots, p = it - hh * slots;
-      const uint16_t* src = hh < a.Hq ? a.q + (static_cast<int64_t>(row) * a.Hq + hh) * a.D
-                                      : a.k + (static_cast<int64_t>(row) * a.Hkv + (hh - a.Hq)) * a.D;
+      const uint16_t* src = head_src(hh);
       const int d0 = p < half ? p : a.r + 2 * (p - half);
       const int d1 = p < half ? p + half : d0 + 1;
       uint16_t x = src[d0], y = src[d1];
@@ -192,7 +197,7 @@ __global__ void __launch_bounds__(kRopeThreads) append_kernel(const AppendArgs a
     // the row's accepted nodes must form a path from a root: else nothing of
     // the row is written
     const int32_t* acc = a.gather + static_cast<int64_t>(b) * a.Tmax;
-    const int32_t* par = a.parent + static_cast<int64_t>(b) * a.Tmax;
+    const int32_t* par = a.parent + static_cast<int64_t>(b) * a.in_T;
     for (int d = 0; d < cnt; ++d) {
       const int node = acc[d];
       if (node < 0 || node >= a.Tmax || par[node] != (d == 0 ? -1 : acc[d - 1])) {
@@ -228,7 +233,7 @@ __global__ void __launch_bounds__(kRopeThreads) append_kernel(const AppendArgs a
     dst0 = (static_cast<int64_t>(row) * a.Hkv * c.R + idx % c.R) * a.D;
     head_stride = static_cast<int64_t>(c.R) * a.D;
   }
-  const int64_t src0 = (static_cast<int64_t>(b) * a.Tmax + src_t) * a.Hkv * a.D;
+  const int64_t src0 = (static_cast<int64_t>(b) * a.in_T + a.row0 + src_t) * a.Hkv * a.D;
   // V: plain copy, 16 bytes per thread-step.  (Every return above is taken by
   // the whole CTA.)
   for (int e = threadIdx.x; e < a.Hkv * a.D / 8; e += kRopeThreads) {
@@ -280,12 +285,50 @@ __global__ void __launch_bounds__(kRopeThreads) append_kernel(const AppendArgs a
   }
 }
 
+// The cache state, token count and root position of one prefill chunk, per
+// stream (PrefillMetaArgs). A stream with metadata out of range is reported
+// and gets no tokens.
+__global__ void __launch_bounds__(128) prefill_meta_kernel(const PrefillMetaArgs a) {
+  const CacheView& c = a.c;
+  for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < a.S; s += gridDim.x * blockDim.x) {
+    int cnt = a.count[s];
+    bool bad = cnt < 0 || cnt > a.Tmax;
+    if (!c.paged) {
+      const int hd = c.ring_head[s], rc = c.ring_count[s];
+      bad = bad || hd < 0 || hd >= c.R || rc < 0 || rc > c.R;
+      const int m = bad ? 0 : min(cnt, a.row0);
+      a.head_c[s] = bad ? 0 : (hd + m) % c.R;
+      a.cnt_c[s] = bad ? 0 : min(rc + m, c.R);
+    } else {
+      const int n = c.seq_len[s];
+      bad = bad || n < 0;
+      a.seq_c[s] = bad ? 0 : n + min(cnt, a.row0);
+    }
+    if (bad) {
+      if (a.row0 == 0) raise_error(a.err, ERR_INDEX);
+      cnt = 0;
+    }
+    a.pos_c[s] = a.start_pos ? a.start_pos[s] + a.row0 : 0;
+    a.n_c[s] = max(0, min(cnt - a.row0, a.Tc));
+    for (int i = 0; i < a.Tc; ++i) a.chain[s * a.Tc + i] = i - 1;
+  }
+}
+
 }  // namespace
 
-cudaError_t launch_rope(const RopeArgs& a, cudaStream_t s) {
+cudaError_t launch_prefill_meta(const PrefillMetaArgs& a, cudaStream_t s) {
+  prefill_meta_kernel<<<(a.S + 127) / 128, 128, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope(const RopeArgs& a, cudaStream_t s, bool pdl) {
   if ((a.Hq + a.Hkv) * (a.D / 2) > kRowThreads * kMaxItems || a.Hq + a.Hkv > kMaxHeads || a.r > 256 ||
       (a.parent && a.T > kMaxT))
     return cudaErrorNotSupported;
+  if (!pdl) {  // after a launch whose outputs it reads before its wait
+    rope_kernel<<<a.rows, kRowThreads, 0, s>>>(a);
+    return cudaGetLastError();
+  }
   return launch_pdl(rope_kernel, dim3(a.rows), dim3(kRowThreads), 0, s, a);
 }
 

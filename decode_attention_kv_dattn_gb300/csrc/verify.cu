@@ -719,7 +719,10 @@ __global__ void __launch_bounds__(256) verify_combine_kernel(const VerifyCombine
   const int i = blockIdx.x, j = blockIdx.y, s = blockIdx.z;
   const int g = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.G, T = a.T, Hkv = a.Hkv, Hq = Hkv * G, R = G * T, h = j * G + g;
-  const int64_t tok = static_cast<int64_t>(s) * T + i;
+  const int64_t tok = static_cast<int64_t>(s) * T + i;          // row of the workspace arrays
+  const int64_t ctok = static_cast<int64_t>(s) * a.in_T + a.row0 + i;  // row of the caller's v, gate, out
+  // (a prefill chunk's rows past the stream's new tokens are neither read nor stored)
+  const bool stored = a.rows_valid ? i < a.rows_valid[s] : true;
   const CacheView& c = a.c;
 
   // ---- caller inputs: tree, gate, prefix length, write-back target
@@ -741,7 +744,7 @@ __global__ void __launch_bounds__(256) verify_combine_kernel(const VerifyCombine
     npath_s = np;
   }
   float sig = 1.f;
-  if (a.gate) sig = 1.f / (1.f + expf(-bf16_to_f32(a.gate[tok * Hq + h])));
+  if (a.gate && stored) sig = 1.f / (1.f + expf(-bf16_to_f32(a.gate[ctok * Hq + h])));
   int64_t wb_off = -1;
   if (a.write_back && c.paged && g == 0) {  // (ring layers commit the accepted path instead)
     int n = c.seq_len[s];
@@ -795,7 +798,9 @@ __global__ void __launch_bounds__(256) verify_combine_kernel(const VerifyCombine
   for (int p = 0; p < np; ++p) {
     const float w = exp2_fast(sw[p] - M);
     L += w;
-    const uint16_t* vp = a.v + ((static_cast<int64_t>(s) * T + path_s[p]) * Hkv + j) * D + lane * EPL;
+    if (!stored) break;  // (its ancestors may lie past the caller's rows)
+    const uint16_t* vp =
+        a.v + ((static_cast<int64_t>(s) * a.in_T + a.row0 + path_s[p]) * Hkv + j) * D + lane * EPL;
 #pragma unroll
     for (int e = 0; e < EPL; e += 2) {
       const uint32_t x = *reinterpret_cast<const uint32_t*>(vp + e);
@@ -859,16 +864,18 @@ __global__ void __launch_bounds__(256) verify_combine_kernel(const VerifyCombine
     M = Mn;
   }
   const float scale = sig / L;
-  float* dst = a.out + (tok * Hq + h) * D + lane * EPL;
+  float* dst = a.out + (ctok * Hq + h) * D + lane * EPL;
+  if (stored) {
 #pragma unroll
-  for (int e = 0; e < EPL; e += 4)
-    *reinterpret_cast<float4*>(dst + e) =
-        make_float4(acc[e] * scale, acc[e + 1] * scale, acc[e + 2] * scale, acc[e + 3] * scale);
+    for (int e = 0; e < EPL; e += 4)
+      *reinterpret_cast<float4*>(dst + e) =
+          make_float4(acc[e] * scale, acc[e + 1] * scale, acc[e + 2] * scale, acc[e + 3] * scale);
+  }
 
   // ---- write-back of this node's entry at token index prefix_len + i
   if (wb_off >= 0) {
     const uint16_t* kh = a.khat + (tok * Hkv + j) * D + lane * EPL;
-    const uint16_t* vv = a.v + (tok * Hkv + j) * D + lane * EPL;
+    const uint16_t* vv = a.v + (ctok * Hkv + j) * D + lane * EPL;
 #pragma unroll
     for (int e = 0; e < EPL; e += 4) {
       *reinterpret_cast<uint2*>(c.k + wb_off + lane * EPL + e) = *reinterpret_cast<const uint2*>(kh + e);

@@ -231,6 +231,27 @@ DATTN_API int dattn_commit(dattn_t* h, int layer, const dattn_cache* cache, int 
                            const void* k, const void* v, const int32_t* parent, const int32_t* accepted,
                            const int32_t* num_accepted, const int32_t* pos, dattn_stream_t stream);
 
+/* Ragged prefill ("TensorFold PR #608" and "pega-omni PR #4": prefill rows
+ * beside the decode steps): stream s brings count[s] (0..max_tokens) new
+ * tokens, token t at position start_pos[s] + t. Each token attends to the
+ * stream's cache and to new tokens 0..t, and every new entry is written to
+ * the cache (ring: slot head + t, the ring keeping its newest R entries;
+ * paged: token index seq_len[s] + t) - the same as decoding the tokens one
+ * after another with write-back. q [S, max_tokens, Hq, D], k, v [S, max_tokens,
+ * Hkv, D] bf16, gate [S, max_tokens, Hq] or NULL; out [S, max_tokens, Hq, D]
+ * fp32: rows t < count[s] are written, the others are left as they are.
+ * The tokens go through the verify pass in chunks of min(max_verify_rows,
+ * 128 / G, R) rows as chain trees, each chunk committed before the next
+ * (five launches per chunk), so the handle needs max_verify_rows > 0
+ * (DATTN_EXCEEDS otherwise); a paged stream's cache must hold its new tokens
+ * (seq_len[s] + count[s] <= max_context, pages in its table). A stream whose
+ * count or ring metadata is out of range gets no tokens and is reported as
+ * DATTN_EINDEX (dattn_get_error). The caller then advances its metadata by
+ * count[s]. */
+DATTN_API int dattn_prefill(dattn_t* h, int layer, const dattn_cache* cache, int num_streams, int max_tokens,
+                            const void* q, const void* k, const void* v, const void* gate,
+                            const int32_t* count, const int32_t* start_pos, float* out, dattn_stream_t stream);
+
 /* Synchronize `stream`, then return and clear the sticky device error word:
  * DATTN_OK, DATTN_ETIMEOUT, DATTN_EINDEX, DATTN_ERANGE or DATTN_ELENGTH (the
  * first found in that order of severity). */
