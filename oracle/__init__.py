@@ -86,6 +86,13 @@ class Oracle:
                                           _P, _P, _P, _P, _P] + N3
         L.oracle_prefill_paged.argtypes = [_I, _I, _I, _I, _I, _I, _D, _P, _P, _I, _I, _P, _I, _P, _P, _P,
                                            _P, _P, _P, _P, _P] + N3
+        L.oracle_decode_fp8.argtypes = [_I, _I, _I, _I, _I, _I, _D, _P, _P, _I, _I, _P, _P, _P, _P, _I, _P,
+                                        _D, _D, _P, _P, _P, _P, _P, _P, _P, _P] + N3
+        L.oracle_decode_fp8.restype = _I
+        L.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+        L.oracle_e4m3_value.restype = _D
+        L.oracle_e4m3_round.argtypes = [_D]
+        L.oracle_e4m3_round.restype = ctypes.c_uint8
         L.oracle_qk_norm.argtypes = [_P, _P, _I, _D, _P]
         L.oracle_qk_norm.restype = None
         for f in ("oracle_rope_f64", "oracle_rope_bf16", "oracle_decode_ring",
@@ -257,6 +264,42 @@ class Oracle:
         if rc not in (0, 3):
             self._check(rc, "commit_paged")
         return kp, vp, rc
+
+    # ---- fp8 (E4M3) caches
+    def e4m3_value(self, b) -> float:
+        return float(self.lib.oracle_e4m3_value(int(b)))
+
+    def e4m3_round(self, x) -> int:
+        return int(self.lib.oracle_e4m3_round(float(x)))
+
+    def decode_fp8(self, k_cache, v_cache, q, k_new, v_new, pos, r, theta, k_scale, v_scale, gate=None,
+                   ring=None, paged=None, qk_norm=None):
+        """Decode over E4M3 caches (uint8): ring=(head, count, stream_rows or None) with
+        k/v [rows, Hkv, R, D], or paged=(block_table, seq_len) with k/v [pages, Hkv, P, D].
+        Returns (out f64, k_entry u8, v_entry u8)."""
+        k_cache = np.ascontiguousarray(k_cache, np.uint8)
+        v_cache = np.ascontiguousarray(v_cache, np.uint8)
+        q, k_new, v_new = map(_u16, (q, k_new, v_new))
+        gate = None if gate is None else _u16(gate)
+        n_rows, Hkv, RP, D = k_cache.shape
+        B, Hq, _ = q.shape
+        out = np.empty((B, Hq, D), np.float64)
+        ke = np.empty((B, Hkv, D), np.uint8)
+        ve = np.empty((B, Hkv, D), np.uint8)
+        if ring is not None:
+            head, count, rows = map(_i32, ring)
+            bt, sl, bts = None, None, 0
+        else:
+            bt, sl = map(_i32, paged)
+            head = count = rows = None
+            bts = bt.shape[1]
+        rc = self.lib.oracle_decode_fp8(0 if ring is not None else 1, B, Hq, Hkv, D, r, theta, _ptr(k_cache),
+                                        _ptr(v_cache), n_rows, RP, _ptr(rows), _ptr(head), _ptr(count), _ptr(bt),
+                                        bts, _ptr(sl), float(k_scale), float(v_scale), _ptr(q), _ptr(k_new),
+                                        _ptr(v_new), _ptr(gate), _ptr(_i32(pos)), _ptr(out), _ptr(ke), _ptr(ve),
+                                        *_norm(qk_norm))
+        self._check(rc, "decode_fp8")
+        return out, ke, ve
 
     # ---- ragged prefill (returns out and updated copies of the pools)
     def prefill_ring(self, k_ring, v_ring, ring_head, ring_count, count, start_pos, q, k, v, r, theta,

@@ -344,6 +344,72 @@ void attend_score_space(const double* qhat, int D,
   for (int d = 0; d < D; ++d) o[d] /= z;
 }
 
+// ---------------------------------------------------------------- fp8 cache
+// An fp8 KV cache ("TensorFold PR #608" names the fp8 cache and leaves it
+// out; reading: OCP FP8 E4M3 values with one dequantisation scale per layer
+// for K and one for V, cached value = e4m3 * scale).
+
+// Exact value of an E4M3 byte: 1 sign, 4 exponent (bias 7), 3 mantissa bits;
+// no infinities, 0x7f / 0xff are NaN; subnormals are multiples of 2^-9.
+double e4m3_value(uint8_t b) {
+  const int sign = b >> 7, e = (b >> 3) & 15, m = b & 7;
+  if (e == 15 && m == 7) return std::nan("");
+  const double mag = e == 0 ? std::ldexp(static_cast<double>(m), -9) : std::ldexp(8.0 + m, e - 10);
+  return sign ? -mag : mag;
+}
+
+// The E4M3 byte nearest to x (ties to even); magnitudes past 448, the largest
+// finite value, saturate to 448; NaN stays NaN.
+uint8_t e4m3_round(double x) {
+  if (std::isnan(x)) return 0x7f;
+  const uint8_t sign = std::signbit(x) ? 0x80 : 0x00;
+  const double a = std::fabs(x);
+  if (a >= 448.0) return sign | 0x7e;
+  int e2;
+  std::frexp(a, &e2);                   // a = f * 2^e2, f in [0.5, 1)
+  const int lead = std::max(e2 - 1, -6);  // exponent of the leading bit; subnormals share -6
+  const double spacing = std::ldexp(1.0, lead - 3);
+#if ORACLE_MUTATION == 24
+  const double q = std::floor(a / spacing) * spacing;  // planted: truncation
+#else
+  const double q = std::nearbyint(a / spacing) * spacing;  // nearest, ties to even
+#endif
+  if (q >= 448.0) return sign | 0x7e;
+  // encode q exactly
+  if (q < std::ldexp(1.0, -6)) return sign | static_cast<uint8_t>(q / std::ldexp(1.0, -9));
+  int e;
+  const double f = std::frexp(q, &e);  // q = f * 2^e
+  const int E = e - 1 + 7;
+  const int M = static_cast<int>((f * 2.0 - 1.0) * 8.0);
+  return sign | static_cast<uint8_t>((E << 3) | M);
+}
+
+// attend_score_space with every row given as fp64 values
+void attend_score_space_f64(const double* qhat, int D, const std::vector<const double*>& cached_k,
+                            const std::vector<const double*>& cached_v, const double* extra_k,
+                            const double* extra_v, double* o) {
+  const double scale = score_scale(D);
+  const size_t n = cached_k.size();
+  std::vector<double> s(n + 1);
+  for (size_t t = 0; t <= n; ++t) {
+    const double* k = t < n ? cached_k[t] : extra_k;
+    double acc = 0.0;
+    for (int d = 0; d < D; ++d) acc += qhat[d] * k[d];
+    s[t] = acc * scale;  // [s_cache (length n) | s_new (length 1)]
+  }
+  double m = -INFINITY;
+  for (double v : s) m = std::max(m, v);
+  double z = 0.0;
+  for (int d = 0; d < D; ++d) o[d] = 0.0;
+  for (size_t t = 0; t <= n; ++t) {
+    const double p = std::exp(s[t] - m);
+    z += p;
+    const double* v = t < n ? cached_v[t] : extra_v;
+    for (int d = 0; d < D; ++d) o[d] += p * v[d];
+  }
+  for (int d = 0; d < D; ++d) o[d] /= z;
+}
+
 // Key-space form: the keys (already rotated, as fp64 values of bf16 numbers)
 // and values are stacked into explicit matrices and attended in one pass.
 void attend_key_matrix(const double* qhat, int D, const std::vector<double>& K,
@@ -982,6 +1048,94 @@ int oracle_prefill_paged(int S, int Tmax, int Hq, int Hkv, int D, int r, double 
         const size_t dst = ((static_cast<size_t>(bt[idx]) * Hkv + j) * P + n % P) * D;
         std::memcpy(k_pages + dst, ke.data() + static_cast<size_t>(j) * D, D * 2);
         std::memcpy(v_pages + dst, ve.data() + static_cast<size_t>(j) * D, D * 2);
+      }
+    }
+  }
+  return 0;
+}
+
+// ----- E4M3 conversions, for the pins
+double oracle_e4m3_value(uint8_t b) { return e4m3_value(b); }
+uint8_t oracle_e4m3_round(double x) { return e4m3_round(x); }
+
+// ----- decode over an fp8 (E4M3) cache, ring (paged == 0: k/v [n_rows, Hkv,
+// R, D], valid slots the ring_count[b] before ring_head[b], stream_rows) or
+// paged (k/v [n_rows pages, Hkv, P, D], block_table, seq_len). Cached K value =
+// e4m3 * k_scale, V value = e4m3 * v_scale. The new token's K entry (the bf16
+// nearest its exact rotation, as in the bf16 cache) and its v_new are stored
+// as the E4M3 bytes nearest entry / k_scale and v_new / v_scale (fp64
+// quotients), and the new token is joined in score space as stored: the
+// values a later decode reads. k_entry, v_entry [B, Hkv, D] receive the bytes.
+int oracle_decode_fp8(int paged, int B, int Hq, int Hkv, int D, int r, double theta, const uint8_t* k_cache,
+                      const uint8_t* v_cache, int n_rows, int R_or_P, const int32_t* stream_rows,
+                      const int32_t* ring_head, const int32_t* ring_count, const int32_t* block_table,
+                      int bt_stride, const int32_t* seq_len, double k_scale, double v_scale, const uint16_t* q,
+                      const uint16_t* k_new, const uint16_t* v_new, const uint16_t* gate, const int32_t* pos,
+                      double* out, uint8_t* k_entry, uint8_t* v_entry, const uint16_t* q_norm,
+                      const uint16_t* k_norm, double norm_eps) {
+  if (!shape_ok(Hq, Hkv, D, r) || R_or_P <= 0 || !(k_scale > 0.0) || !(v_scale > 0.0)) return 1;
+  const Rot rot{r, theta, q_norm, k_norm, norm_eps};
+  for (int b = 0; b < B; ++b) {
+    for (int j = 0; j < Hkv; ++j) {
+      // the valid cached rows, dequantised
+      std::vector<std::vector<double>> kd, vd;
+      auto add = [&](size_t row) {
+        kd.emplace_back(D);
+        vd.emplace_back(D);
+        for (int d = 0; d < D; ++d) {
+#if ORACLE_MUTATION == 25
+          kd.back()[d] = e4m3_value(k_cache[row * D + d]);  // planted: K scale dropped
+#else
+          kd.back()[d] = e4m3_value(k_cache[row * D + d]) * k_scale;
+#endif
+          vd.back()[d] = e4m3_value(v_cache[row * D + d]) * v_scale;
+        }
+      };
+      if (!paged) {
+        const int R = R_or_P, row = stream_rows ? stream_rows[b] : b;
+        if (row < 0 || row >= n_rows || ring_head[b] < 0 || ring_head[b] >= R || ring_count[b] < 0 ||
+            ring_count[b] > R)
+          return 2;
+        for (int i = 0; i < ring_count[b]; ++i)
+          add((static_cast<size_t>(row) * Hkv + j) * R + ((ring_head[b] - 1 - i) % R + R) % R);
+      } else {
+        const int P = R_or_P;
+        if (seq_len[b] < 0 || (seq_len[b] + P - 1) / P > bt_stride) return 2;
+        for (int t = 0; t < seq_len[b]; ++t) {
+          const int pg = block_table[static_cast<size_t>(b) * bt_stride + t / P];
+          if (pg < 0 || pg >= n_rows) return 2;
+          add((static_cast<size_t>(pg) * Hkv + j) * P + t % P);
+        }
+      }
+      std::vector<const double*> ck, cv;
+      for (size_t t = 0; t < kd.size(); ++t) {
+        ck.push_back(kd[t].data());
+        cv.push_back(vd[t].data());
+      }
+      // the new token, quantised as stored
+      std::vector<uint16_t> kbuf, qbuf, entry(D);
+      const size_t nb = (static_cast<size_t>(b) * Hkv + j) * D;
+      rope_entry(normed(k_new + nb, rot.kn, D, rot.eps, kbuf), D, r, theta, pos[b], entry.data());
+      std::vector<double> kn(D), vn(D);
+      for (int d = 0; d < D; ++d) {
+        const uint8_t k8 = e4m3_round(bf16_value(entry[d]) / k_scale);
+        const uint8_t v8 = e4m3_round(bf16_value(v_new[nb + d]) / v_scale);
+        if (k_entry) k_entry[nb + d] = k8;
+        if (v_entry) v_entry[nb + d] = v8;
+        kn[d] = e4m3_value(k8) * k_scale;
+        vn[d] = e4m3_value(v8) * v_scale;
+      }
+      std::vector<double> qhat(D);
+      for (int h = 0; h < Hq; ++h) {
+        if (kv_head_of(h, Hq, Hkv) != j) continue;
+        rope_rotate(normed(q + (static_cast<size_t>(b) * Hq + h) * D, rot.qn, D, rot.eps, qbuf), D, r, theta,
+                    pos[b], qhat.data());
+        double* o = out + (static_cast<size_t>(b) * Hq + h) * D;
+        attend_score_space_f64(qhat.data(), D, ck, cv, kn.data(), vn.data(), o);
+        if (gate) {
+          const double g = sigmoid(bf16_value(gate[static_cast<size_t>(b) * Hq + h]));
+          for (int d = 0; d < D; ++d) o[d] *= g;
+        }
       }
     }
   }

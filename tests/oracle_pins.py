@@ -884,6 +884,63 @@ def pin_prefill_equals_chain_verify_then_commit(o):
     assert rc == 0 and np.array_equal(Kf, Kc) and np.array_equal(Vf, Vc), "paged: prefill vs commit"
 
 
+# ------------------------------------------------------------------ fp8 cache
+# OCP FP8 E4M3: 1 sign, 4 exponent bits (bias 7), 3 mantissa bits, no
+# infinities (0x7f is NaN), subnormals m * 2^-9. Golden values worked out by
+# hand from that definition.
+E4M3_GOLDEN = [  # (byte, value)
+    (0x00, 0.0), (0x01, 2.0 ** -9), (0x07, 7 * 2.0 ** -9), (0x08, 2.0 ** -6), (0x38, 1.0), (0x39, 1.125),
+    (0x3C, 1.5), (0x40, 2.0), (0x7E, 448.0), (0xB8, -1.0), (0xFE, -448.0), (0x30, 0.5), (0x58, 16.0),
+]
+E4M3_ROUNDING = [  # (x, byte): nearest, ties to even, saturating at 448
+    (1.0625, 0x38),          # tie between 1.0 (even) and 1.125
+    (1.1875, 0x3A),          # tie between 1.125 and 1.25 (even)
+    (1.06, 0x38), (1.07, 0x39),
+    (2.0 ** -10, 0x00),      # tie between 0 and 2^-9
+    (3 * 2.0 ** -10, 0x02),  # tie between 2^-9 and 2^-8 (even)
+    (7.5 * 2.0 ** -9, 0x08), # rounds up into the normals
+    (447.0, 0x7E), (460.0, 0x7E), (1e6, 0x7E), (-1e6, 0xFE), (-0.0, 0x80),
+    (0.3, 0x2A),             # 0.3 = 1.2 * 2^-2 -> 1.25 * 2^-2 (mantissa 2)
+]
+
+
+def pin_e4m3_golden_values_and_rounding(o):
+    """E4M3 decoding and nearest-even saturating rounding against values
+    worked out by hand from the format's definition; every byte round-trips."""
+    for b, v in E4M3_GOLDEN:
+        assert o.e4m3_value(b) == v, (hex(b), o.e4m3_value(b), v)
+    for x, b in E4M3_ROUNDING:
+        assert o.e4m3_round(x) == b, (x, hex(o.e4m3_round(x)), hex(b))
+    for b in range(256):
+        if b & 0x7F == 0x7F:
+            assert math.isnan(o.e4m3_value(b))
+            continue
+        v = o.e4m3_value(b)
+        assert o.e4m3_round(v) == (0x00 if v == 0 and b == 0 else b) or (v == 0 and b == 0x80), hex(b)
+
+
+def pin_fp8_decode_equals_bf16_decode_on_exact_values(o):
+    """When every cached value and the new token are E4M3 numbers times the
+    scales (powers of two, so every step is exact), the fp8 decode equals the
+    bf16 decode of the dequantised cache, and stores the token's bytes."""
+    rng = np.random.default_rng(2101)
+    Hq, Hkv, D, R = 4, 2, 32, 6
+    ks, vs = 0.5, 4.0
+    bytes_ok = np.array([b for b in range(256) if b & 0x7F != 0x7F and b & 0x78 != 0x78], np.uint8)  # |x| < 256
+    K8 = rng.choice(bytes_ok, (2, Hkv, R, D)).astype(np.uint8)
+    V8 = rng.choice(bytes_ok, (2, Hkv, R, D)).astype(np.uint8)
+    deq = lambda a, s: bf16(np.vectorize(o.e4m3_value)(a) * s)
+    q = rand_bf16((1, Hq, D), 2102)
+    kn8 = rng.choice(bytes_ok, (1, Hkv, D)).astype(np.uint8)
+    vn8 = rng.choice(bytes_ok, (1, Hkv, D)).astype(np.uint8)
+    k_new, v_new = deq(kn8, ks), deq(vn8, vs)
+    # no rotation (r = 0): the new K entry is k_new itself, exactly E4M3 * ks
+    out8, ke, ve = o.decode_fp8(K8, V8, q, k_new, v_new, [13], 0, 0.0, ks, vs, ring=([2], [5], [1]))
+    out, _, _ = o.decode_ring(deq(K8, ks), deq(V8, vs), [2], [5], q, k_new, v_new, [13], 0, 0.0, stream_rows=[1])
+    close(out8, out, 1e-12, "fp8 vs bf16 on exact values")
+    assert np.array_equal(ke, kn8) and np.array_equal(ve, vn8), "stored bytes"
+
+
 # ------------------------------------------------------------------ QK-norm
 # "pega-omni PR #4", talker kernels: RoPE with QK-norm. Reading (the page
 # gives no formula): y = bf16(w * x / sqrt(mean(x^2) + eps)), per head.

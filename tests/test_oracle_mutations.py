@@ -11,7 +11,8 @@ from the fp64-rounded sum instead of the exact one, a ring append slot off by
 one, the QK-norm eps outside the root, the QK-norm sum of squares not divided
 by D, a ring verify row that keeps the entries its path pushed out, a commit
 that takes the first nodes instead of the accepted path's, prefill positions
-shifted by one. If one of them passed every
+shifted by one, E4M3 rounding by truncation, the fp8 K scale dropped. If one
+of them passed every
 pin, the pins would not be sharp enough to trust the oracle.
 """
 import pytest
@@ -19,7 +20,7 @@ import pytest
 import oracle as oracle_pkg
 from oracle_pins import ALL_PINS
 
-MUTATIONS = list(range(1, 24))
+MUTATIONS = list(range(1, 26))
 
 
 @pytest.mark.parametrize("mutation", MUTATIONS)
