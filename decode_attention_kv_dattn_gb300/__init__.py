@@ -26,6 +26,7 @@ lib = ctypes.CDLL(LIB_PATH)
 
 OK, EINVAL, EXCEEDS, ECUDA, EINDEX, ETIMEOUT, EUNSUPPORTED, ELENGTH, ERANGE = range(9)
 CACHE_RING, CACHE_PAGED = 0, 1
+KV_BF16, KV_E4M3 = 0, 1
 
 _vp = ctypes.c_void_p
 _int = ctypes.c_int
@@ -34,7 +35,8 @@ _int = ctypes.c_int
 class LayerConfig(ctypes.Structure):
     _fields_ = [("cache_kind", _int), ("ring_slots", _int), ("page_size", _int),
                 ("rotary_dim", _int), ("rope_theta", ctypes.c_double),
-                ("q_norm_weight", _vp), ("k_norm_weight", _vp), ("norm_eps", ctypes.c_double)]
+                ("q_norm_weight", _vp), ("k_norm_weight", _vp), ("norm_eps", ctypes.c_double),
+                ("kv_format", _int), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
 
 
 def _host_bf16(w, D, what):
@@ -181,7 +183,8 @@ class Handle:
                                     l.get("rotary_dim", 0), float(l.get("rope_theta", 0.0)),
                                     None if qn is None else qn.ctypes.data,
                                     None if kn is None else kn.ctypes.data,
-                                    float(l.get("norm_eps", 0.0))))
+                                    float(l.get("norm_eps", 0.0)), int(l.get("kv_format", KV_BF16)),
+                                    float(l.get("k_scale", 1.0)), float(l.get("v_scale", 1.0))))
         self._layers = (LayerConfig * len(layers))(*cfgs)
         self.config = Config(num_q_heads, num_kv_heads, head_dim, max_streams, max_context,
                              max_verify_rows, len(layers), self._layers)

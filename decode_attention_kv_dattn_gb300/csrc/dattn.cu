@@ -273,6 +273,10 @@ int dattn_create(const dattn_config* cfg, int device, dattn_t** out) {
     if (L.rotary_dim < 0 || L.rotary_dim > D || L.rotary_dim % 2) return DATTN_EINVAL;
     if (L.rotary_dim > 0 && !(L.rope_theta > 0.0)) return DATTN_EINVAL;
     if ((L.q_norm_weight || L.k_norm_weight) && !(L.norm_eps >= 0.0)) return DATTN_EINVAL;
+    if (L.kv_format != DATTN_KV_BF16 && L.kv_format != DATTN_KV_E4M3) return DATTN_EINVAL;
+    if (L.kv_format == DATTN_KV_E4M3 &&
+        !(L.k_scale > 0.f && L.v_scale > 0.f && std::isfinite(L.k_scale) && std::isfinite(L.v_scale)))
+      return DATTN_EINVAL;
   }
   DeviceGuard guard(device);
   if (!guard.ok) return DATTN_ECUDA;
@@ -455,6 +459,9 @@ int dattn_append_kv(dattn_t* h, int layer, const dattn_cache* cache, int num_str
   a.k_norm = h->k_norm[layer];
   a.norm_eps = L.norm_eps;
   a.in_T = max_tokens;
+  a.f8 = L.kv_format == DATTN_KV_E4M3;
+  a.k_scale = L.k_scale;
+  a.v_scale = L.v_scale;
   rc = cuda_status(launch_append(a, reinterpret_cast<cudaStream_t>(stream)), "append");
   if (rc == DATTN_OK) record_launch(stream, cache->k);
   return rc;
@@ -469,6 +476,7 @@ int dattn_commit(dattn_t* h, int layer, const dattn_cache* cache, int num_stream
   if (rc != DATTN_OK) return rc;
   if (num_streams <= 0 || rows <= 0 || !k || !v || !parent || !accepted || !num_accepted) return DATTN_EINVAL;
   if (L.rotary_dim > 0 && !pos) return DATTN_EINVAL;
+  if (L.kv_format != DATTN_KV_BF16) return DATTN_EUNSUPPORTED;
   if (!aligned16(k) || !aligned16(v)) return DATTN_EINVAL;
   if (rows > 16) return DATTN_EXCEEDS;
   DeviceGuard guard(h->device);
@@ -524,11 +532,12 @@ int dattn_decode(dattn_t* h, int layer, const dattn_cache* cache, const dattn_de
   if (!guard.ok) return DATTN_ECUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-  const int ctas = plan_decode_ctas(h->decode_resident, B * h->Hkv, n_max, decode_tile_keys(h->D, h->G));
+  const bool f8 = L.kv_format == DATTN_KV_E4M3;
+  const int ctas = plan_decode_ctas(h->decode_resident, B * h->Hkv, n_max, decode_tile_keys(h->D, h->G, f8));
   if (static_cast<size_t>(ctas) + static_cast<size_t>(B) * h->Hkv > h->part_units) return DATTN_EXCEEDS;
   DecodeArgs da{};
   da.c = make_view(h, L, cache);
-  if (encode_cache_maps(da.c, h->Hkv, h->D, &da.tmap_k, &da.tmap_v) != cudaSuccess) return DATTN_EUNSUPPORTED;
+  if (encode_cache_maps(da.c, h->Hkv, h->D, &da.tmap_k, &da.tmap_v, f8) != cudaSuccess) return DATTN_EUNSUPPORTED;
   da.B = B;
   da.Hkv = h->Hkv;
   da.G = h->G;
@@ -553,6 +562,13 @@ int dattn_decode(dattn_t* h, int layer, const dattn_cache* cache, const dattn_de
   da.q_norm = h->q_norm[layer];
   da.k_norm = h->k_norm[layer];
   da.norm_eps = L.norm_eps;
+  if (f8) {
+    // the K scale rides on q's pre-scale; V's is applied to each partial output
+    da.f8 = 1;
+    da.k_scale = L.k_scale;
+    da.v_scale = L.v_scale;
+    da.q_scale = static_cast<float>(static_cast<double>(da.q_scale) * L.k_scale);
+  }
   rc = cuda_status(launch_decode(da, h->D, ctas, s), "decode");
   if (rc == DATTN_OK) {
     record_launch(stream, args->write_back ? cache->k : nullptr);
@@ -566,8 +582,8 @@ int dattn_verify(dattn_t* h, int layer, const dattn_cache* cache, const dattn_ve
   if (!h || !args || layer < 0 || layer >= static_cast<int>(h->layers.size())) return DATTN_EINVAL;
   const dattn_layer_config& L = h->layers[layer];
   const bool ring = L.cache_kind == DATTN_CACHE_RING;
-  // the prefix pass reads pages as 16-row groups
-  if (!ring && L.page_size % 16 != 0) return DATTN_EUNSUPPORTED;
+  // the prefix pass reads pages as 16-row groups, of bf16
+  if ((!ring && L.page_size % 16 != 0) || L.kv_format != DATTN_KV_BF16) return DATTN_EUNSUPPORTED;
   int rc = check_cache(L, cache);
   if (rc != DATTN_OK) return rc;
   const int S = args->num_streams, T = args->rows;
@@ -612,7 +628,7 @@ int dattn_prefill(dattn_t* h, int layer, const dattn_cache* cache, int num_strea
   if (!h || layer < 0 || layer >= static_cast<int>(h->layers.size())) return DATTN_EINVAL;
   const dattn_layer_config& L = h->layers[layer];
   const bool ring = L.cache_kind == DATTN_CACHE_RING;
-  if (!ring && L.page_size % 16 != 0) return DATTN_EUNSUPPORTED;
+  if ((!ring && L.page_size % 16 != 0) || L.kv_format != DATTN_KV_BF16) return DATTN_EUNSUPPORTED;
   int rc = check_cache(L, cache);
   if (rc != DATTN_OK) return rc;
   const int S = num_streams;

@@ -60,6 +60,7 @@
 //    rescaled only when some head's running maximum moved.
 #include "bf16_exact.h"
 #include "common.cuh"
+#include "e4m3.cuh"
 #include "qk_norm.cuh"
 #include "mma.cuh"
 
@@ -95,13 +96,14 @@ constexpr int kPiecesSlack = DATTN_PIECES_SLACK;
 template <int D>
 constexpr bool kGroupBox = D == 128;
 
-template <int D, int NT>
+template <int D, int NT, bool F8 = false>
 struct Geo {
   static constexpr int GP = 4 * NT;                  // heads per partial slot
   static constexpr int KSTEPS = D / 16;              // MMA k-steps of a score, m-tiles of an output
-  static constexpr int BOXES = D / 64;               // TMA boxes per 16-row group of K (or V)
+  static constexpr int ROWB = F8 ? D : 2 * D;        // bytes of one cached row (bf16, or E4M3)
+  static constexpr int BOXES = ROWB / 128;           // 128-byte boxes per 16-row group of K (or V)
   static constexpr int GBYTES = BOXES * kBoxBytes;   // K (or V) bytes of one group
-  static constexpr int KG = 256 / D;                 // groups per stage tile
+  static constexpr int KG = 512 / ROWB;              // groups per stage tile (16 KB of K and V)
   static constexpr int KHALF = KG * GBYTES;          // K part of a stage; V follows
   static constexpr int STAGE = 2 * KHALF;
   static constexpr int NS = 3;
@@ -272,6 +274,10 @@ __device__ __forceinline__ void prep_token(const DecodeArgs& a, const float* qs,
   float* sn = reinterpret_cast<float*>(slot + Gm::IN_SN);
   float* sig = reinterpret_cast<float*>(slot + Gm::IN_SIG);
   if (t < G) sig[t] = a.gate ? 1.f / (1.f + expf(-bf16_to_f32(gate_raw))) : 1.f;
+  // E4M3 cache: the entry and v_new are stored (and scored) as the E4M3 bytes
+  // nearest entry / k_scale and v_new / v_scale, at IN_KH (K, then V)
+  uint8_t* k8 = slot + Gm::IN_KH;
+  const uint16_t* vsrc = reinterpret_cast<const uint16_t*>(slot + Gm::IN_V);
   for (int e = t; e < D; e += NTH) {
     uint16_t v = ksrc[e];
     if (e < half) {
@@ -281,14 +287,20 @@ __device__ __forceinline__ void prep_token(const DecodeArgs& a, const float* qs,
       const float2 q = cs[e - half];  // y c + x s with y = k[e], x = k[e - half]
       v = bf16_dot2(ksrc[e], __float_as_uint(q.x), ksrc[e - half], __float_as_uint(q.y));
     }
-    kh[e] = v;
+    if (a.f8) {
+      k8[e] = e4m3_from_f64(static_cast<double>(bf16_to_f32(v)) / static_cast<double>(a.k_scale));
+      k8[D + e] = e4m3_from_f64(static_cast<double>(bf16_to_f32(vsrc[e])) / static_cast<double>(a.v_scale));
+    } else {
+      kh[e] = v;
+    }
   }
   team_sync<NTH>();
   constexpr int W = NTH / 32;
   const int w = t >> 5, lane = t & 31;
   for (int g = w; g < G; g += W) {
     float dot = 0.f;
-    for (int d = lane; d < D; d += 32) dot = fmaf(qs[g * D + d], bf16_to_f32(kh[d]), dot);
+    for (int d = lane; d < D; d += 32)
+      dot = fmaf(qs[g * D + d], a.f8 ? e4m3_to_f32(k8[d]) : bf16_to_f32(kh[d]), dot);
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) dot += __shfl_xor_sync(kFull, dot, o);
     if (lane == 0) sn[g] = dot;
@@ -330,11 +342,17 @@ __device__ __forceinline__ void finish_unit(const DecodeArgs& a, int u, const ui
     Merge8 mg;
     mg.M = sn[g];
     mg.L = 1.f;
-    const uint4 vw = *reinterpret_cast<const uint4*>(vsrc + d);
-    mg.o[0] = bf16_lo(vw.x); mg.o[1] = bf16_hi(vw.x);
-    mg.o[2] = bf16_lo(vw.y); mg.o[3] = bf16_hi(vw.y);
-    mg.o[4] = bf16_lo(vw.z); mg.o[5] = bf16_hi(vw.z);
-    mg.o[6] = bf16_lo(vw.w); mg.o[7] = bf16_hi(vw.w);
+    if (a.f8) {
+      const uint8_t* v8 = slot + Gm::IN_KH + D;  // the new token's V as stored
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mg.o[i] = e4m3_to_f32(v8[d + i]) * a.v_scale;
+    } else {
+      const uint4 vw = *reinterpret_cast<const uint4*>(vsrc + d);
+      mg.o[0] = bf16_lo(vw.x); mg.o[1] = bf16_hi(vw.x);
+      mg.o[2] = bf16_lo(vw.y); mg.o[3] = bf16_hi(vw.y);
+      mg.o[4] = bf16_lo(vw.z); mg.o[5] = bf16_hi(vw.z);
+      mg.o[6] = bf16_lo(vw.w); mg.o[7] = bf16_hi(vw.w);
+    }
     states(g, d, mg);
     const float scale = sig[g] / mg.L;
     float* dst = a.out + (static_cast<int64_t>(b) * Hq + j * G + g) * D + d;
@@ -358,7 +376,15 @@ __device__ __forceinline__ void finish_unit(const DecodeArgs& a, int u, const ui
       if (!(row < 0 || row >= c.n_rows || head < 0 || head >= c.R || cnt < 0 || cnt > c.R))
         wb = ((static_cast<int64_t>(row) * Hkv + j) * c.R + head) * D;
     }
-    if (wb >= 0) {
+    if (wb >= 0 && a.f8) {
+      // E4M3 rows: wb counts elements, which are bytes here
+      const uint8_t* k8 = slot + Gm::IN_KH;
+      for (int d = t * 16; d < D; d += NTH * 16) {
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(c.k) + wb + d) = *reinterpret_cast<const uint4*>(k8 + d);
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(c.v) + wb + d) =
+            *reinterpret_cast<const uint4*>(k8 + D + d);
+      }
+    } else if (wb >= 0) {
       for (int d = t * 8; d < D; d += NTH * 8) {
         *reinterpret_cast<uint4*>(c.k + wb + d) = *reinterpret_cast<const uint4*>(kh + d);
         *reinterpret_cast<uint4*>(c.v + wb + d) = *reinterpret_cast<const uint4*>(vsrc + d);
@@ -545,9 +571,9 @@ __device__ void end_segment(const DecodeArgs& a, const Split& sp, int pieces, in
   team_sync<NTH>();
 }
 
-template <int D, int NT, bool PAGED>
+template <int D, int NT, bool PAGED, bool F8>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeArgs a) {
-  using Gm = Geo<D, NT>;
+  using Gm = Geo<D, NT, F8>;
   constexpr int GP = Gm::GP, KSTEPS = Gm::KSTEPS, BOXES = Gm::BOXES, KG = Gm::KG, NS = Gm::NS;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int warp_max[kThreads / 32];
@@ -769,8 +795,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       for (int kg = 0; kg < KG; ++kg) {
         if (kg < gn) {
           const int row0 = wr[kg];
-          if constexpr (kGroupBox<D>) {
-            // one box per group: 16 rows x both 64-dim regions
+          if constexpr (kGroupBox<D> || F8) {
+            // one box per group: 16 rows x every 128-byte region
             tma_load_3d(kd + kg * Gm::GBYTES, &a.tmap_k, 0, row0, 0, bar, policy);
             tma_load_3d(kd + Gm::KHALF + kg * Gm::GBYTES, &a.tmap_v, 0, row0, 0, bar, policy);
           } else {
@@ -830,14 +856,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       for (int t = 0; t < NT; ++t) {
         const int head = NT == 1 ? (fg & 3) : fg;
         const bool lo = NT == 1 ? fg >= 4 : t == 1;
-        const float* src = qs + head * D + fc;
+        const float* src = qs + head * D;
 #pragma unroll
         for (int ks = 0; ks < KSTEPS; ++ks) {
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
-            const float2 x = *reinterpret_cast<const float2*>(src + ks * 16 + h2 * 8);
+            // bf16 K: the fragment's k-pairs are dims 2c, 2c + 8 of the step
+            // (c = lane % 4); E4M3 K: dims 4c and 4c + 2 (the order its bytes
+            // reach the A fragment, applied to both operands alike)
+            const int dim = F8 ? ks * 16 + 4 * (lane & 3) + 2 * h2 : ks * 16 + fc + 8 * h2;
+            const float2 x = *reinterpret_cast<const float2*>(src + dim);
             uint32_t hi, lw;
-            split_bf16x2(x.x, x.y, hi, lw);
+            if constexpr (F8)
+              split_f16x2(x.x, x.y, hi, lw);
+            else
+              split_bf16x2(x.x, x.y, hi, lw);
             qb[ks][t][h2] = lo ? lw : hi;
           }
         }
@@ -910,12 +943,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
               for (int t = 0; t < NT; ++t)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) sacc[h2][t][e] = 0.f;
+            if constexpr (F8) {
+              // 32 bytes of 16 rows per load: E4M3 dims 4c..4c+3 of rows r and
+              // r + 8 (and 16 dims on), widened exactly to fp16 pairs: two k-steps
 #pragma unroll
-            for (int ks = 0; ks < KSTEPS; ++ks) {
-              uint32_t af[4];
-              ldsm_x4(kbase + (ks >> 2) * kBoxBytes + koff[ks & 3], af);
+              for (int j = 0; j < KSTEPS / 2; ++j) {
+                uint32_t af[4];
+                ldsm_x4(kbase + (j >> 2) * kBoxBytes + koff[j & 3], af);
+                const uint32_t a0[4] = {e4m3x2_lo(af[0]), e4m3x2_lo(af[1]), e4m3x2_hi(af[0]), e4m3x2_hi(af[1])};
+                const uint32_t a1[4] = {e4m3x2_lo(af[2]), e4m3x2_lo(af[3]), e4m3x2_hi(af[2]), e4m3x2_hi(af[3])};
 #pragma unroll
-              for (int t = 0; t < NT; ++t) mma_bf16(sacc[ks & 1][t], af, qb[ks][t][0], qb[ks][t][1]);
+                for (int t = 0; t < NT; ++t) {
+                  mma_f16(sacc[0][t], a0, qb[2 * j][t][0], qb[2 * j][t][1]);
+                  mma_f16(sacc[1][t], a1, qb[2 * j + 1][t][0], qb[2 * j + 1][t][1]);
+                }
+              }
+            } else {
+#pragma unroll
+              for (int ks = 0; ks < KSTEPS; ++ks) {
+                uint32_t af[4];
+                ldsm_x4(kbase + (ks >> 2) * kBoxBytes + koff[ks & 3], af);
+#pragma unroll
+                for (int t = 0; t < NT; ++t) mma_bf16(sacc[ks & 1][t], af, qb[ks][t][0], qb[ks][t][1]);
+              }
             }
             // full scores of heads hbase + e at keys fg (i = e) and fg + 8 (i = 2 + e)
             float s[4];
@@ -963,8 +1013,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
             uint32_t pb[NT][2];
             {
               uint32_t h01, l01, h23, l23;
-              split_bf16x2(p[0], p[1], h01, l01);
-              split_bf16x2(p[2], p[3], h23, l23);
+              if constexpr (F8) {
+                split_f16x2(p[0], p[1], h01, l01);
+                split_f16x2(p[2], p[3], h23, l23);
+              } else {
+                split_bf16x2(p[0], p[1], h01, l01);
+                split_bf16x2(p[2], p[3], h23, l23);
+              }
               if (NT == 1) {
                 pb[0][0] = movm_t(lo_lane ? l01 : h01);
                 pb[0][1] = movm_t(lo_lane ? l23 : h23);
@@ -977,12 +1032,38 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
             }
 
             // ---- outputs O^T += V^T . P^T
+            if constexpr (F8) {
+              // V^T from byte pairs of two key rows: for dims 4f..4f+3 (f = lane / 4)
+              // of 32-dim block p, keys 2c, 2c + 1, 2c + 8, 2c + 9 (c = lane % 4).
+              // The A rows of m-tile 2p + e are dims 4f + 2e (row f) and 4f + 2e + 1
+              // (row f + 8); the outputs are put back in order when stored.
 #pragma unroll
-            for (int mt = 0; mt < KSTEPS; ++mt) {
-              uint32_t af[4];
-              ldsm_x4_t(vbase + (mt >> 2) * kBoxBytes + voff[mt & 3], af);
+              for (int pj = 0; pj < KSTEPS / 2; ++pj) {
+                uint32_t w[4];
 #pragma unroll
-              for (int t = 0; t < NT; ++t) mma_bf16(o[mt][t], af, pb[t][0], pb[t][1]);
+                for (int kr = 0; kr < 4; ++kr) {
+                  const int r = 2 * (lane & 3) + (kr & 1) + 8 * (kr >> 1);
+                  const int chunk = (2 * (pj & 3) + (fg >> 2)) ^ (r & 7);
+                  w[kr] = ld_shared_u32(vbase + (pj >> 2) * kBoxBytes + r * 128 + chunk * 16 + 4 * (fg & 3));
+                }
+                const uint32_t lo01 = prmt(w[0], w[1], 0x5140u), hi01 = prmt(w[0], w[1], 0x7362u);
+                const uint32_t lo89 = prmt(w[2], w[3], 0x5140u), hi89 = prmt(w[2], w[3], 0x7362u);
+                const uint32_t a0[4] = {e4m3x2_lo(lo01), e4m3x2_hi(lo01), e4m3x2_lo(lo89), e4m3x2_hi(lo89)};
+                const uint32_t a1[4] = {e4m3x2_lo(hi01), e4m3x2_hi(hi01), e4m3x2_lo(hi89), e4m3x2_hi(hi89)};
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                  mma_f16(o[2 * pj][t], a0, pb[t][0], pb[t][1]);
+                  mma_f16(o[2 * pj + 1][t], a1, pb[t][0], pb[t][1]);
+                }
+              }
+            } else {
+#pragma unroll
+              for (int mt = 0; mt < KSTEPS; ++mt) {
+                uint32_t af[4];
+                ldsm_x4_t(vbase + (mt >> 2) * kBoxBytes + voff[mt & 3], af);
+#pragma unroll
+                for (int t = 0; t < NT; ++t) mma_bf16(o[mt][t], af, pb[t][0], pb[t][1]);
+              }
             }
           }
           __syncwarp();
@@ -1032,7 +1113,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
             } else {
               v = o[mt][0][i] + o[mt][NT - 1][i];
             }
-            if (writer) os[(hbase + (i & 1)) * D + mt * 16 + fg + 8 * (i >> 1)] = v;
+            // (E4M3 V: its m-tiles hold permuted dims, and its values its scale)
+            const int dim = F8 ? 32 * (mt >> 1) + 4 * fg + 2 * (mt & 1) + (i >> 1) : mt * 16 + fg + 8 * (i >> 1);
+            if (writer) os[(hbase + (i & 1)) * D + dim] = F8 ? v * a.v_scale : v;
           }
         fence_proxy_async_smem();  // the buffer is refilled by TMA after the merge
       }
@@ -1159,10 +1242,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 
 // ---------------------------------------------------------------- launch
 
-template <int D, int NT, bool PAGED>
+template <int D, int NT, bool PAGED, bool F8>
 cudaError_t decode_launch(const DecodeArgs& a, int ctas, cudaStream_t s, bool pdl) {
-  using Gm = Geo<D, NT>;
-  auto k = decode_kernel<D, NT, PAGED>;
+  using Gm = Geo<D, NT, F8>;
+  auto k = decode_kernel<D, NT, PAGED, F8>;
   static std::atomic<uint64_t> opted{0};
   const cudaError_t e = opt_in_smem(k, Gm::SMEM_MAX, opted);
   if (e != cudaSuccess) return e;
@@ -1174,10 +1257,33 @@ cudaError_t decode_launch(const DecodeArgs& a, int ctas, cudaStream_t s, bool pd
   return launch_pdl(k, dim3(ctas), dim3(kThreads), smem, s, a);
 }
 
-template <int D, int NT>
+template <int D, int NT, bool F8>
 cudaError_t decode_dispatch_paged(const DecodeArgs& a, int ctas, cudaStream_t s, bool pdl) {
-  return a.c.paged ? decode_launch<D, NT, true>(a, ctas, s, pdl) : decode_launch<D, NT, false>(a, ctas, s, pdl);
+  return a.c.paged ? decode_launch<D, NT, true, F8>(a, ctas, s, pdl) : decode_launch<D, NT, false, F8>(a, ctas, s, pdl);
 }
+
+template <bool F8>
+cudaError_t decode_dispatch(const DecodeArgs& a, int D, int GP, int ctas, cudaStream_t s, bool pdl) {
+  if (D == 256) {
+    if (GP == 4) return decode_dispatch_paged<256, 1, F8>(a, ctas, s, pdl);
+    if (GP == 8) return decode_dispatch_paged<256, 2, F8>(a, ctas, s, pdl);
+  } else if (D == 128) {
+    if (GP == 4) return decode_dispatch_paged<128, 1, F8>(a, ctas, s, pdl);
+    if (GP == 8) return decode_dispatch_paged<128, 2, F8>(a, ctas, s, pdl);
+  }
+  return cudaErrorNotSupported;
+}
+
+}  // namespace
+
+#ifdef DATTN_DECODE_FP8_UNIT
+// This translation unit holds the E4M3-cache instantiations only (compiled
+// beside the bf16 ones, in parallel).
+cudaError_t launch_decode_fp8(const DecodeArgs& a, int D, int GP, int ctas, cudaStream_t s, bool pdl) {
+  return decode_dispatch<true>(a, D, GP, ctas, s, pdl);
+}
+#else
+namespace {
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -1200,11 +1306,26 @@ EncodeTiledFn encode_tiled() {
 
 }  // namespace
 
-cudaError_t encode_cache_maps(const CacheView& c, int Hkv, int D, CUtensorMap* k, CUtensorMap* v) {
+cudaError_t encode_cache_maps(const CacheView& c, int Hkv, int D, CUtensorMap* k, CUtensorMap* v, bool f8) {
   const EncodeTiledFn fn = encode_tiled();
   if (!fn) return cudaErrorNotSupported;
   const uint64_t rows = static_cast<uint64_t>(c.n_rows) * Hkv * (c.paged ? c.P : c.R);
   if (rows == 0 || rows > 0x7fffffffull) return cudaErrorNotSupported;
+  if (f8) {
+    // E4M3 rows of D bytes: a 3D view (128 bytes, row, D/128 regions), one
+    // box per 16-row group, 128-byte swizzled like the bf16 groups
+    const cuuint64_t dims[3] = {128, rows, static_cast<cuuint64_t>(D / 128)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D), 128};
+    const cuuint32_t box[3] = {128, kGroup, static_cast<cuuint32_t>(D / 128)};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    for (int i = 0; i < 2; ++i) {
+      const CUresult r = fn(i ? v : k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, i ? c.v : c.k, dims, strides, box,
+                            estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    return cudaSuccess;
+  }
   // D = 128: a 3D view of the [rows, D] bf16 cache, (64 dims, row, 64-dim
   // region), so that one box brings a 16-row group as its regions of 16 rows x
   // 128 bytes one after the other; D = 256: the 2D [rows, D] view, one box
@@ -1272,26 +1393,28 @@ cudaError_t launch_decode(const DecodeArgs& args, int D, int ctas, cudaStream_t 
   const int GP = decode_group_pad(a.G);
   if (a.B * a.Hkv > kMaxUnits) return cudaErrorNotSupported;
   if (a.r > D || a.r % 2 != 0) return cudaErrorNotSupported;
-  if (D == 256) {
-    if (GP == 4) return decode_dispatch_paged<256, 1>(a, ctas, s, pdl);
-    if (GP == 8) return decode_dispatch_paged<256, 2>(a, ctas, s, pdl);
-  } else if (D == 128) {
-    if (GP == 4) return decode_dispatch_paged<128, 1>(a, ctas, s, pdl);
-    if (GP == 8) return decode_dispatch_paged<128, 2>(a, ctas, s, pdl);
-  }
-  return cudaErrorNotSupported;
+  if (a.f8) return launch_decode_fp8(a, D, GP, ctas, s, pdl);
+  return decode_dispatch<false>(a, D, GP, ctas, s, pdl);
 }
 
-int decode_tile_keys(int D, int G) {
+int decode_tile_keys(int D, int G, bool f8) {
   if (decode_group_pad(G) == 0 || (D != 128 && D != 256)) return 0;
-  return 256 / D * kGroup;
+  return (f8 ? 512 : 256) / D * kGroup;
 }
 
 int decode_ctas_per_sm(int D, int G) {
   const int GP = decode_group_pad(G);
   int smem = 0;
-  if (D == 256) smem = GP == 4 ? Geo<256, 1>::SMEM_MAX : GP == 8 ? Geo<256, 2>::SMEM_MAX : 0;
-  if (D == 128) smem = GP == 4 ? Geo<128, 1>::SMEM_MAX : GP == 8 ? Geo<128, 2>::SMEM_MAX : 0;
+  // (the larger of the bf16 and E4M3 layouts: an E4M3 tile holds more groups)
+  const auto larger = [](int x, int y) { return x > y ? x : y; };
+  if (D == 256)
+    smem = GP == 4   ? larger(Geo<256, 1>::SMEM_MAX, Geo<256, 1, true>::SMEM_MAX)
+           : GP == 8 ? larger(Geo<256, 2>::SMEM_MAX, Geo<256, 2, true>::SMEM_MAX)
+                     : 0;
+  if (D == 128)
+    smem = GP == 4   ? larger(Geo<128, 1>::SMEM_MAX, Geo<128, 1, true>::SMEM_MAX)
+           : GP == 8 ? larger(Geo<128, 2>::SMEM_MAX, Geo<128, 2, true>::SMEM_MAX)
+                     : 0;
   if (smem == 0) return 0;
   // 228 KB of shared memory per SM; 1 KB reserved and the static block-scan scratch per CTA
   const int per_sm = 233472 / (smem + 1024 + 64);
@@ -1299,5 +1422,6 @@ int decode_ctas_per_sm(int D, int G) {
 }
 
 int decode_max_units() { return kMaxUnits; }
+#endif  // DATTN_DECODE_FP8_UNIT
 
 }  // namespace dattn

@@ -114,6 +114,10 @@ struct DecodeArgs {
   const uint16_t* q_norm;      // [D] QK-norm weights of the queries, or null
   const uint16_t* k_norm;      // [D] of the new key, or null
   double norm_eps;
+  // E4M3 cache (the pools hold bytes; k, v of CacheView are byte arrays):
+  // cached value = e4m3 * scale. q_scale then includes k_scale.
+  int f8;
+  float k_scale, v_scale;
 };
 
 struct AppendArgs {
@@ -132,6 +136,10 @@ struct AppendArgs {
   // source rows: b * in_T + row0 + t of k/v (in_T = Tmax, row0 = 0 but for
   // prefill chunks)
   int in_T, row0;
+  // E4M3 pools: entries stored as the E4M3 bytes nearest entry / k_scale
+  // (K) and v / v_scale (V)
+  int f8;
+  float k_scale, v_scale;
   // commit of verify paths: token t of row b is source row gather[b * Tmax + t]
   // of k/v ([B, Tmax, Hkv, D]), and the row's first count[b] entries of gather
   // must form a path from a root under parent [B, Tmax]; null for a plain append
@@ -225,8 +233,10 @@ cudaError_t launch_decode(const DecodeArgs& a, int D, int ctas, cudaStream_t s, 
 // Hkv * (R or P), D] bf16 rows, 128-byte swizzle: at D = 128 seen as (64 dims,
 // row, 2 regions) with one box per 16-row group; at D = 256 as [rows, D] with
 // boxes of 16 rows x 64 dims.
-cudaError_t encode_cache_maps(const CacheView& c, int Hkv, int D, CUtensorMap* k, CUtensorMap* v);
+cudaError_t encode_cache_maps(const CacheView& c, int Hkv, int D, CUtensorMap* k, CUtensorMap* v, bool f8 = false);
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
+// decode over an E4M3 cache (decode_fp8.cu); GP = decode_group_pad(G)
+cudaError_t launch_decode_fp8(const DecodeArgs& a, int D, int GP, int ctas, cudaStream_t s, bool pdl);
 cudaError_t launch_verify_split(const VerifySplitArgs& a, int D, cudaStream_t s);
 cudaError_t launch_verify_combine(const VerifyCombineArgs& a, int D, cudaStream_t s);
 // Keys per tile of the verify pass and its largest unit count.
@@ -247,7 +257,7 @@ cudaError_t encode_verify_maps(const CacheView& c, int Hkv, int D, const uint16_
 // Resident CTAs per SM of the decode kernel for (D, G) (0 if unsupported).
 int decode_ctas_per_sm(int D, int G);
 // Keys per stage tile of the decode kernel for (D, G).
-int decode_tile_keys(int D, int G);
+int decode_tile_keys(int D, int G, bool f8 = false);
 // Largest number of (stream, KV head) units of one decode call.
 int decode_max_units();
 

@@ -12,6 +12,8 @@
 // Each 32-bit register holds two bf16 values, the lower index in the low half.
 #pragma once
 
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 namespace dattn {
@@ -45,6 +47,58 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// d += A * B, fp16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two floats to fp16 (nearest-even), `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// x as hi + lo, both fp16: returns the two packed pairs for (x0, x1).
+__device__ __forceinline__ void split_f16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_f16x2(x0, x1);
+  const float h0 = __half2float(__ushort_as_half(static_cast<unsigned short>(hi & 0xffffu)));
+  const float h1 = __half2float(__ushort_as_half(static_cast<unsigned short>(hi >> 16)));
+  lo = pack_f16x2(x0 - h0, x1 - h1);
+}
+
+// Two E4M3 values (the low and high byte of x) widened to an fp16 pair, low
+// byte in the low half (exact: every E4M3 value is an fp16 value).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t x) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(x), __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+__device__ __forceinline__ uint32_t e4m3x2_lo(uint32_t w) { return e4m3x2_to_f16x2(static_cast<uint16_t>(w)); }
+__device__ __forceinline__ uint32_t e4m3x2_hi(uint32_t w) { return e4m3x2_to_f16x2(static_cast<uint16_t>(w >> 16)); }
+
+// The value of one E4M3 byte.
+__device__ __forceinline__ float e4m3_to_f32(uint8_t b) {
+  const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(b), __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+// Bytes of {b, a} picked by the four selector nibbles (prmt).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
 }
 
 // Two floats to bf16 (nearest-even), `lo` in the low half.

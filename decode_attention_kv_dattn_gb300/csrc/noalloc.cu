@@ -92,6 +92,7 @@ extern "C" DATTN_API int dattn_decode_noalloc(const dattn_config* cfg, int layer
   if (L.rotary_dim < 0 || L.rotary_dim > D || L.rotary_dim % 2 || (L.rotary_dim > 0 && !(L.rope_theta > 0.0)))
     return DATTN_EINVAL;
   if ((L.q_norm_weight || L.k_norm_weight) && !(L.norm_eps >= 0.0)) return DATTN_EINVAL;
+  if (L.kv_format != DATTN_KV_BF16) return DATTN_EUNSUPPORTED;
   if (!cache->k || !cache->v || cache->n_rows <= 0) return DATTN_EINVAL;
   if ((reinterpret_cast<uintptr_t>(cache->k) | reinterpret_cast<uintptr_t>(cache->v)) & 15u) return DATTN_EINVAL;
   int n_max;

@@ -16,6 +16,7 @@
 #include <cuda_fp16.h>
 
 #include "bf16_exact.h"
+#include "e4m3.cuh"
 #include "common.cuh"
 #include "qk_norm.cuh"
 
@@ -234,6 +235,45 @@ __global__ void __launch_bounds__(kRopeThreads) append_kernel(const AppendArgs a
     head_stride = static_cast<int64_t>(c.R) * a.D;
   }
   const int64_t src0 = (static_cast<int64_t>(b) * a.in_T + a.row0 + src_t) * a.Hkv * a.D;
+  if (a.f8) {
+    // E4M3 pools (rows of D bytes): every element quantised on its own; the
+    // key from its entry (QK-norm and RoPE as below when rotating)
+    uint8_t* k8 = reinterpret_cast<uint8_t*>(c.k);
+    uint8_t* v8 = reinterpret_cast<uint8_t*>(c.v);
+    __shared__ double inv8[kMaxAppendHeads];
+    const uint16_t* kn8 = a.rotate ? a.k_norm : nullptr;
+    if (kn8) {
+      const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+      for (int h = w; h < a.Hkv; h += kRopeThreads / 32) {
+        const double inv = qk_norm_inv(a.k + src0 + h * a.D, a.D, a.norm_eps, lane);
+        if (lane == 0) inv8[h] = inv;
+      }
+      __syncthreads();
+    }
+    auto kv = [&](int h, int d) {
+      const uint16_t x = a.k[src0 + h * a.D + d];
+      return kn8 ? qk_norm_apply(x, kn8[d], inv8[h]) : x;
+    };
+    const int half = a.r / 2;
+    const int64_t pos = a.start_pos ? static_cast<int64_t>(a.start_pos[b]) + t : 0;
+    for (int e = threadIdx.x; e < a.Hkv * a.D; e += kRopeThreads) {
+      const int h = e / a.D, d = e - h * a.D;
+      uint16_t entry = kv(h, d);
+      if (a.rotate && d < a.r) {
+        const int i = d < half ? d : d - half;
+        float cf, sf;
+        rope_cos_sin(pos, a.rope_step[i], cf, sf);
+        const uint32_t cb = __float_as_uint(cf), sb = __float_as_uint(sf);
+        entry = d < half ? bf16_dot2(kv(h, d), cb, kv(h, d + half), sb ^ 0x80000000u)  // x c - y s
+                         : bf16_dot2(kv(h, d), cb, kv(h, d - half), sb);               // y c + x s
+      }
+      const int64_t o = dst0 + h * head_stride + d;
+      k8[o] = e4m3_from_f64(static_cast<double>(bf16_to_f32(entry)) / static_cast<double>(a.k_scale));
+      v8[o] = e4m3_from_f64(static_cast<double>(bf16_to_f32(a.v[src0 + h * a.D + d])) /
+                            static_cast<double>(a.v_scale));
+    }
+    return;
+  }
   // V: plain copy, 16 bytes per thread-step.  (Every return above is taken by
   // the whole CTA.)
   for (int e = threadIdx.x; e < a.Hkv * a.D / 8; e += kRopeThreads) {

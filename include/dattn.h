@@ -74,6 +74,14 @@ enum {
 
 enum { DATTN_CACHE_RING = 0, DATTN_CACHE_PAGED = 1 };
 
+/* Element format of a layer's K/V pools. */
+enum {
+  DATTN_KV_BF16 = 0,  /* bf16 (raw 16-bit patterns)                                 */
+  DATTN_KV_E4M3 = 1   /* OCP FP8 E4M3 bytes; value = e4m3 * scale ("TensorFold PR
+                         #608" names the fp8 cache and leaves it out): decode and
+                         append only                                              */
+};
+
 /* cudaStream_t without including the CUDA headers. */
 typedef struct CUstream_st* dattn_stream_t;
 
@@ -94,6 +102,18 @@ typedef struct {
   const uint16_t* q_norm_weight;
   const uint16_t* k_norm_weight;
   double norm_eps;    /* eps (>= 0) of both norms                               */
+  /* DATTN_KV_BF16 (0) or DATTN_KV_E4M3. An E4M3 layer's pools hold bytes
+   * [.., D] instead of bf16; a cached K value is e4m3 * k_scale, a V value
+   * e4m3 * v_scale (finite, > 0; quantisation divides by these fp32 values
+   * in fp64). Decode scores the cache as stored, stores
+   * the new entry as the E4M3 bytes nearest entry / k_scale and
+   * v_new / v_scale (ties to even, saturating at 448) and joins the new token
+   * as stored; dattn_append_kv stores the same bytes. dattn_verify,
+   * dattn_commit, dattn_prefill and dattn_decode_noalloc return
+   * DATTN_EUNSUPPORTED for such a layer. */
+  int kv_format;
+  float k_scale;
+  float v_scale;
 } dattn_layer_config;
 
 typedef struct {

@@ -127,6 +127,28 @@ def decode_inputs(gen, B, Hq, Hkv, D, pos, gate: bool) -> DecodeInputs:
     return DecodeInputs(q, k, v, g, np.asarray(pos, np.int32).reshape(B))
 
 
+NAN_E4M3 = 0x7F
+
+
+def rand_e4m3(shape, gen: torch.Generator, max_exp: int = 8) -> np.ndarray:
+    """Random E4M3 codes as uint8, drawn as bit fields: a uniform sign, an
+    exponent field in [0, max_exp] (magnitudes below 2^(max_exp - 6)) and a
+    uniform 3-bit mantissa."""
+    n = int(np.prod(shape))
+    sign = torch.randint(0, 2, (n,), generator=gen).numpy().astype(np.uint8)
+    exp = torch.randint(0, max_exp + 1, (n,), generator=gen).numpy().astype(np.uint8)
+    man = torch.randint(0, 8, (n,), generator=gen).numpy().astype(np.uint8)
+    return ((sign << 7) | (exp << 3) | man).reshape(shape)
+
+
+def e4m3_pool_like(pool_bf16: np.ndarray, gen: torch.Generator, max_exp: int = 8) -> np.ndarray:
+    """An E4M3 pool with the same written slots as a bf16 pool: random codes
+    where the bf16 pool holds data, NaN (0x7f) where it holds NaN."""
+    out = rand_e4m3(pool_bf16.shape, gen, max_exp)
+    out[pool_bf16 == NAN_BF16] = NAN_E4M3
+    return out
+
+
 def ring_cache(gen, B, Hkv, D, R, counts, heads=None, n_rows=None, stream_rows=None) -> RingCache:
     """Ring of R slots per (row, KV head). Stream b holds counts[b] entries that
     end just before heads[b] (a uniform random head if not given); every other
