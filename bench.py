@@ -303,6 +303,10 @@ class DecodeCall(Workload):
         g.manual_seed(seed)
         hg = synth.generator(seed)
         rnd = lambda *sh: torch.randn(*sh, generator=g, device=device).to(torch.bfloat16)
+        # "fp8_<name>": the same workload over E4M3 K/V pools (scale 1/64 each)
+        f8 = name.startswith("fp8_")
+        if f8:
+            name = name[4:]
         if name == "sliding":
             B, Hq, Hkv, Dh, R = 1, 8, 2, 256, 511
             start = int(synth.randint(0, R - 1, 1, hg)[0])
@@ -342,6 +346,10 @@ class DecodeCall(Workload):
                 raise ValueError(name)
             k, v, bt, seq = synth.paged_device(g, B, Hkv, Dh, P, self.lens, room=1, device=device)
             layer = {"kind": dattn.CACHE_PAGED, "page_size": P, "rotary_dim": r, "rope_theta": th}
+            if f8:
+                k, v = synth.e4m3_device(g, k.shape, device), synth.e4m3_device(g, v.shape, device)
+                layer.update(kv_format=dattn.KV_E4M3, k_scale=1 / 64, v_scale=1 / 64)
+                desc = desc + "; E4M3 KV cache, scales 1/64"
             self.desc = dattn.paged_cache(k, v, bt, seq)
             self._keep = (k, v, bt, seq)
             pos, kind = self.lens, "full"
@@ -361,11 +369,13 @@ class DecodeCall(Workload):
         kv = io = 0
         for n in self.lens:
             a, b_ = layer_bytes(kind, 1, n, P, Hq, Hkv, Dh, gate)
+            if f8:  # one byte per cached and written K/V element
+                a, b_ = a // 2, b_ - 2 * Hkv * Dh
             kv += a
             io += b_
         self.bytes_step, self.tokens_step = kv + io, sum(n + 1 for n in self.lens)
         self.dominant, self.others, self.dominant_kv_bytes = [0], [], kv
-        self.kernel = "decode_kernel (" + self.config["workload"].split(":")[0] + ")"
+        self.kernel = ("decode_kernel E4M3 (" if f8 else "decode_kernel (") + self.config["workload"].split(":")[0] + ")"
 
     def run_call(self, i, stream=None):
         self.h.decode(0, self.desc, self.q, self.k_new, self.v_new, self.pos, self.out, gate=self.g,
@@ -575,6 +585,9 @@ SURVEY = [
     ("long128k_b1", lambda: DecodeCall("long128k_b1", SEED)),
     ("long128k_b8", lambda: DecodeCall("long128k_b8", SEED)),
     ("long128k_b64", lambda: DecodeCall("long128k_b64", SEED)),
+    ("fp8_paged", lambda: DecodeCall("fp8_paged", SEED)),
+    ("fp8_long128k_b8", lambda: DecodeCall("fp8_long128k_b8", SEED)),
+    ("fp8_long262k", lambda: DecodeCall("fp8_long262k", SEED)),
     ("hybrid_b1_c1024", lambda: Step(1, 1024, SEED)),
     ("hybrid_b1_c4096", lambda: Step(1, 4096, SEED)),
     ("hybrid_b8_c1024", lambda: Step(8, 1024, SEED)),

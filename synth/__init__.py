@@ -356,6 +356,14 @@ def hybrid_step_device(seed: int, B: int, context: int, device="cuda"):
     return layers
 
 
+def e4m3_device(gen, shape, device="cuda"):
+    """Random E4M3 codes drawn on the device (uniform bytes, NaN codes
+    0x7f / 0xff replaced by zero)."""
+    t = torch.randint(0, 256, tuple(shape), generator=gen, device=device, dtype=torch.int32).to(torch.uint8)
+    t[(t & 0x7F) == 0x7F] = 0
+    return t
+
+
 def paged_device(gen, B, Hkv, D, P, lens, room=1, device="cuda"):
     """Paged pools drawn on the device (bf16 N(0,1) everywhere), page table
     from a random permutation; lens is a host list of cached lengths."""
