@@ -1033,23 +1033,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 
             // ---- outputs O^T += V^T . P^T
             if constexpr (F8) {
-              // V^T from byte pairs of two key rows: for dims 4f..4f+3 (f = lane / 4)
-              // of 32-dim block p, keys 2c, 2c + 1, 2c + 8, 2c + 9 (c = lane % 4).
-              // The A rows of m-tile 2p + e are dims 4f + 2e (row f) and 4f + 2e + 1
-              // (row f + 8); the outputs are put back in order when stored.
+              // V^T from E4M3 rows: the transposing load of 16 keys x 32 bytes
+              // (the bf16 path's offsets) gives each lane, per 8x8 b16 matrix,
+              // dims 2f, 2f + 1 (f = lane / 4) of keys 2c, 2c + 1 (c = lane % 4);
+              // one byte permute makes key pairs per dim, widened exactly to
+              // fp16. The A rows of m-tile mt are dims 16 mt + 2f (row f) and
+              // 16 mt + 2f + 1 (row f + 8); the outputs are put back in order
+              // when stored.
 #pragma unroll
               for (int pj = 0; pj < KSTEPS / 2; ++pj) {
-                uint32_t w[4];
+                uint32_t af[4];
+                ldsm_x4_t(vbase + (pj >> 2) * kBoxBytes + voff[pj & 3], af);
+                uint32_t kp[4];
 #pragma unroll
-                for (int kr = 0; kr < 4; ++kr) {
-                  const int r = 2 * (lane & 3) + (kr & 1) + 8 * (kr >> 1);
-                  const int chunk = (2 * (pj & 3) + (fg >> 2)) ^ (r & 7);
-                  w[kr] = ld_shared_u32(vbase + (pj >> 2) * kBoxBytes + r * 128 + chunk * 16 + 4 * (fg & 3));
-                }
-                const uint32_t lo01 = prmt(w[0], w[1], 0x5140u), hi01 = prmt(w[0], w[1], 0x7362u);
-                const uint32_t lo89 = prmt(w[2], w[3], 0x5140u), hi89 = prmt(w[2], w[3], 0x7362u);
-                const uint32_t a0[4] = {e4m3x2_lo(lo01), e4m3x2_hi(lo01), e4m3x2_lo(lo89), e4m3x2_hi(lo89)};
-                const uint32_t a1[4] = {e4m3x2_lo(hi01), e4m3x2_hi(hi01), e4m3x2_lo(hi89), e4m3x2_hi(hi89)};
+                for (int x = 0; x < 4; ++x) kp[x] = prmt(af[x], 0u, 0x3120u);
+                // matrices: 0 = keys 0-7 / dims 0-15, 1 = keys 0-7 / dims 16-31,
+                // 2 = keys 8-15 / dims 0-15, 3 = keys 8-15 / dims 16-31
+                const uint32_t a0[4] = {e4m3x2_lo(kp[0]), e4m3x2_hi(kp[0]), e4m3x2_lo(kp[2]), e4m3x2_hi(kp[2])};
+                const uint32_t a1[4] = {e4m3x2_lo(kp[1]), e4m3x2_hi(kp[1]), e4m3x2_lo(kp[3]), e4m3x2_hi(kp[3])};
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
                   mma_f16(o[2 * pj][t], a0, pb[t][0], pb[t][1]);
@@ -1114,7 +1115,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
               v = o[mt][0][i] + o[mt][NT - 1][i];
             }
             // (E4M3 V: its m-tiles hold permuted dims, and its values its scale)
-            const int dim = F8 ? 32 * (mt >> 1) + 4 * fg + 2 * (mt & 1) + (i >> 1) : mt * 16 + fg + 8 * (i >> 1);
+            const int dim = F8 ? mt * 16 + 2 * fg + (i >> 1) : mt * 16 + fg + 8 * (i >> 1);
             if (writer) os[(hbase + (i & 1)) * D + dim] = F8 ? v * a.v_scale : v;
           }
         fence_proxy_async_smem();  // the buffer is refilled by TMA after the merge
