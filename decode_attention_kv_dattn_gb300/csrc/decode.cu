@@ -84,6 +84,10 @@ constexpr int64_t kPrefetchLines = 1 << 15;  // largest page table (128-byte lin
 #define DATTN_SEGMENT_COST 12
 #endif
 constexpr int kSegmentCost = DATTN_SEGMENT_COST;
+#ifndef DATTN_MERGE_BATCH
+#define DATTN_MERGE_BATCH 8
+#endif
+constexpr int kMergeBatch = DATTN_MERGE_BATCH;  // partials read per round trip by a unit's final merge
 // Largest excess (percent) of the biggest piece over a fair share of the tiles
 // for which the split cuts every unit into equal pieces instead of stream-K.
 #ifndef DATTN_PIECES_SLACK
@@ -544,10 +548,12 @@ __device__ void end_segment(const DecodeArgs& a, const Split& sp, int pieces, in
   };
   const int stride = GP * (D + 2);
   finish_unit<D, GP, PAGED, NTH>(a, u, slot, t, [&](int g, int d, Merge8& mg) {
-    for (int k0 = 0; k0 < S; k0 += 4) {
-      float m[4], l[4], x[4][8];
+    // kMergeBatch partials' loads in flight at a time: a long stream's last
+    // segment merges ~76 of them, and each batch is one L2 round trip
+    for (int k0 = 0; k0 < S; k0 += kMergeBatch) {
+      float m[kMergeBatch], l[kMergeBatch], x[kMergeBatch][8];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < kMergeBatch; ++q) {
         const int k = k0 + q;
         m[q] = -INFINITY;
         l[q] = 0.f;
@@ -564,7 +570,7 @@ __device__ void end_segment(const DecodeArgs& a, const Split& sp, int pieces, in
         }
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) mg.add(m[q], l[q], x[q]);
+      for (int q = 0; q < kMergeBatch; ++q) mg.add(m[q], l[q], x[q]);
     }
   });
   if (t == 0) a.counters[u] = 0;
