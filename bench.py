@@ -526,7 +526,8 @@ class _Rope:
         self.rotary_dim, self.theta = rotary_dim, theta
 
 
-WORKLOADS = ("hybrid", "sliding", "paged", "verify", "verify_sliding", "long1m", "long262k")
+WORKLOADS = ("hybrid", "sliding", "paged", "verify", "verify_sliding", "long1m", "long262k",
+             "fp8_paged", "fp8_long128k_b8", "fp8_long262k")
 
 
 def make_workload(name, seed, args):

@@ -69,9 +69,16 @@ namespace dattn {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kWarps = 4;                // streaming warps
-constexpr int kHelper = kWarps;          // the helper warp's index
-constexpr int kThreads = (kWarps + 1) * 32;
+// Streaming warps of a kernel variant: 4 with 16 KB stage tiles, or 7 with
+// 8 KB tiles for E4M3 at D = 256, so that every SM sub-partition runs two
+// warps (7 streaming + the helper; 255 registers a thread still fit each
+// sub-partition's register file) that hide one another's conversion chains:
+// 128k x 8 streams 241 -> 230 us per call. At D = 128 the same split measured
+// slower (bf16 paged batch 106 -> 121 us, E4M3 133 -> 149 us).
+template <int D, int NT, bool F8>
+constexpr int stream_warps() {
+  return (F8 && D == 256) ? 7 : 4;
+}
 constexpr int kMaxUnits = 512;           // (stream, KV head) units per call
 constexpr int kGroup = 16;               // keys per MMA group
 constexpr int kBoxBytes = kGroup * 128;  // one TMA box: 16 rows x 64 bf16
@@ -102,33 +109,35 @@ constexpr bool kGroupBox = D == 128;
 
 template <int D, int NT, bool F8 = false>
 struct Geo {
+  static constexpr int W = stream_warps<D, NT, F8>();  // streaming warps; the helper is warp W
+  static constexpr int THREADS = (W + 1) * 32;
   static constexpr int GP = 4 * NT;                  // heads per partial slot
   static constexpr int KSTEPS = D / 16;              // MMA k-steps of a score, m-tiles of an output
   static constexpr int ROWB = F8 ? D : 2 * D;        // bytes of one cached row (bf16, or E4M3)
   static constexpr int BOXES = ROWB / 128;           // 128-byte boxes per 16-row group of K (or V)
   static constexpr int GBYTES = BOXES * kBoxBytes;   // K (or V) bytes of one group
-  static constexpr int KG = 512 / ROWB;              // groups per stage tile (16 KB of K and V)
+  static constexpr int KG = (W > 4 ? 4096 : 8192) / (16 * ROWB);  // groups per stage tile (8 or 16 KB of K and V)
   static constexpr int KHALF = KG * GBYTES;          // K part of a stage; V follows
   static constexpr int STAGE = 2 * KHALF;
   static constexpr int NS = 3;
-  // mbarriers: [kWarps][NS] stages, 2 input slots, then the four hand-offs
+  // mbarriers: [W][NS] stages, 2 input slots, then the four hand-offs
   // between the streaming warps and the helper
-  static constexpr int NBAR = kWarps * NS + 2 + 4;
+  static constexpr int NBAR = W * NS + 2 + 4;
   // offsets from the 1024-byte aligned base of dynamic shared memory
-  static constexpr int BAR_OFF = kWarps * NS * STAGE;
-  static constexpr int INBAR_OFF = BAR_OFF + kWarps * NS * 8;
+  static constexpr int BAR_OFF = W * NS * STAGE;
+  static constexpr int INBAR_OFF = BAR_OFF + W * NS * 8;
   static constexpr int PREP_FULL_OFF = INBAR_OFF + 16;   // q of the next segment is in qs
   static constexpr int PREP_EMPTY_OFF = INBAR_OFF + 24;  // every streaming warp has read qs
   static constexpr int MERGE_FULL_OFF = INBAR_OFF + 32;  // every warp's state is in its buffer
   static constexpr int MERGE_EMPTY_OFF = INBAR_OFF + 40; // the helper has read the states
-  static constexpr int ML_OFF = BAR_OFF + NBAR * 8;               // float [kWarps][2*GP]
-  static constexpr int SLOT_OFF = ML_OFF + kWarps * 2 * GP * 4;   // int [kWarps]
-  static constexpr int FLAG_OFF = SLOT_OFF + kWarps * 4;          // int: "this CTA combines"
+  static constexpr int ML_OFF = BAR_OFF + NBAR * 8;               // float [W][2*GP]
+  static constexpr int SLOT_OFF = ML_OFF + W * 2 * GP * 4;   // int [W]
+  static constexpr int FLAG_OFF = SLOT_OFF + W * 4;          // int: "this CTA combines"
   static constexpr int CS_OFF = (FLAG_OFF + 4 + 15) / 16 * 16;    // float2 [D/2]: cos, sin
   static constexpr int QS_OFF = CS_OFF + D / 2 * 8;               // float [GP][D]: rotated q
-  static constexpr int WROW_OFF = QS_OFF + GP * D * 4;            // int [kWarps][2][kWin*KG]
-  static constexpr int WMASK_OFF = WROW_OFF + kWarps * 2 * kWin * KG * 4;
-  static constexpr int STEP_OFF = WMASK_OFF + kWarps * 2 * kWin * KG * 4;  // uint64 [D/2]: RoPE steps
+  static constexpr int WROW_OFF = QS_OFF + GP * D * 4;            // int [W][2][kWin*KG]
+  static constexpr int WMASK_OFF = WROW_OFF + W * 2 * kWin * KG * 4;
+  static constexpr int STEP_OFF = WMASK_OFF + W * 2 * kWin * KG * 4;  // uint64 [D/2]: RoPE steps
   // input slot: q [GP][D] bf16, k_new [D], v_new [D] (one bulk copy each),
   // then the new token worked out from them: K entry [D] bf16, scores [GP],
   // sigmoid(gate) [GP]
@@ -399,10 +408,11 @@ __device__ __forceinline__ void finish_unit(const DecodeArgs& a, int u, const ui
 
 // The streaming warps' states of one segment (merge buffers: warp w's stage
 // SLOT[w], or none when SLOT[w] < 0) folded into mg for head g, dims d..d+7.
-template <int D, int NT>
+template <int D, int NT, bool F8>
 __device__ __forceinline__ void fold_warps(const uint8_t* smem, const float* ML, const int* SLOT, int g, int d,
                                            Merge8& mg) {
-  using Gm = Geo<D, NT>;
+  using Gm = Geo<D, NT, F8>;
+  constexpr int kWarps = Gm::W;
   constexpr int GP = Gm::GP;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) {
@@ -419,10 +429,11 @@ __device__ __forceinline__ void fold_warps(const uint8_t* smem, const float* ML,
 // The streaming warps' states of one segment merged into the partial slot
 // dst: o[GP][D] (relative to the merged maximum), then m[GP], l[GP]. No
 // barrier at the end.
-template <int D, int NT, int NTH>
+template <int D, int NT, bool F8, int NTH>
 __device__ __forceinline__ void write_partial(const uint8_t* smem, const float* ML, const int* SLOT, float* dst,
                                               int t) {
-  using Gm = Geo<D, NT>;
+  using Gm = Geo<D, NT, F8>;
+  constexpr int kWarps = Gm::W;
   constexpr int GP = Gm::GP;
   for (int e = t * 8; e < GP * D; e += NTH * 8) {
     const int h = e / D;
@@ -494,7 +505,7 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, int u, int n, u
 // segment's partial slot, and the CTA finishing the unit's last segment (a
 // per-unit counter) merges all of its partials. `release()` runs once the
 // merge buffers have been read; `wait_prev()` before the first output store.
-template <int D, int NT, bool PAGED, int NTH, typename WaitPrev, typename Release>
+template <int D, int NT, bool PAGED, bool F8, int NTH, typename WaitPrev, typename Release>
 __device__ void end_segment(const DecodeArgs& a, const Split& sp, int pieces, int u, bool first_seg, int cta,
                             const uint8_t* smem, const float* ML, const int* SLOT, const uint8_t* slot, int* flag,
                             int t, WaitPrev wait_prev, Release release) {
@@ -513,14 +524,14 @@ __device__ void end_segment(const DecodeArgs& a, const Split& sp, int pieces, in
     // the whole unit lies in this CTA: the warps' states go straight into the output
     wait_prev();
     finish_unit<D, GP, PAGED, NTH>(a, u, slot, t, [&](int g, int d, Merge8& mg) {
-      fold_warps<D, NT>(smem, ML, SLOT, g, d, mg);
+      fold_warps<D, NT, F8>(smem, ML, SLOT, g, d, mg);
     });
     team_sync<NTH>();
     release();
     return;
   }
   const int pslot = first_seg ? cta : NC + u;
-  write_partial<D, NT, NTH>(smem, ML, SLOT, a.part + static_cast<int64_t>(pslot) * (GP * (D + 2)), t);
+  write_partial<D, NT, F8, NTH>(smem, ML, SLOT, a.part + static_cast<int64_t>(pslot) * (GP * (D + 2)), t);
   __threadfence();
   team_sync<NTH>();
   release();
@@ -578,8 +589,9 @@ __device__ void end_segment(const DecodeArgs& a, const Split& sp, int pieces, in
 }
 
 template <int D, int NT, bool PAGED, bool F8>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeArgs a) {
+__global__ void __launch_bounds__(Geo<D, NT, F8>::THREADS, 1) decode_kernel(const __grid_constant__ DecodeArgs a) {
   using Gm = Geo<D, NT, F8>;
+  constexpr int kWarps = Gm::W, kHelper = Gm::W, kThreads = Gm::THREADS;
   constexpr int GP = Gm::GP, KSTEPS = Gm::KSTEPS, BOXES = Gm::BOXES, KG = Gm::KG, NS = Gm::NS;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int warp_max[kThreads / 32];
@@ -1201,7 +1213,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       prep(seg + 1);
       // this segment's end
       if (!failed) check(mbar_wait_bounded(merge_full, seg & 1, a.wait_ns));
-      end_segment<D, NT, PAGED, 32>(a, sp, pieces, u, seg == 0, cta, smem, ML, SLOT,
+      end_segment<D, NT, PAGED, F8, 32>(a, sp, pieces, u, seg == 0, cta, smem, ML, SLOT,
                                     in_slots + (seg & 1) * Gm::IN_BYTES, flag, lane, wait_prev, [&] {
                                       fence_proxy_async_smem();
                                       __syncwarp();
@@ -1218,7 +1230,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   __syncthreads();
   if (u_last < U) {
     const int sl = n_segs - 1;
-    end_segment<D, NT, PAGED, kThreads>(a, sp, pieces, u_last, sl == 0, cta, smem, ML, SLOT,
+    end_segment<D, NT, PAGED, F8, kThreads>(a, sp, pieces, u_last, sl == 0, cta, smem, ML, SLOT,
                                         in_slots + (sl & 1) * Gm::IN_BYTES, flag, threadIdx.x, wait_prev, [] {});
   }
 
@@ -1258,10 +1270,10 @@ cudaError_t decode_launch(const DecodeArgs& a, int ctas, cudaStream_t s, bool pd
   if (e != cudaSuccess) return e;
   const size_t smem = 1024 + Gm::TAB_OFF + (4 * a.B * a.Hkv + 1) * sizeof(int);
   if (!pdl) {
-    k<<<ctas, kThreads, smem, s>>>(a);
+    k<<<ctas, Gm::THREADS, smem, s>>>(a);
     return cudaGetLastError();
   }
-  return launch_pdl(k, dim3(ctas), dim3(kThreads), smem, s, a);
+  return launch_pdl(k, dim3(ctas), dim3(Gm::THREADS), smem, s, a);
 }
 
 template <int D, int NT, bool F8>
@@ -1404,9 +1416,18 @@ cudaError_t launch_decode(const DecodeArgs& args, int D, int ctas, cudaStream_t 
   return decode_dispatch<false>(a, D, GP, ctas, s, pdl);
 }
 
+// Keys of one round of stage tiles over the streaming warps, in units of 4
+// tiles (the grid plan gives each CTA at least one round).
 int decode_tile_keys(int D, int G, bool f8) {
-  if (decode_group_pad(G) == 0 || (D != 128 && D != 256)) return 0;
-  return (f8 ? 512 : 256) / D * kGroup;
+  const int GP = decode_group_pad(G);
+  if (GP == 0 || (D != 128 && D != 256)) return 0;
+  auto keys = [](int kg, int w) { return kGroup * kg * w / 4; };
+  if (D == 256) {
+    if (f8) return GP == 4 ? keys(Geo<256, 1, true>::KG, Geo<256, 1, true>::W) : keys(Geo<256, 2, true>::KG, Geo<256, 2, true>::W);
+    return GP == 4 ? keys(Geo<256, 1>::KG, Geo<256, 1>::W) : keys(Geo<256, 2>::KG, Geo<256, 2>::W);
+  }
+  if (f8) return GP == 4 ? keys(Geo<128, 1, true>::KG, Geo<128, 1, true>::W) : keys(Geo<128, 2, true>::KG, Geo<128, 2, true>::W);
+  return GP == 4 ? keys(Geo<128, 1>::KG, Geo<128, 1>::W) : keys(Geo<128, 2>::KG, Geo<128, 2>::W);
 }
 
 int decode_ctas_per_sm(int D, int G) {
