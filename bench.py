@@ -618,7 +618,8 @@ def survey_workloads(peak, steps=10, warmup=3, names=None):
                  "us_per_step": t / steps * 1e6,
                  "l2": "flushed before each step" if step.flush_l2 else "step larger than L2",
                  "roofline": {"bound": "hbm", "kernel": step.kernel, "achieved": achieved, "peak": peak,
-                              "unit": "GB/s", "frac": achieved / peak, "us_per_call": t_dom * 1e6},
+                              "unit": "GB/s", "frac": achieved / peak, "us_per_call": t_dom * 1e6,
+                              "traffic": recorded_traffic(name)},
                  "config": step.config}
         out[name] = entry
         del step
