@@ -79,6 +79,15 @@ template <int D, int NT, bool F8>
 constexpr int stream_warps() {
   return (F8 && D == 256) ? 7 : 4;
 }
+// Stage tiles per streaming warp, and bytes of K and V in one stage tile.
+template <int D, int NT, bool F8>
+constexpr int stage_count() {
+  return 3;
+}
+template <int D, int NT, bool F8>
+constexpr int stage_bytes() {
+  return stream_warps<D, NT, F8>() > 4 ? 8192 : 16384;
+}
 constexpr int kMaxUnits = 512;           // (stream, KV head) units per call
 constexpr int kGroup = 16;               // keys per MMA group
 constexpr int kBoxBytes = kGroup * 128;  // one TMA box: 16 rows x 64 bf16
@@ -116,10 +125,10 @@ struct Geo {
   static constexpr int ROWB = F8 ? D : 2 * D;        // bytes of one cached row (bf16, or E4M3)
   static constexpr int BOXES = ROWB / 128;           // 128-byte boxes per 16-row group of K (or V)
   static constexpr int GBYTES = BOXES * kBoxBytes;   // K (or V) bytes of one group
-  static constexpr int KG = (W > 4 ? 4096 : 8192) / (16 * ROWB);  // groups per stage tile (8 or 16 KB of K and V)
+  static constexpr int KG = stage_bytes<D, NT, F8>() / (2 * 16 * ROWB);  // groups per stage tile
   static constexpr int KHALF = KG * GBYTES;          // K part of a stage; V follows
   static constexpr int STAGE = 2 * KHALF;
-  static constexpr int NS = 3;
+  static constexpr int NS = stage_count<D, NT, F8>();
   // mbarriers: [W][NS] stages, 2 input slots, then the four hand-offs
   // between the streaming warps and the helper
   static constexpr int NBAR = W * NS + 2 + 4;
@@ -152,6 +161,7 @@ struct Geo {
   static constexpr int TAB_OFF = IN_OFF + 2 * IN_BYTES;
   static constexpr int SMEM_MAX = 1024 + TAB_OFF + (4 * kMaxUnits + 1) * 4;  // P, N, ring head/row
   static_assert(D == 128 || D == 256, "head_dim");
+  static_assert(KG >= 1 && KG * 2 * 16 * ROWB == STAGE, "a stage tile holds whole 16-row groups");
   static_assert(GP * D * 4 <= STAGE, "a stage buffer holds one warp's partial output");
   static_assert(NS < kWin, "issue runs at most one window ahead");
   static_assert(SMEM_MAX <= 232448, "shared memory per CTA");
