@@ -717,7 +717,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_split_kernel(const __grid
 // ---------------------------------------------------------------- combine
 
 template <int D>
-__global__ void __launch_bounds__(256) verify_combine_kernel(const VerifyCombineArgs a) {
+__global__ void __launch_bounds__(256, 6) verify_combine_kernel(const VerifyCombineArgs a) {
   constexpr int EPL = D / 32;  // dims per lane
   __shared__ int par_s[16];
   __shared__ int path_s[16];
@@ -779,39 +779,64 @@ __global__ void __launch_bounds__(256) verify_combine_kernel(const VerifyCombine
       q[e] = x.x; q[e + 1] = x.y; q[e + 2] = x.z; q[e + 3] = x.w;
     }
   }
+  // path nodes four at a time: their rows' loads go out together (the
+  // scores stay in registers: every index below is a compile-time one)
+  constexpr int kPathBatch = 4;
   float sw[16];
   float M = -INFINITY;
-#pragma unroll 1
-  for (int p = 0; p < np; ++p) {
-    const uint16_t* kp = a.khat + ((static_cast<int64_t>(s) * T + path_s[p]) * Hkv + j) * D + lane * EPL;
-    float dot = 0.f;
 #pragma unroll
-    for (int e = 0; e < EPL; e += 2) {
-      const uint32_t w = *reinterpret_cast<const uint32_t*>(kp + e);
-      dot = fmaf(q[e], bf16_lo(w), dot);
-      dot = fmaf(q[e + 1], bf16_hi(w), dot);
+  for (int p0 = 0; p0 < 16; p0 += kPathBatch) {
+    if (p0 >= np) break;
+    uint32_t kw[kPathBatch][EPL / 2];
+#pragma unroll
+    for (int b = 0; b < kPathBatch; ++b) {
+      if (p0 + b >= np) break;
+      const uint16_t* kp = a.khat + ((static_cast<int64_t>(s) * T + path_s[p0 + b]) * Hkv + j) * D + lane * EPL;
+#pragma unroll
+      for (int e = 0; e < EPL; e += 2) kw[b][e / 2] = *reinterpret_cast<const uint32_t*>(kp + e);
     }
 #pragma unroll
-    for (int w = 16; w >= 1; w >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, w);
-    sw[p] = dot;
-    M = fmaxf(M, dot);
+    for (int b = 0; b < kPathBatch; ++b) {
+      if (p0 + b >= np) break;
+      float dot = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPL; e += 2) {
+        dot = fmaf(q[e], bf16_lo(kw[b][e / 2]), dot);
+        dot = fmaf(q[e + 1], bf16_hi(kw[b][e / 2]), dot);
+      }
+#pragma unroll
+      for (int w = 16; w >= 1; w >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, w);
+      sw[p0 + b] = dot;
+      M = fmaxf(M, dot);
+    }
   }
   float acc[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
   float L = 0.f;  // relative to M
-#pragma unroll 1
-  for (int p = 0; p < np; ++p) {
-    const float w = exp2_fast(sw[p] - M);
-    L += w;
-    if (!stored) break;  // (its ancestors may lie past the caller's rows)
-    const uint16_t* vp =
-        a.v + ((static_cast<int64_t>(s) * a.in_T + a.row0 + path_s[p]) * Hkv + j) * D + lane * EPL;
 #pragma unroll
-    for (int e = 0; e < EPL; e += 2) {
-      const uint32_t x = *reinterpret_cast<const uint32_t*>(vp + e);
-      acc[e] = fmaf(w, bf16_lo(x), acc[e]);
-      acc[e + 1] = fmaf(w, bf16_hi(x), acc[e + 1]);
+  for (int p0 = 0; p0 < 16; p0 += kPathBatch) {
+    if (p0 >= np) break;
+    uint32_t vw[kPathBatch][EPL / 2];
+#pragma unroll
+    for (int b = 0; b < kPathBatch; ++b) {
+      if (p0 + b >= np || !stored) break;  // (a stored row's ancestors lie within the caller's rows)
+      const uint16_t* vp =
+          a.v + ((static_cast<int64_t>(s) * a.in_T + a.row0 + path_s[p0 + b]) * Hkv + j) * D + lane * EPL;
+#pragma unroll
+      for (int e = 0; e < EPL; e += 2) vw[b][e / 2] = *reinterpret_cast<const uint32_t*>(vp + e);
+    }
+#pragma unroll
+    for (int b = 0; b < kPathBatch; ++b) {
+      if (p0 + b >= np) break;
+      const float w = exp2_fast(sw[p0 + b] - M);
+      L += w;
+      if (!stored) continue;
+#pragma unroll
+      for (int e = 0; e < EPL; e += 2) {
+        acc[e] = fmaf(w, bf16_lo(vw[b][e / 2]), acc[e]);
+        acc[e + 1] = fmaf(w, bf16_hi(vw[b][e / 2]), acc[e + 1]);
+      }
     }
   }
 
