@@ -17,10 +17,12 @@
 
 #include <stdint.h>
 
+#if !defined(DATTN_HD)
 #if defined(__CUDACC__)
 #define DATTN_HD __host__ __device__ __forceinline__
 #else
 #define DATTN_HD inline
+#endif
 #endif
 
 namespace dattn {

@@ -60,8 +60,8 @@
 //    rescaled only when some head's running maximum moved.
 #include "bf16_exact.h"
 #include "common.cuh"
-#include "e4m3.cuh"
 #include "qk_norm.cuh"
+#include "round_f64.h"
 #include "mma.cuh"
 
 namespace dattn {

@@ -14,30 +14,9 @@
 #include <cstdint>
 
 #include "common.cuh"
+#include "round_f64.h"
 
 namespace dattn {
-
-// The bf16 nearest to y (ties to even), in one rounding from fp64.
-__device__ __forceinline__ uint16_t bf16_from_f64(double y) {
-  const unsigned long long b = static_cast<unsigned long long>(__double_as_longlong(y));
-  const uint16_t sign = static_cast<uint16_t>((b >> 48) & 0x8000u);
-  const int e = static_cast<int>((b >> 52) & 0x7ff);
-  const unsigned long long m = b & 0xfffffffffffffull;
-  if (e == 0x7ff) return m ? 0x7fc0 : static_cast<uint16_t>(sign | 0x7f80u);
-  const double a = fabs(y);
-  if (a < 0x1p-126) {
-    // bf16 subnormals are the multiples of 2^-133; 128 of them is the
-    // smallest normal, whose encoding is 128 as well
-    const double q = rint(a * 0x1p133);
-    return static_cast<uint16_t>(sign | static_cast<uint16_t>(q));
-  }
-  const uint32_t keep = static_cast<uint32_t>(m >> 45);
-  const unsigned long long rem = m & ((1ull << 45) - 1);
-  uint32_t v = (static_cast<uint32_t>(e - 1023 + 127) << 7) | keep;
-  if (rem > (1ull << 44) || (rem == (1ull << 44) && (keep & 1u))) ++v;
-  if (v >= 0x7f80u) v = 0x7f80u;  // past the largest finite value: infinity
-  return static_cast<uint16_t>(sign | v);
-}
 
 // 1 / sqrt(mean(x^2) + eps) of one head vector x[0, D), by one warp: a
 // lane-strided sum, then a butterfly, after which every lane holds the same

@@ -16,9 +16,9 @@
 #include <cuda_fp16.h>
 
 #include "bf16_exact.h"
-#include "e4m3.cuh"
 #include "common.cuh"
 #include "qk_norm.cuh"
+#include "round_f64.h"
 
 namespace dattn {
 
