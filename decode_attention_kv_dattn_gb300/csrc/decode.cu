@@ -172,23 +172,24 @@ struct Geo {
 template <bool PAGED>
 __device__ __forceinline__ int unit_length(const CacheView& c, int b, int max_len, bool report,
                                            int* err) {
-  if constexpr (PAGED) {
-    int n = c.seq_len[b];
-    const int cap = min(max_len, c.bt_stride * c.P);
-    if (n < 0 || n > cap) {
-      if (report) raise_error(err, ERR_LENGTH);
-      n = n < 0 ? 0 : cap;
-    }
-    return n;
-  } else {
-    const int row = c.stream_rows ? c.stream_rows[b] : b;
-    const int head = c.ring_head[b], cnt = c.ring_count[b];
-    if (row < 0 || row >= c.n_rows || head < 0 || head >= c.R || cnt < 0 || cnt > c.R) {
-      if (report) raise_error(err, ERR_INDEX);
-      return 0;
-    }
-    return cnt;
+  static_assert(PAGED, "ring units: ring_length");
+  int n = c.seq_len[b];
+  const int cap = min(max_len, c.bt_stride * c.P);
+  if (n < 0 || n > cap) {
+    if (report) raise_error(err, ERR_LENGTH);
+    n = n < 0 ? 0 : cap;
   }
+  return n;
+}
+
+// Valid slots of a ring from its metadata (cache row, head slot, count): 0,
+// and an index error, when any of them is out of range.
+__device__ __forceinline__ int ring_length(const CacheView& c, int row, int head, int cnt, bool report, int* err) {
+  if (row < 0 || row >= c.n_rows || head < 0 || head >= c.R || cnt < 0 || cnt > c.R) {
+    if (report) raise_error(err, ERR_INDEX);
+    return 0;
+  }
+  return cnt;
 }
 
 // First slot of a ring holding `n` valid slots before `head`.
@@ -196,23 +197,12 @@ __device__ __forceinline__ int ring_start(int head, int n, int R) {
   return head - n < 0 ? head - n + R : head - n;
 }
 
-// 16-row groups of a unit with n cached keys (`head` is the ring head).
-template <bool PAGED>
-__device__ __forceinline__ int unit_groups(const CacheView& c, int head, int n) {
+// 16-row groups of a paged unit with n cached keys.
+__device__ __forceinline__ int paged_groups(const CacheView& c, int n) {
   if (n <= 0) return 0;
-  if constexpr (PAGED) {
-    (void)head;
-    const int gpp = (c.P + kGroup - 1) / kGroup;
-    const int full = n / c.P, rest = n - full * c.P;
-    return full * gpp + (rest + kGroup - 1) / kGroup;
-  } else {
-    const int R = c.R, nb = (R + kGroup - 1) / kGroup;
-    if (n >= R) return nb;
-    const int start = ring_start(head, n, R);
-    const int b0 = start >> 4, end = start + n - 1;
-    if (end < R) return (end >> 4) - b0 + 1;
-    return min(nb, nb - b0 + ((end - R) >> 4) + 1);  // wraps past the last slot
-  }
+  const int gpp = (c.P + kGroup - 1) / kGroup;
+  const int full = n / c.P, rest = n - full * c.P;
+  return full * gpp + (rest + kGroup - 1) / kGroup;
 }
 
 // Bits r of the valid rows [lo, hi) of a 16-row group (empty when hi <= lo).
@@ -652,20 +642,21 @@ __global__ void __launch_bounds__(Geo<D, NT, F8>::THREADS, 1) decode_kernel(cons
     fence_mbar_init();
   }
 
-  // ---- unit table from caller metadata (no kernel of this library writes
-  // it): tiles per unit, then their prefix sum
+  // ---- unit table: tiles per unit, then their prefix sum. A paged unit's
+  // tiles follow from its length (caller metadata; no kernel of this library
+  // writes it). A ring unit scans every 16-slot block of its ring, the valid
+  // slots masked in when scored, so a ring layer's split needs none of its
+  // metadata and its first copies go out before that metadata is read.
+  const int ring_tiles = PAGED ? 0 : ((c.R + kGroup - 1) / kGroup + KG - 1) / KG;
   int max_tiles = 0;
   for (int u = threadIdx.x; u < U; u += kThreads) {
-    const int b = u / Hkv;
-    const int n = unit_length<PAGED>(c, b, a.max_len, cta == 0 && u - b * Hkv == 0, a.err);
-    int head = 0;
-    if constexpr (!PAGED) {
-      head = n > 0 ? c.ring_head[b] : 0;
-      HD[u] = head;
-      RW[u] = c.stream_rows ? c.stream_rows[b] : b;
+    int tiles = ring_tiles;
+    if constexpr (PAGED) {
+      const int b = u / Hkv;
+      const int n = unit_length<true>(c, b, a.max_len, cta == 0 && u - b * Hkv == 0, a.err);
+      N[u] = n;
+      tiles = (paged_groups(c, n) + KG - 1) / KG;
     }
-    N[u] = n;
-    const int tiles = (unit_groups<PAGED>(c, head, n) + KG - 1) / KG;
     P[u + 1] = tiles;
     max_tiles = max(max_tiles, tiles);
   }
@@ -757,7 +748,7 @@ __global__ void __launch_bounds__(Geo<D, NT, F8>::THREADS, 1) decode_kernel(cons
         const int n = N[u];
         if constexpr (PAGED) {
           const int gpp = (c.P + kGroup - 1) / kGroup;
-          const int groups = unit_groups<true>(c, 0, n);
+          const int groups = paged_groups(c, n);
 #pragma unroll
           for (int kg = 0; kg < KG; ++kg) {
             const int gi = (g - P[u]) * KG + kg;
@@ -773,17 +764,16 @@ __global__ void __launch_bounds__(Geo<D, NT, F8>::THREADS, 1) decode_kernel(cons
             }
           }
         } else {
+          // block gi of the ring: slots 16 gi .. 16 gi + 15, valid when they are
+          // among the n slots before the head
           const int R = c.R, nb = (R + kGroup - 1) / kGroup;
           const int head = HD[u], row = RW[u];
-          const int groups = unit_groups<false>(c, head, n);
           const int start = ring_start(head, n, R), end = start + n;  // valid: [start, end) mod R
 #pragma unroll
           for (int kg = 0; kg < KG; ++kg) {
             const int gi = (g - P[u]) * KG + kg;
-            if (gi < groups) {
-              int pb = (start >> 4) + gi;
-              if (pb >= nb) pb -= nb;
-              const int s0 = pb * kGroup;
+            if (gi < nb) {
+              const int s0 = gi * kGroup;
               rows[kg] = (row * Hkv + j) * R + s0;
               uint32_t m = row_bits(start - s0, min(end, R) - s0);
               if (end > R) m |= row_bits(-s0, end - R - s0);
@@ -801,14 +791,28 @@ __global__ void __launch_bounds__(Geo<D, NT, F8>::THREADS, 1) decode_kernel(cons
       }
       __syncwarp();
     };
-    fill(0);  // window 1 is filled once the first tiles are requested
-
     const uint64_t policy = l2_evict_first_policy();
     // Stages with copies in flight (bit st, kept by the issuing lane) and the
     // parity of each stage's next wait (bit 8 + st): a warp that gave up
     // waiting still lets its copies land before the CTA exits.
     uint32_t copies = 0;
-    // Request tile x of this warp into stage x % NS (one lane).
+    // The K and V rows of group kg of a stage from tensor row row0 on.
+    auto load_group = [&](uint32_t kd, int kg, int row0, uint32_t bar) {
+      if constexpr (kGroupBox<D> || F8) {
+        // one box per group: 16 rows x every 128-byte region
+        tma_load_3d(kd + kg * Gm::GBYTES, &a.tmap_k, 0, row0, 0, bar, policy);
+        tma_load_3d(kd + Gm::KHALF + kg * Gm::GBYTES, &a.tmap_v, 0, row0, 0, bar, policy);
+      } else {
+        // one box per 64-dim region of the group
+#pragma unroll
+        for (int bx = 0; bx < BOXES; ++bx) {
+          tma_load_2d(kd + kg * Gm::GBYTES + bx * kBoxBytes, &a.tmap_k, 64 * bx, row0, bar, policy);
+          tma_load_2d(kd + Gm::KHALF + kg * Gm::GBYTES + bx * kBoxBytes, &a.tmap_v, 64 * bx, row0, bar, policy);
+        }
+      }
+    };
+    // Request tile x of this warp into stage x % NS (one lane): the groups
+    // that hold a valid row.
     auto issue = [&](int x) {
       copies |= 1u << (x % NS);
       const int* wr = wrow + ((x / kWin) & 1) * kWin * KG + (x % kWin) * KG;
@@ -820,29 +824,74 @@ __global__ void __launch_bounds__(Geo<D, NT, F8>::THREADS, 1) decode_kernel(cons
       const uint32_t kd = wsm_a + (x % NS) * Gm::STAGE;
       mbar_arrive_expect_tx(bar, 2u * gn * Gm::GBYTES);
 #pragma unroll
-      for (int kg = 0; kg < KG; ++kg) {
-        if (kg < gn) {
-          const int row0 = wr[kg];
-          if constexpr (kGroupBox<D> || F8) {
-            // one box per group: 16 rows x every 128-byte region
-            tma_load_3d(kd + kg * Gm::GBYTES, &a.tmap_k, 0, row0, 0, bar, policy);
-            tma_load_3d(kd + Gm::KHALF + kg * Gm::GBYTES, &a.tmap_v, 0, row0, 0, bar, policy);
-          } else {
-            // one box per 64-dim region of the group
+      for (int kg = 0; kg < KG; ++kg)
+        if (wm[kg] != 0) load_group(kd, kg, wr[kg], bar);
+    };
+    const int pre = my_n < NS ? my_n : NS;
+    if constexpr (!PAGED) {
+      // A ring's first NS tiles go out from the split alone, every block of
+      // them whole (the blocks past the ring's last slot are not requested);
+      // which of their rows are valid is known by the time they are scored.
+      // This thread's first unit's ring metadata is requested first, so that
+      // its loads are in flight across the copies.
+      const int um = threadIdx.x;  // (the streaming threads are 0 .. kWarps * 32 - 1)
+      int m_row = 0, m_head = 0, m_cnt = 0;
+      if (um < U) {
+        const int b = um / Hkv;
+        m_row = c.stream_rows ? c.stream_rows[b] : b;
+        m_head = c.ring_head[b];
+        m_cnt = c.ring_count[b];
+      }
+      // Lane x < NS works out tile x's first tensor row (its stream's cache
+      // row loads for all tiles at once); lane 0 issues, once the helper warp
+      // has requested the first units' inputs (their copies then go first).
+      const int nb = (c.R + kGroup - 1) / kGroup;
+      int row0 = 0, gi0 = 0;
+      if (lane < pre) {
+        const int g = g0 + warp + kWarps * lane;
+        const int u = unit_of(P, U, g);
+        const int b = u / Hkv, j = u - b * Hkv;
+        int row = c.stream_rows ? c.stream_rows[b] : b;
+        if (row < 0 || row >= c.n_rows) row = 0;  // (reported below; every slot is masked)
+        gi0 = (g - P[u]) * KG;
+        row0 = (row * Hkv + j) * c.R + gi0 * kGroup;
+      }
+      asm volatile("bar.sync 2, %0;" ::"r"(kThreads) : "memory");
+      for (int x = 0; x < pre; ++x) {
+        const int r0 = __shfl_sync(kFull, row0, x), b0 = __shfl_sync(kFull, gi0, x);
+        if (lane == 0) {
+          copies |= 1u << (x % NS);
+          int gn = 0;
 #pragma unroll
-            for (int bx = 0; bx < BOXES; ++bx) {
-              tma_load_2d(kd + kg * Gm::GBYTES + bx * kBoxBytes, &a.tmap_k, 64 * bx, row0, bar, policy);
-              tma_load_2d(kd + Gm::KHALF + kg * Gm::GBYTES + bx * kBoxBytes, &a.tmap_v, 64 * bx, row0, bar,
-                          policy);
-            }
-          }
+          for (int kg = 0; kg < KG; ++kg) gn += b0 + kg < nb;
+          const uint32_t bar = bar0 + 8 * (x % NS);
+          const uint32_t kd = wsm_a + (x % NS) * Gm::STAGE;
+          mbar_arrive_expect_tx(bar, 2u * gn * Gm::GBYTES);
+#pragma unroll
+          for (int kg = 0; kg < KG; ++kg)
+            if (b0 + kg < nb) load_group(kd, kg, r0 + kg * kGroup, bar);
         }
       }
-    };
-    if (lane == 0) {
-      const int pre = my_n < NS ? my_n : NS;
-      for (int x = 0; x < pre; ++x) issue(x);
+      // then the ring metadata, shared out over the streaming warps (the only
+      // readers: the windows' rows and masks)
+      for (int u = um; u < U; u += kWarps * 32) {
+        const int b = u / Hkv;
+        int row = m_row, head = m_head, cnt = m_cnt;
+        if (u != um) {
+          row = c.stream_rows ? c.stream_rows[b] : b;
+          head = c.ring_head[b];
+          cnt = c.ring_count[b];
+        }
+        const int n = ring_length(c, row, head, cnt, cta == 0 && u - b * Hkv == 0, a.err);
+        HD[u] = n > 0 ? head : 0;
+        RW[u] = row;
+        N[u] = n;
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(kWarps * 32) : "memory");
     }
+    fill(0);  // window 1 is filled once the first tiles are requested
+    if (PAGED && lane == 0)
+      for (int x = 0; x < pre; ++x) issue(x);
 
     // Per-lane ldmatrix offsets inside a group's 2 KB boxes (128-byte swizzle:
     // the 16-byte chunk index is XORed with the row mod 8). K (scores, A = K):
@@ -946,7 +995,7 @@ __global__ void __launch_bounds__(Geo<D, NT, F8>::THREADS, 1) decode_kernel(cons
 #pragma unroll
           for (int kg = 0; kg < KG; ++kg) {
             const uint32_t mask = static_cast<uint32_t>(wm[kg]);
-            if (mask == 0u) break;  // the unit's last tile has fewer groups
+            if (mask == 0u) continue;  // no valid row (past a unit's end, or a ring's unwritten block)
             const uint32_t kbase = wsm_a + stg * Gm::STAGE + kg * Gm::GBYTES;
             const uint32_t vbase = kbase + Gm::KHALF;
             if (mask != 0xffffu) {
@@ -1212,8 +1261,10 @@ __global__ void __launch_bounds__(Geo<D, NT, F8>::THREADS, 1) decode_kernel(cons
       stage(u_first);
       const int u1 = next_unit(u_first);
       if (u1 < U) stage(u1);
-      prep(0);
     }
+    // (a ring layer's streaming warps issue their first copies after this)
+    if constexpr (!PAGED) asm volatile("bar.arrive 2, %0;" ::"r"(kThreads) : "memory");
+    if (u_first < U) prep(0);
     int seg = 0;
     for (int u = u_first; u < U; ++seg) {
       const int un = next_unit(u);
