@@ -17,9 +17,11 @@
 // GB300 design.
 //  * Work split (stream-K). A "unit" is one (stream, KV head). Its cached keys
 //    are visited in groups of 16 rows: 16-row runs of a page (a page of P
-//    rows gives ceil(P / 16) groups), or 16-slot blocks of the ring's physical
-//    slots (only the blocks that hold valid slots; softmax does not care about
-//    the order). A stage tile is 256 / D groups (16 KB of K and V). All units'
+//    rows gives ceil(P / 16) groups), or every 16-slot block of the ring's
+//    physical slots, in slot order (the unwritten slots masked: a ring
+//    layer's split then needs none of its metadata, and its first copies go
+//    out before that metadata has arrived). A stage tile is 256 / D groups
+//    (16 KB of K and V). All units'
 //    tiles are laid end to end and the grid - one CTA per SM - cuts that
 //    sequence into equal contiguous ranges, so every CTA moves the same number
 //    of bytes whatever the mix of lengths. Each piece of a unit inside one CTA
