@@ -30,9 +30,10 @@
  *   - All tensor and index pointers are DEVICE pointers on the handle's GPU,
  *     owned by the caller, dense row-major in the layouts stated below. bf16
  *     data is passed as raw 16-bit patterns. Pointers must be 16-byte aligned.
- *   - Calls are asynchronous on `stream` (NULL = legacy default stream) and
- *     may be captured in a CUDA graph. Calls that share one handle use its
- *     workspace and must be ordered (one stream, or one handle per stream).
+ *   - Calls are asynchronous on `stream` (NULL = legacy default stream); the
+ *     calls that take a handle may be captured in a CUDA graph. Calls that
+ *     share one handle use its workspace and must be ordered (one stream, or
+ *     one handle per stream).
  *   - The return value is a dattn status. Host-side argument checks return
  *     DATTN_EINVAL / DATTN_EXCEEDS / DATTN_EUNSUPPORTED before anything is
  *     launched. Bad device-side metadata (a page id outside the pool, a ring
@@ -309,7 +310,7 @@ DATTN_API void dattn_destroy(dattn_t* h);
  * defines at file scope; every GPU that loads the library holds it until the
  * process exits. Nothing is allocated or freed by this call.
  *   - The first call on a device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ *     that device current).
  *   - A call whose scratch would not fit in 8 MiB returns DATTN_EXCEEDS
  *     (about 1.2 MiB for 64 streams x 2 KV heads x 8 query heads x head_dim
  *     256 on a 152-SM GPU).
