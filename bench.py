@@ -527,7 +527,7 @@ class _Rope:
 
 
 WORKLOADS = ("hybrid", "sliding", "paged", "verify", "verify_sliding", "long1m", "long262k",
-             "fp8_paged", "fp8_long128k_b8", "fp8_long262k")
+             "long128k_b1", "long128k_b8", "long128k_b64", "fp8_paged", "fp8_long128k_b8", "fp8_long262k")
 
 
 def make_workload(name, seed, args):
