@@ -344,11 +344,12 @@ int dattn_create(const dattn_config* cfg, int device, dattn_t** out) {
   h->qhl_rows = static_cast<int>(rows);
   if (cudaMalloc(&h->qhl, 2 * rows * Hq * D * sizeof(uint16_t)) != cudaSuccess) return fail(DATTN_ECUDA);
   if (cudaMalloc(&h->khat, rows * Hkv * D * sizeof(uint16_t)) != cudaSuccess) return fail(DATTN_ECUDA);
-  // Decode partials: one slot per CTA plus one per unit; per-unit counters.
+  // Decode partials: one slot per CTA plus one per unit; per-unit counters,
+  // then one per CTA (the group counters of units merged in two levels).
   if (static_cast<int64_t>(h->max_streams) * Hkv > decode_max_units()) return fail(DATTN_EUNSUPPORTED);
   h->part_units = static_cast<size_t>(h->decode_resident) + static_cast<size_t>(h->max_streams) * Hkv;
   for (int i = 0; i < 2; ++i) {
-    const size_t nc = static_cast<size_t>(h->max_streams) * Hkv;
+    const size_t nc = static_cast<size_t>(h->max_streams) * Hkv + static_cast<size_t>(h->decode_resident);
     if (cudaMalloc(&h->counters[i], nc * sizeof(int)) != cudaSuccess) return fail(DATTN_ECUDA);
     if (cudaMemset(h->counters[i], 0, nc * sizeof(int)) != cudaSuccess) return fail(DATTN_ECUDA);
   }
@@ -415,8 +416,9 @@ int dattn_get_error(dattn_t* h, dattn_stream_t stream) {
   if (cudaMemsetAsync(h->err, 0, sizeof(int), s) != cudaSuccess) return DATTN_ECUDA;
   // a call that gave up waiting still counts its segments; clear them anyway
   for (int i = 0; i < 2 && bits; ++i)
-    if (cudaMemsetAsync(h->counters[i], 0, static_cast<size_t>(h->max_streams) * h->Hkv * sizeof(int), s) !=
-        cudaSuccess)
+    if (cudaMemsetAsync(h->counters[i], 0,
+                        (static_cast<size_t>(h->max_streams) * h->Hkv + h->decode_resident) * sizeof(int),
+                        s) != cudaSuccess)
       return DATTN_ECUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return DATTN_ECUDA;
   if (bits & ERR_TIMEOUT) return DATTN_ETIMEOUT;

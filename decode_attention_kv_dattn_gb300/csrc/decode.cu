@@ -501,6 +501,121 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, int u, int n, u
   bulk_copy_g2s(dst + Gm::IN_V, a.v_new + (static_cast<int64_t>(b) * Hkv + j) * D, 2u * D, bar, pol);
 }
 
+// Folds the partial slots base[k * slot_stride] (k in [k0, k1), where ok(k))
+// into mg, kMergeBatch slots' loads in flight at a time, for head g, dims
+// d..d+7. Slots with no valid key (m = -inf) are skipped.
+template <int D, int GP, typename Ok, typename Slot>
+__device__ __forceinline__ void fold_slots(const float* part, int k0, int k1, Ok ok, Slot slot_of, int g, int d,
+                                           Merge8& mg) {
+  constexpr int stride = GP * (D + 2);
+  for (int kb = k0; kb < k1; kb += kMergeBatch) {
+    float m[kMergeBatch], l[kMergeBatch], x[kMergeBatch][8];
+#pragma unroll
+    for (int q = 0; q < kMergeBatch; ++q) {
+      const int k = kb + q;
+      m[q] = -INFINITY;
+      l[q] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[q][i] = 0.f;
+      if (k < k1 && ok(k)) {
+        const float* pk = part + static_cast<int64_t>(slot_of(k)) * stride;
+        m[q] = __ldcg(pk + GP * D + g);
+        l[q] = __ldcg(pk + GP * D + GP + g);
+        const float4 y0 = __ldcg(reinterpret_cast<const float4*>(pk + g * D + d));
+        const float4 y1 = __ldcg(reinterpret_cast<const float4*>(pk + g * D + d + 4));
+        x[q][0] = y0.x; x[q][1] = y0.y; x[q][2] = y0.z; x[q][3] = y0.w;
+        x[q][4] = y1.x; x[q][5] = y1.y; x[q][6] = y1.z; x[q][7] = y1.w;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kMergeBatch; ++q)
+      if (m[q] != -INFINITY) mg.add(m[q], l[q], x[q]);
+  }
+}
+
+// A unit cut into many pieces (one per CTA: a long stream on a GPU of many
+// SMs; 76 pieces at 1 x 131,072) is merged in two levels, so that its final
+// merge is not one CTA reading every partial (~17 us for 76 of them): the CTA
+// that finishes the last piece of a group of kMergeBatch pieces merges the
+// group into the slot of its first piece (per-group counters follow the unit
+// counters), and the CTA that finishes the last group merges the groups'
+// results with the new token. Called by the whole CTA after its piece's
+// partial is stored and published.
+template <int D, int GP, bool PAGED, int NTH, typename WaitPrev>
+__device__ void merge_in_groups(const DecodeArgs& a, int U, int pieces, int u, int cta, int unit_tiles,
+                                const uint8_t* slot, int* flag, int t, WaitPrev wait_prev) {
+  constexpr int stride = GP * (D + 2);
+  constexpr int IPT = (GP * D / 8 + NTH - 1) / NTH;  // 8-dim items per thread
+  const int S = pieces;
+  auto piece_ok = [&](int k) { return k < S && (k + 1) * unit_tiles / pieces > k * unit_tiles / pieces; };
+  auto piece_slot = [&](int k) { return u * pieces + k; };
+  auto group_first = [&](int kb) {  // first piece of group [kb, kb + kMergeBatch) with tiles, or -1
+    for (int k = kb; k < min(S, kb + kMergeBatch); ++k)
+      if (piece_ok(k)) return k;
+    return -1;
+  };
+  const int kb = (cta - u * pieces) / kMergeBatch * kMergeBatch, ke = min(S, kb + kMergeBatch);
+  int n_in = 0;
+  for (int k = kb; k < ke; ++k) n_in += piece_ok(k);
+  int* gcount = a.counters + U + piece_slot(kb);
+  if (t == 0) *flag = atomicAdd(gcount, 1) == n_in - 1;
+  __syncthreads();
+  if (!*flag) return;
+  __threadfence();
+  // ---- the group, into the slot of its first piece: o first (each thread
+  // reads and writes only its own items' dims), m and l once every thread
+  // has read the group's
+  float* gdst = a.part + static_cast<int64_t>(piece_slot(group_first(kb))) * stride;
+  float gM[IPT], gL[IPT];
+#pragma unroll
+  for (int i = 0; i < IPT; ++i) {
+    gM[i] = -INFINITY;
+    gL[i] = 0.f;
+    const int e = t * 8 + i * NTH * 8;
+    if (e < a.G * D) {
+      const int g = e / D, d = e - g * D;
+      Merge8 r;
+      r.M = -INFINITY;
+      r.L = 0.f;
+#pragma unroll
+      for (int x = 0; x < 8; ++x) r.o[x] = 0.f;
+      fold_slots<D, GP>(a.part, kb, ke, piece_ok, piece_slot, g, d, r);
+      gM[i] = r.M;
+      gL[i] = r.L;
+      *reinterpret_cast<float4*>(gdst + g * D + d) = make_float4(r.o[0], r.o[1], r.o[2], r.o[3]);
+      *reinterpret_cast<float4*>(gdst + g * D + d + 4) = make_float4(r.o[4], r.o[5], r.o[6], r.o[7]);
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < IPT; ++i) {
+    const int e = t * 8 + i * NTH * 8;
+    if (e < a.G * D && e % D == 0) {
+      gdst[GP * D + e / D] = gM[i];
+      gdst[GP * D + GP + e / D] = gL[i];
+    }
+  }
+  if (t == 0) *gcount = 0;
+  __threadfence();
+  __syncthreads();
+  // ---- count this group; the CTA finishing the unit's last group combines
+  int n_groups = 0;
+  for (int k = 0; k < S; k += kMergeBatch) n_groups += group_first(k) >= 0;
+  if (t == 0) *flag = atomicAdd(a.counters + u, 1) == n_groups - 1;
+  __syncthreads();
+  if (!*flag) return;
+  __threadfence();
+  wait_prev();
+  auto group_ok = [&](int gi) { return group_first(gi * kMergeBatch) >= 0; };
+  auto group_slot = [&](int gi) { return piece_slot(group_first(gi * kMergeBatch)); };
+  const int ng = (S + kMergeBatch - 1) / kMergeBatch;
+  finish_unit<D, GP, PAGED, NTH>(a, u, slot, t, [&](int g, int d, Merge8& mg) {
+    fold_slots<D, GP>(a.part, 0, ng, group_ok, group_slot, g, d, mg);
+  });
+  if (t == 0) a.counters[u] = 0;
+  __syncthreads();
+}
+
 // End of one segment of unit u, whose streaming warps' states are in their
 // merge buffers. When the unit lies wholly in this CTA, its output and
 // write-back follow from those states; otherwise they are merged into the
@@ -537,6 +652,12 @@ __device__ void end_segment(const DecodeArgs& a, const Split& sp, int pieces, in
   __threadfence();
   team_sync<NTH>();
   release();
+  if constexpr (NTH != 32) {
+    if (pieces && S > 2 * kMergeBatch) {
+      merge_in_groups<D, GP, PAGED, NTH>(a, sp.U, pieces, u, cta, p1 - p0, slot, flag, t, wait_prev);
+      return;
+    }
+  }
   // count this segment; the team finishing the unit's last segment combines it
   int last;
   if constexpr (NTH == 32) {

@@ -102,7 +102,7 @@ struct DecodeArgs {
   int write_back;
   float* part;                 // [ctas + B*Hkv][GP*(D+2)]: o[GP][D], m[GP], l[GP]
                                // (GP = decode_group_pad(G))
-  int* counters;               // [B*Hkv] finished segments; zero between calls
+  int* counters;               // [B*Hkv] finished segments, then [ctas] group counters; zero between calls
   int* err;
   int early;                   // nonzero: the preceding launch on the stream writes
                                // no part of this cache, so the first cache loads may

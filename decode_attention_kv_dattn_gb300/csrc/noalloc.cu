@@ -150,7 +150,7 @@ extern "C" DATTN_API int dattn_decode_noalloc(const dattn_config* cfg, int layer
   const size_t norm_off = off;
   off = align256(off + 2 * static_cast<size_t>(D) * sizeof(uint16_t));
   const size_t counters_off = off;
-  off = align256(off + static_cast<size_t>(B) * Hkv * sizeof(int));
+  off = align256(off + (static_cast<size_t>(B) * Hkv + ctas) * sizeof(int));  // units, then one per CTA
   const size_t part_off = off;
   off = align256(off + (static_cast<size_t>(ctas) + static_cast<size_t>(B) * Hkv) * GP * (D + 2) * sizeof(float));
   if (off > kNoAllocScratchBytes) return DATTN_EXCEEDS;
@@ -194,7 +194,7 @@ extern "C" DATTN_API int dattn_decode_noalloc(const dattn_config* cfg, int layer
   setup.half = half;
   setup.err = err;
   setup.counters = counters;
-  setup.n_counters = B * Hkv;
+  setup.n_counters = B * Hkv + ctas;
   noalloc_setup_kernel<<<1, 256, 0, s>>>(setup);
   if (cudaGetLastError() != cudaSuccess) return DATTN_ECUDA;
 
