@@ -158,7 +158,8 @@ struct Geo {
   static constexpr int IN_KH = IN_V + D * 2;
   static constexpr int IN_SN = IN_KH + D * 2;
   static constexpr int IN_SIG = IN_SN + GP * 4;
-  static constexpr int IN_BYTES = (IN_SIG + GP * 4 + 15) / 16 * 16;
+  static constexpr int IN_WB = (IN_SIG + GP * 4 + 7) / 8 * 8;  // int64: the new entry's pool offset
+  static constexpr int IN_BYTES = (IN_WB + 8 + 15) / 16 * 16;
   static constexpr int IN_OFF = (STEP_OFF + D / 2 * 8 + 15) / 16 * 16;  // 2 input slots
   static constexpr int TAB_OFF = IN_OFF + 2 * IN_BYTES;
   static constexpr int SMEM_MAX = 1024 + TAB_OFF + (4 * kMaxUnits + 1) * 4;  // P, N, ring head/row
@@ -337,6 +338,27 @@ struct Merge8 {
   }
 };
 
+// Where unit (b, j)'s new entry goes: its element offset in the K and V
+// pools (bytes for E4M3), or -1 when the metadata is out of range (a bad
+// page is reported here; a bad ring was reported when the unit table was read).
+template <bool PAGED>
+__device__ __forceinline__ int64_t write_back_offset(const DecodeArgs& a, int b, int j, int D) {
+  const CacheView& c = a.c;
+  if constexpr (PAGED) {
+    const int n = min(max(c.seq_len[b], 0), min(a.max_len, c.bt_stride * c.P));
+    const int pi = n / c.P;
+    const int pg = pi < c.bt_stride ? c.block_table[static_cast<int64_t>(b) * c.bt_stride + pi] : -1;
+    if (pg >= 0 && pg < c.n_rows) return ((static_cast<int64_t>(pg) * a.Hkv + j) * c.P + n % c.P) * D;
+    raise_error(a.err, ERR_INDEX);
+    return -1;
+  } else {
+    const int row = c.stream_rows ? c.stream_rows[b] : b;
+    const int head = c.ring_head[b], cnt = c.ring_count[b];
+    if (row < 0 || row >= c.n_rows || head < 0 || head >= c.R || cnt < 0 || cnt > c.R) return -1;
+    return ((static_cast<int64_t>(row) * a.Hkv + j) * c.R + head) * D;
+  }
+}
+
 // Output and write-back of unit u = (b, j) once all of its segments are done.
 // Each thread takes 8 consecutive dims of one head; `states(g, d, mg)` folds
 // the unit's segment states for head g, dims d..d+7 into mg. Needs the new
@@ -374,23 +396,10 @@ __device__ __forceinline__ void finish_unit(const DecodeArgs& a, int u, const ui
     *reinterpret_cast<float4*>(dst) = make_float4(mg.o[0] * scale, mg.o[1] * scale, mg.o[2] * scale, mg.o[3] * scale);
     *reinterpret_cast<float4*>(dst + 4) = make_float4(mg.o[4] * scale, mg.o[5] * scale, mg.o[6] * scale, mg.o[7] * scale);
   }
-  // write-back of the new entry: every segment of this unit has finished reading
+  // write-back of the new entry: every segment of this unit has finished
+  // reading; its target was worked out when the unit's inputs were prepared
   if (a.write_back) {
-    int64_t wb = -1;
-    if constexpr (PAGED) {
-      const int n = min(max(c.seq_len[b], 0), min(a.max_len, c.bt_stride * c.P));
-      const int pi = n / c.P;
-      const int pg = pi < c.bt_stride ? c.block_table[static_cast<int64_t>(b) * c.bt_stride + pi] : -1;
-      if (pg >= 0 && pg < c.n_rows)
-        wb = ((static_cast<int64_t>(pg) * Hkv + j) * c.P + n % c.P) * D;
-      else if (t == 0)
-        raise_error(a.err, ERR_INDEX);
-    } else {
-      const int row = c.stream_rows ? c.stream_rows[b] : b;
-      const int head = c.ring_head[b], cnt = c.ring_count[b];
-      if (!(row < 0 || row >= c.n_rows || head < 0 || head >= c.R || cnt < 0 || cnt > c.R))
-        wb = ((static_cast<int64_t>(row) * Hkv + j) * c.R + head) * D;
-    }
+    const int64_t wb = *reinterpret_cast<const int64_t*>(slot + Gm::IN_WB);
     if (wb >= 0 && a.f8) {
       // E4M3 rows: wb counts elements, which are bytes here
       const uint8_t* k8 = slot + Gm::IN_KH;
@@ -1347,7 +1356,7 @@ __global__ void __launch_bounds__(Geo<D, NT, F8>::THREADS, 1) decode_kernel(cons
       }
     };
     int n_st = 0;  // units staged so far; unit k of this CTA uses input slot k & 1
-    int pos_s[2] = {0, 0};
+    int pos_s[2] = {0, 0}, unit_s[2] = {0, 0};
     uint16_t gate_s[2] = {0, 0};  // raw bf16: converting here would wait for the load
     auto stage = [&](int u) {
       const int b = u / Hkv, j = u - b * Hkv, sl = n_st & 1;
@@ -1358,9 +1367,11 @@ __global__ void __launch_bounds__(Geo<D, NT, F8>::THREADS, 1) decode_kernel(cons
       if (sl == 0) {
         pos_s[0] = pv;
         gate_s[0] = gv;
+        unit_s[0] = u;
       } else {
         pos_s[1] = pv;
         gate_s[1] = gv;
+        unit_s[1] = u;
       }
       ++n_st;
     };
@@ -1378,6 +1389,12 @@ __global__ void __launch_bounds__(Geo<D, NT, F8>::THREADS, 1) decode_kernel(cons
       // (a testing aid can withhold the first unit's q, so that every
       // streaming warp's bounded wait for it runs out)
       if (lane == 0 && !(k == 0 && (a.debug_flags & kDebugWithholdQ))) mbar_arrive(prep_full);
+      // the new entry's target, read once the unit's segments are done: its
+      // metadata loads are off the CTA's tail (prep_token ends with a barrier)
+      if (a.write_back && lane == 0) {
+        const int uk = sl ? unit_s[1] : unit_s[0];
+        *reinterpret_cast<int64_t*>(slot + Gm::IN_WB) = write_back_offset<PAGED>(a, uk / Hkv, uk % Hkv, D);
+      }
       prep_token<D, GP, 32>(a, qs, cs, slot, sl ? gate_s[1] : gate_s[0], lane);
     };
     if (u_first < U) {
@@ -1434,6 +1451,8 @@ __global__ void __launch_bounds__(Geo<D, NT, F8>::THREADS, 1) decode_kernel(cons
       norm_staged<D, kThreads>(a, reinterpret_cast<uint16_t*>(slot + Gm::IN_Q),
                                reinterpret_cast<uint16_t*>(slot + Gm::IN_K), threadIdx.x);
     prep_q<D, GP, kThreads>(a, reinterpret_cast<const uint16_t*>(slot + Gm::IN_Q), pos, step, qs, cs, threadIdx.x);
+    if (a.write_back && threadIdx.x == 0)
+      *reinterpret_cast<int64_t*>(slot + Gm::IN_WB) = write_back_offset<PAGED>(a, b, j, D);
     __syncthreads();
     prep_token<D, GP, kThreads>(a, qs, cs, slot, gr, threadIdx.x);
     wait_prev();
