@@ -892,7 +892,9 @@ def run_dattn(args, world, rank, local):
         surveyed = survey_workloads(peak0)
     if rank != 0:
         return
-    traffic = recorded_traffic(args.workload)
+    # (the recorded hybrid capture is of the headline's 64 x 4096 step)
+    sized = args.workload != "hybrid" or (args.streams, args.context) == (B_STREAMS, CONTEXT)
+    traffic = recorded_traffic(args.workload) if sized else None
     config = dict(step.config)
     config.update({"l2": ("flushed (256 MiB write) before every step" if step.flush_l2 else
                           f"inputs larger than L2: {bytes_step / 1e9:.3f} GB per step vs 129 MB L2"),
